@@ -1,0 +1,403 @@
+"""MiTA forward throughput on GB300 (queries/s), with per-stage roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long_1m]
+    python bench.py --impl reference ...     # the fp64 CPU oracle, timed on host cores
+
+One step = one full forward pass (pool, landmark experts + shared values,
+route, bucket, expert attention) over one batch of the workload, inputs
+already resident in HBM.  Inputs are larger than L2 for both long workloads,
+so no flush is needed between steps.  N > 1 runs one independent replica per
+GPU (the forward does not shard); `value` counts the queries of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sparse_top_landmark_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MiTA fwd queries/sec at N=64K and 1M on 1 GB300; % of per-stage roofline"
+UNIT = "queries/s"
+KERNELS_PER_FORWARD = 9   # pool 1, landmark 3, route 1, bucket 3, expert 1
+L2_BYTES = 129 * 2 ** 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], tc=d["bf16_tflops"], tc_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work per stage (flops, bytes) for the whole batch
+# ---------------------------------------------------------------------------
+def stage_work(w):
+    BH, N, d, m, k = w.B * w.H, w.N, w.d, w.m, w.topk
+    e = 2 if w.dtype == "bf16" else 4
+    return {
+        "pool": (0.0, BH * (N * d * e + m * d * e)),
+        "landmark": (BH * 4.0 * m * N * d, BH * (2 * N * d * e + m * d * e + m * k * 4 + m * d * 4)),
+        "route": (BH * 2.0 * N * m * d, BH * (N * d * e + m * d * e + 4 * N)),
+        "bucket": (0.0, BH * (12 * N + 4 * (m + 1))),
+        "expert": (BH * (4.0 * N * k * d + 2.0 * N * m * d),
+                   BH * (2 * N * d * e + 2 * m * k * d * e + 4 * m * k + 4 * N + m * d * (e + 4))),
+    }
+
+
+def roofline_s(flops, nbytes, pk, sustained=False):
+    tc = (pk["tc_sus"] if sustained else pk["tc"]) * 1e12
+    return max(flops / tc, nbytes / (pk["hbm"] * 1e9))
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.05)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing on a bounded sample (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_time(w, q, k, v, rows=None, queries=None, seed=0):
+    """Time the oracle on a sample; return (estimated seconds for the whole
+    workload, description, threads)."""
+    import oracle
+    g = torch.Generator().manual_seed(seed)
+    BH, N, m = w.B * w.H, w.N, w.m
+    threads = oracle.num_threads()
+    nrows = rows or max(2 * threads, 8)
+    nq = queries or 8192
+    t0 = time.perf_counter()
+    qt = oracle.pool(q, w.grid_h, w.grid_w, m)
+    t_pool = time.perf_counter() - t0
+    rsel = torch.randint(0, BH * m, (min(nrows, BH * m),), generator=g)
+    t0 = time.perf_counter()
+    ti, vt, _ = oracle.landmark(qt, k, v, w.topk, rows=rsel)
+    t_rows = time.perf_counter() - t0
+    # per-query work does not depend on the values: every landmark reuses the
+    # sampled rows' outputs
+    full_ti = ti[torch.arange(BH * m) % ti.shape[0]].view(w.B, w.H, m, w.topk).contiguous()
+    full_vt = vt[torch.arange(BH * m) % vt.shape[0]].view(w.B, w.H, m, w.d).contiguous()
+    qsel = torch.randint(0, BH * N, (min(nq, BH * N),), generator=g)
+    t0 = time.perf_counter()
+    r, _ = oracle.route(q, qt, w.s, queries=qsel)
+    oracle.attend(q, k, v, qt, full_vt, full_ti, r, queries=qsel)
+    t_q = time.perf_counter() - t0
+    est = t_pool + t_rows * (BH * m) / rsel.numel() + t_q * (BH * N) / qsel.numel()
+    desc = (f"oracle on {threads} threads: pool of all {BH * m} windows, "
+            f"{rsel.numel()} of {BH * m} landmark rows, route+attend of {qsel.numel()} of "
+            f"{BH * N} queries; time scaled to the whole workload")
+    return est, desc, threads, t_pool + t_rows + t_q
+
+
+# ---------------------------------------------------------------------------
+def smi_index(local):
+    """nvidia-smi index of this process's GPU."""
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p for p in cvd.split(",") if p.strip()]
+    if parts:
+        p = parts[local] if local < len(parts) else parts[0]
+        return int(p) if p.strip().isdigit() else local
+    return local
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def config_of(w, n_gpus):
+    total = 3 * w.B * w.H * w.N * w.d * (2 if w.dtype == "bf16" else 4)
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m,
+            "topk": w.topk, "s": w.s, "grid": [w.grid_h, w.grid_w],
+            "qk": f"{w.clusters}-cluster Gaussian mixture sigma={w.sigma}" if w.qk == "mixture"
+            else "iid N(0,1)",
+            "l2": f"inputs larger than L2 ({total / 2**20:.0f} MiB of Q,K,V vs "
+                  f"{L2_BYTES / 2**20:.0f} MiB), no flush",
+            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.WORKLOADS[args.workload]
+    q, k, v = W.make_qkv(w, 0)
+    per = []
+    for i in range(args.warmup + args.steps):
+        est, desc, threads, spent = oracle_sample_time(w, q, k, v, rows=8, queries=2048, seed=i)
+        if i >= args.warmup:
+            per.append(est)
+    est = statistics.median(per)
+    value = w.queries / est
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def time_forward(mita, w, dq, dk, dv, out, steps, stream):
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        mita.mita_forward(dq, dk, dv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=out, stream=stream)
+    ev1.record(stream)
+    ev1.synchronize()
+    return ev0.elapsed_time(ev1) / 1e3
+
+
+def stage_times(mita, w, dq, dk, dv, reps, stream):
+    """Average device time of each stage, run through the stage entry points."""
+    BH = w.B * w.H
+    qt = torch.empty((w.B, w.H, w.m, w.d), dtype=dq.dtype, device=dq.device)
+    ti = torch.empty((w.B, w.H, w.m, w.topk), dtype=torch.int32, device=dq.device)
+    vt = torch.empty((w.B, w.H, w.m, w.d), dtype=torch.float32, device=dq.device)
+    r = torch.empty((w.B, w.H, w.N, 1), dtype=torch.int32, device=dq.device)
+    off = torch.empty((w.B, w.H, w.m + 1), dtype=torch.int32, device=dq.device)
+    qi = torch.empty((w.B, w.H, w.N), dtype=torch.int32, device=dq.device)
+    out = torch.empty_like(dq)
+    calls = {
+        "pool": lambda: mita.mita_pool(dq, w.grid_h, w.grid_w, w.m, q_tilde=qt, stream=stream),
+        "landmark": lambda: mita.mita_landmark_topk_shared(qt, dk, dv, w.topk, topk_idx=ti,
+                                                           v_tilde=vt, stream=stream),
+        "route": lambda: mita.mita_route(dq, qt, route_idx=r, stream=stream),
+        "bucket": lambda: mita.mita_bucket(r, w.m, bucket_off=off, bucket_qidx=qi, stream=stream),
+        "expert": lambda: mita.mita_expert_attn(dq, dk, dv, qt, vt, ti, off, qi, out=out,
+                                                stream=stream),
+    }
+    for fn in calls.values():     # warm, and fill every intermediate
+        fn()
+    res = {}
+    for name, fn in calls.items():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+        for i in range(reps):
+            evs[2 * i].record(stream)
+            fn()
+            evs[2 * i + 1].record(stream)
+        evs[-1].synchronize()
+        res[name] = sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(reps)) / reps / 1e3
+    del BH
+    return res
+
+
+def bench_workload(mita, w, args, dev, stream, n_gpus, do_e2e=True):
+    q, k, v = W.make_qkv(w, 0)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty_like(dq)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            mita.mita_forward(dq, dk, dv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=out,
+                              stream=stream)
+    torch.cuda.synchronize(dev)
+    if n_gpus > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(smi_index(dev.index))
+    with sampler:
+        secs = time_forward(mita, w, dq, dk, dv, out, args.steps, stream)
+    torch.cuda.synchronize(dev)
+    if n_gpus > 1:
+        t = torch.tensor([secs], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        secs = t.item()
+        torch.distributed.barrier()
+    res = {"secs": secs, "clocks": sampler.summary()}
+    res["value"] = n_gpus * w.queries * args.steps / secs
+    res["ms_per_step"] = secs / args.steps * 1e3
+    res["stages"] = stage_times(mita, w, dq, dk, dv, max(3, min(args.steps, 10)), stream)
+    if do_e2e:
+        hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        hout = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        for _ in range(max(1, args.warmup // 2)):
+            mita.mita_forward(hq, hk, hv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=hout,
+                              stream=stream, device=dev)
+        if n_gpus > 1:
+            torch.distributed.barrier()
+        esteps = max(2, min(args.steps, 5))
+        t0 = time.perf_counter()
+        for _ in range(esteps):
+            mita.mita_forward(hq, hk, hv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=hout,
+                              stream=stream, device=dev)
+        es = time.perf_counter() - t0
+        if n_gpus > 1:
+            t = torch.tensor([es], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            es = t.item()
+        e = q.element_size()
+        res["e2e"] = {"value": n_gpus * w.queries * esteps / es, "unit": UNIT,
+                      "h2d_bytes_per_step": 3 * q.numel() * e,
+                      "d2h_bytes_per_step": q.numel() * e}
+    res["inputs"] = (q, k, v)
+    return res
+
+
+def roofline_entry(w, stages, pk):
+    work = stage_work(w)
+    name = max(stages, key=lambda s: stages[s])
+    fl, by = work[name]
+    t = stages[name]
+    tc_time = fl / (pk["tc"] * 1e12)
+    hbm_time = by / (pk["hbm"] * 1e9)
+    if tc_time >= hbm_time:
+        ach = fl / t / 1e12
+        ent = {"bound": "tensor", "achieved": ach, "peak": pk["tc"], "unit": "TFLOP/s"}
+    else:
+        ach = by / t / 1e9
+        ent = {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s"}
+    ent["frac"] = ent["achieved"] / ent["peak"]
+    ent["kernel"] = name
+    ent["peak_source"] = pk["src"]
+    ent["traffic"] = None
+    per = {}
+    for s, tt in stages.items():
+        rl = roofline_s(*work[s], pk)
+        per[s] = {"ms": tt * 1e3, "roofline_ms": rl * 1e3, "frac": rl / tt if tt > 0 else None}
+    return ent, per
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="mita", choices=["mita", "reference"])
+    ap.add_argument("--workload", default="long_1m", choices=list(W.WORKLOADS))
+    ap.add_argument("--secondary", default="long_64k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    ws, rank, local = dist_env()
+    n_gpus = max(ws, 1)
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    from sparse_top_landmark_gb300 import build, mita
+    if rank == 0 or ws == 1:
+        build.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    mita.load()
+    stream = torch.cuda.Stream(dev)
+    pk = peaks()
+
+    w = W.WORKLOADS[args.workload]
+    main_res = bench_workload(mita, w, args, dev, stream, n_gpus)
+    roof, per_stage = roofline_entry(w, main_res["stages"], pk)
+    sec = None
+    if args.secondary and args.secondary != args.workload:
+        w2 = W.WORKLOADS[args.secondary]
+        r2 = bench_workload(mita, w2, args, dev, stream, n_gpus, do_e2e=False)
+        roof2, per2 = roofline_entry(w2, r2["stages"], pk)
+        sec = {"workload": w2.name, "value": r2["value"], "ms_per_step": r2["ms_per_step"],
+               "roofline": roof2, "stages": per2, "clocks": r2["clocks"]}
+
+    cpu = None
+    if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
+        q, k, v = main_res["inputs"]
+        est, desc, threads, spent = oracle_sample_time(w, q, k, v)
+        cpu = {"value": w.queries / est, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": desc, "sample_seconds": spent}
+
+    if rank == 0:
+        total_rl = sum(roofline_s(*wk, pk) for wk in stage_work(w).values())
+        line = {
+            "metric": METRIC, "value": main_res["value"], "unit": UNIT, "n_gpus": n_gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": main_res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": config_of(w, n_gpus),
+            "clocks": main_res["clocks"],
+            "e2e": main_res["e2e"],
+            "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+            "roofline": roof,
+            "forward_roofline_frac": total_rl / (main_res["ms_per_step"] / 1e3),
+            "stages": per_stage,
+            "cpu_baseline": cpu,
+            "secondary": sec,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,197 @@
+/*
+ * mita.h -- C ABI of libmita.so: the MiTA (Mixture-of-Top-k Attention)
+ * forward pass on NVIDIA GB300 (sm_103a).
+ *
+ * Method (cited per entry point below):
+ *   MiTA tutorial, iwxt.cn/tutorials/mita-attention, ch. 4 (paper Sec. 3.2,
+ *   eq. 5-12) and ch. 8; gist.science summary of arXiv 2602.01219, Sec. 2.2-2.3
+ *   (Algorithm 1); bit.fan news article on MiTA (expert construction,
+ *   grouping by expert with online softmax).
+ *
+ * Conventions (all entry points):
+ *   - Tensors are dense, row-major.  Q, K, V and the output are [B, H, N, d]:
+ *     head (b, h) owns N consecutive rows of d elements.  For a 2D token grid
+ *     (grid_h > 1) token t sits at row t / grid_w, column t % grid_w.
+ *   - Unsuffixed entry points take bfloat16 data (`const void*` holding
+ *     __nv_bfloat16); the `_f32` twins take float with the same parameters.
+ *     Landmark values v~ and the optional shared-branch partial are float.
+ *     Index outputs are int32.
+ *   - Every pointer is a DEVICE pointer owned by the caller; the library never
+ *     frees or retains it.  Element arrays must start on a 16-byte boundary.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     never synchronise the host.  Arguments are validated on the host before
+ *     any launch; an invalid call launches nothing and returns non-zero.
+ *   - Launch failures return MITA_ERR_CUDA.  Faults during execution surface
+ *     at the caller's next synchronisation.  Data-dependent problems the
+ *     kernels detect (an index out of range in caller-supplied arrays) set a
+ *     per-device status word read by mita_get_last_device_error(); the
+ *     offending entry is skipped, never dereferenced.
+ *   - Stages that need scratch memory (landmark, bucket, forward) draw it from
+ *     a library-owned, stream-ordered cache (cudaMallocAsync on `stream`),
+ *     one buffer per (device, stream), grown when a call needs more.  Growing
+ *     is refused (MITA_ERR_UNSUPPORTED) while `stream` is being captured into
+ *     a CUDA graph: make one call of the same size outside capture first.
+ *     mita_workspace_release() frees the cache.
+ *   - Supported: d in {16, 32, 64, 128}; 1 <= topk <= min(N, 4096);
+ *     1 <= m <= N; s == 1 (the setting of every experiment on the pages;
+ *     s > 1 returns MITA_ERR_UNSUPPORTED); B*H*N < 2^31.
+ */
+#ifndef MITA_H_
+#define MITA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* mita_stream_t;
+
+enum mita_status {
+  MITA_OK = 0,
+  MITA_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer      */
+  MITA_ERR_UNSUPPORTED = 2,   /* valid but outside this build's limits       */
+  MITA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed        */
+  MITA_ERR_OOM = 4,           /* workspace allocation failed                 */
+  MITA_ERR_DEVICE_CHECK = 5   /* a kernel flagged inconsistent input data    */
+};
+
+/*
+ * mita_pool -- landmark queries by local average pooling of Q.
+ * Tutorial ch. 4 step 1 (paper eq. 5): each landmark query q~_i is the mean of
+ * a group of queries; the bit.fan article calls it local average pooling.
+ *   q        [B,H,N,d]  input queries.
+ *   grid_h, grid_w      token grid, grid_h * grid_w == N.  grid_h == 1: 1D,
+ *                       m windows of the sequence; else m must be a perfect
+ *                       square and the grid is pooled to sqrt(m) x sqrt(m).
+ *                       Window i covers [floor(i*in/out), ceil((i+1)*in/out))
+ *                       along each axis (adaptive average pooling).
+ *   q_tilde  [B,H,m,d]  output, the exact window mean rounded once to the
+ *                       element type (round to nearest even).
+ */
+int mita_pool(const void* q, int B, int H, int N, int d, int grid_h, int grid_w, int m,
+              void* q_tilde, mita_stream_t stream);
+int mita_pool_f32(const float* q, int B, int H, int N, int d, int grid_h, int grid_w, int m,
+                  float* q_tilde, mita_stream_t stream);
+
+/*
+ * mita_landmark_topk_shared -- routed experts and shared landmark values.
+ * Tutorial ch. 4 step 2 (eq. 6-7): s_ij = q~_i . k_j / sqrt(d) over all N
+ * keys; expert i is the top-k keys of row i.  Step 3 (eq. 8-9): the same
+ * scores, softmax over all N, weight all of V: v~_i.
+ *   q_tilde  [B,H,m,d], k, v [B,H,N,d]   inputs.
+ *   topk_idx [B,H,m,topk] int32  output: the topk key indices of each
+ *            landmark in ascending index order.  The set is the one exact
+ *            scores select, ties broken toward the lowest key index.
+ *   v_tilde  [B,H,m,d] float     output.
+ * Uses the workspace cache.
+ */
+int mita_landmark_topk_shared(const void* q_tilde, const void* k, const void* v, int B, int H,
+                              int N, int d, int m, int topk, int32_t* topk_idx, float* v_tilde,
+                              mita_stream_t stream);
+int mita_landmark_topk_shared_f32(const float* q_tilde, const float* k, const float* v, int B,
+                                  int H, int N, int d, int m, int topk, int32_t* topk_idx,
+                                  float* v_tilde, mita_stream_t stream);
+
+/*
+ * mita_route -- route each query to its best landmark.
+ * Tutorial ch. 4 step 4 (eq. 10): compare q . q~_i and keep the top-s; the
+ * scores select, no gate.  The bit.fan article: those logits are reused for
+ * the shared branch.
+ *   q [B,H,N,d], q_tilde [B,H,m,d]  inputs.
+ *   v_tilde [B,H,m,d] float          input, read only when a shared output is
+ *                                    requested (may be NULL otherwise).
+ *   route_idx [B,H,N,s] int32        output: argmax_i q . q~_i (exact; ties
+ *                                    to the lowest landmark index).
+ *   shared_lse [B,H,N] float or NULL output: ln sum_i exp(q . q~_i / sqrt(d)).
+ *   shared_o [B,H,N,d] float or NULL output: softmax-weighted sum of v~ over
+ *                                    the m shared pairs.
+ *   s must be 1.
+ */
+int mita_route(const void* q, const void* q_tilde, const float* v_tilde, int B, int H, int N,
+               int d, int m, int s, int32_t* route_idx, float* shared_lse, float* shared_o,
+               mita_stream_t stream);
+int mita_route_f32(const float* q, const float* q_tilde, const float* v_tilde, int B, int H,
+                   int N, int d, int m, int s, int32_t* route_idx, float* shared_lse,
+                   float* shared_o, mita_stream_t stream);
+
+/*
+ * mita_bucket -- group queries by routed expert (Algorithm 1, bit.fan
+ * article: queries are grouped by routing result).
+ *   route_idx [B,H,N,s] int32          input, values in [0, m).
+ *   bucket_off [B,H,m+1] int32         output: exclusive prefix of the
+ *                                      per-expert query counts.
+ *   bucket_qidx [B,H,N*s] int32        output: for expert e, the query
+ *                                      indices bucket_qidx[off[e]:off[e+1]]
+ *                                      in ascending order (a stable sort).
+ * Values outside [0, m) are skipped and flag MITA_ERR_DEVICE_CHECK.  Uses the
+ * workspace cache.  s must be 1.
+ */
+int mita_bucket(const int32_t* route_idx, int B, int H, int N, int m, int s,
+                int32_t* bucket_off, int32_t* bucket_qidx, mita_stream_t stream);
+
+/*
+ * mita_expert_attn -- joint softmax over the shared pairs and the routed
+ * expert's raw pairs, computed expert by expert.
+ * Tutorial ch. 4 steps 5-6 (eq. 11-12): logits [q . q~_i / sqrt(d)]_{i<m}
+ * followed by [q . k_j / sqrt(d)]_{j in expert}, one softmax, values
+ * [v~_i] then [v_j].  With a precomputed shared partial the two branches are
+ * merged by (Z1 o1 + Z2 o2) / (Z1 + Z2) (tutorial ch. 4).
+ *   q, k, v [B,H,N,d]; q_tilde [B,H,m,d]; v_tilde [B,H,m,d] float;
+ *   topk_idx [B,H,m,topk]; bucket_off [B,H,m+1]; bucket_qidx [B,H,N]   inputs.
+ *   shared_lse, shared_o   the partial from mita_route, or both NULL to
+ *                          recompute the shared branch here.
+ *   out [B,H,N,d]          output (every query appearing in bucket_qidx).
+ * Indices outside their range are skipped and flag MITA_ERR_DEVICE_CHECK.
+ */
+int mita_expert_attn(const void* q, const void* k, const void* v, const void* q_tilde,
+                     const float* v_tilde, const int32_t* topk_idx, const int32_t* bucket_off,
+                     const int32_t* bucket_qidx, const float* shared_lse, const float* shared_o,
+                     int B, int H, int N, int d, int m, int topk, int s, void* out,
+                     mita_stream_t stream);
+int mita_expert_attn_f32(const float* q, const float* k, const float* v, const float* q_tilde,
+                         const float* v_tilde, const int32_t* topk_idx,
+                         const int32_t* bucket_off, const int32_t* bucket_qidx,
+                         const float* shared_lse, const float* shared_o, int B, int H, int N,
+                         int d, int m, int topk, int s, float* out, mita_stream_t stream);
+
+/*
+ * mita_forward -- the whole MiTA forward pass (pool, landmark experts and
+ * shared values, route, bucket, expert attention), gist.science summary
+ * Sec. 2.3 Algorithm 1, tutorial ch. 4 eq. 5-12.
+ *   q, k, v [B,H,N,d] inputs; out [B,H,N,d] output.  Intermediates live in
+ *   the workspace cache.
+ */
+int mita_forward(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                 int grid_h, int grid_w, int m, int topk, int s, void* out,
+                 mita_stream_t stream);
+int mita_forward_f32(const float* q, const float* k, const float* v, int B, int H, int N, int d,
+                     int grid_h, int grid_w, int m, int topk, int s, float* out,
+                     mita_stream_t stream);
+
+/* Bytes of workspace mita_forward needs for this shape (0 if invalid). */
+uint64_t mita_forward_workspace_bytes(int B, int H, int N, int d, int m, int topk, int is_f32);
+
+/* Text for a status code (static storage). */
+const char* mita_status_string(int status);
+
+/* Detail of the last non-zero status returned on this host thread. */
+const char* mita_last_error_message(void);
+
+/*
+ * Synchronises `stream`, reads and clears the current device's status word.
+ * Returns MITA_OK if no kernel flagged bad input data since the last call,
+ * MITA_ERR_DEVICE_CHECK otherwise (the flag bits go to *bits if non-NULL),
+ * MITA_ERR_CUDA if the synchronisation itself failed.
+ */
+int mita_get_last_device_error(mita_stream_t stream, int* bits);
+
+/* Frees every cached workspace (synchronises each owning device first). */
+int mita_workspace_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MITA_H_ */

@@ -34,6 +34,7 @@
 #include <cstdint>
 #include <cstring>
 #include <numeric>
+#include <utility>
 #include <vector>
 
 #ifdef _OPENMP
@@ -156,50 +157,69 @@ int orc_landmark_rows(const double* q_tilde, const void* k, const void* v,
   (void)B; (void)H;
   if (topk < 1 || topk > N) return 1;
   const double sqrt_d = std::sqrt((double)d);
-#pragma omp parallel
-  {
-    std::vector<double> s(N);
-    std::vector<int> ord(N);
-#pragma omp for schedule(dynamic, 1)
-    for (long r = 0; r < nrows; ++r) {
-      long row = rows ? rows[r] : r;
-      long bh = row / m;
-      size_t kv0 = (size_t)bh * N * d;
-      const double* qt = q_tilde + (size_t)row * d;
-      double smax = -INFINITY, amax = 0.0;
-      for (int j = 0; j < N; ++j) {
-        double acc = 0.0;
-        for (int l = 0; l < d; ++l) acc += qt[l] * widen(k, dt, kv0 + (size_t)j * d + l);
-        s[j] = acc / sqrt_d;
-        smax = std::max(smax, s[j]);
-        amax = std::max(amax, std::fabs(s[j]));
-      }
-      // Top-k selection with the (score desc, index asc) order.
-      std::iota(ord.begin(), ord.end(), 0);
-      Better better{s.data()};
-      if (topk < N)
-        std::nth_element(ord.begin(), ord.begin() + topk, ord.end(), better);
-      std::vector<int> sel(ord.begin(), ord.begin() + topk);
-      int kth = *std::max_element(sel.begin(), sel.end(),
-                                  [&](int a, int b) { return better(a, b); });
-      if (topk < N) {
-        int next = ord[topk];  // nth_element puts the (k+1)-th best here
-        gap[r] = amax > 0 ? (s[kth] - s[next]) / amax : 0.0;
-      } else {
-        gap[r] = 1e300;
-      }
-      std::sort(sel.begin(), sel.end());
-      for (int t = 0; t < topk; ++t) topk_idx[(size_t)r * topk + t] = sel[t];
-      // Shared landmark value: full softmax over all N scores.
-      double z = 0.0;
-      std::vector<double> acc(d, 0.0);
-      for (int j = 0; j < N; ++j) {
-        double w = std::exp(s[j] - smax);
-        z += w;
-        for (int l = 0; l < d; ++l) acc[l] += w * widen(v, dt, kv0 + (size_t)j * d + l);
-      }
-      for (int l = 0; l < d; ++l) v_tilde[(size_t)r * d + l] = acc[l] / z;
+  // requested rows grouped by head, so each head's K and V are widened once
+  std::vector<std::pair<long, long>> order(nrows);  // (head, position in request)
+  for (long r = 0; r < nrows; ++r) order[r] = {(rows ? rows[r] : r) / m, r};
+  std::sort(order.begin(), order.end());
+  std::vector<double> kd((size_t)N * d), vd((size_t)N * d);
+  for (long g0 = 0; g0 < nrows;) {
+    long g1 = g0;
+    const long bh = order[g0].first;
+    while (g1 < nrows && order[g1].first == bh) ++g1;
+    const size_t kv0 = (size_t)bh * N * d;
+#pragma omp parallel for schedule(static)
+    for (long t = 0; t < (long)N * d; ++t) {
+      kd[t] = widen(k, dt, kv0 + t);
+      vd[t] = widen(v, dt, kv0 + t);
     }
+#pragma omp parallel
+    {
+      std::vector<double> s(N);
+      std::vector<int> ord(N);
+      std::vector<double> acc(d);
+#pragma omp for schedule(dynamic, 1)
+      for (long g = g0; g < g1; ++g) {
+        const long r = order[g].second;
+        const long row = rows ? rows[r] : r;
+        const double* qt = q_tilde + (size_t)row * d;
+        double smax = -INFINITY, amax = 0.0;
+        for (int j = 0; j < N; ++j) {
+          const double* kr = kd.data() + (size_t)j * d;
+          double a = 0.0;
+          for (int l = 0; l < d; ++l) a += qt[l] * kr[l];
+          s[j] = a / sqrt_d;
+          smax = std::max(smax, s[j]);
+          amax = std::max(amax, std::fabs(s[j]));
+        }
+        // Top-k selection with the (score desc, index asc) order.
+        std::iota(ord.begin(), ord.end(), 0);
+        Better better{s.data()};
+        if (topk < N)
+          std::nth_element(ord.begin(), ord.begin() + topk, ord.end(), better);
+        std::vector<int> sel(ord.begin(), ord.begin() + topk);
+        int kth = *std::max_element(sel.begin(), sel.end(),
+                                    [&](int a, int b) { return better(a, b); });
+        if (topk < N) {
+          int next = ord[topk];  // nth_element puts the (k+1)-th best here
+          gap[r] = amax > 0 ? (s[kth] - s[next]) / amax : 0.0;
+        } else {
+          gap[r] = 1e300;
+        }
+        std::sort(sel.begin(), sel.end());
+        for (int t = 0; t < topk; ++t) topk_idx[(size_t)r * topk + t] = sel[t];
+        // Shared landmark value: full softmax over all N scores.
+        double z = 0.0;
+        std::fill(acc.begin(), acc.end(), 0.0);
+        for (int j = 0; j < N; ++j) {
+          double w = std::exp(s[j] - smax);
+          z += w;
+          const double* vr = vd.data() + (size_t)j * d;
+          for (int l = 0; l < d; ++l) acc[l] += w * vr[l];
+        }
+        for (int l = 0; l < d; ++l) v_tilde[(size_t)r * d + l] = acc[l] / z;
+      }
+    }
+    g0 = g1;
   }
   return 0;
 }

@@ -1,0 +1,453 @@
+// C ABI of libmita.so: argument validation, workspace cache, stage
+// orchestration.  Every arithmetic step runs in the kernels of this library.
+#include "mita.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mita {
+namespace {
+
+thread_local std::string g_msg;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(MITA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+struct DevState {
+  int* status = nullptr;
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DevState> g_dev;
+struct WsEntry {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws;
+
+int device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& s = g_dev[dev];
+  if (s.status == nullptr) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    int* p = nullptr;
+    e = cudaMalloc(&p, sizeof(int));
+    if (e != cudaSuccess) return fail(MITA_ERR_OOM, "status word: %s", cudaGetErrorString(e));
+    e = cudaMemset(p, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    s.status = p;
+    s.num_sms = sms;
+  }
+  *out = &s;
+  return MITA_OK;
+}
+
+int workspace(size_t bytes, cudaStream_t st, void** out) {
+  *out = nullptr;
+  if (bytes == 0) return MITA_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  WsEntry& w = g_ws[{dev, st}];
+  if (w.bytes >= bytes) {
+    *out = w.ptr;
+    return MITA_OK;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(MITA_ERR_UNSUPPORTED,
+                "workspace must grow to %zu bytes while the stream is capturing; make one "
+                "call of this size outside capture first", bytes);
+  if (w.ptr) {
+    e = cudaFreeAsync(w.ptr, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+    w.ptr = nullptr;
+    w.bytes = 0;
+  }
+  const size_t want = bytes + bytes / 8;
+  void* p = nullptr;
+  e = cudaMallocAsync(&p, want, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MITA_ERR_OOM, "workspace of %zu bytes: %s", want, cudaGetErrorString(e));
+  }
+  w.ptr = p;
+  w.bytes = want;
+  *out = p;
+  return MITA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Validation
+// ---------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ptrs(std::initializer_list<std::pair<const void*, const char*>> ps) {
+  for (auto& p : ps) {
+    if (p.first == nullptr) return fail(MITA_ERR_INVALID_ARG, "%s is NULL", p.second);
+    if (!aligned16(p.first))
+      return fail(MITA_ERR_INVALID_ARG, "%s is not 16-byte aligned", p.second);
+  }
+  return MITA_OK;
+}
+
+int check_shape(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1)
+    return fail(MITA_ERR_INVALID_ARG, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if (d != 16 && d != 32 && d != 64 && d != 128)
+    return fail(MITA_ERR_UNSUPPORTED, "head dim d=%d not in {16, 32, 64, 128}", d);
+  if ((long long)B * H * N >= (1LL << 31))
+    return fail(MITA_ERR_UNSUPPORTED, "B*H*N must be < 2^31");
+  return MITA_OK;
+}
+
+int check_m(int N, int m) {
+  if (m < 1 || m > N) return fail(MITA_ERR_INVALID_ARG, "need 1 <= m <= N (m=%d, N=%d)", m, N);
+  return MITA_OK;
+}
+
+int check_topk(int N, int topk) {
+  if (topk < 1 || topk > N)
+    return fail(MITA_ERR_INVALID_ARG, "need 1 <= topk <= N (topk=%d, N=%d)", topk, N);
+  if (topk > kMaxTopk)
+    return fail(MITA_ERR_UNSUPPORTED, "topk=%d above this build's limit %d", topk, kMaxTopk);
+  return MITA_OK;
+}
+
+int check_s(int m, int s) {
+  if (s < 1 || s > m) return fail(MITA_ERR_INVALID_ARG, "need 1 <= s <= m (s=%d)", s);
+  if (s != 1) return fail(MITA_ERR_UNSUPPORTED, "s=%d: only s=1 is implemented", s);
+  return MITA_OK;
+}
+
+int check_grid(int N, int grid_h, int grid_w, int m) {
+  if (grid_h < 1 || grid_w < 1 || (long long)grid_h * grid_w != N)
+    return fail(MITA_ERR_INVALID_ARG, "grid %dx%d does not hold N=%d tokens", grid_h, grid_w, N);
+  if (grid_h != 1) {
+    int r = 1;
+    while ((r + 1) * (r + 1) <= m) ++r;
+    if (r * r != m)
+      return fail(MITA_ERR_INVALID_ARG, "2D pooling needs a square m (got %d)", m);
+  }
+  return MITA_OK;
+}
+
+#define MITA_TRY(x)                  \
+  do {                               \
+    int rc_ = (x);                   \
+    if (rc_ != MITA_OK) return rc_;  \
+  } while (0)
+
+#define MITA_CUDA(x, where)                            \
+  do {                                                 \
+    cudaError_t e_ = (x);                              \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// ---------------------------------------------------------------------------
+// Stage implementations (T = float or bf16)
+// ---------------------------------------------------------------------------
+template <typename T>
+int pool_impl(const T* q, int B, int H, int N, int d, int gh, int gw, int m, T* qt,
+              cudaStream_t st) {
+  MITA_TRY(check_shape(B, H, N, d));
+  MITA_TRY(check_m(N, m));
+  MITA_TRY(check_grid(N, gh, gw, m));
+  MITA_TRY(check_ptrs({{q, "q"}, {qt, "q_tilde"}}));
+  MITA_CUDA(launch_pool<T>(q, B * H, N, d, gh, gw, m, qt, st), "pool launch");
+  return MITA_OK;
+}
+
+template <typename T>
+int landmark_impl(const T* qt, const T* k, const T* v, int B, int H, int N, int d, int m,
+                  int topk, int32_t* ti, float* vt, cudaStream_t st) {
+  MITA_TRY(check_shape(B, H, N, d));
+  MITA_TRY(check_m(N, m));
+  MITA_TRY(check_topk(N, topk));
+  MITA_TRY(check_ptrs({{qt, "q_tilde"}, {k, "k"}, {v, "v"}, {ti, "topk_idx"}, {vt, "v_tilde"}}));
+  DevState* ds = nullptr;
+  MITA_TRY(device_state(&ds));
+  const LandmarkPlan plan = plan_landmark(B * H, N, d, m, topk, ds->num_sms);
+  void* ws = nullptr;
+  MITA_TRY(workspace(landmark_ws_bytes(plan, B * H, N, d, m), st, &ws));
+  const LandmarkWs lw = carve_landmark_ws(ws, plan, B * H, N, d, m);
+  MITA_CUDA(launch_landmark<T>(qt, k, v, B * H, N, d, m, topk, plan, lw, ti, vt, st),
+            "landmark launch");
+  return MITA_OK;
+}
+
+template <typename T>
+int route_impl(const T* q, const T* qt, const float* vt, int B, int H, int N, int d, int m,
+               int s, int32_t* route, float* lse, float* so, cudaStream_t st) {
+  MITA_TRY(check_shape(B, H, N, d));
+  MITA_TRY(check_m(N, m));
+  MITA_TRY(check_s(m, s));
+  MITA_TRY(check_ptrs({{q, "q"}, {qt, "q_tilde"}, {route, "route_idx"}}));
+  if (lse || so) MITA_TRY(check_ptrs({{vt, "v_tilde"}}));
+  if (so) MITA_TRY(check_ptrs({{so, "shared_o"}}));
+  MITA_CUDA(launch_route<T>(q, qt, vt, B * H, N, d, m, route, lse, so, st), "route launch");
+  return MITA_OK;
+}
+
+int bucket_impl(const int32_t* route, int B, int H, int N, int m, int s, int32_t* off,
+                int32_t* qidx, cudaStream_t st) {
+  if (B < 1 || H < 1 || N < 1) return fail(MITA_ERR_INVALID_ARG, "B, H, N must be >= 1");
+  if ((long long)B * H * N >= (1LL << 31)) return fail(MITA_ERR_UNSUPPORTED, "B*H*N >= 2^31");
+  MITA_TRY(check_m(N, m));
+  MITA_TRY(check_s(m, s));
+  if (!route || !off || !qidx) return fail(MITA_ERR_INVALID_ARG, "NULL bucket argument");
+  DevState* ds = nullptr;
+  MITA_TRY(device_state(&ds));
+  void* ws = nullptr;
+  MITA_TRY(workspace(bucket_ws_bytes(B * H, N, m), st, &ws));
+  MITA_CUDA(launch_bucket(route, B * H, N, m, ws, off, qidx, ds->status, st), "bucket launch");
+  return MITA_OK;
+}
+
+template <typename T>
+int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt,
+                const int32_t* ti, const int32_t* off, const int32_t* qidx, const float* lse,
+                const float* so, int B, int H, int N, int d, int m, int topk, int s, T* out,
+                cudaStream_t st) {
+  MITA_TRY(check_shape(B, H, N, d));
+  MITA_TRY(check_m(N, m));
+  MITA_TRY(check_topk(N, topk));
+  MITA_TRY(check_s(m, s));
+  MITA_TRY(check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}}));
+  if (!ti || !off || !qidx) return fail(MITA_ERR_INVALID_ARG, "NULL index argument");
+  if ((lse == nullptr) != (so == nullptr))
+    return fail(MITA_ERR_INVALID_ARG, "shared_lse and shared_o must be both set or both NULL");
+  if (so == nullptr) MITA_TRY(check_ptrs({{qt, "q_tilde"}, {vt, "v_tilde"}}));
+  DevState* ds = nullptr;
+  MITA_TRY(device_state(&ds));
+  MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, B * H, N, d, m, topk,
+                                  out, ds->status, st),
+            "expert launch");
+  return MITA_OK;
+}
+
+struct ForwardLayout {
+  size_t qt, vt, ti, route, off, qidx, lm, bk, total;
+  LandmarkPlan plan;
+};
+
+ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, size_t esize, int sms) {
+  ForwardLayout L{};
+  L.plan = plan_landmark(BH, N, d, m, topk, sms);
+  size_t o = 0;
+  L.qt = o; o += align256((size_t)BH * m * d * esize);
+  L.vt = o; o += align256((size_t)BH * m * d * 4);
+  L.ti = o; o += align256((size_t)BH * m * topk * 4);
+  L.route = o; o += align256((size_t)BH * N * 4);
+  L.off = o; o += align256((size_t)BH * (m + 1) * 4);
+  L.qidx = o; o += align256((size_t)BH * N * 4);
+  L.lm = o; o += align256(landmark_ws_bytes(L.plan, BH, N, d, m));
+  L.bk = o; o += align256(bucket_ws_bytes(BH, N, m));
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d, int gh, int gw,
+                 int m, int topk, int s, T* out, cudaStream_t st) {
+  MITA_TRY(check_shape(B, H, N, d));
+  MITA_TRY(check_m(N, m));
+  MITA_TRY(check_grid(N, gh, gw, m));
+  MITA_TRY(check_topk(N, topk));
+  MITA_TRY(check_s(m, s));
+  MITA_TRY(check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}}));
+  DevState* ds = nullptr;
+  MITA_TRY(device_state(&ds));
+  const int BH = B * H;
+  const ForwardLayout L = forward_layout(BH, N, d, m, topk, sizeof(T), ds->num_sms);
+  void* wsv = nullptr;
+  MITA_TRY(workspace(L.total, st, &wsv));
+  char* ws = static_cast<char*>(wsv);
+  T* qt = reinterpret_cast<T*>(ws + L.qt);
+  float* vt = reinterpret_cast<float*>(ws + L.vt);
+  int32_t* ti = reinterpret_cast<int32_t*>(ws + L.ti);
+  int32_t* route = reinterpret_cast<int32_t*>(ws + L.route);
+  int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
+  int32_t* qidx = reinterpret_cast<int32_t*>(ws + L.qidx);
+  const LandmarkWs lw = carve_landmark_ws(ws + L.lm, L.plan, BH, N, d, m);
+  MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, m, qt, st), "pool launch");
+  MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, st),
+            "landmark launch");
+  MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, st), "route launch");
+  MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st), "bucket launch");
+  MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, nullptr, nullptr, BH, N, d, m,
+                                  topk, out, ds->status, st),
+            "expert launch");
+  return MITA_OK;
+}
+
+}  // namespace
+}  // namespace mita
+
+using mita::bf16;
+
+extern "C" {
+
+int mita_pool(const void* q, int B, int H, int N, int d, int grid_h, int grid_w, int m,
+              void* q_tilde, mita_stream_t stream) {
+  return mita::pool_impl<bf16>(static_cast<const bf16*>(q), B, H, N, d, grid_h, grid_w, m,
+                               static_cast<bf16*>(q_tilde), stream);
+}
+int mita_pool_f32(const float* q, int B, int H, int N, int d, int grid_h, int grid_w, int m,
+                  float* q_tilde, mita_stream_t stream) {
+  return mita::pool_impl<float>(q, B, H, N, d, grid_h, grid_w, m, q_tilde, stream);
+}
+
+int mita_landmark_topk_shared(const void* q_tilde, const void* k, const void* v, int B, int H,
+                              int N, int d, int m, int topk, int32_t* topk_idx, float* v_tilde,
+                              mita_stream_t stream) {
+  return mita::landmark_impl<bf16>(static_cast<const bf16*>(q_tilde),
+                                   static_cast<const bf16*>(k), static_cast<const bf16*>(v), B,
+                                   H, N, d, m, topk, topk_idx, v_tilde, stream);
+}
+int mita_landmark_topk_shared_f32(const float* q_tilde, const float* k, const float* v, int B,
+                                  int H, int N, int d, int m, int topk, int32_t* topk_idx,
+                                  float* v_tilde, mita_stream_t stream) {
+  return mita::landmark_impl<float>(q_tilde, k, v, B, H, N, d, m, topk, topk_idx, v_tilde,
+                                    stream);
+}
+
+int mita_route(const void* q, const void* q_tilde, const float* v_tilde, int B, int H, int N,
+               int d, int m, int s, int32_t* route_idx, float* shared_lse, float* shared_o,
+               mita_stream_t stream) {
+  return mita::route_impl<bf16>(static_cast<const bf16*>(q), static_cast<const bf16*>(q_tilde),
+                                v_tilde, B, H, N, d, m, s, route_idx, shared_lse, shared_o,
+                                stream);
+}
+int mita_route_f32(const float* q, const float* q_tilde, const float* v_tilde, int B, int H,
+                   int N, int d, int m, int s, int32_t* route_idx, float* shared_lse,
+                   float* shared_o, mita_stream_t stream) {
+  return mita::route_impl<float>(q, q_tilde, v_tilde, B, H, N, d, m, s, route_idx, shared_lse,
+                                 shared_o, stream);
+}
+
+int mita_bucket(const int32_t* route_idx, int B, int H, int N, int m, int s,
+                int32_t* bucket_off, int32_t* bucket_qidx, mita_stream_t stream) {
+  return mita::bucket_impl(route_idx, B, H, N, m, s, bucket_off, bucket_qidx, stream);
+}
+
+int mita_expert_attn(const void* q, const void* k, const void* v, const void* q_tilde,
+                     const float* v_tilde, const int32_t* topk_idx, const int32_t* bucket_off,
+                     const int32_t* bucket_qidx, const float* shared_lse, const float* shared_o,
+                     int B, int H, int N, int d, int m, int topk, int s, void* out,
+                     mita_stream_t stream) {
+  return mita::expert_impl<bf16>(
+      static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
+      static_cast<const bf16*>(q_tilde), v_tilde, topk_idx, bucket_off, bucket_qidx, shared_lse,
+      shared_o, B, H, N, d, m, topk, s, static_cast<bf16*>(out), stream);
+}
+int mita_expert_attn_f32(const float* q, const float* k, const float* v, const float* q_tilde,
+                         const float* v_tilde, const int32_t* topk_idx,
+                         const int32_t* bucket_off, const int32_t* bucket_qidx,
+                         const float* shared_lse, const float* shared_o, int B, int H, int N,
+                         int d, int m, int topk, int s, float* out, mita_stream_t stream) {
+  return mita::expert_impl<float>(q, k, v, q_tilde, v_tilde, topk_idx, bucket_off, bucket_qidx,
+                                  shared_lse, shared_o, B, H, N, d, m, topk, s, out, stream);
+}
+
+int mita_forward(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                 int grid_h, int grid_w, int m, int topk, int s, void* out,
+                 mita_stream_t stream) {
+  return mita::forward_impl<bf16>(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                  static_cast<const bf16*>(v), B, H, N, d, grid_h, grid_w, m,
+                                  topk, s, static_cast<bf16*>(out), stream);
+}
+int mita_forward_f32(const float* q, const float* k, const float* v, int B, int H, int N, int d,
+                     int grid_h, int grid_w, int m, int topk, int s, float* out,
+                     mita_stream_t stream) {
+  return mita::forward_impl<float>(q, k, v, B, H, N, d, grid_h, grid_w, m, topk, s, out, stream);
+}
+
+uint64_t mita_forward_workspace_bytes(int B, int H, int N, int d, int m, int topk, int is_f32) {
+  if (mita::check_shape(B, H, N, d) || mita::check_m(N, m) || mita::check_topk(N, topk))
+    return 0;
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaGetLastError();
+  return mita::forward_layout(B * H, N, d, m, topk, is_f32 ? 4 : 2, sms).total;
+}
+
+const char* mita_status_string(int status) {
+  switch (status) {
+    case MITA_OK: return "ok";
+    case MITA_ERR_INVALID_ARG: return "invalid argument";
+    case MITA_ERR_UNSUPPORTED: return "unsupported by this build";
+    case MITA_ERR_CUDA: return "CUDA error";
+    case MITA_ERR_OOM: return "out of device memory";
+    case MITA_ERR_DEVICE_CHECK: return "a kernel flagged inconsistent input data";
+    default: return "unknown status";
+  }
+}
+
+const char* mita_last_error_message(void) { return mita::g_msg.c_str(); }
+
+int mita_get_last_device_error(mita_stream_t stream, int* bits) {
+  if (bits) *bits = 0;
+  mita::DevState* ds = nullptr;
+  int rc = mita::device_state(&ds);
+  if (rc != MITA_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return mita::cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, ds->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return mita::cuda_fail(e, "cudaMemcpy");
+  e = cudaMemset(ds->status, 0, sizeof(int));
+  if (e != cudaSuccess) return mita::cuda_fail(e, "cudaMemset");
+  if (bits) *bits = v;
+  return v ? mita::fail(MITA_ERR_DEVICE_CHECK, "device status bits 0x%x", v) : MITA_OK;
+}
+
+int mita_workspace_release(void) {
+  std::lock_guard<std::mutex> lk(mita::g_mu);
+  int prev = 0;
+  cudaGetDevice(&prev);
+  for (auto& kv : mita::g_ws) {
+    if (kv.second.ptr) {
+      cudaSetDevice(kv.first.first);
+      cudaDeviceSynchronize();
+      cudaFree(kv.second.ptr);
+    }
+  }
+  mita::g_ws.clear();
+  cudaSetDevice(prev);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MITA_OK : mita::cuda_fail(e, "workspace release");
+}
+
+}  // extern "C"

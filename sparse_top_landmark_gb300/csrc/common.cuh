@@ -1,0 +1,259 @@
+// Internal helpers shared by the MiTA CUDA kernels (not part of the C-ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdint>
+
+namespace mita {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------------------
+// Limits of this build (checked on the host before any launch).
+// ---------------------------------------------------------------------------
+constexpr int kMaxTopk = 4096;   // experts keep at most this many KV rows
+constexpr int kTcapMax = 64;     // per-split candidates kept by the landmark sweep
+constexpr int kBandCap = 1024;   // near-boundary candidates re-scored exactly
+constexpr int kKeyTile = 32;     // keys staged per shared-memory tile (SIMT path)
+constexpr int kExactCtas = 8;    // CTAs (and scratch rows) of the exact fallback
+
+// Bits of the per-device status word (read by mita_get_last_device_error).
+enum : int {
+  kDevErrBadIndex = 1,    // an expert index outside [0, N)
+  kDevErrBadBucket = 2,   // bucket offsets / query ids inconsistent
+  kDevErrRoute = 4,       // a routed landmark outside [0, m)
+};
+
+// Relative bound on |fp32 dot - exact dot| per unit of |a|_2 |b|_2 for a
+// length-D dot product accumulated in fp32 (sequential FMA or tensor-core
+// fp32 accumulation).  The classical bound is D * 2^-24 * sum|a_l b_l|; this
+// takes 8x that, which also covers the fp32 norms used to evaluate it.
+__host__ __device__ constexpr float err_gamma(int D) { return (float)D * 4.76837158203125e-07f; }  // D * 2^-21
+
+// ---------------------------------------------------------------------------
+// Element access
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const float* p, float* o) {
+    float4 x = *reinterpret_cast<const float4*>(p);
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+  }
+  __device__ __forceinline__ static void store(float* p, const float* o) {
+    *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+  }
+};
+template <> struct Vec<bf16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void load(const bf16* p, float* o) {
+    uint4 x = *reinterpret_cast<const uint4*>(p);
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ __forceinline__ static void store(bf16* p, const float* o) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// Load a full D-element row as floats (row start must be 16-byte aligned).
+template <typename T, int D>
+__device__ __forceinline__ void load_row(const T* p, float* o) {
+#pragma unroll
+  for (int i = 0; i < D; i += Vec<T>::N) Vec<T>::load(p + i, o + i);
+}
+template <typename T, int D>
+__device__ __forceinline__ void store_row(T* p, const float* o) {
+#pragma unroll
+  for (int i = 0; i < D; i += Vec<T>::N) Vec<T>::store(p + i, o + i);
+}
+
+// double -> T with one rounding to nearest (ties to even).
+template <typename T> __device__ T round_double(double x);
+template <> __device__ __forceinline__ float round_double<float>(double x) {
+  return __double2float_rn(x);
+}
+// Round to odd into float (24 bits), then to nearest into bf16 (8 bits): the
+// 16 spare bits make the two-step rounding equal to one direct rounding.
+template <> __device__ __forceinline__ bf16 round_double<bf16>(double x) {
+  float f = __double2float_rz(x);
+  if ((double)f != x) f = __uint_as_float(__float_as_uint(f) | 1u);
+  return __float2bfloat16_rn(f);
+}
+
+// Error-free accumulation: after any sequence of calls, s + c equals the sum
+// of the inputs up to the (second-order) rounding of c.
+__device__ __forceinline__ void two_sum_acc(float& s, float& c, float x) {
+  float t = s + x;
+  float bp = t - s;
+  float e = (s - (t - bp)) + (x - bp);
+  s = t;
+  c += e;
+}
+
+// Lexicographic order of (score, index): higher score first, then lower index.
+__device__ __forceinline__ bool ranks_before(float sa, int ia, float sb, int ib) {
+  return sa > sb || (sa == sb && ia < ib);
+}
+__device__ __forceinline__ bool ranks_before(double sa, int ia, double sb, int ib) {
+  return sa > sb || (sa == sb && ia < ib);
+}
+
+// Monotone map double -> uint64 (larger double -> larger key).
+__device__ __forceinline__ unsigned long long order_key(double x) {
+  if (x == 0.0) x = 0.0;  // fold -0 onto +0
+  unsigned long long u = (unsigned long long)__double_as_longlong(x);
+  return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+}
+
+// Exact (fp64) dot product of a T row with a double row.  Products of two
+// bf16 (or fp32) values are exact in fp64 and, for the value ranges of
+// attention inputs, so are the sums.
+template <typename T, int D>
+__device__ __forceinline__ double dot_exact(const double* a, const T* b) {
+  double acc = 0.0;
+#pragma unroll 8
+  for (int l = 0; l < D; ++l) acc = fma(a[l], (double)to_f(b[l]), acc);
+  return acc;
+}
+
+// ---------------------------------------------------------------------------
+// Warp / block helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+// Block-wide max of one float per thread; `red` needs blockDim/32 floats.
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float r = -INFINITY;
+  for (int i = 0; i < nw; ++i) r = fmaxf(r, red[i]);
+  return r;
+}
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float r = 0.f;
+  for (int i = 0; i < nw; ++i) r += red[i];
+  return r;
+}
+
+// Exclusive block scan of one int per thread; returns the block total in
+// *total.  `red` needs blockDim/32 + 1 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* red, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = warp_incl_scan(v);
+  __syncthreads();
+  if (lane == 31) red[w] = inc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < nw; ++i) { int t = red[i]; red[i] = run; run += t; }
+    red[nw] = run;
+  }
+  __syncthreads();
+  *total = red[nw];
+  return red[w] + inc - v;
+}
+
+// Bitonic sort in shared memory of P (power of two) (key, index) pairs into
+// ranks_before order (best first).  Called by the whole block.
+template <typename K>
+__device__ void bitonic_sort_desc(K* key, int* idx, int P) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
+        int lo = 2 * i - (i & (stride - 1));
+        int hi = lo + stride;
+        bool up = (lo & size) == 0;
+        K klo = key[lo], khi = key[hi];
+        int ilo = idx[lo], ihi = idx[hi];
+        bool swap = up ? ranks_before(khi, ihi, klo, ilo) : ranks_before(klo, ilo, khi, ihi);
+        if (swap) { key[lo] = khi; key[hi] = klo; idx[lo] = ihi; idx[hi] = ilo; }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Bitonic sort of P ints ascending.
+__device__ inline void bitonic_sort_int_asc(int* a, int P) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
+        int lo = 2 * i - (i & (stride - 1));
+        int hi = lo + stride;
+        bool up = (lo & size) == 0;
+        int x = a[lo], y = a[hi];
+        if (up ? (y < x) : (x < y)) { a[lo] = y; a[hi] = x; }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+__host__ __device__ __forceinline__ int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+__device__ __forceinline__ void flag_error(int* status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Half-open adaptive window [floor(i*in/out), ceil((i+1)*in/out)).
+__host__ __device__ __forceinline__ void adaptive_window(long long i, long long in,
+                                                         long long out, int* lo, int* hi) {
+  *lo = (int)((i * in) / out);
+  *hi = (int)(((i + 1) * in + out - 1) / out);
+}
+
+}  // namespace mita

@@ -1,0 +1,222 @@
+// Step 6: one joint softmax per query over the m shared pairs and the k raw
+// pairs of its routed expert, computed expert by expert.
+//
+// MiTA tutorial (iwxt.cn), ch. 4 steps 5-6 (paper eq. 11-12): all queries
+// see the m shared pairs (q~_i, v~_i); each adds the s*k raw pairs of its
+// chosen experts; the m + s*k logits (all scaled by 1/sqrt(d)) share one
+// softmax.  The bit.fan article: queries are processed grouped by expert with
+// an online softmax.  Tutorial ch. 4 also states the merge rule used when the
+// shared part arrives as a partial: (Z1 o1 + Z2 o2) / (Z1 + Z2).
+//
+// One CTA handles one tile of (up to kQTile) queries of one expert; the tile
+// is found from bucket_off (tiles of all experts of a head, in expert order).
+// The expert's K/V rows are gathered once per tile into shared memory.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mita {
+namespace {
+
+constexpr int kQTile = 64;   // queries per CTA (one per thread)
+constexpr int kRows = 32;    // KV rows staged per chunk
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kQTile)
+expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                   const T* __restrict__ q_tilde, const float* __restrict__ v_tilde,
+                   const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ bucket_off,
+                   const int32_t* __restrict__ bucket_qidx, const float* __restrict__ shared_lse,
+                   const float* __restrict__ shared_o, int N, int m, int topk,
+                   int tiles_per_bh, T* __restrict__ out, int* status) {
+  __shared__ __align__(16) float ks[kRows][D];
+  __shared__ __align__(16) float vs[kRows][D];
+  __shared__ int rowid[kRows];
+  __shared__ int s_e, s_t;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long bh = blockIdx.x / tiles_per_bh;
+  const int t = blockIdx.x % tiles_per_bh;
+  const int32_t* off = bucket_off + (size_t)bh * (m + 1);
+
+  // ---- locate (expert, tile within expert) for this CTA ---------------------
+  if (warp == 0) {
+    int run = 0, fe = -1, ft = 0;
+    for (int e0 = 0; e0 < m && fe < 0; e0 += 32) {
+      const int e = e0 + lane;
+      int cnt = 0;
+      if (e < m) {
+        const int a = off[e], b = off[e + 1];
+        if (a < 0 || b > N || b < a) flag_error(status, kDevErrBadBucket);
+        else cnt = b - a;
+      }
+      const int nt = (cnt + kQTile - 1) / kQTile;
+      const int inc = warp_incl_scan(nt);
+      const int tot = __shfl_sync(0xffffffffu, inc, 31);
+      if (t < run + tot) {
+        const unsigned hit = __ballot_sync(0xffffffffu, run + inc > t);
+        const int f = __ffs(hit) - 1;
+        const int before = __shfl_sync(0xffffffffu, inc - nt, f);
+        fe = e0 + f;
+        ft = t - (run + before);
+      }
+      run += tot;
+    }
+    if (lane == 0) { s_e = fe; s_t = ft; }
+  }
+  __syncthreads();
+  const int e = s_e;
+  if (e < 0) return;
+  const int slot = off[e] + s_t * kQTile + tid;
+  bool live = slot < off[e + 1];
+  int n = 0;
+  if (live) {
+    n = bucket_qidx[(size_t)bh * N + slot];
+    if (n < 0 || n >= N) { flag_error(status, kDevErrBadBucket); live = false; }
+  }
+
+  float qr[D];
+  if (live) load_row<T, D>(q + ((size_t)bh * N + n) * D, qr);
+  else {
+#pragma unroll
+    for (int l = 0; l < D; ++l) qr[l] = 0.f;
+  }
+  const float c = (float)(1.4426950408889634 / sqrt((double)D));
+  float mrun = -INFINITY, lsum = 0.f;
+  float acc[D];
+#pragma unroll
+  for (int l = 0; l < D; ++l) acc[l] = 0.f;
+
+  auto absorb = [&](float x, const float* vr) {
+    if (x > mrun) {
+      const float sc = exp2f(mrun - x);
+      lsum *= sc;
+#pragma unroll
+      for (int l = 0; l < D; ++l) acc[l] *= sc;
+      mrun = x;
+    }
+    const float p = exp2f(x - mrun);
+    lsum += p;
+#pragma unroll
+    for (int l = 0; l < D; ++l) acc[l] = fmaf(p, vr[l], acc[l]);
+  };
+
+  // ---- shared branch: the m pairs (q~_i, v~_i) -------------------------------
+  if (shared_o != nullptr) {
+    if (live) {
+      const size_t qi = (size_t)bh * N + n;
+      mrun = shared_lse[qi] * 1.4426950408889634f;  // natural -> log2 units
+      lsum = 1.f;
+#pragma unroll
+      for (int l = 0; l < D; ++l) acc[l] = shared_o[qi * D + l];
+    }
+  } else {
+    const T* qtb = q_tilde + (size_t)bh * m * D;
+    const float* vtb = v_tilde + (size_t)bh * m * D;
+    for (int i0 = 0; i0 < m; i0 += kRows) {
+      const int nc = min(kRows, m - i0);
+      __syncthreads();
+      for (int x = tid; x < nc * D; x += kQTile) {
+        const int r = x / D, l = x % D;
+        ks[r][l] = to_f(qtb[(size_t)(i0 + r) * D + l]);
+        vs[r][l] = vtb[(size_t)(i0 + r) * D + l];
+      }
+      __syncthreads();
+      if (!live) continue;
+      for (int r = 0; r < nc; ++r) {
+        float s = 0.f;
+#pragma unroll
+        for (int l = 0; l < D; ++l) s = fmaf(qr[l], ks[r][l], s);
+        absorb(s * c, vs[r]);
+      }
+    }
+  }
+
+  // ---- routed branch: the expert's k raw pairs ------------------------------
+  const int32_t* idx = topk_idx + ((size_t)bh * m + e) * topk;
+  const T* kb = k + (size_t)bh * N * D;
+  const T* vb = v + (size_t)bh * N * D;
+  constexpr int VEC = Vec<T>::N;
+  for (int j0 = 0; j0 < topk; j0 += kRows) {
+    const int nc = min(kRows, topk - j0);
+    __syncthreads();
+    if (tid < nc) {
+      int j = idx[j0 + tid];
+      if (j < 0 || j >= N) { flag_error(status, kDevErrBadIndex); j = -1; }
+      rowid[tid] = j;
+    }
+    __syncthreads();
+    for (int x = tid; x < nc * (D / VEC); x += kQTile) {
+      const int r = x / (D / VEC), part = (x % (D / VEC)) * VEC;
+      const int j = rowid[r];
+      float xk[VEC], xv[VEC];
+      if (j >= 0) {
+        Vec<T>::load(kb + (size_t)j * D + part, xk);
+        Vec<T>::load(vb + (size_t)j * D + part, xv);
+      } else {
+#pragma unroll
+        for (int u = 0; u < VEC; ++u) { xk[u] = 0.f; xv[u] = 0.f; }
+      }
+#pragma unroll
+      for (int u = 0; u < VEC; ++u) { ks[r][part + u] = xk[u]; vs[r][part + u] = xv[u]; }
+    }
+    __syncthreads();
+    if (!live) continue;
+    for (int r = 0; r < nc; ++r) {
+      if (rowid[r] < 0) continue;
+      float s = 0.f;
+#pragma unroll
+      for (int l = 0; l < D; ++l) s = fmaf(qr[l], ks[r][l], s);
+      absorb(s * c, vs[r]);
+    }
+  }
+  if (!live) return;
+  const float inv = 1.f / lsum;
+#pragma unroll
+  for (int l = 0; l < D; ++l) acc[l] *= inv;
+  store_row<T, D>(out + ((size_t)bh * N + n) * D, acc);
+}
+
+template <typename T, int D>
+cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt,
+                const int32_t* ti, const int32_t* off, const int32_t* qidx, const float* lse,
+                const float* so, int BH, int N, int m, int topk, T* out, int* status,
+                cudaStream_t st) {
+  const int tiles = (N + kQTile - 1) / kQTile + m;
+  const long long blocks = (long long)BH * tiles;
+  expert_attn_kernel<T, D><<<(unsigned)blocks, kQTile, 0, st>>>(
+      q, k, v, qt, vt, ti, off, qidx, lse, so, N, m, topk, tiles, out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_tilde,
+                               const float* v_tilde, const int32_t* topk_idx,
+                               const int32_t* bucket_off, const int32_t* bucket_qidx,
+                               const float* shared_lse, const float* shared_o, int BH, int N,
+                               int d, int m, int topk, T* out, int* status, cudaStream_t st) {
+#define MITA_EXPERT_CASE(DD)                                                                 \
+  case DD:                                                                                   \
+    return run<T, DD>(q, k, v, q_tilde, v_tilde, topk_idx, bucket_off, bucket_qidx,          \
+                      shared_lse, shared_o, BH, N, m, topk, out, status, st);
+  switch (d) {
+    MITA_EXPERT_CASE(16)
+    MITA_EXPERT_CASE(32)
+    MITA_EXPERT_CASE(64)
+    MITA_EXPERT_CASE(128)
+    default: return cudaErrorInvalidValue;
+  }
+#undef MITA_EXPERT_CASE
+}
+
+template cudaError_t launch_expert_attn<float>(const float*, const float*, const float*,
+                                               const float*, const float*, const int32_t*,
+                                               const int32_t*, const int32_t*, const float*,
+                                               const float*, int, int, int, int, int, float*,
+                                               int*, cudaStream_t);
+template cudaError_t launch_expert_attn<bf16>(const bf16*, const bf16*, const bf16*, const bf16*,
+                                              const float*, const int32_t*, const int32_t*,
+                                              const int32_t*, const float*, const float*, int,
+                                              int, int, int, int, bf16*, int*, cudaStream_t);
+
+}  // namespace mita

@@ -1,0 +1,73 @@
+// Host-side launchers of the MiTA kernels (internal; the C-ABI is in mita.h).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace mita {
+
+// ---- step 1: landmark pooling --------------------------------------------
+template <typename T>
+cudaError_t launch_pool(const T* q, int BH, int N, int d, int grid_h, int grid_w,
+                        int m, T* q_tilde, cudaStream_t st);
+
+// ---- steps 2-3: landmark top-k experts + shared values --------------------
+struct LandmarkPlan {
+  int RT;         // landmark rows per CTA (32, 64 or 128)
+  int nrt;        // row tiles per head
+  int Tcap;       // candidates kept per (row, split)
+  int S;          // key splits per head
+  int split_len;  // keys per split (last one may be shorter)
+  int P;          // padded candidate count per row in the merge (power of 2)
+};
+
+struct LandmarkWs {
+  float* M;        // [BH, m, S]      running max (log2 domain, scaled)
+  float* L;        // [BH, m, S]      softmax denominator at that max
+  float* A;        // [BH, m, S, d]   unnormalised numerator
+  float* cs;       // [BH, m, S, Tcap] candidate scores (unscaled fp32 dots)
+  int* ci;         // [BH, m, S, Tcap] candidate key indices
+  int* cn;         // [BH, m, S]       candidates kept
+  float* theta;    // [BH, m, S]       worst kept score if the split dropped keys, else -inf
+  float* kmax2;    // [BH, S]          max squared key norm per split
+  int* nslow;      // [1]              rows routed to the exact fallback
+  int* slow_rows;  // [BH * m]
+  double* exact;   // [kExactCtas, N]  fp64 score scratch of the fallback
+};
+
+LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms);
+size_t landmark_ws_bytes(const LandmarkPlan& p, int BH, int N, int d, int m);
+LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, int d, int m);
+
+template <typename T>
+cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, int N, int d,
+                            int m, int topk, const LandmarkPlan& plan, const LandmarkWs& ws,
+                            int32_t* topk_idx, float* v_tilde, cudaStream_t st);
+
+// ---- step 4: routing (optionally emitting the shared-branch partial) ------
+template <typename T>
+cudaError_t launch_route(const T* q, const T* q_tilde, const float* v_tilde, int BH, int N,
+                         int d, int m, int32_t* route_idx, float* shared_lse,
+                         float* shared_o, cudaStream_t st);
+
+// ---- step 5: stable grouping of queries by expert -------------------------
+constexpr int kBucketChunk = 4096;   // queries per chunk (one warp each)
+size_t bucket_ws_bytes(int BH, int N, int m);
+cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* ws,
+                          int32_t* bucket_off, int32_t* bucket_qidx, int* status,
+                          cudaStream_t st);
+
+// ---- step 6: expert-grouped joint attention -------------------------------
+template <typename T>
+cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_tilde,
+                               const float* v_tilde, const int32_t* topk_idx,
+                               const int32_t* bucket_off, const int32_t* bucket_qidx,
+                               const float* shared_lse, const float* shared_o, int BH,
+                               int N, int d, int m, int topk, T* out, int* status,
+                               cudaStream_t st);
+
+int num_sms_of_current_device();
+
+}  // namespace mita

@@ -1,0 +1,497 @@
+// Steps 2-3: routed experts (per-landmark top-k keys) and shared landmark
+// values, from one sweep over the keys.
+//
+// MiTA tutorial (iwxt.cn), ch. 4 step 2 (paper eq. 6-7): landmark i scores
+// all N keys with q~_i . k_j / sqrt(d) and keeps the top-k raw KV rows as
+// routed expert i (bit.fan article: experts may overlap and span any
+// positions).  Ch. 4 step 3 (eq. 8-9): the same N scores go through a
+// softmax over all N that weights all of V into the shared value v~_i.
+//
+// Pipeline (split-N, flash-decoding style, to fill the GPU when B*H*m is
+// small):
+//   1. landmark_partial_kernel: CTA = (head, tile of RT landmarks, key split).
+//      One thread per landmark row.  Scores are fp32 dots; an online softmax
+//      accumulates (max, sum, sum p v); a per-row min-heap in shared memory
+//      keeps the split's best Tcap (score, index) pairs.
+//   2. landmark_merge_kernel: CTA = one landmark row.  Merges the softmax
+//      partials (the merge identity of tutorial ch. 4) and selects the top-k
+//      exactly: the fp32 candidates fix a threshold tau; keys whose fp32
+//      score is within 2E of tau (E bounds the fp32 error) are re-scored in
+//      fp64, so the selected set equals the one exact scores give, ties to the
+//      lowest index.  Rows where a split might have dropped a qualifying key,
+//      or with too many near-ties, go to
+//   3. landmark_exact_kernel: fp64 scores for all N keys of the row and a
+//      radix select on (score, index) -- slow, used only for degenerate inputs
+//      (mass ties, adversarial key order).
+#include "common.cuh"
+#include "kernels.h"
+
+#include <algorithm>
+
+namespace mita {
+namespace {
+
+// Scaled log2-domain softmax constant log2(e) / sqrt(d).
+__host__ __device__ inline float softmax_scale_log2(int D) {
+  return (float)(1.4426950408889634 / sqrt((double)D));
+}
+
+// ---------------------------------------------------------------------------
+// Per-row min-heap (worst kept candidate at the root) in shared memory,
+// transposed as [slot][row] so that lanes never share a bank.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool worse(float sa, int ia, float sb, int ib) {
+  return sa < sb || (sa == sb && ia > ib);
+}
+
+template <int RT>
+__device__ __forceinline__ void heap_offer(float* hs, int* hi, int lane, int& cnt, int cap,
+                                           float s, int j) {
+  if (cnt < cap) {
+    int pos = cnt++;
+    while (pos > 0) {
+      int par = (pos - 1) >> 1;
+      float ps = hs[par * RT + lane];
+      int pi = hi[par * RT + lane];
+      if (!worse(s, j, ps, pi)) break;
+      hs[pos * RT + lane] = ps;
+      hi[pos * RT + lane] = pi;
+      pos = par;
+    }
+    hs[pos * RT + lane] = s;
+    hi[pos * RT + lane] = j;
+  } else if (s > hs[lane]) {
+    // keys arrive in increasing index order, so an equal score is worse
+    int pos = 0;
+    for (;;) {
+      int ch = 2 * pos + 1;
+      if (ch >= cap) break;
+      float cs = hs[ch * RT + lane];
+      int ci = hi[ch * RT + lane];
+      if (ch + 1 < cap) {
+        float cs2 = hs[(ch + 1) * RT + lane];
+        int ci2 = hi[(ch + 1) * RT + lane];
+        if (worse(cs2, ci2, cs, ci)) { ch = ch + 1; cs = cs2; ci = ci2; }
+      }
+      if (!worse(cs, ci, s, j)) break;
+      hs[pos * RT + lane] = cs;
+      hi[pos * RT + lane] = ci;
+      pos = ch;
+    }
+    hs[pos * RT + lane] = s;
+    hi[pos * RT + lane] = j;
+  }
+}
+
+template <typename T, int D, int RT>
+__global__ void __launch_bounds__(RT)
+landmark_partial_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k,
+                        const T* __restrict__ v, int N, int m, int S, int split_len,
+                        int Tcap, LandmarkWs ws) {
+  constexpr int KT = kKeyTile;
+  constexpr int VEC = Vec<T>::N;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* ks = reinterpret_cast<float*>(smem_raw);           // [KT][D]
+  float* vs = ks + KT * D;                                  // [KT][D]
+  float* hs = vs + KT * D;                                  // [Tcap][RT]
+  int* hi = reinterpret_cast<int*>(hs + Tcap * RT);         // [Tcap][RT]
+
+  const int nrt = (m + RT - 1) / RT;
+  long long b = blockIdx.x;
+  const int split = (int)(b % S); b /= S;
+  const int tile = (int)(b % nrt);
+  const long long bh = b / nrt;
+  const int tid = threadIdx.x;
+  const int row = tile * RT + tid;
+  const bool live = row < m;
+  const int j0 = split * split_len;
+  const int j1 = min(N, j0 + split_len);
+
+  float qr[D];
+  if (live) load_row<T, D>(q_tilde + (bh * m + row) * D, qr);
+  else {
+#pragma unroll
+    for (int l = 0; l < D; ++l) qr[l] = 0.f;
+  }
+  const float c = softmax_scale_log2(D);
+  float mrun = -INFINITY, lsum = 0.f;
+  float acc[D];
+#pragma unroll
+  for (int l = 0; l < D; ++l) acc[l] = 0.f;
+  int hcnt = 0;
+  float kmax2 = 0.f;
+
+  const T* kb = k + (size_t)bh * N * D;
+  const T* vb = v + (size_t)bh * N * D;
+  for (int jt = j0; jt < j1; jt += KT) {
+    const int nk = min(KT, j1 - jt);
+    __syncthreads();
+    for (int e = tid; e < KT * (D / VEC); e += RT) {
+      const int key = e / (D / VEC), part = (e % (D / VEC)) * VEC;
+      float xk[VEC], xv[VEC];
+      if (key < nk) {
+        Vec<T>::load(kb + (size_t)(jt + key) * D + part, xk);
+        Vec<T>::load(vb + (size_t)(jt + key) * D + part, xv);
+      } else {
+#pragma unroll
+        for (int t = 0; t < VEC; ++t) { xk[t] = 0.f; xv[t] = 0.f; }
+      }
+#pragma unroll
+      for (int t = 0; t < VEC; ++t) { ks[key * D + part + t] = xk[t]; vs[key * D + part + t] = xv[t]; }
+    }
+    __syncthreads();
+    if (live) {
+      for (int t = 0; t < nk; ++t) {
+        const float* kr = ks + t * D;
+        float sdot = 0.f;
+#pragma unroll
+        for (int l = 0; l < D; ++l) sdot = fmaf(qr[l], kr[l], sdot);
+        heap_offer<RT>(hs, hi, tid, hcnt, Tcap, sdot, jt + t);
+        const float x = sdot * c;
+        if (x > mrun) {
+          const float sc = exp2f(mrun - x);
+          lsum *= sc;
+#pragma unroll
+          for (int l = 0; l < D; ++l) acc[l] *= sc;
+          mrun = x;
+        }
+        const float p = exp2f(x - mrun);
+        lsum += p;
+        const float* vr = vs + t * D;
+#pragma unroll
+        for (int l = 0; l < D; ++l) acc[l] = fmaf(p, vr[l], acc[l]);
+      }
+    }
+    if (tid < nk) {
+      const float* kr = ks + tid * D;
+      float n2 = 0.f;
+#pragma unroll
+      for (int l = 0; l < D; ++l) n2 = fmaf(kr[l], kr[l], n2);
+      kmax2 = fmaxf(kmax2, n2);
+    }
+  }
+
+  if (tid < 32) {
+    float km = warp_max(kmax2);
+    if (tid == 0 && tile == 0) ws.kmax2[bh * S + split] = km;
+  }
+  if (!live) return;
+  const size_t rs = (size_t)(bh * m + row) * S + split;
+  ws.M[rs] = mrun;
+  ws.L[rs] = lsum;
+  float* A = ws.A + rs * D;
+#pragma unroll
+  for (int l = 0; l < D; ++l) A[l] = acc[l];
+  ws.cn[rs] = hcnt;
+  ws.theta[rs] = (j1 - j0 > Tcap) ? hs[tid] : -INFINITY;
+  float* cs = ws.cs + rs * Tcap;
+  int* ci = ws.ci + rs * Tcap;
+  for (int t = 0; t < hcnt; ++t) { cs[t] = hs[t * RT + tid]; ci[t] = hi[t * RT + tid]; }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, int N, int m,
+                      int topk, int S, int Tcap, int P, LandmarkWs ws,
+                      int32_t* __restrict__ topk_idx, float* __restrict__ v_tilde) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* us = reinterpret_cast<float*>(smem_raw);           // [P]
+  int* ui = reinterpret_cast<int*>(us + P);                 // [P]
+  double* bx = reinterpret_cast<double*>(ui + P);           // [kBandCap]
+  int* bi = reinterpret_cast<int*>(bx + kBandCap);          // [kBandCap]
+  __shared__ double qd[D];
+  __shared__ int soff[257];
+  __shared__ float red[8];
+  __shared__ int ired[9];
+  __shared__ int s_slow;
+
+  const long long rowflat = blockIdx.x;                     // bh * m + i
+  const long long bh = rowflat / m;
+  const int tid = threadIdx.x;
+  const size_t r0 = (size_t)rowflat * S;
+
+  // --- shared value: merge the split softmax partials -----------------------
+  float mx = -INFINITY;
+  for (int s = tid; s < S; s += blockDim.x) mx = fmaxf(mx, ws.M[r0 + s]);
+  mx = block_max(mx, red);
+  for (int l = tid; l < D; l += blockDim.x) {
+    float num = 0.f, den = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float w = exp2f(ws.M[r0 + s] - mx);
+      num = fmaf(w, ws.A[(r0 + s) * D + l], num);
+      den = fmaf(w, ws.L[r0 + s], den);
+    }
+    v_tilde[rowflat * D + l] = num / den;
+  }
+
+  // --- gather the kept candidates of every split -----------------------------
+  if (tid == 0) {
+    int run = 0;
+    for (int s = 0; s < S; ++s) { soff[s] = run; run += ws.cn[r0 + s]; }
+    soff[S] = run;
+    s_slow = 0;
+  }
+  for (int l = tid; l < D; l += blockDim.x) qd[l] = (double)to_f(q_tilde[rowflat * D + l]);
+  __syncthreads();
+  const int total = soff[S];
+  for (int s = 0; s < S; ++s) {
+    const int n = soff[s + 1] - soff[s];
+    for (int t = tid; t < n; t += blockDim.x) {
+      us[soff[s] + t] = ws.cs[(r0 + s) * Tcap + t];
+      ui[soff[s] + t] = ws.ci[(r0 + s) * Tcap + t];
+    }
+  }
+  for (int t = total + tid; t < P; t += blockDim.x) { us[t] = -INFINITY; ui[t] = 0x7fffffff; }
+  bitonic_sort_desc(us, ui, P);
+
+  // --- threshold and fp32 error bound ---------------------------------------
+  float qn2 = 0.f;
+  for (int l = tid; l < D; l += blockDim.x) qn2 += (float)(qd[l] * qd[l]);
+  qn2 = block_sum(qn2, red);
+  float km2 = 0.f;
+  for (int s = tid; s < S; s += blockDim.x) km2 = fmaxf(km2, ws.kmax2[bh * S + s]);
+  km2 = block_max(km2, red);
+  const float E = err_gamma(D) * sqrtf(qn2) * sqrtf(km2);
+  bool slow = total < topk;
+  const float tau = slow ? 0.f : us[topk - 1];
+  const float lo_band = tau - 2.f * E, hi_band = tau + 2.f * E;
+  if (!slow) {
+    // a split that dropped keys scoring at or above tau - 2E may hide a member
+    for (int s = tid; s < S; s += blockDim.x)
+      if (ws.theta[r0 + s] >= lo_band) s_slow = 1;
+  }
+  __syncthreads();
+  slow = slow || s_slow;
+  int a = 0, bnd_end = 0;
+  if (!slow) {
+    // us is sorted best first: [0, a) above the band, [a, bnd_end) in it
+    int ca = 0, cb = 0;
+    for (int t = tid; t < total; t += blockDim.x) {
+      ca += us[t] > hi_band;
+      cb += us[t] >= lo_band;
+    }
+    int dummy;
+    a = block_excl_scan(ca, ired, &dummy);   // total of ca lands in `dummy`
+    a = dummy;
+    __syncthreads();
+    block_excl_scan(cb, ired, &bnd_end);
+    if (bnd_end - a > kBandCap) slow = true;
+  }
+  if (slow) {
+    if (tid == 0) {
+      const int p = atomicAdd(ws.nslow, 1);
+      ws.slow_rows[p] = (int)rowflat;
+    }
+    return;
+  }
+
+  // --- exact re-scoring of the band -------------------------------------------
+  const int nb = bnd_end - a;
+  const int PB = next_pow2(max(nb, 1));
+  const T* kb = k + (size_t)bh * N * D;
+  for (int t = tid; t < PB; t += blockDim.x) {
+    if (t < nb) {
+      const int j = ui[a + t];
+      bx[t] = dot_exact<T, D>(qd, kb + (size_t)j * D);
+      bi[t] = j;
+    } else {
+      bx[t] = -INFINITY;
+      bi[t] = 0x7fffffff;
+    }
+  }
+  bitonic_sort_desc(bx, bi, PB);
+
+  // --- output: the a sure members plus the best (topk - a) of the band, ascending
+  const int need = topk - a;
+  const int PK = next_pow2(topk);
+  __syncthreads();
+  // reuse ui[topk..] region is not safe (ui holds the sure members); write the
+  // output set into `us` reinterpreted as ints.
+  int* outset = reinterpret_cast<int*>(us);
+  for (int t = tid; t < PK; t += blockDim.x) {
+    int val;
+    if (t < a) val = ui[t];
+    else if (t < topk) val = bi[t - a];
+    else val = 0x7fffffff;
+    outset[t] = val;
+  }
+  (void)need;
+  bitonic_sort_int_asc(outset, PK);
+  for (int t = tid; t < topk; t += blockDim.x) topk_idx[rowflat * topk + t] = outset[t];
+}
+
+// Exact fallback: fp64 scores of all N keys, radix select on the monotone
+// 64-bit key, ties at the k-th value resolved by the lowest index.
+template <typename T, int D>
+__global__ void __launch_bounds__(512)
+landmark_exact_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, int N, int m,
+                      int topk, LandmarkWs ws, int32_t* __restrict__ topk_idx) {
+  __shared__ double qd[D];
+  __shared__ int hist[256];
+  __shared__ int ired[17];
+  __shared__ unsigned long long s_prefix;
+  __shared__ int s_need;
+  double* sc = ws.exact + (size_t)blockIdx.x * N;
+  const int tid = threadIdx.x;
+  const int nslow = *ws.nslow;
+  for (int w = blockIdx.x; w < nslow; w += gridDim.x) {
+    const long long rowflat = ws.slow_rows[w];
+    const long long bh = rowflat / m;
+    __syncthreads();
+    for (int l = tid; l < D; l += blockDim.x) qd[l] = (double)to_f(q_tilde[rowflat * D + l]);
+    __syncthreads();
+    const T* kb = k + (size_t)bh * N * D;
+    for (int j = tid; j < N; j += blockDim.x) sc[j] = dot_exact<T, D>(qd, kb + (size_t)j * D);
+    if (tid == 0) { s_prefix = 0ull; s_need = topk; }
+    unsigned long long mask = 0ull;
+    for (int pass = 0; pass < 8; ++pass) {
+      const int shift = 56 - 8 * pass;
+      for (int t = tid; t < 256; t += blockDim.x) hist[t] = 0;
+      __syncthreads();
+      const unsigned long long prefix = s_prefix;
+      for (int j = tid; j < N; j += blockDim.x) {
+        const unsigned long long u = order_key(sc[j]);
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255], 1);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int need = s_need, cum = 0, dg = 255;
+        for (; dg > 0; --dg) {
+          if (cum + hist[dg] >= need) break;
+          cum += hist[dg];
+        }
+        s_need = need - cum;
+        s_prefix = prefix | ((unsigned long long)dg << shift);
+      }
+      mask |= 0xffull << shift;
+      __syncthreads();
+    }
+    const unsigned long long kstar = s_prefix;
+    const int need_eq = s_need;           // how many keys equal to kstar to take
+    int out_base = 0, eq_base = 0;
+    for (int j0 = 0; j0 < N; j0 += blockDim.x) {
+      const int j = j0 + tid;
+      unsigned long long u = 0ull;
+      if (j < N) u = order_key(sc[j]);
+      const int is_eq = (j < N && u == kstar) ? 1 : 0;
+      int eq_tot;
+      const int eq_rank = eq_base + block_excl_scan(is_eq, ired, &eq_tot);
+      const int take = (j < N) && (u > kstar || (is_eq && eq_rank < need_eq));
+      int take_tot;
+      const int pos = out_base + block_excl_scan(take, ired, &take_tot);
+      if (take && pos < topk) topk_idx[rowflat * topk + pos] = j;
+      out_base += take_tot;
+      eq_base += eq_tot;
+    }
+  }
+}
+
+template <typename T, int D, int RT>
+cudaError_t run_partial(const T* qt, const T* k, const T* v, int BH, int N, int m,
+                        const LandmarkPlan& p, const LandmarkWs& ws, cudaStream_t st) {
+  const size_t smem = (size_t)2 * kKeyTile * D * sizeof(float) + (size_t)p.Tcap * RT * 8;
+  auto kern = landmark_partial_kernel<T, D, RT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)BH * p.nrt * p.S;
+  kern<<<(unsigned)blocks, RT, smem, st>>>(qt, k, v, N, m, p.S, p.split_len, p.Tcap, ws);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int topk,
+                const LandmarkPlan& p, const LandmarkWs& ws, int32_t* topk_idx, float* vt,
+                cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ws.nslow, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  switch (p.RT) {
+    case 32: e = run_partial<T, D, 32>(qt, k, v, BH, N, m, p, ws, st); break;
+    case 64: e = run_partial<T, D, 64>(qt, k, v, BH, N, m, p, ws, st); break;
+    default: e = run_partial<T, D, 128>(qt, k, v, BH, N, m, p, ws, st); break;
+  }
+  if (e != cudaSuccess) return e;
+  const size_t msmem = (size_t)p.P * 8 + (size_t)kBandCap * 12;
+  auto mk = landmark_merge_kernel<T, D>;
+  e = cudaFuncSetAttribute(mk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+  if (e != cudaSuccess) return e;
+  mk<<<(unsigned)((long long)BH * m), 256, msmem, st>>>(qt, k, N, m, topk, p.S, p.Tcap, p.P,
+                                                        ws, topk_idx, vt);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  landmark_exact_kernel<T, D><<<kExactCtas, 512, 0, st>>>(qt, k, N, m, topk, ws, topk_idx);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms) {
+  (void)d;
+  LandmarkPlan p{};
+  p.RT = m >= 128 ? 128 : (m > 32 ? 64 : 32);
+  p.nrt = (m + p.RT - 1) / p.RT;
+  p.Tcap = std::min(kTcapMax, topk + 32);
+  const long long ctas_per_split = (long long)BH * p.nrt;
+  const long long target = 2LL * std::max(num_sms, 1);
+  int s_occ = (int)std::max(1LL, (target + ctas_per_split - 1) / ctas_per_split);
+  int s_need = (p.Tcap < topk + 32) ? (2 * (topk + 32) + p.Tcap - 1) / p.Tcap : 1;
+  int S = std::max(s_occ, s_need);
+  S = std::min(S, std::max(1, (N + 31) / 32));      // at least 32 keys per split
+  S = std::min(S, std::max(s_need, 256));
+  p.split_len = (N + S - 1) / S;
+  p.S = (N + p.split_len - 1) / p.split_len;        // no empty split
+  p.P = next_pow2(std::max(p.S * p.Tcap, 2));
+  return p;
+}
+
+size_t landmark_ws_bytes(const LandmarkPlan& p, int BH, int N, int d, int m) {
+  const size_t rows = (size_t)BH * m, rs = rows * p.S;
+  size_t b = 0;
+  auto add = [&](size_t n) { b += (n + 255) / 256 * 256; };
+  add(rs * 4); add(rs * 4); add(rs * d * 4);
+  add(rs * p.Tcap * 4); add(rs * p.Tcap * 4);
+  add(rs * 4); add(rs * 4);
+  add((size_t)BH * p.S * 4);
+  add(4); add(rows * 4);
+  add((size_t)kExactCtas * N * 8);
+  return b;
+}
+
+LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, int d, int m) {
+  const size_t rows = (size_t)BH * m, rs = rows * p.S;
+  char* c = static_cast<char*>(base);
+  auto take = [&](size_t n) { char* r = c; c += (n + 255) / 256 * 256; return r; };
+  LandmarkWs w;
+  w.M = (float*)take(rs * 4);
+  w.L = (float*)take(rs * 4);
+  w.A = (float*)take(rs * d * 4);
+  w.cs = (float*)take(rs * p.Tcap * 4);
+  w.ci = (int*)take(rs * p.Tcap * 4);
+  w.cn = (int*)take(rs * 4);
+  w.theta = (float*)take(rs * 4);
+  w.kmax2 = (float*)take((size_t)BH * p.S * 4);
+  w.nslow = (int*)take(4);
+  w.slow_rows = (int*)take(rows * 4);
+  w.exact = (double*)take((size_t)kExactCtas * N * 8);
+  return w;
+}
+
+template <typename T>
+cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, int N, int d,
+                            int m, int topk, const LandmarkPlan& plan, const LandmarkWs& ws,
+                            int32_t* topk_idx, float* v_tilde, cudaStream_t st) {
+  switch (d) {
+    case 16: return run<T, 16>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, st);
+    case 32: return run<T, 32>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, st);
+    case 64: return run<T, 64>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, st);
+    case 128: return run<T, 128>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template cudaError_t launch_landmark<float>(const float*, const float*, const float*, int, int,
+                                            int, int, int, const LandmarkPlan&,
+                                            const LandmarkWs&, int32_t*, float*, cudaStream_t);
+template cudaError_t launch_landmark<bf16>(const bf16*, const bf16*, const bf16*, int, int, int,
+                                           int, int, const LandmarkPlan&, const LandmarkWs&,
+                                           int32_t*, float*, cudaStream_t);
+
+}  // namespace mita

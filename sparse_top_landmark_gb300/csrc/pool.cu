@@ -1,0 +1,96 @@
+// Step 1: landmark queries by local average pooling of Q.
+//
+// MiTA tutorial (iwxt.cn), ch. 4 step 1 (paper Sec. 3.2, eq. 5): every
+// landmark query is the mean of a group of queries; the bit.fan article calls
+// it local average pooling; tutorial ch. 5 pools a 2 x 4 token grid in 2D.
+// Windows follow the adaptive-average-pool rule on the grid_h x grid_w token
+// grid (1D: 1 x N pooled to 1 x m; 2D: pooled to sqrt(m) x sqrt(m)).
+//
+// HBM-bound: one CTA per landmark streams its window once with 16-byte loads.
+// Sums are error-free per thread (fp32 two-sum) and combined in fp64, so the
+// mean is rounded once into the input dtype -- the same value an fp64 mean
+// rounded to nearest gives.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mita {
+namespace {
+
+constexpr int kPoolThreads = 256;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kPoolThreads)
+pool_kernel(const T* __restrict__ q, int N, int grid_h, int grid_w, int mh, int mw,
+            T* __restrict__ q_tilde) {
+  constexpr int VEC = Vec<T>::N;
+  constexpr int NV = D / VEC;              // 16-byte vectors per row
+  constexpr int TL = kPoolThreads / NV;    // token lanes
+  static_assert(D % VEC == 0, "row must be a whole number of 16-byte vectors");
+  __shared__ double red[TL][D];
+
+  const int m = mh * mw;
+  const long long flat = blockIdx.x;       // bh * m + i
+  const int i = (int)(flat % m);
+  const long long bh = flat / m;
+  int r0, r1, c0, c1;
+  adaptive_window(i / mw, grid_h, mh, &r0, &r1);
+  adaptive_window(i % mw, grid_w, mw, &c0, &c1);
+  const int nc = c1 - c0;
+  const int cnt = (r1 - r0) * nc;
+
+  const int vlane = threadIdx.x % NV, tl = threadIdx.x / NV;
+  float s[VEC], c[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) { s[e] = 0.f; c[e] = 0.f; }
+  const T* base = q + (size_t)bh * N * D + vlane * VEC;
+  for (int t = tl; t < cnt; t += TL) {
+    const int r = r0 + t / nc, col = c0 + t % nc;
+    float x[VEC];
+    Vec<T>::load(base + ((size_t)r * grid_w + col) * D, x);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) two_sum_acc(s[e], c[e], x[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) red[tl][vlane * VEC + e] = (double)s[e] + (double)c[e];
+  __syncthreads();
+  for (int l = threadIdx.x; l < D; l += kPoolThreads) {
+    double acc = 0.0;
+    for (int t = 0; t < TL; ++t) acc += red[t][l];
+    q_tilde[flat * D + l] = round_double<T>(acc / (double)cnt);
+  }
+}
+
+template <typename T, int D>
+cudaError_t run(const T* q, int BH, int N, int grid_h, int grid_w, int m, T* qt,
+                cudaStream_t st) {
+  int mh = 1, mw = m;
+  if (grid_h != 1) {
+    int r = 1;
+    while ((r + 1) * (r + 1) <= m) ++r;
+    mh = mw = r;
+  }
+  const long long blocks = (long long)BH * m;
+  pool_kernel<T, D><<<(unsigned)blocks, kPoolThreads, 0, st>>>(q, N, grid_h, grid_w, mh, mw, qt);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_pool(const T* q, int BH, int N, int d, int grid_h, int grid_w, int m,
+                        T* q_tilde, cudaStream_t st) {
+  switch (d) {
+    case 16: return run<T, 16>(q, BH, N, grid_h, grid_w, m, q_tilde, st);
+    case 32: return run<T, 32>(q, BH, N, grid_h, grid_w, m, q_tilde, st);
+    case 64: return run<T, 64>(q, BH, N, grid_h, grid_w, m, q_tilde, st);
+    case 128: return run<T, 128>(q, BH, N, grid_h, grid_w, m, q_tilde, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template cudaError_t launch_pool<float>(const float*, int, int, int, int, int, int, float*,
+                                        cudaStream_t);
+template cudaError_t launch_pool<bf16>(const bf16*, int, int, int, int, int, int, bf16*,
+                                       cudaStream_t);
+
+}  // namespace mita

@@ -1,0 +1,42 @@
+"""Shared comparison rules of the GPU-vs-oracle parity tests.
+
+Rules (applied element by element on the same seeded inputs):
+  * index outputs (top-k sets, routes, buckets) match bit-exactly, except a
+    row whose oracle score gap at the selection boundary is below 1e-6
+    relative to that row's largest |score| (then either choice is correct);
+  * float outputs: fp32 inputs -> max-abs error <= 1e-4; bf16 inputs ->
+    max-abs error <= 2e-2 and relative L2 error <= 5e-3.
+"""
+import torch
+
+GAP_TOL = 1e-6
+F32_MAX_ABS = 1e-4
+BF16_MAX_ABS = 2e-2
+BF16_REL_L2 = 5e-3
+
+
+def assert_index_sets_match(gpu, ora, gap, what="top-k"):
+    """gpu/ora: [..., k] int index lists (ascending), gap: [...] oracle gaps."""
+    g = gpu.to("cpu").to(torch.int64).reshape(-1, gpu.shape[-1])
+    o = ora.to("cpu").to(torch.int64).reshape(-1, ora.shape[-1])
+    gp = gap.to("cpu").reshape(-1)
+    diff = (g != o).any(-1)
+    bad = diff & (gp >= GAP_TOL)
+    nbad = int(bad.sum())
+    assert nbad == 0, (f"{what}: {nbad} rows differ with oracle gap >= {GAP_TOL} "
+                       f"(first row {int(bad.nonzero()[0])})")
+    return int(diff.sum())
+
+
+def assert_close(gpu, ora, dtype, what="output"):
+    g = gpu.to("cpu").double()
+    o = ora.to("cpu").double()
+    err = (g - o).abs()
+    mx = err.max().item() if err.numel() else 0.0
+    if dtype == torch.float32:
+        assert mx <= F32_MAX_ABS, f"{what}: max-abs {mx:.3e} > {F32_MAX_ABS}"
+    else:
+        rel = (torch.linalg.vector_norm(g - o) / torch.linalg.vector_norm(o).clamp_min(1e-30)).item()
+        assert mx <= BF16_MAX_ABS, f"{what}: max-abs {mx:.3e} > {BF16_MAX_ABS}"
+        assert rel <= BF16_REL_L2, f"{what}: rel-L2 {rel:.3e} > {BF16_REL_L2}"
+    return mx
