@@ -132,6 +132,29 @@ int mita_bucket(const int32_t* route_idx, int B, int H, int N, int m, int s,
                 int32_t* bucket_off, int32_t* bucket_qidx, mita_stream_t stream);
 
 /*
+ * mita_bucket_noalloc -- mita_bucket for callers that cannot allocate device
+ * memory.  The paper has no counterpart: this is an engineering variant.
+ * Callers that own every byte of device memory through their own allocator,
+ * or that forbid allocation after start-up (real-time loops), cannot let the
+ * library grow its workspace cache.  This entry point computes exactly what
+ * mita_bucket computes but keeps its counters in a fixed 4 MiB device array
+ * compiled into the library (held by every GPU that loads it until exit), so
+ * it calls no allocator at all.
+ *   Same arguments and outputs as mita_bucket.
+ *   Limit: B*H*ceil(N/4096)*m <= 1048576, else MITA_ERR_UNSUPPORTED and
+ *   nothing runs.
+ *   The array is shared by every call and keeps the last call's contents;
+ *   each call clears what it uses first.  Calls that overlap on the GPU
+ *   (unordered streams) race on it: order them.
+ *   The first call on a device looks up the array's address with that device
+ *   current; make it before any stream capture starts.
+ *   Out-of-range route values are skipped but not recorded in the status word
+ *   of mita_get_last_device_error.
+ */
+int mita_bucket_noalloc(const int32_t* route_idx, int B, int H, int N, int m, int s,
+                        int32_t* bucket_off, int32_t* bucket_qidx, mita_stream_t stream);
+
+/*
  * mita_expert_attn -- joint softmax over the shared pairs and the routed
  * expert's raw pairs, computed expert by expert.
  * Tutorial ch. 4 steps 5-6 (eq. 11-12): logits [q . q~_i / sqrt(d)]_{i<m}

@@ -311,6 +311,9 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
 }
 
 }  // namespace
+
+int report_error(int code, const char* text) { return fail(code, "%s", text); }
+
 }  // namespace mita
 
 using mita::bf16;

@@ -1,0 +1,87 @@
+// mita_bucket_noalloc: the bucket step for callers that cannot allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc (or let this library call it for them):
+// code running while a custom allocator owns all device memory, real-time
+// loops that forbid allocation after start-up, or hosts where the CUDA
+// memory pool is disabled.  This entry point does the same stable grouping as
+// mita_bucket, but its per-chunk counters live in a fixed, file-scope device
+// array instead of the library's workspace cache, so it never allocates.
+//
+// Limits and sharing rules:
+//   * The array holds kNoAllocScratchInts int32 counters (4 MiB).  A call
+//     needs B*H*ceil(N/4096)*m of them; larger calls are rejected with
+//     MITA_ERR_UNSUPPORTED before anything runs.
+//   * Every GPU that loads this library's module keeps the 4 MiB until the
+//     process exits.
+//   * All calls share the one array, and it keeps whatever the last call
+//     left there.  Each call clears the counters it uses before use.  Calls
+//     whose executions overlap on the GPU (different streams, no ordering
+//     between them) race on the array and give wrong results: order them.
+//   * The first call on a device looks up the array's device address
+//     (cudaGetSymbolAddress) with that device current and caches it.  Make
+//     that first call before any stream capture begins.
+//   * Route values outside [0, m) are skipped, as in mita_bucket, but are not
+//     recorded in the status word read by mita_get_last_device_error (that
+//     word needs a one-time allocation).
+#include "mita.h"
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mita {
+namespace {
+
+constexpr size_t kNoAllocScratchInts = size_t(1) << 20;   // 4 MiB of int32
+
+static __device__ __align__(256) int g_bucket_scratch[kNoAllocScratchInts];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_na_mu;
+void* g_na_ptr[kMaxDevices] = {};
+
+}  // namespace
+}  // namespace mita
+
+extern "C" int mita_bucket_noalloc(const int32_t* route_idx, int B, int H, int N, int m, int s,
+                                   int32_t* bucket_off, int32_t* bucket_qidx,
+                                   mita_stream_t stream) {
+  using namespace mita;
+  if (B < 1 || H < 1 || N < 1 || (long long)B * H * N >= (1LL << 31) || m < 1 || m > N ||
+      s < 1 || s > m)
+    return report_error(MITA_ERR_INVALID_ARG, "mita_bucket_noalloc: invalid B, H, N, m or s");
+  if (s != 1) return report_error(MITA_ERR_UNSUPPORTED, "mita_bucket_noalloc: only s = 1");
+  if (!route_idx || !bucket_off || !bucket_qidx)
+    return report_error(MITA_ERR_INVALID_ARG, "mita_bucket_noalloc: NULL argument");
+  const size_t need = bucket_ws_bytes(B * H, N, m);
+  if (need > kNoAllocScratchInts * sizeof(int))
+    return report_error(MITA_ERR_UNSUPPORTED,
+                        "mita_bucket_noalloc: B*H*ceil(N/4096)*m exceeds the 1048576 counters "
+                        "(4 MiB) of its static scratch; use mita_bucket");
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return report_error(MITA_ERR_CUDA, "mita_bucket_noalloc: no current CUDA device");
+  }
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    if (g_na_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_bucket_scratch);
+      if (e != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return report_error(MITA_ERR_CUDA, "mita_bucket_noalloc: cudaGetSymbolAddress failed");
+      }
+      g_na_ptr[dev] = p;
+    }
+    scratch = g_na_ptr[dev];
+  }
+  const cudaError_t e =
+      launch_bucket(route_idx, B * H, N, m, scratch, bucket_off, bucket_qidx, nullptr, stream);
+  return e == cudaSuccess ? MITA_OK
+                          : report_error(MITA_ERR_CUDA, "mita_bucket_noalloc: launch failed");
+}

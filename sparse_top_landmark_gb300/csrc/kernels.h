@@ -70,4 +70,8 @@ cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_ti
 
 int num_sms_of_current_device();
 
+// Records `text` as the message mita_last_error_message() returns on this
+// thread and returns `code`.
+int report_error(int code, const char* text);
+
 }  // namespace mita

@@ -59,6 +59,8 @@ def load() -> ctypes.CDLL:
                     f.restype = I
             lib.mita_bucket.argtypes = [P, I, I, I, I, I, P, P, P]
             lib.mita_bucket.restype = I
+            lib.mita_bucket_noalloc.argtypes = [P, I, I, I, I, I, P, P, P]
+            lib.mita_bucket_noalloc.restype = I
             lib.mita_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
             lib.mita_forward_workspace_bytes.restype = ctypes.c_uint64
             lib.mita_status_string.argtypes = [I]
@@ -181,6 +183,20 @@ def mita_bucket(route_idx, m: int, bucket_off=None, bucket_qidx=None, stream=Non
     _need(bucket_qidx, "bucket_qidx", torch.int32, route_idx.device)
     _check(load().mita_bucket(_ptr(route_idx), B, H, N, m, s, _ptr(bucket_off),
                               _ptr(bucket_qidx), _stream(stream, route_idx.device)))
+    return bucket_off, bucket_qidx
+
+
+def mita_bucket_noalloc(route_idx, m: int, bucket_off, bucket_qidx, stream=None):
+    """mita_bucket for callers that cannot allocate device memory: the caller
+    passes both outputs, and the library uses its fixed 4 MiB device scratch
+    instead of its workspace cache (limit B*H*ceil(N/4096)*m <= 1048576).
+    Calls that overlap on the GPU race on that scratch; order them."""
+    _need(route_idx, "route_idx", torch.int32)
+    B, H, N, s = route_idx.shape
+    _need(bucket_off, "bucket_off", torch.int32, route_idx.device)
+    _need(bucket_qidx, "bucket_qidx", torch.int32, route_idx.device)
+    _check(load().mita_bucket_noalloc(_ptr(route_idx), B, H, N, m, s, _ptr(bucket_off),
+                                      _ptr(bucket_qidx), _stream(stream, route_idx.device)))
     return bucket_off, bucket_qidx
 
 
