@@ -7,6 +7,7 @@
 #include <map>
 #include <mutex>
 #include <string>
+#include <type_traits>
 #include <utility>
 
 #include "common.cuh"
@@ -196,13 +197,26 @@ int landmark_impl(const T* qt, const T* k, const T* v, int B, int H, int N, int 
   MITA_TRY(check_ptrs({{qt, "q_tilde"}, {k, "k"}, {v, "v"}, {ti, "topk_idx"}, {vt, "v_tilde"}}));
   DevState* ds = nullptr;
   MITA_TRY(device_state(&ds));
-  const LandmarkPlan plan = plan_landmark(B * H, N, d, m, topk, ds->num_sms);
+  const LandmarkPlan plan =
+      plan_landmark(B * H, N, d, m, topk, ds->num_sms, std::is_same<T, bf16>::value);
   void* ws = nullptr;
   MITA_TRY(workspace(landmark_ws_bytes(plan, B * H, N, d, m), st, &ws));
   const LandmarkWs lw = carve_landmark_ws(ws, plan, B * H, N, d, m);
-  MITA_CUDA(launch_landmark<T>(qt, k, v, B * H, N, d, m, topk, plan, lw, ti, vt, st),
+  MITA_CUDA(launch_landmark<T>(qt, k, v, B * H, N, d, m, topk, plan, lw, ti, vt, ds->status, st),
             "landmark launch");
   return MITA_OK;
+}
+
+// Tensor-core route for bf16 / d = 64 / m <= 512 when no shared partial is
+// requested; the SIMT kernel otherwise.
+template <typename T>
+cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int N, int d, int m,
+                           int32_t* route, float* lse, float* so, DevState* ds, cudaStream_t st) {
+  if constexpr (std::is_same<T, bf16>::value) {
+    if (!lse && !so && route_tc_supported(d, m))
+      return launch_route_tc(q, qt, BH, N, m, ds->num_sms, route, ds->status, st);
+  }
+  return launch_route<T>(q, qt, vt, BH, N, d, m, route, lse, so, st);
 }
 
 template <typename T>
@@ -214,7 +228,9 @@ int route_impl(const T* q, const T* qt, const float* vt, int B, int H, int N, in
   MITA_TRY(check_ptrs({{q, "q"}, {qt, "q_tilde"}, {route, "route_idx"}}));
   if (lse || so) MITA_TRY(check_ptrs({{vt, "v_tilde"}}));
   if (so) MITA_TRY(check_ptrs({{so, "shared_o"}}));
-  MITA_CUDA(launch_route<T>(q, qt, vt, B * H, N, d, m, route, lse, so, st), "route launch");
+  DevState* ds = nullptr;
+  MITA_TRY(device_state(&ds));
+  MITA_CUDA(route_dispatch<T>(q, qt, vt, B * H, N, d, m, route, lse, so, ds, st), "route launch");
   return MITA_OK;
 }
 
@@ -262,7 +278,7 @@ struct ForwardLayout {
 
 ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, size_t esize, int sms) {
   ForwardLayout L{};
-  L.plan = plan_landmark(BH, N, d, m, topk, sms);
+  L.plan = plan_landmark(BH, N, d, m, topk, sms, esize == 2);
   size_t o = 0;
   L.qt = o; o += align256((size_t)BH * m * d * esize);
   L.vt = o; o += align256((size_t)BH * m * d * 4);
@@ -300,9 +316,10 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   int32_t* qidx = reinterpret_cast<int32_t*>(ws + L.qidx);
   const LandmarkWs lw = carve_landmark_ws(ws + L.lm, L.plan, BH, N, d, m);
   MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, m, qt, st), "pool launch");
-  MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, st),
+  MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, ds->status, st),
             "landmark launch");
-  MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, st), "route launch");
+  MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, ds, st),
+            "route launch");
   MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st), "bucket launch");
   MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, nullptr, nullptr, BH, N, d, m,
                                   topk, out, ds->status, st),

@@ -25,6 +25,7 @@ enum : int {
   kDevErrBadIndex = 1,    // an expert index outside [0, N)
   kDevErrBadBucket = 2,   // bucket offsets / query ids inconsistent
   kDevErrRoute = 4,       // a routed landmark outside [0, m)
+  kDevErrTimeout = 8,     // a bounded wait inside a kernel gave up
 };
 
 // Relative bound on |fp32 dot - exact dot| per unit of |a|_2 |b|_2 for a
@@ -98,14 +99,49 @@ template <> __device__ __forceinline__ bf16 round_double<bf16>(double x) {
 }
 
 // Error-free accumulation: after any sequence of calls, s + c equals the sum
-// of the inputs up to the (second-order) rounding of c.
+// of the inputs up to the (second-order) rounding of c.  The _rn intrinsics
+// keep the compiler from contracting or reassociating the two-sum.
 __device__ __forceinline__ void two_sum_acc(float& s, float& c, float x) {
-  float t = s + x;
-  float bp = t - s;
-  float e = (s - (t - bp)) + (x - bp);
+  const float t = __fadd_rn(s, x);
+  const float bp = __fsub_rn(t, s);
+  const float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(x, bp));
   s = t;
-  c += e;
+  c = __fadd_rn(c, e);
 }
+
+// A value carried as an unevaluated sum hi + lo (|lo| <= ulp(hi) / 2).
+struct F2 {
+  float hi, lo;
+};
+__device__ __forceinline__ F2 f2_normalize(float s, float c) {
+  const float hi = __fadd_rn(s, c);
+  return {hi, __fsub_rn(c, __fsub_rn(hi, s))};
+}
+__device__ __forceinline__ bool f2_greater(F2 x, F2 y) {
+  return x.hi > y.hi || (x.hi == y.hi && x.lo > y.lo);
+}
+__device__ __forceinline__ bool ranks_before(F2 a, int ia, F2 b, int ib) {
+  return f2_greater(a, b) || (a.hi == b.hi && a.lo == b.lo && ia < ib);
+}
+
+// Dot product with every product split exactly (two-product via FMA) and
+// every sum error-free (two-sum): hi + lo is the exact dot up to ~n * 2^-48
+// relative -- exact enough to order candidates whose exact scores differ by
+// far less than the 1e-6 relative gap the parity rule allows.  fp32 only:
+// fp64 runs at a small fraction of the fp32 rate on this part.
+template <int D>
+__device__ __forceinline__ F2 dot_f2(const float* a, const float* b) {
+  float s = 0.f, c = 0.f;
+#pragma unroll 8
+  for (int l = 0; l < D; ++l) {
+    const float p = __fmul_rn(a[l], b[l]);
+    const float e = fmaf(a[l], b[l], -p);
+    two_sum_acc(s, c, p);
+    c = __fadd_rn(c, e);
+  }
+  return f2_normalize(s, c);
+}
+
 
 // Lexicographic order of (score, index): higher score first, then lower index.
 __device__ __forceinline__ bool ranks_before(float sa, int ia, float sb, int ib) {

@@ -1,6 +1,8 @@
 // Host-side launchers of the MiTA kernels (internal; the C-ABI is in mita.h).
 #pragma once
 
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -15,12 +17,15 @@ cudaError_t launch_pool(const T* q, int BH, int N, int d, int grid_h, int grid_w
 
 // ---- steps 2-3: landmark top-k experts + shared values --------------------
 struct LandmarkPlan {
+  bool tc;        // tensor-core two-pass path (bf16, d = 64, long N)
   int RT;         // landmark rows per CTA (32, 64 or 128)
   int nrt;        // row tiles per head
-  int Tcap;       // candidates kept per (row, split)
+  int Tcap;       // candidates kept per (row, split)          (SIMT path)
   int S;          // key splits per head
   int split_len;  // keys per split (last one may be shorter)
   int P;          // padded candidate count per row in the merge (power of 2)
+  int ntiles;     // 128-key tiles per head                      (tc path)
+  int cap;        // candidate capacity per row                  (tc path)
 };
 
 struct LandmarkWs {
@@ -35,16 +40,30 @@ struct LandmarkWs {
   int* nslow;      // [1]              rows routed to the exact fallback
   int* slow_rows;  // [BH * m]
   double* exact;   // [kExactCtas, N]  fp64 score scratch of the fallback
+  // tensor-core path (M/L/A then hold 2 partials per split: one per softmax slot)
+  float* bm;       // [BH, ntiles, m]  largest raw score of each 128-key tile
+  float* thr;      // [BH, m]          collection threshold tau_L - 4E
+  float* E;        // [BH, m]          fp32 score error bound
+  int* cnt;        // [BH, m]          candidates collected
+  float* cand_s;   // [BH, m, cap]
+  int* cand_i;     // [BH, m, cap]
 };
 
-LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms);
+LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms, bool bf16_input);
 size_t landmark_ws_bytes(const LandmarkPlan& p, int BH, int N, int d, int m);
 LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, int d, int m);
 
 template <typename T>
 cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, int N, int d,
                             int m, int topk, const LandmarkPlan& plan, const LandmarkWs& ws,
-                            int32_t* topk_idx, float* v_tilde, cudaStream_t st);
+                            int32_t* topk_idx, float* v_tilde, int* status, cudaStream_t st);
+
+bool landmark_tc_eligible(int d, int N, int topk);
+void plan_landmark_tc(LandmarkPlan& p, int BH, int N, int m, int topk, int num_sms);
+cudaError_t launch_landmark_tc_passes(const __nv_bfloat16* q_tilde, const __nv_bfloat16* k,
+                                      const __nv_bfloat16* v, int BH, int N, int m, int topk,
+                                      const LandmarkPlan& p, const LandmarkWs& ws, float* v_tilde,
+                                      int* status, cudaStream_t st);
 
 // ---- step 4: routing (optionally emitting the shared-branch partial) ------
 template <typename T>
@@ -67,6 +86,14 @@ cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_ti
                                const float* shared_lse, const float* shared_o, int BH,
                                int N, int d, int m, int topk, T* out, int* status,
                                cudaStream_t st);
+
+// ---- tensor-core (tcgen05) kernels: bf16, d = 64 ---------------------------
+// TMA map over a [batches, rows, 64] bf16 array, boxes of box_rows rows.
+bool make_tmap_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t batches,
+                      uint32_t box_rows);
+bool route_tc_supported(int d, int m);
+cudaError_t launch_route_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH, int N,
+                            int m, int num_sms, int32_t* route, int* status, cudaStream_t st);
 
 int num_sms_of_current_device();
 

@@ -16,10 +16,11 @@
 //   2. landmark_merge_kernel: CTA = one landmark row.  Merges the softmax
 //      partials (the merge identity of tutorial ch. 4) and selects the top-k
 //      exactly: the fp32 candidates fix a threshold tau; keys whose fp32
-//      score is within 2E of tau (E bounds the fp32 error) are re-scored in
-//      fp64, so the selected set equals the one exact scores give, ties to the
-//      lowest index.  Rows where a split might have dropped a qualifying key,
-//      or with too many near-ties, go to
+//      score is within 2E of tau (E bounds the fp32 error) are re-scored with
+//      exact-product fp32 arithmetic (two-product + two-sum; fp64 runs at a
+//      small fraction of the fp32 rate here), so the selected set is the one
+//      exact scores give, ties to the lowest index.  Rows where a split might
+//      have dropped a qualifying key, or with too many near-ties, go to
 //   3. landmark_exact_kernel: fp64 scores for all N keys of the row and a
 //      radix select on (score, index) -- slow, used only for degenerate inputs
 //      (mass ties, adversarial key order).
@@ -27,6 +28,7 @@
 #include "kernels.h"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace mita {
 namespace {
@@ -189,6 +191,72 @@ landmark_partial_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k,
   for (int t = 0; t < hcnt; ++t) { cs[t] = hs[t * RT + tid]; ci[t] = hi[t * RT + tid]; }
 }
 
+// Exact top-k from fp32 candidates sorted best first (us/ui; `total` real
+// entries).  tau = the k-th fp32 score.  Keys above tau + 2E are members,
+// keys below tau - 2E are not (E bounds the fp32 error; the caller guarantees
+// every key that could reach tau - 2E is among the candidates); the band in
+// between is re-scored with exact-product arithmetic and ranked (score desc,
+// index asc).  With `slow` set, or a band too wide to rank here, the row goes
+// to the exact fallback.  Writes the member indices ascending.
+template <typename T, int D>
+__device__ void finish_topk(float* us, int* ui, int total, int topk, float E, bool slow,
+                            const float* qd, const T* kb, F2* bx, int* bi, int* ired,
+                            long long rowflat, const LandmarkWs& ws,
+                            int32_t* __restrict__ topk_idx) {
+  const int tid = threadIdx.x;
+  int a = 0, bnd_end = 0;
+  if (!slow) {
+    const float tau = us[topk - 1];
+    const float lo_band = tau - 2.f * E, hi_band = tau + 2.f * E;
+    // us is sorted best first: [0, a) above the band, [a, bnd_end) in it
+    int ca = 0, cb = 0;
+    for (int t = tid; t < total; t += blockDim.x) {
+      ca += us[t] > hi_band;
+      cb += us[t] >= lo_band;
+    }
+    block_excl_scan(ca, ired, &a);
+    __syncthreads();
+    block_excl_scan(cb, ired, &bnd_end);
+    if (bnd_end - a > kBandCap) slow = true;
+  }
+  if (slow) {
+    if (tid == 0) {
+      const int p = atomicAdd(ws.nslow, 1);
+      ws.slow_rows[p] = (int)rowflat;
+    }
+    return;
+  }
+  // --- exact re-scoring of the band -------------------------------------------
+  const int nb = bnd_end - a;
+  const int PB = next_pow2(max(nb, 1));
+  for (int t = tid; t < PB; t += blockDim.x) {
+    if (t < nb) {
+      const int j = ui[a + t];
+      float kr[D];
+      load_row<T, D>(kb + (size_t)j * D, kr);
+      bx[t] = dot_f2<D>(qd, kr);
+      bi[t] = j;
+    } else {
+      bx[t] = F2{-INFINITY, 0.f};
+      bi[t] = 0x7fffffff;
+    }
+  }
+  bitonic_sort_desc(bx, bi, PB);
+  // --- the a sure members plus the best (topk - a) of the band, ascending ----
+  const int PK = next_pow2(topk);
+  __syncthreads();
+  int* outset = reinterpret_cast<int*>(us);   // us is no longer needed
+  for (int t = tid; t < PK; t += blockDim.x) {
+    int val;
+    if (t < a) val = ui[t];
+    else if (t < topk) val = bi[t - a];
+    else val = 0x7fffffff;
+    outset[t] = val;
+  }
+  bitonic_sort_int_asc(outset, PK);
+  for (int t = tid; t < topk; t += blockDim.x) topk_idx[rowflat * topk + t] = outset[t];
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, int N, int m,
@@ -197,9 +265,9 @@ landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, in
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* us = reinterpret_cast<float*>(smem_raw);           // [P]
   int* ui = reinterpret_cast<int*>(us + P);                 // [P]
-  double* bx = reinterpret_cast<double*>(ui + P);           // [kBandCap]
+  F2* bx = reinterpret_cast<F2*>(ui + P);                   // [kBandCap]
   int* bi = reinterpret_cast<int*>(bx + kBandCap);          // [kBandCap]
-  __shared__ double qd[D];
+  __shared__ float qd[D];
   __shared__ int soff[257];
   __shared__ float red[8];
   __shared__ int ired[9];
@@ -231,7 +299,7 @@ landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, in
     soff[S] = run;
     s_slow = 0;
   }
-  for (int l = tid; l < D; l += blockDim.x) qd[l] = (double)to_f(q_tilde[rowflat * D + l]);
+  for (int l = tid; l < D; l += blockDim.x) qd[l] = to_f(q_tilde[rowflat * D + l]);
   __syncthreads();
   const int total = soff[S];
   for (int s = 0; s < S; ++s) {
@@ -246,78 +314,57 @@ landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, in
 
   // --- threshold and fp32 error bound ---------------------------------------
   float qn2 = 0.f;
-  for (int l = tid; l < D; l += blockDim.x) qn2 += (float)(qd[l] * qd[l]);
+  for (int l = tid; l < D; l += blockDim.x) qn2 += qd[l] * qd[l];
   qn2 = block_sum(qn2, red);
   float km2 = 0.f;
   for (int s = tid; s < S; s += blockDim.x) km2 = fmaxf(km2, ws.kmax2[bh * S + s]);
   km2 = block_max(km2, red);
   const float E = err_gamma(D) * sqrtf(qn2) * sqrtf(km2);
   bool slow = total < topk;
-  const float tau = slow ? 0.f : us[topk - 1];
-  const float lo_band = tau - 2.f * E, hi_band = tau + 2.f * E;
   if (!slow) {
     // a split that dropped keys scoring at or above tau - 2E may hide a member
+    const float lo_band = us[topk - 1] - 2.f * E;
     for (int s = tid; s < S; s += blockDim.x)
       if (ws.theta[r0 + s] >= lo_band) s_slow = 1;
   }
   __syncthreads();
   slow = slow || s_slow;
-  int a = 0, bnd_end = 0;
+  finish_topk<T, D>(us, ui, total, topk, E, slow, qd, k + (size_t)bh * N * D, bx, bi, ired,
+                    rowflat, ws, topk_idx);
+}
+
+// Candidates of the tensor-core path: the keys whose fp32 score reached the
+// row's collection threshold, gathered by the collect kernel.
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+landmark_select_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, int N, int m,
+                       int topk, int cap, int P, LandmarkWs ws, int32_t* __restrict__ topk_idx) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* us = reinterpret_cast<float*>(smem_raw);           // [P]
+  int* ui = reinterpret_cast<int*>(us + P);                 // [P]
+  F2* bx = reinterpret_cast<F2*>(ui + P);                   // [kBandCap]
+  int* bi = reinterpret_cast<int*>(bx + kBandCap);          // [kBandCap]
+  __shared__ float qd[D];
+  __shared__ int ired[9];
+  const long long rowflat = blockIdx.x;
+  const long long bh = rowflat / m;
+  const int tid = threadIdx.x;
+  const int cnt = ws.cnt[rowflat];
+  const int total = min(cnt, cap);
+  const bool slow = cnt > cap || cnt < topk;
+  for (int l = tid; l < D; l += blockDim.x) qd[l] = to_f(q_tilde[rowflat * D + l]);
   if (!slow) {
-    // us is sorted best first: [0, a) above the band, [a, bnd_end) in it
-    int ca = 0, cb = 0;
-    for (int t = tid; t < total; t += blockDim.x) {
-      ca += us[t] > hi_band;
-      cb += us[t] >= lo_band;
+    const float* cs = ws.cand_s + (size_t)rowflat * cap;
+    const int* ci = ws.cand_i + (size_t)rowflat * cap;
+    for (int t = tid; t < P; t += blockDim.x) {
+      us[t] = t < total ? cs[t] : -INFINITY;
+      ui[t] = t < total ? ci[t] : 0x7fffffff;
     }
-    int dummy;
-    a = block_excl_scan(ca, ired, &dummy);   // total of ca lands in `dummy`
-    a = dummy;
-    __syncthreads();
-    block_excl_scan(cb, ired, &bnd_end);
-    if (bnd_end - a > kBandCap) slow = true;
+    bitonic_sort_desc(us, ui, P);
   }
-  if (slow) {
-    if (tid == 0) {
-      const int p = atomicAdd(ws.nslow, 1);
-      ws.slow_rows[p] = (int)rowflat;
-    }
-    return;
-  }
-
-  // --- exact re-scoring of the band -------------------------------------------
-  const int nb = bnd_end - a;
-  const int PB = next_pow2(max(nb, 1));
-  const T* kb = k + (size_t)bh * N * D;
-  for (int t = tid; t < PB; t += blockDim.x) {
-    if (t < nb) {
-      const int j = ui[a + t];
-      bx[t] = dot_exact<T, D>(qd, kb + (size_t)j * D);
-      bi[t] = j;
-    } else {
-      bx[t] = -INFINITY;
-      bi[t] = 0x7fffffff;
-    }
-  }
-  bitonic_sort_desc(bx, bi, PB);
-
-  // --- output: the a sure members plus the best (topk - a) of the band, ascending
-  const int need = topk - a;
-  const int PK = next_pow2(topk);
   __syncthreads();
-  // reuse ui[topk..] region is not safe (ui holds the sure members); write the
-  // output set into `us` reinterpreted as ints.
-  int* outset = reinterpret_cast<int*>(us);
-  for (int t = tid; t < PK; t += blockDim.x) {
-    int val;
-    if (t < a) val = ui[t];
-    else if (t < topk) val = bi[t - a];
-    else val = 0x7fffffff;
-    outset[t] = val;
-  }
-  (void)need;
-  bitonic_sort_int_asc(outset, PK);
-  for (int t = tid; t < topk; t += blockDim.x) topk_idx[rowflat * topk + t] = outset[t];
+  finish_topk<T, D>(us, ui, total, topk, ws.E[rowflat], slow, qd, k + (size_t)bh * N * D, bx, bi,
+                    ired, rowflat, ws, topk_idx);
 }
 
 // Exact fallback: fp64 scores of all N keys, radix select on the monotone
@@ -338,7 +385,7 @@ landmark_exact_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, in
     const long long rowflat = ws.slow_rows[w];
     const long long bh = rowflat / m;
     __syncthreads();
-    for (int l = tid; l < D; l += blockDim.x) qd[l] = (double)to_f(q_tilde[rowflat * D + l]);
+    for (int l = tid; l < D; l += blockDim.x) qd[l] = to_f(q_tilde[rowflat * D + l]);
     __syncthreads();
     const T* kb = k + (size_t)bh * N * D;
     for (int j = tid; j < N; j += blockDim.x) sc[j] = dot_exact<T, D>(qd, kb + (size_t)j * D);
@@ -401,16 +448,32 @@ cudaError_t run_partial(const T* qt, const T* k, const T* v, int BH, int N, int 
 template <typename T, int D>
 cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int topk,
                 const LandmarkPlan& p, const LandmarkWs& ws, int32_t* topk_idx, float* vt,
-                cudaStream_t st) {
+                int* status, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(ws.nslow, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
+  if constexpr (std::is_same<T, bf16>::value && D == 64) {
+    if (p.tc) {
+      e = launch_landmark_tc_passes(qt, k, v, BH, N, m, topk, p, ws, vt, status, st);
+      if (e != cudaSuccess) return e;
+      const size_t ssmem = (size_t)p.P * 8 + (size_t)kBandCap * (sizeof(F2) + 4);
+      auto sk = landmark_select_kernel<T, D>;
+      e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+      if (e != cudaSuccess) return e;
+      sk<<<(unsigned)((long long)BH * m), 256, ssmem, st>>>(qt, k, N, m, topk, p.cap, p.P, ws,
+                                                            topk_idx);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      landmark_exact_kernel<T, D><<<kExactCtas, 512, 0, st>>>(qt, k, N, m, topk, ws, topk_idx);
+      return cudaGetLastError();
+    }
+  }
+  (void)status;
   switch (p.RT) {
     case 32: e = run_partial<T, D, 32>(qt, k, v, BH, N, m, p, ws, st); break;
     case 64: e = run_partial<T, D, 64>(qt, k, v, BH, N, m, p, ws, st); break;
     default: e = run_partial<T, D, 128>(qt, k, v, BH, N, m, p, ws, st); break;
   }
   if (e != cudaSuccess) return e;
-  const size_t msmem = (size_t)p.P * 8 + (size_t)kBandCap * 12;
+  const size_t msmem = (size_t)p.P * 8 + (size_t)kBandCap * (sizeof(F2) + 4);
   auto mk = landmark_merge_kernel<T, D>;
   e = cudaFuncSetAttribute(mk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
   if (e != cudaSuccess) return e;
@@ -423,9 +486,13 @@ cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int t
 
 }  // namespace
 
-LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms) {
-  (void)d;
+LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms, bool bf16_input) {
   LandmarkPlan p{};
+  if (bf16_input && landmark_tc_eligible(d, N, topk)) {
+    plan_landmark_tc(p, BH, N, m, topk, num_sms);
+    return p;
+  }
+  p.tc = false;
   p.RT = m >= 128 ? 128 : (m > 32 ? 64 : 32);
   p.nrt = (m + p.RT - 1) / p.RT;
   p.Tcap = std::min(kTcapMax, topk + 32);
@@ -443,55 +510,76 @@ LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms) {
 }
 
 size_t landmark_ws_bytes(const LandmarkPlan& p, int BH, int N, int d, int m) {
-  const size_t rows = (size_t)BH * m, rs = rows * p.S;
+  const size_t rows = (size_t)BH * m;
+  const size_t parts = rows * (p.tc ? 2 * p.S : p.S);
   size_t b = 0;
   auto add = [&](size_t n) { b += (n + 255) / 256 * 256; };
-  add(rs * 4); add(rs * 4); add(rs * d * 4);
-  add(rs * p.Tcap * 4); add(rs * p.Tcap * 4);
-  add(rs * 4); add(rs * 4);
+  add(parts * 4); add(parts * 4); add(parts * d * 4);
+  if (!p.tc) { add(parts * p.Tcap * 4); add(parts * p.Tcap * 4); add(parts * 4); add(parts * 4); }
   add((size_t)BH * p.S * 4);
   add(4); add(rows * 4);
   add((size_t)kExactCtas * N * 8);
+  if (p.tc) {
+    add((size_t)BH * p.ntiles * m * 4);
+    add(rows * 4); add(rows * 4); add(rows * 4);
+    add(rows * p.cap * 4); add(rows * p.cap * 4);
+  }
   return b;
 }
 
 LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, int d, int m) {
-  const size_t rows = (size_t)BH * m, rs = rows * p.S;
+  const size_t rows = (size_t)BH * m;
+  const size_t parts = rows * (p.tc ? 2 * p.S : p.S);
   char* c = static_cast<char*>(base);
   auto take = [&](size_t n) { char* r = c; c += (n + 255) / 256 * 256; return r; };
-  LandmarkWs w;
-  w.M = (float*)take(rs * 4);
-  w.L = (float*)take(rs * 4);
-  w.A = (float*)take(rs * d * 4);
-  w.cs = (float*)take(rs * p.Tcap * 4);
-  w.ci = (int*)take(rs * p.Tcap * 4);
-  w.cn = (int*)take(rs * 4);
-  w.theta = (float*)take(rs * 4);
+  LandmarkWs w{};
+  w.M = (float*)take(parts * 4);
+  w.L = (float*)take(parts * 4);
+  w.A = (float*)take(parts * d * 4);
+  if (!p.tc) {
+    w.cs = (float*)take(parts * p.Tcap * 4);
+    w.ci = (int*)take(parts * p.Tcap * 4);
+    w.cn = (int*)take(parts * 4);
+    w.theta = (float*)take(parts * 4);
+  }
   w.kmax2 = (float*)take((size_t)BH * p.S * 4);
   w.nslow = (int*)take(4);
   w.slow_rows = (int*)take(rows * 4);
   w.exact = (double*)take((size_t)kExactCtas * N * 8);
+  if (p.tc) {
+    w.bm = (float*)take((size_t)BH * p.ntiles * m * 4);
+    w.thr = (float*)take(rows * 4);
+    w.E = (float*)take(rows * 4);
+    w.cnt = (int*)take(rows * 4);
+    w.cand_s = (float*)take(rows * p.cap * 4);
+    w.cand_i = (int*)take(rows * p.cap * 4);
+  }
   return w;
 }
 
 template <typename T>
 cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, int N, int d,
                             int m, int topk, const LandmarkPlan& plan, const LandmarkWs& ws,
-                            int32_t* topk_idx, float* v_tilde, cudaStream_t st) {
+                            int32_t* topk_idx, float* v_tilde, int* status, cudaStream_t st) {
+#define MITA_LM_CASE(DD)                                                                     \
+  case DD:                                                                                   \
+    return run<T, DD>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, status, st);
   switch (d) {
-    case 16: return run<T, 16>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, st);
-    case 32: return run<T, 32>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, st);
-    case 64: return run<T, 64>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, st);
-    case 128: return run<T, 128>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, st);
+    MITA_LM_CASE(16)
+    MITA_LM_CASE(32)
+    MITA_LM_CASE(64)
+    MITA_LM_CASE(128)
     default: return cudaErrorInvalidValue;
   }
+#undef MITA_LM_CASE
 }
 
 template cudaError_t launch_landmark<float>(const float*, const float*, const float*, int, int,
                                             int, int, int, const LandmarkPlan&,
-                                            const LandmarkWs&, int32_t*, float*, cudaStream_t);
+                                            const LandmarkWs&, int32_t*, float*, int*,
+                                            cudaStream_t);
 template cudaError_t launch_landmark<bf16>(const bf16*, const bf16*, const bf16*, int, int, int,
                                            int, int, const LandmarkPlan&, const LandmarkWs&,
-                                           int32_t*, float*, cudaStream_t);
+                                           int32_t*, float*, int*, cudaStream_t);
 
 }  // namespace mita

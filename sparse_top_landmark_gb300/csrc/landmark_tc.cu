@@ -1,0 +1,597 @@
+// Steps 2-3 on the tensor cores (bf16, d = 64): shared landmark values and
+// the per-landmark top-k key sets, for long sequences.
+//
+// MiTA tutorial (iwxt.cn), ch. 4 step 2 (paper eq. 6-7): landmark i scores
+// all N keys with q~_i . k_j / sqrt(d) and keeps its top-k rows as expert i;
+// ch. 4 step 3 (eq. 8-9): softmax over all N of the same scores weights V
+// into v~_i.  The m x N score matrix never reaches HBM.
+//
+// Two sweeps over the keys, each split over CTAs (flash-decoding style):
+//
+// sweep (pass 1), CTA = (head, 128 landmarks, key split):
+//   warp 0       TMA: K and V tiles of 128 keys into a 4-stage ring;
+//   warp 1       MMA: S = q~ K^T (tensor memory), then O += P V with P read
+//                from tensor memory;
+//   warps 2-3    squared key norms (error bound of the fp32 scores);
+//   warps 4-7,   two softmax warpgroups that take alternate key tiles, each
+//   warps 8-11   with its own online-softmax state (max, sum) and its own O
+//                accumulator, so one computes while the other's MMAs run.
+//                Rescaling of O is lazy (only when the max grows by more than
+//                2^8).  They also record each tile's largest raw score.
+// threshold, CTA = (head, 32 landmarks): merges the softmax partials into v~
+//   (tutorial ch. 4: (Z1 o1 + Z2 o2) / (Z1 + Z2)) and radix-selects the k-th
+//   largest tile maximum tau_L.  k distinct tiles reach tau_L, so at least k
+//   keys score >= tau_L: every top-k key scores >= tau_L - E (exactly) and
+//   >= tau_L - 2E in fp32 (E bounds the fp32 error).  Collection uses
+//   tau_L - 4E, which stays valid even if pass 2's fp32 scores differ from
+//   pass 1's by up to 2E.
+// collect (pass 2): S = q~ K^T again; keys at or above the threshold are
+//   appended to the row's candidate list (typically k plus a few).
+// The exact selection over the candidates is landmark_select_kernel.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace mita {
+namespace {
+using namespace sm100;
+
+constexpr int BN = 128;          // keys per tile
+constexpr int kStages = 4;       // K/V ring depth
+constexpr int kThreads = 384;    // 12 warps
+constexpr float kLazy = 8.0f;    // rescale O only when the max grows by > 2^8
+
+__device__ __forceinline__ float softmax_c() { return 0.18033688011112042f; }  // log2(e)/8
+
+struct alignas(1024) SweepSmem {
+  bf16 qt[128 * 64];
+  bf16 k[kStages][BN * 64];
+  bf16 v[kStages][BN * 64];
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t qt_full, drain;
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  float nred[2];
+  uint32_t tmem;
+};
+
+// squared norm of row r of a 128B-swizzled bf16 tile
+__device__ __forceinline__ float swz_row_norm2(const bf16* tile, int r) {
+  const char* base = reinterpret_cast<const char*>(tile);
+  float a = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 x = *reinterpret_cast<const uint4*>(base + sw128_offset(r, c));
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+      a = fmaf(lo, lo, a);
+      a = fmaf(hi, hi, a);
+    }
+  }
+  return a;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// -------------------------------------------------------------------------------------------
+// pass 1
+// -------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constant__ CUtensorMap map_k,
+                const __grid_constant__ CUtensorMap map_v, int N, int m, int S, int split_len,
+                int ntiles_head, LandmarkWs ws, int* status) {
+  extern __shared__ unsigned char smem_raw[];
+  SweepSmem& s = *reinterpret_cast<SweepSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nrt = (m + 127) / 128;
+  int b = blockIdx.x;                 // row tiles of one key split are adjacent (L2 reuse)
+  const int rt = b % nrt; b /= nrt;
+  const int sp = b % S;
+  const int bh = b / S;
+  const int j0 = sp * split_len;
+  const int j1 = min(N, j0 + split_len);
+  const int ntl = (j1 - j0 + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.kv_full[i], 1);
+      mbar_init(&s.kv_empty[i], 3);        // MMA commit + two norm warps
+    }
+    mbar_init(&s.qt_full, 1);
+    mbar_init(&s.drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 4);          // one arrival per softmax warp
+      mbar_init(&s.pv_done[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem;
+  // tensor memory columns: S_slot at 128*slot, P_slot at 256 + 64*slot, O_slot at 384 + 64*slot
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&map_qt);
+      prefetch_tmap(&map_k);
+      prefetch_tmap(&map_v);
+      mbar_expect_tx(&s.qt_full, 128 * 128);
+      tma_load_3d(s.qt, &map_qt, &s.qt_full, 0, rt * 128, bh);
+      for (int j = 0; j < ntl; ++j) {
+        const int st = j % kStages;
+        if (!mbar_wait(&s.kv_empty[st], ((j / kStages) & 1) ^ 1)) {
+          flag_error(status, kDevErrTimeout);
+          break;
+        }
+        mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
+        tma_load_3d(s.k[st], &map_k, &s.kv_full[st], 0, j0 + j * BN, bh);
+        tma_load_3d(s.v[st], &map_v, &s.kv_full[st], 0, j0 + j * BN, bh);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f16(128, BN, false);
+      const uint32_t id_pv = idesc_f16(128, 64, true);
+      bool ok = mbar_wait(&s.qt_full, 0);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kStages, slot = j & 1;
+        if (!mbar_wait(&s.kv_full[st], (j / kStages) & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t da = smem_desc_sw128(smem_u32(s.qt) + kk * 32, 1024);
+          const uint64_t db = smem_desc_sw128(smem_u32(s.k[st]) + kk * 32, 1024);
+          mma_ss(tbase + slot * 128, da, db, id_s, kk > 0);
+        }
+        mma_commit(&s.s_full[slot]);
+        return true;
+      };
+      if (ok && ntl > 0) ok = issue_s(0);
+      if (ok && ntl > 1) ok = issue_s(1);
+      for (int j = 0; j < ntl && ok; ++j) {
+        const int st = j % kStages, slot = j & 1, t = j >> 1;
+        if (!mbar_wait(&s.p_full[slot], t & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t dv = smem_desc_sw128(smem_u32(s.v[st]) + kk * 2048, 1024);
+          mma_ts(tbase + 384 + slot * 64, tbase + 256 + slot * 64 + kk * 8, dv, id_pv,
+                 t > 0 || kk > 0);
+        }
+        mma_commit(&s.kv_empty[st]);
+        mma_commit(&s.pv_done[slot]);
+        if (j + 2 < ntl) ok = issue_s(j + 2);
+      }
+      if (!ok) flag_error(status, kDevErrTimeout);
+      mma_commit(&s.drain);
+      mbar_wait(&s.drain, 0);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // squared key norms; each warp takes 64 keys of every tile
+    float km = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntl; ++j) {
+      const int st = j % kStages;
+      if (ok && !mbar_wait(&s.kv_full[st], (j / kStages) & 1)) ok = false;
+      if (ok) {
+        for (int r = (warp - 2) * 64 + lane; r < (warp - 2) * 64 + 64; r += 32)
+          if (j0 + j * BN + r < j1) km = fmaxf(km, swz_row_norm2(s.k[st], r));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.kv_empty[st]);
+    }
+    km = warp_max(km);
+    if (lane == 0) s.nred[warp - 2] = km;
+    if (!ok) flag_error(status, kDevErrTimeout);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int slot = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int grow = rt * 128 + row;                // landmark index
+    const bool live_row = grow < m;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tbase + lane_off + slot * 128;
+    const uint32_t tP = tbase + lane_off + 256 + slot * 64;
+    const uint32_t tO = tbase + lane_off + 384 + slot * 64;
+    const float c = softmax_c();
+    float mref = -INFINITY, lsum = 0.f;
+    bool ok = true;
+    int t = 0;
+    for (int j = slot; j < ntl; j += 2, ++t) {
+      if (ok && !mbar_wait(&s.s_full[slot], t & 1)) ok = false;
+      tc_fence_after();
+      const int kbase = j0 + j * BN;
+      const int nvalid = min(BN, j1 - kbase);
+      // pass A over S: the tile's largest raw score
+      float tm = -INFINITY;
+      if (ok) {
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          float v[32];
+          tmem_ld32(tS + cc * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) tm = fmaxf(tm, (cc * 32 + i < nvalid) ? v[i] : -INFINITY);
+        }
+      }
+      if (live_row && ok)
+        ws.bm[((size_t)bh * ntiles_head + (kbase / BN)) * m + grow] = tm;
+      const float xm = tm * c;
+      // P_slot and O_slot are free once the previous P.V of this slot is done
+      if (t > 0 && ok && !mbar_wait(&s.pv_done[slot], (t - 1) & 1)) ok = false;
+      tc_fence_after();
+      const bool need = (t == 0) || (xm > mref + kLazy);
+      if (t > 0 && __any_sync(0xffffffffu, need)) {
+        const float f = need ? exp2f(mref - xm) : 1.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float o[32];
+          tmem_ld32(tO + h * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= f;
+          tmem_st16(tO + h * 32, reinterpret_cast<uint32_t*>(o));
+          tmem_st16(tO + h * 32 + 16, reinterpret_cast<uint32_t*>(o + 16));
+        }
+        tmem_st_wait();
+      }
+      if (need) {
+        if (t > 0) lsum *= exp2f(mref - xm);
+        mref = xm;
+      }
+      // pass B over S: P = exp2(s * c - mref) as bf16 pairs into tensor memory
+      const float nm = -mref;
+      float ls = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        float v[32];
+        tmem_ld32(tS + cc * 32, v);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = (cc * 32 + i < nvalid) ? exp2f(fmaf(v[i], c, nm)) : 0.f;
+          const float p1 = (cc * 32 + i + 1 < nvalid) ? exp2f(fmaf(v[i + 1], c, nm)) : 0.f;
+          ls += p0 + p1;
+          pk[i / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tP + cc * 16, pk);
+      }
+      lsum += ls;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.p_full[slot]);
+    }
+    // final O of this slot
+    float o[64];
+    if (t > 0) {
+      if (ok && !mbar_wait(&s.pv_done[slot], (t - 1) & 1)) ok = false;
+      tc_fence_after();
+      tmem_ld32(tO, o);
+      tmem_ld32(tO + 32, o + 32);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) o[i] = 0.f;
+    }
+    if (live_row) {
+      const size_t pidx = ((size_t)bh * m + grow) * (2 * S) + sp * 2 + slot;
+      ws.M[pidx] = mref;
+      ws.L[pidx] = lsum;
+      float4* dst = reinterpret_cast<float4*>(ws.A + pidx * 64);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    }
+    if (!ok) flag_error(status, kDevErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && rt == 0) ws.kmax2[(size_t)bh * S + sp] = fmaxf(s.nred[0], s.nred[1]);
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// -------------------------------------------------------------------------------------------
+// threshold: v~ from the partials, tau_L by radix select over the tile maxima
+// -------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t fkey(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__global__ void __launch_bounds__(256)
+lm_threshold_kernel(const bf16* __restrict__ q_tilde, int N, int m, int topk, int S2, int S,
+                    int ntiles_head, LandmarkWs ws, float* __restrict__ v_tilde) {
+  __shared__ int hist[32][257];
+  __shared__ uint32_t s_prefix[32];
+  __shared__ int s_need[32];
+  __shared__ float s_km2;
+  const int ngroups = (m + 31) / 32;
+  const int bh = blockIdx.x / ngroups;
+  const int r0 = (blockIdx.x % ngroups) * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  (void)N;
+
+  // ---- v~ : 8 threads per row, 8 dims each
+  {
+    const int rr = tid >> 3, part = tid & 7;
+    const int row = r0 + rr;
+    if (row < m) {
+      const size_t base = ((size_t)bh * m + row) * S2;
+      float mx = -INFINITY;
+      for (int q = 0; q < S2; ++q) mx = fmaxf(mx, ws.M[base + q]);
+      float num[8], den = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) num[i] = 0.f;
+      for (int q = 0; q < S2; ++q) {
+        const float w = exp2f(ws.M[base + q] - mx);
+        den = fmaf(w, ws.L[base + q], den);
+        const float* o = ws.A + (base + q) * 64 + part * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) num[i] = fmaf(w, o[i], num[i]);
+      }
+      float* out = v_tilde + ((size_t)bh * m + row) * 64 + part * 8;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = num[i] / den;
+    }
+  }
+  // ---- largest squared key norm of the head
+  if (warp == 0) {
+    float km = 0.f;
+    for (int q = lane; q < S; q += 32) km = fmaxf(km, ws.kmax2[(size_t)bh * S + q]);
+    km = warp_max(km);
+    if (lane == 0) s_km2 = km;
+  }
+  if (tid < 32) { s_prefix[tid] = 0u; s_need[tid] = topk; }
+  // ---- radix select (4 passes of 8 bits) of the topk-th largest tile max per row
+  const float* bm = ws.bm + (size_t)bh * ntiles_head * m;
+  uint32_t mask = 0u;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 32 * 257; i += 256) (&hist[0][0])[i] = 0;
+    __syncthreads();
+    const int row = r0 + lane;
+    if (row < m) {
+      const uint32_t pre = s_prefix[lane];
+      for (int tl = warp; tl < ntiles_head; tl += 8) {
+        const uint32_t key = fkey(bm[(size_t)tl * m + row]);
+        if ((key & mask) == pre) atomicAdd(&hist[lane][(key >> shift) & 255], 1);
+      }
+    }
+    __syncthreads();
+    if (tid < 32 && r0 + tid < m) {
+      int need = s_need[tid], cum = 0, dg = 255;
+      for (; dg > 0; --dg) {
+        if (cum + hist[tid][dg] >= need) break;
+        cum += hist[tid][dg];
+      }
+      s_need[tid] = need - cum;
+      s_prefix[tid] |= (uint32_t)dg << shift;
+    }
+    mask |= 0xffu << shift;
+    __syncthreads();
+  }
+  if (tid < 32 && r0 + tid < m) {
+    const int row = r0 + tid;
+    const size_t rf = (size_t)bh * m + row;
+    const bf16* qr = q_tilde + rf * 64;
+    float qn2 = 0.f;
+    for (int l = 0; l < 64; ++l) { const float x = __bfloat162float(qr[l]); qn2 = fmaf(x, x, qn2); }
+    const float E = err_gamma(64) * sqrtf(qn2) * sqrtf(s_km2);
+    const float tauL = ntiles_head >= topk ? fkey_inv(s_prefix[tid]) : -INFINITY;
+    ws.E[rf] = E;
+    ws.thr[rf] = tauL - 4.f * E;
+    ws.cnt[rf] = 0;
+  }
+}
+
+// -------------------------------------------------------------------------------------------
+// pass 2: collect the keys at or above the threshold
+// -------------------------------------------------------------------------------------------
+constexpr int kKStages = 4;
+
+struct alignas(1024) CollectSmem {
+  bf16 qt[128 * 64];
+  bf16 k[kKStages][BN * 64];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t qt_full, drain;
+  uint64_t s_full[2], s_free[2];
+  uint32_t tmem;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constant__ CUtensorMap map_k,
+                  int N, int m, int S, int split_len, int cap, LandmarkWs ws, int* status) {
+  extern __shared__ unsigned char smem_raw[];
+  CollectSmem& s = *reinterpret_cast<CollectSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nrt = (m + 127) / 128;
+  int b = blockIdx.x;                 // row tiles of one key split are adjacent (L2 reuse)
+  const int rt = b % nrt; b /= nrt;
+  const int sp = b % S;
+  const int bh = b / S;
+  const int j0 = sp * split_len;
+  const int j1 = min(N, j0 + split_len);
+  const int ntl = (j1 - j0 + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+    }
+    mbar_init(&s.qt_full, 1);
+    mbar_init(&s.drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_free[i], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&map_qt);
+      prefetch_tmap(&map_k);
+      mbar_expect_tx(&s.qt_full, 128 * 128);
+      tma_load_3d(s.qt, &map_qt, &s.qt_full, 0, rt * 128, bh);
+      for (int j = 0; j < ntl; ++j) {
+        const int st = j % kKStages;
+        if (!mbar_wait(&s.k_empty[st], ((j / kKStages) & 1) ^ 1)) {
+          flag_error(status, kDevErrTimeout);
+          break;
+        }
+        mbar_expect_tx(&s.k_full[st], BN * 128);
+        tma_load_3d(s.k[st], &map_k, &s.k_full[st], 0, j0 + j * BN, bh);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f16(128, BN, false);
+      bool ok = mbar_wait(&s.qt_full, 0);
+      for (int j = 0; j < ntl && ok; ++j) {
+        const int st = j % kKStages, slot = j & 1, t = j >> 1;
+        if (!mbar_wait(&s.k_full[st], (j / kKStages) & 1)) { ok = false; break; }
+        if (!mbar_wait(&s.s_free[slot], (t & 1) ^ 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t da = smem_desc_sw128(smem_u32(s.qt) + kk * 32, 1024);
+          const uint64_t db = smem_desc_sw128(smem_u32(s.k[st]) + kk * 32, 1024);
+          mma_ss(tbase + slot * 128, da, db, id_s, kk > 0);
+        }
+        mma_commit(&s.s_full[slot]);
+        mma_commit(&s.k_empty[st]);
+      }
+      if (!ok) flag_error(status, kDevErrTimeout);
+      mma_commit(&s.drain);
+      mbar_wait(&s.drain, 0);
+    }
+  } else if (warp >= 4) {
+    const int slot = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int grow = rt * 128 + row;
+    const bool live_row = grow < m;
+    const size_t rf = (size_t)bh * m + grow;
+    const float thr = live_row ? ws.thr[rf] : INFINITY;
+    const uint32_t tS = tbase + ((uint32_t)(quad * 32) << 16) + slot * 128;
+    bool ok = true;
+    int t = 0;
+    for (int j = slot; j < ntl; j += 2, ++t) {
+      if (ok && !mbar_wait(&s.s_full[slot], t & 1)) ok = false;
+      tc_fence_after();
+      const int kbase = j0 + j * BN;
+      const int nvalid = min(BN, j1 - kbase);
+      if (ok) {
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          float v[32];
+          tmem_ld32(tS + cc * 32, v);
+          tmem_ld_wait();
+          float cm = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cm = fmaxf(cm, v[i]);
+          if (cm >= thr) {
+            for (int i = 0; i < 32; ++i) {
+              const int kk = cc * 32 + i;
+              if (kk < nvalid && v[i] >= thr) {
+                const int pos = atomicAdd(ws.cnt + rf, 1);
+                if (pos < cap) {
+                  ws.cand_s[rf * cap + pos] = v[i];
+                  ws.cand_i[rf * cap + pos] = kbase + kk;
+                }
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.s_free[slot]);
+    }
+    if (!ok) flag_error(status, kDevErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 256);
+}
+
+}  // namespace
+
+bool landmark_tc_eligible(int d, int N, int topk) {
+  return d == 64 && (N + BN - 1) / BN >= 2 * topk;
+}
+
+void plan_landmark_tc(LandmarkPlan& p, int BH, int N, int m, int topk, int num_sms) {
+  p.tc = true;
+  p.RT = 128;
+  p.nrt = (m + 127) / 128;
+  const int ctas_per_split = BH * p.nrt;
+  int S = std::max(1, (num_sms + ctas_per_split - 1) / ctas_per_split);
+  S = std::min(S, (N + BN - 1) / BN);
+  p.split_len = ((N + S - 1) / S + BN - 1) / BN * BN;
+  p.S = (N + p.split_len - 1) / p.split_len;
+  p.ntiles = (N + BN - 1) / BN;
+  p.cap = std::min(8192, next_pow2(std::max(1024, 2 * topk + 256)));
+  p.P = p.cap;
+  p.Tcap = 0;
+}
+
+cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const bf16* v, int BH,
+                                      int N, int m, int topk, const LandmarkPlan& p,
+                                      const LandmarkWs& ws, float* v_tilde, int* status,
+                                      cudaStream_t st) {
+  CUtensorMap mqt, mk, mv;
+  if (!make_tmap_rows64(&mqt, q_tilde, (uint64_t)m, (uint64_t)BH, 128) ||
+      !make_tmap_rows64(&mk, k, (uint64_t)N, (uint64_t)BH, BN) ||
+      !make_tmap_rows64(&mv, v, (uint64_t)N, (uint64_t)BH, BN))
+    return cudaErrorInvalidValue;
+  const unsigned blocks = (unsigned)(BH * p.nrt * p.S);
+  const size_t sm1 = sizeof(SweepSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(lm_sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sm1);
+  if (e != cudaSuccess) return e;
+  lm_sweep_kernel<<<blocks, kThreads, sm1, st>>>(mqt, mk, mv, N, m, p.S, p.split_len, p.ntiles, ws,
+                                                 status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const unsigned tblocks = (unsigned)(BH * ((m + 31) / 32));
+  lm_threshold_kernel<<<tblocks, 256, 0, st>>>(q_tilde, N, m, topk, 2 * p.S, p.S, p.ntiles, ws,
+                                               v_tilde);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t sm2 = sizeof(CollectSmem) + 1024;
+  e = cudaFuncSetAttribute(lm_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
+  if (e != cudaSuccess) return e;
+  lm_collect_kernel<<<blocks, kThreads, sm2, st>>>(mqt, mk, N, m, p.S, p.split_len, p.cap, ws,
+                                                   status);
+  return cudaGetLastError();
+}
+
+}  // namespace mita

@@ -43,12 +43,25 @@ pool_kernel(const T* __restrict__ q, int N, int grid_h, int grid_w, int mh, int 
 #pragma unroll
   for (int e = 0; e < VEC; ++e) { s[e] = 0.f; c[e] = 0.f; }
   const T* base = q + (size_t)bh * N * D + vlane * VEC;
-  for (int t = tl; t < cnt; t += TL) {
-    const int r = r0 + t / nc, col = c0 + t % nc;
-    float x[VEC];
-    Vec<T>::load(base + ((size_t)r * grid_w + col) * D, x);
+  // UNR independent 16-byte loads in flight per thread (the window is read once)
+  constexpr int UNR = 4;
+  for (int t0 = tl; t0 < cnt; t0 += TL * UNR) {
+    float x[UNR][VEC];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) two_sum_acc(s[e], c[e], x[e]);
+    for (int u = 0; u < UNR; ++u) {
+      const int t = t0 + u * TL;
+      if (t < cnt) {
+        const int r = r0 + t / nc, col = c0 + t % nc;
+        Vec<T>::load(base + ((size_t)r * grid_w + col) * D, x[u]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) x[u][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) two_sum_acc(s[e], c[e], x[u][e]);
   }
 #pragma unroll
   for (int e = 0; e < VEC; ++e) red[tl][vlane * VEC + e] = (double)s[e] + (double)c[e];

@@ -9,8 +9,8 @@
 //
 // Exactness: the fp32 argmax is accepted when it beats the runner-up by more
 // than 2E (E bounds the fp32 dot error); otherwise every landmark within 2E of
-// the best is re-scored in fp64 and the exact maximum wins, ties to the lowest
-// landmark index.
+// the best is re-scored with exact-product fp32 arithmetic and the exact
+// maximum wins, ties to the lowest landmark index.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -102,7 +102,7 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
   const float E = err_gamma(D) * sqrtf(qn2) * sqrtf(qt2);
   if (best - second <= 2.f * E) {
     // near tie: re-score the candidates exactly
-    double bx = -INFINITY;
+    F2 bx{-INFINITY, 0.f};
     int bi = ib;
     for (int i = 0; i < m; ++i) {
       float r[D];
@@ -111,10 +111,8 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
 #pragma unroll
       for (int l = 0; l < D; ++l) s = fmaf(qr[l], r[l], s);
       if (s >= best - 2.f * E) {
-        double x = 0.0;
-#pragma unroll
-        for (int l = 0; l < D; ++l) x = fma((double)qr[l], (double)r[l], x);
-        if (x > bx) { bx = x; bi = i; }
+        const F2 x = dot_f2<D>(qr, r);
+        if (f2_greater(x, bx)) { bx = x; bi = i; }
       }
     }
     ib = bi;

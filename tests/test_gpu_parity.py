@@ -227,11 +227,14 @@ def test_edge_case_end_to_end_and_stages(case):
 
 @pytest.mark.parametrize("pattern", ["duplicated_keys", "all_equal_keys", "sorted_keys",
                                      "zero_landmark"])
-def test_forced_ties_and_adversarial_order(pattern):
+@pytest.mark.parametrize("N,topk", [(32768, 300), (65536, 64)], ids=["heap_path", "tc_path"])
+def test_forced_ties_and_adversarial_order(pattern, N, topk):
     """Mass ties and a key order that puts every top-k member in one split
-    drive the exact fallback; the result must still be the lowest-index set."""
+    drive the exact fallback; the result must still be the lowest-index set.
+    (65536, 64) runs the two-pass tensor-core selection, (32768, 300) the
+    per-split candidate heaps."""
     mita = M()
-    B, H, N, d, m, topk = 1, 2, 32768, 64, 8, 300
+    B, H, d, m = 1, 2, 64, 8
     w = W.custom(pattern, B, H, N, d, "bf16", 1, N, m, topk, index=300)
     q, k, v = W.make_qkv(w, 0)
     if pattern == "duplicated_keys":
