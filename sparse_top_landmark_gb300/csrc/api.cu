@@ -265,6 +265,16 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
   if (so == nullptr) MITA_TRY(check_ptrs({{qt, "q_tilde"}, {vt, "v_tilde"}}));
   DevState* ds = nullptr;
   MITA_TRY(device_state(&ds));
+  if constexpr (std::is_same<T, bf16>::value) {
+    if (so == nullptr && expert_tc_supported(d, m, topk)) {
+      void* ws = nullptr;
+      MITA_TRY(workspace(expert_tc_ws_bytes(B * H, m), st, &ws));
+      MITA_CUDA(launch_expert_tc(q, k, v, qt, vt, ti, off, qidx, B * H, N, m, topk, ds->num_sms,
+                                 ws, out, ds->status, st),
+                "expert launch");
+      return MITA_OK;
+    }
+  }
   MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, B * H, N, d, m, topk,
                                   out, ds->status, st),
             "expert launch");
@@ -272,7 +282,7 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
 }
 
 struct ForwardLayout {
-  size_t qt, vt, ti, route, off, qidx, lm, bk, total;
+  size_t qt, vt, ti, route, off, qidx, lm, bk, ex, total;
   LandmarkPlan plan;
 };
 
@@ -288,6 +298,7 @@ ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, size_t esize
   L.qidx = o; o += align256((size_t)BH * N * 4);
   L.lm = o; o += align256(landmark_ws_bytes(L.plan, BH, N, d, m));
   L.bk = o; o += align256(bucket_ws_bytes(BH, N, m));
+  L.ex = o; o += align256(expert_tc_ws_bytes(BH, m));
   L.total = o;
   return L;
 }
@@ -321,6 +332,14 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, ds, st),
             "route launch");
   MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st), "bucket launch");
+  if constexpr (std::is_same<T, bf16>::value) {
+    if (expert_tc_supported(d, m, topk)) {
+      MITA_CUDA(launch_expert_tc(q, k, v, qt, vt, ti, off, qidx, BH, N, m, topk, ds->num_sms,
+                                 ws + L.ex, out, ds->status, st),
+                "expert launch");
+      return MITA_OK;
+    }
+  }
   MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, nullptr, nullptr, BH, N, d, m,
                                   topk, out, ds->status, st),
             "expert launch");

@@ -30,9 +30,11 @@ enum : int {
 
 // Relative bound on |fp32 dot - exact dot| per unit of |a|_2 |b|_2 for a
 // length-D dot product accumulated in fp32 (sequential FMA or tensor-core
-// fp32 accumulation).  The classical bound is D * 2^-24 * sum|a_l b_l|; this
-// takes 8x that, which also covers the fp32 norms used to evaluate it.
-__host__ __device__ constexpr float err_gamma(int D) { return (float)D * 4.76837158203125e-07f; }  // D * 2^-21
+// fp32 accumulation).  Rounding every partial sum gives at most
+// D * 2^-24 * sum|a_l b_l|, truncating it at most twice that; this takes
+// twice the truncation bound, which also covers the fp32 norms used to
+// evaluate it (sum|a_l b_l| <= |a|_2 |b|_2).
+__host__ __device__ constexpr float err_gamma(int D) { return (float)D * 2.384185791015625e-07f; }  // D * 2^-22
 
 // ---------------------------------------------------------------------------
 // Element access

@@ -41,7 +41,7 @@ struct LandmarkWs {
   int* slow_rows;  // [BH * m]
   double* exact;   // [kExactCtas, N]  fp64 score scratch of the fallback
   // tensor-core path (M/L/A then hold 2 partials per split: one per softmax slot)
-  float* bm;       // [BH, ntiles, m]  largest raw score of each 128-key tile
+  float* bm;       // [BH, m, 2S, 32]  largest tile maxima (raw scores) per split slot
   float* thr;      // [BH, m]          collection threshold tau_L - 4E
   float* E;        // [BH, m]          fp32 score error bound
   int* cnt;        // [BH, m]          candidates collected
@@ -59,6 +59,7 @@ cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, in
                             int32_t* topk_idx, float* v_tilde, int* status, cudaStream_t st);
 
 bool landmark_tc_eligible(int d, int N, int topk);
+int landmark_tc_top_tiles();
 void plan_landmark_tc(LandmarkPlan& p, int BH, int N, int m, int topk, int num_sms);
 cudaError_t launch_landmark_tc_passes(const __nv_bfloat16* q_tilde, const __nv_bfloat16* k,
                                       const __nv_bfloat16* v, int BH, int N, int m, int topk,
@@ -90,10 +91,21 @@ cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_ti
 // ---- tensor-core (tcgen05) kernels: bf16, d = 64 ---------------------------
 // TMA map over a [batches, rows, 64] bf16 array, boxes of box_rows rows.
 bool make_tmap_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t batches,
-                      uint32_t box_rows);
+                      uint32_t box_rows, bool fp16 = false);
+// TMA map over a [rows, 64] bf16 array for tile::gather4 (four scattered rows).
+bool make_tmap_gather64(CUtensorMap* map, const void* base, uint64_t rows);
 bool route_tc_supported(int d, int m);
 cudaError_t launch_route_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH, int N,
                             int m, int num_sms, int32_t* route, int* status, cudaStream_t st);
+
+bool expert_tc_supported(int d, int m, int topk);
+size_t expert_tc_ws_bytes(int BH, int m);
+cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                             const __nv_bfloat16* v, const __nv_bfloat16* q_tilde,
+                             const float* v_tilde, const int32_t* topk_idx,
+                             const int32_t* bucket_off, const int32_t* bucket_qidx, int BH, int N,
+                             int m, int topk, int num_sms, void* ws, __nv_bfloat16* out,
+                             int* status, cudaStream_t st);
 
 int num_sms_of_current_device();
 

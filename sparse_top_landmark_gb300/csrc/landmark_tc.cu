@@ -17,10 +17,11 @@
 //   warps 8-11   with its own online-softmax state (max, sum) and its own O
 //                accumulator, so one computes while the other's MMAs run.
 //                Rescaling of O is lazy (only when the max grows by more than
-//                2^8).  They also record each tile's largest raw score.
-// threshold, CTA = (head, 32 landmarks): merges the softmax partials into v~
-//   (tutorial ch. 4: (Z1 o1 + Z2 o2) / (Z1 + Z2)) and radix-selects the k-th
-//   largest tile maximum tau_L.  k distinct tiles reach tau_L, so at least k
+//                2^8).  Each also keeps the 32 largest tile maxima (raw
+//                scores) it saw, in a small shared-memory min-heap.
+// threshold, CTA = one landmark: merges the softmax partials into v~
+//   (tutorial ch. 4: (Z1 o1 + Z2 o2) / (Z1 + Z2)) and takes the k-th largest
+//   kept tile maximum tau_L.  k distinct tiles reach tau_L, so at least k
 //   keys score >= tau_L: every top-k key scores >= tau_L - E (exactly) and
 //   >= tau_L - 2E in fp32 (E bounds the fp32 error).  Collection uses
 //   tau_L - 4E, which stays valid even if pass 2's fp32 scores differ from
@@ -42,6 +43,7 @@ constexpr int BN = 128;          // keys per tile
 constexpr int kStages = 4;       // K/V ring depth
 constexpr int kThreads = 384;    // 12 warps
 constexpr float kLazy = 8.0f;    // rescale O only when the max grows by > 2^8
+constexpr int kTopTiles = 32;    // tile maxima kept per (landmark, split, slot)
 
 __device__ __forceinline__ float softmax_c() { return 0.18033688011112042f; }  // log2(e)/8
 
@@ -49,6 +51,7 @@ struct alignas(1024) SweepSmem {
   bf16 qt[128 * 64];
   bf16 k[kStages][BN * 64];
   bf16 v[kStages][BN * 64];
+  float top[2][kTopTiles][128];    // per slot: min-heap of tile maxima, [entry][row]
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t qt_full, drain;
   uint64_t s_full[2], p_full[2], pv_done[2];
@@ -56,27 +59,48 @@ struct alignas(1024) SweepSmem {
   uint32_t tmem;
 };
 
-// squared norm of row r of a 128B-swizzled bf16 tile
-__device__ __forceinline__ float swz_row_norm2(const bf16* tile, int r) {
-  const char* base = reinterpret_cast<const char*>(tile);
-  float a = 0.f;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 x = *reinterpret_cast<const uint4*>(base + sw128_offset(r, c));
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-      a = fmaf(lo, lo, a);
-      a = fmaf(hi, hi, a);
-    }
-  }
-  return a;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Single MUFU 2^x (flushes subnormal results to zero; P is bf16 anyway).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// Paired fp32 arithmetic (two lanes of work per instruction).
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max of |x| over the 64 bf16 values of a 128-byte row group: bf16 magnitudes
+// (sign cleared) order like their 15-bit integer patterns.
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // -------------------------------------------------------------------------------------------
@@ -85,7 +109,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 __global__ void __launch_bounds__(kThreads, 1)
 lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, int N, int m, int S, int split_len,
-                int ntiles_head, LandmarkWs ws, int* status) {
+                LandmarkWs ws, int* status) {
   extern __shared__ unsigned char smem_raw[];
   SweepSmem& s = *reinterpret_cast<SweepSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -180,21 +204,30 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       mbar_wait(&s.drain, 0);
     }
   } else if (warp == 2 || warp == 3) {
-    // squared key norms; each warp takes 64 keys of every tile
-    float km = 0.f;
+    // largest |k| element of the split (bounds every key norm by 8 max|k|);
+    // each warp scans half of every tile, zero-filled rows past N are harmless
+    uint32_t mx = 0u;
     bool ok = true;
     for (int j = 0; j < ntl; ++j) {
       const int st = j % kStages;
       if (ok && !mbar_wait(&s.kv_full[st], (j / kStages) & 1)) ok = false;
       if (ok) {
-        for (int r = (warp - 2) * 64 + lane; r < (warp - 2) * 64 + 64; r += 32)
-          if (j0 + j * BN + r < j1) km = fmaxf(km, swz_row_norm2(s.k[st], r));
+        const uint4* src = reinterpret_cast<const uint4*>(s.k[st]) + (warp - 2) * 512;
+#pragma unroll 4
+        for (int i = lane; i < 512; i += 32) {
+          const uint4 x = src[i];
+          mx = umax16x2(mx, x.x & 0x7fff7fffu);
+          mx = umax16x2(mx, x.y & 0x7fff7fffu);
+          mx = umax16x2(mx, x.z & 0x7fff7fffu);
+          mx = umax16x2(mx, x.w & 0x7fff7fffu);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.kv_empty[st]);
     }
-    km = warp_max(km);
-    if (lane == 0) s.nred[warp - 2] = km;
+    const float a = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
+    const float km = warp_max(a);
+    if (lane == 0) s.nred[warp - 2] = 64.f * km * km;   // bound on |k|^2
     if (!ok) flag_error(status, kDevErrTimeout);
   } else {
     // ------------------------------------------------------------ softmax
@@ -211,12 +244,15 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
     float mref = -INFINITY, lsum = 0.f;
     bool ok = true;
     int t = 0;
+    for (int e = 0; e < kTopTiles; ++e) s.top[slot][e][row] = -INFINITY;
+    float theta = -INFINITY;
     for (int j = slot; j < ntl; j += 2, ++t) {
       if (ok && !mbar_wait(&s.s_full[slot], t & 1)) ok = false;
       tc_fence_after();
       const int kbase = j0 + j * BN;
       const int nvalid = min(BN, j1 - kbase);
       // pass A over S: the tile's largest raw score
+      const bool full = nvalid == BN;
       float tm = -INFINITY;
       if (ok) {
 #pragma unroll
@@ -224,19 +260,41 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
           float v[32];
           tmem_ld32(tS + cc * 32, v);
           tmem_ld_wait();
+          if (!full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) tm = fmaxf(tm, (cc * 32 + i < nvalid) ? v[i] : -INFINITY);
+            for (int i = 0; i < 32; ++i) v[i] = (cc * 32 + i < nvalid) ? v[i] : -INFINITY;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) tm = max3(tm, v[i], v[i + 1]);
         }
       }
-      if (live_row && ok)
-        ws.bm[((size_t)bh * ntiles_head + (kbase / BN)) * m + grow] = tm;
+      // keep the kTopTiles largest tile maxima of this slot (min-heap, root = smallest)
+      if (tm > theta) {
+        float* hp = &s.top[slot][0][row];
+        int pos = 0;
+        for (;;) {
+          const int ch = 2 * pos + 1;
+          if (ch >= kTopTiles) break;
+          float cv = hp[ch * 128];
+          int cix = ch;
+          if (ch + 1 < kTopTiles) {
+            const float cv2 = hp[(ch + 1) * 128];
+            if (cv2 < cv) { cv = cv2; cix = ch + 1; }
+          }
+          if (cv >= tm) break;
+          hp[pos * 128] = cv;
+          pos = cix;
+        }
+        hp[pos * 128] = tm;
+        theta = hp[0];
+      }
       const float xm = tm * c;
       // P_slot and O_slot are free once the previous P.V of this slot is done
       if (t > 0 && ok && !mbar_wait(&s.pv_done[slot], (t - 1) & 1)) ok = false;
       tc_fence_after();
       const bool need = (t == 0) || (xm > mref + kLazy);
       if (t > 0 && __any_sync(0xffffffffu, need)) {
-        const float f = need ? exp2f(mref - xm) : 1.f;
+        const float f = need ? ex2(mref - xm) : 1.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float o[32];
@@ -250,12 +308,12 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
         tmem_st_wait();
       }
       if (need) {
-        if (t > 0) lsum *= exp2f(mref - xm);
+        if (t > 0) lsum *= ex2(mref - xm);
         mref = xm;
       }
       // pass B over S: P = exp2(s * c - mref) as bf16 pairs into tensor memory
-      const float nm = -mref;
-      float ls = 0.f;
+      const unsigned long long c2 = f2pack(c, c), nm2 = f2pack(-mref, -mref);
+      unsigned long long ls2 = f2pack(0.f, 0.f);
 #pragma unroll
       for (int cc = 0; cc < BN / 32; ++cc) {
         float v[32];
@@ -264,13 +322,21 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = (cc * 32 + i < nvalid) ? exp2f(fmaf(v[i], c, nm)) : 0.f;
-          const float p1 = (cc * 32 + i + 1 < nvalid) ? exp2f(fmaf(v[i + 1], c, nm)) : 0.f;
-          ls += p0 + p1;
+          float x0, x1;
+          f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, nm2), x0, x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
+          if (!full) {
+            p0 = (cc * 32 + i < nvalid) ? p0 : 0.f;
+            p1 = (cc * 32 + i + 1 < nvalid) ? p1 : 0.f;
+          }
+          ls2 = add2(ls2, f2pack(p0, p1));
           pk[i / 2] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tP + cc * 16, pk);
       }
+      float ls_a, ls_b;
+      f2unpack(ls2, ls_a, ls_b);
+      const float ls = ls_a + ls_b;
       lsum += ls;
       tmem_st_wait();
       tc_fence_before();
@@ -291,6 +357,9 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
     }
     if (live_row) {
       const size_t pidx = ((size_t)bh * m + grow) * (2 * S) + sp * 2 + slot;
+      float* tt = ws.bm + pidx * kTopTiles;
+#pragma unroll 8
+      for (int e = 0; e < kTopTiles; ++e) tt[e] = s.top[slot][e][row];
       ws.M[pidx] = mref;
       ws.L[pidx] = lsum;
       float4* dst = reinterpret_cast<float4*>(ws.A + pidx * 64);
@@ -307,96 +376,52 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
 }
 
 // -------------------------------------------------------------------------------------------
-// threshold: v~ from the partials, tau_L by radix select over the tile maxima
+// threshold, one CTA per landmark: v~ from the partials; tau_L = the topk-th
+// largest of the kept tile maxima (each is the maximum of a distinct tile, so
+// at least topk keys score >= tau_L)
 // -------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t fkey(float x) {
-  const uint32_t u = __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float fkey_inv(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 __global__ void __launch_bounds__(256)
-lm_threshold_kernel(const bf16* __restrict__ q_tilde, int N, int m, int topk, int S2, int S,
-                    int ntiles_head, LandmarkWs ws, float* __restrict__ v_tilde) {
-  __shared__ int hist[32][257];
-  __shared__ uint32_t s_prefix[32];
-  __shared__ int s_need[32];
-  __shared__ float s_km2;
-  const int ngroups = (m + 31) / 32;
-  const int bh = blockIdx.x / ngroups;
-  const int r0 = (blockIdx.x % ngroups) * 32;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  (void)N;
-
-  // ---- v~ : 8 threads per row, 8 dims each
-  {
-    const int rr = tid >> 3, part = tid & 7;
-    const int row = r0 + rr;
-    if (row < m) {
-      const size_t base = ((size_t)bh * m + row) * S2;
-      float mx = -INFINITY;
-      for (int q = 0; q < S2; ++q) mx = fmaxf(mx, ws.M[base + q]);
-      float num[8], den = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) num[i] = 0.f;
-      for (int q = 0; q < S2; ++q) {
-        const float w = exp2f(ws.M[base + q] - mx);
-        den = fmaf(w, ws.L[base + q], den);
-        const float* o = ws.A + (base + q) * 64 + part * 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) num[i] = fmaf(w, o[i], num[i]);
-      }
-      float* out = v_tilde + ((size_t)bh * m + row) * 64 + part * 8;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) out[i] = num[i] / den;
+lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, int S, int P,
+                    LandmarkWs ws, float* __restrict__ v_tilde) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* val = reinterpret_cast<float*>(smem_raw);   // [P]
+  int* idx = reinterpret_cast<int*>(val + P);         // [P]
+  __shared__ float red[8];
+  const long long rf = blockIdx.x;
+  const long long bh = rf / m;
+  const int tid = threadIdx.x;
+  const size_t base = (size_t)rf * S2;
+  // ---- v~
+  float mx = -INFINITY;
+  for (int q = tid; q < S2; q += 256) mx = fmaxf(mx, ws.M[base + q]);
+  mx = block_max(mx, red);
+  if (tid < 64) {
+    float num = 0.f, den = 0.f;
+    for (int q = 0; q < S2; ++q) {
+      const float w = exp2f(ws.M[base + q] - mx);
+      den = fmaf(w, ws.L[base + q], den);
+      num = fmaf(w, ws.A[(base + q) * 64 + tid], num);
     }
+    v_tilde[rf * 64 + tid] = num / den;
   }
-  // ---- largest squared key norm of the head
-  if (warp == 0) {
-    float km = 0.f;
-    for (int q = lane; q < S; q += 32) km = fmaxf(km, ws.kmax2[(size_t)bh * S + q]);
-    km = warp_max(km);
-    if (lane == 0) s_km2 = km;
+  // ---- tau_L
+  const int n = S2 * kTopTiles;
+  const float* tops = ws.bm + base * kTopTiles;
+  for (int t = tid; t < P; t += 256) {
+    val[t] = t < n ? tops[t] : -INFINITY;
+    idx[t] = t;
   }
-  if (tid < 32) { s_prefix[tid] = 0u; s_need[tid] = topk; }
-  // ---- radix select (4 passes of 8 bits) of the topk-th largest tile max per row
-  const float* bm = ws.bm + (size_t)bh * ntiles_head * m;
-  uint32_t mask = 0u;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 32 * 257; i += 256) (&hist[0][0])[i] = 0;
-    __syncthreads();
-    const int row = r0 + lane;
-    if (row < m) {
-      const uint32_t pre = s_prefix[lane];
-      for (int tl = warp; tl < ntiles_head; tl += 8) {
-        const uint32_t key = fkey(bm[(size_t)tl * m + row]);
-        if ((key & mask) == pre) atomicAdd(&hist[lane][(key >> shift) & 255], 1);
-      }
-    }
-    __syncthreads();
-    if (tid < 32 && r0 + tid < m) {
-      int need = s_need[tid], cum = 0, dg = 255;
-      for (; dg > 0; --dg) {
-        if (cum + hist[tid][dg] >= need) break;
-        cum += hist[tid][dg];
-      }
-      s_need[tid] = need - cum;
-      s_prefix[tid] |= (uint32_t)dg << shift;
-    }
-    mask |= 0xffu << shift;
-    __syncthreads();
-  }
-  if (tid < 32 && r0 + tid < m) {
-    const int row = r0 + tid;
-    const size_t rf = (size_t)bh * m + row;
-    const bf16* qr = q_tilde + rf * 64;
-    float qn2 = 0.f;
-    for (int l = 0; l < 64; ++l) { const float x = __bfloat162float(qr[l]); qn2 = fmaf(x, x, qn2); }
-    const float E = err_gamma(64) * sqrtf(qn2) * sqrtf(s_km2);
-    const float tauL = ntiles_head >= topk ? fkey_inv(s_prefix[tid]) : -INFINITY;
+  bitonic_sort_desc(val, idx, P);
+  // ---- error bound
+  float km = 0.f;
+  for (int q = tid; q < S; q += 256) km = fmaxf(km, ws.kmax2[(size_t)bh * S + q]);
+  km = block_max(km, red);
+  float qn2 = 0.f;
+  if (tid < 64) { const float x = __bfloat162float(q_tilde[rf * 64 + tid]); qn2 = x * x; }
+  qn2 = block_sum(qn2, red);
+  if (tid == 0) {
+    const float E = err_gamma(64) * sqrtf(qn2) * sqrtf(km);
+    const float tauL = val[topk - 1];          // -inf when fewer than topk maxima exist
     ws.E[rf] = E;
     ws.thr[rf] = tauL - 4.f * E;
     ws.cnt[rf] = 0;
@@ -408,9 +433,14 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int N, int m, int topk, in
 // -------------------------------------------------------------------------------------------
 constexpr int kKStages = 4;
 
+constexpr int kLocalCand = 64;   // candidates per row buffered in shared memory
+
 struct alignas(1024) CollectSmem {
   bf16 qt[128 * 64];
   bf16 k[kKStages][BN * 64];
+  float cs[kLocalCand][128];      // [slot][row]: lanes never share a bank
+  int ci[kLocalCand][128];
+  int cn[128];
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t qt_full, drain;
   uint64_t s_full[2], s_free[2];
@@ -433,6 +463,7 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
   const int j1 = min(N, j0 + split_len);
   const int ntl = (j1 - j0 + BN - 1) / BN;
 
+  if (threadIdx.x < 128) s.cn[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&s.k_full[i], 1);
@@ -515,18 +546,27 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
           float v[32];
           tmem_ld32(tS + cc * 32, v);
           tmem_ld_wait();
-          float cm = -INFINITY;
+          // bitmask of the scores at or above the threshold (branch-free), then
+          // visit only its set bits
+          uint32_t msk = 0u;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) cm = fmaxf(cm, v[i]);
-          if (cm >= thr) {
-            for (int i = 0; i < 32; ++i) {
-              const int kk = cc * 32 + i;
-              if (kk < nvalid && v[i] >= thr) {
-                const int pos = atomicAdd(ws.cnt + rf, 1);
-                if (pos < cap) {
-                  ws.cand_s[rf * cap + pos] = v[i];
-                  ws.cand_i[rf * cap + pos] = kbase + kk;
-                }
+          for (int i = 0; i < 32; ++i) msk |= (v[i] >= thr ? 1u : 0u) << i;
+          if (nvalid - cc * 32 < 32) msk &= (nvalid - cc * 32 <= 0) ? 0u : (0xffffffffu >> (32 - (nvalid - cc * 32)));
+          while (msk) {
+            const int i = __ffs(msk) - 1;
+            msk &= msk - 1;
+            float x = v[0];
+#pragma unroll
+            for (int u = 1; u < 32; ++u) x = (u == i) ? v[u] : x;
+            const int pos = atomicAdd(&s.cn[row], 1);
+            if (pos < kLocalCand) {
+              s.cs[pos][row] = x;
+              s.ci[pos][row] = kbase + cc * 32 + i;
+            } else {
+              const int gpos = atomicAdd(ws.cnt + rf, 1);
+              if (gpos < cap) {
+                ws.cand_s[rf * cap + gpos] = x;
+                ws.cand_i[rf * cap + gpos] = kbase + cc * 32 + i;
               }
             }
           }
@@ -542,6 +582,22 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tbase, 256);
+  // flush the shared-memory candidate lists, one global reservation per row
+  if (warp >= 4 && warp < 8) {
+    const int row = (warp & 3) * 32 + lane;
+    const int grow = rt * 128 + row;
+    if (grow < m) {
+      const size_t rf = (size_t)bh * m + grow;
+      const int n = min(s.cn[row], kLocalCand);
+      if (n > 0) {
+        const int base = atomicAdd(ws.cnt + rf, n);
+        for (int i = 0; i < n && base + i < cap; ++i) {
+          ws.cand_s[rf * cap + base + i] = s.cs[i][row];
+          ws.cand_i[rf * cap + base + i] = s.ci[i][row];
+        }
+      }
+    }
+  }
 }
 
 }  // namespace
@@ -550,12 +606,16 @@ bool landmark_tc_eligible(int d, int N, int topk) {
   return d == 64 && (N + BN - 1) / BN >= 2 * topk;
 }
 
+int landmark_tc_top_tiles() { return kTopTiles; }
+
 void plan_landmark_tc(LandmarkPlan& p, int BH, int N, int m, int topk, int num_sms) {
   p.tc = true;
   p.RT = 128;
   p.nrt = (m + 127) / 128;
   const int ctas_per_split = BH * p.nrt;
   int S = std::max(1, (num_sms + ctas_per_split - 1) / ctas_per_split);
+  // at least 2*topk kept tile maxima per landmark (2 slots x kTopTiles per split)
+  S = std::max(S, (topk + kTopTiles - 1) / kTopTiles);
   S = std::min(S, (N + BN - 1) / BN);
   p.split_len = ((N + S - 1) / S + BN - 1) / BN * BN;
   p.S = (N + p.split_len - 1) / p.split_len;
@@ -579,12 +639,15 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
   cudaError_t e = cudaFuncSetAttribute(lm_sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sm1);
   if (e != cudaSuccess) return e;
-  lm_sweep_kernel<<<blocks, kThreads, sm1, st>>>(mqt, mk, mv, N, m, p.S, p.split_len, p.ntiles, ws,
-                                                 status);
+  lm_sweep_kernel<<<blocks, kThreads, sm1, st>>>(mqt, mk, mv, N, m, p.S, p.split_len, ws, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const unsigned tblocks = (unsigned)(BH * ((m + 31) / 32));
-  lm_threshold_kernel<<<tblocks, 256, 0, st>>>(q_tilde, N, m, topk, 2 * p.S, p.S, p.ntiles, ws,
-                                               v_tilde);
+  const int P = next_pow2(2 * p.S * kTopTiles);
+  const size_t tsm = (size_t)P * 8;
+  e = cudaFuncSetAttribute(lm_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tsm);
+  if (e != cudaSuccess) return e;
+  lm_threshold_kernel<<<(unsigned)((long long)BH * m), 256, tsm, st>>>(q_tilde, m, topk, 2 * p.S,
+                                                                       p.S, P, ws, v_tilde);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t sm2 = sizeof(CollectSmem) + 1024;
   e = cudaFuncSetAttribute(lm_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);

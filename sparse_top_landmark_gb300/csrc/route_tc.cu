@@ -11,7 +11,9 @@
 //               W <= 256 landmarks, two chunk buffers (ping-pong);
 //   warps 4-11  epilogue: TMEM lane quadrant = warp % 4 (one query row per
 //               thread), two warps per quadrant split each chunk's columns.
-// Each thread keeps the top fp32 scores of its query.  If the runner-up is
+// Each thread keeps the best and runner-up fp32 scores of its query with
+// branch-free min/max (the index of the best is looked up only in the rare
+// 16-score group that raises it).  If the runner-up is
 // within 2E of the best (E bounds the fp32 dot error), the warp re-scores the
 // query's plausible winners with exact-product fp32 arithmetic (no fp64: it
 // runs at a small fraction of the fp32 rate here).  The result is the exact
@@ -32,8 +34,8 @@ constexpr int kThreads = (4 + kEpiWarps) * 32;
 constexpr int kMaxM = 512;
 
 struct Cand {
-  float v1, v2, v3;
-  int i1, i2;
+  float v1, v2;   // best and runner-up fp32 scores
+  int i1;         // lowest index reaching v1
 };
 
 struct alignas(1024) RouteSmem {
@@ -112,19 +114,31 @@ __device__ void resolve_near_ties(const bf16* qtile, const bf16* qt, int m, int 
   }
 }
 
-// Insert (x, i) into the running top three (value desc; an equal value keeps
-// the earlier, lower index ahead).
-__device__ __forceinline__ void top3_offer(Cand& c, float x, int i) {
-  if (x > c.v3) {
-    if (x > c.v2) {
-      if (x > c.v1) {
-        c.v3 = c.v2; c.v2 = c.v1; c.i2 = c.i1; c.v1 = x; c.i1 = i;
-      } else {
-        c.v3 = c.v2; c.v2 = x; c.i2 = i;
-      }
-    } else {
-      c.v3 = x;
-    }
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Running best value v1 (at index i1, the lowest index reaching it) and
+// runner-up value v2, over 16 scores starting at index i0.  Branch-free except
+// for the rare group that raises v1, where the index is looked up.
+__device__ __forceinline__ void top2_group(Cand& c, const float* v, int i0, int nvalid) {
+  const float before = c.v1;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float a = (i < nvalid) ? v[i] : -INFINITY;
+    const float b = (i + 1 < nvalid) ? v[i + 1] : -INFINITY;
+    const float hi = fmaxf(a, b), lo = fminf(a, b);
+    c.v2 = max3f(c.v2, lo, fminf(c.v1, hi));
+    c.v1 = fmaxf(c.v1, hi);
+  }
+  if (c.v1 > before) {
+    int k = 0;
+#pragma unroll
+    for (int i = 15; i >= 0; --i)
+      if (i < nvalid && v[i] == c.v1) k = i;
+    c.i1 = i0 + k;
   }
 }
 
@@ -238,7 +252,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     for (int it = 0; it < ntiles; ++it) {
       const int st = it % kQStages;
       if (ok && !mbar_wait(&s.q_full[st], (it / kQStages) & 1)) ok = false;
-      Cand c{-INFINITY, -INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff};
+      Cand c{-INFINITY, -INFINITY, 0x7fffffff};
       for (int ch = 0; ch < nch; ++ch, ++gch) {
         const int b = gch & 1;
         if (ok && !mbar_wait(&s.s_full[b], (gch >> 1) & 1)) ok = false;
@@ -250,9 +264,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             tmem_ld16(tbase + taddr_lane + (uint32_t)(b * W + col0 + cc), v);
             tmem_ld_wait();
             const int i0 = ch * W + col0 + cc;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (i0 + i < m) top3_offer(c, v[i], i0 + i);
+            top2_group(c, v, i0, m - i0);
           }
         }
         tc_fence_before();
@@ -267,18 +279,11 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       epi_bar();
       if (half == 0) {
         const Cand o = s.cand[it & 1][row];
-        // merge the two halves' top three, (value desc, index asc)
+        // merge the two halves: best (ties to the lower index) and runner-up
         Cand r = c;
-        const bool w1 = ranks_before(o.v1, o.i1, c.v1, c.i1);
-        if (w1) {
-          r.v1 = o.v1; r.i1 = o.i1;
-          // runner-up: best of (c.v1, o.v2)
-          if (ranks_before(c.v1, c.i1, o.v2, o.i2)) { r.v2 = c.v1; r.i2 = c.i1; r.v3 = fmaxf(c.v2, o.v2); }
-          else { r.v2 = o.v2; r.i2 = o.i2; r.v3 = fmaxf(c.v1, o.v3); }
-        } else {
-          if (ranks_before(o.v1, o.i1, c.v2, c.i2)) { r.v2 = o.v1; r.i2 = o.i1; r.v3 = fmaxf(c.v2, o.v2); }
-          else { r.v2 = c.v2; r.i2 = c.i2; r.v3 = fmaxf(c.v3, o.v1); }
-        }
+        const bool w1 = o.v1 > c.v1 || (o.v1 == c.v1 && o.i1 < c.i1);
+        r.v2 = max3f(c.v2, o.v2, fminf(c.v1, o.v1));
+        if (w1) { r.v1 = o.v1; r.i1 = o.i1; }
         const int n = (c0 + it * G_h) * 128 + row;
         const bool live = ok && n < N;
         float twoE = 0.f;
