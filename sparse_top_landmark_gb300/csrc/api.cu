@@ -209,12 +209,21 @@ int landmark_impl(const T* qt, const T* k, const T* v, int B, int H, int N, int 
 
 // Tensor-core route for bf16 / d = 64 / m <= 512 when no shared partial is
 // requested; the SIMT kernel otherwise.
+size_t route_ws_bytes(int BH, int N) { return ((size_t)BH * N + 1) * sizeof(int); }
+
+template <typename T>
+bool route_uses_tc(int d, int m, const float* lse, const float* so) {
+  return std::is_same<T, bf16>::value && !lse && !so && route_tc_supported(d, m);
+}
+
 template <typename T>
 cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int N, int d, int m,
-                           int32_t* route, float* lse, float* so, DevState* ds, cudaStream_t st) {
+                           int32_t* route, float* lse, float* so, DevState* ds, void* ws,
+                           cudaStream_t st) {
   if constexpr (std::is_same<T, bf16>::value) {
-    if (!lse && !so && route_tc_supported(d, m))
-      return launch_route_tc(q, qt, BH, N, m, ds->num_sms, route, ds->status, st);
+    if (route_uses_tc<T>(d, m, lse, so))
+      return launch_route_tc(q, qt, BH, N, m, ds->num_sms, route, static_cast<int*>(ws),
+                             ds->status, st);
   }
   return launch_route<T>(q, qt, vt, BH, N, d, m, route, lse, so, st);
 }
@@ -230,7 +239,10 @@ int route_impl(const T* q, const T* qt, const float* vt, int B, int H, int N, in
   if (so) MITA_TRY(check_ptrs({{so, "shared_o"}}));
   DevState* ds = nullptr;
   MITA_TRY(device_state(&ds));
-  MITA_CUDA(route_dispatch<T>(q, qt, vt, B * H, N, d, m, route, lse, so, ds, st), "route launch");
+  void* ws = nullptr;
+  if (route_uses_tc<T>(d, m, lse, so)) MITA_TRY(workspace(route_ws_bytes(B * H, N), st, &ws));
+  MITA_CUDA(route_dispatch<T>(q, qt, vt, B * H, N, d, m, route, lse, so, ds, ws, st),
+            "route launch");
   return MITA_OK;
 }
 
@@ -282,7 +294,7 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
 }
 
 struct ForwardLayout {
-  size_t qt, vt, ti, route, off, qidx, lm, bk, ex, total;
+  size_t qt, vt, ti, route, off, qidx, lm, bk, ex, rt, total;
   LandmarkPlan plan;
 };
 
@@ -299,6 +311,7 @@ ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, size_t esize
   L.lm = o; o += align256(landmark_ws_bytes(L.plan, BH, N, d, m));
   L.bk = o; o += align256(bucket_ws_bytes(BH, N, m));
   L.ex = o; o += align256(expert_tc_ws_bytes(BH, m));
+  L.rt = o; o += align256(route_ws_bytes(BH, N));
   L.total = o;
   return L;
 }
@@ -329,7 +342,7 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, m, qt, st), "pool launch");
   MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, ds->status, st),
             "landmark launch");
-  MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, ds, st),
+  MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, ds, ws + L.rt, st),
             "route launch");
   MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st), "bucket launch");
   if constexpr (std::is_same<T, bf16>::value) {

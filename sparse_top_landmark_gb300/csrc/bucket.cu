@@ -4,22 +4,27 @@
 // experts, then grouping the queries by routing result so that each expert's
 // KV rows are gathered once for all of its queries.  The grouping here is a
 // stable counting sort in three launches (phases meet at kernel boundaries,
-// no inter-CTA waiting):
-//   count   -- one warp per chunk of kBucketChunk queries adds its per-expert
-//              counts into hist[bh][chunk][e];
-//   scan    -- one CTA per head: bucket_off = exclusive prefix of the counts,
-//              and hist[bh][chunk][e] becomes the chunk's first slot in e;
-//   scatter -- the same warps walk their chunk in query order and place each
-//              query at its slot (warp match + popcount gives the rank among
-//              equal experts in a batch of 32), so every bucket lists its
-//              queries in ascending order.
+// no inter-CTA waiting), with the queries of a head cut into chunks of
+// kBucketChunk:
+//   count   -- one CTA per chunk: shared-memory histogram of its experts,
+//              written as hist[bh][e][chunk];
+//   scan    -- one CTA per head: per-expert totals, their exclusive prefix
+//              (bucket_off), and for every (expert, chunk) the chunk's first
+//              slot in that expert's bucket (one warp per expert);
+//   scatter -- one CTA per chunk, eight warps on consecutive sub-chunks: a
+//              per-expert prefix across the warps, then each warp places its
+//              queries in order (warp match + popcount ranks equal experts in
+//              a batch of 32), so every bucket lists its queries ascending.
+// Experts beyond kSmemExperts use the same passes with global counters.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mita {
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
+constexpr int kWarps = 8;
+constexpr int kSub = kBucketChunk / kWarps;     // queries per warp in the scatter
+constexpr int kSmemExperts = 2048;               // 8 x 2048 ints = 64 KB of shared memory
 
 __device__ __forceinline__ int load_route(const int32_t* route, long long bh, int N, int n,
                                           int m, int* status) {
@@ -32,79 +37,144 @@ __device__ __forceinline__ int load_route(const int32_t* route, long long bh, in
   return e;
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-bucket_count_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks, int cpb,
+__global__ void __launch_bounds__(256)
+bucket_count_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks,
                     int* __restrict__ hist, int* status) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long bh = blockIdx.x / cpb;
-  const int chunk = (blockIdx.x % cpb) * kWarpsPerBlock + warp;
-  if (chunk >= nchunks) return;
-  int* h = hist + ((size_t)bh * nchunks + chunk) * m;
+  extern __shared__ int h[];                     // [m] when m <= kSmemExperts
+  const long long bh = blockIdx.x / nchunks;
+  const int chunk = blockIdx.x % nchunks;
+  const bool smem = m <= kSmemExperts;
+  int* hg = hist + (size_t)bh * m * nchunks;      // [e][chunk]
+  if (smem) {
+    for (int e = threadIdx.x; e < m; e += 256) h[e] = 0;
+    __syncthreads();
+  }
   const int n0 = chunk * kBucketChunk;
-  for (int it = 0; it < kBucketChunk; it += 32) {
-    const int e = load_route(route, bh, N, n0 + it + lane, m, status);
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int leader = __ffs(peers) - 1;
-    if (e >= 0 && lane == leader) atomicAdd(h + e, __popc(peers));
+#pragma unroll 4
+  for (int t = threadIdx.x; t < kBucketChunk; t += 256) {
+    const int e = load_route(route, bh, N, n0 + t, m, status);
+    if (e >= 0) {
+      if (smem) atomicAdd(&h[e], 1);
+      else atomicAdd(&hg[(size_t)e * nchunks + chunk], 1);
+    }
+  }
+  if (smem) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < m; e += 256) hg[(size_t)e * nchunks + chunk] = h[e];
   }
 }
 
 __global__ void __launch_bounds__(1024)
-bucket_scan_kernel(int N, int m, int nchunks, int* __restrict__ hist,
-                   int32_t* __restrict__ bucket_off) {
+bucket_scan_kernel(int m, int nchunks, int* __restrict__ hist, int32_t* __restrict__ bucket_off) {
   __shared__ int red[33];
+  __shared__ int carry_s;
   const long long bh = blockIdx.x;
-  int* hb = hist + (size_t)bh * nchunks * m;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* hb = hist + (size_t)bh * m * nchunks;
   int32_t* off = bucket_off + (size_t)bh * (m + 1);
-  int carry = 0;
-  for (int e0 = 0; e0 < m; e0 += blockDim.x) {
+  // per-expert totals into bucket_off[e] (temporarily)
+  for (int e = warp; e < m; e += 32) {
+    int tot = 0;
+    for (int c = lane; c < nchunks; c += 32) tot += hb[(size_t)e * nchunks + c];
+    tot = warp_sum(tot);
+    if (lane == 0) off[e] = tot;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) carry_s = 0;
+  __syncthreads();
+  for (int e0 = 0; e0 < m; e0 += 1024) {
     const int e = e0 + threadIdx.x;
-    int cnt = 0;
-    if (e < m)
-      for (int c = 0; c < nchunks; ++c) cnt += hb[(size_t)c * m + e];
+    const int cnt = e < m ? off[e] : 0;
     int tot;
-    const int excl = block_excl_scan(cnt, red, &tot);
-    if (e < m) {
-      int run = carry + excl;
-      off[e] = run;
-      for (int c = 0; c < nchunks; ++c) {
-        const int t = hb[(size_t)c * m + e];
-        hb[(size_t)c * m + e] = run;
+    const int ex = block_excl_scan(cnt, red, &tot);
+    const int base = carry_s;
+    __syncthreads();
+    if (e < m) off[e] = base + ex;
+    if (threadIdx.x == 0) carry_s = base + tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) off[m] = carry_s;
+  __syncthreads();
+  // each (expert, chunk): first slot of the chunk's queries in the expert's bucket
+  for (int e = warp; e < m; e += 32) {
+    int run = off[e];
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int x = c < nchunks ? hb[(size_t)e * nchunks + c] : 0;
+      const int inc = warp_incl_scan(x);
+      if (c < nchunks) hb[(size_t)e * nchunks + c] = run + inc - x;
+      run += __shfl_sync(0xffffffffu, inc, 31);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks,
+                      int* __restrict__ hist, int32_t* __restrict__ bucket_qidx, int* status) {
+  extern __shared__ int hw[];                    // [kWarps][m] when m <= kSmemExperts
+  const long long bh = blockIdx.x / nchunks;
+  const int chunk = blockIdx.x % nchunks;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int* hg = hist + (size_t)bh * m * nchunks;
+  int32_t* out = bucket_qidx + (size_t)bh * N;
+  const int n0 = chunk * kBucketChunk + warp * kSub;
+  const unsigned lt = (1u << lane) - 1u;
+  if (m <= kSmemExperts) {
+    for (int i = threadIdx.x; i < kWarps * m; i += 256) hw[i] = 0;
+    __syncthreads();
+    // per-warp counts of its sub-chunk
+    for (int it = 0; it < kSub; it += 32) {
+      const int e = load_route(route, bh, N, n0 + it + lane, m, nullptr);
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) hw[warp * m + e] += __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    // exclusive prefix across the warps, starting at the chunk's slot
+    for (int e = threadIdx.x; e < m; e += 256) {
+      int run = hg[(size_t)e * nchunks + chunk];
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const int t = hw[w * m + e];
+        hw[w * m + e] = run;
         run += t;
       }
     }
-    carry += tot;
-  }
-  if (threadIdx.x == 0) off[m] = carry;
-  (void)N;
-}
-
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks, int cpb,
-                      int* __restrict__ hist, int32_t* __restrict__ bucket_qidx, int* status) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long bh = blockIdx.x / cpb;
-  const int chunk = (blockIdx.x % cpb) * kWarpsPerBlock + warp;
-  if (chunk >= nchunks) return;
-  int* h = hist + ((size_t)bh * nchunks + chunk) * m;
-  int32_t* out = bucket_qidx + (size_t)bh * N;
-  const int n0 = chunk * kBucketChunk;
-  const unsigned lt = (1u << lane) - 1u;
-  for (int it = 0; it < kBucketChunk; it += 32) {
-    const int n = n0 + it + lane;
-    const int e = load_route(route, bh, N, n, m, nullptr);
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int leader = __ffs(peers) - 1;
-    int base = 0;
-    if (e >= 0) base = h[e];
-    __syncwarp();
-    if (e >= 0) {
-      const int pos = base + __popc(peers & lt);
-      if (pos >= 0 && pos < N) out[pos] = n;
-      else flag_error(status, kDevErrBadBucket);
-      if (lane == leader) h[e] = base + __popc(peers);
+    __syncthreads();
+    int* my = hw + warp * m;
+    for (int it = 0; it < kSub; it += 32) {
+      const int n = n0 + it + lane;
+      const int e = load_route(route, bh, N, n, m, nullptr);
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      int base = 0;
+      if (e >= 0) base = my[e];
+      __syncwarp();
+      if (e >= 0) {
+        const int pos = base + __popc(peers & lt);
+        if (pos >= 0 && pos < N) out[pos] = n;
+        else flag_error(status, kDevErrBadBucket);
+        if (lane == __ffs(peers) - 1) my[e] = base + __popc(peers);
+      }
+      __syncwarp();
     }
-    __syncwarp();
+  } else if (warp == 0) {
+    // many experts: one warp walks the chunk in order with global counters
+    int* hgw = hist + (size_t)bh * m * nchunks;
+    for (int it = 0; it < kBucketChunk; it += 32) {
+      const int n = chunk * kBucketChunk + it + lane;
+      const int e = load_route(route, bh, N, n, m, nullptr);
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      int base = 0;
+      if (e >= 0) base = hgw[(size_t)e * nchunks + chunk];
+      __syncwarp();
+      if (e >= 0) {
+        const int pos = base + __popc(peers & lt);
+        if (pos >= 0 && pos < N) out[pos] = n;
+        else flag_error(status, kDevErrBadBucket);
+        if (lane == __ffs(peers) - 1) hgw[(size_t)e * nchunks + chunk] = base + __popc(peers);
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -119,18 +189,23 @@ cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* 
                           int32_t* bucket_off, int32_t* bucket_qidx, int* status,
                           cudaStream_t st) {
   const int nchunks = (N + kBucketChunk - 1) / kBucketChunk;
-  const int cpb = (nchunks + kWarpsPerBlock - 1) / kWarpsPerBlock;
   int* hist = static_cast<int*>(ws);
   cudaError_t e = cudaMemsetAsync(hist, 0, bucket_ws_bytes(BH, N, m), st);
   if (e != cudaSuccess) return e;
-  const unsigned blocks = (unsigned)((long long)BH * cpb);
-  bucket_count_kernel<<<blocks, kWarpsPerBlock * 32, 0, st>>>(route_idx, N, m, nchunks, cpb,
-                                                               hist, status);
+  const unsigned blocks = (unsigned)((long long)BH * nchunks);
+  const bool smem = m <= kSmemExperts;
+  const size_t s1 = smem ? (size_t)m * 4 : 0, s3 = smem ? (size_t)kWarps * m * 4 : 0;
+  if (s3 > 48 * 1024) {
+    e = cudaFuncSetAttribute(bucket_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)s3);
+    if (e != cudaSuccess) return e;
+  }
+  bucket_count_kernel<<<blocks, 256, s1, st>>>(route_idx, N, m, nchunks, hist, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bucket_scan_kernel<<<BH, 1024, 0, st>>>(N, m, nchunks, hist, bucket_off);
+  bucket_scan_kernel<<<BH, 1024, 0, st>>>(m, nchunks, hist, bucket_off);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bucket_scatter_kernel<<<blocks, kWarpsPerBlock * 32, 0, st>>>(route_idx, N, m, nchunks, cpb,
-                                                                 hist, bucket_qidx, status);
+  bucket_scatter_kernel<<<blocks, 256, s3, st>>>(route_idx, N, m, nchunks, hist, bucket_qidx,
+                                                 status);
   return cudaGetLastError();
 }
 

@@ -356,11 +356,12 @@ landmark_select_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, i
   if (!slow) {
     const float* cs = ws.cand_s + (size_t)rowflat * cap;
     const int* ci = ws.cand_i + (size_t)rowflat * cap;
-    for (int t = tid; t < P; t += blockDim.x) {
+    const int Ps = min(P, next_pow2(max(total, topk)));   // sort only what is there
+    for (int t = tid; t < Ps; t += blockDim.x) {
       us[t] = t < total ? cs[t] : -INFINITY;
       ui[t] = t < total ? ci[t] : 0x7fffffff;
     }
-    bitonic_sort_desc(us, ui, P);
+    bitonic_sort_desc(us, ui, Ps);
   }
   __syncthreads();
   finish_topk<T, D>(us, ui, total, topk, ws.E[rowflat], slow, qd, k + (size_t)bh * N * D, bx, bi,

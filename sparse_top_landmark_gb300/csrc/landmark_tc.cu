@@ -397,6 +397,7 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, i
   mx = block_max(mx, red);
   if (tid < 64) {
     float num = 0.f, den = 0.f;
+#pragma unroll 8
     for (int q = 0; q < S2; ++q) {
       const float w = exp2f(ws.M[base + q] - mx);
       den = fmaf(w, ws.L[base + q], den);

@@ -51,8 +51,10 @@ pool_kernel(const T* __restrict__ q, int N, int grid_h, int grid_w, int mh, int 
     for (int u = 0; u < UNR; ++u) {
       const int t = t0 + u * TL;
       if (t < cnt) {
-        const int r = r0 + t / nc, col = c0 + t % nc;
-        Vec<T>::load(base + ((size_t)r * grid_w + col) * D, x[u]);
+        // 1D windows (grid_h == 1) are contiguous: no division
+        const size_t tok = (r1 - r0 == 1) ? (size_t)r0 * grid_w + c0 + t
+                                          : (size_t)(r0 + t / nc) * grid_w + c0 + t % nc;
+        Vec<T>::load(base + tok * D, x[u]);
       } else {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) x[u][e] = 0.f;

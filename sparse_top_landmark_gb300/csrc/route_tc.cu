@@ -11,13 +11,14 @@
 //               W <= 256 landmarks, two chunk buffers (ping-pong);
 //   warps 4-11  epilogue: TMEM lane quadrant = warp % 4 (one query row per
 //               thread), two warps per quadrant split each chunk's columns.
-// Each thread keeps the best and runner-up fp32 scores of its query with
-// branch-free min/max (the index of the best is looked up only in the rare
-// 16-score group that raises it).  If the runner-up is
-// within 2E of the best (E bounds the fp32 dot error), the warp re-scores the
-// query's plausible winners with exact-product fp32 arithmetic (no fp64: it
-// runs at a small fraction of the fp32 rate here).  The result is the exact
-// argmax, ties to the lowest landmark index.
+// Each score's 9 low mantissa bits are replaced by (511 - landmark index);
+// a branch-free running top-2 over these packed values gives the best index
+// directly.  The packing moves a score by at most 2^-14 of its magnitude, so
+// when the packed best beats the runner-up by more than 2E + 2^-12 |best|
+// (E bounds the fp32 dot error) the index is the exact argmax.  Otherwise the
+// query is appended to an "ambiguous" list and route_fixup_kernel re-routes it
+// exactly (fp32 screening + exact-product re-scoring, ties to the lowest
+// index) -- about 0.2% of the queries on the long-sequence workloads.
 #include <algorithm>
 
 #include "common.cuh"
@@ -34,8 +35,7 @@ constexpr int kThreads = (4 + kEpiWarps) * 32;
 constexpr int kMaxM = 512;
 
 struct Cand {
-  float v1, v2;   // best and runner-up fp32 scores
-  int i1;         // lowest index reaching v1
+  float v1, v2;   // best and runner-up packed scores
 };
 
 struct alignas(1024) RouteSmem {
@@ -67,85 +67,34 @@ __device__ __forceinline__ void load_swizzled_row(const bf16* tile, int r, float
   }
 }
 
-// Exact-enough score of swizzled row ra of `ta` against row rb of `tb`.
-__device__ __forceinline__ F2 dot_rows_f2(const bf16* ta, int ra, const bf16* tb, int rb) {
-  float a[64], b[64];
-  load_swizzled_row(ta, ra, a);
-  load_swizzled_row(tb, rb, b);
-  return dot_f2<64>(a, b);
-}
-
-// Whole-warp exact argmax for every lane that flagged a near tie: the warp
-// splits the m landmarks, screens them with fp32 dots (a landmark can win only
-// if its fp32 score is within 2E of the tensor-core best), re-scores the
-// survivors with dot_f2 and reduces (score desc, index asc).
-__device__ void resolve_near_ties(const bf16* qtile, const bf16* qt, int m, int row, bool need,
-                                  float best, float twoE, int& ib) {
-  const int lane = threadIdx.x & 31;
-  unsigned mask = __ballot_sync(0xffffffffu, need);
-  while (mask) {
-    const int src = __ffs(mask) - 1;
-    mask &= mask - 1;
-    const int srow = __shfl_sync(0xffffffffu, row, src);
-    const float sbest = __shfl_sync(0xffffffffu, best, src);
-    const float stwoE = __shfl_sync(0xffffffffu, twoE, src);
-    float qr[64];
-    load_swizzled_row(qtile, srow, qr);
-    F2 bv{-INFINITY, 0.f};
-    int bi = 0x7fffffff;
-    for (int i = lane; i < m; i += 32) {
-      float r[64];
-      load_swizzled_row(qt, i, r);
-      float d = 0.f;
-#pragma unroll
-      for (int l = 0; l < 64; ++l) d = fmaf(qr[l], r[l], d);
-      if (d >= sbest - stwoE) {
-        const F2 x = dot_f2<64>(qr, r);
-        if (ranks_before(x, i, bv, bi)) { bv = x; bi = i; }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const F2 ov{__shfl_xor_sync(0xffffffffu, bv.hi, o), __shfl_xor_sync(0xffffffffu, bv.lo, o)};
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (lane == src) ib = bi;
-  }
-}
-
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
-// Running best value v1 (at index i1, the lowest index reaching it) and
-// runner-up value v2, over 16 scores starting at index i0.  Branch-free except
-// for the rare group that raises v1, where the index is looked up.
-__device__ __forceinline__ void top2_group(Cand& c, const float* v, int i0, int nvalid) {
-  const float before = c.v1;
+// Score with its low 9 mantissa bits replaced by (511 - index).
+__device__ __forceinline__ float pack_idx(float x, int i) {
+  return __uint_as_float((__float_as_uint(x) & ~511u) | (uint32_t)(511 - i));
+}
+__device__ __forceinline__ int unpack_idx(float x) { return 511 - (int)(__float_as_uint(x) & 511u); }
+
+// Running top-2 of 32 packed scores (indices i0..i0+31, those >= nvalid skipped).
+__device__ __forceinline__ void top2_32(Cand& c, const float* v, int i0, int nvalid) {
 #pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    const float a = (i < nvalid) ? v[i] : -INFINITY;
-    const float b = (i + 1 < nvalid) ? v[i + 1] : -INFINITY;
+  for (int i = 0; i < 32; i += 2) {
+    const float a = (i < nvalid) ? pack_idx(v[i], i0 + i) : -INFINITY;
+    const float b = (i + 1 < nvalid) ? pack_idx(v[i + 1], i0 + i + 1) : -INFINITY;
     const float hi = fmaxf(a, b), lo = fminf(a, b);
     c.v2 = max3f(c.v2, lo, fminf(c.v1, hi));
     c.v1 = fmaxf(c.v1, hi);
-  }
-  if (c.v1 > before) {
-    int k = 0;
-#pragma unroll
-    for (int i = 15; i >= 0; --i)
-      if (i < nvalid && v[i] == c.v1) k = i;
-    c.i1 = i0 + k;
   }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_qt,
                 int N, int m, int W, int nch, int G_h, uint32_t tmem_cols,
-                int32_t* __restrict__ route, int* status) {
+                int32_t* __restrict__ route, int* __restrict__ amb, int* status) {
   extern __shared__ unsigned char smem_raw[];
   RouteSmem& s = *reinterpret_cast<RouteSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -252,19 +201,28 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     for (int it = 0; it < ntiles; ++it) {
       const int st = it % kQStages;
       if (ok && !mbar_wait(&s.q_full[st], (it / kQStages) & 1)) ok = false;
-      Cand c{-INFINITY, -INFINITY, 0x7fffffff};
+      Cand c{-INFINITY, -INFINITY};
       for (int ch = 0; ch < nch; ++ch, ++gch) {
         const int b = gch & 1;
         if (ok && !mbar_wait(&s.s_full[b], (gch >> 1) & 1)) ok = false;
         tc_fence_after();
         if (ok) {
           const int col0 = half * cols_half;
-          for (int cc = 0; cc < cols_half; cc += 16) {
-            float v[16];
-            tmem_ld16(tbase + taddr_lane + (uint32_t)(b * W + col0 + cc), v);
+          for (int cc = 0; cc < cols_half; cc += 64) {
+            float v[64];
+            const uint32_t ta = tbase + taddr_lane + (uint32_t)(b * W + col0 + cc);
+            if (cols_half - cc >= 64) {
+              tmem_ld32(ta, v);
+              tmem_ld32(ta + 32, v + 32);
+            } else {
+              tmem_ld16(ta, v);          // cols_half is a multiple of 16
+              if (cols_half - cc > 16) tmem_ld16(ta + 16, v + 16);
+            }
             tmem_ld_wait();
             const int i0 = ch * W + col0 + cc;
-            top2_group(c, v, i0, m - i0);
+            const int lim = min(m - i0, cols_half - cc);
+            top2_32(c, v, i0, lim);
+            if (lim > 32) top2_32(c, v + 32, i0 + 32, lim - 32);
           }
         }
         tc_fence_before();
@@ -279,25 +237,29 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       epi_bar();
       if (half == 0) {
         const Cand o = s.cand[it & 1][row];
-        // merge the two halves: best (ties to the lower index) and runner-up
-        Cand r = c;
-        const bool w1 = o.v1 > c.v1 || (o.v1 == c.v1 && o.i1 < c.i1);
-        r.v2 = max3f(c.v2, o.v2, fminf(c.v1, o.v1));
-        if (w1) { r.v1 = o.v1; r.i1 = o.i1; }
+        const float v1 = fmaxf(c.v1, o.v1);
+        const float v2 = max3f(c.v2, o.v2, fminf(c.v1, o.v1));
         const int n = (c0 + it * G_h) * 128 + row;
         const bool live = ok && n < N;
-        float twoE = 0.f;
+        bool ambiguous = false;
         if (live) {
           float qr[64];
           load_swizzled_row(s.q[st], row, qr);
           float qn2 = 0.f;
 #pragma unroll
           for (int l = 0; l < 64; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
-          twoE = 2.f * gam * sqrtf(qn2) * sqrtf(qtmax2);
+          const float twoE = 2.f * gam * sqrtf(qn2) * sqrtf(qtmax2);
+          ambiguous = !(v1 - v2 > twoE + fabsf(v1) * 2.44140625e-4f);   // 2^-12
+          route[(size_t)bh * N + n] = unpack_idx(v1);
         }
-        int ib = r.i1;
-        resolve_near_ties(s.q[st], s.qt, m, row, live && (r.v1 - r.v2 <= twoE), r.v1, twoE, ib);
-        if (live) route[(size_t)bh * N + n] = ib;
+        // append ambiguous queries (one reservation per warp)
+        const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
+        if (am) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(amb, __popc(am));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          if (ambiguous) amb[1 + base + __popc(am & ((1u << lane) - 1u))] = (int)((size_t)bh * N + n);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.q_empty[st]);
       }
@@ -310,6 +272,60 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   if (warp == 1) tmem_dealloc(tbase, tmem_cols);
 }
 
+// Exact routing of the ambiguous queries: one warp per query.  Lanes screen
+// all m landmarks with fp32 dots (only those within 2E of the fp32 best can
+// win), re-score the survivors with exact-product arithmetic and reduce
+// (score desc, index asc).
+__global__ void __launch_bounds__(256)
+route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde, int N, int m,
+                   const int* __restrict__ amb, int32_t* __restrict__ route) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * 8;
+  const int count = amb[0];
+  for (int w = blockIdx.x * 8 + (threadIdx.x >> 5); w < count; w += nwarps) {
+    const int qflat = amb[1 + w];
+    const int bh = qflat / N;
+    float qr[64];
+    load_row<bf16, 64>(q + (size_t)qflat * 64, qr);
+    float qn2 = 0.f, best = -INFINITY, qt2 = 0.f;
+#pragma unroll
+    for (int l = 0; l < 64; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
+    const bf16* qtb = q_tilde + (size_t)bh * m * 64;
+    for (int i = lane; i < m; i += 32) {
+      float r[64];
+      load_row<bf16, 64>(qtb + (size_t)i * 64, r);
+      float d = 0.f, n2 = 0.f;
+#pragma unroll
+      for (int l = 0; l < 64; ++l) { d = fmaf(qr[l], r[l], d); n2 = fmaf(r[l], r[l], n2); }
+      best = fmaxf(best, d);
+      qt2 = fmaxf(qt2, n2);
+    }
+    best = warp_max(best);
+    qt2 = warp_max(qt2);
+    const float twoE = 2.f * err_gamma(64) * sqrtf(qn2) * sqrtf(qt2);
+    F2 bv{-INFINITY, 0.f};
+    int bi = 0x7fffffff;
+    for (int i = lane; i < m; i += 32) {
+      float r[64];
+      load_row<bf16, 64>(qtb + (size_t)i * 64, r);
+      float d = 0.f;
+#pragma unroll
+      for (int l = 0; l < 64; ++l) d = fmaf(qr[l], r[l], d);
+      if (d >= best - twoE) {
+        const F2 x = dot_f2<64>(qr, r);
+        if (ranks_before(x, i, bv, bi)) { bv = x; bi = i; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const F2 ov{__shfl_xor_sync(0xffffffffu, bv.hi, o), __shfl_xor_sync(0xffffffffu, bv.lo, o)};
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) route[qflat] = bi;
+  }
+}
+
 }  // namespace
 
 size_t route_tc_smem_bytes() { return sizeof(RouteSmem) + 1024; }
@@ -317,7 +333,7 @@ size_t route_tc_smem_bytes() { return sizeof(RouteSmem) + 1024; }
 bool route_tc_supported(int d, int m) { return d == 64 && m >= 1 && m <= kMaxM; }
 
 cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, int m,
-                            int num_sms, int32_t* route, int* status, cudaStream_t st) {
+                            int num_sms, int32_t* route, int* amb, int* status, cudaStream_t st) {
   const int W = std::min(256, (m + 31) / 32 * 32);
   const int nch = (m + W - 1) / W;
   uint32_t cols = 32;
@@ -333,8 +349,12 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(amb, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
   route_tc_kernel<<<(unsigned)(BH * G_h), kThreads, smem, st>>>(mq, mqt, N, m, W, nch, G_h, cols,
-                                                                 route, status);
+                                                                 route, amb, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  route_fixup_kernel<<<std::max(num_sms, 1) * 4, 256, 0, st>>>(q, q_tilde, N, m, amb, route);
   return cudaGetLastError();
 }
 
