@@ -141,7 +141,7 @@ int mita_bucket(const int32_t* route_idx, int B, int H, int N, int m, int s,
  * compiled into the library (held by every GPU that loads it until exit), so
  * it calls no allocator at all.
  *   Same arguments and outputs as mita_bucket.
- *   Limit: B*H*ceil(N/4096)*m <= 1048576, else MITA_ERR_UNSUPPORTED and
+ *   Limit: B*H*(ceil(N/4096)+1)*m <= 1048576, else MITA_ERR_UNSUPPORTED and
  *   nothing runs.
  *   The array is shared by every call and keeps the last call's contents;
  *   each call clears what it uses first.  Calls that overlap on the GPU

@@ -280,7 +280,7 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
   if constexpr (std::is_same<T, bf16>::value) {
     if (so == nullptr && expert_tc_supported(d, m, topk)) {
       void* ws = nullptr;
-      MITA_TRY(workspace(expert_tc_ws_bytes(B * H, m), st, &ws));
+      MITA_TRY(workspace(expert_tc_ws_bytes(B * H, N, m, topk), st, &ws));
       MITA_CUDA(launch_expert_tc(q, k, v, qt, vt, ti, off, qidx, B * H, N, m, topk, ds->num_sms,
                                  ws, out, ds->status, st),
                 "expert launch");
@@ -310,7 +310,8 @@ ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, size_t esize
   L.qidx = o; o += align256((size_t)BH * N * 4);
   L.lm = o; o += align256(landmark_ws_bytes(L.plan, BH, N, d, m));
   L.bk = o; o += align256(bucket_ws_bytes(BH, N, m));
-  L.ex = o; o += align256(expert_tc_ws_bytes(BH, m));
+  L.ex = o;
+  if (esize == 2 && expert_tc_supported(d, m, topk)) o += align256(expert_tc_ws_bytes(BH, N, m, topk));
   L.rt = o; o += align256(route_ws_bytes(BH, N));
   L.total = o;
   return L;

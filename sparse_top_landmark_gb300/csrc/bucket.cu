@@ -8,13 +8,14 @@
 // kBucketChunk:
 //   count   -- one CTA per chunk: shared-memory histogram of its experts,
 //              written as hist[bh][e][chunk];
-//   scan    -- one CTA per head: per-expert totals, their exclusive prefix
-//              (bucket_off), and for every (expert, chunk) the chunk's first
-//              slot in that expert's bucket (one warp per expert);
-//   scatter -- one CTA per chunk, eight warps on consecutive sub-chunks: a
-//              per-expert prefix across the warps, then each warp places its
-//              queries in order (warp match + popcount ranks equal experts in
-//              a batch of 32), so every bucket lists its queries ascending.
+//   scan    -- one warp per (head, expert): the expert's total, and for every
+//              chunk the chunk's first slot relative to the expert's bucket;
+//   scatter -- one CTA per chunk: the exclusive prefix of the expert totals
+//              (bucket_off, written by the head's first chunk), then eight
+//              warps on consecutive sub-chunks: a per-expert prefix across the
+//              warps, then each warp places its queries in order (warp match +
+//              popcount ranks equal experts in a batch of 32), so every bucket
+//              lists its queries ascending.
 // Experts beyond kSmemExperts use the same passes with global counters.
 #include "common.cuh"
 #include "kernels.h"
@@ -64,62 +65,71 @@ bucket_count_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks
   }
 }
 
-__global__ void __launch_bounds__(1024)
-bucket_scan_kernel(int m, int nchunks, int* __restrict__ hist, int32_t* __restrict__ bucket_off) {
-  __shared__ int red[33];
-  __shared__ int carry_s;
-  const long long bh = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* hb = hist + (size_t)bh * m * nchunks;
-  int32_t* off = bucket_off + (size_t)bh * (m + 1);
-  // per-expert totals into bucket_off[e] (temporarily)
-  for (int e = warp; e < m; e += 32) {
-    int tot = 0;
-    for (int c = lane; c < nchunks; c += 32) tot += hb[(size_t)e * nchunks + c];
-    tot = warp_sum(tot);
-    if (lane == 0) off[e] = tot;
+__global__ void __launch_bounds__(256)
+bucket_scan_kernel(long long BHm, int nchunks, int* __restrict__ hist, int* __restrict__ total) {
+  const long long be = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);   // bh * m + e
+  const int lane = threadIdx.x & 31;
+  if (be >= BHm) return;
+  int* h = hist + (size_t)be * nchunks;
+  int run = 0;
+  for (int c0 = 0; c0 < nchunks; c0 += 32) {
+    const int c = c0 + lane;
+    const int x = c < nchunks ? h[c] : 0;
+    const int inc = warp_incl_scan(x);
+    if (c < nchunks) h[c] = run + inc - x;
+    run += __shfl_sync(0xffffffffu, inc, 31);
   }
-  __syncthreads();
+  if (lane == 0) total[be] = run;
+}
+
+// exclusive prefix of the head's expert totals into off[0..m] (shared or global)
+__device__ void expert_offsets(const int* __restrict__ tot, int m, int* off, int* red) {
+  __shared__ int carry_s;
   if (threadIdx.x == 0) carry_s = 0;
   __syncthreads();
-  for (int e0 = 0; e0 < m; e0 += 1024) {
+  for (int e0 = 0; e0 < m; e0 += 256) {
     const int e = e0 + threadIdx.x;
-    const int cnt = e < m ? off[e] : 0;
-    int tot;
-    const int ex = block_excl_scan(cnt, red, &tot);
+    const int cnt = e < m ? tot[e] : 0;
+    int t;
+    const int ex = block_excl_scan(cnt, red, &t);
     const int base = carry_s;
     __syncthreads();
     if (e < m) off[e] = base + ex;
-    if (threadIdx.x == 0) carry_s = base + tot;
+    if (threadIdx.x == 0) carry_s = base + t;
     __syncthreads();
   }
   if (threadIdx.x == 0) off[m] = carry_s;
   __syncthreads();
-  // each (expert, chunk): first slot of the chunk's queries in the expert's bucket
-  for (int e = warp; e < m; e += 32) {
-    int run = off[e];
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int x = c < nchunks ? hb[(size_t)e * nchunks + c] : 0;
-      const int inc = warp_incl_scan(x);
-      if (c < nchunks) hb[(size_t)e * nchunks + c] = run + inc - x;
-      run += __shfl_sync(0xffffffffu, inc, 31);
-    }
-  }
+}
+
+// many experts: one CTA per head writes bucket_off before the scatter
+__global__ void __launch_bounds__(256)
+bucket_offsets_kernel(const int* __restrict__ total, int m, int32_t* __restrict__ bucket_off) {
+  __shared__ int red[33];
+  const long long bh = blockIdx.x;
+  expert_offsets(total + (size_t)bh * m, m, bucket_off + (size_t)bh * (m + 1), red);
 }
 
 __global__ void __launch_bounds__(256)
 bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks,
-                      int* __restrict__ hist, int32_t* __restrict__ bucket_qidx, int* status) {
-  extern __shared__ int hw[];                    // [kWarps][m] when m <= kSmemExperts
+                      int* __restrict__ hist, const int* __restrict__ total,
+                      int32_t* __restrict__ bucket_off, int32_t* __restrict__ bucket_qidx,
+                      int* status) {
+  extern __shared__ int hw[];                    // [kWarps][m] + off[m + 1] when m <= kSmemExperts
+  __shared__ int red[33];
   const long long bh = blockIdx.x / nchunks;
   const int chunk = blockIdx.x % nchunks;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* hg = hist + (size_t)bh * m * nchunks;
+  int* hg = hist + (size_t)bh * m * nchunks;
   int32_t* out = bucket_qidx + (size_t)bh * N;
+  int32_t* boff = bucket_off + (size_t)bh * (m + 1);
   const int n0 = chunk * kBucketChunk + warp * kSub;
   const unsigned lt = (1u << lane) - 1u;
   if (m <= kSmemExperts) {
+    int* off = hw + kWarps * m;
+    expert_offsets(total + (size_t)bh * m, m, off, red);
+    if (chunk == 0)
+      for (int e = threadIdx.x; e <= m; e += 256) boff[e] = off[e];
     for (int i = threadIdx.x; i < kWarps * m; i += 256) hw[i] = 0;
     __syncthreads();
     // per-warp counts of its sub-chunk
@@ -132,7 +142,7 @@ bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchun
     __syncthreads();
     // exclusive prefix across the warps, starting at the chunk's slot
     for (int e = threadIdx.x; e < m; e += 256) {
-      int run = hg[(size_t)e * nchunks + chunk];
+      int run = off[e] + hg[(size_t)e * nchunks + chunk];
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const int t = hw[w * m + e];
@@ -158,20 +168,21 @@ bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchun
       __syncwarp();
     }
   } else if (warp == 0) {
-    // many experts: one warp walks the chunk in order with global counters
-    int* hgw = hist + (size_t)bh * m * nchunks;
+    // many experts (bucket_off written by bucket_offsets_kernel): one warp
+    // walks the chunk in order with global counters
+    int* hgw = hg;
     for (int it = 0; it < kBucketChunk; it += 32) {
       const int n = chunk * kBucketChunk + it + lane;
       const int e = load_route(route, bh, N, n, m, nullptr);
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       int base = 0;
-      if (e >= 0) base = hgw[(size_t)e * nchunks + chunk];
+      if (e >= 0) base = boff[e] + hgw[(size_t)e * nchunks + chunk];
       __syncwarp();
       if (e >= 0) {
         const int pos = base + __popc(peers & lt);
         if (pos >= 0 && pos < N) out[pos] = n;
         else flag_error(status, kDevErrBadBucket);
-        if (lane == __ffs(peers) - 1) hgw[(size_t)e * nchunks + chunk] = base + __popc(peers);
+        if (lane == __ffs(peers) - 1) hgw[(size_t)e * nchunks + chunk] = base - boff[e] + __popc(peers);
       }
       __syncwarp();
     }
@@ -182,19 +193,23 @@ bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchun
 
 size_t bucket_ws_bytes(int BH, int N, int m) {
   const size_t nchunks = (N + kBucketChunk - 1) / kBucketChunk;
-  return (size_t)BH * nchunks * m * sizeof(int);
+  return (size_t)BH * (nchunks + 1) * m * sizeof(int);
 }
 
 cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* ws,
                           int32_t* bucket_off, int32_t* bucket_qidx, int* status,
                           cudaStream_t st) {
   const int nchunks = (N + kBucketChunk - 1) / kBucketChunk;
-  int* hist = static_cast<int*>(ws);
-  cudaError_t e = cudaMemsetAsync(hist, 0, bucket_ws_bytes(BH, N, m), st);
-  if (e != cudaSuccess) return e;
-  const unsigned blocks = (unsigned)((long long)BH * nchunks);
+  int* hist = static_cast<int*>(ws);                       // [BH][m][nchunks]
+  int* total = hist + (size_t)BH * m * nchunks;             // [BH][m]
   const bool smem = m <= kSmemExperts;
-  const size_t s1 = smem ? (size_t)m * 4 : 0, s3 = smem ? (size_t)kWarps * m * 4 : 0;
+  cudaError_t e;
+  if (!smem) {
+    e = cudaMemsetAsync(hist, 0, (size_t)BH * m * nchunks * sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
+  const unsigned blocks = (unsigned)((long long)BH * nchunks);
+  const size_t s1 = smem ? (size_t)m * 4 : 0, s3 = smem ? ((size_t)kWarps * m + m + 1) * 4 : 0;
   if (s3 > 48 * 1024) {
     e = cudaFuncSetAttribute(bucket_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)s3);
@@ -202,10 +217,16 @@ cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* 
   }
   bucket_count_kernel<<<blocks, 256, s1, st>>>(route_idx, N, m, nchunks, hist, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bucket_scan_kernel<<<BH, 1024, 0, st>>>(m, nchunks, hist, bucket_off);
+  const long long BHm = (long long)BH * m;
+  bucket_scan_kernel<<<(unsigned)((BHm + kWarps - 1) / kWarps), 256, 0, st>>>(BHm, nchunks, hist,
+                                                                               total);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bucket_scatter_kernel<<<blocks, 256, s3, st>>>(route_idx, N, m, nchunks, hist, bucket_qidx,
-                                                 status);
+  if (!smem) {
+    bucket_offsets_kernel<<<BH, 256, 0, st>>>(total, m, bucket_off);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  bucket_scatter_kernel<<<blocks, 256, s3, st>>>(route_idx, N, m, nchunks, hist, total, bucket_off,
+                                                 bucket_qidx, status);
   return cudaGetLastError();
 }
 

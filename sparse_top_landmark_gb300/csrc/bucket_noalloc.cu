@@ -10,12 +10,12 @@
 //
 // Limits and sharing rules:
 //   * The array holds kNoAllocScratchInts int32 counters (4 MiB).  A call
-//     needs B*H*ceil(N/4096)*m of them; larger calls are rejected with
+//     needs B*H*(ceil(N/4096)+1)*m of them; larger calls are rejected with
 //     MITA_ERR_UNSUPPORTED before anything runs.
 //   * Every GPU that loads this library's module keeps the 4 MiB until the
 //     process exits.
 //   * All calls share the one array, and it keeps whatever the last call
-//     left there.  Each call clears the counters it uses before use.  Calls
+//     left there.  Each call writes every counter it uses before reading it.  Calls
 //     whose executions overlap on the GPU (different streams, no ordering
 //     between them) race on the array and give wrong results: order them.
 //   * The first call on a device looks up the array's device address
@@ -58,7 +58,7 @@ extern "C" int mita_bucket_noalloc(const int32_t* route_idx, int B, int H, int N
   const size_t need = bucket_ws_bytes(B * H, N, m);
   if (need > kNoAllocScratchInts * sizeof(int))
     return report_error(MITA_ERR_UNSUPPORTED,
-                        "mita_bucket_noalloc: B*H*ceil(N/4096)*m exceeds the 1048576 counters "
+                        "mita_bucket_noalloc: B*H*(ceil(N/4096)+1)*m exceeds the 1048576 counters "
                         "(4 MiB) of its static scratch; use mita_bucket");
 
   int dev = 0;

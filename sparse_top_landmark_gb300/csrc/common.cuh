@@ -153,6 +153,15 @@ __device__ __forceinline__ bool ranks_before(double sa, int ia, double sb, int i
   return sa > sb || (sa == sb && ia < ib);
 }
 
+// Monotone map float -> uint32 (larger float -> larger key) and back.
+__device__ __forceinline__ uint32_t fkey(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // Monotone map double -> uint64 (larger double -> larger key).
 __device__ __forceinline__ unsigned long long order_key(double x) {
   if (x == 0.0) x = 0.0;  // fold -0 onto +0
@@ -275,6 +284,50 @@ __device__ inline void bitonic_sort_int_asc(int* a, int P) {
     }
   }
   __syncthreads();
+}
+
+// The k-th largest of n floats in shared memory (1 <= k <= n), by a 4-pass
+// 8-bit radix select on the monotone keys.  Whole block; `hist` holds 256
+// ints, `sh` 4 ints.
+__device__ inline float block_kth_largest(const float* x, int n, int k, int* hist, int* sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0u, mask = 0u;
+  int need = k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int b = tid; b < 256; b += blockDim.x) hist[b] = 0;
+    __syncthreads();
+    for (int t = tid; t < n; t += blockDim.x) {
+      const uint32_t key = fkey(x[t]);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 248-8l (high to low)
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { cnt[j] = hist[255 - 8 * lane - j]; tot += cnt[j]; }
+      const int inc = warp_incl_scan(tot);
+      const unsigned hit = __ballot_sync(0xffffffffu, inc >= need);
+      const int src = __ffs(hit) - 1;
+      if (lane == src) {
+        int cum = inc - tot, dg = 255 - 8 * lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cum + cnt[j] >= need) { dg = 255 - 8 * lane - j; break; }
+          cum += cnt[j];
+        }
+        sh[0] = dg;
+        sh[1] = need - cum;
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sh[0] << shift;
+    mask |= 0xffu << shift;
+    need = sh[1];
+    __syncthreads();
+  }
+  return fkey_inv(prefix);
 }
 
 __host__ __device__ __forceinline__ int next_pow2(int x) {

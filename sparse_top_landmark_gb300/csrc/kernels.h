@@ -101,7 +101,7 @@ cudaError_t launch_route_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde
                             cudaStream_t st);
 
 bool expert_tc_supported(int d, int m, int topk);
-size_t expert_tc_ws_bytes(int BH, int m);
+size_t expert_tc_ws_bytes(int BH, int N, int m, int topk);
 cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                              const __nv_bfloat16* v, const __nv_bfloat16* q_tilde,
                              const float* v_tilde, const int32_t* topk_idx,

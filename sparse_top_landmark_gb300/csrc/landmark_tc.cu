@@ -385,8 +385,9 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, i
                     LandmarkWs ws, float* __restrict__ v_tilde) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* val = reinterpret_cast<float*>(smem_raw);   // [P]
-  int* idx = reinterpret_cast<int*>(val + P);         // [P]
   __shared__ float red[8];
+  __shared__ int hist[256];
+  __shared__ int sh[4];
   const long long rf = blockIdx.x;
   const long long bh = rf / m;
   const int tid = threadIdx.x;
@@ -408,11 +409,10 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, i
   // ---- tau_L
   const int n = S2 * kTopTiles;
   const float* tops = ws.bm + base * kTopTiles;
-  for (int t = tid; t < P; t += 256) {
-    val[t] = t < n ? tops[t] : -INFINITY;
-    idx[t] = t;
-  }
-  bitonic_sort_desc(val, idx, P);
+  for (int t = tid; t < n; t += 256) val[t] = tops[t];
+  __syncthreads();
+  // -inf when fewer than topk tile maxima exist
+  const float tauL = n >= topk ? block_kth_largest(val, n, topk, hist, sh) : -INFINITY;
   // ---- error bound
   float km = 0.f;
   for (int q = tid; q < S; q += 256) km = fmaxf(km, ws.kmax2[(size_t)bh * S + q]);
@@ -422,7 +422,6 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, i
   qn2 = block_sum(qn2, red);
   if (tid == 0) {
     const float E = err_gamma(64) * sqrtf(qn2) * sqrtf(km);
-    const float tauL = val[topk - 1];          // -inf when fewer than topk maxima exist
     ws.E[rf] = E;
     ws.thr[rf] = tauL - 4.f * E;
     ws.cnt[rf] = 0;
@@ -642,8 +641,8 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
   if (e != cudaSuccess) return e;
   lm_sweep_kernel<<<blocks, kThreads, sm1, st>>>(mqt, mk, mv, N, m, p.S, p.split_len, ws, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int P = next_pow2(2 * p.S * kTopTiles);
-  const size_t tsm = (size_t)P * 8;
+  const int P = 2 * p.S * kTopTiles;
+  const size_t tsm = (size_t)P * 4;
   e = cudaFuncSetAttribute(lm_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tsm);
   if (e != cudaSuccess) return e;

@@ -7,8 +7,9 @@
 // grid (1D: 1 x N pooled to 1 x m; 2D: pooled to sqrt(m) x sqrt(m)).
 //
 // HBM-bound: one CTA per landmark streams its window once with 16-byte loads.
-// Sums are error-free per thread (fp32 two-sum) and combined in fp64, so the
-// mean is rounded once into the input dtype -- the same value an fp64 mean
+// Sums are error-free (fp32 two-sum per thread and across threads; one fp64
+// division per output), so the mean is rounded once into the input dtype --
+// the same value an fp64 mean
 // rounded to nearest gives.
 #include "common.cuh"
 #include "kernels.h"
@@ -19,14 +20,15 @@ namespace {
 constexpr int kPoolThreads = 256;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPoolThreads)
+__global__ void __launch_bounds__(kPoolThreads, 4)
 pool_kernel(const T* __restrict__ q, int N, int grid_h, int grid_w, int mh, int mw,
             T* __restrict__ q_tilde) {
   constexpr int VEC = Vec<T>::N;
   constexpr int NV = D / VEC;              // 16-byte vectors per row
   constexpr int TL = kPoolThreads / NV;    // token lanes
+  constexpr int UNR = 8;                   // 16-byte loads in flight per thread
   static_assert(D % VEC == 0, "row must be a whole number of 16-byte vectors");
-  __shared__ double red[TL][D];
+  __shared__ float red_s[TL][D], red_c[TL][D];
 
   const int m = mh * mw;
   const long long flat = blockIdx.x;       // bh * m + i
@@ -37,41 +39,48 @@ pool_kernel(const T* __restrict__ q, int N, int grid_h, int grid_w, int mh, int 
   adaptive_window(i % mw, grid_w, mw, &c0, &c1);
   const int nc = c1 - c0;
   const int cnt = (r1 - r0) * nc;
+  const bool one_row = r1 - r0 == 1;       // 1D windows are contiguous
 
   const int vlane = threadIdx.x % NV, tl = threadIdx.x / NV;
   float s[VEC], c[VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) { s[e] = 0.f; c[e] = 0.f; }
   const T* base = q + (size_t)bh * N * D + vlane * VEC;
-  // UNR independent 16-byte loads in flight per thread (the window is read once)
-  constexpr int UNR = 4;
   for (int t0 = tl; t0 < cnt; t0 += TL * UNR) {
-    float x[UNR][VEC];
+    uint4 raw[UNR];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int t = t0 + u * TL;
       if (t < cnt) {
-        // 1D windows (grid_h == 1) are contiguous: no division
-        const size_t tok = (r1 - r0 == 1) ? (size_t)r0 * grid_w + c0 + t
-                                          : (size_t)(r0 + t / nc) * grid_w + c0 + t % nc;
-        Vec<T>::load(base + tok * D, x[u]);
+        const size_t tok = one_row ? (size_t)r0 * grid_w + c0 + t
+                                   : (size_t)(r0 + t / nc) * grid_w + c0 + t % nc;
+        raw[u] = *reinterpret_cast<const uint4*>(base + tok * D);
       } else {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) x[u][e] = 0.f;
+        raw[u] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
-    for (int u = 0; u < UNR; ++u)
+    for (int u = 0; u < UNR; ++u) {
+      float x[VEC];
+      Vec<T>::load(reinterpret_cast<const T*>(&raw[u]), x);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) two_sum_acc(s[e], c[e], x[u][e]);
+      for (int e = 0; e < VEC; ++e) two_sum_acc(s[e], c[e], x[e]);
+    }
   }
 #pragma unroll
-  for (int e = 0; e < VEC; ++e) red[tl][vlane * VEC + e] = (double)s[e] + (double)c[e];
+  for (int e = 0; e < VEC; ++e) {
+    red_s[tl][vlane * VEC + e] = s[e];
+    red_c[tl][vlane * VEC + e] = c[e];
+  }
   __syncthreads();
   for (int l = threadIdx.x; l < D; l += kPoolThreads) {
-    double acc = 0.0;
-    for (int t = 0; t < TL; ++t) acc += red[t][l];
-    q_tilde[flat * D + l] = round_double<T>(acc / (double)cnt);
+    // error-free combination of the token lanes, then one rounding
+    float S = 0.f, C = 0.f;
+    for (int t = 0; t < TL; ++t) {
+      two_sum_acc(S, C, red_s[t][l]);
+      C = __fadd_rn(C, red_c[t][l]);
+    }
+    q_tilde[flat * D + l] = round_double<T>(((double)S + (double)C) / (double)cnt);
   }
 }
 

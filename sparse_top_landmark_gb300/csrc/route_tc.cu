@@ -11,14 +11,14 @@
 //               W <= 256 landmarks, two chunk buffers (ping-pong);
 //   warps 4-11  epilogue: TMEM lane quadrant = warp % 4 (one query row per
 //               thread), two warps per quadrant split each chunk's columns.
-// Each score's 9 low mantissa bits are replaced by (511 - landmark index);
-// a branch-free running top-2 over these packed values gives the best index
-// directly.  The packing moves a score by at most 2^-14 of its magnitude, so
-// when the packed best beats the runner-up by more than 2E + 2^-12 |best|
-// (E bounds the fp32 dot error) the index is the exact argmax.  Otherwise the
-// query is appended to an "ambiguous" list and route_fixup_kernel re-routes it
-// exactly (fp32 screening + exact-product re-scoring, ties to the lowest
-// index) -- about 0.2% of the queries on the long-sequence workloads.
+// Each thread keeps the exact best and runner-up fp32 scores of its query
+// (branch-free min/max) and a register copy of the 32-score block holding the
+// running best, so the best's index (lowest on ties) is looked up once at the
+// end.  When the best beats the runner-up by more than 2E (E bounds the fp32
+// dot error) it is the exact argmax; otherwise the query goes on an
+// "ambiguous" list and route_fixup_kernel re-routes it exactly (fp32
+// screening + exact-product re-scoring, ties to the lowest index) -- about
+// 0.2% of the queries on the long-sequence workloads.
 #include <algorithm>
 
 #include "common.cuh"
@@ -35,7 +35,8 @@ constexpr int kThreads = (4 + kEpiWarps) * 32;
 constexpr int kMaxM = 512;
 
 struct Cand {
-  float v1, v2;   // best and runner-up packed scores
+  float v1, v2;   // best and runner-up scores
+  int i1;         // lowest index reaching v1
 };
 
 struct alignas(1024) RouteSmem {
@@ -73,22 +74,40 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
-// Score with its low 9 mantissa bits replaced by (511 - index).
-__device__ __forceinline__ float pack_idx(float x, int i) {
-  return __uint_as_float((__float_as_uint(x) & ~511u) | (uint32_t)(511 - i));
-}
-__device__ __forceinline__ int unpack_idx(float x) { return 511 - (int)(__float_as_uint(x) & 511u); }
-
-// Running top-2 of 32 packed scores (indices i0..i0+31, those >= nvalid skipped).
-__device__ __forceinline__ void top2_32(Cand& c, const float* v, int i0, int nvalid) {
+// Top-2 update over a block of 32 scores starting at index i0 (entries at or
+// past nvalid ignored); bb keeps a copy of the block that holds the best.
+__device__ __forceinline__ void top2_block(Cand& c, float* bb, int& bb0, const float* v, int i0,
+                                           int nvalid) {
+  const float before = c.v1;
+  if (nvalid >= 32) {
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const float a = (i < nvalid) ? pack_idx(v[i], i0 + i) : -INFINITY;
-    const float b = (i + 1 < nvalid) ? pack_idx(v[i + 1], i0 + i + 1) : -INFINITY;
-    const float hi = fmaxf(a, b), lo = fminf(a, b);
-    c.v2 = max3f(c.v2, lo, fminf(c.v1, hi));
-    c.v1 = fmaxf(c.v1, hi);
+    for (int i = 0; i < 32; i += 2) {
+      const float hi = fmaxf(v[i], v[i + 1]), lo = fminf(v[i], v[i + 1]);
+      c.v2 = max3f(c.v2, lo, fminf(c.v1, hi));
+      c.v1 = fmaxf(c.v1, hi);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float a = (i < nvalid) ? v[i] : -INFINITY;
+      const float b = (i + 1 < nvalid) ? v[i + 1] : -INFINITY;
+      const float hi = fmaxf(a, b), lo = fminf(a, b);
+      c.v2 = max3f(c.v2, lo, fminf(c.v1, hi));
+      c.v1 = fmaxf(c.v1, hi);
+    }
   }
+  const bool up = c.v1 > before;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) bb[i] = up ? v[i] : bb[i];
+  bb0 = up ? i0 : bb0;
+}
+
+// lowest index in the saved block whose score equals the best
+__device__ __forceinline__ int block_argmax(const float* bb, int bb0, float v1) {
+  int k = 31;
+#pragma unroll
+  for (int i = 31; i >= 0; --i) k = (bb[i] == v1) ? i : k;
+  return bb0 + k;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -201,34 +220,32 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     for (int it = 0; it < ntiles; ++it) {
       const int st = it % kQStages;
       if (ok && !mbar_wait(&s.q_full[st], (it / kQStages) & 1)) ok = false;
-      Cand c{-INFINITY, -INFINITY};
+      Cand c{-INFINITY, -INFINITY, 0x7fffffff};
+      float bb[32];
+      int bb0 = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) bb[i] = -INFINITY;
       for (int ch = 0; ch < nch; ++ch, ++gch) {
         const int b = gch & 1;
         if (ok && !mbar_wait(&s.s_full[b], (gch >> 1) & 1)) ok = false;
         tc_fence_after();
         if (ok) {
           const int col0 = half * cols_half;
-          for (int cc = 0; cc < cols_half; cc += 64) {
-            float v[64];
+          for (int cc = 0; cc < cols_half; cc += 32) {
+            float v[32];
             const uint32_t ta = tbase + taddr_lane + (uint32_t)(b * W + col0 + cc);
-            if (cols_half - cc >= 64) {
-              tmem_ld32(ta, v);
-              tmem_ld32(ta + 32, v + 32);
-            } else {
-              tmem_ld16(ta, v);          // cols_half is a multiple of 16
-              if (cols_half - cc > 16) tmem_ld16(ta + 16, v + 16);
-            }
+            tmem_ld16(ta, v);                 // cols_half is a multiple of 16
+            if (cols_half - cc > 16) tmem_ld16(ta + 16, v + 16);
             tmem_ld_wait();
             const int i0 = ch * W + col0 + cc;
-            const int lim = min(m - i0, cols_half - cc);
-            top2_32(c, v, i0, lim);
-            if (lim > 32) top2_32(c, v + 32, i0 + 32, lim - 32);
+            top2_block(c, bb, bb0, v, i0, min(m - i0, cols_half - cc));
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.s_empty[b]);
       }
+      if (c.v1 > -INFINITY) c.i1 = block_argmax(bb, bb0, c.v1);
       if (half == 1) {
         s.cand[it & 1][row] = c;
         __syncwarp();
@@ -237,7 +254,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       epi_bar();
       if (half == 0) {
         const Cand o = s.cand[it & 1][row];
-        const float v1 = fmaxf(c.v1, o.v1);
+        const bool w1 = o.v1 > c.v1 || (o.v1 == c.v1 && o.i1 < c.i1);
+        const float v1 = w1 ? o.v1 : c.v1;
+        const int i1 = w1 ? o.i1 : c.i1;
         const float v2 = max3f(c.v2, o.v2, fminf(c.v1, o.v1));
         const int n = (c0 + it * G_h) * 128 + row;
         const bool live = ok && n < N;
@@ -249,8 +268,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
           for (int l = 0; l < 64; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
           const float twoE = 2.f * gam * sqrtf(qn2) * sqrtf(qtmax2);
-          ambiguous = !(v1 - v2 > twoE + fabsf(v1) * 2.44140625e-4f);   // 2^-12
-          route[(size_t)bh * N + n] = unpack_idx(v1);
+          ambiguous = !(v1 - v2 > twoE);
+          route[(size_t)bh * N + n] = i1;
         }
         // append ambiguous queries (one reservation per warp)
         const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
