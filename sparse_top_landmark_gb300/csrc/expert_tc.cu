@@ -19,14 +19,16 @@
 //                then the entries in chunks of 128 -- the expert's gathered
 //                K / V block first, then the q~ / v~ blocks -- as tiled loads
 //                into a 4-stage ring shared by the two query tiles;
-//     warp 1     MMA: S = Q . B^T per tile into tensor memory; O += P . V with
-//                P read from tensor memory (shared chunks as fp16 x fp16, v~
-//                kept in fp16; raw chunks bf16 x bf16).  Three S buffers
-//                rotate over the sequence (chunk, tile), P overwriting its own
-//                S, so the next score tile is computed while both softmax
-//                groups are busy;
-//     warps 2-5 / 6-9    online softmax of query tile 0 / 1 (one query row per
-//                thread, lazy O rescaling), then O / l to the output rows.
+//     warps 1-2  MMA, one issuing thread per query tile (one thread issues a
+//                tcgen05.mma only every ~130 cycles, so the two tiles get an
+//                issuer each): S = Q . B^T into the tile's S columns, and as
+//                soon as the softmax has copied S out, the next chunk's S;
+//                then O += P . V with P read from tensor memory (shared chunks
+//                as fp16 x fp16, v~ kept in fp16; raw chunks bf16 x bf16);
+//     warps 4-7 / 8-11   online softmax of query tile 0 / 1 (one query row per
+//                thread, lazy O rescaling; the exponentials of a chunk are
+//                computed before waiting for the previous P . V), then O / l
+//                to the output rows.
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -41,8 +43,7 @@ using namespace sm100;
 
 constexpr int BN = 128;          // entries per chunk
 constexpr int kStages = 4;
-constexpr int kThreads = 320;   // 10 warps: producer, MMA, 8 softmax
-constexpr int kSBuf = 3;         // S / P buffers in tensor memory, shared by the two tiles
+constexpr int kThreads = 384;   // producer, two MMA issuers, one spare, 8 softmax warps
 constexpr int kUnitQ = 256;      // queries per work unit (two MMA tiles)
 constexpr float kLazy = 8.0f;
 constexpr int kGatherThreads = 256;
@@ -53,8 +54,8 @@ struct alignas(1024) ExpertSmem {
   bf16 vb[kStages][BN * 64];       // v~ block (fp16) or the expert's V rows
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t q_full[2], q_empty[2];
-  uint64_t s_full[3], p_full[3], pv_done[2];
-  uint64_t drain;
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t drain[2];               // one per MMA issuer
   uint32_t tmem;
 };
 
@@ -203,18 +204,18 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.kv_full[i], 1);
-      mbar_init(&s.kv_empty[i], 1);
+      mbar_init(&s.kv_empty[i], 2);     // both tiles' P . V
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.q_full[i], 1);
-      mbar_init(&s.q_empty[i], 1);
+      mbar_init(&s.q_empty[i], 2);      // both tiles' last S
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_free[i], 4);
+      mbar_init(&s.p_full[i], 4);
       mbar_init(&s.pv_done[i], 1);
     }
-    for (int i = 0; i < kSBuf; ++i) {
-      mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 4);
-    }
-    mbar_init(&s.drain, 1);
+    mbar_init(&s.drain[0], 1);
+    mbar_init(&s.drain[1], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -225,223 +226,146 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem;
-  // tensor memory: three S buffers at 0 / 128 / 256 (P written over the first half of its S),
-  // O of query tile t at 384 + 64*t.  Tile sequence j = 2*chunk + query tile, buffer j % 3.
+  // tensor memory, query tile t at 256*t: S (128 columns), P (64, bf16 / fp16 pairs), O (64)
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    bool ok = true;
-    if (lane == 0) {
-      prefetch_tmap(&map_qg);
-      prefetch_tmap(&map_kg);
-      prefetch_tmap(&map_vg);
-      prefetch_tmap(&map_qt);
-      prefetch_tmap(&map_vt);
-    }
-    int gi = 0;
-    int4 nxt = units > 0 ? unit_tab[ubase] : make_int4(0, 0, 0, 0);
-    for (int it = 0; it < units && ok; ++it) {
-      const int4 cur = nxt;
-      if (it + 1 < units) nxt = unit_tab[ubase + it + 1];
-      const int idx = cur.x, bh = idx / m, qbase = cur.y, qcnt = cur.z;
-      const int qb = it & 1;
-      // ---- the unit's query rows (two tiles): lane l owns rows 8l .. 8l+7
-      int rows[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = 8 * lane + j;
-        rows[j] = null_row;
-        if (r < qcnt) {
-          const int qi = bucket_qidx[(size_t)bh * N + qbase + r];
-          if (qi >= 0 && qi < N) rows[j] = bh * N + qi;
-          else flag_error(status, kDevErrBadBucket);
-        }
+  // registers: the launch grants 384 x 168; warps 0-3 keep 56 each, the two softmax
+  // warpgroups take 224 each (128*56 + 2*128*224 = 384*168), via setmaxnreg in each role
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      bool ok = true;
+      if (lane == 0) {
+        prefetch_tmap(&map_qg);
+        prefetch_tmap(&map_kg);
+        prefetch_tmap(&map_vg);
+        prefetch_tmap(&map_qt);
+        prefetch_tmap(&map_vt);
       }
-      if (lane == 0 && !mbar_wait(&s.q_empty[qb], ((it >> 1) & 1) ^ 1)) ok = false;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) mbar_expect_tx(&s.q_full[qb], 2 * 128 * 128);
-      __syncwarp();
-      {
-        const int r = 8 * lane;
-        bf16* dst = &s.q[qb][r >> 7][(r & 127) * 64];
-        tma_gather4(dst, &map_qg, &s.q_full[qb], 0, rows[0], rows[1], rows[2], rows[3]);
-        tma_gather4(dst + 4 * 64, &map_qg, &s.q_full[qb], 0, rows[4], rows[5], rows[6], rows[7]);
-      }
-      // ---- the entries: the expert's gathered rows, then the shared blocks
-      for (int c = 0; c < nc; ++c, ++gi) {
-        const int st = gi % kStages;
-        if (lane == 0) {
-          if (!mbar_wait(&s.kv_empty[st], ((gi / kStages) & 1) ^ 1)) {
-            ok = false;
-          } else {
-            mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
-            if (c < nrc) {
-              tma_load_3d(s.kb[st], &map_kg, &s.kv_full[st], 0, c * BN, idx);
-              tma_load_3d(s.vb[st], &map_vg, &s.kv_full[st], 0, c * BN, idx);
-            } else {
-              tma_load_3d(s.kb[st], &map_qt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
-              tma_load_3d(s.vb[st], &map_vt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
-            }
+      int gi = 0;
+      int4 nxt = units > 0 ? unit_tab[ubase] : make_int4(0, 0, 0, 0);
+      for (int it = 0; it < units && ok; ++it) {
+        const int4 cur = nxt;
+        if (it + 1 < units) nxt = unit_tab[ubase + it + 1];
+        const int idx = cur.x, bh = idx / m, qbase = cur.y, qcnt = cur.z;
+        const int qb = it & 1;
+        // ---- the unit's query rows (two tiles): lane l owns rows 8l .. 8l+7
+        int rows[8];
+  #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = 8 * lane + j;
+          rows[j] = null_row;
+          if (r < qcnt) {
+            const int qi = bucket_qidx[(size_t)bh * N + qbase + r];
+            if (qi >= 0 && qi < N) rows[j] = bh * N + qi;
+            else flag_error(status, kDevErrBadBucket);
           }
         }
+        if (lane == 0 && !mbar_wait(&s.q_empty[qb], ((it >> 1) & 1) ^ 1)) ok = false;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        if (lane == 0) mbar_expect_tx(&s.q_full[qb], 2 * 128 * 128);
+        __syncwarp();
+        {
+          const int r = 8 * lane;
+          bf16* dst = &s.q[qb][r >> 7][(r & 127) * 64];
+          tma_gather4(dst, &map_qg, &s.q_full[qb], 0, rows[0], rows[1], rows[2], rows[3]);
+          tma_gather4(dst + 4 * 64, &map_qg, &s.q_full[qb], 0, rows[4], rows[5], rows[6], rows[7]);
+        }
+        // ---- the entries: the expert's gathered rows, then the shared blocks
+        for (int c = 0; c < nc; ++c, ++gi) {
+          const int st = gi % kStages;
+          if (lane == 0) {
+            if (!mbar_wait(&s.kv_empty[st], ((gi / kStages) & 1) ^ 1)) {
+              ok = false;
+            } else {
+              mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
+              if (c < nrc) {
+                tma_load_3d(s.kb[st], &map_kg, &s.kv_full[st], 0, c * BN, idx);
+                tma_load_3d(s.vb[st], &map_vg, &s.kv_full[st], 0, c * BN, idx);
+              } else {
+                tma_load_3d(s.kb[st], &map_qt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
+                tma_load_3d(s.vb[st], &map_vt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
+              }
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
       }
-    }
-    if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = idesc_f16(128, BN, false);
-      const uint32_t id_pv_raw = idesc_f16(128, 64, true, false);
-      const uint32_t id_pv_sh = idesc_f16(128, 64, true, true);
-      const int T = 2 * G;
-      bool ok = true;
-      // S(j) = Q_tile . B(chunk)^T into buffer j % 3
-      auto issue_s = [&](int j) -> bool {
-        const int g = j >> 1, slot = j & 1;
-        const int it = g / nc, c = g % nc, qb = it & 1, st = g % kStages;
-        if (slot == 0) {
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
+    } else if (warp == 1 || warp == 2) {
+      // ------------------------------------------------------------ MMA issuer of one tile
+      const int slot = warp - 1;
+      if (lane == 0) {
+        const uint32_t id_s = idesc_f16(128, BN, false);
+        const uint32_t id_pv_raw = idesc_f16(128, 64, true, false);
+        const uint32_t id_pv_sh = idesc_f16(128, 64, true, true);
+        const uint32_t tS = tbase + slot * 256, tP = tS + 128, tO = tS + 192;
+        bool ok = true;
+        // S(g) = Q_slot . B(g)^T
+        auto issue_s = [&](int g) -> bool {
+          const int it = g / nc, c = g % nc, qb = it & 1, st = g % kStages;
           if (c == 0 && !mbar_wait(&s.q_full[qb], (it >> 1) & 1)) return false;
           if (!mbar_wait(&s.kv_full[st], (g / kStages) & 1)) return false;
+          tc_fence_after();
+  #pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = smem_desc_sw128(smem_u32(s.q[qb][slot]) + kk * 32, 1024);
+            const uint64_t db = smem_desc_sw128(smem_u32(s.kb[st]) + kk * 32, 1024);
+            mma_ss(tS, da, db, id_s, kk > 0);
+          }
+          mma_commit(&s.s_full[slot]);
+          if (c == nc - 1) mma_commit(&s.q_empty[qb]);
+          return true;
+        };
+        if (G > 0) ok = issue_s(0);
+        for (int g = 0; g < G && ok; ++g) {
+          const int c = g % nc, st = g % kStages;
+          if (g + 1 < G) {
+            if (!mbar_wait(&s.s_free[slot], g & 1)) { ok = false; break; }
+            if (!issue_s(g + 1)) { ok = false; break; }
+          }
+          if (!mbar_wait(&s.p_full[slot], g & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t id_pv = c < nrc ? id_pv_raw : id_pv_sh;
+  #pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t dv = smem_desc_sw128(smem_u32(s.vb[st]) + kk * 2048, 1024);
+            mma_ts(tO, tP + kk * 8, dv, id_pv, c > 0 || kk > 0);
+          }
+          mma_commit(&s.pv_done[slot]);
+          mma_commit(&s.kv_empty[st]);
         }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t da = smem_desc_sw128(smem_u32(s.q[qb][slot]) + kk * 32, 1024);
-          const uint64_t db = smem_desc_sw128(smem_u32(s.kb[st]) + kk * 32, 1024);
-          mma_ss(tbase + (j % kSBuf) * 128, da, db, id_s, kk > 0);
-        }
-        mma_commit(&s.s_full[j % kSBuf]);
-        if (slot == 1 && c == nc - 1) mma_commit(&s.q_empty[qb]);
-        return true;
-      };
-      for (int j = 0; j < kSBuf && j < T && ok; ++j) ok = issue_s(j);
-      for (int j = 0; j < T && ok; ++j) {
-        const int g = j >> 1, slot = j & 1, c = g % nc, st = g % kStages, b = j % kSBuf;
-        if (!mbar_wait(&s.p_full[b], (j / kSBuf) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t id_pv = c < nrc ? id_pv_raw : id_pv_sh;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t dv = smem_desc_sw128(smem_u32(s.vb[st]) + kk * 2048, 1024);
-          mma_ts(tbase + 384 + slot * 64, tbase + b * 128 + kk * 8, dv, id_pv, c > 0 || kk > 0);
-        }
-        mma_commit(&s.pv_done[slot]);
-        if (slot == 1) mma_commit(&s.kv_empty[st]);
-        // the buffer is rewritten only after this product has read P (in-order pipe)
-        if (j + kSBuf < T) ok = issue_s(j + kSBuf);
+        mma_commit(&s.drain[slot]);
+        if (!mbar_wait(&s.drain[slot], 0)) ok = false;
+        if (!ok) flag_error(status, kDevErrTimeout);
       }
-      if (!ok) flag_error(status, kDevErrTimeout);
-      mma_commit(&s.drain);
-      mbar_wait(&s.drain, 0);
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
     // ------------------------------------------------------------ softmax
-    const int slot = (warp - 2) >> 2;
+    const int slot = (warp - 4) >> 2;
     const int quad = warp & 3;             // tensor-memory lanes this warp may access
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tO = tbase + lane_off + 384 + slot * 64;
+    const uint32_t tS = tbase + lane_off + slot * 256, tP = tS + 128, tO = tS + 192;
     const float cs = 0.18033688011112042f;   // log2(e) / sqrt(64)
     bool ok = true;
-    int g = 0;
-    for (int it = 0; it < units; ++it) {
-      const int4 cur = unit_tab[ubase + it];
-      const int bh = cur.x / m;
-      const int qr = slot * 128 + row;
-      int qi = -1;
-      if (qr < cur.z) {
-        qi = bucket_qidx[(size_t)bh * N + cur.y + qr];
-        if (qi < 0 || qi >= N) qi = -1;
-      }
-      float mref = -INFINITY, lsum = 0.f;
-      for (int c = 0; c < nc; ++c, ++g) {
-        const int j = 2 * g + slot;
-        const uint32_t tS = tbase + lane_off + (j % kSBuf) * 128;
-        if (ok && !mbar_wait(&s.s_full[j % kSBuf], (j / kSBuf) & 1)) ok = false;
-        tc_fence_after();
-        const int nvalid = c < nrc ? min(BN, topk - c * BN) : min(BN, m - (c - nrc) * BN);
-        const bool full = nvalid == BN;
-        float tm = -INFINITY;
-        if (ok) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[64];
-            tmem_ld32(tS + h * 64, v);
-            tmem_ld32(tS + h * 64 + 32, v + 32);
-            tmem_ld_wait();
-            if (!full) {
-#pragma unroll
-              for (int i = 0; i < 64; ++i) v[i] = (h * 64 + i < nvalid) ? v[i] : -INFINITY;
-            }
-#pragma unroll
-            for (int i = 0; i < 64; i += 2) tm = max3(tm, v[i], v[i + 1]);
-          }
-        }
-        const float xm = tm * cs;
-        if (c > 0 && ok && !mbar_wait(&s.pv_done[slot], (g - 1) & 1)) ok = false;
-        tc_fence_after();
-        const bool need = (c == 0) || (xm > mref + kLazy);
-        if (c > 0 && __any_sync(0xffffffffu, need)) {
-          const float f = need ? ex2(mref - xm) : 1.f;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float o[32];
-            tmem_ld32(tO + h * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= f;
-            tmem_st16(tO + h * 32, reinterpret_cast<uint32_t*>(o));
-            tmem_st16(tO + h * 32 + 16, reinterpret_cast<uint32_t*>(o + 16));
-          }
-          tmem_st_wait();
-        }
-        if (need) {
-          if (c > 0) lsum *= ex2(mref - xm);
-          mref = xm;
-        }
-        const bool fp16 = c >= nrc;
-        const float nm = -mref;
-        float ls = 0.f;
-        if (ok) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[64];
-            tmem_ld32(tS + h * 64, v);
-            tmem_ld32(tS + h * 64 + 32, v + 32);
-            tmem_ld_wait();
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-              float p0 = ex2(fmaf(v[i], cs, nm)), p1 = ex2(fmaf(v[i + 1], cs, nm));
-              if (!full) {
-                p0 = (h * 64 + i < nvalid) ? p0 : 0.f;
-                p1 = (h * 64 + i + 1 < nvalid) ? p1 : 0.f;
-              }
-              ls += p0 + p1;
-              pk[i / 2] = pack_pair(p0, p1, fp16);
-            }
-            // P columns h*32 .. h*32+31 lie below the S columns already read
-            tmem_st16(tS + h * 32, pk);
-            tmem_st16(tS + h * 32 + 16, pk + 16);
-          }
-        }
-        lsum += ls;
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.p_full[j % kSBuf]);
-      }
-      // ---- output row: O / l
-      if (ok && !mbar_wait(&s.pv_done[slot], (g - 1) & 1)) ok = false;
-      tc_fence_after();
+    const int qr = slot * 128 + row;
+    // query id of this thread's row in unit u (-1: padding row)
+    auto row_query = [&](const int4& u) -> int {
+      if (qr >= u.z) return -1;
+      const int qi = bucket_qidx[(size_t)(u.x / m) * N + u.y + qr];
+      return (qi >= 0 && qi < N) ? qi : -1;
+    };
+    // O / l of the finished unit to its query's output row
+    auto write_row = [&](int bh, int qi, float lsum) {
       float o[64];
       tmem_ld32(tO, o);
       tmem_ld32(tO + 32, o + 32);
       tmem_ld_wait();
-      tc_fence_before();
       if (ok && qi >= 0) {
         const float inv = 1.f / lsum;
         uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)bh * N + qi) * 64);
@@ -455,7 +379,109 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
           dst[i] = w;
         }
       }
+    };
+    int4 cur = units > 0 ? unit_tab[ubase] : make_int4(0, 0, 0, 0);
+    int4 nxt = units > 1 ? unit_tab[ubase + 1] : cur;
+    int qi = units > 0 ? row_query(cur) : -1;
+    int it = 0, c = 0;
+    int prev_bh = 0, prev_qi = -1;
+    float prev_lsum = 1.f;
+    bool pending = false;          // a finished unit's O still waits in tensor memory
+    float mref = -INFINITY, lsum = 0.f;
+    for (int g = 0; g < G; ++g, ++c) {
+      if (c == nc) {
+        // next unit; the finished one is written out inside this chunk, once its
+        // last P . V is done
+        prev_bh = cur.x / m;
+        prev_qi = qi;
+        prev_lsum = lsum;
+        pending = true;
+        ++it;
+        c = 0;
+        cur = nxt;
+        if (it + 1 < units) nxt = unit_tab[ubase + it + 1];
+        qi = row_query(cur);
+        mref = -INFINITY;
+        lsum = 0.f;
+      }
+      if (ok && !mbar_wait(&s.s_full[slot], g & 1)) ok = false;
+      tc_fence_after();
+      const int nvalid = c < nrc ? min(BN, topk - c * BN) : min(BN, m - (c - nrc) * BN);
+      float v[BN];
+      if (ok) {
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tS + cc * 32, v + cc * 32);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.s_free[slot]);   // the next S may overwrite these columns
+      if (nvalid < BN) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
+      }
+      float tm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BN; i += 2) tm = max3(tm, v[i], v[i + 1]);
+      const float xm = tm * cs;
+      const bool need = (c == 0) || (xm > mref + kLazy);
+      const float f = (c > 0 && need) ? ex2(mref - xm) : 1.f;
+      if (need) {
+        lsum *= f;
+        mref = xm;
+      }
+      const bool fp16 = c >= nrc;
+      const float nm = -mref;
+      float ls = 0.f;
+      // first half of P while the previous P . V may still run
+      uint32_t pk0[BN / 4];
+#pragma unroll
+      for (int i = 0; i < BN / 2; i += 2) {
+        const float p0 = ex2(fmaf(v[i], cs, nm)), p1 = ex2(fmaf(v[i + 1], cs, nm));
+        ls += p0 + p1;
+        pk0[i / 2] = pack_pair(p0, p1, fp16);
+      }
+      // the previous P . V must have read P and finished with O
+      if (g > 0 && ok && !mbar_wait(&s.pv_done[slot], (g - 1) & 1)) ok = false;
+      tc_fence_after();
+      tmem_st16(tP, pk0);
+      tmem_st16(tP + 16, pk0 + 16);
+      if (pending) {
+        write_row(prev_bh, prev_qi, prev_lsum);
+        pending = false;
+      }
+      uint32_t pk1[BN / 4];
+#pragma unroll
+      for (int i = 0; i < BN / 2; i += 2) {
+        const float p0 = ex2(fmaf(v[BN / 2 + i], cs, nm)), p1 = ex2(fmaf(v[BN / 2 + i + 1], cs, nm));
+        ls += p0 + p1;
+        pk1[i / 2] = pack_pair(p0, p1, fp16);
+      }
+      tmem_st16(tP + 32, pk1);
+      tmem_st16(tP + 48, pk1 + 16);
+      lsum += ls;
+      if (c > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float o[16];
+          tmem_ld16(tO + h * 16, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] *= f;
+          tmem_st16(tO + h * 16, reinterpret_cast<uint32_t*>(o));
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.p_full[slot]);
     }
+    if (G > 0) {
+      if (ok && !mbar_wait(&s.pv_done[slot], (G - 1) & 1)) ok = false;
+      tc_fence_after();
+      write_row(cur.x / m, qi, lsum);
+    }
+    tc_fence_before();
     if (!ok) flag_error(status, kDevErrTimeout);
   }
   tc_fence_before();

@@ -199,9 +199,9 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
         mma_commit(&s.pv_done[slot]);
         if (j + 2 < ntl) ok = issue_s(j + 2);
       }
-      if (!ok) flag_error(status, kDevErrTimeout);
       mma_commit(&s.drain);
-      mbar_wait(&s.drain, 0);
+      if (!mbar_wait(&s.drain, 0)) ok = false;
+      if (!ok) flag_error(status, kDevErrTimeout);
     }
   } else if (warp == 2 || warp == 3) {
     // largest |k| element of the split (bounds every key norm by 8 max|k|);
@@ -520,9 +520,9 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
         mma_commit(&s.s_full[slot]);
         mma_commit(&s.k_empty[st]);
       }
-      if (!ok) flag_error(status, kDevErrTimeout);
       mma_commit(&s.drain);
-      mbar_wait(&s.drain, 0);
+      if (!mbar_wait(&s.drain, 0)) ok = false;
+      if (!ok) flag_error(status, kDevErrTimeout);
     }
   } else if (warp >= 4) {
     const int slot = (warp - 4) >> 2;

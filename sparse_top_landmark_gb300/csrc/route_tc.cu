@@ -186,9 +186,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         mma_commit(&s.q_empty[st]);
       }
-      if (!ok) flag_error(status, kDevErrTimeout);
       mma_commit(&s.drain);
-      mbar_wait(&s.drain, 0);
+      if (!mbar_wait(&s.drain, 0)) ok = false;
+      if (!ok) flag_error(status, kDevErrTimeout);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
