@@ -252,7 +252,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         const int qb = it & 1;
         // ---- the unit's query rows (two tiles): lane l owns rows 8l .. 8l+7
         int rows[8];
-  #pragma unroll
+#pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int r = 8 * lane + j;
           rows[j] = null_row;
@@ -262,9 +262,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
             else flag_error(status, kDevErrBadBucket);
           }
         }
-        if (lane == 0 && !mbar_wait(&s.q_empty[qb], ((it >> 1) & 1) ^ 1)) ok = false;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        if (!mbar_wait_warp(&s.q_empty[qb], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
         if (lane == 0) mbar_expect_tx(&s.q_full[qb], 2 * 128 * 128);
         __syncwarp();
         {
@@ -276,72 +274,73 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         // ---- the entries: the expert's gathered rows, then the shared blocks
         for (int c = 0; c < nc; ++c, ++gi) {
           const int st = gi % kStages;
-          if (lane == 0) {
-            if (!mbar_wait(&s.kv_empty[st], ((gi / kStages) & 1) ^ 1)) {
-              ok = false;
+          if (!mbar_wait_warp(&s.kv_empty[st], ((gi / kStages) & 1) ^ 1)) { ok = false; break; }
+          if (elect_one()) {
+            mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
+            if (c < nrc) {
+              tma_load_3d(s.kb[st], &map_kg, &s.kv_full[st], 0, c * BN, idx);
+              tma_load_3d(s.vb[st], &map_vg, &s.kv_full[st], 0, c * BN, idx);
             } else {
-              mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
-              if (c < nrc) {
-                tma_load_3d(s.kb[st], &map_kg, &s.kv_full[st], 0, c * BN, idx);
-                tma_load_3d(s.vb[st], &map_vg, &s.kv_full[st], 0, c * BN, idx);
-              } else {
-                tma_load_3d(s.kb[st], &map_qt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
-                tma_load_3d(s.vb[st], &map_vt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
-              }
+              tma_load_3d(s.kb[st], &map_qt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
+              tma_load_3d(s.vb[st], &map_vt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
             }
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
+          __syncwarp();
         }
       }
       if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     } else if (warp == 1 || warp == 2) {
-      // ------------------------------------------------------------ MMA issuer of one tile
+      // ---------------------------------------------------------- MMA issuer of one tile
+      // the whole warp walks the schedule (waits without loops on the fast path);
+      // one elected lane issues each batch of MMAs and its commits
       const int slot = warp - 1;
-      if (lane == 0) {
-        const uint32_t id_s = idesc_f16(128, BN, false);
-        const uint32_t id_pv_raw = idesc_f16(128, 64, true, false);
-        const uint32_t id_pv_sh = idesc_f16(128, 64, true, true);
-        const uint32_t tS = tbase + slot * 256, tP = tS + 128, tO = tS + 192;
-        bool ok = true;
-        // S(g) = Q_slot . B(g)^T
-        auto issue_s = [&](int g) -> bool {
-          const int it = g / nc, c = g % nc, qb = it & 1, st = g % kStages;
-          if (c == 0 && !mbar_wait(&s.q_full[qb], (it >> 1) & 1)) return false;
-          if (!mbar_wait(&s.kv_full[st], (g / kStages) & 1)) return false;
-          tc_fence_after();
-  #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da = smem_desc_sw128(smem_u32(s.q[qb][slot]) + kk * 32, 1024);
-            const uint64_t db = smem_desc_sw128(smem_u32(s.kb[st]) + kk * 32, 1024);
-            mma_ss(tS, da, db, id_s, kk > 0);
-          }
+      const uint32_t id_s = idesc_f16(128, BN, false);
+      const uint32_t id_pv_raw = idesc_f16(128, 64, true, false);
+      const uint32_t id_pv_sh = idesc_f16(128, 64, true, true);
+      const uint32_t tS = tbase + slot * 256, tP = tS + 128, tO = tS + 192;
+      bool ok = true;
+      // S(g) = Q_slot . B(g)^T
+      auto issue_s = [&](int g) -> bool {
+        const int it = g / nc, c = g % nc, qb = it & 1, st = g % kStages;
+        if (c == 0 && !mbar_wait_warp(&s.q_full[qb], (it >> 1) & 1)) return false;
+        if (!mbar_wait_warp(&s.kv_full[st], (g / kStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(s.q[qb][slot]), kb = smem_u32(s.kb[st]);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tS, smem_desc_sw128(qa + kk * 32, 1024), smem_desc_sw128(kb + kk * 32, 1024),
+                   id_s, kk > 0);
           mma_commit(&s.s_full[slot]);
           if (c == nc - 1) mma_commit(&s.q_empty[qb]);
-          return true;
-        };
-        if (G > 0) ok = issue_s(0);
-        for (int g = 0; g < G && ok; ++g) {
-          const int c = g % nc, st = g % kStages;
-          if (g + 1 < G) {
-            if (!mbar_wait(&s.s_free[slot], g & 1)) { ok = false; break; }
-            if (!issue_s(g + 1)) { ok = false; break; }
-          }
-          if (!mbar_wait(&s.p_full[slot], g & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t id_pv = c < nrc ? id_pv_raw : id_pv_sh;
-  #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t dv = smem_desc_sw128(smem_u32(s.vb[st]) + kk * 2048, 1024);
-            mma_ts(tO, tP + kk * 8, dv, id_pv, c > 0 || kk > 0);
-          }
+        }
+        __syncwarp();
+        return true;
+      };
+      if (G > 0) ok = issue_s(0);
+      for (int g = 0; g < G && ok; ++g) {
+        const int c = g % nc, st = g % kStages;
+        if (g + 1 < G) {
+          if (!mbar_wait_warp(&s.s_free[slot], g & 1)) { ok = false; break; }
+          if (!issue_s(g + 1)) { ok = false; break; }
+        }
+        if (!mbar_wait_warp(&s.p_full[slot], g & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t id_pv = c < nrc ? id_pv_raw : id_pv_sh;
+        const uint32_t vb = smem_u32(s.vb[st]);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tO, tP + kk * 8, smem_desc_sw128(vb + kk * 2048, 1024), id_pv, c > 0 || kk > 0);
           mma_commit(&s.pv_done[slot]);
           mma_commit(&s.kv_empty[st]);
         }
-        mma_commit(&s.drain[slot]);
-        if (!mbar_wait(&s.drain[slot], 0)) ok = false;
-        if (!ok) flag_error(status, kDevErrTimeout);
+        __syncwarp();
       }
+      if (elect_one()) mma_commit(&s.drain[slot]);
+      __syncwarp();
+      if (!mbar_wait_warp(&s.drain[slot], 0)) ok = false;
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
@@ -368,18 +367,22 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       tmem_ld_wait();
       if (ok && qi >= 0) {
         const float inv = 1.f / lsum;
-        uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)bh * N + qi) * 64);
+        bf16* dst = out + ((size_t)bh * N + qi) * 64;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint4 w;
-          w.x = pack_pair(o[8 * i] * inv, o[8 * i + 1] * inv, false);
-          w.y = pack_pair(o[8 * i + 2] * inv, o[8 * i + 3] * inv, false);
-          w.z = pack_pair(o[8 * i + 4] * inv, o[8 * i + 5] * inv, false);
-          w.w = pack_pair(o[8 * i + 6] * inv, o[8 * i + 7] * inv, false);
-          dst[i] = w;
+        for (int i = 0; i < 4; ++i) {   // 32-byte stores
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[e] = pack_pair(o[16 * i + 2 * e] * inv, o[16 * i + 2 * e + 1] * inv, false);
+          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * i),
+                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                       "r"(w[7])
+                       : "memory");
         }
       }
     };
+    // start the second tile's group half a chunk late: the two groups then take turns on
+    // the exponential unit instead of competing for it in lockstep
+    if (slot == 1) __nanosleep(500);
     int4 cur = units > 0 ? unit_tab[ubase] : make_int4(0, 0, 0, 0);
     int4 nxt = units > 1 ? unit_tab[ubase + 1] : cur;
     int qi = units > 0 ? row_query(cur) : -1;

@@ -56,6 +56,48 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return false;
 }
 
+// One poll that may suspend the thread until the phase completes (the hint, in
+// ns, caps the suspension; the thread wakes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return done != 0;
+}
+
+// Slow path of mbar_wait_warp, kept out of line: a loop anywhere near a
+// tcgen05.mma issue sequence slows the issue several-fold, even when the loop
+// body never runs.  Gives up after about 2^31 SM cycles (~1 s).
+static __device__ __noinline__ bool mbar_wait_warp_slow(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_hint(bar, parity))) return true;
+    if (clock64() - t0 > (1ll << 31)) break;
+  }
+  return false;
+}
+
+// Whole-warp bounded wait (all 32 lanes call it; they leave together).  The
+// common case -- the phase completes within one poll -- has no loop.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  if (__all_sync(0xffffffffu, mbar_try_wait_hint(bar, parity))) return true;
+  return mbar_wait_warp_slow(bar, parity);
+}
+
+// One lane of a converged warp (always the same one for a full warp).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b32 r;\n elect.sync r|p, 0xffffffff;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
