@@ -10,9 +10,11 @@
 //
 // sweep (pass 1), CTA = (head, 128 landmarks, key split):
 //   warp 0       TMA: K and V tiles of 128 keys into a 4-stage ring;
-//   warp 1       MMA: S = q~ K^T (tensor memory), then O += P V with P read
-//                from tensor memory;
-//   warps 2-3    squared key norms (error bound of the fp32 scores);
+//   warps 1-2    MMA, one issuing warp per softmax group: S = q~ K^T into the
+//                group's tensor memory, the group's next S as soon as the
+//                softmax has copied S out, then O += P V with P read from
+//                tensor memory;
+//   warp 3       largest |k| element (error bound of the fp32 scores);
 //   warps 4-7,   two softmax warpgroups that take alternate key tiles, each
 //   warps 8-11   with its own online-softmax state (max, sum) and its own O
 //                accumulator, so one computes while the other's MMAs run.
@@ -53,9 +55,9 @@ struct alignas(1024) SweepSmem {
   bf16 v[kStages][BN * 64];
   float top[2][kTopTiles][128];    // per slot: min-heap of tile maxima, [entry][row]
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t qt_full, drain;
-  uint64_t s_full[2], p_full[2], pv_done[2];
-  float nred[2];
+  uint64_t qt_full, drain[2];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  float nred;
   uint32_t tmem;
 };
 
@@ -126,13 +128,14 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.kv_full[i], 1);
-      mbar_init(&s.kv_empty[i], 3);        // MMA commit + two norm warps
+      mbar_init(&s.kv_empty[i], 2);        // the tile's MMA commit + the norm warp
     }
     mbar_init(&s.qt_full, 1);
-    mbar_init(&s.drain, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.drain[i], 1);
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 4);          // one arrival per softmax warp
+      mbar_init(&s.s_free[i], 4);          // one arrival per softmax warp
+      mbar_init(&s.p_full[i], 4);
       mbar_init(&s.pv_done[i], 1);
     }
     fence_mbar_init();
@@ -145,91 +148,110 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem;
-  // tensor memory columns: S_slot at 128*slot, P_slot at 256 + 64*slot, O_slot at 384 + 64*slot
+  // tensor memory, softmax group (slot) g at 256*g: S (128 columns), P (64, bf16 pairs), O (64).
+  // registers: the launch grants 384 x 168; warps 0-3 keep 56 each, the two softmax
+  // warpgroups take 224 each (128*56 + 2*128*224 = 384*168).
 
-  if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tmap(&map_qt);
-      prefetch_tmap(&map_k);
-      prefetch_tmap(&map_v);
-      mbar_expect_tx(&s.qt_full, 128 * 128);
-      tma_load_3d(s.qt, &map_qt, &s.qt_full, 0, rt * 128, bh);
-      for (int j = 0; j < ntl; ++j) {
-        const int st = j % kStages;
-        if (!mbar_wait(&s.kv_empty[st], ((j / kStages) & 1) ^ 1)) {
-          flag_error(status, kDevErrTimeout);
-          break;
-        }
-        mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
-        tma_load_3d(s.k[st], &map_k, &s.kv_full[st], 0, j0 + j * BN, bh);
-        tma_load_3d(s.v[st], &map_v, &s.kv_full[st], 0, j0 + j * BN, bh);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t id_s = idesc_f16(128, BN, false);
-      const uint32_t id_pv = idesc_f16(128, 64, true);
-      bool ok = mbar_wait(&s.qt_full, 0);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kStages, slot = j & 1;
-        if (!mbar_wait(&s.kv_full[st], (j / kStages) & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t da = smem_desc_sw128(smem_u32(s.qt) + kk * 32, 1024);
-          const uint64_t db = smem_desc_sw128(smem_u32(s.k[st]) + kk * 32, 1024);
-          mma_ss(tbase + slot * 128, da, db, id_s, kk > 0);
-        }
-        mma_commit(&s.s_full[slot]);
-        return true;
-      };
-      if (ok && ntl > 0) ok = issue_s(0);
-      if (ok && ntl > 1) ok = issue_s(1);
-      for (int j = 0; j < ntl && ok; ++j) {
-        const int st = j % kStages, slot = j & 1, t = j >> 1;
-        if (!mbar_wait(&s.p_full[slot], t & 1)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t dv = smem_desc_sw128(smem_u32(s.v[st]) + kk * 2048, 1024);
-          mma_ts(tbase + 384 + slot * 64, tbase + 256 + slot * 64 + kk * 8, dv, id_pv,
-                 t > 0 || kk > 0);
-        }
-        mma_commit(&s.kv_empty[st]);
-        mma_commit(&s.pv_done[slot]);
-        if (j + 2 < ntl) ok = issue_s(j + 2);
-      }
-      mma_commit(&s.drain);
-      if (!mbar_wait(&s.drain, 0)) ok = false;
-      if (!ok) flag_error(status, kDevErrTimeout);
-    }
-  } else if (warp == 2 || warp == 3) {
-    // largest |k| element of the split (bounds every key norm by 8 max|k|);
-    // each warp scans half of every tile, zero-filled rows past N are harmless
-    uint32_t mx = 0u;
-    bool ok = true;
-    for (int j = 0; j < ntl; ++j) {
-      const int st = j % kStages;
-      if (ok && !mbar_wait(&s.kv_full[st], (j / kStages) & 1)) ok = false;
-      if (ok) {
-        const uint4* src = reinterpret_cast<const uint4*>(s.k[st]) + (warp - 2) * 512;
-#pragma unroll 4
-        for (int i = lane; i < 512; i += 32) {
-          const uint4 x = src[i];
-          mx = umax16x2(mx, x.x & 0x7fff7fffu);
-          mx = umax16x2(mx, x.y & 0x7fff7fffu);
-          mx = umax16x2(mx, x.z & 0x7fff7fffu);
-          mx = umax16x2(mx, x.w & 0x7fff7fffu);
-        }
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    if (warp == 0) {
+      bool ok = true;
+      if (elect_one()) {
+        prefetch_tmap(&map_qt);
+        prefetch_tmap(&map_k);
+        prefetch_tmap(&map_v);
+        mbar_expect_tx(&s.qt_full, 128 * 128);
+        tma_load_3d(s.qt, &map_qt, &s.qt_full, 0, rt * 128, bh);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.kv_empty[st]);
+      for (int j = 0; j < ntl; ++j) {
+        const int st = j % kStages;
+        if (!mbar_wait_warp(&s.kv_empty[st], ((j / kStages) & 1) ^ 1)) { ok = false; break; }
+        if (elect_one()) {
+          mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
+          tma_load_3d(s.k[st], &map_k, &s.kv_full[st], 0, j0 + j * BN, bh);
+          tma_load_3d(s.v[st], &map_v, &s.kv_full[st], 0, j0 + j * BN, bh);
+        }
+        __syncwarp();
+      }
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
+    } else if (warp == 1 || warp == 2) {
+      // MMA issuer of softmax group `slot` (tiles j = slot, slot + 2, ...): whole warp,
+      // one elected lane issues
+      const int slot = warp - 1;
+      const uint32_t id_s = idesc_f16(128, BN, false);
+      const uint32_t id_pv = idesc_f16(128, 64, true);
+      const uint32_t tS = tbase + slot * 256, tP = tS + 128, tO = tS + 192;
+      const uint32_t qa = smem_u32(s.qt);
+      bool ok = mbar_wait_warp(&s.qt_full, 0);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kStages;
+        if (!mbar_wait_warp(&s.kv_full[st], (j / kStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(s.k[st]);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tS, smem_desc_sw128(qa + kk * 32, 1024), smem_desc_sw128(kb + kk * 32, 1024),
+                   id_s, kk > 0);
+          mma_commit(&s.s_full[slot]);
+        }
+        __syncwarp();
+        return true;
+      };
+      if (ok && slot < ntl) ok = issue_s(slot);
+      int t = 0;
+      for (int j = slot; j < ntl && ok; j += 2, ++t) {
+        const int st = j % kStages;
+        if (j + 2 < ntl) {
+          if (!mbar_wait_warp(&s.s_free[slot], t & 1)) { ok = false; break; }
+          if (!issue_s(j + 2)) { ok = false; break; }
+        }
+        if (!mbar_wait_warp(&s.p_full[slot], t & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t vb = smem_u32(s.v[st]);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tO, tP + kk * 8, smem_desc_sw128(vb + kk * 2048, 1024), id_pv, t > 0 || kk > 0);
+          mma_commit(&s.kv_empty[st]);
+          mma_commit(&s.pv_done[slot]);
+        }
+        __syncwarp();
+      }
+      if (elect_one()) mma_commit(&s.drain[slot]);
+      __syncwarp();
+      if (!mbar_wait_warp(&s.drain[slot], 0)) ok = false;
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
+    } else {
+      // largest |k| element of the split (bounds every key norm by 8 max|k|);
+      // zero-filled rows past N are harmless
+      uint32_t mx = 0u;
+      bool ok = true;
+      for (int j = 0; j < ntl; ++j) {
+        const int st = j % kStages;
+        if (ok && !mbar_wait(&s.kv_full[st], (j / kStages) & 1)) ok = false;
+        if (ok) {
+          const uint4* src = reinterpret_cast<const uint4*>(s.k[st]);
+#pragma unroll 8
+          for (int i = lane; i < 1024; i += 32) {
+            const uint4 x = src[i];
+            mx = umax16x2(mx, x.x & 0x7fff7fffu);
+            mx = umax16x2(mx, x.y & 0x7fff7fffu);
+            mx = umax16x2(mx, x.z & 0x7fff7fffu);
+            mx = umax16x2(mx, x.w & 0x7fff7fffu);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.kv_empty[st]);
+      }
+      const float a = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
+      const float km = warp_max(a);
+      if (lane == 0) s.nred = 64.f * km * km;   // bound on |k|^2
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     }
-    const float a = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
-    const float km = warp_max(a);
-    if (lane == 0) s.nred[warp - 2] = 64.f * km * km;   // bound on |k|^2
-    if (!ok) flag_error(status, kDevErrTimeout);
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int slot = (warp - 4) >> 2;
     const int quad = warp & 3;
@@ -237,37 +259,39 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
     const int grow = rt * 128 + row;                // landmark index
     const bool live_row = grow < m;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tbase + lane_off + slot * 128;
-    const uint32_t tP = tbase + lane_off + 256 + slot * 64;
-    const uint32_t tO = tbase + lane_off + 384 + slot * 64;
+    const uint32_t tS = tbase + lane_off + slot * 256, tP = tS + 128, tO = tS + 192;
     const float c = softmax_c();
     float mref = -INFINITY, lsum = 0.f;
     bool ok = true;
     int t = 0;
     for (int e = 0; e < kTopTiles; ++e) s.top[slot][e][row] = -INFINITY;
     float theta = -INFINITY;
+    // the second group starts half a tile late, so the two take turns on the
+    // exponential unit instead of competing for it in lockstep
+    if (slot == 1) __nanosleep(500);
     for (int j = slot; j < ntl; j += 2, ++t) {
       if (ok && !mbar_wait(&s.s_full[slot], t & 1)) ok = false;
       tc_fence_after();
       const int kbase = j0 + j * BN;
       const int nvalid = min(BN, j1 - kbase);
-      // pass A over S: the tile's largest raw score
       const bool full = nvalid == BN;
-      float tm = -INFINITY;
+      float v[BN];
       if (ok) {
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          float v[32];
-          tmem_ld32(tS + cc * 32, v);
-          tmem_ld_wait();
-          if (!full) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = (cc * 32 + i < nvalid) ? v[i] : -INFINITY;
-          }
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) tm = max3(tm, v[i], v[i + 1]);
-        }
+        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tS + cc * 32, v + cc * 32);
+        tmem_ld_wait();
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.s_free[slot]);   // the next S may overwrite these columns
+      if (!full) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
+      }
+      // the tile's largest raw score
+      float tm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BN; i += 2) tm = max3(tm, v[i], v[i + 1]);
       // keep the kTopTiles largest tile maxima of this slot (min-heap, root = smallest)
       if (tm > theta) {
         float* hp = &s.top[slot][0][row];
@@ -289,55 +313,53 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
         theta = hp[0];
       }
       const float xm = tm * c;
-      // P_slot and O_slot are free once the previous P.V of this slot is done
-      if (t > 0 && ok && !mbar_wait(&s.pv_done[slot], (t - 1) & 1)) ok = false;
-      tc_fence_after();
       const bool need = (t == 0) || (xm > mref + kLazy);
-      if (t > 0 && __any_sync(0xffffffffu, need)) {
-        const float f = need ? ex2(mref - xm) : 1.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float o[32];
-          tmem_ld32(tO + h * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= f;
-          tmem_st16(tO + h * 32, reinterpret_cast<uint32_t*>(o));
-          tmem_st16(tO + h * 32 + 16, reinterpret_cast<uint32_t*>(o + 16));
-        }
-        tmem_st_wait();
-      }
+      const float f = (t > 0 && need) ? ex2(mref - xm) : 1.f;
       if (need) {
-        if (t > 0) lsum *= ex2(mref - xm);
+        lsum *= f;
         mref = xm;
       }
-      // pass B over S: P = exp2(s * c - mref) as bf16 pairs into tensor memory
+      // P = exp2(s * c - mref) as bf16 pairs; the first half before waiting for the
+      // previous P . V of this slot (which still reads P and accumulates O)
       const unsigned long long c2 = f2pack(c, c), nm2 = f2pack(-mref, -mref);
       unsigned long long ls2 = f2pack(0.f, 0.f);
+      uint32_t pk[BN / 2];
 #pragma unroll
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        float v[32];
-        tmem_ld32(tS + cc * 32, v);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float x0, x1;
-          f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, nm2), x0, x1);
-          float p0 = ex2(x0), p1 = ex2(x1);
-          if (!full) {
-            p0 = (cc * 32 + i < nvalid) ? p0 : 0.f;
-            p1 = (cc * 32 + i + 1 < nvalid) ? p1 : 0.f;
-          }
-          ls2 = add2(ls2, f2pack(p0, p1));
-          pk[i / 2] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tP + cc * 16, pk);
+      for (int i = 0; i < BN / 2; i += 2) {
+        float x0, x1;
+        f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, nm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        ls2 = add2(ls2, f2pack(p0, p1));
+        pk[i / 2] = pack_bf16x2(p0, p1);
       }
+      if (t > 0 && ok && !mbar_wait(&s.pv_done[slot], (t - 1) & 1)) ok = false;
+      tc_fence_after();
+      tmem_st16(tP, pk);
+      tmem_st16(tP + 16, pk + 16);
+#pragma unroll
+      for (int i = BN / 2; i < BN; i += 2) {
+        float x0, x1;
+        f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, nm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        ls2 = add2(ls2, f2pack(p0, p1));
+        pk[i / 2] = pack_bf16x2(p0, p1);
+      }
+      tmem_st16(tP + 32, pk + 32);
+      tmem_st16(tP + 48, pk + 48);
       float ls_a, ls_b;
       f2unpack(ls2, ls_a, ls_b);
-      const float ls = ls_a + ls_b;
-      lsum += ls;
+      lsum += ls_a + ls_b;
+      if (t > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float o[16];
+          tmem_ld16(tO + h * 16, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] *= f;
+          tmem_st16(tO + h * 16, reinterpret_cast<uint32_t*>(o));
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -371,7 +393,7 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (threadIdx.x == 0 && rt == 0) ws.kmax2[(size_t)bh * S + sp] = fmaxf(s.nred[0], s.nred[1]);
+  if (threadIdx.x == 0 && rt == 0) ws.kmax2[(size_t)bh * S + sp] = s.nred;
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
@@ -442,7 +464,7 @@ struct alignas(1024) CollectSmem {
   int ci[kLocalCand][128];
   int cn[128];
   uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t qt_full, drain;
+  uint64_t qt_full, drain[2];
   uint64_t s_full[2], s_free[2];
   uint32_t tmem;
 };
@@ -470,8 +492,8 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
       mbar_init(&s.k_empty[i], 1);
     }
     mbar_init(&s.qt_full, 1);
-    mbar_init(&s.drain, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.drain[i], 1);
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], 4);
     }
@@ -487,43 +509,52 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
   const uint32_t tbase = s.tmem;
 
   if (warp == 0) {
-    if (lane == 0) {
+    bool ok = true;
+    if (elect_one()) {
       prefetch_tmap(&map_qt);
       prefetch_tmap(&map_k);
       mbar_expect_tx(&s.qt_full, 128 * 128);
       tma_load_3d(s.qt, &map_qt, &s.qt_full, 0, rt * 128, bh);
-      for (int j = 0; j < ntl; ++j) {
-        const int st = j % kKStages;
-        if (!mbar_wait(&s.k_empty[st], ((j / kKStages) & 1) ^ 1)) {
-          flag_error(status, kDevErrTimeout);
-          break;
-        }
+    }
+    __syncwarp();
+    for (int j = 0; j < ntl; ++j) {
+      const int st = j % kKStages;
+      if (!mbar_wait_warp(&s.k_empty[st], ((j / kKStages) & 1) ^ 1)) { ok = false; break; }
+      if (elect_one()) {
         mbar_expect_tx(&s.k_full[st], BN * 128);
         tma_load_3d(s.k[st], &map_k, &s.k_full[st], 0, j0 + j * BN, bh);
       }
+      __syncwarp();
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t id_s = idesc_f16(128, BN, false);
-      bool ok = mbar_wait(&s.qt_full, 0);
-      for (int j = 0; j < ntl && ok; ++j) {
-        const int st = j % kKStages, slot = j & 1, t = j >> 1;
-        if (!mbar_wait(&s.k_full[st], (j / kKStages) & 1)) { ok = false; break; }
-        if (!mbar_wait(&s.s_free[slot], (t & 1) ^ 1)) { ok = false; break; }
-        tc_fence_after();
+    if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
+  } else if (warp == 1 || warp == 2) {
+    // MMA issuer of tile group `slot` (tiles slot, slot + 2, ...): whole warp, one
+    // elected lane issues
+    const int slot = warp - 1;
+    const uint32_t id_s = idesc_f16(128, BN, false);
+    const uint32_t qa = smem_u32(s.qt);
+    bool ok = mbar_wait_warp(&s.qt_full, 0);
+    int t = 0;
+    for (int j = slot; j < ntl && ok; j += 2, ++t) {
+      const int st = j % kKStages;
+      if (!mbar_wait_warp(&s.k_full[st], (j / kKStages) & 1)) { ok = false; break; }
+      if (!mbar_wait_warp(&s.s_free[slot], (t & 1) ^ 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t kb = smem_u32(s.k[st]);
+      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t da = smem_desc_sw128(smem_u32(s.qt) + kk * 32, 1024);
-          const uint64_t db = smem_desc_sw128(smem_u32(s.k[st]) + kk * 32, 1024);
-          mma_ss(tbase + slot * 128, da, db, id_s, kk > 0);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tbase + slot * 128, smem_desc_sw128(qa + kk * 32, 1024),
+                 smem_desc_sw128(kb + kk * 32, 1024), id_s, kk > 0);
         mma_commit(&s.s_full[slot]);
         mma_commit(&s.k_empty[st]);
       }
-      mma_commit(&s.drain);
-      if (!mbar_wait(&s.drain, 0)) ok = false;
-      if (!ok) flag_error(status, kDevErrTimeout);
+      __syncwarp();
     }
+    if (elect_one()) mma_commit(&s.drain[slot]);
+    __syncwarp();
+    if (!mbar_wait_warp(&s.drain[slot], 0)) ok = false;
+    if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
   } else if (warp >= 4) {
     const int slot = (warp - 4) >> 2;
     const int quad = warp & 3;
@@ -540,12 +571,19 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
       tc_fence_after();
       const int kbase = j0 + j * BN;
       const int nvalid = min(BN, j1 - kbase);
+      float vv[BN];
+      if (ok) {
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tS + cc * 32, vv + cc * 32);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.s_free[slot]);   // the next S may overwrite these columns
       if (ok) {
 #pragma unroll
         for (int cc = 0; cc < BN / 32; ++cc) {
-          float v[32];
-          tmem_ld32(tS + cc * 32, v);
-          tmem_ld_wait();
+          const float* v = vv + cc * 32;
           // bitmask of the scores at or above the threshold (branch-free), then
           // visit only its set bits
           uint32_t msk = 0u;
@@ -572,9 +610,6 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.s_free[slot]);
     }
     if (!ok) flag_error(status, kDevErrTimeout);
   }
