@@ -131,10 +131,10 @@ __device__ __forceinline__ bool ranks_before(F2 a, int ia, F2 b, int ib) {
 // relative -- exact enough to order candidates whose exact scores differ by
 // far less than the 1e-6 relative gap the parity rule allows.  fp32 only:
 // fp64 runs at a small fraction of the fp32 rate on this part.
-template <int D>
+template <int D, int UNROLL = 8>
 __device__ __forceinline__ F2 dot_f2(const float* a, const float* b) {
   float s = 0.f, c = 0.f;
-#pragma unroll 8
+#pragma unroll UNROLL
   for (int l = 0; l < D; ++l) {
     const float p = __fmul_rn(a[l], b[l]);
     const float e = fmaf(a[l], b[l], -p);

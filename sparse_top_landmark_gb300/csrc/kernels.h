@@ -95,7 +95,7 @@ bool make_tmap_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 // TMA map over a [rows, 64] bf16 array for tile::gather4 (four scattered rows).
 bool make_tmap_gather64(CUtensorMap* map, const void* base, uint64_t rows);
 bool route_tc_supported(int d, int m);
-// `amb` is scratch of 1 + BH*N ints (count, then ambiguous query ids).
+// `amb` is scratch of BH*(N+1) ints: per head, a count then ambiguous query ids.
 cudaError_t launch_route_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH, int N,
                             int m, int num_sms, int32_t* route, int* amb, int* status,
                             cudaStream_t st);

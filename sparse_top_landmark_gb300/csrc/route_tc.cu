@@ -7,15 +7,17 @@
 // One CTA owns a head's landmark block q~ (TMA, resident in shared memory)
 // and walks query tiles of 128 rows of that head:
 //   warp 0      TMA producer: query tiles into a 3-stage ring;
-//   warp 1      MMA issuer: S = Q_tile . q~^T into tensor memory, in chunks of
-//               W <= 256 landmarks, two chunk buffers (ping-pong);
+//   warp 1      MMA issuer (whole warp, one elected lane issues): S = Q_tile .
+//               q~^T into tensor memory, in chunks of W <= 256 landmarks, two
+//               chunk buffers (ping-pong);
 //   warps 4-11  epilogue: TMEM lane quadrant = warp % 4 (one query row per
-//               thread), two warps per quadrant split each chunk's columns.
-// Each thread keeps the exact best and runner-up fp32 scores of its query
-// (branch-free min/max) and a register copy of the 32-score block holding the
-// running best, so the best's index (lowest on ties) is looked up once at the
-// end.  When the best beats the runner-up by more than 2E (E bounds the fp32
-// dot error) it is the exact argmax; otherwise the query goes on an
+//               thread), two warps per quadrant split each chunk's columns and
+//               meet on a 64-thread barrier per tile.
+// Each thread keeps, over blocks of 32 scores, the running best with a
+// register copy of the block holding it, and the maxima of all other blocks;
+// the exact best, runner-up and the best's index (lowest on ties) follow at
+// the end of the row.  When the best beats the runner-up by more than 2E (E bounds the fp32
+// dot error) it is the exact argmax; otherwise the query goes on its head's
 // "ambiguous" list and route_fixup_kernel re-routes it exactly (fp32
 // screening + exact-product re-scoring, ties to the lowest index) -- about
 // 0.2% of the queries on the long-sequence workloads.
@@ -45,6 +47,7 @@ struct alignas(1024) RouteSmem {
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t qt_full, drain;
   uint64_t s_full[2], s_empty[2];
+  // (drain: completion of the issuer's last products before tensor memory is freed)
   Cand cand[2][128];                   // half-1 partial results, by tile parity
   float red[kEpiWarps];
   float qtmax2;
@@ -52,6 +55,10 @@ struct alignas(1024) RouteSmem {
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// the two epilogue warps of one TMEM lane quadrant
+__device__ __forceinline__ void quad_bar(int quad) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
+}
 
 // Row r (128 bytes) of a 128B-swizzled bf16 tile -> 64 floats.
 __device__ __forceinline__ void load_swizzled_row(const bf16* tile, int r, float* out) {
@@ -74,46 +81,61 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
-// Top-2 update over a block of 32 scores starting at index i0 (entries at or
-// past nvalid ignored); bb keeps a copy of the block that holds the best.
-__device__ __forceinline__ void top2_block(Cand& c, float* bb, int& bb0, const float* v, int i0,
-                                           int nvalid) {
-  const float before = c.v1;
-  if (nvalid >= 32) {
+// Running best over blocks of 32 scores.  Per block only its maximum is
+// computed; the block holding the running best is kept in registers (bb,
+// first index bb0) and every other block contributes its maximum to v2c.  At
+// the end the best's index (lowest on ties) and the runner-up come from bb:
+// the runner-up of the whole row is the larger of v2c and the second largest
+// entry of bb.
+struct RowTop {
+  float v1 = -INFINITY, v2c = -INFINITY;
+  int bb0 = 0;
+  float bb[32];
+};
+
+__device__ __forceinline__ void top_block(RowTop& t, const float* v, int i0, int nvalid) {
+  float x[32];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      const float hi = fmaxf(v[i], v[i + 1]), lo = fminf(v[i], v[i + 1]);
-      c.v2 = max3f(c.v2, lo, fminf(c.v1, hi));
-      c.v1 = fmaxf(c.v1, hi);
-    }
-  } else {
+  for (int i = 0; i < 32; ++i) x[i] = v[i];
+  if (nvalid < 32) {                 // ragged last block (uniform across the warp)
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      const float a = (i < nvalid) ? v[i] : -INFINITY;
-      const float b = (i + 1 < nvalid) ? v[i + 1] : -INFINITY;
-      const float hi = fmaxf(a, b), lo = fminf(a, b);
-      c.v2 = max3f(c.v2, lo, fminf(c.v1, hi));
-      c.v1 = fmaxf(c.v1, hi);
-    }
+    for (int i = 0; i < 32; ++i) x[i] = i < nvalid ? x[i] : -INFINITY;
   }
-  const bool up = c.v1 > before;
+  float a[11];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) bb[i] = up ? v[i] : bb[i];
-  bb0 = up ? i0 : bb0;
+  for (int i = 0; i < 10; ++i) a[i] = max3f(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  a[10] = fmaxf(x[30], x[31]);
+  const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]);
+  const float b2 = max3f(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+  const float mb = fmaxf(max3f(b0, b1, b2), b3);
+  const bool up = mb > t.v1;
+  t.v2c = fmaxf(t.v2c, up ? t.v1 : mb);
+  t.v1 = up ? mb : t.v1;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) t.bb[i] = up ? x[i] : t.bb[i];
+  t.bb0 = up ? i0 : t.bb0;
 }
 
-// lowest index in the saved block whose score equals the best
-__device__ __forceinline__ int block_argmax(const float* bb, int bb0, float v1) {
+// (best, runner-up, lowest index of the best) of a finished row
+__device__ __forceinline__ Cand finish_top(const RowTop& t) {
+  Cand c{t.v1, t.v2c, 0x7fffffff};
+  if (t.v1 == -INFINITY) return c;
   int k = 31;
 #pragma unroll
-  for (int i = 31; i >= 0; --i) k = (bb[i] == v1) ? i : k;
-  return bb0 + k;
+  for (int i = 31; i >= 0; --i) k = (t.bb[i] == t.v1) ? i : k;
+  float s2 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) s2 = (i == k) ? s2 : fmaxf(s2, t.bb[i]);
+  c.v2 = fmaxf(c.v2, s2);
+  c.i1 = t.bb0 + k;
+  return c;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_qt,
                 int N, int m, int W, int nch, int G_h, uint32_t tmem_cols,
                 int32_t* __restrict__ route, int* __restrict__ amb, int* status) {
+  // amb: per head, [count, query ids...] at amb + bh * (N + 1)
   extern __shared__ unsigned char smem_raw[];
   RouteSmem& s = *reinterpret_cast<RouteSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -144,53 +166,64 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   tc_fence_after();
   const uint32_t tbase = s.tmem;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&map_q);
-      prefetch_tmap(&map_qt);
-      mbar_expect_tx(&s.qt_full, (uint32_t)(nch * W * 128));
-      for (int ch = 0; ch < nch; ++ch)
-        tma_load_3d(s.qt + ch * W * 64, &map_qt, &s.qt_full, 0, ch * W, bh);
+  // registers: the launch grants 384 x 168; warps 0-3 keep 56 each, the two epilogue
+  // warpgroups take 224 each (128*56 + 2*128*224 = 384*168)
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      bool ok = true;
+      if (elect_one()) {
+        prefetch_tmap(&map_q);
+        prefetch_tmap(&map_qt);
+        mbar_expect_tx(&s.qt_full, (uint32_t)(nch * W * 128));
+        for (int ch = 0; ch < nch; ++ch)
+          tma_load_3d(s.qt + ch * W * 64, &map_qt, &s.qt_full, 0, ch * W, bh);
+      }
+      __syncwarp();
       for (int it = 0; it < ntiles; ++it) {
         const int st = it % kQStages;
-        if (!mbar_wait(&s.q_empty[st], ((it / kQStages) & 1) ^ 1)) {
-          flag_error(status, kDevErrTimeout);
-          break;
+        if (!mbar_wait_warp(&s.q_empty[st], ((it / kQStages) & 1) ^ 1)) { ok = false; break; }
+        if (elect_one()) {
+          mbar_expect_tx(&s.q_full[st], 128 * 128);
+          tma_load_3d(s.q[st], &map_q, &s.q_full[st], 0, (c0 + it * G_h) * 128, bh);
         }
-        mbar_expect_tx(&s.q_full[st], 128 * 128);
-        tma_load_3d(s.q[st], &map_q, &s.q_full[st], 0, (c0 + it * G_h) * 128, bh);
+        __syncwarp();
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
       const uint32_t idesc = idesc_f16(128, W, false);
-      bool ok = mbar_wait(&s.qt_full, 0);
+      const uint32_t qtb = smem_u32(s.qt);
+      bool ok = mbar_wait_warp(&s.qt_full, 0);
       int gch = 0;
       for (int it = 0; it < ntiles && ok; ++it) {
         const int st = it % kQStages;
-        if (!mbar_wait(&s.q_full[st], (it / kQStages) & 1)) { ok = false; break; }
-        tc_fence_after();
+        if (!mbar_wait_warp(&s.q_full[st], (it / kQStages) & 1)) { ok = false; break; }
+        const uint32_t qa = smem_u32(s.q[st]);
         for (int ch = 0; ch < nch; ++ch, ++gch) {
           const int b = gch & 1;
-          if (!mbar_wait(&s.s_empty[b], ((gch >> 1) & 1) ^ 1)) { ok = false; break; }
+          if (!mbar_wait_warp(&s.s_empty[b], ((gch >> 1) & 1) ^ 1)) { ok = false; break; }
           tc_fence_after();
+          const uint32_t qb = qtb + ch * W * 128;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da = smem_desc_sw128(smem_u32(s.q[st]) + kk * 32, 1024);
-            const uint64_t db = smem_desc_sw128(smem_u32(s.qt + ch * W * 64) + kk * 32, 1024);
-            mma_ss(tbase + b * W, da, db, idesc, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tbase + b * W, smem_desc_sw128(qa + kk * 32, 1024),
+                     smem_desc_sw128(qb + kk * 32, 1024), idesc, kk > 0);
+            mma_commit(&s.s_full[b]);
+            if (ch == nch - 1) mma_commit(&s.q_empty[st]);
           }
-          mma_commit(&s.s_full[b]);
+          __syncwarp();
         }
-        mma_commit(&s.q_empty[st]);
       }
-      mma_commit(&s.drain);
-      if (!mbar_wait(&s.drain, 0)) ok = false;
-      if (!ok) flag_error(status, kDevErrTimeout);
+      if (elect_one()) mma_commit(&s.drain);
+      __syncwarp();
+      if (!mbar_wait_warp(&s.drain, 0)) ok = false;
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     }
-  } else if (warp >= 4) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
     // ------------------------------------------------------------ epilogue
     const int et = threadIdx.x - 128;              // 0..255
     const int quad = warp & 3, half = (warp - 4) >> 2;
@@ -215,72 +248,90 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     float qtmax2 = 0.f;
     for (int i = 0; i < kEpiWarps; ++i) qtmax2 = fmaxf(qtmax2, s.red[i]);
     const float gam = err_gamma(64);
-    const int cols_half = W / 2;
+    const int cols_half = W / 2;                   // a multiple of 16, at most 128
+    int* hamb = amb + (size_t)bh * (N + 1);
     int gch = 0;
     for (int it = 0; it < ntiles; ++it) {
       const int st = it % kQStages;
       if (ok && !mbar_wait(&s.q_full[st], (it / kQStages) & 1)) ok = false;
-      Cand c{-INFINITY, -INFINITY, 0x7fffffff};
-      float bb[32];
-      int bb0 = 0;
+      // the query's error bound first (half 0), while the scores are computed
+      const int n = (c0 + it * G_h) * 128 + row;
+      const bool live = ok && n < N;
+      float twoE = 0.f;
+      if (half == 0 && live) {
+        float qr[64];
+        load_swizzled_row(s.q[st], row, qr);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) bb[i] = -INFINITY;
+        for (int l = 0; l < 64; l += 4) {
+          a0 = fmaf(qr[l], qr[l], a0);
+          a1 = fmaf(qr[l + 1], qr[l + 1], a1);
+          a2 = fmaf(qr[l + 2], qr[l + 2], a2);
+          a3 = fmaf(qr[l + 3], qr[l + 3], a3);
+        }
+        twoE = 2.f * gam * sqrtf((a0 + a1) + (a2 + a3)) * sqrtf(qtmax2);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.q_empty[st]);   // this warp is done with the query tile
+      RowTop top;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) top.bb[i] = -INFINITY;
       for (int ch = 0; ch < nch; ++ch, ++gch) {
         const int b = gch & 1;
         if (ok && !mbar_wait(&s.s_full[b], (gch >> 1) & 1)) ok = false;
         tc_fence_after();
+        const int col0 = half * cols_half;
+        float v[128];
         if (ok) {
-          const int col0 = half * cols_half;
-          for (int cc = 0; cc < cols_half; cc += 32) {
-            float v[32];
-            const uint32_t ta = tbase + taddr_lane + (uint32_t)(b * W + col0 + cc);
-            tmem_ld16(ta, v);                 // cols_half is a multiple of 16
-            if (cols_half - cc > 16) tmem_ld16(ta + 16, v + 16);
-            tmem_ld_wait();
-            const int i0 = ch * W + col0 + cc;
-            top2_block(c, bb, bb0, v, i0, min(m - i0, cols_half - cc));
+          const uint32_t ta = tbase + taddr_lane + (uint32_t)(b * W + col0);
+          if (cols_half >= 64) {
+            tmem_ld64(ta, v);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 64; cc += 16)
+              if (cc < cols_half) tmem_ld16(ta + cc, v + cc);
           }
+          if (cols_half >= 128) {
+            tmem_ld64(ta + 64, v + 64);
+          } else {
+#pragma unroll
+            for (int cc = 64; cc < 128; cc += 16)
+              if (cc < cols_half) tmem_ld16(ta + cc, v + cc);
+          }
+          tmem_ld_wait();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.s_empty[b]);
+        if (lane == 0) mbar_arrive(&s.s_empty[b]);   // the buffer may be overwritten now
+        if (ok) {
+#pragma unroll
+          for (int cc = 0; cc < 128; cc += 32) {
+            if (cc < cols_half) {
+              const int i0 = ch * W + col0 + cc;
+              top_block(top, v + cc, i0, min(m - i0, cols_half - cc));
+            }
+          }
+        }
       }
-      if (c.v1 > -INFINITY) c.i1 = block_argmax(bb, bb0, c.v1);
-      if (half == 1) {
-        s.cand[it & 1][row] = c;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.q_empty[st]);
-      }
-      epi_bar();
+      const Cand c = finish_top(top);
+      if (half == 1) s.cand[it & 1][row] = c;
+      quad_bar(quad);
       if (half == 0) {
         const Cand o = s.cand[it & 1][row];
         const bool w1 = o.v1 > c.v1 || (o.v1 == c.v1 && o.i1 < c.i1);
         const float v1 = w1 ? o.v1 : c.v1;
         const int i1 = w1 ? o.i1 : c.i1;
         const float v2 = max3f(c.v2, o.v2, fminf(c.v1, o.v1));
-        const int n = (c0 + it * G_h) * 128 + row;
-        const bool live = ok && n < N;
-        bool ambiguous = false;
-        if (live) {
-          float qr[64];
-          load_swizzled_row(s.q[st], row, qr);
-          float qn2 = 0.f;
-#pragma unroll
-          for (int l = 0; l < 64; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
-          const float twoE = 2.f * gam * sqrtf(qn2) * sqrtf(qtmax2);
-          ambiguous = !(v1 - v2 > twoE);
-          route[(size_t)bh * N + n] = i1;
-        }
-        // append ambiguous queries (one reservation per warp)
+        const bool ambiguous = live && !(v1 - v2 > twoE);
+        if (live) route[(size_t)bh * N + n] = i1;
+        // append ambiguous queries to the head's list (one reservation per warp)
         const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
         if (am) {
           int base = 0;
-          if (lane == 0) base = atomicAdd(amb, __popc(am));
+          if (lane == 0) base = atomicAdd(hamb, __popc(am));
           base = __shfl_sync(0xffffffffu, base, 0);
-          if (ambiguous) amb[1 + base + __popc(am & ((1u << lane) - 1u))] = (int)((size_t)bh * N + n);
+          if (ambiguous) hamb[1 + base + __popc(am & ((1u << lane) - 1u))] = n;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.q_empty[st]);
       }
     }
     if (!ok) flag_error(status, kDevErrTimeout);
@@ -291,47 +342,80 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   if (warp == 1) tmem_dealloc(tbase, tmem_cols);
 }
 
-// Exact routing of the ambiguous queries: one warp per query.  Lanes screen
-// all m landmarks with fp32 dots (only those within 2E of the fp32 best can
-// win), re-score the survivors with exact-product arithmetic and reduce
-// (score desc, index asc).
+// Exact routing of the ambiguous queries.  CTA = (head, slice of the head's
+// list) with the head's q~ block in shared memory (rows padded to 144 bytes:
+// a warp's 16-byte reads of 32 different rows then hit every bank evenly);
+// one warp per query: lanes screen the landmarks with fp32 dots (only those
+// within 2E of the fp32 best can win), re-score the survivors with
+// exact-product arithmetic and reduce (score desc, index asc).
+constexpr int kFixRow = 72;            // bf16 per padded landmark row
+
 __global__ void __launch_bounds__(256)
 route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde, int N, int m,
-                   const int* __restrict__ amb, int32_t* __restrict__ route) {
-  const int lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * 8;
-  const int count = amb[0];
-  for (int w = blockIdx.x * 8 + (threadIdx.x >> 5); w < count; w += nwarps) {
-    const int qflat = amb[1 + w];
-    const int bh = qflat / N;
+                   int per_head, const int* __restrict__ amb, int32_t* __restrict__ route) {
+  extern __shared__ __align__(16) unsigned char fix_raw[];
+  bf16* qt = reinterpret_cast<bf16*>(fix_raw);       // [m][kFixRow]
+  __shared__ float red[8];
+  const int bh = blockIdx.x / per_head, part = blockIdx.x % per_head;
+  const int* hamb = amb + (size_t)bh * (N + 1);
+  const int count = hamb[0];
+  if (count <= part * 8) return;                      // no query for this CTA
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bf16* qtb = q_tilde + (size_t)bh * m * 64;
+  float n2 = 0.f;
+  for (int t = threadIdx.x; t < m * 8; t += 256) {
+    const int i = t >> 3, c = t & 7;
+    const uint4 x = reinterpret_cast<const uint4*>(qtb + (size_t)i * 64)[c];
+    *reinterpret_cast<uint4*>(qt + i * kFixRow + c * 8) = x;
+    float f[8];
+    Vec<bf16>::load(reinterpret_cast<const bf16*>(&x), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) n2 = fmaf(f[e], f[e], n2);
+  }
+  // largest squared landmark norm: per-row sums of 8 lanes' partials
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 4);
+  n2 = warp_max(n2);
+  if (lane == 0) red[warp] = n2;
+  __syncthreads();
+  float qt2 = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) qt2 = fmaxf(qt2, red[w]);
+  for (int w = part * 8 + warp; w < count; w += per_head * 8) {
+    const int n = hamb[1 + w];
+    if (n < 0 || n >= N) continue;
     float qr[64];
-    load_row<bf16, 64>(q + (size_t)qflat * 64, qr);
-    float qn2 = 0.f, best = -INFINITY, qt2 = 0.f;
+    load_row<bf16, 64>(q + ((size_t)bh * N + n) * 64, qr);
+    float qn2 = 0.f;
 #pragma unroll
     for (int l = 0; l < 64; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
-    const bf16* qtb = q_tilde + (size_t)bh * m * 64;
+    // pass 1: the fp32 best (the landmark loops stay rolled: unrolled copies of
+    // these bodies overflow the instruction cache)
+    float best = -INFINITY;
+#pragma unroll 1
     for (int i = lane; i < m; i += 32) {
       float r[64];
-      load_row<bf16, 64>(qtb + (size_t)i * 64, r);
-      float d = 0.f, n2 = 0.f;
+      load_row<bf16, 64>(qt + i * kFixRow, r);
+      float a = 0.f;
 #pragma unroll
-      for (int l = 0; l < 64; ++l) { d = fmaf(qr[l], r[l], d); n2 = fmaf(r[l], r[l], n2); }
-      best = fmaxf(best, d);
-      qt2 = fmaxf(qt2, n2);
+      for (int l = 0; l < 64; ++l) a = fmaf(qr[l], r[l], a);
+      best = fmaxf(best, a);
     }
     best = warp_max(best);
-    qt2 = warp_max(qt2);
     const float twoE = 2.f * err_gamma(64) * sqrtf(qn2) * sqrtf(qt2);
+    // pass 2: exact re-scoring of the landmarks within 2E of it
     F2 bv{-INFINITY, 0.f};
     int bi = 0x7fffffff;
+#pragma unroll 1
     for (int i = lane; i < m; i += 32) {
       float r[64];
-      load_row<bf16, 64>(qtb + (size_t)i * 64, r);
-      float d = 0.f;
+      load_row<bf16, 64>(qt + i * kFixRow, r);
+      float a = 0.f;
 #pragma unroll
-      for (int l = 0; l < 64; ++l) d = fmaf(qr[l], r[l], d);
-      if (d >= best - twoE) {
-        const F2 x = dot_f2<64>(qr, r);
+      for (int l = 0; l < 64; ++l) a = fmaf(qr[l], r[l], a);
+      if (a >= best - twoE) {
+        const F2 x = dot_f2<64, 64>(qr, r);   // fully unrolled: qr, r stay in registers
         if (ranks_before(x, i, bv, bi)) { bv = x; bi = i; }
       }
     }
@@ -341,7 +425,7 @@ route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde,
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
-    if (lane == 0) route[qflat] = bi;
+    if (lane == 0) route[(size_t)bh * N + n] = bi;
   }
 }
 
@@ -368,12 +452,19 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(amb, 0, sizeof(int), st);
-  if (e != cudaSuccess) return e;
+  for (int b = 0; b < BH; ++b) {
+    e = cudaMemsetAsync(amb + (size_t)b * (N + 1), 0, sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
   route_tc_kernel<<<(unsigned)(BH * G_h), kThreads, smem, st>>>(mq, mqt, N, m, W, nch, G_h, cols,
                                                                  route, amb, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  route_fixup_kernel<<<std::max(num_sms, 1) * 4, 256, 0, st>>>(q, q_tilde, N, m, amb, route);
+  const int per_head = std::max(1, std::max(num_sms, 1) / BH);
+  const size_t fsm = (size_t)m * kFixRow * 2;
+  e = cudaFuncSetAttribute(route_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm);
+  if (e != cudaSuccess) return e;
+  route_fixup_kernel<<<(unsigned)(BH * per_head), 256, fsm, st>>>(q, q_tilde, N, m, per_head, amb,
+                                                                 route);
   return cudaGetLastError();
 }
 
