@@ -28,8 +28,11 @@ from sparse_top_landmark_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MiTA fwd queries/sec at N=64K and 1M on 1 GB300; % of per-stage roofline"
 UNIT = "queries/s"
-KERNELS_PER_FORWARD = 13  # pool 1, landmark 5, route 2, bucket 3, expert 2 (bf16, d=64 path)
 L2_BYTES = 129 * 2 ** 20
+# DRAM traffic of the expert stage's kernels from an ncu capture, with the
+# hash of the kernel source it was taken on (stale counters are not reported)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "expert_long_1m_dram.txt")
+EXPERT_SOURCE = os.path.join(ROOT, "sparse_top_landmark_gb300", "csrc", "expert_tc.cu")
 
 
 def peaks():
@@ -121,36 +124,75 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle timing on a bounded sample (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample_time(w, q, k, v, rows=None, queries=None, seed=0):
-    """Time the oracle on a sample; return (estimated seconds for the whole
-    workload, description, threads)."""
+def oracle_sample_time(w, q, k, v, budget=15.0, seed=0):
+    """Time the oracle on a bounded sample of the workload: every pooling
+    window, then batches of landmark rows (one per thread) for about 60% of
+    `budget` seconds, then batches of queries (route + joint attention) for
+    about 30%.  Returns (estimated seconds for the whole workload,
+    description, threads, seconds spent)."""
     import oracle
     g = torch.Generator().manual_seed(seed)
     BH, N, m = w.B * w.H, w.N, w.m
     threads = oracle.num_threads()
-    nrows = rows or max(2 * threads, 8)
-    nq = queries or 8192
     t0 = time.perf_counter()
     qt = oracle.pool(q, w.grid_h, w.grid_w, m)
     t_pool = time.perf_counter() - t0
-    rsel = torch.randint(0, BH * m, (min(nrows, BH * m),), generator=g)
-    t0 = time.perf_counter()
-    ti, vt, _ = oracle.landmark(qt, k, v, w.topk, rows=rsel)
-    t_rows = time.perf_counter() - t0
+    rows, t_rows = [], 0.0
+    tis, vts = [], []
+    while len(rows) < BH * m and (not rows or t_rows < 0.6 * budget):
+        sel = torch.randint(0, BH * m, (min(threads, BH * m),), generator=g)
+        t0 = time.perf_counter()
+        ti, vt, _ = oracle.landmark(qt, k, v, w.topk, rows=sel)
+        t_rows += time.perf_counter() - t0
+        rows.append(sel)
+        tis.append(ti)
+        vts.append(vt)
+    nrows = sum(r.numel() for r in rows)
+    ti, vt = torch.cat(tis), torch.cat(vts)
     # per-query work does not depend on the values: every landmark reuses the
     # sampled rows' outputs
     full_ti = ti[torch.arange(BH * m) % ti.shape[0]].view(w.B, w.H, m, w.topk).contiguous()
     full_vt = vt[torch.arange(BH * m) % vt.shape[0]].view(w.B, w.H, m, w.d).contiguous()
-    qsel = torch.randint(0, BH * N, (min(nq, BH * N),), generator=g)
-    t0 = time.perf_counter()
-    r, _ = oracle.route(q, qt, w.s, queries=qsel)
-    oracle.attend(q, k, v, qt, full_vt, full_ti, r, queries=qsel)
-    t_q = time.perf_counter() - t0
-    est = t_pool + t_rows * (BH * m) / rsel.numel() + t_q * (BH * N) / qsel.numel()
+    nq, t_q = 0, 0.0
+    while nq < BH * N and (nq == 0 or t_q < 0.3 * budget):
+        qsel = torch.randint(0, BH * N, (min(8192, BH * N),), generator=g)
+        t0 = time.perf_counter()
+        r, _ = oracle.route(q, qt, w.s, queries=qsel)
+        oracle.attend(q, k, v, qt, full_vt, full_ti, r, queries=qsel)
+        t_q += time.perf_counter() - t0
+        nq += qsel.numel()
+    est = t_pool + t_rows * (BH * m) / nrows + t_q * (BH * N) / nq
     desc = (f"oracle on {threads} threads: pool of all {BH * m} windows, "
-            f"{rsel.numel()} of {BH * m} landmark rows, route+attend of {qsel.numel()} of "
-            f"{BH * N} queries; time scaled to the whole workload")
+            f"{nrows} of {BH * m} landmark rows (top-k + shared value), route + joint "
+            f"attention of {nq} of {BH * N} queries; times scaled to the whole workload")
     return est, desc, threads, t_pool + t_rows + t_q
+
+
+def expert_traffic(workload):
+    """DRAM bytes per expert-stage launch from the committed ncu summary, or
+    None when missing or taken on a different kernel source."""
+    import hashlib
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    a, b = line.split(":", 1)
+                    kv[a.strip()] = b.strip()
+        with open(EXPERT_SOURCE, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if kv.get("source_sha256") != sha or kv.get("workload") != workload:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def count_launches(mita, w, dq, dk, dv, out, stream):
+    """Library kernels one forward launches (the library's own launch counter)."""
+    n0 = mita.kernel_launches()
+    mita.mita_forward(dq, dk, dv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=out, stream=stream)
+    return mita.kernel_launches() - n0
 
 
 # ---------------------------------------------------------------------------
@@ -189,8 +231,9 @@ def run_reference(args):
     w = W.WORKLOADS[args.workload]
     q, k, v = W.make_qkv(w, 0)
     per = []
+    budget = max(2.0, min(15.0, 150.0 / (args.warmup + args.steps)))
     for i in range(args.warmup + args.steps):
-        est, desc, threads, spent = oracle_sample_time(w, q, k, v, rows=8, queries=2048, seed=i)
+        est, desc, threads, spent = oracle_sample_time(w, q, k, v, budget=budget, seed=i)
         if i >= args.warmup:
             per.append(est)
     est = statistics.median(per)
@@ -277,6 +320,7 @@ def bench_workload(mita, w, args, dev, stream, n_gpus, do_e2e=True):
     res["value"] = n_gpus * w.queries * args.steps / secs
     res["ms_per_step"] = secs / args.steps * 1e3
     res["stages"] = stage_times(mita, w, dq, dk, dv, max(3, min(args.steps, 10)), stream)
+    res["launches"] = count_launches(mita, w, dq, dk, dv, out, stream)
     if do_e2e:
         hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
         hout = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
@@ -319,12 +363,27 @@ def roofline_entry(w, stages, pk):
     ent["frac"] = ent["achieved"] / ent["peak"]
     ent["kernel"] = name
     ent["peak_source"] = pk["src"]
-    ent["traffic"] = None
+    ent["traffic"] = expert_traffic(w.name) if name == "expert" else None
     per = {}
     for s, tt in stages.items():
         rl = roofline_s(*work[s], pk)
         per[s] = {"ms": tt * 1e3, "roofline_ms": rl * 1e3, "frac": rl / tt if tt > 0 else None}
     return ent, per
+
+
+def forward_only(args):
+    from sparse_top_landmark_gb300 import build, mita
+    build.build()
+    w = W.WORKLOADS[args.workload]
+    q, k, v = W.make_qkv(w, 0)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    out = torch.empty_like(dq)
+    for _ in range(args.forward_only):
+        mita.mita_forward(dq, dk, dv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=out)
+    torch.cuda.synchronize()
+    print(json.dumps({"forward_only": w.name, "runs": args.forward_only,
+                      "device_error": mita.get_last_device_error()}))
+    return 0
 
 
 def main():
@@ -336,10 +395,14 @@ def main():
     ap.add_argument("--workload", default="long_1m", choices=list(W.WORKLOADS))
     ap.add_argument("--secondary", default="long_64k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--forward-only", type=int, default=0, metavar="R",
+                    help="run R untimed forwards of --workload and exit (for profilers)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return run_reference(args)
+    if args.forward_only > 0:
+        return forward_only(args)
 
     ws, rank, local = dist_env()
     n_gpus = max(ws, 1)
@@ -361,7 +424,7 @@ def main():
     main_res = bench_workload(mita, w, args, dev, stream, n_gpus)
     roof, per_stage = roofline_entry(w, main_res["stages"], pk)
     sec = None
-    if args.secondary and args.secondary != args.workload:
+    if args.secondary and args.secondary not in ("none", args.workload):
         w2 = W.WORKLOADS[args.secondary]
         r2 = bench_workload(mita, w2, args, dev, stream, n_gpus, do_e2e=False)
         roof2, per2 = roofline_entry(w2, r2["stages"], pk)
@@ -385,7 +448,8 @@ def main():
             "config": config_of(w, n_gpus),
             "clocks": main_res["clocks"],
             "e2e": main_res["e2e"],
-            "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+            "gpu_launches": (main_res["launches"] * args.steps
+                             if main_res["launches"] is not None else None),
             "roofline": roof,
             "forward_roofline_frac": total_rl / (main_res["ms_per_step"] / 1e3),
             "stages": per_stage,

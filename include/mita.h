@@ -213,6 +213,14 @@ int mita_get_last_device_error(mita_stream_t stream, int* bits);
 /* Frees every cached workspace (synchronises each owning device first). */
 int mita_workspace_release(void);
 
+/*
+ * Number of kernel launches this library has issued in this process so far
+ * (all devices, all threads; a launch counts when it is enqueued).  The
+ * difference of two readings around a section of host code is the number of
+ * library kernels that section launched.  Never fails.
+ */
+uint64_t mita_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

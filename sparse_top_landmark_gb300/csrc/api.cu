@@ -2,6 +2,7 @@
 // orchestration.  Every arithmetic step runs in the kernels of this library.
 #include "mita.h"
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <map>
@@ -368,6 +369,11 @@ int report_error(int code, const char* text) { return fail(code, "%s", text); }
 
 using mita::bf16;
 
+namespace mita {
+std::atomic<unsigned long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace mita
+
 extern "C" {
 
 int mita_pool(const void* q, int B, int H, int N, int d, int grid_h, int grid_w, int m,
@@ -485,6 +491,8 @@ int mita_get_last_device_error(mita_stream_t stream, int* bits) {
   if (bits) *bits = v;
   return v ? mita::fail(MITA_ERR_DEVICE_CHECK, "device status bits 0x%x", v) : MITA_OK;
 }
+
+uint64_t mita_kernel_launches(void) { return mita::g_launches.load(std::memory_order_relaxed); }
 
 int mita_workspace_release(void) {
   std::lock_guard<std::mutex> lk(mita::g_mu);

@@ -216,17 +216,21 @@ cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* 
     if (e != cudaSuccess) return e;
   }
   bucket_count_kernel<<<blocks, 256, s1, st>>>(route_idx, N, m, nchunks, hist, status);
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long BHm = (long long)BH * m;
   bucket_scan_kernel<<<(unsigned)((BHm + kWarps - 1) / kWarps), 256, 0, st>>>(BHm, nchunks, hist,
                                                                                total);
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (!smem) {
     bucket_offsets_kernel<<<BH, 256, 0, st>>>(total, m, bucket_off);
+    count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   bucket_scatter_kernel<<<blocks, 256, s3, st>>>(route_idx, N, m, nchunks, hist, total, bucket_off,
                                                  bucket_qidx, status);
+  count_launch();
   return cudaGetLastError();
 }
 

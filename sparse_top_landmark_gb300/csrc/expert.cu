@@ -184,6 +184,7 @@ cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt
   const long long blocks = (long long)BH * tiles;
   expert_attn_kernel<T, D><<<(unsigned)blocks, kQTile, 0, st>>>(
       q, k, v, qt, vt, ti, off, qidx, lse, so, N, m, topk, tiles, out, status);
+  count_launch();
   return cudaGetLastError();
 }
 

@@ -412,8 +412,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       const int nvalid = c < nrc ? min(BN, topk - c * BN) : min(BN, m - (c - nrc) * BN);
       float v[BN];
       if (ok) {
-#pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tS + cc * 32, v + cc * 32);
+        tmem_ld64(tS, v);
+        tmem_ld64(tS + 64, v + 64);
         tmem_ld_wait();
       }
       tc_fence_before();
@@ -514,9 +514,11 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
                                                 (long long)std::max(num_sms, 1) * 8);
   expert_gather_kernel<<<(unsigned)gblocks, kGatherThreads, 0, st>>>(k, v, topk_idx, rows, N, m,
                                                                       topk, w.kg, w.vg, status);
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   expert_prep_kernel<<<1, 1024, 0, st>>>(bucket_off, v_tilde, BH, N, m, w, status);
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   CUtensorMap mqg, mkg, mvg, mqt, mvt;
   if (!make_tmap_gather64(&mqg, q, (uint64_t)BH * N) ||
@@ -531,6 +533,7 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   expert_tc_kernel<<<(unsigned)std::max(num_sms, 1), kThreads, smem, st>>>(
       mqg, mkg, mvg, mqt, mvt, bucket_qidx, w.unit_start + (size_t)BH * m, w.unit, BH, N, m, topk,
       out, status);
+  count_launch();
   return cudaGetLastError();
 }
 

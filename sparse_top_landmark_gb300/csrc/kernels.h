@@ -111,6 +111,10 @@ cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
 
 int num_sms_of_current_device();
 
+// Records one kernel launch by this library (process-wide counter behind
+// mita_kernel_launches()).
+void count_launch();
+
 // Records `text` as the message mita_last_error_message() returns on this
 // thread and returns `code`.
 int report_error(int code, const char* text);

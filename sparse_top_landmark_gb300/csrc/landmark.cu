@@ -443,6 +443,7 @@ cudaError_t run_partial(const T* qt, const T* k, const T* v, int BH, int N, int 
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)BH * p.nrt * p.S;
   kern<<<(unsigned)blocks, RT, smem, st>>>(qt, k, v, N, m, p.S, p.split_len, p.Tcap, ws);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -462,8 +463,10 @@ cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int t
       if (e != cudaSuccess) return e;
       sk<<<(unsigned)((long long)BH * m), 256, ssmem, st>>>(qt, k, N, m, topk, p.cap, p.P, ws,
                                                             topk_idx);
+      count_launch();
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       landmark_exact_kernel<T, D><<<kExactCtas, 512, 0, st>>>(qt, k, N, m, topk, ws, topk_idx);
+      count_launch();
       return cudaGetLastError();
     }
   }
@@ -480,8 +483,10 @@ cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int t
   if (e != cudaSuccess) return e;
   mk<<<(unsigned)((long long)BH * m), 256, msmem, st>>>(qt, k, N, m, topk, p.S, p.Tcap, p.P,
                                                         ws, topk_idx, vt);
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   landmark_exact_kernel<T, D><<<kExactCtas, 512, 0, st>>>(qt, k, N, m, topk, ws, topk_idx);
+  count_launch();
   return cudaGetLastError();
 }
 

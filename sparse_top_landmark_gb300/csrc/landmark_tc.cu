@@ -277,8 +277,8 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       const bool full = nvalid == BN;
       float v[BN];
       if (ok) {
-#pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tS + cc * 32, v + cc * 32);
+        tmem_ld64(tS, v);
+        tmem_ld64(tS + 64, v + 64);
         tmem_ld_wait();
       }
       tc_fence_before();
@@ -573,8 +573,8 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
       const int nvalid = min(BN, j1 - kbase);
       float vv[BN];
       if (ok) {
-#pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tS + cc * 32, vv + cc * 32);
+        tmem_ld64(tS, vv);
+        tmem_ld64(tS + 64, vv + 64);
         tmem_ld_wait();
       }
       tc_fence_before();
@@ -675,6 +675,7 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
                                        (int)sm1);
   if (e != cudaSuccess) return e;
   lm_sweep_kernel<<<blocks, kThreads, sm1, st>>>(mqt, mk, mv, N, m, p.S, p.split_len, ws, status);
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int P = 2 * p.S * kTopTiles;
   const size_t tsm = (size_t)P * 4;
@@ -683,12 +684,14 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
   if (e != cudaSuccess) return e;
   lm_threshold_kernel<<<(unsigned)((long long)BH * m), 256, tsm, st>>>(q_tilde, m, topk, 2 * p.S,
                                                                        p.S, P, ws, v_tilde);
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t sm2 = sizeof(CollectSmem) + 1024;
   e = cudaFuncSetAttribute(lm_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
   if (e != cudaSuccess) return e;
   lm_collect_kernel<<<blocks, kThreads, sm2, st>>>(mqt, mk, N, m, p.S, p.split_len, p.cap, ws,
                                                    status);
+  count_launch();
   return cudaGetLastError();
 }
 

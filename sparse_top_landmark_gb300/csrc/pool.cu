@@ -95,6 +95,7 @@ cudaError_t run(const T* q, int BH, int N, int grid_h, int grid_w, int m, T* qt,
   }
   const long long blocks = (long long)BH * m;
   pool_kernel<T, D><<<(unsigned)blocks, kPoolThreads, 0, st>>>(q, N, grid_h, grid_w, mh, mw, qt);
+  count_launch();
   return cudaGetLastError();
 }
 

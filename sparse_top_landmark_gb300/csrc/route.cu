@@ -135,6 +135,7 @@ cudaError_t run(const T* q, const T* qt, const float* vt, int BH, int N, int m, 
   const long long nqt = (N + kRouteThreads - 1) / kRouteThreads;
   route_kernel<T, D><<<(unsigned)(BH * nqt), kRouteThreads, 0, st>>>(q, qt, vt, N, m, route,
                                                                       lse, o);
+  count_launch();
   return cudaGetLastError();
 }
 

@@ -458,6 +458,7 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   }
   route_tc_kernel<<<(unsigned)(BH * G_h), kThreads, smem, st>>>(mq, mqt, N, m, W, nch, G_h, cols,
                                                                  route, amb, status);
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int per_head = std::max(1, std::max(num_sms, 1) / BH);
   const size_t fsm = (size_t)m * kFixRow * 2;
@@ -465,6 +466,7 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   if (e != cudaSuccess) return e;
   route_fixup_kernel<<<(unsigned)(BH * per_head), 256, fsm, st>>>(q, q_tilde, N, m, per_head, amb,
                                                                  route);
+  count_launch();
   return cudaGetLastError();
 }
 

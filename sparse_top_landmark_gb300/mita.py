@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
             lib.mita_get_last_device_error.restype = I
             lib.mita_workspace_release.argtypes = []
             lib.mita_workspace_release.restype = I
+            lib.mita_kernel_launches.argtypes = []
+            lib.mita_kernel_launches.restype = ctypes.c_uint64
             _lib = lib
     return _lib
 
@@ -271,3 +273,8 @@ def get_last_device_error(stream=None, device=None) -> int:
 
 def workspace_release() -> None:
     _check(load().mita_workspace_release())
+
+
+def kernel_launches() -> int:
+    """Kernel launches this library has issued in this process so far."""
+    return int(load().mita_kernel_launches())

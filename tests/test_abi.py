@@ -97,3 +97,9 @@ def test_workspace_bytes_query(lib):
     n = lib.mita_forward_workspace_bytes(4, 2, 65536, 64, 128, 128, 0)
     assert n > 4 * 2 * 65536 * 8        # at least the route + bucket arrays
     assert lib.mita_forward_workspace_bytes(1, 1, 64, 48, 4, 4, 0) == 0
+
+
+def test_launch_counter_is_readable_without_a_gpu(lib):
+    lib.mita_kernel_launches.restype = ctypes.c_uint64
+    a = lib.mita_kernel_launches()
+    assert lib.mita_kernel_launches() == a      # nothing launched in between

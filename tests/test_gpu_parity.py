@@ -182,9 +182,14 @@ def test_forward_host_buffers_match_device_path():
 def test_forward_is_deterministic():
     mita = M()
     w, q, k, v = inputs("long_64k")
+    n0 = mita.kernel_launches()
     a = mita.mita_forward(dev(q), dev(k), dev(v), w.grid_h, w.grid_w, w.m, w.topk)
+    n1 = mita.kernel_launches()
     b = mita.mita_forward(dev(q), dev(k), dev(v), w.grid_h, w.grid_w, w.m, w.topk)
+    n2 = mita.kernel_launches()
     assert torch.equal(a, b)
+    # the library's own kernels run the forward, the same set each time
+    assert n1 - n0 == n2 - n1 >= 10
 
 
 # ----------------------------------------------------------------------------
