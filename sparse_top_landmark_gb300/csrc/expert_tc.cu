@@ -228,11 +228,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
   const uint32_t tbase = s.tmem;
   // tensor memory, query tile t at 256*t: S (128 columns), P (64, bf16 / fp16 pairs), O (64)
 
-  // registers: the launch grants 384 x 168; warps 0-3 keep 56 each, the two softmax
-  // warpgroups take 224 each (128*56 + 2*128*224 = 384*168), via setmaxnreg in each role
+  // registers: the launch grants 384 x 168; warps 0-3 keep 40 each, the two softmax
+  // warpgroups take 232 each (128*40 + 2*128*232 = 384*168), via setmaxnreg in each role
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory");
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       bool ok = true;
@@ -343,7 +343,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int slot = (warp - 4) >> 2;
     const int quad = warp & 3;             // tensor-memory lanes this warp may access
@@ -423,9 +423,13 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
 #pragma unroll
         for (int i = 0; i < BN; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
       }
-      float tm = -INFINITY;
+      // row maximum with four independent chains
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < BN; i += 2) tm = max3(tm, v[i], v[i + 1]);
+      for (int i = 0; i < BN; i += 8)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
+      const float tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       const float xm = tm * cs;
       const bool need = (c == 0) || (xm > mref + kLazy);
       const float f = (c > 0 && need) ? ex2(mref - xm) : 1.f;
@@ -435,15 +439,18 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       }
       const bool fp16 = c >= nrc;
       const float nm = -mref;
-      float ls = 0.f;
+      // P = 2^(s * cs - mref); row sum in two independent chains
+      float lsa = 0.f, lsb = 0.f;
+      auto pexp = [&](int i, uint32_t& packed) {
+        const float p0 = ex2(fmaf(v[i], cs, nm)), p1 = ex2(fmaf(v[i + 1], cs, nm));
+        if ((i >> 1) & 1) lsb += p0 + p1;
+        else lsa += p0 + p1;
+        packed = pack_pair(p0, p1, fp16);
+      };
       // first half of P while the previous P . V may still run
       uint32_t pk0[BN / 4];
 #pragma unroll
-      for (int i = 0; i < BN / 2; i += 2) {
-        const float p0 = ex2(fmaf(v[i], cs, nm)), p1 = ex2(fmaf(v[i + 1], cs, nm));
-        ls += p0 + p1;
-        pk0[i / 2] = pack_pair(p0, p1, fp16);
-      }
+      for (int i = 0; i < BN / 2; i += 2) pexp(i, pk0[i / 2]);
       // the previous P . V must have read P and finished with O
       if (g > 0 && ok && !mbar_wait(&s.pv_done[slot], (g - 1) & 1)) ok = false;
       tc_fence_after();
@@ -455,14 +462,10 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       }
       uint32_t pk1[BN / 4];
 #pragma unroll
-      for (int i = 0; i < BN / 2; i += 2) {
-        const float p0 = ex2(fmaf(v[BN / 2 + i], cs, nm)), p1 = ex2(fmaf(v[BN / 2 + i + 1], cs, nm));
-        ls += p0 + p1;
-        pk1[i / 2] = pack_pair(p0, p1, fp16);
-      }
+      for (int i = 0; i < BN / 2; i += 2) pexp(BN / 2 + i, pk1[i / 2]);
       tmem_st16(tP + 32, pk1);
       tmem_st16(tP + 48, pk1 + 16);
-      lsum += ls;
+      lsum += lsa + lsb;
       if (c > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int h = 0; h < 4; ++h) {

@@ -289,9 +289,12 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
         for (int i = 0; i < BN; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
       }
       // the tile's largest raw score
-      float tm = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four independent chains
 #pragma unroll
-      for (int i = 0; i < BN; i += 2) tm = max3(tm, v[i], v[i + 1]);
+      for (int i = 0; i < BN; i += 8)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
+      const float tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       // keep the kTopTiles largest tile maxima of this slot (min-heap, root = smallest)
       if (tm > theta) {
         float* hp = &s.top[slot][0][row];
@@ -322,14 +325,15 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       // P = exp2(s * c - mref) as bf16 pairs; the first half before waiting for the
       // previous P . V of this slot (which still reads P and accumulates O)
       const unsigned long long c2 = f2pack(c, c), nm2 = f2pack(-mref, -mref);
-      unsigned long long ls2 = f2pack(0.f, 0.f);
+      unsigned long long ls2 = f2pack(0.f, 0.f), ls3 = ls2;   // two independent sum chains
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int i = 0; i < BN / 2; i += 2) {
         float x0, x1;
         f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, nm2), x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
-        ls2 = add2(ls2, f2pack(p0, p1));
+        if ((i >> 1) & 1) ls3 = add2(ls3, f2pack(p0, p1));
+        else ls2 = add2(ls2, f2pack(p0, p1));
         pk[i / 2] = pack_bf16x2(p0, p1);
       }
       if (t > 0 && ok && !mbar_wait(&s.pv_done[slot], (t - 1) & 1)) ok = false;
@@ -341,14 +345,16 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
         float x0, x1;
         f2unpack(fma2(f2pack(v[i], v[i + 1]), c2, nm2), x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
-        ls2 = add2(ls2, f2pack(p0, p1));
+        if ((i >> 1) & 1) ls3 = add2(ls3, f2pack(p0, p1));
+        else ls2 = add2(ls2, f2pack(p0, p1));
         pk[i / 2] = pack_bf16x2(p0, p1);
       }
       tmem_st16(tP + 32, pk + 32);
       tmem_st16(tP + 48, pk + 48);
-      float ls_a, ls_b;
+      float ls_a, ls_b, ls_c, ls_d;
       f2unpack(ls2, ls_a, ls_b);
-      lsum += ls_a + ls_b;
+      f2unpack(ls3, ls_c, ls_d);
+      lsum += (ls_a + ls_b) + (ls_c + ls_d);
       if (t > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
