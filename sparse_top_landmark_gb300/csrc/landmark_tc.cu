@@ -459,8 +459,9 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, i
 // -------------------------------------------------------------------------------------------
 // pass 2: collect the keys at or above the threshold
 // -------------------------------------------------------------------------------------------
-constexpr int kKStages = 4;
-
+constexpr int kKStages = 6;
+constexpr int kCSlots = 4;                  // tile groups in flight (tensor-memory buffers)
+constexpr int kCThreads = (4 + 4 * kCSlots) * 32;
 constexpr int kLocalCand = 64;   // candidates per row buffered in shared memory
 
 struct alignas(1024) CollectSmem {
@@ -470,12 +471,16 @@ struct alignas(1024) CollectSmem {
   int ci[kLocalCand][128];
   int cn[128];
   uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t qt_full, drain[2];
-  uint64_t s_full[2], s_free[2];
+  uint64_t qt_full, drain;
+  uint64_t s_full[kCSlots], s_free[kCSlots];
   uint32_t tmem;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+// pass 2, CTA = (head, 128 landmarks, key split): warp 0 streams K tiles by TMA,
+// warp 1 issues S = q~ K^T for tile j into tensor-memory buffer j % 4, and four
+// epilogue warpgroups (one per buffer, one landmark row per thread) compare the
+// scores with the row's threshold and keep the keys at or above it.
+__global__ void __launch_bounds__(kCThreads, 1)
 lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constant__ CUtensorMap map_k,
                   int N, int m, int S, int split_len, int cap, LandmarkWs ws, int* status) {
   extern __shared__ unsigned char smem_raw[];
@@ -498,70 +503,73 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
       mbar_init(&s.k_empty[i], 1);
     }
     mbar_init(&s.qt_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.drain[i], 1);
+    mbar_init(&s.drain, 1);
+    for (int i = 0; i < kCSlots; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], 4);
     }
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&s.tmem, 256);
+    tmem_alloc(&s.tmem, 128 * kCSlots);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem;
+  // registers: the launch grants 640 x 96; warps 0-3 keep 40 each, the four epilogue
+  // warpgroups take 104 each (128*40 + 4*128*104 = 58368 <= 640*96)
 
-  if (warp == 0) {
-    bool ok = true;
-    if (elect_one()) {
-      prefetch_tmap(&map_qt);
-      prefetch_tmap(&map_k);
-      mbar_expect_tx(&s.qt_full, 128 * 128);
-      tma_load_3d(s.qt, &map_qt, &s.qt_full, 0, rt * 128, bh);
-    }
-    __syncwarp();
-    for (int j = 0; j < ntl; ++j) {
-      const int st = j % kKStages;
-      if (!mbar_wait_warp(&s.k_empty[st], ((j / kKStages) & 1) ^ 1)) { ok = false; break; }
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory");
+    if (warp == 0) {
+      bool ok = true;
       if (elect_one()) {
-        mbar_expect_tx(&s.k_full[st], BN * 128);
-        tma_load_3d(s.k[st], &map_k, &s.k_full[st], 0, j0 + j * BN, bh);
+        prefetch_tmap(&map_qt);
+        prefetch_tmap(&map_k);
+        mbar_expect_tx(&s.qt_full, 128 * 128);
+        tma_load_3d(s.qt, &map_qt, &s.qt_full, 0, rt * 128, bh);
       }
       __syncwarp();
-    }
-    if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
-  } else if (warp == 1 || warp == 2) {
-    // MMA issuer of tile group `slot` (tiles slot, slot + 2, ...): whole warp, one
-    // elected lane issues
-    const int slot = warp - 1;
-    const uint32_t id_s = idesc_f16(128, BN, false);
-    const uint32_t qa = smem_u32(s.qt);
-    bool ok = mbar_wait_warp(&s.qt_full, 0);
-    int t = 0;
-    for (int j = slot; j < ntl && ok; j += 2, ++t) {
-      const int st = j % kKStages;
-      if (!mbar_wait_warp(&s.k_full[st], (j / kKStages) & 1)) { ok = false; break; }
-      if (!mbar_wait_warp(&s.s_free[slot], (t & 1) ^ 1)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t kb = smem_u32(s.k[st]);
-      if (elect_one()) {
+      for (int j = 0; j < ntl; ++j) {
+        const int st = j % kKStages;
+        if (!mbar_wait_warp(&s.k_empty[st], ((j / kKStages) & 1) ^ 1)) { ok = false; break; }
+        if (elect_one()) {
+          mbar_expect_tx(&s.k_full[st], BN * 128);
+          tma_load_3d(s.k[st], &map_k, &s.k_full[st], 0, j0 + j * BN, bh);
+        }
+        __syncwarp();
+      }
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
+    } else if (warp == 1) {
+      // MMA issuer: whole warp, one elected lane issues
+      const uint32_t id_s = idesc_f16(128, BN, false);
+      const uint32_t qa = smem_u32(s.qt);
+      bool ok = mbar_wait_warp(&s.qt_full, 0);
+      for (int j = 0; j < ntl && ok; ++j) {
+        const int st = j % kKStages, slot = j % kCSlots, t = j / kCSlots;
+        if (!mbar_wait_warp(&s.k_full[st], (j / kKStages) & 1)) { ok = false; break; }
+        if (!mbar_wait_warp(&s.s_free[slot], (t & 1) ^ 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = smem_u32(s.k[st]);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tbase + slot * 128, smem_desc_sw128(qa + kk * 32, 1024),
-                 smem_desc_sw128(kb + kk * 32, 1024), id_s, kk > 0);
-        mma_commit(&s.s_full[slot]);
-        mma_commit(&s.k_empty[st]);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tbase + slot * 128, smem_desc_sw128(qa + kk * 32, 1024),
+                   smem_desc_sw128(kb + kk * 32, 1024), id_s, kk > 0);
+          mma_commit(&s.s_full[slot]);
+          mma_commit(&s.k_empty[st]);
+        }
+        __syncwarp();
       }
+      if (elect_one()) mma_commit(&s.drain);
       __syncwarp();
+      if (!mbar_wait_warp(&s.drain, 0)) ok = false;
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     }
-    if (elect_one()) mma_commit(&s.drain[slot]);
-    __syncwarp();
-    if (!mbar_wait_warp(&s.drain[slot], 0)) ok = false;
-    if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
-  } else if (warp >= 4) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 104;\n" ::: "memory");
     const int slot = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
@@ -572,45 +580,49 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
     const uint32_t tS = tbase + ((uint32_t)(quad * 32) << 16) + slot * 128;
     bool ok = true;
     int t = 0;
-    for (int j = slot; j < ntl; j += 2, ++t) {
+    for (int j = slot; j < ntl; j += kCSlots, ++t) {
       if (ok && !mbar_wait(&s.s_full[slot], t & 1)) ok = false;
       tc_fence_after();
       const int kbase = j0 + j * BN;
       const int nvalid = min(BN, j1 - kbase);
-      float vv[BN];
-      if (ok) {
-        tmem_ld64(tS, vv);
-        tmem_ld64(tS + 64, vv + 64);
-        tmem_ld_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.s_free[slot]);   // the next S may overwrite these columns
-      if (ok) {
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          const float* v = vv + cc * 32;
+      for (int h = 0; h < 2; ++h) {
+        float v[64];
+        if (ok) {
+          tmem_ld64(tS + h * 64, v);
+          tmem_ld_wait();
+        }
+        if (h == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.s_free[slot]);   // the next S may overwrite these columns
+        }
+        if (!ok) continue;
+#pragma unroll
+        for (int cc = 0; cc < 64; cc += 32) {
+          const float* vv = v + cc;
+          const int c0 = h * 64 + cc;
           // bitmask of the scores at or above the threshold (branch-free), then
           // visit only its set bits
           uint32_t msk = 0u;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) msk |= (v[i] >= thr ? 1u : 0u) << i;
-          if (nvalid - cc * 32 < 32) msk &= (nvalid - cc * 32 <= 0) ? 0u : (0xffffffffu >> (32 - (nvalid - cc * 32)));
+          for (int i = 0; i < 32; ++i) msk |= (vv[i] >= thr ? 1u : 0u) << i;
+          if (nvalid - c0 < 32) msk &= (nvalid - c0 <= 0) ? 0u : (0xffffffffu >> (32 - (nvalid - c0)));
           while (msk) {
             const int i = __ffs(msk) - 1;
             msk &= msk - 1;
-            float x = v[0];
+            float x = vv[0];
 #pragma unroll
-            for (int u = 1; u < 32; ++u) x = (u == i) ? v[u] : x;
+            for (int u = 1; u < 32; ++u) x = (u == i) ? vv[u] : x;
             const int pos = atomicAdd(&s.cn[row], 1);
             if (pos < kLocalCand) {
               s.cs[pos][row] = x;
-              s.ci[pos][row] = kbase + cc * 32 + i;
+              s.ci[pos][row] = kbase + c0 + i;
             } else {
               const int gpos = atomicAdd(ws.cnt + rf, 1);
               if (gpos < cap) {
                 ws.cand_s[rf * cap + gpos] = x;
-                ws.cand_i[rf * cap + gpos] = kbase + cc * 32 + i;
+                ws.cand_i[rf * cap + gpos] = kbase + c0 + i;
               }
             }
           }
@@ -622,7 +634,7 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tbase, 256);
+  if (warp == 1) tmem_dealloc(tbase, 128 * kCSlots);
   // flush the shared-memory candidate lists, one global reservation per row
   if (warp >= 4 && warp < 8) {
     const int row = (warp & 3) * 32 + lane;
@@ -695,7 +707,7 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
   const size_t sm2 = sizeof(CollectSmem) + 1024;
   e = cudaFuncSetAttribute(lm_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
   if (e != cudaSuccess) return e;
-  lm_collect_kernel<<<blocks, kThreads, sm2, st>>>(mqt, mk, N, m, p.S, p.split_len, p.cap, ws,
+  lm_collect_kernel<<<blocks, kCThreads, sm2, st>>>(mqt, mk, N, m, p.S, p.split_len, p.cap, ws,
                                                    status);
   count_launch();
   return cudaGetLastError();
