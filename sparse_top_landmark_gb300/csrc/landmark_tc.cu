@@ -602,6 +602,18 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
         for (int cc = 0; cc < 64; cc += 32) {
           const float* vv = v + cc;
           const int c0 = h * 64 + cc;
+          // most blocks of 32 hold no candidate for any row of the warp: screen with
+          // the block maximum (half an operation per score) before building the mask
+          float bm[4];
+#pragma unroll
+          for (int a = 0; a < 4; ++a) bm[a] = max3(vv[8 * a], vv[8 * a + 1], vv[8 * a + 2]);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) bm[a] = max3(bm[a], vv[8 * a + 3], vv[8 * a + 4]);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) bm[a] = max3(bm[a], vv[8 * a + 5], vv[8 * a + 6]);
+          const float bmax = fmaxf(max3(max3(bm[0], bm[1], bm[2]), max3(bm[3], vv[7], vv[15]), vv[23]),
+                                   vv[31]);
+          if (!__any_sync(0xffffffffu, bmax >= thr)) continue;
           // bitmask of the scores at or above the threshold (branch-free), then
           // visit only its set bits
           uint32_t msk = 0u;
