@@ -41,7 +41,7 @@ struct LandmarkWs {
   int* slow_rows;  // [BH * m]
   double* exact;   // [kExactCtas, N]  fp64 score scratch of the fallback
   // tensor-core path (M/L/A then hold 2 partials per split: one per softmax slot)
-  float* bm;       // [BH, m, 2S, 32]  largest tile maxima (raw scores) per split slot
+  float* bm;       // [BH*m, ntiles]  every key tile's maximum raw score per landmark
   float* thr;      // [BH, m]          collection threshold tau_L - 4E
   float* E;        // [BH, m]          fp32 score error bound
   int* cnt;        // [BH, m]          candidates collected
@@ -59,7 +59,6 @@ cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, in
                             int32_t* topk_idx, float* v_tilde, int* status, cudaStream_t st);
 
 bool landmark_tc_eligible(int d, int N, int topk);
-int landmark_tc_top_tiles();
 void plan_landmark_tc(LandmarkPlan& p, int BH, int N, int m, int topk, int num_sms);
 cudaError_t launch_landmark_tc_passes(const __nv_bfloat16* q_tilde, const __nv_bfloat16* k,
                                       const __nv_bfloat16* v, int BH, int N, int m, int topk,

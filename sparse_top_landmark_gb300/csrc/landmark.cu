@@ -526,7 +526,7 @@ size_t landmark_ws_bytes(const LandmarkPlan& p, int BH, int N, int d, int m) {
   add(4); add(rows * 4);
   add((size_t)kExactCtas * N * 8);
   if (p.tc) {
-    add(parts * landmark_tc_top_tiles() * 4);
+    add((size_t)p.ntiles * rows * 4);
     add(rows * 4); add(rows * 4); add(rows * 4);
     add(rows * p.cap * 4); add(rows * p.cap * 4);
   }
@@ -553,7 +553,7 @@ LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, i
   w.slow_rows = (int*)take(rows * 4);
   w.exact = (double*)take((size_t)kExactCtas * N * 8);
   if (p.tc) {
-    w.bm = (float*)take(parts * landmark_tc_top_tiles() * 4);
+    w.bm = (float*)take((size_t)p.ntiles * rows * 4);
     w.thr = (float*)take(rows * 4);
     w.E = (float*)take(rows * 4);
     w.cnt = (int*)take(rows * 4);

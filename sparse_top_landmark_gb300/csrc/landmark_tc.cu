@@ -42,19 +42,18 @@ namespace {
 using namespace sm100;
 
 constexpr int BN = 128;          // keys per tile
-constexpr int kStages = 4;       // K/V ring depth
+constexpr int kKRing = 6;        // sweep: K ring depth (K is freed as soon as S is computed)
+constexpr int kVRing = 4;        // sweep: V ring depth (V is held until P . V is done)
 constexpr int kThreads = 384;    // 12 warps
 constexpr float kLazy = 8.0f;    // rescale O only when the max grows by > 2^8
-constexpr int kTopTiles = 32;    // tile maxima kept per (landmark, split, slot)
 
 __device__ __forceinline__ float softmax_c() { return 0.18033688011112042f; }  // log2(e)/8
 
 struct alignas(1024) SweepSmem {
   bf16 qt[128 * 64];
-  bf16 k[kStages][BN * 64];
-  bf16 v[kStages][BN * 64];
-  float top[2][kTopTiles][128];    // per slot: min-heap of tile maxima, [entry][row]
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  bf16 k[kKRing][BN * 64];
+  bf16 v[kVRing][BN * 64];
+  uint64_t k_full[kKRing], k_empty[kKRing], v_full[kVRing], v_empty[kVRing];
   uint64_t qt_full, drain[2];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   float nred;
@@ -126,9 +125,13 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
   const int ntl = (j1 - j0 + BN - 1) / BN;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.kv_full[i], 1);
-      mbar_init(&s.kv_empty[i], 2);        // the tile's MMA commit + the norm warp
+    for (int i = 0; i < kKRing; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 2);         // the tile's S commit + the norm warp
+    }
+    for (int i = 0; i < kVRing; ++i) {
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_empty[i], 1);         // the tile's P . V commit
     }
     mbar_init(&s.qt_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -165,12 +168,11 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       }
       __syncwarp();
       for (int j = 0; j < ntl; ++j) {
-        const int st = j % kStages;
-        if (!mbar_wait_warp(&s.kv_empty[st], ((j / kStages) & 1) ^ 1)) { ok = false; break; }
+        const int st = j % kKRing;
+        if (!mbar_wait_warp(&s.k_empty[st], ((j / kKRing) & 1) ^ 1)) { ok = false; break; }
         if (elect_one()) {
-          mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
-          tma_load_3d(s.k[st], &map_k, &s.kv_full[st], 0, j0 + j * BN, bh);
-          tma_load_3d(s.v[st], &map_v, &s.kv_full[st], 0, j0 + j * BN, bh);
+          mbar_expect_tx(&s.k_full[st], BN * 128);
+          tma_load_3d(s.k[st], &map_k, &s.k_full[st], 0, j0 + j * BN, bh);
         }
         __syncwarp();
       }
@@ -185,8 +187,8 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       const uint32_t qa = smem_u32(s.qt);
       bool ok = mbar_wait_warp(&s.qt_full, 0);
       auto issue_s = [&](int j) -> bool {
-        const int st = j % kStages;
-        if (!mbar_wait_warp(&s.kv_full[st], (j / kStages) & 1)) return false;
+        const int st = j % kKRing;
+        if (!mbar_wait_warp(&s.k_full[st], (j / kKRing) & 1)) return false;
         tc_fence_after();
         const uint32_t kb = smem_u32(s.k[st]);
         if (elect_one()) {
@@ -195,6 +197,7 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
             mma_ss(tS, smem_desc_sw128(qa + kk * 32, 1024), smem_desc_sw128(kb + kk * 32, 1024),
                    id_s, kk > 0);
           mma_commit(&s.s_full[slot]);
+          mma_commit(&s.k_empty[st]);
         }
         __syncwarp();
         return true;
@@ -202,19 +205,20 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       if (ok && slot < ntl) ok = issue_s(slot);
       int t = 0;
       for (int j = slot; j < ntl && ok; j += 2, ++t) {
-        const int st = j % kStages;
+        const int st = j % kVRing;
         if (j + 2 < ntl) {
           if (!mbar_wait_warp(&s.s_free[slot], t & 1)) { ok = false; break; }
           if (!issue_s(j + 2)) { ok = false; break; }
         }
         if (!mbar_wait_warp(&s.p_full[slot], t & 1)) { ok = false; break; }
+        if (!mbar_wait_warp(&s.v_full[st], (j / kVRing) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t vb = smem_u32(s.v[st]);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts(tO, tP + kk * 8, smem_desc_sw128(vb + kk * 2048, 1024), id_pv, t > 0 || kk > 0);
-          mma_commit(&s.kv_empty[st]);
+          mma_commit(&s.v_empty[st]);
           mma_commit(&s.pv_done[slot]);
         }
         __syncwarp();
@@ -224,13 +228,27 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       if (!mbar_wait_warp(&s.drain[slot], 0)) ok = false;
       if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     } else {
+      // V producer (tile j into the V ring as soon as its slot is free), and the
       // largest |k| element of the split (bounds every key norm by 8 max|k|);
       // zero-filled rows past N are harmless
       uint32_t mx = 0u;
       bool ok = true;
+      int vj = 0;                       // next V tile to request
+      auto issue_v = [&](int upto) {
+        for (; vj < upto && vj < ntl && ok; ++vj) {
+          const int vs = vj % kVRing;
+          if (!mbar_wait_warp(&s.v_empty[vs], ((vj / kVRing) & 1) ^ 1)) { ok = false; break; }
+          if (elect_one()) {
+            mbar_expect_tx(&s.v_full[vs], BN * 128);
+            tma_load_3d(s.v[vs], &map_v, &s.v_full[vs], 0, j0 + vj * BN, bh);
+          }
+          __syncwarp();
+        }
+      };
+      issue_v(kVRing);
       for (int j = 0; j < ntl; ++j) {
-        const int st = j % kStages;
-        if (ok && !mbar_wait(&s.kv_full[st], (j / kStages) & 1)) ok = false;
+        const int st = j % kKRing;
+        if (ok && !mbar_wait(&s.k_full[st], (j / kKRing) & 1)) ok = false;
         if (ok) {
           const uint4* src = reinterpret_cast<const uint4*>(s.k[st]);
 #pragma unroll 8
@@ -243,8 +261,10 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.kv_empty[st]);
+        if (lane == 0) mbar_arrive(&s.k_empty[st]);
+        issue_v(j + kVRing + 1);
       }
+      issue_v(ntl);
       const float a = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
       const float km = warp_max(a);
       if (lane == 0) s.nred = 64.f * km * km;   // bound on |k|^2
@@ -264,8 +284,8 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
     float mref = -INFINITY, lsum = 0.f;
     bool ok = true;
     int t = 0;
-    for (int e = 0; e < kTopTiles; ++e) s.top[slot][e][row] = -INFINITY;
-    float theta = -INFINITY;
+    const size_t rf = (size_t)bh * m + grow;
+    float* tmax = ws.bm + rf * (size_t)((N + BN - 1) / BN) + j0 / BN;   // this split's tiles
     // the second group starts half a tile late, so the two take turns on the
     // exponential unit instead of competing for it in lockstep
     if (slot == 1) __nanosleep(500);
@@ -295,26 +315,9 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
 #pragma unroll
         for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
       const float tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      // keep the kTopTiles largest tile maxima of this slot (min-heap, root = smallest)
-      if (tm > theta) {
-        float* hp = &s.top[slot][0][row];
-        int pos = 0;
-        for (;;) {
-          const int ch = 2 * pos + 1;
-          if (ch >= kTopTiles) break;
-          float cv = hp[ch * 128];
-          int cix = ch;
-          if (ch + 1 < kTopTiles) {
-            const float cv2 = hp[(ch + 1) * 128];
-            if (cv2 < cv) { cv = cv2; cix = ch + 1; }
-          }
-          if (cv >= tm) break;
-          hp[pos * 128] = cv;
-          pos = cix;
-        }
-        hp[pos * 128] = tm;
-        theta = hp[0];
-      }
+      // every tile's maximum raw score goes out; the threshold pass takes the
+      // k-th largest of the row's
+      if (live_row) tmax[j] = tm;
       const float xm = tm * c;
       const bool need = (t == 0) || (xm > mref + kLazy);
       const float f = (t > 0 && need) ? ex2(mref - xm) : 1.f;
@@ -385,9 +388,6 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
     }
     if (live_row) {
       const size_t pidx = ((size_t)bh * m + grow) * (2 * S) + sp * 2 + slot;
-      float* tt = ws.bm + pidx * kTopTiles;
-#pragma unroll 8
-      for (int e = 0; e < kTopTiles; ++e) tt[e] = s.top[slot][e][row];
       ws.M[pidx] = mref;
       ws.L[pidx] = lsum;
       float4* dst = reinterpret_cast<float4*>(ws.A + pidx * 64);
@@ -405,17 +405,16 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
 
 // -------------------------------------------------------------------------------------------
 // threshold, one CTA per landmark: v~ from the partials; tau_L = the topk-th
-// largest of the kept tile maxima (each is the maximum of a distinct tile, so
+// largest of the row's tile maxima (each is the maximum of a distinct tile, so
 // at least topk keys score >= tau_L)
 // -------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
-lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, int S, int P,
-                    LandmarkWs ws, float* __restrict__ v_tilde) {
+lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, int S,
+                    int ntiles, LandmarkWs ws, float* __restrict__ v_tilde) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* val = reinterpret_cast<float*>(smem_raw);   // [P]
+  float* val = reinterpret_cast<float*>(smem_raw);   // [ntiles]
   __shared__ float red[8];
-  __shared__ int hist[256];
-  __shared__ int sh[4];
+  __shared__ int hist[8 * 256];
   const long long rf = blockIdx.x;
   const long long bh = rf / m;
   const int tid = threadIdx.x;
@@ -435,12 +434,12 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, i
     v_tilde[rf * 64 + tid] = num / den;
   }
   // ---- tau_L
-  const int n = S2 * kTopTiles;
-  const float* tops = ws.bm + base * kTopTiles;
-  for (int t = tid; t < n; t += 256) val[t] = tops[t];
+  const int n = ntiles;
+  const float* tm = ws.bm + (size_t)rf * ntiles;
+  for (int t = tid; t < n; t += 256) val[t] = tm[t];
   __syncthreads();
-  // -inf when fewer than topk tile maxima exist
-  const float tauL = n >= topk ? block_kth_largest(val, n, topk, hist, sh) : -INFINITY;
+  // at least topk tile maxima are >= tau_L (-inf when fewer than topk exist)
+  const float tauL = n >= topk ? block_kth_lower_bound(val, n, topk, hist, red) : -INFINITY;
   // ---- error bound
   float km = 0.f;
   for (int q = tid; q < S; q += 256) km = fmaxf(km, ws.kmax2[(size_t)bh * S + q]);
@@ -668,10 +667,11 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
 }  // namespace
 
 bool landmark_tc_eligible(int d, int N, int topk) {
-  return d == 64 && (N + BN - 1) / BN >= 2 * topk;
+  // the threshold pass holds one row's tile maxima in shared memory (<= 192 KB)
+  const long long ntiles = ((long long)N + BN - 1) / BN;
+  return d == 64 && ntiles >= 2LL * topk && ntiles <= 49152;
 }
 
-int landmark_tc_top_tiles() { return kTopTiles; }
 
 void plan_landmark_tc(LandmarkPlan& p, int BH, int N, int m, int topk, int num_sms) {
   p.tc = true;
@@ -679,8 +679,6 @@ void plan_landmark_tc(LandmarkPlan& p, int BH, int N, int m, int topk, int num_s
   p.nrt = (m + 127) / 128;
   const int ctas_per_split = BH * p.nrt;
   int S = std::max(1, (num_sms + ctas_per_split - 1) / ctas_per_split);
-  // at least 2*topk kept tile maxima per landmark (2 slots x kTopTiles per split)
-  S = std::max(S, (topk + kTopTiles - 1) / kTopTiles);
   S = std::min(S, (N + BN - 1) / BN);
   p.split_len = ((N + S - 1) / S + BN - 1) / BN * BN;
   p.S = (N + p.split_len - 1) / p.split_len;
@@ -707,13 +705,12 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
   lm_sweep_kernel<<<blocks, kThreads, sm1, st>>>(mqt, mk, mv, N, m, p.S, p.split_len, ws, status);
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int P = 2 * p.S * kTopTiles;
-  const size_t tsm = (size_t)P * 4;
+  const size_t tsm = (size_t)p.ntiles * 4;
   e = cudaFuncSetAttribute(lm_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tsm);
   if (e != cudaSuccess) return e;
   lm_threshold_kernel<<<(unsigned)((long long)BH * m), 256, tsm, st>>>(q_tilde, m, topk, 2 * p.S,
-                                                                       p.S, P, ws, v_tilde);
+                                                                       p.S, p.ntiles, ws, v_tilde);
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t sm2 = sizeof(CollectSmem) + 1024;
