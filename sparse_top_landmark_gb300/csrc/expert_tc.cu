@@ -30,6 +30,7 @@
 //                computed before waiting for the previous P . V), then O / l
 //                to the output rows.
 #include <algorithm>
+#include <type_traits>
 
 #include <cuda_fp16.h>
 
@@ -439,18 +440,25 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       }
       const bool fp16 = c >= nrc;
       const float nm = -mref;
-      // P = 2^(s * cs - mref); row sum in two independent chains
-      float lsa = 0.f, lsb = 0.f;
-      auto pexp = [&](int i, uint32_t& packed) {
-        const float p0 = ex2(fmaf(v[i], cs, nm)), p1 = ex2(fmaf(v[i + 1], cs, nm));
-        if ((i >> 1) & 1) lsb += p0 + p1;
-        else lsa += p0 + p1;
-        packed = pack_pair(p0, p1, fp16);
+      // P = 2^(s * cs - mref) in fp32 pairs, packed to the branch's type (the type is
+      // uniform per chunk, so each loop is specialised); row sum in two pair chains
+      const unsigned long long c2 = f2pack(cs, cs), nm2 = f2pack(nm, nm);
+      unsigned long long lsa = f2pack(0.f, 0.f), lsb = lsa;
+      auto exp_half = [&](auto is_fp16, int base, uint32_t* pk) {
+#pragma unroll
+        for (int i = 0; i < BN / 2; i += 2) {
+          float x0, x1;
+          f2unpack(fma2(f2pack(v[base + i], v[base + i + 1]), c2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          if ((i >> 1) & 1) lsb = add2(lsb, f2pack(p0, p1));
+          else lsa = add2(lsa, f2pack(p0, p1));
+          pk[i / 2] = pack_pair(p0, p1, decltype(is_fp16)::value);
+        }
       };
       // first half of P while the previous P . V may still run
       uint32_t pk0[BN / 4];
-#pragma unroll
-      for (int i = 0; i < BN / 2; i += 2) pexp(i, pk0[i / 2]);
+      if (fp16) exp_half(std::true_type{}, 0, pk0);
+      else exp_half(std::false_type{}, 0, pk0);
       // the previous P . V must have read P and finished with O
       if (g > 0 && ok && !mbar_wait(&s.pv_done[slot], (g - 1) & 1)) ok = false;
       tc_fence_after();
@@ -461,11 +469,14 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         pending = false;
       }
       uint32_t pk1[BN / 4];
-#pragma unroll
-      for (int i = 0; i < BN / 2; i += 2) pexp(BN / 2 + i, pk1[i / 2]);
+      if (fp16) exp_half(std::true_type{}, BN / 2, pk1);
+      else exp_half(std::false_type{}, BN / 2, pk1);
       tmem_st16(tP + 32, pk1);
       tmem_st16(tP + 48, pk1 + 16);
-      lsum += lsa + lsb;
+      float la0, la1, lb0, lb1;
+      f2unpack(lsa, la0, la1);
+      f2unpack(lsb, lb0, lb1);
+      lsum += (la0 + la1) + (lb0 + lb1);
       if (c > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
