@@ -49,6 +49,7 @@ struct alignas(1024) RouteSmem {
   uint64_t s_full[2], s_empty[2];
   // (drain: completion of the issuer's last products before tensor memory is freed)
   Cand cand[2][128];                   // half-1 partial results, by tile parity
+  float4 bbuf[256][8];                 // per epilogue thread: copy of its best 32-score block
   float red[kEpiWarps];
   float qtmax2;
   uint32_t tmem;
@@ -90,42 +91,52 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 struct RowTop {
   float v1 = -INFINITY, v2c = -INFINITY;
   int bb0 = 0;
-  float bb[32];
 };
 
-__device__ __forceinline__ void top_block(RowTop& t, const float* v, int i0, int nvalid) {
-  float x[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = v[i];
+// bb: this thread's 32-float block copy in shared memory, eight 16-byte chunks
+// stored at chunk c ^ sw (sw = thread % 8), so a warp's 16-byte accesses spread
+// over all banks.  The copy goes through shared memory (a few stores, only when
+// the block improves the best) instead of 32 register selects per block.
+__device__ __forceinline__ void top_block(RowTop& t, float* v, int i0, int nvalid, float4* bb,
+                                          int sw) {
   if (nvalid < 32) {                 // ragged last block (uniform across the warp)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = i < nvalid ? x[i] : -INFINITY;
+    for (int i = 0; i < 32; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
   }
   float a[11];
 #pragma unroll
-  for (int i = 0; i < 10; ++i) a[i] = max3f(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
-  a[10] = fmaxf(x[30], x[31]);
+  for (int i = 0; i < 10; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[10] = fmaxf(v[30], v[31]);
   const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]);
   const float b2 = max3f(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
   const float mb = fmaxf(max3f(b0, b1, b2), b3);
   const bool up = mb > t.v1;
   t.v2c = fmaxf(t.v2c, up ? t.v1 : mb);
   t.v1 = up ? mb : t.v1;
+  if (up) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) t.bb[i] = up ? x[i] : t.bb[i];
-  t.bb0 = up ? i0 : t.bb0;
+    for (int c = 0; c < 8; ++c)
+      bb[c ^ sw] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    t.bb0 = i0;
+  }
 }
 
 // (best, runner-up, lowest index of the best) of a finished row
-__device__ __forceinline__ Cand finish_top(const RowTop& t) {
+__device__ __forceinline__ Cand finish_top(const RowTop& t, const float4* bbs, int sw) {
   Cand c{t.v1, t.v2c, 0x7fffffff};
   if (t.v1 == -INFINITY) return c;
+  float bb[32];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 x = bbs[q ^ sw];
+    bb[4 * q] = x.x; bb[4 * q + 1] = x.y; bb[4 * q + 2] = x.z; bb[4 * q + 3] = x.w;
+  }
   int k = 31;
 #pragma unroll
-  for (int i = 31; i >= 0; --i) k = (t.bb[i] == t.v1) ? i : k;
+  for (int i = 31; i >= 0; --i) k = (bb[i] == t.v1) ? i : k;
   float s2 = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) s2 = (i == k) ? s2 : fmaxf(s2, t.bb[i]);
+  for (int i = 0; i < 32; ++i) s2 = (i == k) ? s2 : fmaxf(s2, bb[i]);
   c.v2 = fmaxf(c.v2, s2);
   c.i1 = t.bb0 + k;
   return c;
@@ -274,8 +285,6 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.q_empty[st]);   // this warp is done with the query tile
       RowTop top;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) top.bb[i] = -INFINITY;
       for (int ch = 0; ch < nch; ++ch, ++gch) {
         const int b = gch & 1;
         if (ok && !mbar_wait(&s.s_full[b], (gch >> 1) & 1)) ok = false;
@@ -308,12 +317,12 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           for (int cc = 0; cc < 128; cc += 32) {
             if (cc < cols_half) {
               const int i0 = ch * W + col0 + cc;
-              top_block(top, v + cc, i0, min(m - i0, cols_half - cc));
+              top_block(top, v + cc, i0, min(m - i0, cols_half - cc), s.bbuf[et], et & 7);
             }
           }
         }
       }
-      const Cand c = finish_top(top);
+      const Cand c = finish_top(top, s.bbuf[et], et & 7);
       if (half == 1) s.cand[it & 1][row] = c;
       quad_bar(quad);
       if (half == 0) {
