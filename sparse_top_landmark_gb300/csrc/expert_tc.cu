@@ -366,6 +366,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       tmem_ld32(tO, o);
       tmem_ld32(tO + 32, o + 32);
       tmem_ld_wait();
+      tmem_fence_regs<64>(o);
       if (ok && qi >= 0) {
         const float inv = 1.f / lsum;
         bf16* dst = out + ((size_t)bh * N + qi) * 64;
@@ -416,6 +417,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         tmem_ld64(tS, v);
         tmem_ld64(tS + 64, v + 64);
         tmem_ld_wait();
+        tmem_fence_regs<BN>(v);
       }
       tc_fence_before();
       __syncwarp();
@@ -483,6 +485,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
           float o[16];
           tmem_ld16(tO + h * 16, o);
           tmem_ld_wait();
+          tmem_fence_regs<16>(o);
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] *= f;
           tmem_st16(tO + h * 16, reinterpret_cast<uint32_t*>(o));

@@ -280,6 +280,7 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
         tmem_ld64(tS, v);
         tmem_ld64(tS + 64, v + 64);
         tmem_ld_wait();
+        tmem_fence_regs<BN>(v);
       }
       tc_fence_before();
       __syncwarp();
@@ -344,6 +345,7 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
           float o[16];
           tmem_ld16(tO + h * 16, o);
           tmem_ld_wait();
+          tmem_fence_regs<16>(o);
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] *= f;
           tmem_st16(tO + h * 16, reinterpret_cast<uint32_t*>(o));
@@ -362,6 +364,7 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       tmem_ld32(tO, o);
       tmem_ld32(tO + 32, o + 32);
       tmem_ld_wait();
+      tmem_fence_regs<64>(o);
     } else {
 #pragma unroll
       for (int i = 0; i < 64; ++i) o[i] = 0.f;
@@ -570,6 +573,7 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
         if (ok) {
           tmem_ld64(tS + h * 64, v);
           tmem_ld_wait();
+          tmem_fence_regs<64>(v);
         }
         if (h == 1) {
           tc_fence_before();

@@ -308,6 +308,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
               if (cc < cols_half) tmem_ld16(ta + cc, v + cc);
           }
           tmem_ld_wait();
+          tmem_fence_regs<128>(v);
         }
         tc_fence_before();
         __syncwarp();

@@ -198,6 +198,15 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
         "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr));
 }
+// tcgen05.ld fills its registers asynchronously, but to the compiler the asm
+// outputs are ready at once: it may move their uses above tcgen05.wait::ld.
+// After the wait, pass the loaded registers through this empty asm so every
+// use depends on something that is ordered after the wait.
+template <int N>
+__device__ __forceinline__ void tmem_fence_regs(float* v) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
