@@ -6,21 +6,25 @@
 //
 // One CTA owns a head's landmark block q~ (TMA, resident in shared memory)
 // and walks query tiles of 128 rows of that head:
-//   warp 0      TMA producer: query tiles into a 3-stage ring;
-//   warp 1      MMA issuer (whole warp, one elected lane issues): S = Q_tile .
-//               q~^T into tensor memory, in chunks of W <= 256 landmarks, two
-//               chunk buffers (ping-pong);
-//   warps 4-11  epilogue: TMEM lane quadrant = warp % 4 (one query row per
-//               thread), two warps per quadrant split each chunk's columns and
-//               meet on a 64-thread barrier per tile.
+//   warp 0       TMA producer: query tiles into a ring of kQStages;
+//   warp 1       MMA issuer (whole warp, one elected lane issues): S = Q_tile .
+//                q~^T into tensor memory, in chunks of W <= 128 landmarks;
+//   warps 4-19   epilogue, four groups of four warps; group g owns the tiles
+//                it = g, g + 4, ... and one W-column tensor-memory buffer; in a
+//                group, warp w serves TMEM lane quadrant w % 4, one query row per
+//                thread, whole rows (no partner to merge with).
+// The issuer walks the tiles in rounds of four (one per group) and, inside a
+// round, chunk by chunk over the four groups, so each group's next chunk is
+// computed while the group reads the previous one and the other three groups'
+// products keep the tensor pipe busy.
 // Each thread keeps, over blocks of 32 scores, the running best with a
-// register copy of the block holding it, and the maxima of all other blocks;
-// the exact best, runner-up and the best's index (lowest on ties) follow at
-// the end of the row.  When the best beats the runner-up by more than 2E (E bounds the fp32
-// dot error) it is the exact argmax; otherwise the query goes on its head's
-// "ambiguous" list and route_fixup_kernel re-routes it exactly (fp32
-// screening + exact-product re-scoring, ties to the lowest index) -- about
-// 0.2% of the queries on the long-sequence workloads.
+// shared-memory copy of the block holding it, and the maxima of all other
+// blocks; the exact best, runner-up and the best's index (lowest on ties)
+// follow at the end of the row.  When the best beats the runner-up by more
+// than 2E (E bounds the fp32 dot error) it is the exact argmax; otherwise the
+// query goes on its head's "ambiguous" list and route_fixup_kernel re-routes it
+// exactly (fp32 screening + exact-product re-scoring, ties to the lowest
+// index) -- about 0.2% of the queries on the long-sequence workloads.
 #include <algorithm>
 
 #include "common.cuh"
@@ -31,10 +35,13 @@ namespace mita {
 namespace {
 using namespace sm100;
 
-constexpr int kQStages = 3;
-constexpr int kEpiWarps = 8;
+constexpr int kQStages = 6;
+constexpr int kGroups = 4;
+constexpr int kEpiWarps = 4 * kGroups;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = (4 + kEpiWarps) * 32;
 constexpr int kMaxM = 512;
+constexpr int kMaxW = 128;
 
 struct Cand {
   float v1, v2;   // best and runner-up scores
@@ -44,22 +51,16 @@ struct Cand {
 struct alignas(1024) RouteSmem {
   bf16 qt[kMaxM * 64];                 // landmark rows, 128B-swizzled
   bf16 q[kQStages][128 * 64];          // query tiles, 128B-swizzled
+  float4 bbuf[kEpiThreads][8];         // per epilogue thread: copy of its best 32-score block
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t qt_full, drain;
-  uint64_t s_full[2], s_empty[2];
+  uint64_t s_full[kGroups], s_empty[kGroups];
   // (drain: completion of the issuer's last products before tensor memory is freed)
-  Cand cand[2][128];                   // half-1 partial results, by tile parity
-  float4 bbuf[256][8];                 // per epilogue thread: copy of its best 32-score block
   float red[kEpiWarps];
-  float qtmax2;
   uint32_t tmem;
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-// the two epilogue warps of one TMEM lane quadrant
-__device__ __forceinline__ void quad_bar(int quad) {
-  asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
-}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
 
 // Row r (128 bytes) of a 128B-swizzled bf16 tile -> 64 floats.
 __device__ __forceinline__ void load_swizzled_row(const bf16* tile, int r, float* out) {
@@ -121,7 +122,11 @@ __device__ __forceinline__ void top_block(RowTop& t, float* v, int i0, int nvali
   }
 }
 
-// (best, runner-up, lowest index of the best) of a finished row
+// (best, runner-up, lowest index of the best) of a finished row.  In the best
+// block: the entries equal to the best form a bit mask (its lowest bit is the
+// index, two or more bits make the runner-up equal to the best), and the
+// runner-up of the block is the largest entry below the best -- independent
+// comparisons and a max3 tree, no serial chain over the 32 entries.
 __device__ __forceinline__ Cand finish_top(const RowTop& t, const float4* bbs, int sw) {
   Cand c{t.v1, t.v2c, 0x7fffffff};
   if (t.v1 == -INFINITY) return c;
@@ -131,14 +136,22 @@ __device__ __forceinline__ Cand finish_top(const RowTop& t, const float4* bbs, i
     const float4 x = bbs[q ^ sw];
     bb[4 * q] = x.x; bb[4 * q + 1] = x.y; bb[4 * q + 2] = x.z; bb[4 * q + 3] = x.w;
   }
-  int k = 31;
+  uint32_t eq[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int i = 31; i >= 0; --i) k = (bb[i] == t.v1) ? i : k;
-  float s2 = -INFINITY;
+  for (int i = 0; i < 32; ++i) {
+    const bool e = bb[i] == t.v1;
+    eq[i & 3] |= e ? (1u << i) : 0u;
+    bb[i] = e ? -INFINITY : bb[i];
+  }
+  const uint32_t mask = (eq[0] | eq[1]) | (eq[2] | eq[3]);
+  float a[11];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) s2 = (i == k) ? s2 : fmaxf(s2, bb[i]);
-  c.v2 = fmaxf(c.v2, s2);
-  c.i1 = t.bb0 + k;
+  for (int i = 0; i < 10; ++i) a[i] = max3f(bb[3 * i], bb[3 * i + 1], bb[3 * i + 2]);
+  a[10] = fmaxf(bb[30], bb[31]);
+  const float s2 = fmaxf(max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), max3f(a[6], a[7], a[8])),
+                         fmaxf(a[9], a[10]));
+  c.v2 = (__popc(mask) > 1) ? t.v1 : fmaxf(c.v2, s2);
+  c.i1 = t.bb0 + (__ffs(mask) - 1);
   return c;
 }
 
@@ -158,13 +171,13 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQStages; ++i) {
       mbar_init(&s.q_full[i], 1);
-      mbar_init(&s.q_empty[i], 1 + kEpiWarps);
+      mbar_init(&s.q_empty[i], 1 + 4);   // the last chunk's MMA + the tile's four warps
     }
     mbar_init(&s.qt_full, 1);
     mbar_init(&s.drain, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s.s_full[b], 1);
-      mbar_init(&s.s_empty[b], kEpiWarps);
+    for (int g = 0; g < kGroups; ++g) {
+      mbar_init(&s.s_full[g], 1);
+      mbar_init(&s.s_empty[g], 4);
     }
     fence_mbar_init();
   }
@@ -177,8 +190,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   tc_fence_after();
   const uint32_t tbase = s.tmem;
 
-  // registers: the launch grants 384 x 168; warps 0-3 keep 56 each, the two epilogue
-  // warpgroups take 224 each (128*56 + 2*128*224 = 384*168)
+  // registers: the launch grants 640 x 96; warps 0-3 keep 56 each, the sixteen
+  // epilogue warps take 104 each (128*56 + 512*104 <= 640*96)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
     if (warp == 0) {
@@ -204,28 +217,32 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
+      // rounds of kGroups tiles; in a round, chunk by chunk over the groups
       const uint32_t idesc = idesc_f16(128, W, false);
       const uint32_t qtb = smem_u32(s.qt);
       bool ok = mbar_wait_warp(&s.qt_full, 0);
-      int gch = 0;
-      for (int it = 0; it < ntiles && ok; ++it) {
-        const int st = it % kQStages;
-        if (!mbar_wait_warp(&s.q_full[st], (it / kQStages) & 1)) { ok = false; break; }
-        const uint32_t qa = smem_u32(s.q[st]);
-        for (int ch = 0; ch < nch; ++ch, ++gch) {
-          const int b = gch & 1;
-          if (!mbar_wait_warp(&s.s_empty[b], ((gch >> 1) & 1) ^ 1)) { ok = false; break; }
-          tc_fence_after();
+      const int nrounds = (ntiles + kGroups - 1) / kGroups;
+      for (int r = 0; r < nrounds && ok; ++r) {
+        const int ng = min(kGroups, ntiles - r * kGroups);
+        for (int ch = 0; ch < nch && ok; ++ch) {
           const uint32_t qb = qtb + ch * W * 128;
-          if (elect_one()) {
+          const int u = r * nch + ch;                  // this buffer's use count
+          for (int g = 0; g < ng; ++g) {
+            const int it = r * kGroups + g, st = it % kQStages;
+            if (ch == 0 && !mbar_wait_warp(&s.q_full[st], (it / kQStages) & 1)) { ok = false; break; }
+            if (!mbar_wait_warp(&s.s_empty[g], (u & 1) ^ 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t qa = smem_u32(s.q[st]);
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tbase + b * W, smem_desc_sw128(qa + kk * 32, 1024),
-                     smem_desc_sw128(qb + kk * 32, 1024), idesc, kk > 0);
-            mma_commit(&s.s_full[b]);
-            if (ch == nch - 1) mma_commit(&s.q_empty[st]);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(tbase + g * W, smem_desc_sw128(qa + kk * 32, 1024),
+                       smem_desc_sw128(qb + kk * 32, 1024), idesc, kk > 0);
+              mma_commit(&s.s_full[g]);
+              if (ch == nch - 1) mma_commit(&s.q_empty[st]);
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       if (elect_one()) mma_commit(&s.drain);
@@ -234,42 +251,46 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 104;\n" ::: "memory");
     // ------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 128;              // 0..255
-    const int quad = warp & 3, half = (warp - 4) >> 2;
+    const int et = threadIdx.x - 128;              // 0..511
+    const int quad = warp & 3, grp = (warp - 4) >> 2;
     const int row = quad * 32 + lane;
-    const uint32_t taddr_lane = (uint32_t)(quad * 32) << 16;
+    const uint32_t tb = tbase + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * W);
+    float4* bb = s.bbuf[et];
+    const int sw = et & 7;
     bool ok = mbar_wait(&s.qt_full, 0);
     // largest landmark norm of the head (error bound)
     float n2max = 0.f;
     if (ok) {
-      for (int i = et; i < m; i += 256) {
+      for (int i = et; i < m; i += kEpiThreads) {
         float r[64];
         load_swizzled_row(s.qt, i, r);
-        float a = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int l = 0; l < 64; ++l) a = fmaf(r[l], r[l], a);
-        n2max = fmaxf(n2max, a);
+        for (int l = 0; l < 64; l += 2) {
+          a0 = fmaf(r[l], r[l], a0);
+          a1 = fmaf(r[l + 1], r[l + 1], a1);
+        }
+        n2max = fmaxf(n2max, a0 + a1);
       }
     }
     n2max = warp_max(n2max);
     if (lane == 0) s.red[warp - 4] = n2max;
     epi_bar();
     float qtmax2 = 0.f;
+#pragma unroll
     for (int i = 0; i < kEpiWarps; ++i) qtmax2 = fmaxf(qtmax2, s.red[i]);
-    const float gam = err_gamma(64);
-    const int cols_half = W / 2;                   // a multiple of 16, at most 128
+    const float gq = 2.f * err_gamma(64) * sqrtf(qtmax2);
     int* hamb = amb + (size_t)bh * (N + 1);
-    int gch = 0;
-    for (int it = 0; it < ntiles; ++it) {
-      const int st = it % kQStages;
+    for (int it = grp; it < ntiles; it += kGroups) {
+      const int st = it % kQStages, r = it / kGroups;
       if (ok && !mbar_wait(&s.q_full[st], (it / kQStages) & 1)) ok = false;
-      // the query's error bound first (half 0), while the scores are computed
       const int n = (c0 + it * G_h) * 128 + row;
       const bool live = ok && n < N;
+      // the query's error bound first, while the scores are computed
       float twoE = 0.f;
-      if (half == 0 && live) {
+      if (live) {
         float qr[64];
         load_swizzled_row(s.q[st], row, qr);
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -280,68 +301,54 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
           a2 = fmaf(qr[l + 2], qr[l + 2], a2);
           a3 = fmaf(qr[l + 3], qr[l + 3], a3);
         }
-        twoE = 2.f * gam * sqrtf((a0 + a1) + (a2 + a3)) * sqrtf(qtmax2);
+        twoE = gq * sqrtf((a0 + a1) + (a2 + a3));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.q_empty[st]);   // this warp is done with the query tile
       RowTop top;
-      for (int ch = 0; ch < nch; ++ch, ++gch) {
-        const int b = gch & 1;
-        if (ok && !mbar_wait(&s.s_full[b], (gch >> 1) & 1)) ok = false;
+      for (int ch = 0; ch < nch; ++ch) {
+        const int u = r * nch + ch;
+        if (ok && !mbar_wait(&s.s_full[grp], u & 1)) ok = false;
         tc_fence_after();
-        const int col0 = half * cols_half;
-        float v[128];
-        if (ok) {
-          const uint32_t ta = tbase + taddr_lane + (uint32_t)(b * W + col0);
-          if (cols_half >= 64) {
-            tmem_ld64(ta, v);
-          } else {
+        // W columns in pieces of 64: load, then two 32-score blocks
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 16)
-              if (cc < cols_half) tmem_ld16(ta + cc, v + cc);
-          }
-          if (cols_half >= 128) {
-            tmem_ld64(ta + 64, v + 64);
-          } else {
+        for (int p = 0; p < kMaxW / 64; ++p) {
+          if (p * 64 < W) {
+            float v[64];
+            if (ok) {
+              if (W - p * 64 >= 64) {
+                tmem_ld64(tb + p * 64, v);
+              } else {
+                tmem_ld32(tb + p * 64, v);
+              }
+              tmem_ld_wait();
+              tmem_fence_regs<64>(v);
+            }
+            if (p * 64 + 64 >= W) {                  // the buffer may be overwritten now
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&s.s_empty[grp]);
+            }
+            if (ok) {
 #pragma unroll
-            for (int cc = 64; cc < 128; cc += 16)
-              if (cc < cols_half) tmem_ld16(ta + cc, v + cc);
-          }
-          tmem_ld_wait();
-          tmem_fence_regs<128>(v);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.s_empty[b]);   // the buffer may be overwritten now
-        if (ok) {
-#pragma unroll
-          for (int cc = 0; cc < 128; cc += 32) {
-            if (cc < cols_half) {
-              const int i0 = ch * W + col0 + cc;
-              top_block(top, v + cc, i0, min(m - i0, cols_half - cc), s.bbuf[et], et & 7);
+              for (int cc = 0; cc < 64; cc += 32) {
+                const int i0 = ch * W + p * 64 + cc;
+                if (p * 64 + cc < W && i0 < m) top_block(top, v + cc, i0, min(m - i0, 32), bb, sw);
+              }
             }
           }
         }
       }
-      const Cand c = finish_top(top, s.bbuf[et], et & 7);
-      if (half == 1) s.cand[it & 1][row] = c;
-      quad_bar(quad);
-      if (half == 0) {
-        const Cand o = s.cand[it & 1][row];
-        const bool w1 = o.v1 > c.v1 || (o.v1 == c.v1 && o.i1 < c.i1);
-        const float v1 = w1 ? o.v1 : c.v1;
-        const int i1 = w1 ? o.i1 : c.i1;
-        const float v2 = max3f(c.v2, o.v2, fminf(c.v1, o.v1));
-        const bool ambiguous = live && !(v1 - v2 > twoE);
-        if (live) route[(size_t)bh * N + n] = i1;
-        // append ambiguous queries to the head's list (one reservation per warp)
-        const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
-        if (am) {
-          int base = 0;
-          if (lane == 0) base = atomicAdd(hamb, __popc(am));
-          base = __shfl_sync(0xffffffffu, base, 0);
-          if (ambiguous) hamb[1 + base + __popc(am & ((1u << lane) - 1u))] = n;
-        }
+      const Cand c = finish_top(top, bb, sw);
+      const bool ambiguous = live && !(c.v1 - c.v2 > twoE);
+      if (live) route[(size_t)bh * N + n] = c.i1;
+      // append ambiguous queries to the head's list (one reservation per warp)
+      const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
+      if (am) {
+        int base = 0;
+        if (lane == 0) base = atomicAdd(hamb, __popc(am));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (ambiguous) hamb[1 + base + __popc(am & ((1u << lane) - 1u))] = n;
       }
     }
     if (!ok) flag_error(status, kDevErrTimeout);
@@ -447,10 +454,12 @@ bool route_tc_supported(int d, int m) { return d == 64 && m >= 1 && m <= kMaxM; 
 
 cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, int m,
                             int num_sms, int32_t* route, int* amb, int* status, cudaStream_t st) {
-  const int W = std::min(256, (m + 31) / 32 * 32);
+  // chunk width: 32, 64 or 128 landmarks (a power of two, so the four group
+  // buffers fill a power-of-two tensor-memory allocation)
+  int W = 32;
+  while (W < kMaxW && W < m) W <<= 1;
   const int nch = (m + W - 1) / W;
-  uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * W)) cols <<= 1;
+  const uint32_t cols = (uint32_t)(kGroups * W);
   CUtensorMap mq, mqt;
   if (!make_tmap_rows64(&mq, q, (uint64_t)N, (uint64_t)BH, 128) ||
       !make_tmap_rows64(&mqt, q_tilde, (uint64_t)m, (uint64_t)BH, (uint32_t)W))
