@@ -16,8 +16,9 @@
  *     __nv_bfloat16); the `_f32` twins take float with the same parameters.
  *     Landmark values v~ and the optional shared-branch partial are float.
  *     Index outputs are int32.
- *   - Every pointer is a DEVICE pointer owned by the caller; the library never
- *     frees or retains it.  Element arrays must start on a 16-byte boundary.
+ *   - Every pointer is a DEVICE pointer owned by the caller (except the data
+ *     pointers of mita_forward_host*, which are host pointers); the library
+ *     never frees or retains it.  Element arrays must start on a 16-byte boundary.
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
  *     never synchronise the host.  Arguments are validated on the host before
  *     any launch; an invalid call launches nothing and returns non-zero.
@@ -192,6 +193,24 @@ int mita_forward(const void* q, const void* k, const void* v, int B, int H, int 
 int mita_forward_f32(const float* q, const float* k, const float* v, int B, int H, int N, int d,
                      int grid_h, int grid_w, int m, int topk, int s, float* out,
                      mita_stream_t stream);
+
+/*
+ * mita_forward_host -- mita_forward on HOST buffers (same method and
+ * parameters).  q, k, v [B,H,N,d] and out [B,H,N,d] are host pointers owned
+ * by the caller; page-locked memory (cudaHostAlloc) copies at full speed,
+ * pageable memory works but copies slower.  The call copies q, k, v to the
+ * current device (a library-owned staging cache, one per (device, stream),
+ * freed by mita_workspace_release), runs the forward on `stream`, copies the
+ * output back into `out` and synchronises `stream` before returning: `out`
+ * holds the result when the call returns MITA_OK.  Arguments are validated
+ * before any copy; on an error `out` is left unspecified.
+ */
+int mita_forward_host(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                      int grid_h, int grid_w, int m, int topk, int s, void* out,
+                      mita_stream_t stream);
+int mita_forward_host_f32(const float* q, const float* k, const float* v, int B, int H, int N,
+                          int d, int grid_h, int grid_w, int m, int topk, int s, float* out,
+                          mita_stream_t stream);
 
 /* Bytes of workspace mita_forward needs for this shape (0 if invalid). */
 uint64_t mita_forward_workspace_bytes(int B, int H, int N, int d, int m, int topk, int is_f32);

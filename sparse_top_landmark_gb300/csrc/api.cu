@@ -45,6 +45,7 @@ struct WsEntry {
   size_t bytes = 0;
 };
 std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws;
+std::map<std::pair<int, cudaStream_t>, WsEntry> g_stage;
 
 int device_state(DevState** out) {
   int dev = 0;
@@ -68,14 +69,17 @@ int device_state(DevState** out) {
   return MITA_OK;
 }
 
-int workspace(size_t bytes, cudaStream_t st, void** out) {
+// One buffer per (device, stream) in `cache`, grown (stream-ordered) when a
+// call needs more.
+int cached_buffer(std::map<std::pair<int, cudaStream_t>, WsEntry>& cache, const char* what,
+                  size_t bytes, cudaStream_t st, void** out) {
   *out = nullptr;
   if (bytes == 0) return MITA_OK;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   std::lock_guard<std::mutex> lk(g_mu);
-  WsEntry& w = g_ws[{dev, st}];
+  WsEntry& w = cache[{dev, st}];
   if (w.bytes >= bytes) {
     *out = w.ptr;
     return MITA_OK;
@@ -85,8 +89,8 @@ int workspace(size_t bytes, cudaStream_t st, void** out) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
   if (cs != cudaStreamCaptureStatusNone)
     return fail(MITA_ERR_UNSUPPORTED,
-                "workspace must grow to %zu bytes while the stream is capturing; make one "
-                "call of this size outside capture first", bytes);
+                "%s must grow to %zu bytes while the stream is capturing; make one "
+                "call of this size outside capture first", what, bytes);
   if (w.ptr) {
     e = cudaFreeAsync(w.ptr, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
@@ -98,12 +102,21 @@ int workspace(size_t bytes, cudaStream_t st, void** out) {
   e = cudaMallocAsync(&p, want, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return fail(MITA_ERR_OOM, "workspace of %zu bytes: %s", want, cudaGetErrorString(e));
+    return fail(MITA_ERR_OOM, "%s of %zu bytes: %s", what, want, cudaGetErrorString(e));
   }
   w.ptr = p;
   w.bytes = want;
   *out = p;
   return MITA_OK;
+}
+
+int workspace(size_t bytes, cudaStream_t st, void** out) {
+  return cached_buffer(g_ws, "workspace", bytes, st, out);
+}
+
+// device copies of the host-buffer forward's inputs and output
+int staging(size_t bytes, cudaStream_t st, void** out) {
+  return cached_buffer(g_stage, "staging buffer", bytes, st, out);
 }
 
 // ---------------------------------------------------------------------------
@@ -361,6 +374,35 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   return MITA_OK;
 }
 
+// The forward on host buffers: H2D copies of q, k, v into the staging cache,
+// the forward, the D2H copy of the output, then a synchronisation of `st`.
+template <typename T>
+int forward_host_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d, int gh,
+                      int gw, int m, int topk, int s, T* out, cudaStream_t st) {
+  MITA_TRY(check_shape(B, H, N, d));
+  MITA_TRY(check_m(N, m));
+  MITA_TRY(check_grid(N, gh, gw, m));
+  MITA_TRY(check_topk(N, topk));
+  MITA_TRY(check_s(m, s));
+  if (!q || !k || !v || !out) return fail(MITA_ERR_INVALID_ARG, "null host pointer");
+  const size_t n = (size_t)B * H * N * d;
+  const size_t bytes = align256(n * sizeof(T));
+  void* sv = nullptr;
+  MITA_TRY(staging(4 * bytes, st, &sv));
+  char* sb = static_cast<char*>(sv);
+  T* dq = reinterpret_cast<T*>(sb);
+  T* dk = reinterpret_cast<T*>(sb + bytes);
+  T* dv = reinterpret_cast<T*>(sb + 2 * bytes);
+  T* dout = reinterpret_cast<T*>(sb + 3 * bytes);
+  MITA_CUDA(cudaMemcpyAsync(dq, q, n * sizeof(T), cudaMemcpyHostToDevice, st), "copy of q");
+  MITA_CUDA(cudaMemcpyAsync(dk, k, n * sizeof(T), cudaMemcpyHostToDevice, st), "copy of k");
+  MITA_CUDA(cudaMemcpyAsync(dv, v, n * sizeof(T), cudaMemcpyHostToDevice, st), "copy of v");
+  MITA_TRY(forward_impl<T>(dq, dk, dv, B, H, N, d, gh, gw, m, topk, s, dout, st));
+  MITA_CUDA(cudaMemcpyAsync(out, dout, n * sizeof(T), cudaMemcpyDeviceToHost, st), "copy of out");
+  MITA_CUDA(cudaStreamSynchronize(st), "synchronisation");
+  return MITA_OK;
+}
+
 }  // namespace
 
 int report_error(int code, const char* text) { return fail(code, "%s", text); }
@@ -451,6 +493,20 @@ int mita_forward_f32(const float* q, const float* k, const float* v, int B, int 
   return mita::forward_impl<float>(q, k, v, B, H, N, d, grid_h, grid_w, m, topk, s, out, stream);
 }
 
+int mita_forward_host(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                      int grid_h, int grid_w, int m, int topk, int s, void* out,
+                      mita_stream_t stream) {
+  return mita::forward_host_impl<bf16>(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                       static_cast<const bf16*>(v), B, H, N, d, grid_h, grid_w,
+                                       m, topk, s, static_cast<bf16*>(out), stream);
+}
+int mita_forward_host_f32(const float* q, const float* k, const float* v, int B, int H, int N,
+                          int d, int grid_h, int grid_w, int m, int topk, int s, float* out,
+                          mita_stream_t stream) {
+  return mita::forward_host_impl<float>(q, k, v, B, H, N, d, grid_h, grid_w, m, topk, s, out,
+                                        stream);
+}
+
 uint64_t mita_forward_workspace_bytes(int B, int H, int N, int d, int m, int topk, int is_f32) {
   if (mita::check_shape(B, H, N, d) || mita::check_m(N, m) || mita::check_topk(N, topk))
     return 0;
@@ -498,14 +554,16 @@ int mita_workspace_release(void) {
   std::lock_guard<std::mutex> lk(mita::g_mu);
   int prev = 0;
   cudaGetDevice(&prev);
-  for (auto& kv : mita::g_ws) {
-    if (kv.second.ptr) {
-      cudaSetDevice(kv.first.first);
-      cudaDeviceSynchronize();
-      cudaFree(kv.second.ptr);
+  for (auto* cache : {&mita::g_ws, &mita::g_stage}) {
+    for (auto& kv : *cache) {
+      if (kv.second.ptr) {
+        cudaSetDevice(kv.first.first);
+        cudaDeviceSynchronize();
+        cudaFree(kv.second.ptr);
+      }
     }
+    cache->clear();
   }
-  mita::g_ws.clear();
   cudaSetDevice(prev);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MITA_OK : mita::cuda_fail(e, "workspace release");

@@ -51,6 +51,7 @@ def load() -> ctypes.CDLL:
                 "mita_route": [P, P, P, I, I, I, I, I, I, P, P, P, P],
                 "mita_expert_attn": [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
                 "mita_forward": [P, P, P, I, I, I, I, I, I, I, I, I, P, P],
+                "mita_forward_host": [P, P, P, I, I, I, I, I, I, I, I, I, P, P],
             }
             for name, at in sigs.items():
                 for suffix in ("", "_f32"):
@@ -229,21 +230,25 @@ def mita_forward(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int = 
     """The whole forward pass.
 
     Device tensors: runs on the GPU and returns the device output.  Host
-    tensors (ideally pinned): copies Q, K, V to `device` (default cuda:0),
-    runs, and copies the output back into `out` (or a new pinned tensor).
+    tensors (ideally pinned) go through the library's host entry point, which
+    copies Q, K, V to `device` (default cuda:0), runs, copies the output back
+    into `out` (or a new pinned tensor) and synchronises before returning.
     """
     if not q.is_cuda:
+        # host buffers: the library copies in, runs and copies out (one C call)
         dev = torch.device(device if device is not None else "cuda:0")
-        st = stream if stream is not None else torch.cuda.current_stream(dev)
+        for t, n in ((q, "q"), (k, "k"), (v, "v")):
+            if t.is_cuda or t.dtype != q.dtype or t.shape != q.shape or not t.is_contiguous():
+                raise ValueError(f"{n}: expected a contiguous host tensor like q")
         if out is None:
             out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
-        with torch.cuda.stream(st):
-            qd = q.to(dev, non_blocking=True)
-            kd = k.to(dev, non_blocking=True)
-            vd = v.to(dev, non_blocking=True)
-            od = mita_forward(qd, kd, vd, grid_h, grid_w, m, topk, s, stream=st)
-            out.copy_(od, non_blocking=True)
-        st.synchronize()
+        if out.is_cuda or out.dtype != q.dtype or out.shape != q.shape or not out.is_contiguous():
+            raise ValueError("out: expected a contiguous host tensor like q")
+        B, H, N, d = q.shape
+        with torch.cuda.device(dev):
+            _check(_fn("mita_forward_host", q.dtype)(
+                _ptr(q), _ptr(k), _ptr(v), B, H, N, d, grid_h, grid_w, m, topk, s, _ptr(out),
+                _stream(stream, dev)))
         return out
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, q.dtype, q.device)

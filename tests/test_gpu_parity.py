@@ -179,6 +179,17 @@ def test_forward_host_buffers_match_device_path():
     assert torch.equal(hout, dout.cpu())
 
 
+def test_forward_host_pageable_buffers_match_device_path():
+    mita = M()
+    w, q, k, v = inputs("seg_32x32")
+    dout = mita.mita_forward(dev(q), dev(k), dev(v), w.grid_h, w.grid_w, w.m, w.topk)
+    hout = torch.empty_like(q)                    # pageable, caller-owned
+    r = mita.mita_forward(q.contiguous(), k.contiguous(), v.contiguous(), w.grid_h, w.grid_w,
+                          w.m, w.topk, out=hout)
+    assert r is hout
+    assert torch.equal(hout, dout.cpu())
+
+
 def test_forward_is_deterministic():
     mita = M()
     w, q, k, v = inputs("long_64k")
