@@ -334,38 +334,151 @@ landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, in
 }
 
 // Candidates of the tensor-core path: the keys whose fp32 score reached the
-// row's collection threshold, gathered by the collect kernel.
+// row's collection threshold, gathered by the collect kernel (in no particular
+// order).  tau, the k-th largest fp32 score, comes from a radix select over
+// the order-preserving 32-bit keys (four 8-bit digits, most significant first,
+// warp-aggregated shared-memory histograms); the keys above tau + 2E are
+// members, the band [tau - 2E, tau + 2E] is re-scored exactly and ranked
+// (score desc, index asc), and the member indices are sorted ascending --
+// the same rule as finish_topk without sorting every candidate.
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 landmark_select_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, int N, int m,
                        int topk, int cap, int P, LandmarkWs ws, int32_t* __restrict__ topk_idx) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* us = reinterpret_cast<float*>(smem_raw);           // [P]
-  int* ui = reinterpret_cast<int*>(us + P);                 // [P]
-  F2* bx = reinterpret_cast<F2*>(ui + P);                   // [kBandCap]
+  float* us = reinterpret_cast<float*>(smem_raw);           // [cap]
+  int* ui = reinterpret_cast<int*>(us + cap);               // [cap]
+  F2* bx = reinterpret_cast<F2*>(ui + cap);                 // [kBandCap]
   int* bi = reinterpret_cast<int*>(bx + kBandCap);          // [kBandCap]
+  int* outset = bi + kBandCap;                              // [next_pow2(topk)]
   __shared__ float qd[D];
-  __shared__ int ired[9];
+  __shared__ int hist[256];
+  __shared__ int s_cnt[2];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  (void)P;
   const long long rowflat = blockIdx.x;
   const long long bh = rowflat / m;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int cnt = ws.cnt[rowflat];
   const int total = min(cnt, cap);
-  const bool slow = cnt > cap || cnt < topk;
+  if (cnt > cap || cnt < topk) {                             // to the exact fallback
+    if (tid == 0) ws.slow_rows[atomicAdd(ws.nslow, 1)] = (int)rowflat;
+    return;
+  }
   for (int l = tid; l < D; l += blockDim.x) qd[l] = to_f(q_tilde[rowflat * D + l]);
-  if (!slow) {
-    const float* cs = ws.cand_s + (size_t)rowflat * cap;
-    const int* ci = ws.cand_i + (size_t)rowflat * cap;
-    const int Ps = min(P, next_pow2(max(total, topk)));   // sort only what is there
-    for (int t = tid; t < Ps; t += blockDim.x) {
-      us[t] = t < total ? cs[t] : -INFINITY;
-      ui[t] = t < total ? ci[t] : 0x7fffffff;
+  const float* cs = ws.cand_s + (size_t)rowflat * cap;
+  const int* ci = ws.cand_i + (size_t)rowflat * cap;
+  for (int t = tid; t < total; t += blockDim.x) {
+    us[t] = cs[t];
+    ui[t] = ci[t];
+  }
+  if (tid == 0) {
+    s_prefix = 0u;
+    s_need = topk;
+    s_cnt[0] = 0;
+    s_cnt[1] = 0;
+  }
+  const int iters = (total + blockDim.x - 1) / blockDim.x;
+  // ---- tau: the k-th largest key, digit by digit
+  uint32_t mask = 0u;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    hist[tid] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix;
+    for (int j = 0; j < iters; ++j) {
+      const int t = j * blockDim.x + tid;
+      int dg = -1;
+      if (t < total) {
+        const uint32_t key = fkey(us[t]);
+        if ((key & mask) == prefix) dg = (int)((key >> shift) & 255u);
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, dg);
+      if (dg >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
     }
-    bitonic_sort_desc(us, ui, Ps);
+    __syncthreads();
+    if (tid < 32) {
+      // lane l holds digits 255 - 8l down to 248 - 8l; counts accumulate from the top
+      int c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[255 - 8 * lane - i];
+        sum += c[i];
+      }
+      int inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const int need = s_need, before = inc - sum;
+      if (before < need && inc >= need) {                    // exactly one lane
+        int run = before, dg = -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (dg < 0) {
+            if (run + c[i] >= need) dg = 255 - 8 * lane - i;
+            else run += c[i];
+          }
+        }
+        s_need = need - run;
+        s_prefix = prefix | ((uint32_t)dg << shift);
+      }
+    }
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  const float tau = fkey_inv(s_prefix);
+  const float E = ws.E[rowflat];
+  const float lo_band = tau - 2.f * E, hi_band = tau + 2.f * E;
+  // ---- members above the band, and the band (both unordered)
+  for (int j = 0; j < iters; ++j) {
+    const int t = j * blockDim.x + tid;
+    const float x = t < total ? us[t] : -INFINITY;
+    const int id = t < total ? ui[t] : 0;
+    const bool above = t < total && x > hi_band;
+    const bool inband = t < total && !above && x >= lo_band;
+    const unsigned ma = __ballot_sync(0xffffffffu, above), mb = __ballot_sync(0xffffffffu, inband);
+    int ba = 0, bb = 0;
+    if (lane == 0) {
+      if (ma) ba = atomicAdd(&s_cnt[0], __popc(ma));
+      if (mb) bb = atomicAdd(&s_cnt[1], __popc(mb));
+    }
+    ba = __shfl_sync(0xffffffffu, ba, 0);
+    bb = __shfl_sync(0xffffffffu, bb, 0);
+    const unsigned lt = (1u << lane) - 1u;
+    if (above) outset[ba + __popc(ma & lt)] = id;           // fewer than topk keys exceed tau
+    if (inband) {
+      const int pb = bb + __popc(mb & lt);
+      if (pb < kBandCap) bi[pb] = id;
+    }
   }
   __syncthreads();
-  finish_topk<T, D>(us, ui, total, topk, ws.E[rowflat], slow, qd, k + (size_t)bh * N * D, bx, bi,
-                    ired, rowflat, ws, topk_idx);
+  const int a = s_cnt[0], nb = s_cnt[1];
+  if (nb > kBandCap) {
+    if (tid == 0) ws.slow_rows[atomicAdd(ws.nslow, 1)] = (int)rowflat;
+    return;
+  }
+  // ---- exact re-scoring and ranking of the band
+  const T* kb = k + (size_t)bh * N * D;
+  const int PB = next_pow2(max(nb, 1));
+  for (int t = tid; t < PB; t += blockDim.x) {
+    if (t < nb) {
+      float kr[D];
+      load_row<T, D>(kb + (size_t)bi[t] * D, kr);
+      bx[t] = dot_f2<D>(qd, kr);
+    } else {
+      bx[t] = F2{-INFINITY, 0.f};
+      bi[t] = 0x7fffffff;
+    }
+  }
+  bitonic_sort_desc(bx, bi, PB);
+  // ---- the a members above the band plus the best (topk - a) of it, ascending
+  const int PK = next_pow2(topk);
+  for (int t = a + tid; t < PK; t += blockDim.x) outset[t] = t < topk ? bi[t - a] : 0x7fffffff;
+  bitonic_sort_int_asc(outset, PK);
+  for (int t = tid; t < topk; t += blockDim.x) topk_idx[rowflat * topk + t] = outset[t];
 }
 
 // Exact fallback: fp64 scores of all N keys, radix select on the monotone
@@ -457,7 +570,8 @@ cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int t
     if (p.tc) {
       e = launch_landmark_tc_passes(qt, k, v, BH, N, m, topk, p, ws, vt, status, st);
       if (e != cudaSuccess) return e;
-      const size_t ssmem = (size_t)p.P * 8 + (size_t)kBandCap * (sizeof(F2) + 4);
+      const size_t ssmem = (size_t)p.cap * 8 + (size_t)kBandCap * (sizeof(F2) + 4) +
+                           (size_t)next_pow2(topk) * 4;
       auto sk = landmark_select_kernel<T, D>;
       e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
       if (e != cudaSuccess) return e;
