@@ -306,68 +306,6 @@ __device__ inline void bitonic_sort_int_asc(int* a, int P) {
   __syncthreads();
 }
 
-// A lower bound on the k-th largest of the n floats at x (1 <= k <= n, -inf
-// entries allowed): the values are binned uniformly between their minimum and
-// maximum (256 bins, one histogram per warp), and the returned value is the
-// lower edge of the highest bin from which the count of values at or above
-// reaches k -- so at least k of the values are >= the result, and it lies
-// within one bin width (1/256 of the value range) of the exact k-th largest.
-// Whole block of nw <= 32 warps; `hist` holds nw*256 ints, `red` 32 floats.
-__device__ inline float block_kth_lower_bound(const float* x, int n, int k, int* hist, float* red) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
-  float lo = INFINITY, hi = -INFINITY;
-  for (int t = tid; t < n; t += blockDim.x) {
-    const float v = x[t];
-    hi = fmaxf(hi, v);
-    if (v > -INFINITY) lo = fminf(lo, v);
-  }
-  hi = block_max(hi, red);
-  lo = -block_max(-lo, red);
-  if (!(hi > lo)) return -INFINITY;   // all equal or none finite: no useful bound
-  const float scale = 256.f / (hi - lo);
-  for (int b = tid; b < nw * 256; b += blockDim.x) hist[b] = 0;
-  __syncthreads();
-  int* hw = hist + w * 256;
-  for (int t = tid; t < n; t += blockDim.x) {
-    const float v = x[t];
-    if (v > -INFINITY) atomicAdd(&hw[min(255, (int)((v - lo) * scale))], 1);
-  }
-  __syncthreads();
-  for (int b = tid; b < 256; b += blockDim.x) {
-    int c = 0;
-    for (int u = 0; u < nw; ++u) c += hist[u * 256 + b];
-    hist[b] = c;
-  }
-  __syncthreads();
-  __shared__ int bstar;
-  if (w == 0) {
-    // lane l owns bins 255-8l .. 248-8l (high to low)
-    int cnt[8], tot = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) { cnt[j] = hist[255 - 8 * lane - j]; tot += cnt[j]; }
-    const int inc = warp_incl_scan(tot);
-    const unsigned hit = __ballot_sync(0xffffffffu, inc >= k);
-    const int src = hit ? __ffs(hit) - 1 : 31;
-    if (lane == src) {
-      int cum = inc - tot, dg = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (cum + cnt[j] >= k) { dg = 255 - 8 * lane - j; break; }
-        cum += cnt[j];
-      }
-      bstar = dg;
-    }
-    if (lane == 0 && !hit) bstar = -1;   // fewer than k finite values
-  }
-  __syncthreads();
-  // values in bin b satisfy v >= lo + b / scale up to rounding; step one bin down
-  // so that the bound holds whatever the rounding of the bin index was
-  const int b = bstar;
-  __syncthreads();
-  if (b < 0) return -INFINITY;
-  return b > 0 ? lo + (float)(b - 1) / scale : lo;
-}
-
 __host__ __device__ __forceinline__ int next_pow2(int x) {
   int p = 1;
   while (p < x) p <<= 1;

@@ -394,47 +394,134 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
 __global__ void __launch_bounds__(256)
 lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, int S,
                     int ntiles, LandmarkWs ws, float* __restrict__ v_tilde) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* val = reinterpret_cast<float*>(smem_raw);   // [ntiles]
-  __shared__ float red[8];
-  __shared__ int hist[8 * 256];
+  __shared__ float red[8][5];
+  __shared__ int hist[8 * 256];               // one histogram per warp
+  __shared__ float vnum[4][64], vden[4];
   const long long rf = blockIdx.x;
   const long long bh = rf / m;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const size_t base = (size_t)rf * S2;
-  // ---- v~
-  float mx = -INFINITY;
+  const float* tm = ws.bm + (size_t)rf * ntiles;
+  const bool vec = (ntiles & 3) == 0;         // rows start on 16 bytes
+  // ---- one pass of reductions: the partials' maximum, the largest |k|^2, |q~|^2 and the
+  // range of the tile maxima
+  float mx = -INFINITY, km = 0.f, qn2 = 0.f, hi = -INFINITY, lo = INFINITY;
   for (int q = tid; q < S2; q += 256) mx = fmaxf(mx, ws.M[base + q]);
-  mx = block_max(mx, red);
+  for (int q = tid; q < S; q += 256) km = fmaxf(km, ws.kmax2[(size_t)bh * S + q]);
   if (tid < 64) {
-    float num = 0.f, den = 0.f;
-#pragma unroll 8
-    for (int q = 0; q < S2; ++q) {
-      const float w = exp2f(ws.M[base + q] - mx);
-      den = fmaf(w, ws.L[base + q], den);
-      num = fmaf(w, ws.A[(base + q) * 64 + tid], num);
+    const float x = __bfloat162float(q_tilde[rf * 64 + tid]);
+    qn2 = x * x;
+  }
+  auto range = [&](float v) {
+    hi = fmaxf(hi, v);
+    if (v > -INFINITY) lo = fminf(lo, v);
+  };
+  if (vec) {
+    for (int t = tid; t < ntiles / 4; t += 256) {
+      const float4 x = reinterpret_cast<const float4*>(tm)[t];
+      range(x.x); range(x.y); range(x.z); range(x.w);
     }
+  } else {
+    for (int t = tid; t < ntiles; t += 256) range(tm[t]);
+  }
+  mx = warp_max(mx);
+  km = warp_max(km);
+  qn2 = warp_sum(qn2);
+  hi = warp_max(hi);
+  lo = -warp_max(-lo);
+  if (lane == 0) {
+    red[w][0] = mx; red[w][1] = km; red[w][2] = qn2; red[w][3] = hi; red[w][4] = lo;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) hist[i * 256 + tid] = 0;
+  __syncthreads();
+  mx = red[0][0]; km = red[0][1]; qn2 = red[0][2]; hi = red[0][3]; lo = red[0][4];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    mx = fmaxf(mx, red[i][0]);
+    km = fmaxf(km, red[i][1]);
+    qn2 += red[i][2];
+    hi = fmaxf(hi, red[i][3]);
+    lo = fminf(lo, red[i][4]);
+  }
+  // ---- v~: the tutorial's (Z1 o1 + Z2 o2) / (Z1 + Z2) merge of the split partials,
+  // four groups of 64 threads over interleaved partials
+  {
+    const int g = tid >> 6, l = tid & 63;
+    float num = 0.f, den = 0.f;
+    for (int q = g; q < S2; q += 4) {
+      const float wq = exp2f(ws.M[base + q] - mx);
+      den = fmaf(wq, ws.L[base + q], den);
+      num = fmaf(wq, ws.A[(base + q) * 64 + l], num);
+    }
+    vnum[g][l] = num;
+    if (l == 0) vden[g] = den;
+  }
+  // ---- tau_L: 256 bins between the smallest and largest finite tile maximum
+  const bool binned = ntiles >= topk && hi > lo;
+  const float scale = binned ? 256.f / (hi - lo) : 0.f;
+  if (binned) {
+    int* hw = hist + w * 256;
+    auto bin = [&](float v) {
+      if (v > -INFINITY) atomicAdd(&hw[min(255, (int)((v - lo) * scale))], 1);
+    };
+    if (vec) {
+      for (int t = tid; t < ntiles / 4; t += 256) {
+        const float4 x = reinterpret_cast<const float4*>(tm)[t];
+        bin(x.x); bin(x.y); bin(x.z); bin(x.w);
+      }
+    } else {
+      for (int t = tid; t < ntiles; t += 256) bin(tm[t]);
+    }
+  }
+  __syncthreads();
+  if (binned) {
+    int c = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) c += hist[u * 256 + tid];
+    hist[tid] = c;                            // column tid is this thread's alone
+  }
+  if (tid < 64) {
+    const float num = (vnum[0][tid] + vnum[1][tid]) + (vnum[2][tid] + vnum[3][tid]);
+    const float den = (vden[0] + vden[1]) + (vden[2] + vden[3]);
     v_tilde[rf * 64 + tid] = num / den;
   }
-  // ---- tau_L
-  const int n = ntiles;
-  const float* tm = ws.bm + (size_t)rf * ntiles;
-  for (int t = tid; t < n; t += 256) val[t] = tm[t];
   __syncthreads();
-  // at least topk tile maxima are >= tau_L (-inf when fewer than topk exist)
-  const float tauL = n >= topk ? block_kth_lower_bound(val, n, topk, hist, red) : -INFINITY;
-  // ---- error bound
-  float km = 0.f;
-  for (int q = tid; q < S; q += 256) km = fmaxf(km, ws.kmax2[(size_t)bh * S + q]);
-  km = block_max(km, red);
-  float qn2 = 0.f;
-  if (tid < 64) { const float x = __bfloat162float(q_tilde[rf * 64 + tid]); qn2 = x * x; }
-  qn2 = block_sum(qn2, red);
-  if (tid == 0) {
-    const float E = err_gamma(64) * sqrtf(qn2) * sqrtf(km);
-    ws.E[rf] = E;
-    ws.thr[rf] = tauL - 4.f * E;
-    ws.cnt[rf] = 0;
+  if (w == 0) {
+    // lane l owns bins 255-8l .. 248-8l (high to low); the highest bin from which the count
+    // of tile maxima at or above reaches topk.  Its lower edge, one bin lower to absorb the
+    // rounding of the bin index, has at least topk tile maxima at or above it.
+    float tauL = -INFINITY;
+    if (binned) {
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = hist[255 - 8 * lane - j];
+        tot += cnt[j];
+      }
+      const int inc = warp_incl_scan(tot);
+      const unsigned hit = __ballot_sync(0xffffffffu, inc >= topk);
+      int b = -1;
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        int cum = inc - tot, dg = -1;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (dg < 0) {
+            if (cum + cnt[j] >= topk) dg = 255 - 8 * lane - j;
+            else cum += cnt[j];
+          }
+        }
+        b = __shfl_sync(0xffffffffu, dg, src);
+      }
+      if (b >= 0) tauL = b > 0 ? lo + (float)(b - 1) / scale : lo;
+    }
+    if (lane == 0) {
+      const float E = err_gamma(64) * sqrtf(qn2) * sqrtf(km);
+      ws.E[rf] = E;
+      ws.thr[rf] = tauL - 4.f * E;
+      ws.cnt[rf] = 0;
+    }
   }
 }
 
@@ -689,11 +776,7 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
   lm_sweep_kernel<<<blocks, kThreads, sm1, st>>>(mqt, mk, mv, N, m, p.S, p.split_len, ws, status);
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t tsm = (size_t)p.ntiles * 4;
-  e = cudaFuncSetAttribute(lm_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tsm);
-  if (e != cudaSuccess) return e;
-  lm_threshold_kernel<<<(unsigned)((long long)BH * m), 256, tsm, st>>>(q_tilde, m, topk, 2 * p.S,
+  lm_threshold_kernel<<<(unsigned)((long long)BH * m), 256, 0, st>>>(q_tilde, m, topk, 2 * p.S,
                                                                        p.S, p.ntiles, ws, v_tilde);
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
