@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_qt,
                 int N, int m, int W, int nch, int G_h, uint32_t tmem_cols,
                 int32_t* __restrict__ route, int* __restrict__ amb, int* status) {
-  // amb: per head, [count, query ids...] at amb + bh * (N + 1)
+  // amb: the heads' counts at amb[0, BH), then head bh's query ids at amb + BH + bh * N
   extern __shared__ unsigned char smem_raw[];
   RouteSmem& s = *reinterpret_cast<RouteSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -282,7 +282,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
     for (int i = 0; i < kEpiWarps; ++i) qtmax2 = fmaxf(qtmax2, s.red[i]);
     const float gq = 2.f * err_gamma(64) * sqrtf(qtmax2);
-    int* hamb = amb + (size_t)bh * (N + 1);
+    int* hcnt = amb + bh;
+    int* hids = amb + (size_t)(gridDim.x / G_h) + (size_t)bh * N;
     for (int it = grp; it < ntiles; it += kGroups) {
       const int st = it % kQStages, r = it / kGroups;
       if (ok && !mbar_wait(&s.q_full[st], (it / kQStages) & 1)) ok = false;
@@ -346,9 +347,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
       if (am) {
         int base = 0;
-        if (lane == 0) base = atomicAdd(hamb, __popc(am));
+        if (lane == 0) base = atomicAdd(hcnt, __popc(am));
         base = __shfl_sync(0xffffffffu, base, 0);
-        if (ambiguous) hamb[1 + base + __popc(am & ((1u << lane) - 1u))] = n;
+        if (ambiguous) hids[base + __popc(am & ((1u << lane) - 1u))] = n;
       }
     }
     if (!ok) flag_error(status, kDevErrTimeout);
@@ -374,8 +375,8 @@ route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde,
   bf16* qt = reinterpret_cast<bf16*>(fix_raw);       // [m][kFixRow]
   __shared__ float red[8];
   const int bh = blockIdx.x / per_head, part = blockIdx.x % per_head;
-  const int* hamb = amb + (size_t)bh * (N + 1);
-  const int count = hamb[0];
+  const int count = amb[bh];
+  const int* hids = amb + (size_t)(gridDim.x / per_head) + (size_t)bh * N;
   if (count <= part * 8) return;                      // no query for this CTA
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bf16* qtb = q_tilde + (size_t)bh * m * 64;
@@ -400,7 +401,7 @@ route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde,
 #pragma unroll
   for (int w = 0; w < 8; ++w) qt2 = fmaxf(qt2, red[w]);
   for (int w = part * 8 + warp; w < count; w += per_head * 8) {
-    const int n = hamb[1 + w];
+    const int n = hids[w];
     if (n < 0 || n >= N) continue;
     float qr[64];
     load_row<bf16, 64>(q + ((size_t)bh * N + n) * 64, qr);
@@ -471,10 +472,8 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  for (int b = 0; b < BH; ++b) {
-    e = cudaMemsetAsync(amb + (size_t)b * (N + 1), 0, sizeof(int), st);
-    if (e != cudaSuccess) return e;
-  }
+  e = cudaMemsetAsync(amb, 0, (size_t)BH * sizeof(int), st);
+  if (e != cudaSuccess) return e;
   route_tc_kernel<<<(unsigned)(BH * G_h), kThreads, smem, st>>>(mq, mqt, N, m, W, nch, G_h, cols,
                                                                  route, amb, status);
   count_launch();
