@@ -223,7 +223,8 @@ int landmark_impl(const T* qt, const T* k, const T* v, int B, int H, int N, int 
 
 // Tensor-core route for bf16 / d = 64 / m <= 512 when no shared partial is
 // requested; the SIMT kernel otherwise.
-size_t route_ws_bytes(int BH, int N) { return (size_t)BH * ((size_t)N + 1) * sizeof(int); }
+// per head: a count, then the ambiguous query ids and their fp32 best scores
+size_t route_ws_bytes(int BH, int N) { return (size_t)BH * (2 * (size_t)N + 1) * sizeof(int); }
 
 template <typename T>
 bool route_uses_tc(int d, int m, const float* lse, const float* so) {

@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_qt,
                 int N, int m, int W, int nch, int G_h, uint32_t tmem_cols,
                 int32_t* __restrict__ route, int* __restrict__ amb, int* status) {
-  // amb: the heads' counts at amb[0, BH), then head bh's query ids at amb + BH + bh * N
+  // amb: the heads' counts at amb[0, BH), then head bh's query ids at amb + BH + bh * N,
+  // then (as floats) their fp32 best scores at amb + BH + BH * N + bh * N
   extern __shared__ unsigned char smem_raw[];
   RouteSmem& s = *reinterpret_cast<RouteSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -283,7 +284,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     for (int i = 0; i < kEpiWarps; ++i) qtmax2 = fmaxf(qtmax2, s.red[i]);
     const float gq = 2.f * err_gamma(64) * sqrtf(qtmax2);
     int* hcnt = amb + bh;
-    int* hids = amb + (size_t)(gridDim.x / G_h) + (size_t)bh * N;
+    const size_t BHs = gridDim.x / G_h;
+    int* hids = amb + BHs + (size_t)bh * N;
+    float* hbest = reinterpret_cast<float*>(amb + BHs + BHs * N) + (size_t)bh * N;
     for (int it = grp; it < ntiles; it += kGroups) {
       const int st = it % kQStages, r = it / kGroups;
       if (ok && !mbar_wait(&s.q_full[st], (it / kQStages) & 1)) ok = false;
@@ -349,7 +352,11 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         int base = 0;
         if (lane == 0) base = atomicAdd(hcnt, __popc(am));
         base = __shfl_sync(0xffffffffu, base, 0);
-        if (ambiguous) hids[base + __popc(am & ((1u << lane) - 1u))] = n;
+        if (ambiguous) {
+          const int pos = base + __popc(am & ((1u << lane) - 1u));
+          hids[pos] = n;
+          hbest[pos] = c.v1;
+        }
       }
     }
     if (!ok) flag_error(status, kDevErrTimeout);
@@ -364,8 +371,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 // list) with the head's q~ block in shared memory (rows padded to 144 bytes:
 // a warp's 16-byte reads of 32 different rows then hit every bank evenly);
 // one warp per query: lanes screen the landmarks with fp32 dots (only those
-// within 2E of the fp32 best can win), re-score the survivors with
-// exact-product arithmetic and reduce (score desc, index asc).
+// within 2E of the routing kernel's fp32 best can win), re-score the
+// survivors with exact-product arithmetic and reduce (score desc, index asc).
 constexpr int kFixRow = 72;            // bf16 per padded landmark row
 
 __global__ void __launch_bounds__(256)
@@ -376,7 +383,9 @@ route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde,
   __shared__ float red[8];
   const int bh = blockIdx.x / per_head, part = blockIdx.x % per_head;
   const int count = amb[bh];
-  const int* hids = amb + (size_t)(gridDim.x / per_head) + (size_t)bh * N;
+  const size_t BHs = gridDim.x / per_head;
+  const int* hids = amb + BHs + (size_t)bh * N;
+  const float* hbest = reinterpret_cast<const float*>(amb + BHs + BHs * N) + (size_t)bh * N;
   if (count <= part * 8) return;                      // no query for this CTA
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bf16* qtb = q_tilde + (size_t)bh * m * 64;
@@ -408,21 +417,12 @@ route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde,
     float qn2 = 0.f;
 #pragma unroll
     for (int l = 0; l < 64; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
-    // pass 1: the fp32 best (the landmark loops stay rolled: unrolled copies of
-    // these bodies overflow the instruction cache)
-    float best = -INFINITY;
-#pragma unroll 1
-    for (int i = lane; i < m; i += 32) {
-      float r[64];
-      load_row<bf16, 64>(qt + i * kFixRow, r);
-      float a = 0.f;
-#pragma unroll
-      for (int l = 0; l < 64; ++l) a = fmaf(qr[l], r[l], a);
-      best = fmaxf(best, a);
-    }
-    best = warp_max(best);
+    // the tensor-core fp32 best v1 is within E of the exact score of the landmark it
+    // came from, so the exact maximum is >= v1 - E and its fp32 dot here >= v1 - 2E
+    const float best = hbest[w];
     const float twoE = 2.f * err_gamma(64) * sqrtf(qn2) * sqrtf(qt2);
-    // pass 2: exact re-scoring of the landmarks within 2E of it
+    // exact re-scoring of the landmarks whose fp32 dot is within 2E of it (the landmark
+    // loop stays rolled: unrolled copies of its body overflow the instruction cache)
     F2 bv{-INFINITY, 0.f};
     int bi = 0x7fffffff;
 #pragma unroll 1
