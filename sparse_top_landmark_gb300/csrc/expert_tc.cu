@@ -7,11 +7,11 @@
 // bit.fan article: queries are grouped by expert and an online softmax runs
 // over the concatenated entries; each expert's k KV rows are gathered once.
 //
-// Three launches:
+// Two launches:
 //   expert_gather_kernel  the k K / V rows of every (head, expert), copied once
-//                         into contiguous [head*m + expert][k][64] blocks;
-//   expert_prep_kernel    the work-unit table (unit = (head, expert, up to 256
-//                         of its queries)) and v~ in fp16;
+//                         into contiguous [head*m + expert][k][64] blocks; one
+//                         more CTA builds the work-unit table (unit = (head,
+//                         expert, up to 256 of its queries)); v~ to fp16;
 //   expert_tc_kernel      persistent CTAs, each over a contiguous run of units
 //                         (units of one expert follow each other, so its
 //                         gathered rows are re-read from L2):
@@ -108,17 +108,62 @@ ExpertTcWs carve(void* ws, int BH, int N, int m, int topk) {
 }
 
 // -------------------------------------------------------------------------------------------
-// gather: row j of expert (head, e) -> kg / vg[(head*m + e)*topk + j]; eight lanes per row,
-// 16 bytes each, four rows per warp step
+// Preparation, one launch: the last CTA builds the work-unit table (unit = (head*m + e, first
+// bucket slot, count <= 256); unit_start[head*m + e] = the expert's first unit, then one
+// entry per unit), every CTA converts a slice of v~ to fp16, and the other CTAs gather the
+// experts' rows: row j of expert (head, e) -> kg / vg[(head*m + e)*topk + j], eight lanes per
+// row, 16 bytes each, four rows per warp step.
 // -------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kGatherThreads)
 expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
                      const int32_t* __restrict__ topk_idx, long long rows, int N, int m, int topk,
-                     bf16* __restrict__ kg, bf16* __restrict__ vg, int* status) {
+                     const int32_t* __restrict__ bucket_off, const float* __restrict__ v_tilde,
+                     int BH, ExpertTcWs w, int* status) {
+  // v~ in fp16, four values per thread step
+  {
+    const long long n4 = (long long)BH * m * 16;
+    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n4;
+         t += (long long)gridDim.x * blockDim.x) {
+      const float4 x = reinterpret_cast<const float4*>(v_tilde)[t];
+      const __half2 lo = __floats2half2_rn(x.x, x.y), hi = __floats2half2_rn(x.z, x.w);
+      uint2 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&lo);
+      o.y = *reinterpret_cast<const uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(w.vt16)[t] = o;
+    }
+  }
+  if (blockIdx.x == gridDim.x - 1) {
+    // the unit table: an exclusive scan of the experts' unit counts
+    __shared__ int red[kGatherThreads / 32 + 1];
+    const int total = BH * m;
+    int carry = 0;
+    for (int i0 = 0; i0 < total; i0 += kGatherThreads) {
+      const int i = i0 + threadIdx.x;
+      int units = 0, a = 0, cnt = 0;
+      if (i < total) {
+        const int bh = i / m, e = i % m;
+        a = bucket_off[(size_t)bh * (m + 1) + e];
+        const int b = bucket_off[(size_t)bh * (m + 1) + e + 1];
+        if (a < 0 || b > N || b < a) flag_error(status, kDevErrBadBucket);
+        else { cnt = b - a; units = (cnt + kUnitQ - 1) / kUnitQ; }
+      }
+      int tot;
+      const int ex = block_excl_scan(units, red, &tot);
+      if (i < total) {
+        w.unit_start[i] = carry + ex;
+        for (int j = 0; j < units; ++j)
+          w.unit[carry + ex + j] = make_int4(i, a + j * kUnitQ, min(kUnitQ, cnt - j * kUnitQ), 0);
+      }
+      carry += tot;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) w.unit_start[total] = carry;
+    return;
+  }
   constexpr int UNR = 4;
   const int piece = threadIdx.x & 7;
   const long long lane_row = (long long)blockIdx.x * (kGatherThreads / 8) + (threadIdx.x >> 3);
-  const long long stride = (long long)gridDim.x * (kGatherThreads / 8);
+  const long long stride = (long long)(gridDim.x - 1) * (kGatherThreads / 8);
   for (long long r0 = lane_row; r0 < rows; r0 += stride * UNR) {
     uint4 kr[UNR], vr[UNR];
 #pragma unroll
@@ -141,46 +186,11 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
     for (int u = 0; u < UNR; ++u) {
       const long long r = r0 + u * stride;
       if (r < rows) {
-        *reinterpret_cast<uint4*>(kg + (size_t)r * 64 + piece * 8) = kr[u];
-        *reinterpret_cast<uint4*>(vg + (size_t)r * 64 + piece * 8) = vr[u];
+        *reinterpret_cast<uint4*>(w.kg + (size_t)r * 64 + piece * 8) = kr[u];
+        *reinterpret_cast<uint4*>(w.vg + (size_t)r * 64 + piece * 8) = vr[u];
       }
     }
   }
-}
-
-// -------------------------------------------------------------------------------------------
-// prep: unit table (units per (head, expert) = ceil(count / 256), exclusive scan,
-// then one entry per unit) and v~ in fp16
-// -------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024)
-expert_prep_kernel(const int32_t* __restrict__ bucket_off, const float* __restrict__ v_tilde,
-                   int BH, int N, int m, ExpertTcWs w, int* status) {
-  __shared__ int red[33];
-  const int total = BH * m;
-  int carry = 0;
-  for (int i0 = 0; i0 < total; i0 += 1024) {
-    const int i = i0 + threadIdx.x;
-    int units = 0, a = 0, cnt = 0;
-    if (i < total) {
-      const int bh = i / m, e = i % m;
-      a = bucket_off[(size_t)bh * (m + 1) + e];
-      const int b = bucket_off[(size_t)bh * (m + 1) + e + 1];
-      if (a < 0 || b > N || b < a) flag_error(status, kDevErrBadBucket);
-      else { cnt = b - a; units = (cnt + kUnitQ - 1) / kUnitQ; }
-    }
-    int tot;
-    const int ex = block_excl_scan(units, red, &tot);
-    if (i < total) {
-      w.unit_start[i] = carry + ex;
-      for (int j = 0; j < units; ++j)
-        w.unit[carry + ex + j] = make_int4(i, a + j * kUnitQ, min(kUnitQ, cnt - j * kUnitQ), 0);
-    }
-    carry += tot;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) w.unit_start[total] = carry;
-  for (size_t t = threadIdx.x; t < (size_t)total * 64; t += 1024)
-    w.vt16[t] = __float2half_rn(v_tilde[t]);
 }
 
 // -------------------------------------------------------------------------------------------
@@ -529,14 +539,12 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   const long long rows = (long long)BH * m * topk;
   const long long gblocks = std::min<long long>((rows + kGatherThreads / 8 - 1) / (kGatherThreads / 8),
                                                 (long long)std::max(num_sms, 1) * 8);
-  expert_gather_kernel<<<(unsigned)gblocks, kGatherThreads, 0, st>>>(k, v, topk_idx, rows, N, m,
-                                                                      topk, w.kg, w.vg, status);
+  // gblocks gathering CTAs plus the one that builds the unit table
+  expert_gather_kernel<<<(unsigned)gblocks + 1, kGatherThreads, 0, st>>>(
+      k, v, topk_idx, rows, N, m, topk, bucket_off, v_tilde, BH, w, status);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  expert_prep_kernel<<<1, 1024, 0, st>>>(bucket_off, v_tilde, BH, N, m, w, status);
-  count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   CUtensorMap mqg, mkg, mvg, mqt, mvt;
   if (!make_tmap_gather64(&mqg, q, (uint64_t)BH * N) ||
       !make_tmap_rows64(&mkg, w.kg, (uint64_t)topk, (uint64_t)BH * m, BN) ||
