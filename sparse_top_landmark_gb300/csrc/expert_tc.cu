@@ -15,8 +15,9 @@
 //   expert_tc_kernel      persistent CTAs, each over a contiguous run of units
 //                         (units of one expert follow each other, so its
 //                         gathered rows are re-read from L2):
-//     warp 0     TMA: the unit's query rows (tile::gather4 of scattered rows),
-//                then the entries in chunks of 128 -- the expert's gathered
+//     warps 0, 3 TMA: the unit's query rows (tile::gather4 of scattered rows;
+//                warp 0 tile 0, warp 3 tile 1); warp 0 then the entries in
+//                chunks of 128 -- the expert's gathered
 //                K / V block first, then the q~ / v~ blocks -- as tiled loads
 //                into a 4-stage ring shared by the two query tiles;
 //     warps 1-2  MMA, one issuing thread per query tile (one thread issues a
@@ -44,7 +45,7 @@ using namespace sm100;
 
 constexpr int BN = 128;          // entries per chunk
 constexpr int kStages = 4;
-constexpr int kThreads = 384;   // producer, two MMA issuers, one spare, 8 softmax warps
+constexpr int kThreads = 384;   // producer, two MMA issuers, second gatherer, 8 softmax warps
 constexpr int kUnitQ = 256;      // queries per work unit (two MMA tiles)
 constexpr float kLazy = 8.0f;
 constexpr int kGatherThreads = 256;
@@ -218,7 +219,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       mbar_init(&s.kv_empty[i], 2);     // both tiles' P . V
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.q_full[i], 1);
+      mbar_init(&s.q_full[i], 2);       // the two gathering warps, one tile each
       mbar_init(&s.q_empty[i], 2);      // both tiles' last S
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], 4);
@@ -261,11 +262,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         if (it + 1 < units) nxt = unit_tab[ubase + it + 1];
         const int idx = cur.x, bh = idx / m, qbase = cur.y, qcnt = cur.z;
         const int qb = it & 1;
-        // ---- the unit's query rows (two tiles): lane l owns rows 8l .. 8l+7
-        int rows[8];
+        // ---- query tile 0 of the unit (warp 3 gathers tile 1): lane l owns rows 4l .. 4l+3
+        int rows[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = 8 * lane + j;
+        for (int j = 0; j < 4; ++j) {
+          const int r = 4 * lane + j;
           rows[j] = null_row;
           if (r < qcnt) {
             const int qi = bucket_qidx[(size_t)bh * N + qbase + r];
@@ -274,14 +275,10 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
           }
         }
         if (!mbar_wait_warp(&s.q_empty[qb], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
-        if (lane == 0) mbar_expect_tx(&s.q_full[qb], 2 * 128 * 128);
+        if (lane == 0) mbar_expect_tx(&s.q_full[qb], 128 * 128);
         __syncwarp();
-        {
-          const int r = 8 * lane;
-          bf16* dst = &s.q[qb][r >> 7][(r & 127) * 64];
-          tma_gather4(dst, &map_qg, &s.q_full[qb], 0, rows[0], rows[1], rows[2], rows[3]);
-          tma_gather4(dst + 4 * 64, &map_qg, &s.q_full[qb], 0, rows[4], rows[5], rows[6], rows[7]);
-        }
+        tma_gather4(&s.q[qb][0][4 * lane * 64], &map_qg, &s.q_full[qb], 0, rows[0], rows[1], rows[2],
+                    rows[3]);
         // ---- the entries: the expert's gathered rows, then the shared blocks
         for (int c = 0; c < nc; ++c, ++gi) {
           const int st = gi % kStages;
@@ -351,6 +348,32 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       if (elect_one()) mma_commit(&s.drain[slot]);
       __syncwarp();
       if (!mbar_wait_warp(&s.drain[slot], 0)) ok = false;
+      if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
+    } else {
+      // ------------------------------------------------------------ query tile 1
+      // of every unit, gathered alongside the producer's tile 0: one warp issues a
+      // four-row TMA gather only every ~130 cycles, so two warps share the 64 per unit
+      bool ok = true;
+      for (int it = 0; it < units && ok; ++it) {
+        const int4 cur = unit_tab[ubase + it];
+        const int bh = cur.x / m, qbase = cur.y, qcnt = cur.z, qb = it & 1;
+        int rows[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 128 + 4 * lane + j;
+          rows[j] = null_row;
+          if (r < qcnt) {
+            const int qi = bucket_qidx[(size_t)bh * N + qbase + r];
+            if (qi >= 0 && qi < N) rows[j] = bh * N + qi;
+            else flag_error(status, kDevErrBadBucket);
+          }
+        }
+        if (!mbar_wait_warp(&s.q_empty[qb], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
+        if (lane == 0) mbar_expect_tx(&s.q_full[qb], 128 * 128);
+        __syncwarp();
+        tma_gather4(&s.q[qb][1][4 * lane * 64], &map_qg, &s.q_full[qb], 0, rows[0], rows[1],
+                    rows[2], rows[3]);
+      }
       if (!ok && lane == 0) flag_error(status, kDevErrTimeout);
     }
   } else {
