@@ -234,11 +234,13 @@ bool route_uses_tc(int d, int m, const float* lse, const float* so) {
 template <typename T>
 cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int N, int d, int m,
                            int32_t* route, float* lse, float* so, DevState* ds, void* ws,
-                           cudaStream_t st) {
+                           cudaStream_t st, int* hist = nullptr, bool* counted = nullptr) {
   if constexpr (std::is_same<T, bf16>::value) {
-    if (route_uses_tc<T>(d, m, lse, so))
+    if (route_uses_tc<T>(d, m, lse, so)) {
+      if (counted) *counted = hist != nullptr;
       return launch_route_tc(q, qt, BH, N, m, ds->num_sms, route, static_cast<int*>(ws),
-                             ds->status, st);
+                             ds->status, hist, st);
+    }
   }
   return launch_route<T>(q, qt, vt, BH, N, d, m, route, lse, so, st);
 }
@@ -358,9 +360,13 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, m, qt, st), "pool launch");
   MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, ds->status, st),
             "landmark launch");
-  MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, ds, ws + L.rt, st),
+  // the tensor-core route also counts the bucket stage's (expert, chunk) histogram
+  bool counted = false;
+  MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, ds, ws + L.rt, st,
+                              reinterpret_cast<int*>(ws + L.bk), &counted),
             "route launch");
-  MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st), "bucket launch");
+  MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, counted),
+            "bucket launch");
   if constexpr (std::is_same<T, bf16>::value) {
     if (expert_tc_supported(d, m, topk)) {
       MITA_CUDA(launch_expert_tc(q, k, v, qt, vt, ti, off, qidx, BH, N, m, topk, ds->num_sms,

@@ -198,13 +198,13 @@ size_t bucket_ws_bytes(int BH, int N, int m) {
 
 cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* ws,
                           int32_t* bucket_off, int32_t* bucket_qidx, int* status,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool counted) {
   const int nchunks = (N + kBucketChunk - 1) / kBucketChunk;
   int* hist = static_cast<int*>(ws);                       // [BH][m][nchunks]
   int* total = hist + (size_t)BH * m * nchunks;             // [BH][m]
   const bool smem = m <= kSmemExperts;
   cudaError_t e;
-  if (!smem) {
+  if (!smem && !counted) {
     e = cudaMemsetAsync(hist, 0, (size_t)BH * m * nchunks * sizeof(int), st);
     if (e != cudaSuccess) return e;
   }
@@ -215,9 +215,11 @@ cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* 
                              (int)s3);
     if (e != cudaSuccess) return e;
   }
-  bucket_count_kernel<<<blocks, 256, s1, st>>>(route_idx, N, m, nchunks, hist, status);
-  count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!counted) {
+    bucket_count_kernel<<<blocks, 256, s1, st>>>(route_idx, N, m, nchunks, hist, status);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   const long long BHm = (long long)BH * m;
   bucket_scan_kernel<<<(unsigned)((BHm + kWarps - 1) / kWarps), 256, 0, st>>>(BHm, nchunks, hist,
                                                                                total);

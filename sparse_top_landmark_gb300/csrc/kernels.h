@@ -74,9 +74,11 @@ cudaError_t launch_route(const T* q, const T* q_tilde, const float* v_tilde, int
 // ---- step 5: stable grouping of queries by expert -------------------------
 constexpr int kBucketChunk = 4096;   // queries per chunk (one warp each)
 size_t bucket_ws_bytes(int BH, int N, int m);
+// ws: [BH][m][nchunks] per-chunk counts, then [BH][m] totals.  counted = the counts are
+// already in ws (left by launch_route_tc's histogram).
 cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* ws,
                           int32_t* bucket_off, int32_t* bucket_qidx, int* status,
-                          cudaStream_t st);
+                          cudaStream_t st, bool counted = false);
 
 // ---- step 6: expert-grouped joint attention -------------------------------
 template <typename T>
@@ -94,9 +96,12 @@ bool make_tmap_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 // TMA map over a [rows, 64] bf16 array for tile::gather4 (four scattered rows).
 bool make_tmap_gather64(CUtensorMap* map, const void* base, uint64_t rows);
 bool route_tc_supported(int d, int m);
-// `amb` is scratch of BH*(N+1) ints: per head, a count then ambiguous query ids.
+// `amb` is scratch of BH*(2N+1) words: the heads' counts, then per head the ambiguous
+// query ids and their fp32 best scores.  `hist`, if not null, receives the bucket
+// stage's per-chunk expert counts ([BH][m][ceil(N / kBucketChunk)], cleared here), so
+// that launch_bucket(..., counted = true) can skip its counting pass.
 cudaError_t launch_route_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH, int N,
-                            int m, int num_sms, int32_t* route, int* amb, int* status,
+                            int m, int num_sms, int32_t* route, int* amb, int* status, int* hist,
                             cudaStream_t st);
 
 bool expert_tc_supported(int d, int m, int topk);

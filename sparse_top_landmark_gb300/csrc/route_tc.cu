@@ -158,7 +158,8 @@ __device__ __forceinline__ Cand finish_top(const RowTop& t, const float4* bbs, i
 __global__ void __launch_bounds__(kThreads, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_qt,
                 int N, int m, int W, int nch, int G_h, uint32_t tmem_cols,
-                int32_t* __restrict__ route, int* __restrict__ amb, int* status) {
+                int32_t* __restrict__ route, int* __restrict__ amb, int* status,
+                int* __restrict__ hist) {
   // amb: the heads' counts at amb[0, BH), then head bh's query ids at amb + BH + bh * N,
   // then (as floats) their fp32 best scores at amb + BH + BH * N + bh * N
   extern __shared__ unsigned char smem_raw[];
@@ -345,7 +346,14 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       }
       const Cand c = finish_top(top, bb, sw);
       const bool ambiguous = live && !(c.v1 - c.v2 > twoE);
-      if (live) route[(size_t)bh * N + n] = c.i1;
+      if (live) {
+        route[(size_t)bh * N + n] = c.i1;
+        // the bucket stage's count of (expert, chunk of 4096 queries); an ambiguous
+        // query is counted by the fix-up, under its exact route
+        if (hist && !ambiguous && c.i1 >= 0 && c.i1 < m)
+          atomicAdd(&hist[((size_t)bh * m + c.i1) * ((N + kBucketChunk - 1) / kBucketChunk) +
+                          n / kBucketChunk], 1);
+      }
       // append ambiguous queries to the head's list (one reservation per warp)
       const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
       if (am) {
@@ -377,7 +385,8 @@ constexpr int kFixRow = 72;            // bf16 per padded landmark row
 
 __global__ void __launch_bounds__(256)
 route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde, int N, int m,
-                   int per_head, const int* __restrict__ amb, int32_t* __restrict__ route) {
+                   int per_head, const int* __restrict__ amb, int32_t* __restrict__ route,
+                   int* __restrict__ hist) {
   extern __shared__ __align__(16) unsigned char fix_raw[];
   bf16* qt = reinterpret_cast<bf16*>(fix_raw);       // [m][kFixRow]
   __shared__ float red[8];
@@ -443,7 +452,12 @@ route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde,
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
-    if (lane == 0) route[(size_t)bh * N + n] = bi;
+    if (lane == 0) {
+      route[(size_t)bh * N + n] = bi;
+      if (hist && bi >= 0 && bi < m)   // the routing kernel left this query uncounted
+        atomicAdd(&hist[((size_t)bh * m + bi) * ((N + kBucketChunk - 1) / kBucketChunk) +
+                        n / kBucketChunk], 1);
+    }
   }
 }
 
@@ -454,7 +468,8 @@ size_t route_tc_smem_bytes() { return sizeof(RouteSmem) + 1024; }
 bool route_tc_supported(int d, int m) { return d == 64 && m >= 1 && m <= kMaxM; }
 
 cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, int m,
-                            int num_sms, int32_t* route, int* amb, int* status, cudaStream_t st) {
+                            int num_sms, int32_t* route, int* amb, int* status, int* hist,
+                            cudaStream_t st) {
   // chunk width: 32, 64 or 128 landmarks (a power of two, so the four group
   // buffers fill a power-of-two tensor-memory allocation)
   int W = 32;
@@ -474,8 +489,12 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(amb, 0, (size_t)BH * sizeof(int), st);
   if (e != cudaSuccess) return e;
+  if (hist) {
+    const size_t nh = (size_t)BH * m * ((N + kBucketChunk - 1) / kBucketChunk);
+    if ((e = cudaMemsetAsync(hist, 0, nh * sizeof(int), st)) != cudaSuccess) return e;
+  }
   route_tc_kernel<<<(unsigned)(BH * G_h), kThreads, smem, st>>>(mq, mqt, N, m, W, nch, G_h, cols,
-                                                                 route, amb, status);
+                                                                 route, amb, status, hist);
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int per_head = std::max(1, std::max(num_sms, 1) / BH);
@@ -483,7 +502,7 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   e = cudaFuncSetAttribute(route_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm);
   if (e != cudaSuccess) return e;
   route_fixup_kernel<<<(unsigned)(BH * per_head), 256, fsm, st>>>(q, q_tilde, N, m, per_head, amb,
-                                                                 route);
+                                                                 route, hist);
   count_launch();
   return cudaGetLastError();
 }
