@@ -333,6 +333,31 @@ landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, in
                     rowflat, ws, topk_idx);
 }
 
+// Exact-product dot of qd (shared memory, fp32) with one key row, by a whole warp: lane l
+// takes the products of elements l, l + 32 (split exactly with an FMA), and the 32
+// partial (sum, error) pairs are combined with error-free two-sums across the lanes.
+// Returns hi + lo on every lane; like dot_f2, exact up to ~2^-48 relative.
+template <typename T, int D>
+__device__ __forceinline__ F2 dot_f2_warp(const float* qd, const T* krow, int lane) {
+  static_assert(D % 32 == 0 && D <= 128, "row split over the warp's lanes");
+  float s = 0.f, c = 0.f;
+#pragma unroll
+  for (int l = lane; l < D; l += 32) {
+    const float a = qd[l], b = to_f(krow[l]);
+    const float p = __fmul_rn(a, b);
+    const float e = fmaf(a, b, -p);
+    two_sum_acc(s, c, p);
+    c = __fadd_rn(c, e);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
+    two_sum_acc(s, c, s2);
+    c = __fadd_rn(c, c2);
+  }
+  return f2_normalize(s, c);
+}
+
 // Candidates of the tensor-core path: the keys whose fp32 score reached the
 // row's collection threshold, gathered by the collect kernel (in no particular
 // order).  tau, the k-th largest fp32 score, comes from a radix select over
@@ -463,15 +488,14 @@ landmark_select_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, i
   // ---- exact re-scoring and ranking of the band
   const T* kb = k + (size_t)bh * N * D;
   const int PB = next_pow2(max(nb, 1));
-  for (int t = tid; t < PB; t += blockDim.x) {
-    if (t < nb) {
-      float kr[D];
-      load_row<T, D>(kb + (size_t)bi[t] * D, kr);
-      bx[t] = dot_f2<D>(qd, kr);
-    } else {
-      bx[t] = F2{-INFINITY, 0.f};
-      bi[t] = 0x7fffffff;
-    }
+  for (int t = nb + tid; t < PB; t += blockDim.x) {
+    bx[t] = F2{-INFINITY, 0.f};
+    bi[t] = 0x7fffffff;
+  }
+  // one warp per band entry
+  for (int t = tid >> 5; t < nb; t += blockDim.x >> 5) {
+    const F2 x = dot_f2_warp<T, D>(qd, kb + (size_t)bi[t] * D, lane);
+    if (lane == 0) bx[t] = x;
   }
   bitonic_sort_desc(bx, bi, PB);
   // ---- the a members above the band plus the best (topk - a) of it, ascending
