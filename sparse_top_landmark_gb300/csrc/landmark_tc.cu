@@ -42,7 +42,7 @@ namespace {
 using namespace sm100;
 
 constexpr int BN = 128;          // keys per tile
-constexpr int kKRing = 6;        // sweep: K ring depth (K is freed as soon as S is computed)
+constexpr int kKRing = 8;        // sweep: K ring depth (K is freed as soon as S is computed)
 constexpr int kVRing = 4;        // sweep: V ring depth (V is held until P . V is done)
 constexpr int kThreads = 384;    // 12 warps
 constexpr float kLazy = 8.0f;    // rescale O only when the max grows by > 2^8
@@ -528,7 +528,7 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, i
 // -------------------------------------------------------------------------------------------
 // pass 2: collect the keys at or above the threshold
 // -------------------------------------------------------------------------------------------
-constexpr int kKStages = 6;
+constexpr int kKStages = 8;
 constexpr int kCSlots = 4;                  // tile groups in flight (tensor-memory buffers)
 constexpr int kCThreads = (4 + 4 * kCSlots) * 32;
 constexpr int kLocalCand = 64;   // candidates per row buffered in shared memory
