@@ -70,55 +70,82 @@ def roofline_s(flops, nbytes, pk, sustained=False):
 # Clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 20 ms, each with its own timestamp); summary()
+    keeps the samples taken inside a given host-time window."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
 
-    def __enter__(self):
+    def start(self):
+        """Start sampling and wait (up to 10 s) for the first sample."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", "100"],
+                 "-i", str(self.gpu), "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
-        time.sleep(0.05)
-        return self
+            return
+        import threading
+        first = threading.Event()
 
-    def __exit__(self, *a):
-        self.lines = []
+        def reader():
+            for ln in self.proc.stdout:
+                if ln.strip():
+                    self.lines.append(ln)
+                    first.set()
+        self._t = threading.Thread(target=reader, daemon=True)
+        self._t.start()
+        first.wait(timeout=10.0)
+
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            self._t.join(timeout=5)
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def summary(self, t0, t1):
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
+            ts = self._stamp(f[0])
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for nm, val in zip(names, f[5:9]):
+        inside = [r for r in rows if r[0] is not None and t0 - 0.005 <= r[0] <= t1 + 0.005]
+        used = inside
+        if not used and rows:   # window shorter than the sampling period: the nearest sample
+            used = [min(rows, key=lambda r: abs((r[0] or t0) - 0.5 * (t0 + t1)))]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        for r in used:
+            for nm, val in zip(names, r[3]):
                 if val.lower().startswith("active"):
                     reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(r[1] for r in used),
+                "sm_max_mhz": max(r[2] for r in used), "reasons": sorted(reasons),
+                "samples": len(inside), "window_ms": round((t1 - t0) * 1e3, 1)}
 
 
 # ---------------------------------------------------------------------------
@@ -299,6 +326,9 @@ def bench_workload(mita, w, args, dev, stream, n_gpus, do_e2e=True):
     q, k, v = W.make_qkv(w, 0)
     dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
     out = torch.empty_like(dq)
+    # clocks: sampling runs from before the warm-up, the timed window is cut out below
+    sampler = ClockSampler(smi_index(dev.index))
+    sampler.start()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             mita.mita_forward(dq, dk, dv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=out,
@@ -307,16 +337,17 @@ def bench_workload(mita, w, args, dev, stream, n_gpus, do_e2e=True):
     if n_gpus > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(smi_index(dev.index))
-    with sampler:
-        secs = time_forward(mita, w, dq, dk, dv, out, args.steps, stream)
+    t0 = time.time()
+    secs = time_forward(mita, w, dq, dk, dv, out, args.steps, stream)
+    t1 = time.time()
+    sampler.stop()
     torch.cuda.synchronize(dev)
     if n_gpus > 1:
         t = torch.tensor([secs], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         secs = t.item()
         torch.distributed.barrier()
-    res = {"secs": secs, "clocks": sampler.summary()}
+    res = {"secs": secs, "clocks": sampler.summary(t0, t1)}
     res["value"] = n_gpus * w.queries * args.steps / secs
     res["ms_per_step"] = secs / args.steps * 1e3
     res["stages"] = stage_times(mita, w, dq, dk, dv, max(3, min(args.steps, 10)), stream)
