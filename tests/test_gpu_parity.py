@@ -190,6 +190,33 @@ def test_forward_host_pageable_buffers_match_device_path():
     assert torch.equal(hout, dout.cpu())
 
 
+@pytest.mark.parametrize("name", ["seg_32x32", "long_64k"])
+def test_forward_replays_from_a_cuda_graph(name):
+    """mita_forward queues its launches without host synchronisation, so it can be
+    captured into a CUDA graph (after one call of the same size has grown the
+    stream's workspace) and replayed with the same result."""
+    mita = M()
+    w, q, k, v = inputs(name)
+    dq, dk, dv = dev(q), dev(k), dev(v)
+    s = torch.cuda.Stream()
+    out = torch.empty_like(dq)
+    with torch.cuda.stream(s):
+        mita.mita_forward(dq, dk, dv, w.grid_h, w.grid_w, w.m, w.topk, out=out, stream=s)
+    s.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+        mita.mita_forward(dq, dk, dv, w.grid_h, w.grid_w, w.m, w.topk, out=out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+
+
 def test_forward_is_deterministic():
     mita = M()
     w, q, k, v = inputs("long_64k")
