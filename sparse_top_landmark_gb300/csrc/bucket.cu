@@ -41,6 +41,7 @@ __device__ __forceinline__ int load_route(const int32_t* route, long long bh, in
 __global__ void __launch_bounds__(256)
 bucket_count_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks,
                     int* __restrict__ hist, int* status) {
+  griddep_wait();
   extern __shared__ int h[];                     // [m] when m <= kSmemExperts
   const long long bh = blockIdx.x / nchunks;
   const int chunk = blockIdx.x % nchunks;
@@ -67,6 +68,7 @@ bucket_count_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks
 
 __global__ void __launch_bounds__(256)
 bucket_scan_kernel(long long BHm, int nchunks, int* __restrict__ hist, int* __restrict__ total) {
+  griddep_wait();
   const long long be = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);   // bh * m + e
   const int lane = threadIdx.x & 31;
   if (be >= BHm) return;
@@ -105,6 +107,7 @@ __device__ void expert_offsets(const int* __restrict__ tot, int m, int* off, int
 // many experts: one CTA per head writes bucket_off before the scatter
 __global__ void __launch_bounds__(256)
 bucket_offsets_kernel(const int* __restrict__ total, int m, int32_t* __restrict__ bucket_off) {
+  griddep_wait();
   __shared__ int red[33];
   const long long bh = blockIdx.x;
   expert_offsets(total + (size_t)bh * m, m, bucket_off + (size_t)bh * (m + 1), red);
@@ -115,6 +118,7 @@ bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchun
                       int* __restrict__ hist, const int* __restrict__ total,
                       int32_t* __restrict__ bucket_off, int32_t* __restrict__ bucket_qidx,
                       int* status) {
+  griddep_wait();
   extern __shared__ int hw[];                    // [kWarps][m] + off[m + 1] when m <= kSmemExperts
   __shared__ int red[33];
   const long long bh = blockIdx.x / nchunks;
@@ -216,24 +220,25 @@ cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* 
     if (e != cudaSuccess) return e;
   }
   if (!counted) {
-    bucket_count_kernel<<<blocks, 256, s1, st>>>(route_idx, N, m, nchunks, hist, status);
+    e = launch_pdl(bucket_count_kernel, dim3(blocks), dim3(256), s1, st, route_idx, N, m, nchunks,
+                   hist, status);
     count_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
   }
   const long long BHm = (long long)BH * m;
-  bucket_scan_kernel<<<(unsigned)((BHm + kWarps - 1) / kWarps), 256, 0, st>>>(BHm, nchunks, hist,
-                                                                               total);
+  e = launch_pdl(bucket_scan_kernel, dim3((unsigned)((BHm + kWarps - 1) / kWarps)), dim3(256), 0, st,
+                 BHm, nchunks, hist, total);
   count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   if (!smem) {
-    bucket_offsets_kernel<<<BH, 256, 0, st>>>(total, m, bucket_off);
+    e = launch_pdl(bucket_offsets_kernel, dim3(BH), dim3(256), 0, st, total, m, bucket_off);
     count_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
   }
-  bucket_scatter_kernel<<<blocks, 256, s3, st>>>(route_idx, N, m, nchunks, hist, total, bucket_off,
-                                                 bucket_qidx, status);
+  e = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), s3, st, route_idx, N, m, nchunks,
+                 hist, total, bucket_off, bucket_qidx, status);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mita

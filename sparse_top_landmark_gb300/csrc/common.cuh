@@ -20,6 +20,33 @@ constexpr int kBandCap = 1024;   // near-boundary candidates re-scored exactly
 constexpr int kKeyTile = 32;     // keys staged per shared-memory tile (SIMT path)
 constexpr int kExactCtas = 8;    // CTAs (and scratch rows) of the exact fallback
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: the forward's kernels are launched so that a
+// kernel's grid becomes resident while the previous kernel's last CTAs still
+// run; each such kernel starts with griddep_wait(), which returns once the
+// previous grid has completed and its memory writes are visible (a no-op for a
+// kernel launched the ordinary way).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Bits of the per-device status word (read by mita_get_last_device_error).
 enum : int {
   kDevErrBadIndex = 1,    // an expert index outside [0, N)

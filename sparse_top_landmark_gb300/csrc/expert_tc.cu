@@ -120,6 +120,7 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
                      const int32_t* __restrict__ topk_idx, long long rows, int N, int m, int topk,
                      const int32_t* __restrict__ bucket_off, const float* __restrict__ v_tilde,
                      int BH, ExpertTcWs w, int* status) {
+  griddep_wait();
   // v~ in fp16, four values per thread step
   {
     const long long n4 = (long long)BH * m * 16;
@@ -201,6 +202,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
                  const __grid_constant__ CUtensorMap map_vt, const int32_t* __restrict__ bucket_qidx,
                  const int* __restrict__ unit_count, const int4* __restrict__ unit_tab, int BH,
                  int N, int m, int topk, bf16* __restrict__ out, int* status) {
+  griddep_wait();
   extern __shared__ unsigned char smem_raw[];
   ExpertSmem& s = *reinterpret_cast<ExpertSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -563,10 +565,10 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   const long long gblocks = std::min<long long>((rows + kGatherThreads / 8 - 1) / (kGatherThreads / 8),
                                                 (long long)std::max(num_sms, 1) * 8);
   // gblocks gathering CTAs plus the one that builds the unit table
-  expert_gather_kernel<<<(unsigned)gblocks + 1, kGatherThreads, 0, st>>>(
-      k, v, topk_idx, rows, N, m, topk, bucket_off, v_tilde, BH, w, status);
+  cudaError_t e = launch_pdl(expert_gather_kernel, dim3((unsigned)gblocks + 1), dim3(kGatherThreads),
+                             0, st, k, v, topk_idx, rows, N, m, topk, bucket_off, v_tilde, BH, w,
+                             status);
   count_launch();
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mqg, mkg, mvg, mqt, mvt;
   if (!make_tmap_gather64(&mqg, q, (uint64_t)BH * N) ||
@@ -578,11 +580,12 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   const size_t smem = sizeof(ExpertSmem) + 1024;
   e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  expert_tc_kernel<<<(unsigned)std::max(num_sms, 1), kThreads, smem, st>>>(
-      mqg, mkg, mvg, mqt, mvt, bucket_qidx, w.unit_start + (size_t)BH * m, w.unit, BH, N, m, topk,
-      out, status);
+  e = launch_pdl(expert_tc_kernel, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
+                 mqg, mkg, mvg, mqt, mvt, bucket_qidx,
+                 static_cast<const int*>(w.unit_start + (size_t)BH * m),
+                 static_cast<const int4*>(w.unit), BH, N, m, topk, out, status);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mita

@@ -370,6 +370,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256)
 landmark_select_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, int N, int m,
                        int topk, int cap, int P, LandmarkWs ws, int32_t* __restrict__ topk_idx) {
+  griddep_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* us = reinterpret_cast<float*>(smem_raw);           // [cap]
   int* ui = reinterpret_cast<int*>(us + cap);               // [cap]
@@ -511,6 +512,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(512)
 landmark_exact_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, int N, int m,
                       int topk, LandmarkWs ws, int32_t* __restrict__ topk_idx) {
+  griddep_wait();
   __shared__ double qd[D];
   __shared__ int hist[256];
   __shared__ int ired[17];
@@ -599,13 +601,14 @@ cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int t
       auto sk = landmark_select_kernel<T, D>;
       e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
       if (e != cudaSuccess) return e;
-      sk<<<(unsigned)((long long)BH * m), 256, ssmem, st>>>(qt, k, N, m, topk, p.cap, p.P, ws,
-                                                            topk_idx);
+      e = launch_pdl(sk, dim3((unsigned)((long long)BH * m)), dim3(256), ssmem, st, qt, k, N, m,
+                     topk, p.cap, p.P, ws, topk_idx);
       count_launch();
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-      landmark_exact_kernel<T, D><<<kExactCtas, 512, 0, st>>>(qt, k, N, m, topk, ws, topk_idx);
+      if (e != cudaSuccess) return e;
+      e = launch_pdl(landmark_exact_kernel<T, D>, dim3(kExactCtas), dim3(512), 0, st, qt, k, N, m,
+                     topk, ws, topk_idx);
       count_launch();
-      return cudaGetLastError();
+      return e;
     }
   }
   (void)status;

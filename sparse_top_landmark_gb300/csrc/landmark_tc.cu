@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, int N, int m, int S, int split_len,
                 LandmarkWs ws, int* status) {
+  griddep_wait();
   extern __shared__ unsigned char smem_raw[];
   SweepSmem& s = *reinterpret_cast<SweepSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -394,6 +395,7 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
 __global__ void __launch_bounds__(256)
 lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, int S,
                     int ntiles, LandmarkWs ws, float* __restrict__ v_tilde) {
+  griddep_wait();
   __shared__ float red[8][5];
   __shared__ int hist[8 * 256];               // one histogram per warp
   __shared__ float vnum[4][64], vden[4];
@@ -552,6 +554,7 @@ struct alignas(1024) CollectSmem {
 __global__ void __launch_bounds__(kCThreads, 1)
 lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constant__ CUtensorMap map_k,
                   int N, int m, int S, int split_len, int cap, LandmarkWs ws, int* status) {
+  griddep_wait();
   extern __shared__ unsigned char smem_raw[];
   CollectSmem& s = *reinterpret_cast<CollectSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -773,20 +776,21 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
   cudaError_t e = cudaFuncSetAttribute(lm_sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sm1);
   if (e != cudaSuccess) return e;
-  lm_sweep_kernel<<<blocks, kThreads, sm1, st>>>(mqt, mk, mv, N, m, p.S, p.split_len, ws, status);
+  e = launch_pdl(lm_sweep_kernel, dim3(blocks), dim3(kThreads), sm1, st, mqt, mk, mv, N, m, p.S,
+                 p.split_len, ws, status);
   count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  lm_threshold_kernel<<<(unsigned)((long long)BH * m), 256, 0, st>>>(q_tilde, m, topk, 2 * p.S,
-                                                                       p.S, p.ntiles, ws, v_tilde);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(lm_threshold_kernel, dim3((unsigned)((long long)BH * m)), dim3(256), 0, st,
+                 q_tilde, m, topk, 2 * p.S, p.S, p.ntiles, ws, v_tilde);
   count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   const size_t sm2 = sizeof(CollectSmem) + 1024;
   e = cudaFuncSetAttribute(lm_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
   if (e != cudaSuccess) return e;
-  lm_collect_kernel<<<blocks, kCThreads, sm2, st>>>(mqt, mk, N, m, p.S, p.split_len, p.cap, ws,
-                                                   status);
+  e = launch_pdl(lm_collect_kernel, dim3(blocks), dim3(kCThreads), sm2, st, mqt, mk, N, m, p.S,
+                 p.split_len, p.cap, ws, status);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mita

@@ -25,6 +25,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kPoolThreads, 8)
 pool_kernel(const T* __restrict__ q, int N, int grid_h, int grid_w, int mh, int mw,
             T* __restrict__ q_tilde) {
+  griddep_wait();
   constexpr int VEC = Vec<T>::N;
   constexpr int NV = D / VEC;              // 16-byte vectors per row
   constexpr int TL = kPoolThreads / NV;    // token lanes
@@ -96,9 +97,10 @@ cudaError_t run(const T* q, int BH, int N, int grid_h, int grid_w, int m, T* qt,
     mh = mw = r;
   }
   const long long blocks = (long long)BH * m;
-  pool_kernel<T, D><<<(unsigned)blocks, kPoolThreads, 0, st>>>(q, N, grid_h, grid_w, mh, mw, qt);
+  const cudaError_t e = launch_pdl(pool_kernel<T, D>, dim3((unsigned)blocks), dim3(kPoolThreads), 0,
+                                   st, q, N, grid_h, grid_w, mh, mw, qt);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

@@ -160,6 +160,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 int N, int m, int W, int nch, int G_h, uint32_t tmem_cols,
                 int32_t* __restrict__ route, int* __restrict__ amb, int* status,
                 int* __restrict__ hist) {
+  griddep_wait();
   // amb: the heads' counts at amb[0, BH), then head bh's query ids at amb + BH + bh * N,
   // then (as floats) their fp32 best scores at amb + BH + BH * N + bh * N
   extern __shared__ unsigned char smem_raw[];
@@ -387,6 +388,7 @@ __global__ void __launch_bounds__(256)
 route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde, int N, int m,
                    int per_head, const int* __restrict__ amb, int32_t* __restrict__ route,
                    int* __restrict__ hist) {
+  griddep_wait();
   extern __shared__ __align__(16) unsigned char fix_raw[];
   bf16* qt = reinterpret_cast<bf16*>(fix_raw);       // [m][kFixRow]
   __shared__ float red[8];
@@ -493,18 +495,18 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
     const size_t nh = (size_t)BH * m * ((N + kBucketChunk - 1) / kBucketChunk);
     if ((e = cudaMemsetAsync(hist, 0, nh * sizeof(int), st)) != cudaSuccess) return e;
   }
-  route_tc_kernel<<<(unsigned)(BH * G_h), kThreads, smem, st>>>(mq, mqt, N, m, W, nch, G_h, cols,
-                                                                 route, amb, status, hist);
+  e = launch_pdl(route_tc_kernel, dim3((unsigned)(BH * G_h)), dim3(kThreads), smem, st, mq, mqt, N,
+                 m, W, nch, G_h, cols, route, amb, status, hist);
   count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   const int per_head = std::max(1, std::max(num_sms, 1) / BH);
   const size_t fsm = (size_t)m * kFixRow * 2;
   e = cudaFuncSetAttribute(route_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm);
   if (e != cudaSuccess) return e;
-  route_fixup_kernel<<<(unsigned)(BH * per_head), 256, fsm, st>>>(q, q_tilde, N, m, per_head, amb,
-                                                                 route, hist);
+  e = launch_pdl(route_fixup_kernel, dim3((unsigned)(BH * per_head)), dim3(256), fsm, st, q, q_tilde,
+                 N, m, per_head, amb, route, hist);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mita
