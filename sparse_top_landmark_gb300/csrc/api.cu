@@ -2,6 +2,7 @@
 // orchestration.  Every arithmetic step runs in the kernels of this library.
 #include "mita.h"
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -234,12 +235,13 @@ bool route_uses_tc(int d, int m, const float* lse, const float* so) {
 template <typename T>
 cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int N, int d, int m,
                            int32_t* route, float* lse, float* so, DevState* ds, void* ws,
-                           cudaStream_t st, int* hist = nullptr, bool* counted = nullptr) {
+                           cudaStream_t st, int* hist = nullptr, bool* counted = nullptr,
+                           bool prezeroed = false) {
   if constexpr (std::is_same<T, bf16>::value) {
     if (route_uses_tc<T>(d, m, lse, so)) {
       if (counted) *counted = hist != nullptr;
       return launch_route_tc(q, qt, BH, N, m, ds->num_sms, route, static_cast<int*>(ws),
-                             ds->status, hist, st);
+                             ds->status, hist, st, prezeroed);
     }
   }
   return launch_route<T>(q, qt, vt, BH, N, d, m, route, lse, so, st);
@@ -334,6 +336,19 @@ ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, size_t esize
   return L;
 }
 
+// The forward's counters, cleared by one kernel at its start (a memset between two
+// kernels would hold back the next kernel's early launch): the landmark stage's
+// slow-row count, the heads' ambiguous-query counts and the bucket histogram.
+__global__ void __launch_bounds__(256)
+forward_zero_kernel(int* a, long long na, int* b, long long nb, int* c, long long nc) {
+  griddep_wait();
+  const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long t = t0; t < na; t += stride) a[t] = 0;
+  for (long long t = t0; t < nb; t += stride) b[t] = 0;
+  for (long long t = t0; t < nc; t += stride) c[t] = 0;
+}
+
 template <typename T>
 int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d, int gh, int gw,
                  int m, int topk, int s, T* out, cudaStream_t st) {
@@ -357,13 +372,23 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
   int32_t* qidx = reinterpret_cast<int32_t*>(ws + L.qidx);
   const LandmarkWs lw = carve_landmark_ws(ws + L.lm, L.plan, BH, N, d, m);
+  {
+    const long long nh = (long long)BH * m * ((N + kBucketChunk - 1) / kBucketChunk);
+    MITA_CUDA(launch_pdl(forward_zero_kernel, dim3((unsigned)std::min<long long>(
+                             (nh + 255) / 256 + 1, (long long)ds->num_sms * 4)),
+                         dim3(256), 0, st, lw.nslow, 1LL, reinterpret_cast<int*>(ws + L.rt),
+                         (long long)BH, reinterpret_cast<int*>(ws + L.bk), nh),
+              "counter clearing");
+    count_launch();
+  }
   MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, m, qt, st), "pool launch");
-  MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, ds->status, st),
+  MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, ds->status, st,
+                               true),
             "landmark launch");
   // the tensor-core route also counts the bucket stage's (expert, chunk) histogram
   bool counted = false;
   MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, ds, ws + L.rt, st,
-                              reinterpret_cast<int*>(ws + L.bk), &counted),
+                              reinterpret_cast<int*>(ws + L.bk), &counted, true),
             "route launch");
   MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, counted),
             "bucket launch");

@@ -56,7 +56,8 @@ LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, i
 template <typename T>
 cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, int N, int d,
                             int m, int topk, const LandmarkPlan& plan, const LandmarkWs& ws,
-                            int32_t* topk_idx, float* v_tilde, int* status, cudaStream_t st);
+                            int32_t* topk_idx, float* v_tilde, int* status, cudaStream_t st,
+                            bool prezeroed = false);   // ws.nslow already cleared on the stream
 
 bool landmark_tc_eligible(int d, int N, int topk);
 void plan_landmark_tc(LandmarkPlan& p, int BH, int N, int m, int topk, int num_sms);
@@ -102,7 +103,7 @@ bool route_tc_supported(int d, int m);
 // that launch_bucket(..., counted = true) can skip its counting pass.
 cudaError_t launch_route_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH, int N,
                             int m, int num_sms, int32_t* route, int* amb, int* status, int* hist,
-                            cudaStream_t st);
+                            cudaStream_t st, bool prezeroed = false);   // amb counts, hist cleared
 
 bool expert_tc_supported(int d, int m, int topk);
 size_t expert_tc_ws_bytes(int BH, int N, int m, int topk);

@@ -589,9 +589,9 @@ cudaError_t run_partial(const T* qt, const T* k, const T* v, int BH, int N, int 
 template <typename T, int D>
 cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int topk,
                 const LandmarkPlan& p, const LandmarkWs& ws, int32_t* topk_idx, float* vt,
-                int* status, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(ws.nslow, 0, sizeof(int), st);
-  if (e != cudaSuccess) return e;
+                int* status, cudaStream_t st, bool prezeroed) {
+  cudaError_t e = cudaSuccess;
+  if (!prezeroed && (e = cudaMemsetAsync(ws.nslow, 0, sizeof(int), st)) != cudaSuccess) return e;
   if constexpr (std::is_same<T, bf16>::value && D == 64) {
     if (p.tc) {
       e = launch_landmark_tc_passes(qt, k, v, BH, N, m, topk, p, ws, vt, status, st);
@@ -707,10 +707,12 @@ LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, i
 template <typename T>
 cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, int N, int d,
                             int m, int topk, const LandmarkPlan& plan, const LandmarkWs& ws,
-                            int32_t* topk_idx, float* v_tilde, int* status, cudaStream_t st) {
+                            int32_t* topk_idx, float* v_tilde, int* status, cudaStream_t st,
+                            bool prezeroed) {
 #define MITA_LM_CASE(DD)                                                                     \
   case DD:                                                                                   \
-    return run<T, DD>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, status, st);
+    return run<T, DD>(q_tilde, k, v, BH, N, m, topk, plan, ws, topk_idx, v_tilde, status, st, \
+                      prezeroed);
   switch (d) {
     MITA_LM_CASE(16)
     MITA_LM_CASE(32)
@@ -724,9 +726,9 @@ cudaError_t launch_landmark(const T* q_tilde, const T* k, const T* v, int BH, in
 template cudaError_t launch_landmark<float>(const float*, const float*, const float*, int, int,
                                             int, int, int, const LandmarkPlan&,
                                             const LandmarkWs&, int32_t*, float*, int*,
-                                            cudaStream_t);
+                                            cudaStream_t, bool);
 template cudaError_t launch_landmark<bf16>(const bf16*, const bf16*, const bf16*, int, int, int,
                                            int, int, const LandmarkPlan&, const LandmarkWs&,
-                                           int32_t*, float*, int*, cudaStream_t);
+                                           int32_t*, float*, int*, cudaStream_t, bool);
 
 }  // namespace mita

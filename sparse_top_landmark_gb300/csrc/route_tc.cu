@@ -471,7 +471,7 @@ bool route_tc_supported(int d, int m) { return d == 64 && m >= 1 && m <= kMaxM; 
 
 cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, int m,
                             int num_sms, int32_t* route, int* amb, int* status, int* hist,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool prezeroed) {
   // chunk width: 32, 64 or 128 landmarks (a power of two, so the four group
   // buffers fill a power-of-two tensor-memory allocation)
   int W = 32;
@@ -489,9 +489,9 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(amb, 0, (size_t)BH * sizeof(int), st);
-  if (e != cudaSuccess) return e;
-  if (hist) {
+  if (!prezeroed && (e = cudaMemsetAsync(amb, 0, (size_t)BH * sizeof(int), st)) != cudaSuccess)
+    return e;
+  if (hist && !prezeroed) {
     const size_t nh = (size_t)BH * m * ((N + kBucketChunk - 1) / kBucketChunk);
     if ((e = cudaMemsetAsync(hist, 0, nh * sizeof(int), st)) != cudaSuccess) return e;
   }
