@@ -12,6 +12,7 @@ GPU (the forward does not shard); `value` counts the queries of all ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -49,15 +50,18 @@ def peaks():
 # Algorithmic work per stage (flops, bytes) for the whole batch
 # ---------------------------------------------------------------------------
 def stage_work(w):
-    BH, N, d, m, k = w.B * w.H, w.N, w.d, w.m, w.topk
+    """s routes per query: s route entries, bucket entries and expert pairs per query (the
+    shared branch's 2Nmd output flops are counted with the expert stage either way)."""
+    BH, N, d, m, k, s = w.B * w.H, w.N, w.d, w.m, w.topk, w.s
     e = 2 if w.dtype == "bf16" else 4
     return {
         "pool": (0.0, BH * (N * d * e + m * d * e)),
         "landmark": (BH * 4.0 * m * N * d, BH * (2 * N * d * e + m * d * e + m * k * 4 + m * d * 4)),
-        "route": (BH * 2.0 * N * m * d, BH * (N * d * e + m * d * e + 4 * N)),
-        "bucket": (0.0, BH * (12 * N + 4 * (m + 1))),
-        "expert": (BH * (4.0 * N * k * d + 2.0 * N * m * d),
-                   BH * (2 * N * d * e + 2 * m * k * d * e + 4 * m * k + 4 * N + m * d * (e + 4))),
+        "route": (BH * 2.0 * N * m * d, BH * (N * d * e + m * d * e + 4 * N * s)),
+        "bucket": (0.0, BH * (12 * N * s + 4 * (m + 1))),
+        "expert": (BH * (4.0 * N * s * k * d + 2.0 * N * m * d),
+                   BH * (2 * N * d * e + 2 * m * k * d * e + 4 * m * k + 4 * N * s
+                         + m * d * (e + 4))),
     }
 
 
@@ -255,7 +259,7 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args.workload, args.s)
     q, k, v = W.make_qkv(w, 0)
     per = []
     budget = max(2.0, min(15.0, 150.0 / (args.warmup + args.steps)))
@@ -294,17 +298,17 @@ def stage_times(mita, w, dq, dk, dv, reps, stream):
     qt = torch.empty((w.B, w.H, w.m, w.d), dtype=dq.dtype, device=dq.device)
     ti = torch.empty((w.B, w.H, w.m, w.topk), dtype=torch.int32, device=dq.device)
     vt = torch.empty((w.B, w.H, w.m, w.d), dtype=torch.float32, device=dq.device)
-    r = torch.empty((w.B, w.H, w.N, 1), dtype=torch.int32, device=dq.device)
+    r = torch.empty((w.B, w.H, w.N, w.s), dtype=torch.int32, device=dq.device)
     off = torch.empty((w.B, w.H, w.m + 1), dtype=torch.int32, device=dq.device)
-    qi = torch.empty((w.B, w.H, w.N), dtype=torch.int32, device=dq.device)
+    qi = torch.empty((w.B, w.H, w.N * w.s), dtype=torch.int32, device=dq.device)
     out = torch.empty_like(dq)
     calls = {
         "pool": lambda: mita.mita_pool(dq, w.grid_h, w.grid_w, w.m, q_tilde=qt, stream=stream),
         "landmark": lambda: mita.mita_landmark_topk_shared(qt, dk, dv, w.topk, topk_idx=ti,
                                                            v_tilde=vt, stream=stream),
-        "route": lambda: mita.mita_route(dq, qt, route_idx=r, stream=stream),
+        "route": lambda: mita.mita_route(dq, qt, s=w.s, route_idx=r, stream=stream),
         "bucket": lambda: mita.mita_bucket(r, w.m, bucket_off=off, bucket_qidx=qi, stream=stream),
-        "expert": lambda: mita.mita_expert_attn(dq, dk, dv, qt, vt, ti, off, qi, out=out,
+        "expert": lambda: mita.mita_expert_attn(dq, dk, dv, qt, vt, ti, off, qi, s=w.s, out=out,
                                                 stream=stream),
     }
     for fn in calls.values():     # warm, and fill every intermediate
@@ -394,7 +398,7 @@ def roofline_entry(w, stages, pk):
     ent["frac"] = ent["achieved"] / ent["peak"]
     ent["kernel"] = name
     ent["peak_source"] = pk["src"]
-    ent["traffic"] = expert_traffic(w.name) if name == "expert" else None
+    ent["traffic"] = expert_traffic(w.name) if name == "expert" and w.s == 1 else None
     per = {}
     for s, tt in stages.items():
         rl = roofline_s(*work[s], pk)
@@ -402,10 +406,18 @@ def roofline_entry(w, stages, pk):
     return ent, per
 
 
+def workload_of(name, s):
+    """A named workload, with its routes per query replaced by `s` when given."""
+    w = W.WORKLOADS[name]
+    if s is not None and s != w.s:
+        w = dataclasses.replace(w, s=s, name=f"{w.name}_s{s}")
+    return w
+
+
 def forward_only(args):
     from sparse_top_landmark_gb300 import build, mita
     build.build()
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args.workload, args.s)
     q, k, v = W.make_qkv(w, 0)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     out = torch.empty_like(dq)
@@ -426,6 +438,8 @@ def main():
     ap.add_argument("--workload", default="long_1m", choices=list(W.WORKLOADS))
     ap.add_argument("--secondary", default="long_64k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--s", type=int, default=None,
+                    help="routes per query (top-s); default: the workload's own (1)")
     ap.add_argument("--forward-only", type=int, default=0, metavar="R",
                     help="run R untimed forwards of --workload and exit (for profilers)")
     args = ap.parse_args()
@@ -451,12 +465,12 @@ def main():
     stream = torch.cuda.Stream(dev)
     pk = peaks()
 
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args.workload, args.s)
     main_res = bench_workload(mita, w, args, dev, stream, n_gpus)
     roof, per_stage = roofline_entry(w, main_res["stages"], pk)
     sec = None
     if args.secondary and args.secondary not in ("none", args.workload):
-        w2 = W.WORKLOADS[args.secondary]
+        w2 = workload_of(args.secondary, args.s)
         r2 = bench_workload(mita, w2, args, dev, stream, n_gpus, do_e2e=False)
         roof2, per2 = roofline_entry(w2, r2["stages"], pk)
         sec = {"workload": w2.name, "value": r2["value"], "ms_per_step": r2["ms_per_step"],

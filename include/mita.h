@@ -34,8 +34,9 @@
  *     a CUDA graph: make one call of the same size outside capture first.
  *     mita_workspace_release() frees the cache.
  *   - Supported: d in {16, 32, 64, 128}; 1 <= topk <= min(N, 4096);
- *     1 <= m <= N; s == 1 (the setting of every experiment on the pages;
- *     s > 1 returns MITA_ERR_UNSUPPORTED); B*H*N < 2^31.
+ *     1 <= m <= N; 1 <= s <= min(m, 8) (s = 1 is the setting of every
+ *     experiment on the pages and the one with the tensor-core path; s > 1
+ *     runs SIMT kernels); B*H*N*s < 2^31.
  */
 #ifndef MITA_H_
 #define MITA_H_
@@ -103,12 +104,12 @@ int mita_landmark_topk_shared_f32(const float* q_tilde, const float* k, const fl
  *   q [B,H,N,d], q_tilde [B,H,m,d]  inputs.
  *   v_tilde [B,H,m,d] float          input, read only when a shared output is
  *                                    requested (may be NULL otherwise).
- *   route_idx [B,H,N,s] int32        output: argmax_i q . q~_i (exact; ties
- *                                    to the lowest landmark index).
+ *   route_idx [B,H,N,s] int32        output: the s landmarks with the largest
+ *                                    q . q~_i, best first (exact; ties to the
+ *                                    lowest landmark index).
  *   shared_lse [B,H,N] float or NULL output: ln sum_i exp(q . q~_i / sqrt(d)).
  *   shared_o [B,H,N,d] float or NULL output: softmax-weighted sum of v~ over
  *                                    the m shared pairs.
- *   s must be 1.
  */
 int mita_route(const void* q, const void* q_tilde, const float* v_tilde, int B, int H, int N,
                int d, int m, int s, int32_t* route_idx, float* shared_lse, float* shared_o,
@@ -125,9 +126,11 @@ int mita_route_f32(const float* q, const float* q_tilde, const float* v_tilde, i
  *                                      per-expert query counts.
  *   bucket_qidx [B,H,N*s] int32        output: for expert e, the query
  *                                      indices bucket_qidx[off[e]:off[e+1]]
- *                                      in ascending order (a stable sort).
+ *                                      in ascending order (a stable sort;
+ *                                      with s > 1 a query is listed once in
+ *                                      each of its s buckets).
  * Values outside [0, m) are skipped and flag MITA_ERR_DEVICE_CHECK.  Uses the
- * workspace cache.  s must be 1.
+ * workspace cache.
  */
 int mita_bucket(const int32_t* route_idx, int B, int H, int N, int m, int s,
                 int32_t* bucket_off, int32_t* bucket_qidx, mita_stream_t stream);
@@ -142,7 +145,7 @@ int mita_bucket(const int32_t* route_idx, int B, int H, int N, int m, int s,
  * compiled into the library (held by every GPU that loads it until exit), so
  * it calls no allocator at all.
  *   Same arguments and outputs as mita_bucket.
- *   Limit: B*H*(ceil(N/4096)+1)*m <= 1048576, else MITA_ERR_UNSUPPORTED and
+ *   Limit: B*H*(ceil(N*s/4096)+1)*m <= 1048576, else MITA_ERR_UNSUPPORTED and
  *   nothing runs.
  *   The array is shared by every call and keeps the last call's contents;
  *   each call clears what it uses first.  Calls that overlap on the GPU
@@ -161,12 +164,17 @@ int mita_bucket_noalloc(const int32_t* route_idx, int B, int H, int N, int m, in
  * Tutorial ch. 4 steps 5-6 (eq. 11-12): logits [q . q~_i / sqrt(d)]_{i<m}
  * followed by [q . k_j / sqrt(d)]_{j in expert}, one softmax, values
  * [v~_i] then [v_j].  With a precomputed shared partial the two branches are
- * merged by (Z1 o1 + Z2 o2) / (Z1 + Z2) (tutorial ch. 4).
+ * merged by (Z1 o1 + Z2 o2) / (Z1 + Z2) (tutorial ch. 4).  With s > 1 each
+ * query gets m + s*k logits: the raw pairs of all s of its experts (rows two
+ * experts share count twice); every (query, expert) pair yields a partial and
+ * the partials are merged per query by the same rule.
  *   q, k, v [B,H,N,d]; q_tilde [B,H,m,d]; v_tilde [B,H,m,d] float;
- *   topk_idx [B,H,m,topk]; bucket_off [B,H,m+1]; bucket_qidx [B,H,N]   inputs.
+ *   topk_idx [B,H,m,topk]; bucket_off [B,H,m+1]; bucket_qidx [B,H,N*s]  inputs.
  *   shared_lse, shared_o   the partial from mita_route, or both NULL to
  *                          recompute the shared branch here.
- *   out [B,H,N,d]          output (every query appearing in bucket_qidx).
+ *   out [B,H,N,d]          output (every query appearing in bucket_qidx; with
+ *                          s > 1 every query must appear in exactly s buckets,
+ *                          else MITA_ERR_DEVICE_CHECK).
  * Indices outside their range are skipped and flag MITA_ERR_DEVICE_CHECK.
  */
 int mita_expert_attn(const void* q, const void* k, const void* v, const void* q_tilde,
@@ -213,7 +221,8 @@ int mita_forward_host_f32(const float* q, const float* k, const float* v, int B,
                           mita_stream_t stream);
 
 /* Bytes of workspace mita_forward needs for this shape (0 if invalid). */
-uint64_t mita_forward_workspace_bytes(int B, int H, int N, int d, int m, int topk, int is_f32);
+uint64_t mita_forward_workspace_bytes(int B, int H, int N, int d, int m, int topk, int s,
+                                      int is_f32);
 
 /* Text for a status code (static storage). */
 const char* mita_status_string(int status);

@@ -159,7 +159,15 @@ int check_topk(int N, int topk) {
 
 int check_s(int m, int s) {
   if (s < 1 || s > m) return fail(MITA_ERR_INVALID_ARG, "need 1 <= s <= m (s=%d)", s);
-  if (s != 1) return fail(MITA_ERR_UNSUPPORTED, "s=%d: only s=1 is implemented", s);
+  if (s > kMaxRouteS)
+    return fail(MITA_ERR_UNSUPPORTED, "s=%d above this build's limit %d", s, kMaxRouteS);
+  return MITA_OK;
+}
+
+// B*H*N*s route entries must stay below 2^31
+int check_entries(int B, int H, int N, int s) {
+  if ((long long)B * H * N * s >= (1LL << 31))
+    return fail(MITA_ERR_UNSUPPORTED, "B*H*N*s must be < 2^31");
   return MITA_OK;
 }
 
@@ -228,23 +236,23 @@ int landmark_impl(const T* qt, const T* k, const T* v, int B, int H, int N, int 
 size_t route_ws_bytes(int BH, int N) { return (size_t)BH * (2 * (size_t)N + 1) * sizeof(int); }
 
 template <typename T>
-bool route_uses_tc(int d, int m, const float* lse, const float* so) {
-  return std::is_same<T, bf16>::value && !lse && !so && route_tc_supported(d, m);
+bool route_uses_tc(int d, int m, int s, const float* lse, const float* so) {
+  return std::is_same<T, bf16>::value && s == 1 && !lse && !so && route_tc_supported(d, m);
 }
 
 template <typename T>
 cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int N, int d, int m,
-                           int32_t* route, float* lse, float* so, DevState* ds, void* ws,
+                           int s, int32_t* route, float* lse, float* so, DevState* ds, void* ws,
                            cudaStream_t st, int* hist = nullptr, bool* counted = nullptr,
                            bool prezeroed = false) {
   if constexpr (std::is_same<T, bf16>::value) {
-    if (route_uses_tc<T>(d, m, lse, so)) {
+    if (route_uses_tc<T>(d, m, s, lse, so)) {
       if (counted) *counted = hist != nullptr;
       return launch_route_tc(q, qt, BH, N, m, ds->num_sms, route, static_cast<int*>(ws),
                              ds->status, hist, st, prezeroed);
     }
   }
-  return launch_route<T>(q, qt, vt, BH, N, d, m, route, lse, so, st);
+  return launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st);
 }
 
 template <typename T>
@@ -253,14 +261,15 @@ int route_impl(const T* q, const T* qt, const float* vt, int B, int H, int N, in
   MITA_TRY(check_shape(B, H, N, d));
   MITA_TRY(check_m(N, m));
   MITA_TRY(check_s(m, s));
+  MITA_TRY(check_entries(B, H, N, s));
   MITA_TRY(check_ptrs({{q, "q"}, {qt, "q_tilde"}, {route, "route_idx"}}));
   if (lse || so) MITA_TRY(check_ptrs({{vt, "v_tilde"}}));
   if (so) MITA_TRY(check_ptrs({{so, "shared_o"}}));
   DevState* ds = nullptr;
   MITA_TRY(device_state(&ds));
   void* ws = nullptr;
-  if (route_uses_tc<T>(d, m, lse, so)) MITA_TRY(workspace(route_ws_bytes(B * H, N), st, &ws));
-  MITA_CUDA(route_dispatch<T>(q, qt, vt, B * H, N, d, m, route, lse, so, ds, ws, st),
+  if (route_uses_tc<T>(d, m, s, lse, so)) MITA_TRY(workspace(route_ws_bytes(B * H, N), st, &ws));
+  MITA_CUDA(route_dispatch<T>(q, qt, vt, B * H, N, d, m, s, route, lse, so, ds, ws, st),
             "route launch");
   return MITA_OK;
 }
@@ -271,12 +280,14 @@ int bucket_impl(const int32_t* route, int B, int H, int N, int m, int s, int32_t
   if ((long long)B * H * N >= (1LL << 31)) return fail(MITA_ERR_UNSUPPORTED, "B*H*N >= 2^31");
   MITA_TRY(check_m(N, m));
   MITA_TRY(check_s(m, s));
+  MITA_TRY(check_entries(B, H, N, s));
   if (!route || !off || !qidx) return fail(MITA_ERR_INVALID_ARG, "NULL bucket argument");
   DevState* ds = nullptr;
   MITA_TRY(device_state(&ds));
   void* ws = nullptr;
-  MITA_TRY(workspace(bucket_ws_bytes(B * H, N, m), st, &ws));
-  MITA_CUDA(launch_bucket(route, B * H, N, m, ws, off, qidx, ds->status, st), "bucket launch");
+  MITA_TRY(workspace(bucket_ws_bytes(B * H, N * s, m), st, &ws));
+  MITA_CUDA(launch_bucket(route, B * H, N, m, ws, off, qidx, ds->status, st, false, s),
+            "bucket launch");
   return MITA_OK;
 }
 
@@ -289,6 +300,7 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
   MITA_TRY(check_m(N, m));
   MITA_TRY(check_topk(N, topk));
   MITA_TRY(check_s(m, s));
+  MITA_TRY(check_entries(B, H, N, s));
   MITA_TRY(check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}}));
   if (!ti || !off || !qidx) return fail(MITA_ERR_INVALID_ARG, "NULL index argument");
   if ((lse == nullptr) != (so == nullptr))
@@ -296,6 +308,29 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
   if (so == nullptr) MITA_TRY(check_ptrs({{qt, "q_tilde"}, {vt, "v_tilde"}}));
   DevState* ds = nullptr;
   MITA_TRY(device_state(&ds));
+  if (s > 1) {
+    // per-expert partials, merged per query with the shared branch's partial; without a
+    // caller-supplied shared partial it is computed here (the SIMT route, s = 1, into scratch)
+    const int BH = B * H;
+    const size_t pb = align256(expert_partials_ws_bytes(BH, N, d, s));
+    const size_t rb = align256((size_t)BH * N * 4), lb = align256((size_t)BH * N * 4);
+    const size_t ob = align256((size_t)BH * N * d * 4);
+    void* wsv = nullptr;
+    MITA_TRY(workspace(pb + (so ? 0 : rb + lb + ob), st, &wsv));
+    char* ws = static_cast<char*>(wsv);
+    if (so == nullptr) {
+      int32_t* r1 = reinterpret_cast<int32_t*>(ws + pb);
+      float* l1 = reinterpret_cast<float*>(ws + pb + rb);
+      float* o1 = reinterpret_cast<float*>(ws + pb + rb + lb);
+      MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, 1, r1, l1, o1, st), "shared partial");
+      lse = l1;
+      so = o1;
+    }
+    MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, BH, N, d, m, topk, s,
+                                    ws, out, ds->status, st),
+              "expert launch");
+    return MITA_OK;
+  }
   if constexpr (std::is_same<T, bf16>::value) {
     if (so == nullptr && expert_tc_supported(d, m, topk)) {
       void* ws = nullptr;
@@ -307,31 +342,36 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
     }
   }
   MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, B * H, N, d, m, topk,
-                                  out, ds->status, st),
+                                  1, nullptr, out, ds->status, st),
             "expert launch");
   return MITA_OK;
 }
 
 struct ForwardLayout {
-  size_t qt, vt, ti, route, off, qidx, lm, bk, ex, rt, total;
+  size_t qt, vt, ti, route, off, qidx, lm, bk, ex, rt, lse, so, total;
   LandmarkPlan plan;
 };
 
-ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, size_t esize, int sms) {
+ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, int s, size_t esize, int sms) {
   ForwardLayout L{};
   L.plan = plan_landmark(BH, N, d, m, topk, sms, esize == 2);
+  const size_t NS = (size_t)N * s;
   size_t o = 0;
   L.qt = o; o += align256((size_t)BH * m * d * esize);
   L.vt = o; o += align256((size_t)BH * m * d * 4);
   L.ti = o; o += align256((size_t)BH * m * topk * 4);
-  L.route = o; o += align256((size_t)BH * N * 4);
+  L.route = o; o += align256((size_t)BH * NS * 4);
   L.off = o; o += align256((size_t)BH * (m + 1) * 4);
-  L.qidx = o; o += align256((size_t)BH * N * 4);
+  L.qidx = o; o += align256((size_t)BH * NS * 4);
   L.lm = o; o += align256(landmark_ws_bytes(L.plan, BH, N, d, m));
-  L.bk = o; o += align256(bucket_ws_bytes(BH, N, m));
+  L.bk = o; o += align256(bucket_ws_bytes(BH, (int)NS, m));
   L.ex = o;
-  if (esize == 2 && expert_tc_supported(d, m, topk)) o += align256(expert_tc_ws_bytes(BH, N, m, topk));
+  if (s > 1) o += align256(expert_partials_ws_bytes(BH, N, d, s));
+  else if (esize == 2 && expert_tc_supported(d, m, topk)) o += align256(expert_tc_ws_bytes(BH, N, m, topk));
   L.rt = o; o += align256(route_ws_bytes(BH, N));
+  // s > 1: the shared branch's partial, emitted by the route kernel
+  L.lse = o; if (s > 1) o += align256((size_t)BH * N * 4);
+  L.so = o; if (s > 1) o += align256((size_t)BH * N * d * 4);
   L.total = o;
   return L;
 }
@@ -357,11 +397,12 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   MITA_TRY(check_grid(N, gh, gw, m));
   MITA_TRY(check_topk(N, topk));
   MITA_TRY(check_s(m, s));
+  MITA_TRY(check_entries(B, H, N, s));
   MITA_TRY(check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}}));
   DevState* ds = nullptr;
   MITA_TRY(device_state(&ds));
   const int BH = B * H;
-  const ForwardLayout L = forward_layout(BH, N, d, m, topk, sizeof(T), ds->num_sms);
+  const ForwardLayout L = forward_layout(BH, N, d, m, topk, s, sizeof(T), ds->num_sms);
   void* wsv = nullptr;
   MITA_TRY(workspace(L.total, st, &wsv));
   char* ws = static_cast<char*>(wsv);
@@ -373,7 +414,7 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   int32_t* qidx = reinterpret_cast<int32_t*>(ws + L.qidx);
   const LandmarkWs lw = carve_landmark_ws(ws + L.lm, L.plan, BH, N, d, m);
   {
-    const long long nh = (long long)BH * m * ((N + kBucketChunk - 1) / kBucketChunk);
+    const long long nh = (long long)BH * m * (((long long)N * s + kBucketChunk - 1) / kBucketChunk);
     MITA_CUDA(launch_pdl(forward_zero_kernel, dim3((unsigned)std::min<long long>(
                              (nh + 255) / 256 + 1, (long long)ds->num_sms * 4)),
                          dim3(256), 0, st, lw.nslow, 1LL, reinterpret_cast<int*>(ws + L.rt),
@@ -385,10 +426,23 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, ds->status, st,
                                true),
             "landmark launch");
+  if (s > 1) {
+    // top-s routing with the shared branch's partial, grouping of the N*s (query, expert)
+    // entries, per-expert partials and their merge
+    float* lse = reinterpret_cast<float*>(ws + L.lse);
+    float* so = reinterpret_cast<float*>(ws + L.so);
+    MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st), "route launch");
+    MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, false, s),
+              "bucket launch");
+    MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, BH, N, d, m, topk, s,
+                                    ws + L.ex, out, ds->status, st),
+              "expert launch");
+    return MITA_OK;
+  }
   // the tensor-core route also counts the bucket stage's (expert, chunk) histogram
   bool counted = false;
-  MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, route, nullptr, nullptr, ds, ws + L.rt, st,
-                              reinterpret_cast<int*>(ws + L.bk), &counted, true),
+  MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, 1, route, nullptr, nullptr, ds, ws + L.rt,
+                              st, reinterpret_cast<int*>(ws + L.bk), &counted, true),
             "route launch");
   MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, counted),
             "bucket launch");
@@ -401,7 +455,7 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
     }
   }
   MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, nullptr, nullptr, BH, N, d, m,
-                                  topk, out, ds->status, st),
+                                  topk, 1, nullptr, out, ds->status, st),
             "expert launch");
   return MITA_OK;
 }
@@ -539,15 +593,17 @@ int mita_forward_host_f32(const float* q, const float* k, const float* v, int B,
                                         stream);
 }
 
-uint64_t mita_forward_workspace_bytes(int B, int H, int N, int d, int m, int topk, int is_f32) {
-  if (mita::check_shape(B, H, N, d) || mita::check_m(N, m) || mita::check_topk(N, topk))
+uint64_t mita_forward_workspace_bytes(int B, int H, int N, int d, int m, int topk, int s,
+                                      int is_f32) {
+  if (mita::check_shape(B, H, N, d) || mita::check_m(N, m) || mita::check_topk(N, topk) ||
+      mita::check_s(m, s) || mita::check_entries(B, H, N, s))
     return 0;
   int sms = 152;
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaGetLastError();
-  return mita::forward_layout(B * H, N, d, m, topk, is_f32 ? 4 : 2, sms).total;
+  return mita::forward_layout(B * H, N, d, m, topk, s, is_f32 ? 4 : 2, sms).total;
 }
 
 const char* mita_status_string(int status) {

@@ -17,6 +17,11 @@
 //              popcount ranks equal experts in a batch of 32), so every bucket
 //              lists its queries ascending.
 // Experts beyond kSmemExperts use the same passes with global counters.
+//
+// With s > 1 the grouped list is the flat [N, s] route array (entry n * s + t
+// is query n's t-th expert), so every bucket still lists its queries in
+// ascending order, each query once per chosen expert; the stored value is the
+// query index n = entry / s.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -114,7 +119,7 @@ bucket_offsets_kernel(const int* __restrict__ total, int m, int32_t* __restrict_
 }
 
 __global__ void __launch_bounds__(256)
-bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchunks,
+bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int s, int nchunks,
                       int* __restrict__ hist, const int* __restrict__ total,
                       int32_t* __restrict__ bucket_off, int32_t* __restrict__ bucket_qidx,
                       int* status) {
@@ -165,7 +170,7 @@ bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchun
       __syncwarp();
       if (e >= 0) {
         const int pos = base + __popc(peers & lt);
-        if (pos >= 0 && pos < N) out[pos] = n;
+        if (pos >= 0 && pos < N) out[pos] = s == 1 ? n : n / s;
         else flag_error(status, kDevErrBadBucket);
         if (lane == __ffs(peers) - 1) my[e] = base + __popc(peers);
       }
@@ -184,7 +189,7 @@ bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchun
       __syncwarp();
       if (e >= 0) {
         const int pos = base + __popc(peers & lt);
-        if (pos >= 0 && pos < N) out[pos] = n;
+        if (pos >= 0 && pos < N) out[pos] = s == 1 ? n : n / s;
         else flag_error(status, kDevErrBadBucket);
         if (lane == __ffs(peers) - 1) hgw[(size_t)e * nchunks + chunk] = base - boff[e] + __popc(peers);
       }
@@ -195,14 +200,16 @@ bucket_scatter_kernel(const int32_t* __restrict__ route, int N, int m, int nchun
 
 }  // namespace
 
-size_t bucket_ws_bytes(int BH, int N, int m) {
-  const size_t nchunks = (N + kBucketChunk - 1) / kBucketChunk;
+size_t bucket_ws_bytes(int BH, int entries, int m) {
+  const size_t nchunks = ((size_t)entries + kBucketChunk - 1) / kBucketChunk;
   return (size_t)BH * (nchunks + 1) * m * sizeof(int);
 }
 
 cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* ws,
                           int32_t* bucket_off, int32_t* bucket_qidx, int* status,
-                          cudaStream_t st, bool counted) {
+                          cudaStream_t st, bool counted, int s) {
+  if (s < 1 || (long long)N * s >= (1LL << 31)) return cudaErrorInvalidValue;
+  N *= s;   // entries of the flat route list per head
   const int nchunks = (N + kBucketChunk - 1) / kBucketChunk;
   int* hist = static_cast<int*>(ws);                       // [BH][m][nchunks]
   int* total = hist + (size_t)BH * m * nchunks;             // [BH][m]
@@ -235,8 +242,8 @@ cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* 
     count_launch();
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), s3, st, route_idx, N, m, nchunks,
-                 hist, total, bucket_off, bucket_qidx, status);
+  e = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), s3, st, route_idx, N, m, s,
+                 nchunks, hist, total, bucket_off, bucket_qidx, status);
   count_launch();
   return e;
 }

@@ -10,7 +10,7 @@
 //
 // Limits and sharing rules:
 //   * The array holds kNoAllocScratchInts int32 counters (4 MiB).  A call
-//     needs B*H*(ceil(N/4096)+1)*m of them; larger calls are rejected with
+//     needs B*H*(ceil(N*s/4096)+1)*m of them; larger calls are rejected with
 //     MITA_ERR_UNSUPPORTED before anything runs.
 //   * Every GPU that loads this library's module keeps the 4 MiB until the
 //     process exits.
@@ -49,16 +49,16 @@ extern "C" int mita_bucket_noalloc(const int32_t* route_idx, int B, int H, int N
                                    int32_t* bucket_off, int32_t* bucket_qidx,
                                    mita_stream_t stream) {
   using namespace mita;
-  if (B < 1 || H < 1 || N < 1 || (long long)B * H * N >= (1LL << 31) || m < 1 || m > N ||
-      s < 1 || s > m)
+  if (B < 1 || H < 1 || N < 1 || m < 1 || m > N || s < 1 || s > m)
     return report_error(MITA_ERR_INVALID_ARG, "mita_bucket_noalloc: invalid B, H, N, m or s");
-  if (s != 1) return report_error(MITA_ERR_UNSUPPORTED, "mita_bucket_noalloc: only s = 1");
+  if (s > kMaxRouteS || (long long)B * H * N * s >= (1LL << 31))
+    return report_error(MITA_ERR_UNSUPPORTED, "mita_bucket_noalloc: s or B*H*N*s too large");
   if (!route_idx || !bucket_off || !bucket_qidx)
     return report_error(MITA_ERR_INVALID_ARG, "mita_bucket_noalloc: NULL argument");
-  const size_t need = bucket_ws_bytes(B * H, N, m);
+  const size_t need = bucket_ws_bytes(B * H, N * s, m);
   if (need > kNoAllocScratchInts * sizeof(int))
     return report_error(MITA_ERR_UNSUPPORTED,
-                        "mita_bucket_noalloc: B*H*(ceil(N/4096)+1)*m exceeds the 1048576 counters "
+                        "mita_bucket_noalloc: B*H*(ceil(N*s/4096)+1)*m exceeds the 1048576 counters "
                         "(4 MiB) of its static scratch; use mita_bucket");
 
   int dev = 0;
@@ -81,7 +81,8 @@ extern "C" int mita_bucket_noalloc(const int32_t* route_idx, int B, int H, int N
     scratch = g_na_ptr[dev];
   }
   const cudaError_t e =
-      launch_bucket(route_idx, B * H, N, m, scratch, bucket_off, bucket_qidx, nullptr, stream);
+      launch_bucket(route_idx, B * H, N, m, scratch, bucket_off, bucket_qidx, nullptr, stream,
+                    false, s);
   return e == cudaSuccess ? MITA_OK
                           : report_error(MITA_ERR_CUDA, "mita_bucket_noalloc: launch failed");
 }

@@ -15,6 +15,7 @@ using bf16 = __nv_bfloat16;
 // Limits of this build (checked on the host before any launch).
 // ---------------------------------------------------------------------------
 constexpr int kMaxTopk = 4096;   // experts keep at most this many KV rows
+constexpr int kMaxRouteS = 8;    // experts a query may be routed to (s)
 constexpr int kTcapMax = 64;     // per-split candidates kept by the landmark sweep
 constexpr int kBandCap = 1024;   // near-boundary candidates re-scored exactly
 constexpr int kKeyTile = 32;     // keys staged per shared-memory tile (SIMT path)

@@ -11,6 +11,15 @@
 // One CTA handles one tile of (up to kQTile) queries of one expert; the tile
 // is found from bucket_off (tiles of all experts of a head, in expert order).
 // The expert's K/V rows are gathered once per tile into shared memory.
+//
+// s > 1: a query sits in s buckets.  Each (query, expert) pair then yields a
+// partial over that expert's k raw pairs only -- its log-sum-exp and
+// normalised output -- in one of the query's s partial slots (taken with an
+// atomic counter; the slot records the bucket position).  A second kernel
+// merges, per query, the shared branch's partial and the s raw partials with
+// the tutorial's rule, in ascending bucket position (= ascending expert), so
+// the result does not depend on which CTA took which slot.  Overlapping
+// experts thus contribute duplicated rows, the literal concatenation.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -19,6 +28,18 @@ namespace {
 
 constexpr int kQTile = 64;   // queries per CTA (one per thread)
 constexpr int kRows = 32;    // KV rows staged per chunk
+constexpr int kMergeWarps = 8;
+
+__device__ __forceinline__ void put(float* p, float x) { *p = x; }
+__device__ __forceinline__ void put(bf16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// the s > 1 partials (null when s = 1)
+struct Partials {
+  float* lse;   // [BH*N, s]     natural log-sum-exp of the expert's raw pairs
+  float* o;     // [BH*N, s, D]  their softmax-weighted mean of V
+  int* pos;     // [BH*N, s]     bucket position of the entry
+  int* cnt;     // [BH*N]        slots taken (cleared before the expert kernel)
+};
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kQTile)
@@ -26,8 +47,8 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
                    const T* __restrict__ q_tilde, const float* __restrict__ v_tilde,
                    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ bucket_off,
                    const int32_t* __restrict__ bucket_qidx, const float* __restrict__ shared_lse,
-                   const float* __restrict__ shared_o, int N, int m, int topk,
-                   int tiles_per_bh, T* __restrict__ out, int* status) {
+                   const float* __restrict__ shared_o, int N, int m, int topk, int s,
+                   int tiles_per_bh, T* __restrict__ out, Partials part, int* status) {
   __shared__ __align__(16) float ks[kRows][D];
   __shared__ __align__(16) float vs[kRows][D];
   __shared__ int rowid[kRows];
@@ -36,6 +57,7 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   const long long bh = blockIdx.x / tiles_per_bh;
   const int t = blockIdx.x % tiles_per_bh;
   const int32_t* off = bucket_off + (size_t)bh * (m + 1);
+  const int NS = N * s;   // bucket entries per head
 
   // ---- locate (expert, tile within expert) for this CTA ---------------------
   if (warp == 0) {
@@ -45,7 +67,7 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
       int cnt = 0;
       if (e < m) {
         const int a = off[e], b = off[e + 1];
-        if (a < 0 || b > N || b < a) flag_error(status, kDevErrBadBucket);
+        if (a < 0 || b > NS || b < a) flag_error(status, kDevErrBadBucket);
         else cnt = b - a;
       }
       const int nt = (cnt + kQTile - 1) / kQTile;
@@ -69,7 +91,7 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   bool live = slot < off[e + 1];
   int n = 0;
   if (live) {
-    n = bucket_qidx[(size_t)bh * N + slot];
+    n = bucket_qidx[(size_t)bh * NS + slot];
     if (n < 0 || n >= N) { flag_error(status, kDevErrBadBucket); live = false; }
   }
 
@@ -100,7 +122,9 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   };
 
   // ---- shared branch: the m pairs (q~_i, v~_i) -------------------------------
-  if (shared_o != nullptr) {
+  if (s > 1) {
+    // merged per query afterwards
+  } else if (shared_o != nullptr) {
     if (live) {
       const size_t qi = (size_t)bh * N + n;
       mrun = shared_lse[qi] * 1.4426950408889634f;  // natural -> log2 units
@@ -169,37 +193,141 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     }
   }
   if (!live) return;
-  const float inv = 1.f / lsum;
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
   for (int l = 0; l < D; ++l) acc[l] *= inv;
-  store_row<T, D>(out + ((size_t)bh * N + n) * D, acc);
+  const size_t qi = (size_t)bh * N + n;
+  if (s == 1) {
+    store_row<T, D>(out + qi * D, acc);
+    return;
+  }
+  const int ps = atomicAdd(&part.cnt[qi], 1);   // this pair's partial slot
+  if (ps >= s) {
+    flag_error(status, kDevErrBadBucket);
+    return;
+  }
+  const size_t pi = qi * s + ps;
+  part.lse[pi] = lsum > 0.f ? (mrun + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+  part.pos[pi] = slot;
+#pragma unroll
+  for (int l = 0; l < D; l += 4)
+    *reinterpret_cast<float4*>(part.o + pi * D + l) = make_float4(acc[l], acc[l + 1], acc[l + 2], acc[l + 3]);
+}
+
+// s > 1: out = (Z_sh o_sh + sum_t Z_t o_t) / (Z_sh + sum_t Z_t), Z = exp(lse), one warp per
+// query; the s partials are taken in ascending bucket position.
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+expert_merge_kernel(const float* __restrict__ shared_lse, const float* __restrict__ shared_o,
+                    Partials part, long long BHN, int s, T* __restrict__ out, int* status) {
+  const int lane = threadIdx.x & 31;
+  const long long qi = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  if (qi >= BHN) return;
+  if (part.cnt[qi] != s) {
+    if (lane == 0) flag_error(status, kDevErrBadBucket);
+    return;
+  }
+  float pl = -INFINITY;
+  int pp = 0x7fffffff;
+  if (lane < s) {
+    pl = part.lse[qi * s + lane];
+    pp = part.pos[qi * s + lane];
+  }
+  int rank = 0;
+  float M = shared_lse[qi];
+  for (int t = 0; t < s; ++t) {
+    rank += __shfl_sync(0xffffffffu, pp, t) < pp ? 1 : 0;
+    M = fmaxf(M, __shfl_sync(0xffffffffu, pl, t));
+  }
+  constexpr float kL2e = 1.4426950408889634f;
+  constexpr int PER = (D + 31) / 32;
+  const float wsh = exp2f((shared_lse[qi] - M) * kL2e);
+  float z = wsh;
+  float acc[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int l = lane + 32 * j;
+    acc[j] = l < D ? wsh * shared_o[qi * D + l] : 0.f;
+  }
+  for (int r = 0; r < s; ++r) {
+    const unsigned who = __ballot_sync(0xffffffffu, lane < s && rank == r);
+    if (who == 0) {   // two partials claim one bucket position
+      if (lane == 0) flag_error(status, kDevErrBadBucket);
+      return;
+    }
+    const int src = __ffs(who) - 1;
+    const float w = exp2f((__shfl_sync(0xffffffffu, pl, src) - M) * kL2e);
+    z += w;
+    const float* o = part.o + ((size_t)qi * s + src) * D;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int l = lane + 32 * j;
+      if (l < D) acc[j] = fmaf(w, o[l], acc[j]);
+    }
+  }
+  const float inv = 1.f / z;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int l = lane + 32 * j;
+    if (l < D) put(out + qi * D + l, acc[j] * inv);
+  }
 }
 
 template <typename T, int D>
 cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt,
                 const int32_t* ti, const int32_t* off, const int32_t* qidx, const float* lse,
-                const float* so, int BH, int N, int m, int topk, T* out, int* status,
-                cudaStream_t st) {
-  const int tiles = (N + kQTile - 1) / kQTile + m;
+                const float* so, int BH, int N, int m, int topk, int s, void* pws, T* out,
+                int* status, cudaStream_t st) {
+  const int tiles = (int)(((long long)N * s + kQTile - 1) / kQTile) + m;
   const long long blocks = (long long)BH * tiles;
+  Partials part{};
+  const long long BHN = (long long)BH * N;
+  if (s > 1) {
+    char* p = static_cast<char*>(pws);
+    part.o = reinterpret_cast<float*>(p);
+    p += (size_t)BHN * s * D * sizeof(float);
+    part.lse = reinterpret_cast<float*>(p);
+    p += (size_t)BHN * s * sizeof(float);
+    part.pos = reinterpret_cast<int*>(p);
+    p += (size_t)BHN * s * sizeof(int);
+    part.cnt = reinterpret_cast<int*>(p);
+    const cudaError_t e = cudaMemsetAsync(part.cnt, 0, (size_t)BHN * sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
   expert_attn_kernel<T, D><<<(unsigned)blocks, kQTile, 0, st>>>(
-      q, k, v, qt, vt, ti, off, qidx, lse, so, N, m, topk, tiles, out, status);
+      q, k, v, qt, vt, ti, off, qidx, lse, so, N, m, topk, s, tiles, out, part, status);
   count_launch();
+  if (s > 1) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    expert_merge_kernel<T, D><<<(unsigned)((BHN + kMergeWarps - 1) / kMergeWarps),
+                                kMergeWarps * 32, 0, st>>>(lse, so, part, BHN, s, out, status);
+    count_launch();
+  }
   return cudaGetLastError();
 }
 
 }  // namespace
+
+size_t expert_partials_ws_bytes(int BH, int N, int d, int s) {
+  if (s <= 1) return 0;
+  const size_t r = (size_t)BH * N;
+  return r * s * d * sizeof(float) + 2 * r * s * sizeof(float) + r * sizeof(int);
+}
 
 template <typename T>
 cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_tilde,
                                const float* v_tilde, const int32_t* topk_idx,
                                const int32_t* bucket_off, const int32_t* bucket_qidx,
                                const float* shared_lse, const float* shared_o, int BH, int N,
-                               int d, int m, int topk, T* out, int* status, cudaStream_t st) {
+                               int d, int m, int topk, int s, void* ws, T* out, int* status,
+                               cudaStream_t st) {
+  if (s < 1 || (s > 1 && (ws == nullptr || shared_lse == nullptr || shared_o == nullptr)))
+    return cudaErrorInvalidValue;
 #define MITA_EXPERT_CASE(DD)                                                                 \
   case DD:                                                                                   \
     return run<T, DD>(q, k, v, q_tilde, v_tilde, topk_idx, bucket_off, bucket_qidx,          \
-                      shared_lse, shared_o, BH, N, m, topk, out, status, st);
+                      shared_lse, shared_o, BH, N, m, topk, s, ws, out, status, st);
   switch (d) {
     MITA_EXPERT_CASE(16)
     MITA_EXPERT_CASE(32)
@@ -213,11 +341,12 @@ cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_ti
 template cudaError_t launch_expert_attn<float>(const float*, const float*, const float*,
                                                const float*, const float*, const int32_t*,
                                                const int32_t*, const int32_t*, const float*,
-                                               const float*, int, int, int, int, int, float*,
-                                               int*, cudaStream_t);
+                                               const float*, int, int, int, int, int, int, void*,
+                                               float*, int*, cudaStream_t);
 template cudaError_t launch_expert_attn<bf16>(const bf16*, const bf16*, const bf16*, const bf16*,
                                               const float*, const int32_t*, const int32_t*,
                                               const int32_t*, const float*, const float*, int,
-                                              int, int, int, int, bf16*, int*, cudaStream_t);
+                                              int, int, int, int, int, void*, bf16*, int*,
+                                              cudaStream_t);
 
 }  // namespace mita

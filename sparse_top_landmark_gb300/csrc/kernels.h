@@ -67,28 +67,34 @@ cudaError_t launch_landmark_tc_passes(const __nv_bfloat16* q_tilde, const __nv_b
                                       int* status, cudaStream_t st);
 
 // ---- step 4: routing (optionally emitting the shared-branch partial) ------
+// route_idx: [BH, N, s], each query's s landmarks best first (1 <= s <= kMaxRouteS).
 template <typename T>
 cudaError_t launch_route(const T* q, const T* q_tilde, const float* v_tilde, int BH, int N,
-                         int d, int m, int32_t* route_idx, float* shared_lse,
+                         int d, int m, int s, int32_t* route_idx, float* shared_lse,
                          float* shared_o, cudaStream_t st);
 
 // ---- step 5: stable grouping of queries by expert -------------------------
-constexpr int kBucketChunk = 4096;   // queries per chunk (one warp each)
-size_t bucket_ws_bytes(int BH, int N, int m);
+constexpr int kBucketChunk = 4096;   // route entries per chunk
+// `entries` = N * s route entries per head
+size_t bucket_ws_bytes(int BH, int entries, int m);
 // ws: [BH][m][nchunks] per-chunk counts, then [BH][m] totals.  counted = the counts are
-// already in ws (left by launch_route_tc's histogram).
+// already in ws (left by launch_route_tc's histogram).  route_idx is [BH, N, s];
+// bucket_qidx receives [BH, N * s] query indices.
 cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* ws,
                           int32_t* bucket_off, int32_t* bucket_qidx, int* status,
-                          cudaStream_t st, bool counted = false);
+                          cudaStream_t st, bool counted = false, int s = 1);
 
 // ---- step 6: expert-grouped joint attention -------------------------------
+// s > 1 needs the shared partial (shared_lse, shared_o) and `ws` of
+// expert_partials_ws_bytes(BH, N, d, s) bytes for the per-expert partials.
+size_t expert_partials_ws_bytes(int BH, int N, int d, int s);
 template <typename T>
 cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_tilde,
                                const float* v_tilde, const int32_t* topk_idx,
                                const int32_t* bucket_off, const int32_t* bucket_qidx,
                                const float* shared_lse, const float* shared_o, int BH,
-                               int N, int d, int m, int topk, T* out, int* status,
-                               cudaStream_t st);
+                               int N, int d, int m, int topk, int s, void* ws, T* out,
+                               int* status, cudaStream_t st);
 
 // ---- tensor-core (tcgen05) kernels: bf16, d = 64 ---------------------------
 // TMA map over a [batches, rows, 64] bf16 array, boxes of box_rows rows.

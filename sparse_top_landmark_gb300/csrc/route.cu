@@ -1,16 +1,19 @@
-// Step 4: route each query to its best landmark (s = 1).
+// Step 4: route each query to its top-s landmarks.
 //
 // MiTA tutorial (iwxt.cn), ch. 4 step 4 (paper eq. 10): a query compares
-// q . q~_i over the m landmarks and keeps the top-s indices; the scores only
-// select (no gate).  gist.science summary Sec. 2.2: s = 1 in practice.
-// The bit.fan article notes that the query-landmark logits are reused as the
-// shared-branch logits; this kernel can emit that branch's partial
-// (log-sum-exp and normalised output over the m shared pairs).
+// q . q~_i over the m landmarks and keeps the top-s indices, best first; the
+// scores only select (no gate).  gist.science summary Sec. 2.2: s = 1 in
+// practice.  The bit.fan article notes that the query-landmark logits are
+// reused as the shared-branch logits; this kernel can emit that branch's
+// partial (log-sum-exp and normalised output over the m shared pairs).
 //
-// Exactness: the fp32 argmax is accepted when it beats the runner-up by more
-// than 2E (E bounds the fp32 dot error); otherwise every landmark within 2E of
-// the best is re-scored with exact-product fp32 arithmetic and the exact
-// maximum wins, ties to the lowest landmark index.
+// Exactness: each thread keeps its s + 1 best fp32 scores in a sorted
+// register list.  The list is accepted when every neighbouring pair in it
+// differs by more than 2E (E bounds the fp32 dot error), i.e. neither the
+// order of the s chosen landmarks nor the cut after the s-th can change in
+// exact arithmetic; otherwise every landmark within 2E of the s-th score is
+// re-scored with exact-product fp32 arithmetic and the exact top-s wins, ties
+// to the lowest landmark index.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,10 +23,27 @@ namespace {
 constexpr int kRouteThreads = 128;   // one query per thread
 constexpr int kLmChunk = 32;         // landmarks staged per smem chunk
 
-template <typename T, int D>
+// Insert (x, i) into the descending list (v, id)[0..L); equal scores keep the
+// earlier entry first (landmarks arrive in ascending index order).
+template <int L, typename S>
+__device__ __forceinline__ void list_insert(S (&v)[L], int (&id)[L], S x, int i) {
+#pragma unroll
+  for (int t = 0; t < L; ++t) {
+    const bool take = x > v[t];
+    const S tv = take ? v[t] : x;
+    const int ti = take ? id[t] : i;
+    v[t] = take ? x : v[t];
+    id[t] = take ? i : id[t];
+    x = tv;
+    i = ti;
+  }
+}
+
+// L = length of the kept list: 2 for s = 1 (best and runner-up), kMaxRouteS + 1 otherwise.
+template <typename T, int D, int L>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
-             const float* __restrict__ v_tilde, int N, int m, int32_t* __restrict__ route,
+             const float* __restrict__ v_tilde, int N, int m, int s, int32_t* __restrict__ route,
              float* __restrict__ shared_lse, float* __restrict__ shared_o) {
   __shared__ __align__(16) float qs[kLmChunk][D];
   __shared__ __align__(16) float vs[kLmChunk][D];
@@ -40,10 +60,10 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
   for (int i = threadIdx.x; i < m; i += kRouteThreads) {
     float r[D];
     load_row<T, D>(qtb + (size_t)i * D, r);
-    float s = 0.f;
+    float nn = 0.f;
 #pragma unroll
-    for (int l = 0; l < D; ++l) s = fmaf(r[l], r[l], s);
-    qt2 = fmaxf(qt2, s);
+    for (int l = 0; l < D; ++l) nn = fmaf(r[l], r[l], nn);
+    qt2 = fmaxf(qt2, nn);
   }
   qt2 = block_max(qt2, red);
 
@@ -58,8 +78,10 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
   for (int l = 0; l < D; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
 
   const float c = (float)(1.4426950408889634 / sqrt((double)D));
-  float best = -INFINITY, second = -INFINITY;
-  int ib = 0;
+  float bv[L];
+  int bi[L];
+#pragma unroll
+  for (int t = 0; t < L; ++t) { bv[t] = -INFINITY; bi[t] = 0; }
   float mrun = -INFINITY, lsum = 0.f;
   float acc[D];
 #pragma unroll
@@ -76,13 +98,12 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
     __syncthreads();
     if (!live) continue;
     for (int t = 0; t < nc; ++t) {
-      float s = 0.f;
+      float sc0 = 0.f;
 #pragma unroll
-      for (int l = 0; l < D; ++l) s = fmaf(qr[l], qs[t][l], s);
-      if (s > best) { second = best; best = s; ib = i0 + t; }
-      else if (s > second) second = s;
+      for (int l = 0; l < D; ++l) sc0 = fmaf(qr[l], qs[t][l], sc0);
+      if (sc0 > bv[L - 1]) list_insert<L>(bv, bi, sc0, i0 + t);
       if (want_shared) {
-        const float x = s * c;
+        const float x = sc0 * c;
         if (x > mrun) {
           const float sc = exp2f(mrun - x);
           lsum *= sc;
@@ -100,25 +121,50 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
   if (!live) return;
 
   const float E = err_gamma(D) * sqrtf(qn2) * sqrtf(qt2);
-  if (best - second <= 2.f * E) {
-    // near tie: re-score the candidates exactly
-    F2 bx{-INFINITY, 0.f};
-    int bi = ib;
+  // the s-th kept score, and whether any neighbouring pair up to the (s+1)-th is within 2E
+  float cut = bv[0];
+  bool near = false;
+#pragma unroll
+  for (int t = 0; t + 1 < L; ++t) {
+    if (t < s) {
+      cut = bv[t];
+      near = near || (bv[t] - bv[t + 1] <= 2.f * E);
+    }
+  }
+  const size_t qi = (size_t)bh * N + n;
+  if (near) {
+    // near tie: re-score every landmark that can still be among the exact top-s
+    F2 xv[L];
+    int xi[L];
+#pragma unroll
+    for (int t = 0; t < L; ++t) { xv[t] = F2{-INFINITY, 0.f}; xi[t] = 0; }
     for (int i = 0; i < m; ++i) {
       float r[D];
       load_row<T, D>(qtb + (size_t)i * D, r);
-      float s = 0.f;
+      float sf = 0.f;
 #pragma unroll
-      for (int l = 0; l < D; ++l) s = fmaf(qr[l], r[l], s);
-      if (s >= best - 2.f * E) {
-        const F2 x = dot_f2<D>(qr, r);
-        if (f2_greater(x, bx)) { bx = x; bi = i; }
+      for (int l = 0; l < D; ++l) sf = fmaf(qr[l], r[l], sf);
+      if (sf >= cut - 2.f * E) {
+        F2 x = dot_f2<D>(qr, r);
+        int ix = i;
+#pragma unroll
+        for (int t = 0; t < L; ++t) {
+          const bool take = f2_greater(x, xv[t]);
+          const F2 tv = take ? xv[t] : x;
+          const int ti = take ? xi[t] : ix;
+          xv[t] = take ? x : xv[t];
+          xi[t] = take ? ix : xi[t];
+          x = tv;
+          ix = ti;
+        }
       }
     }
-    ib = bi;
+#pragma unroll
+    for (int t = 0; t < L; ++t) bi[t] = xi[t];
   }
-  const size_t qi = (size_t)bh * N + n;
-  route[qi] = ib;
+#pragma unroll
+  for (int t = 0; t < L; ++t)
+    if (t < s) route[qi * s + t] = bi[t];
   if (want_shared) {
     const float inv = 1.f / lsum;
     if (shared_lse) shared_lse[qi] = (mrun + log2f(lsum)) * 0.6931471805599453f;  // natural log
@@ -130,11 +176,15 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
 }
 
 template <typename T, int D>
-cudaError_t run(const T* q, const T* qt, const float* vt, int BH, int N, int m, int32_t* route,
-                float* lse, float* o, cudaStream_t st) {
+cudaError_t run(const T* q, const T* qt, const float* vt, int BH, int N, int m, int s,
+                int32_t* route, float* lse, float* o, cudaStream_t st) {
   const long long nqt = (N + kRouteThreads - 1) / kRouteThreads;
-  route_kernel<T, D><<<(unsigned)(BH * nqt), kRouteThreads, 0, st>>>(q, qt, vt, N, m, route,
-                                                                      lse, o);
+  const dim3 grid((unsigned)(BH * nqt));
+  if (s == 1)
+    route_kernel<T, D, 2><<<grid, kRouteThreads, 0, st>>>(q, qt, vt, N, m, 1, route, lse, o);
+  else
+    route_kernel<T, D, kMaxRouteS + 1><<<grid, kRouteThreads, 0, st>>>(q, qt, vt, N, m, s, route,
+                                                                        lse, o);
   count_launch();
   return cudaGetLastError();
 }
@@ -143,20 +193,21 @@ cudaError_t run(const T* q, const T* qt, const float* vt, int BH, int N, int m, 
 
 template <typename T>
 cudaError_t launch_route(const T* q, const T* q_tilde, const float* v_tilde, int BH, int N,
-                         int d, int m, int32_t* route_idx, float* shared_lse, float* shared_o,
-                         cudaStream_t st) {
+                         int d, int m, int s, int32_t* route_idx, float* shared_lse,
+                         float* shared_o, cudaStream_t st) {
+  if (s < 1 || s > kMaxRouteS || s > m) return cudaErrorInvalidValue;
   switch (d) {
-    case 16: return run<T, 16>(q, q_tilde, v_tilde, BH, N, m, route_idx, shared_lse, shared_o, st);
-    case 32: return run<T, 32>(q, q_tilde, v_tilde, BH, N, m, route_idx, shared_lse, shared_o, st);
-    case 64: return run<T, 64>(q, q_tilde, v_tilde, BH, N, m, route_idx, shared_lse, shared_o, st);
-    case 128: return run<T, 128>(q, q_tilde, v_tilde, BH, N, m, route_idx, shared_lse, shared_o, st);
+    case 16: return run<T, 16>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, st);
+    case 32: return run<T, 32>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, st);
+    case 64: return run<T, 64>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, st);
+    case 128: return run<T, 128>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template cudaError_t launch_route<float>(const float*, const float*, const float*, int, int, int,
-                                         int, int32_t*, float*, float*, cudaStream_t);
+                                         int, int, int32_t*, float*, float*, cudaStream_t);
 template cudaError_t launch_route<bf16>(const bf16*, const bf16*, const float*, int, int, int,
-                                        int, int32_t*, float*, float*, cudaStream_t);
+                                        int, int, int32_t*, float*, float*, cudaStream_t);
 
 }  // namespace mita

@@ -62,7 +62,7 @@ def load() -> ctypes.CDLL:
             lib.mita_bucket.restype = I
             lib.mita_bucket_noalloc.argtypes = [P, I, I, I, I, I, P, P, P]
             lib.mita_bucket_noalloc.restype = I
-            lib.mita_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+            lib.mita_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
             lib.mita_forward_workspace_bytes.restype = ctypes.c_uint64
             lib.mita_status_string.argtypes = [I]
             lib.mita_status_string.restype = ctypes.c_char_p
@@ -192,7 +192,7 @@ def mita_bucket(route_idx, m: int, bucket_off=None, bucket_qidx=None, stream=Non
 def mita_bucket_noalloc(route_idx, m: int, bucket_off, bucket_qidx, stream=None):
     """mita_bucket for callers that cannot allocate device memory: the caller
     passes both outputs, and the library uses its fixed 4 MiB device scratch
-    instead of its workspace cache (limit B*H*ceil(N/4096)*m <= 1048576).
+    instead of its workspace cache (limit B*H*(ceil(N*s/4096)+1)*m <= 1048576).
     Calls that overlap on the GPU race on that scratch; order them."""
     _need(route_idx, "route_idx", torch.int32)
     B, H, N, s = route_idx.shape
@@ -214,6 +214,9 @@ def mita_expert_attn(q, k, v, q_tilde, v_tilde, topk_idx, bucket_off, bucket_qid
     _need(out, "out", q.dtype, q.device)
     for t, n in ((topk_idx, "topk_idx"), (bucket_off, "bucket_off"), (bucket_qidx, "bucket_qidx")):
         _need(t, n, torch.int32, q.device)
+    if bucket_qidx.numel() != B * H * N * s:
+        raise ValueError(f"bucket_qidx holds {bucket_qidx.numel()} entries, expected B*H*N*s = "
+                         f"{B * H * N * s}")
     if q_tilde is not None:
         _need(q_tilde, "q_tilde", q.dtype, q.device)
     if v_tilde is not None:
@@ -261,8 +264,8 @@ def mita_forward(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int = 
     return out
 
 
-def forward_workspace_bytes(B, H, N, d, m, topk, dtype=torch.bfloat16) -> int:
-    return int(load().mita_forward_workspace_bytes(B, H, N, d, m, topk,
+def forward_workspace_bytes(B, H, N, d, m, topk, dtype=torch.bfloat16, s: int = 1) -> int:
+    return int(load().mita_forward_workspace_bytes(B, H, N, d, m, topk, s,
                                                     1 if dtype == torch.float32 else 0))
 
 

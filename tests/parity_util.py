@@ -40,3 +40,33 @@ def assert_close(gpu, ora, dtype, what="output"):
         assert mx <= BF16_MAX_ABS, f"{what}: max-abs {mx:.3e} > {BF16_MAX_ABS}"
         assert rel <= BF16_REL_L2, f"{what}: rel-L2 {rel:.3e} > {BF16_REL_L2}"
     return mx
+
+
+def route_scores(q, q_tilde, rows):
+    """fp64 scores q_n . q~_i of the given flat query rows against their head's
+    landmarks: [len(rows), m] (harness-side, for judging near ties)."""
+    B, H, N, d = q.shape
+    m = q_tilde.shape[2]
+    rows = torch.as_tensor(rows, dtype=torch.int64)
+    qr = q.reshape(-1, d)[rows].double()
+    lt = q_tilde.reshape(B * H, m, d)[rows // N].double()
+    return torch.einsum("rd,rmd->rm", qr, lt)
+
+
+def assert_ranked_routes_match(gpu, ora, q, q_tilde, rows=None, what="route"):
+    """Top-s lists, best first: equal, or every position's oracle score within
+    GAP_TOL * max|score| of the other list's (a near tie, either order correct)."""
+    g = gpu.to("cpu").to(torch.int64).reshape(-1, gpu.shape[-1])
+    o = ora.to("cpu").to(torch.int64).reshape(-1, ora.shape[-1])
+    if rows is None:
+        rows = torch.arange(g.shape[0])
+    diff = (g != o).any(-1).nonzero().flatten()
+    if diff.numel():
+        sc = route_scores(q, q_tilde, torch.as_tensor(rows)[diff])
+        amax = sc.abs().amax(-1, keepdim=True)
+        sg = sc.gather(1, g[diff])
+        so = sc.gather(1, o[diff])
+        bad = ((sg - so).abs() > GAP_TOL * amax).any(-1)
+        assert not bool(bad.any()), (f"{what}: {int(bad.sum())} rows differ beyond a near tie "
+                                     f"(first row {int(torch.as_tensor(rows)[diff][bad][0])})")
+    return int(diff.numel())

@@ -77,14 +77,15 @@ def test_forward_validation(lib):
     assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 0, 1, GOOD, NULL) == 1     # topk 0
     assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 65, 1, GOOD, NULL) == 1    # topk > N
     assert f(GOOD, GOOD, GOOD, 1, 1, 8192, 16, 1, 8192, 4, 4097, 1, GOOD, NULL) == 2  # limit
-    assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 4, 2, GOOD, NULL) == 2     # s = 2
+    assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 16, 4, 9, GOOD, NULL) == 2    # s > 8
     assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 4, 5, GOOD, NULL) == 1     # s > m
     assert f(GOOD, GOOD, NULL, 1, 1, 64, 16, 1, 64, 4, 4, 1, GOOD, NULL) == 1     # v NULL
 
 
 def test_stage_validation(lib):
-    assert lib.mita_route(GOOD, GOOD, NULL, 1, 1, 64, 16, 4, 2, GOOD, NULL, NULL, NULL) == 2
-    assert lib.mita_bucket(GOOD, 1, 1, 64, 4, 2, GOOD, GOOD, NULL) == 2
+    assert lib.mita_route(GOOD, GOOD, NULL, 1, 1, 64, 16, 16, 9, GOOD, NULL, NULL, NULL) == 2
+    assert lib.mita_route(GOOD, GOOD, NULL, 1, 1, 64, 16, 4, 5, GOOD, NULL, NULL, NULL) == 1
+    assert lib.mita_bucket(GOOD, 1, 1, 64, 16, 9, GOOD, GOOD, NULL) == 2
     assert lib.mita_bucket(NULL, 1, 1, 64, 4, 1, GOOD, GOOD, NULL) == 1
     assert lib.mita_landmark_topk_shared(GOOD, GOOD, GOOD, 1, 1, 64, 16, 4, 0, GOOD, GOOD,
                                          NULL) == 1
@@ -94,9 +95,13 @@ def test_stage_validation(lib):
 
 
 def test_workspace_bytes_query(lib):
-    n = lib.mita_forward_workspace_bytes(4, 2, 65536, 64, 128, 128, 0)
+    n = lib.mita_forward_workspace_bytes(4, 2, 65536, 64, 128, 128, 1, 0)
     assert n > 4 * 2 * 65536 * 8        # at least the route + bucket arrays
-    assert lib.mita_forward_workspace_bytes(1, 1, 64, 48, 4, 4, 0) == 0
+    assert lib.mita_forward_workspace_bytes(1, 1, 64, 48, 4, 4, 1, 0) == 0
+    # s = 2: routes and bucket lists twice as long, plus the per-expert partials (fp32 rows)
+    n2 = lib.mita_forward_workspace_bytes(4, 2, 65536, 64, 128, 128, 2, 0)
+    assert n2 > 4 * 2 * 65536 * (2 * 64 * 4 + 2 * 2 * 4)
+    assert lib.mita_forward_workspace_bytes(4, 2, 65536, 64, 128, 128, 9, 0) == 0
 
 
 def test_launch_counter_is_readable_without_a_gpu(lib):

@@ -31,7 +31,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     rc = lib.mita_bucket_noalloc(g, 4, 8, 1 << 20, 512, 1, g, g, None)
     assert rc == MITA_ERR_UNSUPPORTED
     assert b"static scratch" in lib.mita_last_error_message()
-    assert lib.mita_bucket_noalloc(g, 1, 1, 100, 4, 2, g, g, None) == MITA_ERR_UNSUPPORTED
+    assert lib.mita_bucket_noalloc(g, 1, 1, 100, 16, 9, g, g, None) == MITA_ERR_UNSUPPORTED
     assert lib.mita_bucket_noalloc(None, 1, 1, 100, 4, 1, g, g, None) == MITA_ERR_INVALID_ARG
 
 
