@@ -46,10 +46,13 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_long
             lib.orc_pool.argtypes = [P, I, I, I, I, I, I, I, I, I, P]
+            lib.orc_pool_grid.argtypes = [P, I, I, I, I, I, I, I, I, I, I, P]
             lib.orc_landmark_rows.argtypes = [P, P, P, I, I, I, I, I, I, I, L, P, P, P, P]
             lib.orc_route_rows.argtypes = [P, I, P, I, I, I, I, I, I, L, P, P, P]
             lib.orc_bucket.argtypes = [P, I, I, I, I, I, P, P]
             lib.orc_attend_rows.argtypes = [P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, L, P, P]
+            lib.orc_attend_rows_t.argtypes = [P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, L, P,
+                                              I, P]
             lib.orc_num_threads.restype = I
             lib.orc_set_num_threads.argtypes = [I]
             _lib = lib
@@ -77,13 +80,23 @@ def _check(rc, what):
         raise ValueError(f"oracle {what}: invalid arguments (rc={rc})")
 
 
-def pool(q, grid_h: int, grid_w: int, m: int):
-    """Landmark queries q~ [B,H,m,d] (float64 holding values of q's dtype)."""
+def pool(q, grid_h: int, grid_w: int, m: int, landmark_grid=None):
+    """Landmark queries q~ [B,H,m,d] (float64 holding values of q's dtype).
+
+    ``landmark_grid`` = (mh, mw) with mh * mw = m pools onto that grid; by
+    default 1D pools to 1 x m and 2D to sqrt(m) x sqrt(m)."""
     q = _cpu(q)
     B, H, N, d = q.shape
     out = torch.empty((B, H, m, d), dtype=torch.float64)
-    _check(_load().orc_pool(_p(q), _DT[q.dtype], B, H, N, d, grid_h, grid_w, m,
-                            _DT[q.dtype], _p(out)), "pool")
+    if landmark_grid is None:
+        _check(_load().orc_pool(_p(q), _DT[q.dtype], B, H, N, d, grid_h, grid_w, m,
+                                _DT[q.dtype], _p(out)), "pool")
+    else:
+        mh, mw = landmark_grid
+        if mh * mw != m:
+            raise ValueError("landmark grid must hold m landmarks")
+        _check(_load().orc_pool_grid(_p(q), _DT[q.dtype], B, H, N, d, grid_h, grid_w, mh, mw,
+                                     _DT[q.dtype], _p(out)), "pool")
     return out
 
 
@@ -145,11 +158,15 @@ def bucket(route_idx, m: int):
     return off, qidx
 
 
-def attend(q, k, v, q_tilde, v_tilde, topk_idx, route_idx, queries=None):
+def attend(q, k, v, q_tilde, v_tilde, topk_idx, route_idx, queries=None,
+           shared_temperature: str = "sqrt_d"):
     """Joint-softmax output (float64) for all queries [B,H,N,d] or a sample [R,d].
 
     ``route_idx`` is [B,H,N,s] for all queries, or [R,s] aligned with ``queries``.
+    ``shared_temperature``: "sqrt_d" (every logit / sqrt(d)) or "d" (the shared
+    logits q . q~ / d, raw logits still / sqrt(d)).
     """
+    temp = {"sqrt_d": 0, "d": 1}[shared_temperature]
     q, k, v = _cpu(q), _cpu(k), _cpu(v)
     B, H, N, d = q.shape
     qt = _cpu(q_tilde).to(torch.float64)
@@ -164,18 +181,19 @@ def attend(q, k, v, q_tilde, v_tilde, topk_idx, route_idx, queries=None):
         qsel = torch.as_tensor(queries, dtype=torch.int64).contiguous()
         R = qsel.numel()
     out = torch.empty((R, d), dtype=torch.float64)
-    _check(_load().orc_attend_rows(_p(q), _p(k), _p(v), _DT[q.dtype], _p(qt), _p(vt),
-                                   _p(ti), _p(r), B, H, N, d, m, topk, s, R, _p(qsel),
-                                   _p(out)), "attend")
+    _check(_load().orc_attend_rows_t(_p(q), _p(k), _p(v), _DT[q.dtype], _p(qt), _p(vt),
+                                     _p(ti), _p(r), B, H, N, d, m, topk, s, R, _p(qsel),
+                                     temp, _p(out)), "attend")
     return out.view(B, H, N, d) if queries is None else out
 
 
-def forward(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int = 1):
+def forward(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int = 1,
+            shared_temperature: str = "sqrt_d", landmark_grid=None):
     """All six steps for every query; returns a dict of every intermediate."""
-    qt = pool(q, grid_h, grid_w, m)
+    qt = pool(q, grid_h, grid_w, m, landmark_grid)
     ti, vt, tgap = landmark(qt, k, v, topk)
     r, rgap = route(q, qt, s)
     off, qidx = bucket(r, m)
-    out = attend(q, k, v, qt, vt, ti, r)
+    out = attend(q, k, v, qt, vt, ti, r, shared_temperature=shared_temperature)
     return dict(q_tilde=qt, topk_idx=ti, v_tilde=vt, topk_gap=tgap, route=r,
                 route_gap=rgap, bucket_off=off, bucket_qidx=qidx, out=out)

@@ -16,14 +16,17 @@
 //
 // Readings where the pages are silent (all listed in the design notes):
 //   * scores use the same 1/sqrt(d) scaling for shared and raw pairs
-//     ([TUT] ch. 5 and ch. 8 caveat 3);
+//     ([TUT] ch. 5 and ch. 8 caveat 3); on request the joint softmax's shared
+//     logits take 1/d instead, q . q~ / d, the temperature [TUT] ch. 8 caveat 3
+//     reads out of the official code (raw logits and the landmark softmax
+//     behind v~ keep 1/sqrt(d));
 //   * top-k and top-s order is (score descending, index ascending), so ties go
 //     to the lowest index; expert index lists are stored ascending;
 //   * the landmark queries are materialised in the input dtype: an fp64 window
 //     mean rounded once (round-to-nearest-even);
 //   * 2D pooling uses the adaptive-average-pool window rule, the landmark grid
-//     is sqrt(m) x sqrt(m); 1D pooling (grid_h == 1) uses the same rule on a
-//     1 x N grid pooled to 1 x m;
+//     is sqrt(m) x sqrt(m) unless a grid of mh x mw = m landmarks is given; 1D
+//     pooling (grid_h == 1) uses the same rule on a 1 x N grid pooled to 1 x m;
 //   * no mask, no dropout, no special self term.
 //
 // Parity pins: every function is pinned by tests that do not call back into
@@ -114,15 +117,11 @@ extern "C" {
 // queries (not of keys); [NEWS]: "local average pooling"; [TUT] ch. 5 pools a
 // 2 x 4 token grid in 2D.  Output is rounded once to `out_dt` and returned as
 // doubles in q_tilde[B, H, m, d].
-int orc_pool(const void* q, int dt, int B, int H, int N, int d, int grid_h,
-             int grid_w, int m, int out_dt, double* q_tilde) {
-  if ((long)grid_h * grid_w != N || m < 1 || m > N) return 1;
-  int mh = 1, mw = m;
-  if (grid_h != 1) {
-    int r = isqrt_exact(m);
-    if (r < 0) return 1;
-    mh = mw = r;
-  }
+// Pooling onto an explicit mh x mw landmark grid (row-major landmark index).
+int orc_pool_grid(const void* q, int dt, int B, int H, int N, int d, int grid_h,
+                  int grid_w, int mh, int mw, int out_dt, double* q_tilde) {
+  if ((long)grid_h * grid_w != N || mh < 1 || mw < 1 || mh > grid_h || mw > grid_w) return 1;
+  const int m = mh * mw;
 #pragma omp parallel for collapse(2) schedule(static)
   for (int bh = 0; bh < B * H; ++bh) {
     for (int i = 0; i < m; ++i) {
@@ -140,6 +139,18 @@ int orc_pool(const void* q, int dt, int B, int H, int N, int d, int grid_h,
     }
   }
   return 0;
+}
+
+int orc_pool(const void* q, int dt, int B, int H, int N, int d, int grid_h,
+             int grid_w, int m, int out_dt, double* q_tilde) {
+  if ((long)grid_h * grid_w != N || m < 1 || m > N) return 1;
+  int mh = 1, mw = m;
+  if (grid_h != 1) {
+    int r = isqrt_exact(m);
+    if (r < 0) return 1;
+    mh = mw = r;
+  }
+  return orc_pool_grid(q, dt, B, H, N, d, grid_h, grid_w, mh, mw, out_dt, q_tilde);
 }
 
 // Steps 2-3 for a list of landmark rows (flat row id = bh * m + i).
@@ -291,13 +302,16 @@ int orc_bucket(const int32_t* route, int B, int H, int N, int m, int s,
 // and routed parts compete for one total weight of 1).  Experts are
 // concatenated in route order; overlapping experts (s > 1) contribute their
 // rows again, as the literal concatenation V* = [V~, V(e1), ..., V(es)] does.
-int orc_attend_rows(const void* q, const void* k, const void* v, int dt,
-                    const double* q_tilde, const double* v_tilde,
-                    const int32_t* topk_idx, const int32_t* route, int B, int H,
-                    int N, int d, int m, int topk, int s, long nq,
-                    const int64_t* qsel, double* out) {
+// shared_temp = 0: every logit / sqrt(d); 1: the shared logits q . q~_i / d.
+int orc_attend_rows_t(const void* q, const void* k, const void* v, int dt,
+                      const double* q_tilde, const double* v_tilde,
+                      const int32_t* topk_idx, const int32_t* route, int B, int H,
+                      int N, int d, int m, int topk, int s, long nq,
+                      const int64_t* qsel, int shared_temp, double* out) {
   (void)B; (void)H;
+  if (shared_temp != 0 && shared_temp != 1) return 1;
   const double sqrt_d = std::sqrt((double)d);
+  const double shared_div = shared_temp ? (double)d : sqrt_d;
   const long E = (long)m + (long)s * topk;
 #pragma omp parallel
   {
@@ -315,7 +329,7 @@ int orc_attend_rows(const void* q, const void* k, const void* v, int dt,
         const double* qt = q_tilde + ((size_t)bh * m + i) * d;
         double a = 0.0;
         for (int l = 0; l < d; ++l) a += widen(q, dt, (size_t)qi * d + l) * qt[l];
-        logit[e] = a / sqrt_d;
+        logit[e] = a / shared_div;
         vrow_d[e] = v_tilde + ((size_t)bh * m + i) * d;
         vrow_raw[e] = -1;
       }
@@ -342,6 +356,15 @@ int orc_attend_rows(const void* q, const void* k, const void* v, int dt,
     }
   }
   return 0;
+}
+
+int orc_attend_rows(const void* q, const void* k, const void* v, int dt,
+                    const double* q_tilde, const double* v_tilde,
+                    const int32_t* topk_idx, const int32_t* route, int B, int H,
+                    int N, int d, int m, int topk, int s, long nq,
+                    const int64_t* qsel, double* out) {
+  return orc_attend_rows_t(q, k, v, dt, q_tilde, v_tilde, topk_idx, route, B, H, N, d, m,
+                           topk, s, nq, qsel, 0, out);
 }
 
 int orc_num_threads(void) {

@@ -71,6 +71,30 @@ def test_appendix_a_counterexample(d, dtype):
     dense = torch.softmax(torch.zeros(2, dtype=torch.float64), 0) @ v[0, 0, :, 0].double()
     assert abs(dense.item() - gold["dense_output"]) < 1e-15
     assert abs(out0 - dense.item()) > 0.05
+    # the official code's shared temperature (q . q~ / d): query 0 has q = 0, so all four
+    # logits stay 0 and the printed value is unchanged
+    res_d = oracle.forward(q, k, v, grid_h=1, grid_w=2, m=2, topk=2, s=1,
+                           shared_temperature="d")
+    assert abs(res_d["out"][0, 0, 0, 0].item() - gold["mita_output"]) <= tol
+
+
+@pytest.mark.parametrize("temp", ["sqrt_d", "d"])
+def test_counterexample_second_query_closed_form(temp):
+    """Query 1 of the same example at d = 16: q1 = 4 e0, k1 = e0, q~ = q.  Raw logits
+    q1 . k / 4 = [0, 1]; shared logits q1 . q~ / 4 = [0, 4] (every logit / sqrt(d)) or
+    q1 . q~ / 16 = [0, 1] (shared logits / d); values [0.5, sigmoid(1)] then [0, 1]."""
+    d = 16
+    q = torch.zeros((1, 1, 2, d), dtype=torch.float64)
+    k = torch.zeros_like(q)
+    v = torch.zeros_like(q)
+    q[0, 0, 1, 0] = 4.0
+    k[0, 0, 1, 0] = 1.0
+    v[0, 0, 1, :] = 1.0
+    res = oracle.forward(q, k, v, grid_h=1, grid_w=2, m=2, topk=2, s=1, shared_temperature=temp)
+    sh = 4.0 if temp == "sqrt_d" else 1.0
+    sig1 = 1 / (1 + math.exp(-1))
+    want = (0.5 + math.exp(sh) * sig1 + math.exp(1.0)) / (2 + math.exp(sh) + math.exp(1.0))
+    assert abs(res["out"][0, 0, 1, 0].item() - want) < 1e-14
 
 
 def test_two_equal_scores_average():
@@ -118,6 +142,18 @@ def test_pool_2d_matches_adaptive_avg_pool(gh, gw, m):
     r = int(round(math.sqrt(m)))
     img = q.double().view(B * H, gh, gw, d).permute(0, 3, 1, 2)
     ref = F.adaptive_avg_pool2d(img, (r, r)).permute(0, 2, 3, 1).reshape(B, H, m, d)
+    _check_rounded_mean(qt, ref, dtype)
+
+
+@pytest.mark.parametrize("gh,gw,mh,mw", [(14, 14, 3, 5), (32, 32, 4, 8), (6, 10, 2, 5),
+                                        (5, 7, 5, 1), (9, 4, 1, 4)])
+def test_pool_2d_nonsquare_landmark_grid_matches_adaptive_avg_pool(gh, gw, mh, mw):
+    B, H, d = 2, 2, 8
+    dtype = torch.bfloat16
+    q = _rand((B, H, gh * gw, d), dtype, 3)
+    qt = oracle.pool(q, gh, gw, mh * mw, landmark_grid=(mh, mw))
+    img = q.double().view(B * H, gh, gw, d).permute(0, 3, 1, 2)
+    ref = F.adaptive_avg_pool2d(img, (mh, mw)).permute(0, 2, 3, 1).reshape(B, H, mh * mw, d)
     _check_rounded_mean(qt, ref, dtype)
 
 
@@ -244,23 +280,25 @@ def test_bucket_is_stable_counting_sort(s):
 # ----------------------------------------------------------------------------
 # Step 6: joint attention
 # ----------------------------------------------------------------------------
-def _setup(seed=0, B=2, H=2, N=256, d=16, m=8, k=12, s=1, dtype="bf16"):
+def _setup(seed=0, B=2, H=2, N=256, d=16, m=8, k=12, s=1, dtype="bf16", temp="sqrt_d"):
     w = W.custom("t", B, H, N, d, dtype, 1, N, m, k, s, index=seed)
     q, kk, vv = W.make_qkv(w, seed)
-    return q, kk, vv, oracle.forward(q, kk, vv, 1, N, m, k, s)
+    return q, kk, vv, oracle.forward(q, kk, vv, 1, N, m, k, s, shared_temperature=temp)
 
 
-@pytest.mark.parametrize("s", [1, 2])
-def test_joint_softmax_equals_branch_merge(s):
-    """Tutorial ch. 4: (Z1 o1 + Z2 o2) / (Z1 + Z2) is the joint softmax; o1 + o2 is not."""
-    q, k, v, res = _setup(seed=1, s=s)
+@pytest.mark.parametrize("s,temp", [(1, "sqrt_d"), (2, "sqrt_d"), (1, "d"), (3, "d")])
+def test_joint_softmax_equals_branch_merge(s, temp):
+    """Tutorial ch. 4: (Z1 o1 + Z2 o2) / (Z1 + Z2) is the joint softmax; o1 + o2 is not.
+    With temp = "d" the shared branch's logits are q . q~ / d (raw ones stay / sqrt(d))."""
+    q, k, v, res = _setup(seed=1, s=s, temp=temp)
     B, H, N, d = q.shape
     qd, kd, vd = q.double(), k.double(), v.double()
     sq = math.sqrt(d)
+    sh = sq if temp == "sqrt_d" else float(d)
     naive_err = 0.0
     for b in range(B):
         for h in range(H):
-            ls = qd[b, h] @ res["q_tilde"][b, h].T / sq                   # [N, m]
+            ls = qd[b, h] @ res["q_tilde"][b, h].T / sh                   # [N, m]
             lse1 = torch.logsumexp(ls, -1)
             o1 = torch.softmax(ls, -1) @ res["v_tilde"][b, h]
             for n in range(0, N, 7):
@@ -290,16 +328,18 @@ def test_output_is_convex_combination():
                 assert bool((o >= vals.min(0).values - 1e-12).all())
 
 
-def test_single_landmark_full_topk_reduces_to_dense_plus_one_shared_pair():
+@pytest.mark.parametrize("temp", ["sqrt_d", "d"])
+def test_single_landmark_full_topk_reduces_to_dense_plus_one_shared_pair(temp):
     """m = 1, k = N: the routed expert is every KV row, so the output is the
-    textbook dense attention merged with the one shared pair (q~_0, v~_0)."""
+    textbook dense attention merged with the one shared pair (q~_0, v~_0), whose
+    logit is q . q~_0 / sqrt(d) or, with the official code's temperature, / d."""
     B, H, N, d = 1, 2, 64, 16
-    q, k, v, res = _setup(seed=3, B=B, H=H, N=N, d=d, m=1, k=N)
+    q, k, v, res = _setup(seed=3, B=B, H=H, N=N, d=d, m=1, k=N, temp=temp)
     qd, kd, vd = q.double(), k.double(), v.double()
     sq = math.sqrt(d)
     dense = F.scaled_dot_product_attention(qd, kd, vd)
     lse_dense = torch.logsumexp(qd @ kd.transpose(-1, -2) / sq, -1)
-    l_sh = (qd @ res["q_tilde"].transpose(-1, -2) / sq)[..., 0]
+    l_sh = (qd @ res["q_tilde"].transpose(-1, -2) / (sq if temp == "sqrt_d" else d))[..., 0]
     w_sh = torch.sigmoid(l_sh - lse_dense).unsqueeze(-1)
     ref = w_sh * res["v_tilde"][:, :, 0:1, :] + (1 - w_sh) * dense
     assert torch.allclose(res["out"], ref, rtol=0, atol=1e-12)
