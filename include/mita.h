@@ -50,6 +50,27 @@ extern "C" {
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* mita_stream_t;
 
+/*
+ * Options of mita_forward_ex (a zeroed struct, or NULL, gives mita_forward).
+ *   shared_temperature  MITA_SHARED_SQRT_D: every joint-softmax logit is
+ *                       divided by sqrt(d) (tutorial ch. 4, eq. 11-12).
+ *                       MITA_SHARED_D: the m shared logits are q . q~_i / d,
+ *                       the temperature tutorial ch. 8 caveat 3 reads out of
+ *                       the official code (shared key pre-scaled by d^-1/2,
+ *                       then the mixed attention's d^-1/2); the raw logits
+ *                       stay q . k_j / sqrt(d) and v~ is unchanged.
+ *   landmark_grid_h,    2D pooling onto this landmark grid (row-major landmark
+ *   landmark_grid_w     index; landmark_grid_h * landmark_grid_w == m), e.g. a
+ *                       non-square grid; 0, 0: 1 x m for a 1D sequence,
+ *                       sqrt(m) x sqrt(m) for a 2D grid.
+ */
+enum { MITA_SHARED_SQRT_D = 0, MITA_SHARED_D = 1 };
+typedef struct mita_options {
+  int shared_temperature;
+  int landmark_grid_h;
+  int landmark_grid_w;
+} mita_options;
+
 enum mita_status {
   MITA_OK = 0,
   MITA_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer      */
@@ -74,6 +95,17 @@ enum mita_status {
  */
 int mita_pool(const void* q, int B, int H, int N, int d, int grid_h, int grid_w, int m,
               void* q_tilde, mita_stream_t stream);
+/*
+ * mita_pool_grid -- mita_pool onto an explicit landmark_grid_h x
+ * landmark_grid_w grid (m = their product; a 1D sequence needs
+ * landmark_grid_h == 1).  q_tilde [B,H,m,d], landmark i = row i / landmark_grid_w,
+ * column i % landmark_grid_w; same window rule and rounding as mita_pool.
+ */
+int mita_pool_grid(const void* q, int B, int H, int N, int d, int grid_h, int grid_w,
+                   int landmark_grid_h, int landmark_grid_w, void* q_tilde, mita_stream_t stream);
+int mita_pool_grid_f32(const float* q, int B, int H, int N, int d, int grid_h, int grid_w,
+                       int landmark_grid_h, int landmark_grid_w, float* q_tilde,
+                       mita_stream_t stream);
 int mita_pool_f32(const float* q, int B, int H, int N, int d, int grid_h, int grid_w, int m,
                   float* q_tilde, mita_stream_t stream);
 
@@ -201,6 +233,17 @@ int mita_forward(const void* q, const void* k, const void* v, int B, int H, int 
 int mita_forward_f32(const float* q, const float* k, const float* v, int B, int H, int N, int d,
                      int grid_h, int grid_w, int m, int topk, int s, float* out,
                      mita_stream_t stream);
+
+/*
+ * mita_forward_ex -- mita_forward with options (see mita_options; NULL gives
+ * mita_forward).  Unknown option values return MITA_ERR_INVALID_ARG.
+ */
+int mita_forward_ex(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                    int grid_h, int grid_w, int m, int topk, int s, const mita_options* options,
+                    void* out, mita_stream_t stream);
+int mita_forward_ex_f32(const float* q, const float* k, const float* v, int B, int H, int N,
+                        int d, int grid_h, int grid_w, int m, int topk, int s,
+                        const mita_options* options, float* out, mita_stream_t stream);
 
 /*
  * mita_forward_host -- mita_forward on HOST buffers (same method and

@@ -171,15 +171,38 @@ int check_entries(int B, int H, int N, int s) {
   return MITA_OK;
 }
 
-int check_grid(int N, int grid_h, int grid_w, int m) {
+// The landmark grid: lm_h x lm_w when given (both > 0), else 1 x m for a 1D
+// sequence (grid_h = 1) and sqrt(m) x sqrt(m) for a 2D grid.
+int check_grid(int N, int grid_h, int grid_w, int m, int lm_h = 0, int lm_w = 0,
+               int* mh = nullptr, int* mw = nullptr) {
   if (grid_h < 1 || grid_w < 1 || (long long)grid_h * grid_w != N)
     return fail(MITA_ERR_INVALID_ARG, "grid %dx%d does not hold N=%d tokens", grid_h, grid_w, N);
-  if (grid_h != 1) {
+  int h = 1, w = m;
+  if (lm_h != 0 || lm_w != 0) {
+    if (lm_h < 1 || lm_w < 1 || (long long)lm_h * lm_w != m)
+      return fail(MITA_ERR_INVALID_ARG, "landmark grid %dx%d does not hold m=%d landmarks", lm_h,
+                  lm_w, m);
+    if (grid_h == 1 && lm_h != 1)
+      return fail(MITA_ERR_INVALID_ARG, "a 1D sequence pools onto 1 x m landmarks");
+    h = lm_h;
+    w = lm_w;
+  } else if (grid_h != 1) {
     int r = 1;
     while ((r + 1) * (r + 1) <= m) ++r;
     if (r * r != m)
-      return fail(MITA_ERR_INVALID_ARG, "2D pooling needs a square m (got %d)", m);
+      return fail(MITA_ERR_INVALID_ARG,
+                  "2D pooling needs a square m (got %d) or an explicit landmark grid", m);
+    h = w = r;
   }
+  if (mh) *mh = h;
+  if (mw) *mw = w;
+  return MITA_OK;
+}
+
+int check_options(const mita_options* o) {
+  if (o == nullptr) return MITA_OK;
+  if (o->shared_temperature != MITA_SHARED_SQRT_D && o->shared_temperature != MITA_SHARED_D)
+    return fail(MITA_ERR_INVALID_ARG, "unknown shared_temperature %d", o->shared_temperature);
   return MITA_OK;
 }
 
@@ -202,12 +225,13 @@ size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 // ---------------------------------------------------------------------------
 template <typename T>
 int pool_impl(const T* q, int B, int H, int N, int d, int gh, int gw, int m, T* qt,
-              cudaStream_t st) {
+              cudaStream_t st, int lm_h = 0, int lm_w = 0) {
   MITA_TRY(check_shape(B, H, N, d));
   MITA_TRY(check_m(N, m));
-  MITA_TRY(check_grid(N, gh, gw, m));
+  int mh = 0, mw = 0;
+  MITA_TRY(check_grid(N, gh, gw, m, lm_h, lm_w, &mh, &mw));
   MITA_TRY(check_ptrs({{q, "q"}, {qt, "q_tilde"}}));
-  MITA_CUDA(launch_pool<T>(q, B * H, N, d, gh, gw, m, qt, st), "pool launch");
+  MITA_CUDA(launch_pool<T>(q, B * H, N, d, gh, gw, mh, mw, qt, st), "pool launch");
   return MITA_OK;
 }
 
@@ -391,10 +415,15 @@ forward_zero_kernel(int* a, long long na, int* b, long long nb, int* c, long lon
 
 template <typename T>
 int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d, int gh, int gw,
-                 int m, int topk, int s, T* out, cudaStream_t st) {
+                 int m, int topk, int s, T* out, cudaStream_t st,
+                 const mita_options* opt = nullptr) {
   MITA_TRY(check_shape(B, H, N, d));
   MITA_TRY(check_m(N, m));
-  MITA_TRY(check_grid(N, gh, gw, m));
+  MITA_TRY(check_options(opt));
+  const int temp = opt ? opt->shared_temperature : MITA_SHARED_SQRT_D;
+  int mh = 0, mw = 0;
+  MITA_TRY(check_grid(N, gh, gw, m, opt ? opt->landmark_grid_h : 0,
+                      opt ? opt->landmark_grid_w : 0, &mh, &mw));
   MITA_TRY(check_topk(N, topk));
   MITA_TRY(check_s(m, s));
   MITA_TRY(check_entries(B, H, N, s));
@@ -422,7 +451,7 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
               "counter clearing");
     count_launch();
   }
-  MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, m, qt, st), "pool launch");
+  MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, mh, mw, qt, st), "pool launch");
   MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, L.plan, lw, ti, vt, ds->status, st,
                                true),
             "landmark launch");
@@ -431,11 +460,12 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
     // entries, per-expert partials and their merge
     float* lse = reinterpret_cast<float*>(ws + L.lse);
     float* so = reinterpret_cast<float*>(ws + L.so);
-    MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st), "route launch");
+    MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st, temp),
+              "route launch");
     MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, false, s),
               "bucket launch");
     MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, BH, N, d, m, topk, s,
-                                    ws + L.ex, out, ds->status, st),
+                                    ws + L.ex, out, ds->status, st, temp),
               "expert launch");
     return MITA_OK;
   }
@@ -449,13 +479,13 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   if constexpr (std::is_same<T, bf16>::value) {
     if (expert_tc_supported(d, m, topk)) {
       MITA_CUDA(launch_expert_tc(q, k, v, qt, vt, ti, off, qidx, BH, N, m, topk, ds->num_sms,
-                                 ws + L.ex, out, ds->status, st),
+                                 ws + L.ex, out, ds->status, st, temp),
                 "expert launch");
       return MITA_OK;
     }
   }
   MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, nullptr, nullptr, BH, N, d, m,
-                                  topk, 1, nullptr, out, ds->status, st),
+                                  topk, 1, nullptr, out, ds->status, st, temp),
             "expert launch");
   return MITA_OK;
 }
@@ -508,6 +538,18 @@ int mita_pool(const void* q, int B, int H, int N, int d, int grid_h, int grid_w,
               void* q_tilde, mita_stream_t stream) {
   return mita::pool_impl<bf16>(static_cast<const bf16*>(q), B, H, N, d, grid_h, grid_w, m,
                                static_cast<bf16*>(q_tilde), stream);
+}
+int mita_pool_grid(const void* q, int B, int H, int N, int d, int grid_h, int grid_w,
+                   int landmark_grid_h, int landmark_grid_w, void* q_tilde, mita_stream_t stream) {
+  return mita::pool_impl<bf16>(static_cast<const bf16*>(q), B, H, N, d, grid_h, grid_w,
+                               landmark_grid_h * landmark_grid_w, static_cast<bf16*>(q_tilde),
+                               stream, landmark_grid_h, landmark_grid_w);
+}
+int mita_pool_grid_f32(const float* q, int B, int H, int N, int d, int grid_h, int grid_w,
+                       int landmark_grid_h, int landmark_grid_w, float* q_tilde,
+                       mita_stream_t stream) {
+  return mita::pool_impl<float>(q, B, H, N, d, grid_h, grid_w, landmark_grid_h * landmark_grid_w,
+                                q_tilde, stream, landmark_grid_h, landmark_grid_w);
 }
 int mita_pool_f32(const float* q, int B, int H, int N, int d, int grid_h, int grid_w, int m,
                   float* q_tilde, mita_stream_t stream) {
@@ -577,6 +619,20 @@ int mita_forward_f32(const float* q, const float* k, const float* v, int B, int 
                      int grid_h, int grid_w, int m, int topk, int s, float* out,
                      mita_stream_t stream) {
   return mita::forward_impl<float>(q, k, v, B, H, N, d, grid_h, grid_w, m, topk, s, out, stream);
+}
+
+int mita_forward_ex(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                    int grid_h, int grid_w, int m, int topk, int s, const mita_options* options,
+                    void* out, mita_stream_t stream) {
+  return mita::forward_impl<bf16>(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                  static_cast<const bf16*>(v), B, H, N, d, grid_h, grid_w, m, topk,
+                                  s, static_cast<bf16*>(out), stream, options);
+}
+int mita_forward_ex_f32(const float* q, const float* k, const float* v, int B, int H, int N,
+                        int d, int grid_h, int grid_w, int m, int topk, int s,
+                        const mita_options* options, float* out, mita_stream_t stream) {
+  return mita::forward_impl<float>(q, k, v, B, H, N, d, grid_h, grid_w, m, topk, s, out, stream,
+                                   options);
 }
 
 int mita_forward_host(const void* q, const void* k, const void* v, int B, int H, int N, int d,

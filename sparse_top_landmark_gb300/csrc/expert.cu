@@ -3,7 +3,8 @@
 //
 // MiTA tutorial (iwxt.cn), ch. 4 steps 5-6 (paper eq. 11-12): all queries
 // see the m shared pairs (q~_i, v~_i); each adds the s*k raw pairs of its
-// chosen experts; the m + s*k logits (all scaled by 1/sqrt(d)) share one
+// chosen experts; the m + s*k logits (all scaled by 1/sqrt(d); on request the
+// shared ones by 1/d, the official code's temperature) share one
 // softmax.  The bit.fan article: queries are processed grouped by expert with
 // an online softmax.  Tutorial ch. 4 also states the merge rule used when the
 // shared part arrives as a partial: (Z1 o1 + Z2 o2) / (Z1 + Z2).
@@ -48,7 +49,8 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
                    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ bucket_off,
                    const int32_t* __restrict__ bucket_qidx, const float* __restrict__ shared_lse,
                    const float* __restrict__ shared_o, int N, int m, int topk, int s,
-                   int tiles_per_bh, T* __restrict__ out, Partials part, int* status) {
+                   float c_shared, int tiles_per_bh, T* __restrict__ out, Partials part,
+                   int* status) {
   __shared__ __align__(16) float ks[kRows][D];
   __shared__ __align__(16) float vs[kRows][D];
   __shared__ int rowid[kRows];
@@ -149,7 +151,7 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
         float s = 0.f;
 #pragma unroll
         for (int l = 0; l < D; ++l) s = fmaf(qr[l], ks[r][l], s);
-        absorb(s * c, vs[r]);
+        absorb(s * c_shared, vs[r]);
       }
     }
   }
@@ -276,8 +278,9 @@ expert_merge_kernel(const float* __restrict__ shared_lse, const float* __restric
 template <typename T, int D>
 cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt,
                 const int32_t* ti, const int32_t* off, const int32_t* qidx, const float* lse,
-                const float* so, int BH, int N, int m, int topk, int s, void* pws, T* out,
-                int* status, cudaStream_t st) {
+                const float* so, int BH, int N, int m, int topk, int s, int temp, void* pws,
+                T* out, int* status, cudaStream_t st) {
+  const float c_shared = (float)(1.4426950408889634 / (temp ? (double)D : sqrt((double)D)));
   const int tiles = (int)(((long long)N * s + kQTile - 1) / kQTile) + m;
   const long long blocks = (long long)BH * tiles;
   Partials part{};
@@ -295,7 +298,7 @@ cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt
     if (e != cudaSuccess) return e;
   }
   expert_attn_kernel<T, D><<<(unsigned)blocks, kQTile, 0, st>>>(
-      q, k, v, qt, vt, ti, off, qidx, lse, so, N, m, topk, s, tiles, out, part, status);
+      q, k, v, qt, vt, ti, off, qidx, lse, so, N, m, topk, s, c_shared, tiles, out, part, status);
   count_launch();
   if (s > 1) {
     const cudaError_t e = cudaGetLastError();
@@ -321,13 +324,13 @@ cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_ti
                                const int32_t* bucket_off, const int32_t* bucket_qidx,
                                const float* shared_lse, const float* shared_o, int BH, int N,
                                int d, int m, int topk, int s, void* ws, T* out, int* status,
-                               cudaStream_t st) {
+                               cudaStream_t st, int shared_temp) {
   if (s < 1 || (s > 1 && (ws == nullptr || shared_lse == nullptr || shared_o == nullptr)))
     return cudaErrorInvalidValue;
 #define MITA_EXPERT_CASE(DD)                                                                 \
   case DD:                                                                                   \
     return run<T, DD>(q, k, v, q_tilde, v_tilde, topk_idx, bucket_off, bucket_qidx,          \
-                      shared_lse, shared_o, BH, N, m, topk, s, ws, out, status, st);
+                      shared_lse, shared_o, BH, N, m, topk, s, shared_temp, ws, out, status, st);
   switch (d) {
     MITA_EXPERT_CASE(16)
     MITA_EXPERT_CASE(32)
@@ -342,11 +345,11 @@ template cudaError_t launch_expert_attn<float>(const float*, const float*, const
                                                const float*, const float*, const int32_t*,
                                                const int32_t*, const int32_t*, const float*,
                                                const float*, int, int, int, int, int, int, void*,
-                                               float*, int*, cudaStream_t);
+                                               float*, int*, cudaStream_t, int);
 template cudaError_t launch_expert_attn<bf16>(const bf16*, const bf16*, const bf16*, const bf16*,
                                               const float*, const int32_t*, const int32_t*,
                                               const int32_t*, const float*, const float*, int,
                                               int, int, int, int, int, void*, bf16*, int*,
-                                              cudaStream_t);
+                                              cudaStream_t, int);
 
 }  // namespace mita

@@ -3,7 +3,9 @@
 // routed expert, computed expert by expert.
 //
 // MiTA tutorial (iwxt.cn), ch. 4 steps 5-6 (paper eq. 11-12): the m + s*k
-// logits, all scaled by 1/sqrt(d), share one softmax over [v~; V(e)].  The
+// logits, all scaled by 1/sqrt(d), share one softmax over [v~; V(e)] (on
+// request the shared logits take 1/d, the official code's temperature read in
+// tutorial ch. 8 caveat 3).  The
 // bit.fan article: queries are grouped by expert and an online softmax runs
 // over the concatenated entries; each expert's k KV rows are gathered once.
 //
@@ -201,7 +203,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
                  const __grid_constant__ CUtensorMap map_vg, const __grid_constant__ CUtensorMap map_qt,
                  const __grid_constant__ CUtensorMap map_vt, const int32_t* __restrict__ bucket_qidx,
                  const int* __restrict__ unit_count, const int4* __restrict__ unit_tab, int BH,
-                 int N, int m, int topk, bf16* __restrict__ out, int* status) {
+                 int N, int m, int topk, float cs_shared, bf16* __restrict__ out, int* status) {
   griddep_wait();
   extern __shared__ unsigned char smem_raw[];
   ExpertSmem& s = *reinterpret_cast<ExpertSmem*>(
@@ -468,18 +470,19 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
 #pragma unroll
         for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
       const float tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      const float xm = tm * cs;
+      const bool fp16 = c >= nrc;                  // shared chunk (v~ in fp16)
+      const float csc = fp16 ? cs_shared : cs;     // the chunk's logit scale, log2 units
+      const float xm = tm * csc;
       const bool need = (c == 0) || (xm > mref + kLazy);
       const float f = (c > 0 && need) ? ex2(mref - xm) : 1.f;
       if (need) {
         lsum *= f;
         mref = xm;
       }
-      const bool fp16 = c >= nrc;
       const float nm = -mref;
       // P = 2^(s * cs - mref) in fp32 pairs, packed to the branch's type (the type is
       // uniform per chunk, so each loop is specialised); row sum in two pair chains
-      const unsigned long long c2 = f2pack(cs, cs), nm2 = f2pack(nm, nm);
+      const unsigned long long c2 = f2pack(csc, csc), nm2 = f2pack(nm, nm);
       unsigned long long lsa = f2pack(0.f, 0.f), lsb = lsa;
       auto exp_half = [&](auto is_fp16, int base, uint32_t* pk) {
 #pragma unroll
@@ -559,8 +562,10 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
                              const float* v_tilde, const int32_t* topk_idx,
                              const int32_t* bucket_off, const int32_t* bucket_qidx, int BH, int N,
                              int m, int topk, int num_sms, void* ws, bf16* out, int* status,
-                             cudaStream_t st) {
+                             cudaStream_t st, int shared_temp) {
   const ExpertTcWs w = carve(ws, BH, N, m, topk);
+  // log2(e) / sqrt(64), or log2(e) / 64 for the shared logits at the official code's temperature
+  const float cs_shared = shared_temp ? 0.022542110013890052f : 0.18033688011112042f;
   const long long rows = (long long)BH * m * topk;
   const long long gblocks = std::min<long long>((rows + kGatherThreads / 8 - 1) / (kGatherThreads / 8),
                                                 (long long)std::max(num_sms, 1) * 8);
@@ -583,7 +588,7 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   e = launch_pdl(expert_tc_kernel, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
                  mqg, mkg, mvg, mqt, mvt, bucket_qidx,
                  static_cast<const int*>(w.unit_start + (size_t)BH * m),
-                 static_cast<const int4*>(w.unit), BH, N, m, topk, out, status);
+                 static_cast<const int4*>(w.unit), BH, N, m, topk, cs_shared, out, status);
   count_launch();
   return e;
 }

@@ -11,9 +11,10 @@
 namespace mita {
 
 // ---- step 1: landmark pooling --------------------------------------------
+// onto an mh x mw landmark grid (m = mh * mw; 1D: mh = 1)
 template <typename T>
 cudaError_t launch_pool(const T* q, int BH, int N, int d, int grid_h, int grid_w,
-                        int m, T* q_tilde, cudaStream_t st);
+                        int mh, int mw, T* q_tilde, cudaStream_t st);
 
 // ---- steps 2-3: landmark top-k experts + shared values --------------------
 struct LandmarkPlan {
@@ -68,10 +69,11 @@ cudaError_t launch_landmark_tc_passes(const __nv_bfloat16* q_tilde, const __nv_b
 
 // ---- step 4: routing (optionally emitting the shared-branch partial) ------
 // route_idx: [BH, N, s], each query's s landmarks best first (1 <= s <= kMaxRouteS).
+// shared_temp: the shared partial's logits are q . q~ / sqrt(d) (0) or q . q~ / d (1).
 template <typename T>
 cudaError_t launch_route(const T* q, const T* q_tilde, const float* v_tilde, int BH, int N,
                          int d, int m, int s, int32_t* route_idx, float* shared_lse,
-                         float* shared_o, cudaStream_t st);
+                         float* shared_o, cudaStream_t st, int shared_temp = 0);
 
 // ---- step 5: stable grouping of queries by expert -------------------------
 constexpr int kBucketChunk = 4096;   // route entries per chunk
@@ -94,7 +96,7 @@ cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_ti
                                const int32_t* bucket_off, const int32_t* bucket_qidx,
                                const float* shared_lse, const float* shared_o, int BH,
                                int N, int d, int m, int topk, int s, void* ws, T* out,
-                               int* status, cudaStream_t st);
+                               int* status, cudaStream_t st, int shared_temp = 0);
 
 // ---- tensor-core (tcgen05) kernels: bf16, d = 64 ---------------------------
 // TMA map over a [batches, rows, 64] bf16 array, boxes of box_rows rows.
@@ -118,7 +120,7 @@ cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                              const float* v_tilde, const int32_t* topk_idx,
                              const int32_t* bucket_off, const int32_t* bucket_qidx, int BH, int N,
                              int m, int topk, int num_sms, void* ws, __nv_bfloat16* out,
-                             int* status, cudaStream_t st);
+                             int* status, cudaStream_t st, int shared_temp = 0);
 
 int num_sms_of_current_device();
 

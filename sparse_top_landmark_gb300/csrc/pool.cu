@@ -4,7 +4,8 @@
 // landmark query is the mean of a group of queries; the bit.fan article calls
 // it local average pooling; tutorial ch. 5 pools a 2 x 4 token grid in 2D.
 // Windows follow the adaptive-average-pool rule on the grid_h x grid_w token
-// grid (1D: 1 x N pooled to 1 x m; 2D: pooled to sqrt(m) x sqrt(m)).
+// grid onto an mh x mw landmark grid (1D: 1 x N pooled to 1 x m; 2D: by
+// default sqrt(m) x sqrt(m), or any mh x mw = m the caller gives).
 //
 // HBM-bound: one CTA per landmark streams its window once with 16-byte loads.
 // Sums are error-free (fp32 two-sum per thread and across threads; one fp64
@@ -88,15 +89,9 @@ pool_kernel(const T* __restrict__ q, int N, int grid_h, int grid_w, int mh, int 
 }
 
 template <typename T, int D>
-cudaError_t run(const T* q, int BH, int N, int grid_h, int grid_w, int m, T* qt,
+cudaError_t run(const T* q, int BH, int N, int grid_h, int grid_w, int mh, int mw, T* qt,
                 cudaStream_t st) {
-  int mh = 1, mw = m;
-  if (grid_h != 1) {
-    int r = 1;
-    while ((r + 1) * (r + 1) <= m) ++r;
-    mh = mw = r;
-  }
-  const long long blocks = (long long)BH * m;
+  const long long blocks = (long long)BH * mh * mw;
   const cudaError_t e = launch_pdl(pool_kernel<T, D>, dim3((unsigned)blocks), dim3(kPoolThreads), 0,
                                    st, q, N, grid_h, grid_w, mh, mw, qt);
   count_launch();
@@ -106,20 +101,21 @@ cudaError_t run(const T* q, int BH, int N, int grid_h, int grid_w, int m, T* qt,
 }  // namespace
 
 template <typename T>
-cudaError_t launch_pool(const T* q, int BH, int N, int d, int grid_h, int grid_w, int m,
-                        T* q_tilde, cudaStream_t st) {
+cudaError_t launch_pool(const T* q, int BH, int N, int d, int grid_h, int grid_w, int mh,
+                        int mw, T* q_tilde, cudaStream_t st) {
+  if (mh < 1 || mw < 1) return cudaErrorInvalidValue;
   switch (d) {
-    case 16: return run<T, 16>(q, BH, N, grid_h, grid_w, m, q_tilde, st);
-    case 32: return run<T, 32>(q, BH, N, grid_h, grid_w, m, q_tilde, st);
-    case 64: return run<T, 64>(q, BH, N, grid_h, grid_w, m, q_tilde, st);
-    case 128: return run<T, 128>(q, BH, N, grid_h, grid_w, m, q_tilde, st);
+    case 16: return run<T, 16>(q, BH, N, grid_h, grid_w, mh, mw, q_tilde, st);
+    case 32: return run<T, 32>(q, BH, N, grid_h, grid_w, mh, mw, q_tilde, st);
+    case 64: return run<T, 64>(q, BH, N, grid_h, grid_w, mh, mw, q_tilde, st);
+    case 128: return run<T, 128>(q, BH, N, grid_h, grid_w, mh, mw, q_tilde, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template cudaError_t launch_pool<float>(const float*, int, int, int, int, int, int, float*,
+template cudaError_t launch_pool<float>(const float*, int, int, int, int, int, int, int, float*,
                                         cudaStream_t);
-template cudaError_t launch_pool<bf16>(const bf16*, int, int, int, int, int, int, bf16*,
+template cudaError_t launch_pool<bf16>(const bf16*, int, int, int, int, int, int, int, bf16*,
                                        cudaStream_t);
 
 }  // namespace mita

@@ -5,7 +5,9 @@
 // scores only select (no gate).  gist.science summary Sec. 2.2: s = 1 in
 // practice.  The bit.fan article notes that the query-landmark logits are
 // reused as the shared-branch logits; this kernel can emit that branch's
-// partial (log-sum-exp and normalised output over the m shared pairs).
+// partial (log-sum-exp and normalised output over the m shared pairs), its
+// logits scaled by 1/sqrt(d) or, on request, by 1/d (the official code's
+// temperature, tutorial ch. 8 caveat 3).
 //
 // Exactness: each thread keeps its s + 1 best fp32 scores in a sorted
 // register list.  The list is accepted when every neighbouring pair in it
@@ -43,8 +45,9 @@ __device__ __forceinline__ void list_insert(S (&v)[L], int (&id)[L], S x, int i)
 template <typename T, int D, int L>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
-             const float* __restrict__ v_tilde, int N, int m, int s, int32_t* __restrict__ route,
-             float* __restrict__ shared_lse, float* __restrict__ shared_o) {
+             const float* __restrict__ v_tilde, int N, int m, int s, float c,
+             int32_t* __restrict__ route, float* __restrict__ shared_lse,
+             float* __restrict__ shared_o) {
   __shared__ __align__(16) float qs[kLmChunk][D];
   __shared__ __align__(16) float vs[kLmChunk][D];
   __shared__ float red[kRouteThreads / 32];
@@ -77,7 +80,6 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
 #pragma unroll
   for (int l = 0; l < D; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
 
-  const float c = (float)(1.4426950408889634 / sqrt((double)D));
   float bv[L];
   int bi[L];
 #pragma unroll
@@ -177,14 +179,16 @@ route_kernel(const T* __restrict__ q, const T* __restrict__ q_tilde,
 
 template <typename T, int D>
 cudaError_t run(const T* q, const T* qt, const float* vt, int BH, int N, int m, int s,
-                int32_t* route, float* lse, float* o, cudaStream_t st) {
+                int32_t* route, float* lse, float* o, int temp, cudaStream_t st) {
   const long long nqt = (N + kRouteThreads - 1) / kRouteThreads;
   const dim3 grid((unsigned)(BH * nqt));
+  // shared logits in log2 units: log2(e) / sqrt(d), or log2(e) / d
+  const float c = (float)(1.4426950408889634 / (temp ? (double)D : sqrt((double)D)));
   if (s == 1)
-    route_kernel<T, D, 2><<<grid, kRouteThreads, 0, st>>>(q, qt, vt, N, m, 1, route, lse, o);
+    route_kernel<T, D, 2><<<grid, kRouteThreads, 0, st>>>(q, qt, vt, N, m, 1, c, route, lse, o);
   else
-    route_kernel<T, D, kMaxRouteS + 1><<<grid, kRouteThreads, 0, st>>>(q, qt, vt, N, m, s, route,
-                                                                        lse, o);
+    route_kernel<T, D, kMaxRouteS + 1><<<grid, kRouteThreads, 0, st>>>(q, qt, vt, N, m, s, c,
+                                                                        route, lse, o);
   count_launch();
   return cudaGetLastError();
 }
@@ -194,20 +198,20 @@ cudaError_t run(const T* q, const T* qt, const float* vt, int BH, int N, int m, 
 template <typename T>
 cudaError_t launch_route(const T* q, const T* q_tilde, const float* v_tilde, int BH, int N,
                          int d, int m, int s, int32_t* route_idx, float* shared_lse,
-                         float* shared_o, cudaStream_t st) {
+                         float* shared_o, cudaStream_t st, int shared_temp) {
   if (s < 1 || s > kMaxRouteS || s > m) return cudaErrorInvalidValue;
   switch (d) {
-    case 16: return run<T, 16>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, st);
-    case 32: return run<T, 32>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, st);
-    case 64: return run<T, 64>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, st);
-    case 128: return run<T, 128>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, st);
+    case 16: return run<T, 16>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, shared_temp, st);
+    case 32: return run<T, 32>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, shared_temp, st);
+    case 64: return run<T, 64>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, shared_temp, st);
+    case 128: return run<T, 128>(q, q_tilde, v_tilde, BH, N, m, s, route_idx, shared_lse, shared_o, shared_temp, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template cudaError_t launch_route<float>(const float*, const float*, const float*, int, int, int,
-                                         int, int, int32_t*, float*, float*, cudaStream_t);
+                                         int, int, int32_t*, float*, float*, cudaStream_t, int);
 template cudaError_t launch_route<bf16>(const bf16*, const bf16*, const float*, int, int, int,
-                                        int, int, int32_t*, float*, float*, cudaStream_t);
+                                        int, int, int32_t*, float*, float*, cudaStream_t, int);
 
 }  // namespace mita

@@ -52,6 +52,8 @@ def load() -> ctypes.CDLL:
                 "mita_expert_attn": [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P],
                 "mita_forward": [P, P, P, I, I, I, I, I, I, I, I, I, P, P],
                 "mita_forward_host": [P, P, P, I, I, I, I, I, I, I, I, I, P, P],
+                "mita_forward_ex": [P, P, P, I, I, I, I, I, I, I, I, I, P, P, P],
+                "mita_pool_grid": [P, I, I, I, I, I, I, I, I, P, P],
             }
             for name, at in sigs.items():
                 for suffix in ("", "_f32"):
@@ -125,7 +127,50 @@ def _need(t: torch.Tensor, name: str, dtype=None, device=None):
     return t
 
 
+class MitaOptions(ctypes.Structure):
+    """mita_options of the C header."""
+    _fields_ = [("shared_temperature", ctypes.c_int), ("landmark_grid_h", ctypes.c_int),
+                ("landmark_grid_w", ctypes.c_int)]
+
+
+SHARED_TEMPERATURES = {"sqrt_d": 0, "d": 1}
+
+
 # ---------------------------------------------------------------------------
+def mita_pool_grid(q, grid_h: int, grid_w: int, landmark_grid_h: int, landmark_grid_w: int,
+                   q_tilde=None, stream=None):
+    """Pooling onto an explicit landmark_grid_h x landmark_grid_w landmark grid."""
+    _need(q, "q")
+    B, H, N, d = q.shape
+    m = landmark_grid_h * landmark_grid_w
+    if q_tilde is None:
+        q_tilde = torch.empty((B, H, m, d), dtype=q.dtype, device=q.device)
+    _need(q_tilde, "q_tilde", q.dtype, q.device)
+    _check(_fn("mita_pool_grid", q.dtype)(_ptr(q), B, H, N, d, grid_h, grid_w, landmark_grid_h,
+                                          landmark_grid_w, _ptr(q_tilde),
+                                          _stream(stream, q.device)))
+    return q_tilde
+
+
+def mita_forward_ex(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int = 1,
+                    shared_temperature: str = "sqrt_d", landmark_grid=None, out=None,
+                    stream=None):
+    """mita_forward on device tensors with options: the shared logits' temperature
+    ("sqrt_d": q.q~/sqrt(d), "d": q.q~/d) and an explicit (rows, cols) landmark grid."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, q.device)
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, q.device)
+    lh, lw = landmark_grid if landmark_grid is not None else (0, 0)
+    opt = MitaOptions(SHARED_TEMPERATURES[shared_temperature], lh, lw)
+    _check(_fn("mita_forward_ex", q.dtype)(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, grid_h, grid_w,
+                                           m, topk, s, ctypes.byref(opt), _ptr(out),
+                                           _stream(stream, q.device)))
+    return out
+
+
 def mita_pool(q, grid_h: int, grid_w: int, m: int, q_tilde=None, stream=None):
     _need(q, "q")
     B, H, N, d = q.shape
