@@ -51,8 +51,9 @@ def _load():
             lib.orc_route_rows.argtypes = [P, I, P, I, I, I, I, I, I, L, P, P, P]
             lib.orc_bucket.argtypes = [P, I, I, I, I, I, P, P]
             lib.orc_attend_rows.argtypes = [P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, L, P, P]
-            lib.orc_attend_rows_t.argtypes = [P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, L, P,
-                                              I, P]
+            lib.orc_attend_rows_v.argtypes = [P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, L, P,
+                                              I, I, P]
+            lib.orc_dense_rows.argtypes = [P, P, P, I, I, I, I, I, L, P, P]
             lib.orc_num_threads.restype = I
             lib.orc_set_num_threads.argtypes = [I]
             _lib = lib
@@ -159,14 +160,17 @@ def bucket(route_idx, m: int):
 
 
 def attend(q, k, v, q_tilde, v_tilde, topk_idx, route_idx, queries=None,
-           shared_temperature: str = "sqrt_d"):
+           shared_temperature: str = "sqrt_d", branches: str = "both"):
     """Joint-softmax output (float64) for all queries [B,H,N,d] or a sample [R,d].
 
     ``route_idx`` is [B,H,N,s] for all queries, or [R,s] aligned with ``queries``.
     ``shared_temperature``: "sqrt_d" (every logit / sqrt(d)) or "d" (the shared
     logits q . q~ / d, raw logits still / sqrt(d)).
+    ``branches``: "both" (the m shared pairs and the s*k raw pairs) or "routed"
+    (the routing-only ablation: the s*k raw pairs alone).
     """
     temp = {"sqrt_d": 0, "d": 1}[shared_temperature]
+    routed = {"both": 0, "routed": 1}[branches]
     q, k, v = _cpu(q), _cpu(k), _cpu(v)
     B, H, N, d = q.shape
     qt = _cpu(q_tilde).to(torch.float64)
@@ -181,19 +185,36 @@ def attend(q, k, v, q_tilde, v_tilde, topk_idx, route_idx, queries=None,
         qsel = torch.as_tensor(queries, dtype=torch.int64).contiguous()
         R = qsel.numel()
     out = torch.empty((R, d), dtype=torch.float64)
-    _check(_load().orc_attend_rows_t(_p(q), _p(k), _p(v), _DT[q.dtype], _p(qt), _p(vt),
+    _check(_load().orc_attend_rows_v(_p(q), _p(k), _p(v), _DT[q.dtype], _p(qt), _p(vt),
                                      _p(ti), _p(r), B, H, N, d, m, topk, s, R, _p(qsel),
-                                     temp, _p(out)), "attend")
+                                     temp, routed, _p(out)), "attend")
+    return out.view(B, H, N, d) if queries is None else out
+
+
+def dense(q, k, v, queries=None):
+    """Dense softmax attention (float64): [B,H,N,d], or [R,d] for the flat query ids
+    ``queries``."""
+    q, k, v = _cpu(q), _cpu(k), _cpu(v)
+    B, H, N, d = q.shape
+    if queries is None:
+        R, qsel = B * H * N, None
+    else:
+        qsel = torch.as_tensor(queries, dtype=torch.int64).contiguous()
+        R = qsel.numel()
+    out = torch.empty((R, d), dtype=torch.float64)
+    _check(_load().orc_dense_rows(_p(q), _p(k), _p(v), _DT[q.dtype], B, H, N, d, R, _p(qsel),
+                                  _p(out)), "dense")
     return out.view(B, H, N, d) if queries is None else out
 
 
 def forward(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int = 1,
-            shared_temperature: str = "sqrt_d", landmark_grid=None):
+            shared_temperature: str = "sqrt_d", landmark_grid=None, branches: str = "both"):
     """All six steps for every query; returns a dict of every intermediate."""
     qt = pool(q, grid_h, grid_w, m, landmark_grid)
     ti, vt, tgap = landmark(qt, k, v, topk)
     r, rgap = route(q, qt, s)
     off, qidx = bucket(r, m)
-    out = attend(q, k, v, qt, vt, ti, r, shared_temperature=shared_temperature)
+    out = attend(q, k, v, qt, vt, ti, r, shared_temperature=shared_temperature,
+                 branches=branches)
     return dict(q_tilde=qt, topk_idx=ti, v_tilde=vt, topk_gap=tgap, route=r,
                 route_gap=rgap, bucket_off=off, bucket_qidx=qidx, out=out)

@@ -303,16 +303,21 @@ int orc_bucket(const int32_t* route, int B, int H, int N, int m, int s,
 // concatenated in route order; overlapping experts (s > 1) contribute their
 // rows again, as the literal concatenation V* = [V~, V(e1), ..., V(es)] does.
 // shared_temp = 0: every logit / sqrt(d); 1: the shared logits q . q~_i / d.
-int orc_attend_rows_t(const void* q, const void* k, const void* v, int dt,
+// routed_only = 1: the model without the shared (compression) branch that
+// [NEWS] (LRA section) compares against at an equal number of entries per
+// query: the softmax runs over the s*k raw pairs alone.
+int orc_attend_rows_v(const void* q, const void* k, const void* v, int dt,
                       const double* q_tilde, const double* v_tilde,
                       const int32_t* topk_idx, const int32_t* route, int B, int H,
                       int N, int d, int m, int topk, int s, long nq,
-                      const int64_t* qsel, int shared_temp, double* out) {
+                      const int64_t* qsel, int shared_temp, int routed_only, double* out) {
   (void)B; (void)H;
   if (shared_temp != 0 && shared_temp != 1) return 1;
+  if (routed_only != 0 && routed_only != 1) return 1;
   const double sqrt_d = std::sqrt((double)d);
   const double shared_div = shared_temp ? (double)d : sqrt_d;
-  const long E = (long)m + (long)s * topk;
+  const int m_used = routed_only ? 0 : m;
+  const long E = (long)m_used + (long)s * topk;
 #pragma omp parallel
   {
     std::vector<double> logit(E);
@@ -325,7 +330,7 @@ int orc_attend_rows_t(const void* q, const void* k, const void* v, int dt,
       long bh = qi / N;
       size_t kv0 = (size_t)bh * N * d;
       long e = 0;
-      for (int i = 0; i < m; ++i, ++e) {
+      for (int i = 0; i < m_used; ++i, ++e) {
         const double* qt = q_tilde + ((size_t)bh * m + i) * d;
         double a = 0.0;
         for (int l = 0; l < d; ++l) a += widen(q, dt, (size_t)qi * d + l) * qt[l];
@@ -363,8 +368,42 @@ int orc_attend_rows(const void* q, const void* k, const void* v, int dt,
                     const int32_t* topk_idx, const int32_t* route, int B, int H,
                     int N, int d, int m, int topk, int s, long nq,
                     const int64_t* qsel, double* out) {
-  return orc_attend_rows_t(q, k, v, dt, q_tilde, v_tilde, topk_idx, route, B, H, N, d, m,
-                           topk, s, nq, qsel, 0, out);
+  return orc_attend_rows_v(q, k, v, dt, q_tilde, v_tilde, topk_idx, route, B, H, N, d, m,
+                           topk, s, nq, qsel, 0, 0, out);
+}
+
+// Dense softmax attention, softmax(q . k_j / sqrt(d)) over all N keys of the
+// query's head, weighting V: the baseline of the long-sequence inference
+// throughput comparison ([TUT] ch. 7, figure 5; [NEWS] throughput section).
+int orc_dense_rows(const void* q, const void* k, const void* v, int dt, int B, int H, int N,
+                   int d, long nq, const int64_t* qsel, double* out) {
+  (void)B; (void)H;
+  const double sqrt_d = std::sqrt((double)d);
+#pragma omp parallel
+  {
+    std::vector<double> logit(N);
+    std::vector<double> acc(d);
+#pragma omp for schedule(static)
+    for (long r = 0; r < nq; ++r) {
+      long qi = qsel ? qsel[r] : r;
+      long bh = qi / N;
+      size_t kv0 = (size_t)bh * N * d;
+      double mx = -INFINITY;
+      for (long j = 0; j < N; ++j) {
+        logit[j] = dot(q, dt, (size_t)qi * d, k, dt, kv0 + (size_t)j * d, d) / sqrt_d;
+        mx = std::max(mx, logit[j]);
+      }
+      double z = 0.0;
+      std::fill(acc.begin(), acc.end(), 0.0);
+      for (long j = 0; j < N; ++j) {
+        double w = std::exp(logit[j] - mx);
+        z += w;
+        for (int l = 0; l < d; ++l) acc[l] += w * widen(v, dt, kv0 + (size_t)j * d + l);
+      }
+      for (int l = 0; l < d; ++l) out[(size_t)r * d + l] = acc[l] / z;
+    }
+  }
+  return 0;
 }
 
 int orc_num_threads(void) {

@@ -394,3 +394,47 @@ def test_tiny_workload_runs():
     assert res["out"].shape == (1, 1, 64, 16)
     assert bool(torch.isfinite(res["out"]).all())
     assert res["bucket_off"][0, 0, -1].item() == 64
+
+
+# ----------------------------------------------------------------------------
+# Dense attention and the routing-only ablation
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_dense_matches_library_attention(dtype):
+    """The dense baseline is the textbook softmax(Q K^T / sqrt(d)) V."""
+    B, H, N, d = 2, 3, 200, 16
+    q, k, v = (_rand((B, H, N, d), dtype, s) for s in (11, 12, 13))
+    out = oracle.dense(q, k, v)
+    ref = F.scaled_dot_product_attention(q.double(), k.double(), v.double())
+    assert torch.allclose(out, ref, rtol=0, atol=1e-12)
+    sel = torch.tensor([0, 5, N - 1, N, B * H * N - 1])
+    assert torch.allclose(oracle.dense(q, k, v, queries=sel), ref.reshape(-1, d)[sel],
+                          rtol=0, atol=1e-12)
+
+
+def test_routed_only_single_expert_of_all_keys_is_dense():
+    """Routing only, m = 1, k = N: the one expert holds every key, so the output is
+    dense attention (no shared pair)."""
+    B, H, N, d = 1, 2, 96, 16
+    q, k, v, res = _setup(seed=14, B=B, H=H, N=N, d=d, m=1, k=N)
+    out = oracle.attend(q, k, v, res["q_tilde"], res["v_tilde"], res["topk_idx"], res["route"],
+                        branches="routed")
+    ref = F.scaled_dot_product_attention(q.double(), k.double(), v.double())
+    assert torch.allclose(out, ref, rtol=0, atol=1e-12)
+    # with the shared branch the same call differs (one more pair in the softmax)
+    assert (res["out"] - ref).abs().max().item() > 1e-3
+
+
+@pytest.mark.parametrize("s", [1, 2])
+def test_routed_only_is_softmax_over_the_routed_rows(s):
+    q, k, v, res = _setup(seed=15, s=s)
+    B, H, N, d = q.shape
+    out = oracle.attend(q, k, v, res["q_tilde"], res["v_tilde"], res["topk_idx"], res["route"],
+                        branches="routed")
+    qd, kd, vd = q.double(), k.double(), v.double()
+    for b in range(B):
+        for h in range(H):
+            for n in range(0, N, 5):
+                rows = torch.cat([res["topk_idx"][b, h, e].long() for e in res["route"][b, h, n]])
+                p = torch.softmax(kd[b, h, rows] @ qd[b, h, n] / math.sqrt(d), 0)
+                assert torch.allclose(out[b, h, n], p @ vd[b, h, rows], rtol=0, atol=1e-12)
