@@ -429,6 +429,64 @@ def forward_only(args):
     return 0
 
 
+# Reported throughput of MiTA over dense attention on the long synthetic sequences (MiTA
+# tutorial ch. 7, figure 5: RTX 4090, a three-layer model, batch tuned per length, m*k ~ N/4).
+PAGES_FIG5 = {1 << 14: 4.7, 1 << 16: 19.0, 1 << 18: 56.0, 1 << 20: 159.0}
+
+
+def _time_calls(fn, reps, stream):
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(reps):
+        fn()
+    ev1.record(stream)
+    ev1.synchronize()
+    return ev0.elapsed_time(ev1) / reps
+
+
+def fig5(args):
+    """The long-sequence sweep of the throughput figure: MiTA (m = k = sqrt(N/4)), the
+    routing-only model at the same entry count per query (topk = m + k, no shared branch) and
+    dense attention, one attention layer each, bf16, d = 64, H = 2, B*N = 2^20 tokens."""
+    from sparse_top_landmark_gb300 import build, mita
+    build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    out_rows = []
+    for i, N in enumerate(sorted(PAGES_FIG5)):
+        m = k = int(round((N / 4) ** 0.5))
+        B = max(1, (1 << 20) // N)
+        w = W.custom(f"fig5_{N}", B, 2, N, 64, "bf16", 1, N, m, k, clusters=max(16, m // 2),
+                     index=80 + i)
+        q, kk, v = W.make_qkv(w, 0)
+        dq, dk, dv = q.to(dev), kk.to(dev), v.to(dev)
+        out = torch.empty_like(dq)
+        with torch.cuda.stream(stream):
+            f_mita = lambda: mita.mita_forward(dq, dk, dv, 1, N, m, k, 1, out=out, stream=stream)
+            f_routed = lambda: mita.mita_forward_ex(dq, dk, dv, 1, N, m, m + k, 1,
+                                                    branches="routed", out=out, stream=stream)
+            f_dense = lambda: mita.mita_dense_attn(dq, dk, dv, out=out, stream=stream)
+            res = {}
+            for name, fn, reps in (("mita", f_mita, max(args.steps, 3)),
+                                   ("routed_equal_entries", f_routed, max(args.steps, 3)),
+                                   ("dense", f_dense, 1 if N >= (1 << 18) else 3)):
+                for _ in range(1 if name == "dense" else args.warmup):
+                    fn()
+                res[name] = _time_calls(fn, reps, stream)
+        assert mita.get_last_device_error(stream) == 0
+        row = {"N": N, "B": B, "H": 2, "d": 64, "m": m, "topk": k,
+               "mita_ms": res["mita"], "routed_equal_entries_ms": res["routed_equal_entries"],
+               "dense_ms": res["dense"], "speedup_vs_dense": res["dense"] / res["mita"],
+               "routed_over_mita": res["routed_equal_entries"] / res["mita"],
+               "pages_speedup_rtx4090_model": PAGES_FIG5[N]}
+        print(json.dumps(row), flush=True)
+        out_rows.append(row)
+        del dq, dk, dv, out
+        torch.cuda.empty_cache()
+    print(json.dumps({"fig5": out_rows}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,6 +496,8 @@ def main():
     ap.add_argument("--workload", default="long_1m", choices=list(W.WORKLOADS))
     ap.add_argument("--secondary", default="long_64k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fig5", action="store_true",
+                    help="sweep N = 16K..1M: MiTA, routing-only at equal entries, dense attention")
     ap.add_argument("--s", type=int, default=None,
                     help="routes per query (top-s); default: the workload's own (1)")
     ap.add_argument("--forward-only", type=int, default=0, metavar="R",
@@ -448,6 +508,8 @@ def main():
         return run_reference(args)
     if args.forward_only > 0:
         return forward_only(args)
+    if args.fig5:
+        return fig5(args)
 
     ws, rank, local = dist_env()
     n_gpus = max(ws, 1)

@@ -63,12 +63,19 @@ typedef struct CUstream_st* mita_stream_t;
  *   landmark_grid_w     index; landmark_grid_h * landmark_grid_w == m), e.g. a
  *                       non-square grid; 0, 0: 1 x m for a 1D sequence,
  *                       sqrt(m) x sqrt(m) for a 2D grid.
+ *   branches            MITA_BRANCHES_BOTH: the m shared pairs and the s*k raw
+ *                       pairs.  MITA_BRANCHES_ROUTED: the routing-only model
+ *                       the bit.fan article's LRA ablation compares against at
+ *                       an equal entry count (no shared branch: one softmax
+ *                       over the s*k raw pairs; choose topk for the count).
  */
 enum { MITA_SHARED_SQRT_D = 0, MITA_SHARED_D = 1 };
+enum { MITA_BRANCHES_BOTH = 0, MITA_BRANCHES_ROUTED = 1 };
 typedef struct mita_options {
   int shared_temperature;
   int landmark_grid_h;
   int landmark_grid_w;
+  int branches;
 } mita_options;
 
 enum mita_status {
@@ -244,6 +251,20 @@ int mita_forward_ex(const void* q, const void* k, const void* v, int B, int H, i
 int mita_forward_ex_f32(const float* q, const float* k, const float* v, int B, int H, int N,
                         int d, int grid_h, int grid_w, int m, int topk, int s,
                         const mita_options* options, float* out, mita_stream_t stream);
+
+/*
+ * mita_dense_attn -- dense softmax attention, out = softmax(q k^T / sqrt(d)) v
+ * over all N keys of each (batch, head): the baseline of the long-sequence
+ * throughput comparison (tutorial ch. 7, figure 5; bit.fan article,
+ * throughput section).  q, k, v, out [B,H,N,d] device pointers; bf16 with
+ * d = 64 runs on the tensor cores (the expert-attention kernel with one
+ * expert of all keys per head), other shapes on SIMT cores.  Uses the
+ * workspace cache.
+ */
+int mita_dense_attn(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                    void* out, mita_stream_t stream);
+int mita_dense_attn_f32(const float* q, const float* k, const float* v, int B, int H, int N,
+                        int d, float* out, mita_stream_t stream);
 
 /*
  * mita_forward_host -- mita_forward on HOST buffers (same method and

@@ -203,6 +203,8 @@ int check_options(const mita_options* o) {
   if (o == nullptr) return MITA_OK;
   if (o->shared_temperature != MITA_SHARED_SQRT_D && o->shared_temperature != MITA_SHARED_D)
     return fail(MITA_ERR_INVALID_ARG, "unknown shared_temperature %d", o->shared_temperature);
+  if (o->branches != MITA_BRANCHES_BOTH && o->branches != MITA_BRANCHES_ROUTED)
+    return fail(MITA_ERR_INVALID_ARG, "unknown branches %d", o->branches);
   return MITA_OK;
 }
 
@@ -421,6 +423,7 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   MITA_TRY(check_m(N, m));
   MITA_TRY(check_options(opt));
   const int temp = opt ? opt->shared_temperature : MITA_SHARED_SQRT_D;
+  const int routed = opt ? (opt->branches == MITA_BRANCHES_ROUTED) : 0;
   int mh = 0, mw = 0;
   MITA_TRY(check_grid(N, gh, gw, m, opt ? opt->landmark_grid_h : 0,
                       opt ? opt->landmark_grid_w : 0, &mh, &mw));
@@ -460,12 +463,14 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
     // entries, per-expert partials and their merge
     float* lse = reinterpret_cast<float*>(ws + L.lse);
     float* so = reinterpret_cast<float*>(ws + L.so);
-    MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st, temp),
+    // routing only: no shared partial
+    MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, routed ? nullptr : lse,
+                              routed ? nullptr : so, st, temp),
               "route launch");
     MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, false, s),
               "bucket launch");
     MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, BH, N, d, m, topk, s,
-                                    ws + L.ex, out, ds->status, st, temp),
+                                    ws + L.ex, out, ds->status, st, temp, routed),
               "expert launch");
     return MITA_OK;
   }
@@ -479,14 +484,36 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
   if constexpr (std::is_same<T, bf16>::value) {
     if (expert_tc_supported(d, m, topk)) {
       MITA_CUDA(launch_expert_tc(q, k, v, qt, vt, ti, off, qidx, BH, N, m, topk, ds->num_sms,
-                                 ws + L.ex, out, ds->status, st, temp),
+                                 ws + L.ex, out, ds->status, st, temp, routed),
                 "expert launch");
       return MITA_OK;
     }
   }
   MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, nullptr, nullptr, BH, N, d, m,
-                                  topk, 1, nullptr, out, ds->status, st, temp),
+                                  topk, 1, nullptr, out, ds->status, st, temp, routed),
             "expert launch");
+  return MITA_OK;
+}
+
+template <typename T>
+int dense_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d, T* out,
+               cudaStream_t st) {
+  MITA_TRY(check_shape(B, H, N, d));
+  MITA_TRY(check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}}));
+  DevState* ds = nullptr;
+  MITA_TRY(device_state(&ds));
+  const int BH = B * H;
+  void* ws = nullptr;
+  if constexpr (std::is_same<T, bf16>::value) {
+    if (d == 64) {
+      MITA_TRY(workspace(dense_tc_ws_bytes(BH, N), st, &ws));
+      MITA_CUDA(launch_dense_tc(q, k, v, BH, N, ds->num_sms, ws, out, ds->status, st),
+                "dense launch");
+      return MITA_OK;
+    }
+  }
+  MITA_TRY(workspace(dense_simt_ws_bytes(BH, N), st, &ws));
+  MITA_CUDA(launch_dense_attn<T>(q, k, v, BH, N, d, ws, out, ds->status, st), "dense launch");
   return MITA_OK;
 }
 
@@ -633,6 +660,17 @@ int mita_forward_ex_f32(const float* q, const float* k, const float* v, int B, i
                         const mita_options* options, float* out, mita_stream_t stream) {
   return mita::forward_impl<float>(q, k, v, B, H, N, d, grid_h, grid_w, m, topk, s, out, stream,
                                    options);
+}
+
+int mita_dense_attn(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                    void* out, mita_stream_t stream) {
+  return mita::dense_impl<bf16>(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                static_cast<const bf16*>(v), B, H, N, d, static_cast<bf16*>(out),
+                                stream);
+}
+int mita_dense_attn_f32(const float* q, const float* k, const float* v, int B, int H, int N,
+                        int d, float* out, mita_stream_t stream) {
+  return mita::dense_impl<float>(q, k, v, B, H, N, d, out, stream);
 }
 
 int mita_forward_host(const void* q, const void* k, const void* v, int B, int H, int N, int d,

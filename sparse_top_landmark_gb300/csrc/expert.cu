@@ -21,6 +21,8 @@
 // the tutorial's rule, in ascending bucket position (= ascending expert), so
 // the result does not depend on which CTA took which slot.  Overlapping
 // experts thus contribute duplicated rows, the literal concatenation.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -49,8 +51,8 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
                    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ bucket_off,
                    const int32_t* __restrict__ bucket_qidx, const float* __restrict__ shared_lse,
                    const float* __restrict__ shared_o, int N, int m, int topk, int s,
-                   float c_shared, int tiles_per_bh, T* __restrict__ out, Partials part,
-                   int* status) {
+                   float c_shared, int routed_only, int tiles_per_bh, T* __restrict__ out,
+                   Partials part, int* status) {
   __shared__ __align__(16) float ks[kRows][D];
   __shared__ __align__(16) float vs[kRows][D];
   __shared__ int rowid[kRows];
@@ -124,8 +126,8 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   };
 
   // ---- shared branch: the m pairs (q~_i, v~_i) -------------------------------
-  if (s > 1) {
-    // merged per query afterwards
+  if (s > 1 || routed_only) {
+    // s > 1: merged per query afterwards; routing only: no shared pairs
   } else if (shared_o != nullptr) {
     if (live) {
       const size_t qi = (size_t)bh * N + n;
@@ -236,20 +238,22 @@ expert_merge_kernel(const float* __restrict__ shared_lse, const float* __restric
     pp = part.pos[qi * s + lane];
   }
   int rank = 0;
-  float M = shared_lse[qi];
+  // routing only: no shared partial
+  const bool sh = shared_lse != nullptr;
+  float M = sh ? shared_lse[qi] : -INFINITY;
   for (int t = 0; t < s; ++t) {
     rank += __shfl_sync(0xffffffffu, pp, t) < pp ? 1 : 0;
     M = fmaxf(M, __shfl_sync(0xffffffffu, pl, t));
   }
   constexpr float kL2e = 1.4426950408889634f;
   constexpr int PER = (D + 31) / 32;
-  const float wsh = exp2f((shared_lse[qi] - M) * kL2e);
+  const float wsh = sh ? exp2f((shared_lse[qi] - M) * kL2e) : 0.f;
   float z = wsh;
   float acc[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int l = lane + 32 * j;
-    acc[j] = l < D ? wsh * shared_o[qi * D + l] : 0.f;
+    acc[j] = (sh && l < D) ? wsh * shared_o[qi * D + l] : 0.f;
   }
   for (int r = 0; r < s; ++r) {
     const unsigned who = __ballot_sync(0xffffffffu, lane < s && rank == r);
@@ -278,8 +282,8 @@ expert_merge_kernel(const float* __restrict__ shared_lse, const float* __restric
 template <typename T, int D>
 cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt,
                 const int32_t* ti, const int32_t* off, const int32_t* qidx, const float* lse,
-                const float* so, int BH, int N, int m, int topk, int s, int temp, void* pws,
-                T* out, int* status, cudaStream_t st) {
+                const float* so, int BH, int N, int m, int topk, int s, int temp, int routed,
+                void* pws, T* out, int* status, cudaStream_t st) {
   const float c_shared = (float)(1.4426950408889634 / (temp ? (double)D : sqrt((double)D)));
   const int tiles = (int)(((long long)N * s + kQTile - 1) / kQTile) + m;
   const long long blocks = (long long)BH * tiles;
@@ -298,13 +302,16 @@ cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt
     if (e != cudaSuccess) return e;
   }
   expert_attn_kernel<T, D><<<(unsigned)blocks, kQTile, 0, st>>>(
-      q, k, v, qt, vt, ti, off, qidx, lse, so, N, m, topk, s, c_shared, tiles, out, part, status);
+      q, k, v, qt, vt, ti, off, qidx, lse, so, N, m, topk, s, c_shared, routed, tiles, out, part,
+      status);
   count_launch();
   if (s > 1) {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     expert_merge_kernel<T, D><<<(unsigned)((BHN + kMergeWarps - 1) / kMergeWarps),
-                                kMergeWarps * 32, 0, st>>>(lse, so, part, BHN, s, out, status);
+                                kMergeWarps * 32, 0, st>>>(routed ? nullptr : lse,
+                                                           routed ? nullptr : so, part, BHN, s,
+                                                           out, status);
     count_launch();
   }
   return cudaGetLastError();
@@ -324,13 +331,15 @@ cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_ti
                                const int32_t* bucket_off, const int32_t* bucket_qidx,
                                const float* shared_lse, const float* shared_o, int BH, int N,
                                int d, int m, int topk, int s, void* ws, T* out, int* status,
-                               cudaStream_t st, int shared_temp) {
-  if (s < 1 || (s > 1 && (ws == nullptr || shared_lse == nullptr || shared_o == nullptr)))
+                               cudaStream_t st, int shared_temp, int routed_only) {
+  if (s < 1 || (s > 1 && (ws == nullptr ||
+                          (!routed_only && (shared_lse == nullptr || shared_o == nullptr)))))
     return cudaErrorInvalidValue;
 #define MITA_EXPERT_CASE(DD)                                                                 \
   case DD:                                                                                   \
     return run<T, DD>(q, k, v, q_tilde, v_tilde, topk_idx, bucket_off, bucket_qidx,          \
-                      shared_lse, shared_o, BH, N, m, topk, s, shared_temp, ws, out, status, st);
+                      shared_lse, shared_o, BH, N, m, topk, s, shared_temp, routed_only, ws,   \
+                      out, status, st);
   switch (d) {
     MITA_EXPERT_CASE(16)
     MITA_EXPERT_CASE(32)
@@ -345,11 +354,54 @@ template cudaError_t launch_expert_attn<float>(const float*, const float*, const
                                                const float*, const float*, const int32_t*,
                                                const int32_t*, const int32_t*, const float*,
                                                const float*, int, int, int, int, int, int, void*,
-                                               float*, int*, cudaStream_t, int);
+                                               float*, int*, cudaStream_t, int, int);
 template cudaError_t launch_expert_attn<bf16>(const bf16*, const bf16*, const bf16*, const bf16*,
                                               const float*, const int32_t*, const int32_t*,
                                               const int32_t*, const float*, const float*, int,
                                               int, int, int, int, int, void*, bf16*, int*,
-                                              cudaStream_t, int);
+                                              cudaStream_t, int, int);
+
+// Dense softmax attention through the same kernel: per head one expert holding every key
+// (identity index list), every query in its bucket, no shared pairs.
+namespace {
+__global__ void __launch_bounds__(256)
+dense_index_kernel(int BH, int N, int32_t* __restrict__ idx, int32_t* __restrict__ off) {
+  const long long nq = (long long)BH * N;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < nq;
+       t += (long long)gridDim.x * blockDim.x) {
+    idx[t] = (int32_t)(t % N);
+    if (t % N == 0) {
+      off[2 * (t / N)] = 0;
+      off[2 * (t / N) + 1] = N;
+    }
+  }
+}
+}  // namespace
+
+size_t dense_simt_ws_bytes(int BH, int N) {
+  return ((size_t)BH * N * 4 + 255) / 256 * 256 + (size_t)BH * 2 * 4;
+}
+
+template <typename T>
+cudaError_t launch_dense_attn(const T* q, const T* k, const T* v, int BH, int N, int d, void* ws,
+                              T* out, int* status, cudaStream_t st) {
+  int32_t* idx = static_cast<int32_t*>(ws);
+  int32_t* off = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
+                                            ((size_t)BH * N * 4 + 255) / 256 * 256);
+  const long long nq = (long long)BH * N;
+  dense_index_kernel<<<(unsigned)std::min<long long>((nq + 255) / 256, 4096), 256, 0, st>>>(
+      BH, N, idx, off);
+  count_launch();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the identity list is both the expert's key list ([BH, 1, N]) and the bucket ([BH, N])
+  return launch_expert_attn<T>(q, k, v, q, nullptr, idx, off, idx, nullptr, nullptr, BH, N, d, 1,
+                               N, 1, nullptr, out, status, st, 0, 1);
+}
+
+template cudaError_t launch_dense_attn<float>(const float*, const float*, const float*, int, int,
+                                              int, void*, float*, int*, cudaStream_t);
+template cudaError_t launch_dense_attn<bf16>(const bf16*, const bf16*, const bf16*, int, int, int,
+                                             void*, bf16*, int*, cudaStream_t);
 
 }  // namespace mita

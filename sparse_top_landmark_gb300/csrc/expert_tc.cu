@@ -203,7 +203,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
                  const __grid_constant__ CUtensorMap map_vg, const __grid_constant__ CUtensorMap map_qt,
                  const __grid_constant__ CUtensorMap map_vt, const int32_t* __restrict__ bucket_qidx,
                  const int* __restrict__ unit_count, const int4* __restrict__ unit_tab, int BH,
-                 int N, int m, int topk, float cs_shared, bf16* __restrict__ out, int* status) {
+                 int N, int m, int topk, float cs_shared, int use_shared, bf16* __restrict__ out,
+                 int* status) {
   griddep_wait();
   extern __shared__ unsigned char smem_raw[];
   ExpertSmem& s = *reinterpret_cast<ExpertSmem*>(
@@ -213,7 +214,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
   const int per = (U + gridDim.x - 1) / gridDim.x;          // contiguous units per CTA
   const int ubase = blockIdx.x * per;
   const int units = max(0, min(per, U - ubase));
-  const int nsc = (m + BN - 1) / BN, nrc = (topk + BN - 1) / BN, nc = nsc + nrc;
+  // shared chunks (none for the routing-only ablation and for dense attention)
+  const int nsc = use_shared ? (m + BN - 1) / BN : 0;
+  const int nrc = (topk + BN - 1) / BN, nc = nsc + nrc;
   const int G = units * nc;
   const int null_row = BH * N;   // out of range: TMA fills zeros
 
@@ -562,7 +565,7 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
                              const float* v_tilde, const int32_t* topk_idx,
                              const int32_t* bucket_off, const int32_t* bucket_qidx, int BH, int N,
                              int m, int topk, int num_sms, void* ws, bf16* out, int* status,
-                             cudaStream_t st, int shared_temp) {
+                             cudaStream_t st, int shared_temp, int routed_only) {
   const ExpertTcWs w = carve(ws, BH, N, m, topk);
   // log2(e) / sqrt(64), or log2(e) / 64 for the shared logits at the official code's temperature
   const float cs_shared = shared_temp ? 0.022542110013890052f : 0.18033688011112042f;
@@ -588,7 +591,72 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   e = launch_pdl(expert_tc_kernel, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
                  mqg, mkg, mvg, mqt, mvt, bucket_qidx,
                  static_cast<const int*>(w.unit_start + (size_t)BH * m),
-                 static_cast<const int4*>(w.unit), BH, N, m, topk, cs_shared, out, status);
+                 static_cast<const int4*>(w.unit), BH, N, m, topk, cs_shared, routed_only ? 0 : 1,
+                 out, status);
+  count_launch();
+  return e;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Dense softmax attention on the same kernel: one "expert" per head holding all N keys in
+// order (K and V are read in place, no gather), no shared chunks, queries in natural order.
+// ---------------------------------------------------------------------------------------------
+namespace {
+__global__ void __launch_bounds__(256)
+dense_units_kernel(int BH, int N, int4* __restrict__ unit, int* __restrict__ unit_count,
+                   int32_t* __restrict__ qidx) {
+  griddep_wait();
+  const long long per = (N + kUnitQ - 1) / kUnitQ;
+  const long long nu = (long long)BH * per, nq = (long long)BH * N;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < nu || t < nq;
+       t += stride) {
+    if (t < nu) {
+      const int bh = (int)(t / per), j = (int)(t % per);
+      unit[t] = make_int4(bh, j * kUnitQ, min(kUnitQ, N - j * kUnitQ), 0);
+    }
+    if (t < nq) qidx[t] = (int32_t)(t % N);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *unit_count = (int)nu;
+}
+}  // namespace
+
+size_t dense_tc_ws_bytes(int BH, int N) {
+  auto r = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t nu = (size_t)BH * ((N + kUnitQ - 1) / kUnitQ);
+  return r(nu * 16) + r(4) + r((size_t)BH * N * 4);
+}
+
+cudaError_t launch_dense_tc(const bf16* q, const bf16* k, const bf16* v, int BH, int N,
+                            int num_sms, void* ws, bf16* out, int* status, cudaStream_t st) {
+  auto r = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t nu = (size_t)BH * ((N + kUnitQ - 1) / kUnitQ);
+  char* p = static_cast<char*>(ws);
+  int4* unit = reinterpret_cast<int4*>(p);
+  int* ucount = reinterpret_cast<int*>(p + r(nu * 16));
+  int32_t* qidx = reinterpret_cast<int32_t*>(p + r(nu * 16) + r(4));
+  const long long work = std::max<long long>((long long)nu, (long long)BH * N);
+  const unsigned blocks =
+      (unsigned)std::min<long long>((work + 255) / 256, (long long)std::max(num_sms, 1) * 8);
+  cudaError_t e = launch_pdl(dense_units_kernel, dim3(blocks), dim3(256), 0, st, BH, N, unit,
+                             ucount, qidx);
+  count_launch();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mqg, mkg, mvg, mqt, mvt;
+  // the shared-block maps are never loaded (no shared chunks); any valid map will do
+  if (!make_tmap_gather64(&mqg, q, (uint64_t)BH * N) ||
+      !make_tmap_rows64(&mkg, k, (uint64_t)N, (uint64_t)BH, BN) ||
+      !make_tmap_rows64(&mvg, v, (uint64_t)N, (uint64_t)BH, BN) ||
+      !make_tmap_rows64(&mqt, k, (uint64_t)N, (uint64_t)BH, BN) ||
+      !make_tmap_rows64(&mvt, v, (uint64_t)N, (uint64_t)BH, BN))
+    return cudaErrorInvalidValue;
+  const size_t smem = sizeof(ExpertSmem) + 1024;
+  e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(expert_tc_kernel, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
+                 mqg, mkg, mvg, mqt, mvt, static_cast<const int32_t*>(qidx),
+                 static_cast<const int*>(ucount), static_cast<const int4*>(unit), BH, N, 1, N,
+                 0.18033688011112042f, 0, out, status);
   count_launch();
   return e;
 }

@@ -96,7 +96,13 @@ cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_ti
                                const int32_t* bucket_off, const int32_t* bucket_qidx,
                                const float* shared_lse, const float* shared_o, int BH,
                                int N, int d, int m, int topk, int s, void* ws, T* out,
-                               int* status, cudaStream_t st, int shared_temp = 0);
+                               int* status, cudaStream_t st, int shared_temp = 0,
+                               int routed_only = 0);
+// dense softmax attention (SIMT, any supported d): scratch of dense_simt_ws_bytes
+size_t dense_simt_ws_bytes(int BH, int N);
+template <typename T>
+cudaError_t launch_dense_attn(const T* q, const T* k, const T* v, int BH, int N, int d, void* ws,
+                              T* out, int* status, cudaStream_t st);
 
 // ---- tensor-core (tcgen05) kernels: bf16, d = 64 ---------------------------
 // TMA map over a [batches, rows, 64] bf16 array, boxes of box_rows rows.
@@ -120,7 +126,13 @@ cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                              const float* v_tilde, const int32_t* topk_idx,
                              const int32_t* bucket_off, const int32_t* bucket_qidx, int BH, int N,
                              int m, int topk, int num_sms, void* ws, __nv_bfloat16* out,
-                             int* status, cudaStream_t st, int shared_temp = 0);
+                             int* status, cudaStream_t st, int shared_temp = 0,
+                             int routed_only = 0);
+// dense softmax attention of every query over all N keys of its head (bf16, d = 64)
+size_t dense_tc_ws_bytes(int BH, int N);
+cudaError_t launch_dense_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                            const __nv_bfloat16* v, int BH, int N, int num_sms, void* ws,
+                            __nv_bfloat16* out, int* status, cudaStream_t st);
 
 int num_sms_of_current_device();
 

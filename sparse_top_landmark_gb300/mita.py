@@ -54,6 +54,7 @@ def load() -> ctypes.CDLL:
                 "mita_forward_host": [P, P, P, I, I, I, I, I, I, I, I, I, P, P],
                 "mita_forward_ex": [P, P, P, I, I, I, I, I, I, I, I, I, P, P, P],
                 "mita_pool_grid": [P, I, I, I, I, I, I, I, I, P, P],
+                "mita_dense_attn": [P, P, P, I, I, I, I, P, P],
             }
             for name, at in sigs.items():
                 for suffix in ("", "_f32"):
@@ -130,10 +131,11 @@ def _need(t: torch.Tensor, name: str, dtype=None, device=None):
 class MitaOptions(ctypes.Structure):
     """mita_options of the C header."""
     _fields_ = [("shared_temperature", ctypes.c_int), ("landmark_grid_h", ctypes.c_int),
-                ("landmark_grid_w", ctypes.c_int)]
+                ("landmark_grid_w", ctypes.c_int), ("branches", ctypes.c_int)]
 
 
 SHARED_TEMPERATURES = {"sqrt_d": 0, "d": 1}
+BRANCHES = {"both": 0, "routed": 1}
 
 
 # ---------------------------------------------------------------------------
@@ -153,10 +155,11 @@ def mita_pool_grid(q, grid_h: int, grid_w: int, landmark_grid_h: int, landmark_g
 
 
 def mita_forward_ex(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int = 1,
-                    shared_temperature: str = "sqrt_d", landmark_grid=None, out=None,
-                    stream=None):
+                    shared_temperature: str = "sqrt_d", landmark_grid=None,
+                    branches: str = "both", out=None, stream=None):
     """mita_forward on device tensors with options: the shared logits' temperature
-    ("sqrt_d": q.q~/sqrt(d), "d": q.q~/d) and an explicit (rows, cols) landmark grid."""
+    ("sqrt_d": q.q~/sqrt(d), "d": q.q~/d), an explicit (rows, cols) landmark grid, and
+    the branches ("both", or "routed": the routing-only ablation without shared pairs)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, q.dtype, q.device)
     B, H, N, d = q.shape
@@ -164,9 +167,22 @@ def mita_forward_ex(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int
         out = torch.empty_like(q)
     _need(out, "out", q.dtype, q.device)
     lh, lw = landmark_grid if landmark_grid is not None else (0, 0)
-    opt = MitaOptions(SHARED_TEMPERATURES[shared_temperature], lh, lw)
+    opt = MitaOptions(SHARED_TEMPERATURES[shared_temperature], lh, lw, BRANCHES[branches])
     _check(_fn("mita_forward_ex", q.dtype)(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, grid_h, grid_w,
                                            m, topk, s, ctypes.byref(opt), _ptr(out),
+                                           _stream(stream, q.device)))
+    return out
+
+
+def mita_dense_attn(q, k, v, out=None, stream=None):
+    """Dense softmax attention over all N keys of each head (the comparison baseline)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, q.device)
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, q.device)
+    _check(_fn("mita_dense_attn", q.dtype)(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, _ptr(out),
                                            _stream(stream, q.device)))
     return out
 

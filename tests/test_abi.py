@@ -112,15 +112,20 @@ def test_launch_counter_is_readable_without_a_gpu(lib):
 
 def test_forward_ex_and_pool_grid_validation(lib):
     f = lib.mita_forward_ex
-    opt = mita.MitaOptions(2, 0, 0)                  # unknown temperature
+    opt = mita.MitaOptions(2, 0, 0, 0)                  # unknown temperature
     assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 4, 1, ctypes.byref(opt), GOOD, NULL) == 1
     assert "shared_temperature" in _msg(lib)
-    opt = mita.MitaOptions(0, 2, 3)                  # 2 x 3 != m
+    opt = mita.MitaOptions(0, 2, 3, 0)                  # 2 x 3 != m
     assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 8, 8, 4, 4, 1, ctypes.byref(opt), GOOD, NULL) == 1
     assert "landmark grid" in _msg(lib)
-    opt = mita.MitaOptions(1, 2, 2)                  # 1D sequence onto a 2-row grid
+    opt = mita.MitaOptions(1, 2, 2, 0)                  # 1D sequence onto a 2-row grid
     assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 4, 1, ctypes.byref(opt), GOOD, NULL) == 1
-    opt = mita.MitaOptions(0, 0, 0)                  # 2D grid, non-square m, no landmark grid
+    opt = mita.MitaOptions(0, 0, 0, 0)                  # 2D grid, non-square m, no landmark grid
     assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 8, 8, 6, 4, 1, ctypes.byref(opt), GOOD, NULL) == 1
+    opt = mita.MitaOptions(0, 0, 0, 2)               # unknown branches
+    assert f(GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 4, 1, ctypes.byref(opt), GOOD, NULL) == 1
+    assert "branches" in _msg(lib)
+    assert lib.mita_dense_attn(GOOD, GOOD, NULL, 1, 1, 64, 16, GOOD, NULL) == 1
+    assert lib.mita_dense_attn_f32(GOOD, GOOD, GOOD, 1, 1, 64, 48, GOOD, NULL) == 2
     assert lib.mita_pool_grid(GOOD, 1, 1, 64, 16, 8, 8, 0, 3, GOOD, NULL) == 1
     assert lib.mita_pool_grid_f32(GOOD, 1, 1, 64, 16, 8, 8, 2, 3, NULL, NULL) == 1
