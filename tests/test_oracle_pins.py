@@ -438,3 +438,61 @@ def test_routed_only_is_softmax_over_the_routed_rows(s):
                 rows = torch.cat([res["topk_idx"][b, h, e].long() for e in res["route"][b, h, n]])
                 p = torch.softmax(kd[b, h, rows] @ qd[b, h, n] / math.sqrt(d), 0)
                 assert torch.allclose(out[b, h, n], p @ vd[b, h, rows], rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# Backward (selections held constant)
+# ----------------------------------------------------------------------------
+from oracle import backward as OB  # noqa: E402
+
+
+@pytest.mark.parametrize("s,temp,branches,grid", [
+    (1, "sqrt_d", "both", None), (2, "d", "both", None), (1, "sqrt_d", "routed", None),
+    (1, "sqrt_d", "both", (6, 8, (2, 3)))])
+def test_backward_forward_matches_c_oracle(s, temp, branches, grid):
+    """The torch restatement the backward differentiates gives the C oracle's output."""
+    if grid is None:
+        B, H, N, d, m, k, gh, gw, lg = 2, 2, 96, 16, 6, 10, 1, 96, None
+    else:
+        gh, gw, lg = grid
+        B, H, N, d, m, k = 2, 2, gh * gw, 16, lg[0] * lg[1], 9
+    w = W.custom("bw", B, H, N, d, "bf16", gh, gw, m, k, s, index=90)
+    q, kk, vv = W.make_qkv(w, 0)
+    ref = oracle.forward(q, kk, vv, gh, gw, m, k, s, shared_temperature=temp, landmark_grid=lg,
+                         branches=branches)
+    out = OB.forward_fixed(q.double(), kk.double(), vv.double(), ref["q_tilde"],
+                           ref["topk_idx"], ref["route"], gh, gw, m, lg, temp, branches)
+    assert torch.allclose(out, ref["out"], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("s,temp,branches", [(1, "sqrt_d", "both"), (2, "d", "both"),
+                                             (2, "sqrt_d", "routed")])
+def test_backward_matches_finite_differences(s, temp, branches):
+    """gradcheck: autograd's gradient of the fixed-selection forward against central
+    differences, on fp64 inputs (q~ rounding is then the identity)."""
+    B, H, N, d, m, k = 1, 2, 12, 4, 3, 5
+    g = torch.Generator().manual_seed(21)
+    q, kk, vv = (torch.randn((B, H, N, d), generator=g, dtype=torch.float64) for _ in range(3))
+    qt = oracle.pool(q, 1, N, m)
+    ti, _, _ = oracle.landmark(qt, kk, vv, k)
+    r, _ = oracle.route(q, qt, s)
+
+    def f(a, b_, c_):
+        return OB.forward_fixed(a, b_, c_, None, ti, r, 1, N, m, None, temp, branches)
+
+    assert torch.autograd.gradcheck(f, (q.requires_grad_(), kk.requires_grad_(),
+                                        vv.requires_grad_()), eps=1e-6, atol=1e-7)
+
+
+def test_backward_routed_single_expert_is_dense_attention_gradient():
+    """Routing only, m = 1, k = N is dense attention, so its gradient is the library
+    attention's gradient."""
+    B, H, N, d = 1, 2, 40, 8
+    g = torch.Generator().manual_seed(22)
+    q, kk, vv, do = (torch.randn((B, H, N, d), generator=g, dtype=torch.float64)
+                     for _ in range(4))
+    got = OB.backward(q, kk, vv, do, 1, N, 1, N, 1, branches="routed")
+    qr, kr, vr = (t.clone().requires_grad_(True) for t in (q, kk, vv))
+    ref = torch.autograd.grad(F.scaled_dot_product_attention(qr, kr, vr), (qr, kr, vr), do)
+    for a, b in zip(got, ref):
+        assert torch.allclose(a, b, rtol=0, atol=1e-12)
