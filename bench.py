@@ -487,6 +487,35 @@ def fig5(args):
     return 0
 
 
+def backward_bench(args):
+    """Device time of mita_backward (selections held constant; SIMT gradient kernels) on
+    --workload, next to the forward's, for one upstream gradient."""
+    from sparse_top_landmark_gb300 import build, mita
+    build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    w = workload_of(args.workload, args.s)
+    q, k, v = W.make_qkv(w, 0)
+    dq_, dk_, dv_ = q.to(dev), k.to(dev), v.to(dev)
+    dout = torch.randn(q.shape, generator=torch.Generator().manual_seed(1)).to(q.dtype).to(dev)
+    out = torch.empty_like(dq_)
+    with torch.cuda.stream(stream):
+        f_fwd = lambda: mita.mita_forward(dq_, dk_, dv_, w.grid_h, w.grid_w, w.m, w.topk, w.s,
+                                          out=out, stream=stream)
+        f_bwd = lambda: mita.mita_backward(dq_, dk_, dv_, dout, w.grid_h, w.grid_w, w.m, w.topk,
+                                           w.s, stream=stream)
+        for _ in range(args.warmup):
+            f_fwd()
+            f_bwd()
+        fwd = _time_calls(f_fwd, args.steps, stream)
+        bwd = _time_calls(f_bwd, args.steps, stream)
+    assert mita.get_last_device_error(stream) == 0
+    print(json.dumps({"backward": w.name, "config": config_of(w, 1), "forward_ms": fwd,
+                      "backward_ms": bwd, "steps": args.steps, "warmup": args.warmup,
+                      "grad_dtype": "f32"}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -496,6 +525,8 @@ def main():
     ap.add_argument("--workload", default="long_1m", choices=list(W.WORKLOADS))
     ap.add_argument("--secondary", default="long_64k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time mita_backward on --workload next to the forward")
     ap.add_argument("--fig5", action="store_true",
                     help="sweep N = 16K..1M: MiTA, routing-only at equal entries, dense attention")
     ap.add_argument("--s", type=int, default=None,
@@ -510,6 +541,8 @@ def main():
         return forward_only(args)
     if args.fig5:
         return fig5(args)
+    if args.backward:
+        return backward_bench(args)
 
     ws, rank, local = dist_env()
     n_gpus = max(ws, 1)

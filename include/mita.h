@@ -267,6 +267,30 @@ int mita_dense_attn_f32(const float* q, const float* k, const float* v, int B, i
                         int d, float* out, mita_stream_t stream);
 
 /*
+ * mita_backward -- gradients of mita_forward_ex's output with respect to q, k
+ * and v.  The pages give no gradient through the selections; reading taken:
+ * every landmark's top-k key set and every query's top-s landmarks are held
+ * constant (top-k and argmax are piecewise constant) and q~'s rounding to the
+ * input dtype passes the gradient straight through.  The gradient then flows
+ * through the joint softmax (tutorial ch. 4 steps 5-6), the shared values
+ * v~ = softmax(q~ K^T / sqrt(d)) V (steps 2-3) and the pooling (step 1).
+ *   q, k, v, dout [B,H,N,d]  inputs (device, bf16 or fp32); dout = dL/dout.
+ *   dq, dk, dv [B,H,N,d]     outputs, fp32 (device; cleared, then accumulated).
+ *   options                  as for mita_forward_ex (NULL: the defaults).
+ * Recomputes the forward's selections and partials with the forward's kernels,
+ * then runs SIMT gradient kernels (fp32 atomics; results vary in the last bits
+ * between runs).  Uses the workspace cache.
+ */
+int mita_backward(const void* q, const void* k, const void* v, const void* dout, int B, int H,
+                  int N, int d, int grid_h, int grid_w, int m, int topk, int s,
+                  const mita_options* options, float* dq, float* dk, float* dv,
+                  mita_stream_t stream);
+int mita_backward_f32(const float* q, const float* k, const float* v, const float* dout, int B,
+                      int H, int N, int d, int grid_h, int grid_w, int m, int topk, int s,
+                      const mita_options* options, float* dq, float* dk, float* dv,
+                      mita_stream_t stream);
+
+/*
  * mita_forward_host -- mita_forward on HOST buffers (same method and
  * parameters).  q, k, v [B,H,N,d] and out [B,H,N,d] are host pointers owned
  * by the caller; page-locked memory (cudaHostAlloc) copies at full speed,

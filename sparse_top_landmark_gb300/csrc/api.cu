@@ -3,6 +3,7 @@
 #include "mita.h"
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -517,6 +518,91 @@ int dense_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d, T
   return MITA_OK;
 }
 
+// The backward with the selections held constant: the forward's selections and partials
+// recomputed by the forward's own kernels, then the gradient kernels (backward.cu).
+template <typename T>
+int backward_impl(const T* q, const T* k, const T* v, const T* dout, int B, int H, int N, int d,
+                  int gh, int gw, int m, int topk, int s, const mita_options* opt, float* dq,
+                  float* dk, float* dv, cudaStream_t st) {
+  MITA_TRY(check_shape(B, H, N, d));
+  MITA_TRY(check_m(N, m));
+  MITA_TRY(check_options(opt));
+  int mh = 0, mw = 0;
+  MITA_TRY(check_grid(N, gh, gw, m, opt ? opt->landmark_grid_h : 0,
+                      opt ? opt->landmark_grid_w : 0, &mh, &mw));
+  MITA_TRY(check_topk(N, topk));
+  MITA_TRY(check_s(m, s));
+  MITA_TRY(check_entries(B, H, N, s));
+  MITA_TRY(check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {dout, "dout"}, {dq, "dq"}, {dk, "dk"},
+                       {dv, "dv"}}));
+  const int temp = opt ? opt->shared_temperature : MITA_SHARED_SQRT_D;
+  const int routed = opt ? (opt->branches == MITA_BRANCHES_ROUTED) : 0;
+  DevState* ds = nullptr;
+  MITA_TRY(device_state(&ds));
+  const int BH = B * H;
+  const size_t BHN = (size_t)BH * N, NS = (size_t)N * s;
+  const LandmarkPlan plan = plan_landmark(BH, N, d, m, topk, ds->num_sms, sizeof(T) == 2);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o += align256(bytes); return at; };
+  const size_t o_qt = take((size_t)BH * m * d * sizeof(T)), o_vt = take((size_t)BH * m * d * 4);
+  const size_t o_ti = take((size_t)BH * m * topk * 4), o_r = take((size_t)BH * NS * 4);
+  const size_t o_off = take((size_t)BH * (m + 1) * 4), o_qi = take((size_t)BH * NS * 4);
+  const size_t o_lm = take(landmark_ws_bytes(plan, BH, N, d, m));
+  const size_t o_bk = take(bucket_ws_bytes(BH, (int)NS, m));
+  const size_t o_sl = take(BHN * 4), o_so = take(BHN * d * 4);
+  const size_t o_pt = take(expert_partials_ws_bytes(BH, N, d, s));
+  const size_t o_lse = take(BHN * 4), o_dn = take(BHN * 4);
+  const size_t o_la = take((size_t)BH * m * 4), o_cv = take((size_t)BH * m * 4);
+  const size_t o_dqt = take((size_t)BH * m * d * 4), o_dvt = take((size_t)BH * m * d * 4);
+  void* wsv = nullptr;
+  MITA_TRY(workspace(o, st, &wsv));
+  char* ws = static_cast<char*>(wsv);
+  T* qt = reinterpret_cast<T*>(ws + o_qt);
+  float* vt = reinterpret_cast<float*>(ws + o_vt);
+  int32_t* ti = reinterpret_cast<int32_t*>(ws + o_ti);
+  int32_t* route = reinterpret_cast<int32_t*>(ws + o_r);
+  int32_t* off = reinterpret_cast<int32_t*>(ws + o_off);
+  int32_t* qidx = reinterpret_cast<int32_t*>(ws + o_qi);
+  float* sl = reinterpret_cast<float*>(ws + o_sl);
+  float* so = reinterpret_cast<float*>(ws + o_so);
+  ExpertPartials part;
+  part.o = reinterpret_cast<float*>(ws + o_pt);
+  part.lse = part.o + BHN * s * d;
+  part.pos = reinterpret_cast<int*>(part.lse + BHN * s);
+  part.cnt = part.pos + BHN * s;
+  const size_t gbytes = BHN * d * sizeof(float);
+  MITA_CUDA(cudaMemsetAsync(dq, 0, gbytes, st), "clearing dq");
+  MITA_CUDA(cudaMemsetAsync(dk, 0, gbytes, st), "clearing dk");
+  MITA_CUDA(cudaMemsetAsync(dv, 0, gbytes, st), "clearing dv");
+  MITA_CUDA(cudaMemsetAsync(ws + o_dqt, 0, (o_dvt - o_dqt) + (size_t)BH * m * d * 4, st),
+            "clearing scratch");
+  MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, mh, mw, qt, st), "pool launch");
+  const LandmarkWs lw = carve_landmark_ws(ws + o_lm, plan, BH, N, d, m);
+  MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, plan, lw, ti, vt, ds->status, st),
+            "landmark launch");
+  MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, routed ? nullptr : sl,
+                            routed ? nullptr : so, st, temp),
+            "route launch");
+  MITA_CUDA(launch_bucket(route, BH, N, m, ws + o_bk, off, qidx, ds->status, st, false, s),
+            "bucket launch");
+  MITA_CUDA(launch_expert_partials<T>(q, k, v, ti, off, qidx, BH, N, d, m, topk, s, part,
+                                      ds->status, st),
+            "expert partials");
+  BwdArgs<T> a{};
+  a.q = q; a.k = k; a.v = v; a.dout = dout; a.q_tilde = qt; a.v_tilde = vt;
+  a.topk_idx = ti; a.bucket_off = off; a.bucket_qidx = qidx;
+  a.sh_lse = routed ? nullptr : sl; a.sh_o = routed ? nullptr : so; a.part = part;
+  a.BH = BH; a.N = N; a.m = m; a.topk = topk; a.s = s; a.routed = routed;
+  a.c_sh = (float)(temp == MITA_SHARED_D ? 1.0 / d : 1.0 / std::sqrt((double)d));
+  a.grid_h = gh; a.grid_w = gw; a.mh = mh; a.mw = mw;
+  a.lse = reinterpret_cast<float*>(ws + o_lse); a.Dn = reinterpret_cast<float*>(ws + o_dn);
+  a.lseA = reinterpret_cast<float*>(ws + o_la); a.cvt = reinterpret_cast<float*>(ws + o_cv);
+  a.dqt = reinterpret_cast<float*>(ws + o_dqt); a.dvt = reinterpret_cast<float*>(ws + o_dvt);
+  a.dq = dq; a.dk = dk; a.dv = dv; a.status = ds->status;
+  MITA_CUDA(launch_backward<T>(a, d, st), "backward launch");
+  return MITA_OK;
+}
+
 // The forward on host buffers: H2D copies of q, k, v into the staging cache,
 // the forward, the D2H copy of the output, then a synchronisation of `st`.
 template <typename T>
@@ -671,6 +757,23 @@ int mita_dense_attn(const void* q, const void* k, const void* v, int B, int H, i
 int mita_dense_attn_f32(const float* q, const float* k, const float* v, int B, int H, int N,
                         int d, float* out, mita_stream_t stream) {
   return mita::dense_impl<float>(q, k, v, B, H, N, d, out, stream);
+}
+
+int mita_backward(const void* q, const void* k, const void* v, const void* dout, int B, int H,
+                  int N, int d, int grid_h, int grid_w, int m, int topk, int s,
+                  const mita_options* options, float* dq, float* dk, float* dv,
+                  mita_stream_t stream) {
+  return mita::backward_impl<bf16>(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                   static_cast<const bf16*>(v), static_cast<const bf16*>(dout), B,
+                                   H, N, d, grid_h, grid_w, m, topk, s, options, dq, dk, dv,
+                                   stream);
+}
+int mita_backward_f32(const float* q, const float* k, const float* v, const float* dout, int B,
+                      int H, int N, int d, int grid_h, int grid_w, int m, int topk, int s,
+                      const mita_options* options, float* dq, float* dk, float* dv,
+                      mita_stream_t stream) {
+  return mita::backward_impl<float>(q, k, v, dout, B, H, N, d, grid_h, grid_w, m, topk, s,
+                                    options, dq, dk, dv, stream);
 }
 
 int mita_forward_host(const void* q, const void* k, const void* v, int B, int H, int N, int d,

@@ -1,0 +1,520 @@
+// Backward pass of the MiTA forward with the selections held constant.
+//
+// The pages train MiTA end to end (MiTA tutorial ch. 7 table 5, LRA; the
+// bit.fan article's LRA section) but give no gradient through the selections.
+// Reading: every landmark's top-k key set and every query's top-s landmarks are
+// constants (top-k and argmax are piecewise constant) and q~'s rounding to the
+// input dtype passes the gradient straight through.  With
+//   q~ = pool(Q);  A = softmax(q~ K^T c);  v~ = A V            (tutorial ch. 4 steps 1-3)
+//   l_n = [q_n.q~_i c_sh]_i ++ [q_n.k_j c]_j;  o_n = softmax(l_n) . [v~; V_rows]  (steps 5-6)
+// (c = 1/sqrt(d), c_sh = c or 1/d) and dO the upstream gradient:
+//   D_n = dO_n . o_n;  for each entry e of query n:  p = exp(l - lse_n),
+//   ds = p (dO_n . val_e - D_n);  dq_n += ds key_e c_e;  dkey_e += ds q_n c_e;  dval_e += p dO_n
+// and through v~ = A V, with dv~ from the shared entries:
+//   dv_j += sum_i A_ij dv~_i;  dS_ij = A_ij (dv~_i . v_j - dv~_i . v~_i);
+//   dk_j += sum_i dS_ij q~_i c;  dq~_i += sum_j dS_ij k_j c;  dq_t += dq~_i / |window_i|.
+//
+// Kernels (SIMT, fp32, gradients accumulated with atomics into fp32 buffers):
+//   bwd_stats_kernel     per query: lse_n and D_n from the shared partial and the s raw
+//                        partials (the forward's own kernels recompute those);
+//   bwd_landmark_lse     per landmark row: ln sum_j exp(q~_i . k_j c);
+//   bwd_raw_kernel       per 64 bucket entries of one expert (its k rows staged 32 at a
+//                        time): dq, and the chunk's dK / dV as dS^T Q and P^T dO;
+//   bwd_shared_kernel    per 64 queries (landmarks staged 32 at a time): dq, dq~, dv~;
+//   bwd_vtilde_kernel    per 64 keys (landmarks staged 32 at a time): dk, dv, dq~;
+//   bwd_pool_kernel      per landmark: dq~ / |window| to every query of its window.
+#include <algorithm>
+#include <cmath>
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mita {
+namespace {
+
+constexpr int kT = 64;       // rows (queries or keys) per CTA, one per thread
+constexpr int kC = 32;       // staged rows per chunk
+constexpr float kL2e = 1.4426950408889634f;
+
+// ---- per-query statistics of the joint softmax -----------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_stats_kernel(const float* __restrict__ sh_lse, const float* __restrict__ sh_o,
+                 ExpertPartials part, long long BHN, int s, const void* __restrict__ dout,
+                 int dout_bf16, float* __restrict__ lse, float* __restrict__ Dn, int* status) {
+  const int lane = threadIdx.x & 31;
+  const long long qi = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (qi >= BHN) return;
+  if (part.cnt[qi] != s) {
+    if (lane == 0) flag_error(status, kDevErrBadBucket);
+    return;
+  }
+  float pl = -INFINITY;
+  if (lane < s) pl = part.lse[qi * s + lane];
+  const bool sh = sh_lse != nullptr;
+  float M = sh ? sh_lse[qi] : -INFINITY;
+  for (int t = 0; t < s; ++t) M = fmaxf(M, __shfl_sync(0xffffffffu, pl, t));
+  constexpr int PER = (D + 31) / 32;
+  const float wsh = sh ? exp2f((sh_lse[qi] - M) * kL2e) : 0.f;
+  float z = wsh, acc[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int l = lane + 32 * j;
+    acc[j] = (sh && l < D) ? wsh * sh_o[qi * D + l] : 0.f;
+  }
+  for (int t = 0; t < s; ++t) {
+    const float w = exp2f((__shfl_sync(0xffffffffu, pl, t) - M) * kL2e);
+    z += w;
+    const float* o = part.o + ((size_t)qi * s + t) * D;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int l = lane + 32 * j;
+      if (l < D) acc[j] = fmaf(w, o[l], acc[j]);
+    }
+  }
+  float dd = 0.f;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int l = lane + 32 * j;
+    if (l < D) {
+      const float g = dout_bf16 ? to_f(static_cast<const bf16*>(dout)[qi * D + l])
+                                : static_cast<const float*>(dout)[qi * D + l];
+      dd = fmaf(g, acc[j] / z, dd);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+  if (lane == 0) {
+    lse[qi] = M + logf(z);
+    Dn[qi] = dd;
+  }
+}
+
+// ---- landmark softmax normaliser: one warp per landmark row -------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+bwd_landmark_lse(const T* __restrict__ q_tilde, const T* __restrict__ k, long long rows, int N,
+                 int m, float c, float* __restrict__ lseA) {
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const long long bh = r / m;
+  float qt[D];
+  load_row<T, D>(q_tilde + (size_t)r * D, qt);
+  float mx = -INFINITY, sum = 0.f;
+  for (int j = lane; j < N; j += 32) {
+    float kr[D];
+    load_row<T, D>(k + ((size_t)bh * N + j) * D, kr);
+    float a = 0.f;
+#pragma unroll
+    for (int l = 0; l < D; ++l) a = fmaf(qt[l], kr[l], a);
+    const float x = a * c;
+    if (x > mx) {
+      sum *= __expf(mx - x);
+      mx = x;
+    }
+    sum += __expf(x - mx);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+    const float mm = fmaxf(mx, m2);
+    sum = (mx == -INFINITY ? 0.f : sum * __expf(mx - mm)) +
+          (m2 == -INFINITY ? 0.f : s2 * __expf(m2 - mm));
+    mx = mm;
+  }
+  if (lane == 0) lseA[r] = mx + logf(sum);
+}
+
+// Shared-memory tiles of one CTA: its kT rows (q or k, and dO or v), and kC staged rows.
+template <int D>
+struct BwdSmem {
+  float a[kT][D + 1];     // this CTA's rows: q (raw / shared) or k (v~ pass)
+  float g[kT][D + 1];     // dO (raw / shared) or v (v~ pass)
+  float ck[kC][D + 1];    // staged keys: k rows, q~ rows, or q~ rows
+  float cv[kC][D + 1];    // staged values: v rows, v~ rows, or dv~ rows
+  float P[kT][kC + 1];    // softmax weights of the chunk
+  float S[kT][kC + 1];    // their logit gradients
+  int rowid[kC];
+};
+
+// After a chunk's P and S are in shared memory: d(keys) = c * S^T A and d(values) = P^T G
+// for the kC staged rows, added with atomics at rows dst_k / dst_v (row r -> base + id*D).
+template <int D>
+__device__ __forceinline__ void chunk_outer(BwdSmem<D>& sm, int nc, float c, float* dkey_base,
+                                           float* dval_base, int tid) {
+  for (int x = tid; x < nc * D; x += kT) {
+    const int r = x / D, l = x % D;
+    const int id = sm.rowid[r];
+    float dk = 0.f, dv = 0.f;
+#pragma unroll 8
+    for (int n = 0; n < kT; ++n) {
+      dk = fmaf(sm.S[n][r], sm.a[n][l], dk);
+      dv = fmaf(sm.P[n][r], sm.g[n][l], dv);
+    }
+    if (id >= 0) {
+      if (dkey_base) atomicAdd(dkey_base + (size_t)id * D + l, dk * c);
+      if (dval_base) atomicAdd(dval_base + (size_t)id * D + l, dv);
+    }
+  }
+}
+
+// ---- raw entries, expert-grouped -----------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(kT)
+bwd_raw_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+               const T* __restrict__ dout, const int32_t* __restrict__ topk_idx,
+               const int32_t* __restrict__ bucket_off, const int32_t* __restrict__ bucket_qidx,
+               const float* __restrict__ lse, const float* __restrict__ Dn, int N, int m, int topk,
+               int s, int tiles_per_bh, float* __restrict__ dq, float* __restrict__ dk,
+               float* __restrict__ dv, int* status) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smraw);
+  __shared__ int s_e, s_t;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long bh = blockIdx.x / tiles_per_bh;
+  const int t = blockIdx.x % tiles_per_bh;
+  const int32_t* off = bucket_off + (size_t)bh * (m + 1);
+  const int NS = N * s;
+  if (warp == 0) {   // locate (expert, tile of the expert)
+    int run = 0, fe = -1, ft = 0;
+    for (int e0 = 0; e0 < m && fe < 0; e0 += 32) {
+      const int e = e0 + lane;
+      int cnt = 0;
+      if (e < m) {
+        const int a = off[e], b = off[e + 1];
+        if (a < 0 || b > NS || b < a) flag_error(status, kDevErrBadBucket);
+        else cnt = b - a;
+      }
+      const int nt = (cnt + kT - 1) / kT;
+      const int inc = warp_incl_scan(nt);
+      const int tot = __shfl_sync(0xffffffffu, inc, 31);
+      if (t < run + tot) {
+        const unsigned hit = __ballot_sync(0xffffffffu, run + inc > t);
+        const int f = __ffs(hit) - 1;
+        fe = e0 + f;
+        ft = t - (run + __shfl_sync(0xffffffffu, inc - nt, f));
+      }
+      run += tot;
+    }
+    if (lane == 0) { s_e = fe; s_t = ft; }
+  }
+  __syncthreads();
+  const int e = s_e;
+  if (e < 0) return;
+  const int slot = off[e] + s_t * kT + tid;
+  bool live = slot < off[e + 1];
+  int n = 0;
+  if (live) {
+    n = bucket_qidx[(size_t)bh * NS + slot];
+    if (n < 0 || n >= N) { flag_error(status, kDevErrBadBucket); live = false; }
+  }
+  const size_t qi = (size_t)bh * N + n;
+  float L = 0.f, Dq = 0.f;
+  if (live) {
+    float x[D];
+    load_row<T, D>(q + qi * D, x);
+#pragma unroll
+    for (int l = 0; l < D; ++l) sm.a[tid][l] = x[l];
+    load_row<T, D>(dout + qi * D, x);
+#pragma unroll
+    for (int l = 0; l < D; ++l) sm.g[tid][l] = x[l];
+    L = lse[qi];
+    Dq = Dn[qi];
+  } else {
+    for (int l = 0; l < D; ++l) { sm.a[tid][l] = 0.f; sm.g[tid][l] = 0.f; }
+  }
+  const float c = rsqrtf((float)D);
+  float dqa[D];
+#pragma unroll
+  for (int l = 0; l < D; ++l) dqa[l] = 0.f;
+  const int32_t* idx = topk_idx + ((size_t)bh * m + e) * topk;
+  const T* kb = k + (size_t)bh * N * D;
+  const T* vb = v + (size_t)bh * N * D;
+  for (int j0 = 0; j0 < topk; j0 += kC) {
+    const int nc = min(kC, topk - j0);
+    __syncthreads();
+    if (tid < kC) {
+      int j = -1;
+      if (tid < nc) {
+        j = idx[j0 + tid];
+        if (j < 0 || j >= N) { flag_error(status, kDevErrBadIndex); j = -1; }
+      }
+      sm.rowid[tid] = j;
+    }
+    __syncthreads();
+    for (int x = tid; x < nc * D; x += kT) {
+      const int r = x / D, l = x % D;
+      const int j = sm.rowid[r];
+      sm.ck[r][l] = j >= 0 ? to_f(kb[(size_t)j * D + l]) : 0.f;
+      sm.cv[r][l] = j >= 0 ? to_f(vb[(size_t)j * D + l]) : 0.f;
+    }
+    __syncthreads();
+    for (int r = 0; r < kC; ++r) {
+      float p = 0.f, ds = 0.f;
+      if (live && r < nc && sm.rowid[r] >= 0) {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int l = 0; l < D; ++l) {
+          a = fmaf(sm.a[tid][l], sm.ck[r][l], a);
+          b = fmaf(sm.g[tid][l], sm.cv[r][l], b);
+        }
+        p = __expf(a * c - L);
+        ds = p * (b - Dq);
+#pragma unroll
+        for (int l = 0; l < D; ++l) dqa[l] = fmaf(ds * c, sm.ck[r][l], dqa[l]);
+      }
+      sm.P[tid][r] = p;
+      sm.S[tid][r] = ds;
+    }
+    __syncthreads();
+    chunk_outer<D>(sm, nc, c, dk + (size_t)bh * N * D, dv + (size_t)bh * N * D, tid);
+  }
+  if (live) {
+#pragma unroll
+    for (int l = 0; l < D; ++l) atomicAdd(dq + qi * D + l, dqa[l]);
+  }
+}
+
+// ---- shared entries, query-major ------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(kT)
+bwd_shared_kernel(const T* __restrict__ q, const T* __restrict__ dout,
+                  const T* __restrict__ q_tilde, const float* __restrict__ v_tilde,
+                  const float* __restrict__ lse, const float* __restrict__ Dn, int N, int m,
+                  float c_sh, int tiles_per_bh, float* __restrict__ dq, float* __restrict__ dqt,
+                  float* __restrict__ dvt) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smraw);
+  const int tid = threadIdx.x;
+  const long long bh = blockIdx.x / tiles_per_bh;
+  const int n = (blockIdx.x % tiles_per_bh) * kT + tid;
+  const bool live = n < N;
+  const size_t qi = (size_t)bh * N + n;
+  float L = 0.f, Dq = 0.f;
+  if (live) {
+    float x[D];
+    load_row<T, D>(q + qi * D, x);
+#pragma unroll
+    for (int l = 0; l < D; ++l) sm.a[tid][l] = x[l];
+    load_row<T, D>(dout + qi * D, x);
+#pragma unroll
+    for (int l = 0; l < D; ++l) sm.g[tid][l] = x[l];
+    L = lse[qi];
+    Dq = Dn[qi];
+  } else {
+    for (int l = 0; l < D; ++l) { sm.a[tid][l] = 0.f; sm.g[tid][l] = 0.f; }
+  }
+  float dqa[D];
+#pragma unroll
+  for (int l = 0; l < D; ++l) dqa[l] = 0.f;
+  for (int i0 = 0; i0 < m; i0 += kC) {
+    const int nc = min(kC, m - i0);
+    __syncthreads();
+    if (tid < kC) sm.rowid[tid] = tid < nc ? i0 + tid : -1;
+    for (int x = tid; x < nc * D; x += kT) {
+      const int r = x / D, l = x % D;
+      sm.ck[r][l] = to_f(q_tilde[((size_t)bh * m + i0 + r) * D + l]);
+      sm.cv[r][l] = v_tilde[((size_t)bh * m + i0 + r) * D + l];
+    }
+    __syncthreads();
+    for (int r = 0; r < kC; ++r) {
+      float p = 0.f, ds = 0.f;
+      if (live && r < nc) {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int l = 0; l < D; ++l) {
+          a = fmaf(sm.a[tid][l], sm.ck[r][l], a);
+          b = fmaf(sm.g[tid][l], sm.cv[r][l], b);
+        }
+        p = __expf(a * c_sh - L);
+        ds = p * (b - Dq);
+#pragma unroll
+        for (int l = 0; l < D; ++l) dqa[l] = fmaf(ds * c_sh, sm.ck[r][l], dqa[l]);
+      }
+      sm.P[tid][r] = p;
+      sm.S[tid][r] = ds;
+    }
+    __syncthreads();
+    chunk_outer<D>(sm, nc, c_sh, dqt + (size_t)bh * m * D, dvt + (size_t)bh * m * D, tid);
+  }
+  if (live) {
+#pragma unroll
+    for (int l = 0; l < D; ++l) atomicAdd(dq + qi * D + l, dqa[l]);
+  }
+}
+
+// ---- through v~ = A V, key-major ------------------------------------------------------------
+// per landmark: cvt_i = dv~_i . v~_i
+__global__ void __launch_bounds__(256)
+bwd_vt_dot_kernel(const float* __restrict__ dvt, const float* __restrict__ v_tilde, long long rows,
+                  int D, float* __restrict__ cvt) {
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  float a = 0.f;
+  for (int l = lane; l < D; l += 32) a = fmaf(dvt[r * D + l], v_tilde[r * D + l], a);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+  if (lane == 0) cvt[r] = a;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kT)
+bwd_vtilde_kernel(const T* __restrict__ k, const T* __restrict__ v, const T* __restrict__ q_tilde,
+                  const float* __restrict__ dvt, const float* __restrict__ lseA,
+                  const float* __restrict__ cvt, int N, int m, int tiles_per_bh,
+                  float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dqt) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smraw);
+  __shared__ float s_lse[kC], s_c[kC];
+  const int tid = threadIdx.x;
+  const long long bh = blockIdx.x / tiles_per_bh;
+  const int j = (blockIdx.x % tiles_per_bh) * kT + tid;
+  const bool live = j < N;
+  const size_t kj = (size_t)bh * N + j;
+  if (live) {
+    float x[D];
+    load_row<T, D>(k + kj * D, x);
+#pragma unroll
+    for (int l = 0; l < D; ++l) sm.a[tid][l] = x[l];
+    load_row<T, D>(v + kj * D, x);
+#pragma unroll
+    for (int l = 0; l < D; ++l) sm.g[tid][l] = x[l];
+  } else {
+    for (int l = 0; l < D; ++l) { sm.a[tid][l] = 0.f; sm.g[tid][l] = 0.f; }
+  }
+  const float c = rsqrtf((float)D);
+  float dka[D], dva[D];
+#pragma unroll
+  for (int l = 0; l < D; ++l) { dka[l] = 0.f; dva[l] = 0.f; }
+  for (int i0 = 0; i0 < m; i0 += kC) {
+    const int nc = min(kC, m - i0);
+    __syncthreads();
+    if (tid < kC) {
+      sm.rowid[tid] = tid < nc ? i0 + tid : -1;
+      s_lse[tid] = tid < nc ? lseA[(size_t)bh * m + i0 + tid] : 0.f;
+      s_c[tid] = tid < nc ? cvt[(size_t)bh * m + i0 + tid] : 0.f;
+    }
+    for (int x = tid; x < nc * D; x += kT) {
+      const int r = x / D, l = x % D;
+      sm.ck[r][l] = to_f(q_tilde[((size_t)bh * m + i0 + r) * D + l]);
+      sm.cv[r][l] = dvt[((size_t)bh * m + i0 + r) * D + l];
+    }
+    __syncthreads();
+    for (int r = 0; r < kC; ++r) {
+      float ds = 0.f;
+      if (live && r < nc) {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int l = 0; l < D; ++l) {
+          a = fmaf(sm.a[tid][l], sm.ck[r][l], a);   // k_j . q~_i
+          b = fmaf(sm.g[tid][l], sm.cv[r][l], b);   // v_j . dv~_i
+        }
+        const float aw = __expf(a * c - s_lse[r]);   // A_ij
+        ds = aw * (b - s_c[r]);
+#pragma unroll
+        for (int l = 0; l < D; ++l) {
+          dva[l] = fmaf(aw, sm.cv[r][l], dva[l]);
+          dka[l] = fmaf(ds * c, sm.ck[r][l], dka[l]);
+        }
+      }
+      sm.S[tid][r] = ds;
+      sm.P[tid][r] = 0.f;
+    }
+    __syncthreads();
+    // dq~_i += c * sum_j dS_ij k_j   (no value-side term here)
+    chunk_outer<D>(sm, nc, c, dqt + (size_t)bh * m * D, nullptr, tid);
+  }
+  if (live) {
+#pragma unroll
+    for (int l = 0; l < D; ++l) {
+      atomicAdd(dk + kj * D + l, dka[l]);
+      atomicAdd(dv + kj * D + l, dva[l]);
+    }
+  }
+}
+
+// ---- pooling: dq_t += dq~_i / |window_i| ---------------------------------------------------
+__global__ void __launch_bounds__(128)
+bwd_pool_kernel(const float* __restrict__ dqt, int N, int D, int grid_h, int grid_w, int mh,
+                int mw, float* __restrict__ dq) {
+  const int m = mh * mw;
+  const long long flat = blockIdx.x;
+  const int i = (int)(flat % m);
+  const long long bh = flat / m;
+  int r0, r1, c0, c1;
+  adaptive_window(i / mw, grid_h, mh, &r0, &r1);
+  adaptive_window(i % mw, grid_w, mw, &c0, &c1);
+  const int nc = c1 - c0, cnt = (r1 - r0) * nc;
+  const float inv = 1.f / (float)cnt;
+  for (int x = threadIdx.x; x < cnt * D; x += blockDim.x) {
+    const int t = x / D, l = x % D;
+    const size_t tok = (size_t)(r0 + t / nc) * grid_w + c0 + t % nc;
+    atomicAdd(dq + ((size_t)bh * N + tok) * D + l, dqt[flat * D + l] * inv);
+  }
+}
+
+template <int D>
+size_t smem_bytes() { return sizeof(BwdSmem<D>); }
+
+template <typename T, int D>
+cudaError_t run(const BwdArgs<T>& A, cudaStream_t st) {
+  const int BH = A.BH, N = A.N, m = A.m;
+  const long long BHN = (long long)BH * N;
+  const size_t sm = smem_bytes<D>();
+  cudaError_t e;
+  for (const void* f : {(const void*)bwd_raw_kernel<T, D>, (const void*)bwd_shared_kernel<T, D>,
+                        (const void*)bwd_vtilde_kernel<T, D>}) {
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+  }
+  bwd_stats_kernel<D><<<(unsigned)((BHN + 7) / 8), 256, 0, st>>>(
+      A.routed ? nullptr : A.sh_lse, A.routed ? nullptr : A.sh_o, A.part, BHN, A.s, A.dout,
+      std::is_same<T, bf16>::value ? 1 : 0, A.lse, A.Dn, A.status);
+  count_launch();
+  const int qtiles = (N + kT - 1) / kT;
+  const int rtiles = (int)(((long long)N * A.s + kT - 1) / kT) + m;
+  bwd_raw_kernel<T, D><<<(unsigned)((long long)BH * rtiles), kT, sm, st>>>(
+      A.q, A.k, A.v, A.dout, A.topk_idx, A.bucket_off, A.bucket_qidx, A.lse, A.Dn, N, m, A.topk,
+      A.s, rtiles, A.dq, A.dk, A.dv, A.status);
+  count_launch();
+  if (!A.routed) {
+    bwd_shared_kernel<T, D><<<(unsigned)((long long)BH * qtiles), kT, sm, st>>>(
+        A.q, A.dout, A.q_tilde, A.v_tilde, A.lse, A.Dn, N, m, A.c_sh, qtiles, A.dq, A.dqt, A.dvt);
+    count_launch();
+    const long long rows = (long long)BH * m;
+    bwd_landmark_lse<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+        A.q_tilde, A.k, rows, N, m, (float)(1.0 / sqrt((double)D)), A.lseA);
+    count_launch();
+    bwd_vt_dot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(A.dvt, A.v_tilde, rows, D,
+                                                                  A.cvt);
+    count_launch();
+    bwd_vtilde_kernel<T, D><<<(unsigned)((long long)BH * qtiles), kT, sm, st>>>(
+        A.k, A.v, A.q_tilde, A.dvt, A.lseA, A.cvt, N, m, qtiles, A.dk, A.dv, A.dqt);
+    count_launch();
+    bwd_pool_kernel<<<(unsigned)rows, 128, 0, st>>>(A.dqt, N, D, A.grid_h, A.grid_w, A.mh, A.mw,
+                                                    A.dq);
+    count_launch();
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_backward(const BwdArgs<T>& a, int d, cudaStream_t st) {
+  switch (d) {
+    case 16: return run<T, 16>(a, st);
+    case 32: return run<T, 32>(a, st);
+    case 64: return run<T, 64>(a, st);
+    case 128: return run<T, 128>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+template cudaError_t launch_backward<float>(const BwdArgs<float>&, int, cudaStream_t);
+template cudaError_t launch_backward<bf16>(const BwdArgs<bf16>&, int, cudaStream_t);
+
+}  // namespace mita

@@ -36,13 +36,7 @@ constexpr int kMergeWarps = 8;
 __device__ __forceinline__ void put(float* p, float x) { *p = x; }
 __device__ __forceinline__ void put(bf16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-// the s > 1 partials (null when s = 1)
-struct Partials {
-  float* lse;   // [BH*N, s]     natural log-sum-exp of the expert's raw pairs
-  float* o;     // [BH*N, s, D]  their softmax-weighted mean of V
-  int* pos;     // [BH*N, s]     bucket position of the entry
-  int* cnt;     // [BH*N]        slots taken (cleared before the expert kernel)
-};
+using Partials = ExpertPartials;   // partial mode when .o is set
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kQTile)
@@ -126,8 +120,9 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   };
 
   // ---- shared branch: the m pairs (q~_i, v~_i) -------------------------------
-  if (s > 1 || routed_only) {
-    // s > 1: merged per query afterwards; routing only: no shared pairs
+  const bool partial = part.o != nullptr;
+  if (partial || routed_only) {
+    // partials: merged per query afterwards; routing only: no shared pairs
   } else if (shared_o != nullptr) {
     if (live) {
       const size_t qi = (size_t)bh * N + n;
@@ -201,7 +196,7 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 #pragma unroll
   for (int l = 0; l < D; ++l) acc[l] *= inv;
   const size_t qi = (size_t)bh * N + n;
-  if (s == 1) {
+  if (!partial) {
     store_row<T, D>(out + qi * D, acc);
     return;
   }
@@ -317,10 +312,46 @@ cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt
   return cudaGetLastError();
 }
 
+template <typename T, int D>
+cudaError_t run_partials(const T* q, const T* k, const T* v, const int32_t* ti, const int32_t* off,
+                         const int32_t* qidx, int BH, int N, int m, int topk, int s,
+                         ExpertPartials part, int* status, cudaStream_t st) {
+  const int tiles = (int)(((long long)N * s + kQTile - 1) / kQTile) + m;
+  const cudaError_t e = cudaMemsetAsync(part.cnt, 0, (size_t)BH * N * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  expert_attn_kernel<T, D><<<(unsigned)((long long)BH * tiles), kQTile, 0, st>>>(
+      q, k, v, q, nullptr, ti, off, qidx, nullptr, nullptr, N, m, topk, s, 0.f, 1, tiles,
+      nullptr, part, status);
+  count_launch();
+  return cudaGetLastError();
+}
+
 }  // namespace
 
+template <typename T>
+cudaError_t launch_expert_partials(const T* q, const T* k, const T* v, const int32_t* topk_idx,
+                                   const int32_t* bucket_off, const int32_t* bucket_qidx, int BH,
+                                   int N, int d, int m, int topk, int s, ExpertPartials part,
+                                   int* status, cudaStream_t st) {
+  switch (d) {
+    case 16: return run_partials<T, 16>(q, k, v, topk_idx, bucket_off, bucket_qidx, BH, N, m, topk, s, part, status, st);
+    case 32: return run_partials<T, 32>(q, k, v, topk_idx, bucket_off, bucket_qidx, BH, N, m, topk, s, part, status, st);
+    case 64: return run_partials<T, 64>(q, k, v, topk_idx, bucket_off, bucket_qidx, BH, N, m, topk, s, part, status, st);
+    case 128: return run_partials<T, 128>(q, k, v, topk_idx, bucket_off, bucket_qidx, BH, N, m, topk, s, part, status, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+template cudaError_t launch_expert_partials<float>(const float*, const float*, const float*,
+                                                   const int32_t*, const int32_t*, const int32_t*,
+                                                   int, int, int, int, int, int, ExpertPartials,
+                                                   int*, cudaStream_t);
+template cudaError_t launch_expert_partials<bf16>(const bf16*, const bf16*, const bf16*,
+                                                  const int32_t*, const int32_t*, const int32_t*,
+                                                  int, int, int, int, int, int, ExpertPartials,
+                                                  int*, cudaStream_t);
+
 size_t expert_partials_ws_bytes(int BH, int N, int d, int s) {
-  if (s <= 1) return 0;
+  if (s <= 0) return 0;
   const size_t r = (size_t)BH * N;
   return r * s * d * sizeof(float) + 2 * r * s * sizeof(float) + r * sizeof(int);
 }

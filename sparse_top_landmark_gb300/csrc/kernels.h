@@ -87,6 +87,19 @@ cudaError_t launch_bucket(const int32_t* route_idx, int BH, int N, int m, void* 
                           cudaStream_t st, bool counted = false, int s = 1);
 
 // ---- step 6: expert-grouped joint attention -------------------------------
+// Per (query, expert) partials over the expert's raw pairs: slot t < s of query qi.
+struct ExpertPartials {
+  float* lse;   // [BH*N, s]     natural log-sum-exp
+  float* o;     // [BH*N, s, d]  softmax-weighted mean of the expert's V rows
+  int* pos;     // [BH*N, s]     bucket position of the (query, expert) entry
+  int* cnt;     // [BH*N]        slots taken (cleared by the launcher)
+};
+// the raw-pair partials only (no shared pairs, no merge), for any s >= 1
+template <typename T>
+cudaError_t launch_expert_partials(const T* q, const T* k, const T* v, const int32_t* topk_idx,
+                                   const int32_t* bucket_off, const int32_t* bucket_qidx, int BH,
+                                   int N, int d, int m, int topk, int s, ExpertPartials part,
+                                   int* status, cudaStream_t st);
 // s > 1 needs the shared partial (shared_lse, shared_o) and `ws` of
 // expert_partials_ws_bytes(BH, N, d, s) bytes for the per-expert partials.
 size_t expert_partials_ws_bytes(int BH, int N, int d, int s);
@@ -133,6 +146,26 @@ size_t dense_tc_ws_bytes(int BH, int N);
 cudaError_t launch_dense_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                             const __nv_bfloat16* v, int BH, int N, int num_sms, void* ws,
                             __nv_bfloat16* out, int* status, cudaStream_t st);
+
+// ---- backward (selections held constant) ------------------------------------
+template <typename T>
+struct BwdArgs {
+  const T *q, *k, *v, *dout, *q_tilde;    // inputs, upstream gradient, the forward's q~
+  const float* v_tilde;                   // the forward's v~
+  const int32_t *topk_idx, *bucket_off, *bucket_qidx;
+  const float *sh_lse, *sh_o;             // the shared branch's partial (null: routing only)
+  ExpertPartials part;                    // the raw partials of every (query, expert)
+  int BH, N, m, topk, s, routed;
+  float c_sh;                             // shared-logit scale (1/sqrt(d) or 1/d)
+  int grid_h, grid_w, mh, mw;             // token grid and landmark grid
+  float *lse, *Dn;                        // [BH*N] scratch
+  float *lseA, *cvt;                      // [BH*m] scratch
+  float *dqt, *dvt;                       // [BH*m*d] scratch, cleared
+  float *dq, *dk, *dv;                    // [BH*N*d] outputs, cleared
+  int* status;
+};
+template <typename T>
+cudaError_t launch_backward(const BwdArgs<T>& a, int d, cudaStream_t st);
 
 int num_sms_of_current_device();
 

@@ -55,6 +55,7 @@ def load() -> ctypes.CDLL:
                 "mita_forward_ex": [P, P, P, I, I, I, I, I, I, I, I, I, P, P, P],
                 "mita_pool_grid": [P, I, I, I, I, I, I, I, I, P, P],
                 "mita_dense_attn": [P, P, P, I, I, I, I, P, P],
+                "mita_backward": [P, P, P, P, I, I, I, I, I, I, I, I, I, P, P, P, P, P],
             }
             for name, at in sigs.items():
                 for suffix in ("", "_f32"):
@@ -166,12 +167,55 @@ def mita_forward_ex(q, k, v, grid_h: int, grid_w: int, m: int, topk: int, s: int
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", q.dtype, q.device)
-    lh, lw = landmark_grid if landmark_grid is not None else (0, 0)
-    opt = MitaOptions(SHARED_TEMPERATURES[shared_temperature], lh, lw, BRANCHES[branches])
+    opt = _options(shared_temperature, landmark_grid, branches)
     _check(_fn("mita_forward_ex", q.dtype)(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, grid_h, grid_w,
                                            m, topk, s, ctypes.byref(opt), _ptr(out),
                                            _stream(stream, q.device)))
     return out
+
+
+def _options(shared_temperature, landmark_grid, branches):
+    lh, lw = landmark_grid if landmark_grid is not None else (0, 0)
+    return MitaOptions(SHARED_TEMPERATURES[shared_temperature], lh, lw, BRANCHES[branches])
+
+
+def mita_backward(q, k, v, dout, grid_h: int, grid_w: int, m: int, topk: int, s: int = 1,
+                  shared_temperature: str = "sqrt_d", landmark_grid=None, branches: str = "both",
+                  stream=None):
+    """(dq, dk, dv), fp32, of mita_forward_ex's output for the upstream gradient ``dout``,
+    with the forward's selections held constant."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, n, q.dtype, q.device)
+    B, H, N, d = q.shape
+    grads = [torch.empty(q.shape, dtype=torch.float32, device=q.device) for _ in range(3)]
+    opt = _options(shared_temperature, landmark_grid, branches)
+    _check(_fn("mita_backward", q.dtype)(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H, N, d, grid_h, grid_w, m, topk, s,
+        ctypes.byref(opt), _ptr(grads[0]), _ptr(grads[1]), _ptr(grads[2]),
+        _stream(stream, q.device)))
+    return tuple(grads)
+
+
+class MiTAFunction(torch.autograd.Function):
+    """MiTA attention as an autograd function: forward through mita_forward_ex, backward
+    through mita_backward (selections held constant; gradients cast to the input dtype)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, grid_h, grid_w, m, topk, s=1, shared_temperature="sqrt_d",
+                landmark_grid=None, branches="both"):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        ctx.save_for_backward(q, k, v)
+        ctx.cfg = (grid_h, grid_w, m, topk, s, shared_temperature, landmark_grid, branches)
+        return mita_forward_ex(q, k, v, grid_h, grid_w, m, topk, s, shared_temperature,
+                               landmark_grid, branches)
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v = ctx.saved_tensors
+        gh, gw, m, topk, s, temp, lg, br = ctx.cfg
+        dq, dk, dv = mita_backward(q, k, v, dout.contiguous().to(q.dtype), gh, gw, m, topk, s,
+                                   temp, lg, br)
+        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype)) + (None,) * 8
 
 
 def mita_dense_attn(q, k, v, out=None, stream=None):

@@ -129,3 +129,20 @@ def test_forward_ex_and_pool_grid_validation(lib):
     assert lib.mita_dense_attn_f32(GOOD, GOOD, GOOD, 1, 1, 64, 48, GOOD, NULL) == 2
     assert lib.mita_pool_grid(GOOD, 1, 1, 64, 16, 8, 8, 0, 3, GOOD, NULL) == 1
     assert lib.mita_pool_grid_f32(GOOD, 1, 1, 64, 16, 8, 8, 2, 3, NULL, NULL) == 1
+
+
+def test_backward_validation(lib):
+    f = lib.mita_backward
+    opt = mita.MitaOptions(0, 0, 0, 0)
+    # dq NULL
+    assert f(GOOD, GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 4, 1, ctypes.byref(opt), NULL, GOOD,
+             GOOD, NULL) == 1
+    assert "dq" in _msg(lib)
+    # s above the build's limit, unknown option
+    assert f(GOOD, GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 16, 4, 9, None, GOOD, GOOD, GOOD,
+             NULL) == 2
+    bad = mita.MitaOptions(0, 0, 0, 5)
+    assert f(GOOD, GOOD, GOOD, GOOD, 1, 1, 64, 16, 1, 64, 4, 4, 1, ctypes.byref(bad), GOOD, GOOD,
+             GOOD, NULL) == 1
+    assert lib.mita_backward_f32(GOOD, GOOD, GOOD, GOOD, 1, 1, 64, 48, 1, 64, 4, 4, 1, None, GOOD,
+                                 GOOD, GOOD, NULL) == 2

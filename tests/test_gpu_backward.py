@@ -1,0 +1,73 @@
+"""mita_backward on the GPU against the fp64 oracle's backward.
+
+Reading (the pages give no gradient through the selections): top-k key sets and
+routes held constant, q~'s rounding passed straight through; the oracle is the
+autograd gradient of a plain fp64 restatement of the forward, pinned by finite
+differences.  The GPU computes every gradient in fp32 from the same inputs:
+fp32 inputs must agree to rel-L2 1e-5; bf16 inputs use the forward's bf16 output
+tolerance on the relative L2 error (5e-3), since the recomputed v~ may come from
+the tensor-core landmark path with bf16 softmax weights.
+"""
+import pytest
+import torch
+
+from oracle import backward as OB
+from sparse_top_landmark_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # name: (workload, s, options)
+    "tiny_f32": (W.WORKLOADS["tiny_1d"], 1, {}),
+    "f32_d32_s1": (W.custom("b1", 2, 2, 300, 32, "f32", 1, 300, 6, 10, index=71), 1, {}),
+    "f32_d64_s2": (W.custom("b2", 1, 2, 256, 64, "f32", 1, 256, 8, 12, index=72), 2, {}),
+    "f32_routed": (W.custom("b3", 2, 1, 200, 16, "f32", 1, 200, 5, 9, index=73), 1,
+                   {"branches": "routed"}),
+    "f32_temp_d_grid": (W.custom("b4", 1, 2, 120, 32, "f32", 10, 12, 6, 8, index=74), 1,
+                        {"shared_temperature": "d", "landmark_grid": (2, 3)}),
+    "bf16_d64_s1": (W.custom("b5", 2, 2, 512, 64, "bf16", 1, 512, 16, 24, index=75), 1, {}),
+    "bf16_d64_s3": (W.custom("b6", 1, 2, 400, 64, "bf16", 1, 400, 10, 16, index=76), 3, {}),
+    "bf16_d128": (W.custom("b7", 1, 2, 256, 128, "bf16", 1, 256, 4, 20, index=77), 1, {}),
+    "bf16_vit_2d": (W.custom("b8", 2, 2, 196, 64, "bf16", 14, 14, 25, 25, index=78), 1, {}),
+}
+
+
+def M():
+    from sparse_top_landmark_gb300 import build, mita
+    build.build()
+    return mita
+
+
+def _rel(a, b):
+    return (torch.linalg.vector_norm(a.double() - b) / torch.linalg.vector_norm(b)).item()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_backward_matches_oracle(name):
+    mita = M()
+    w, s, opt = CASES[name]
+    q, k, v = W.make_qkv(w, 0)
+    g = torch.Generator().manual_seed(5)
+    dout = torch.randn(q.shape, generator=g).to(q.dtype)
+    dq, dk, dv = mita.mita_backward(q.cuda(), k.cuda(), v.cuda(), dout.cuda(), w.grid_h, w.grid_w,
+                                    w.m, w.topk, s, **opt)
+    assert mita.get_last_device_error() == 0
+    ref = OB.backward(q, k, v, dout, w.grid_h, w.grid_w, w.m, w.topk, s, **opt)
+    tol = 1e-5 if w.dtype == "f32" else 5e-3
+    for got, want, nm in zip((dq, dk, dv), ref, ("dq", "dk", "dv")):
+        err = _rel(got.cpu(), want)
+        assert err <= tol, f"{name} {nm}: rel-L2 {err:.3e} > {tol}"
+
+
+def test_autograd_function_trains_like_the_oracle():
+    """loss = sum(out * w): gradients through MiTAFunction equal the oracle's for dout = w."""
+    mita = M()
+    w = W.custom("b9", 2, 2, 256, 32, "f32", 1, 256, 8, 16, index=79)
+    q, k, v = W.make_qkv(w, 0)
+    wt = torch.randn(q.shape, generator=torch.Generator().manual_seed(6))
+    qc, kc, vc = (t.cuda().requires_grad_(True) for t in (q, k, v))
+    out = mita.MiTAFunction.apply(qc, kc, vc, 1, w.N, w.m, w.topk, 2)
+    (out * wt.cuda()).sum().backward()
+    ref = OB.backward(q, k, v, wt, 1, w.N, w.m, w.topk, 2)
+    for got, want in zip((qc.grad, kc.grad, vc.grad), ref):
+        assert _rel(got.cpu(), want) <= 1e-5
