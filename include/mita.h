@@ -298,7 +298,10 @@ int mita_backward_f32(const float* q, const float* k, const float* v, const floa
  * current device (a library-owned staging cache, one per (device, stream),
  * freed by mita_workspace_release), runs the forward on `stream`, copies the
  * output back into `out` and synchronises `stream` before returning: `out`
- * holds the result when the call returns MITA_OK.  Arguments are validated
+ * holds the result when the call returns MITA_OK.  The heads are split into
+ * up to four groups that pipeline (copies in, forward, copies out on two
+ * library-owned copy streams), and each group runs as its own batch, so the
+ * result can differ in the last bits from one mita_forward over all heads.  Arguments are validated
  * before any copy; on an error `out` is left unspecified.
  */
 int mita_forward_host(const void* q, const void* k, const void* v, int B, int H, int N, int d,

@@ -603,8 +603,42 @@ int backward_impl(const T* q, const T* k, const T* v, const T* dout, int B, int 
   return MITA_OK;
 }
 
-// The forward on host buffers: H2D copies of q, k, v into the staging cache,
-// the forward, the D2H copy of the output, then a synchronisation of `st`.
+// The forward on host buffers.  The host link, not the GPU, bounds this call (H2D and D2H
+// each run at about 200 GB/s on this part, whether a copy engine or the SMs drive them), so
+// the heads are split into up to kHostGroups groups that pipeline: a copy stream brings in
+// group g + 1's q, k, v while `st` runs group g's forward, and a second copy stream takes
+// group g's output back meanwhile (the link is full duplex).  Returns after `st` is
+// synchronised.
+constexpr int kHostGroups = 4;
+struct HostPipe {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev[2 + 2 * kHostGroups] = {};
+  std::mutex mu;   // one host-buffer forward at a time per device uses these
+};
+std::map<int, HostPipe*> g_pipe;
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  HostPipe*& p = g_pipe[dev];
+  if (p == nullptr) {
+    HostPipe* np = new HostPipe();
+    e = cudaStreamCreateWithFlags(&np->h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&np->d2h, cudaStreamNonBlocking);
+    for (auto& ev : np->ev)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      delete np;   // (any stream or event created so far is left to the context's teardown)
+      return cuda_fail(e, "copy streams");
+    }
+    p = np;
+  }
+  *out = p;
+  return MITA_OK;
+}
+
 template <typename T>
 int forward_host_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d, int gh,
                       int gw, int m, int topk, int s, T* out, cudaStream_t st) {
@@ -623,11 +657,41 @@ int forward_host_impl(const T* q, const T* k, const T* v, int B, int H, int N, i
   T* dk = reinterpret_cast<T*>(sb + bytes);
   T* dv = reinterpret_cast<T*>(sb + 2 * bytes);
   T* dout = reinterpret_cast<T*>(sb + 3 * bytes);
-  MITA_CUDA(cudaMemcpyAsync(dq, q, n * sizeof(T), cudaMemcpyHostToDevice, st), "copy of q");
-  MITA_CUDA(cudaMemcpyAsync(dk, k, n * sizeof(T), cudaMemcpyHostToDevice, st), "copy of k");
-  MITA_CUDA(cudaMemcpyAsync(dv, v, n * sizeof(T), cudaMemcpyHostToDevice, st), "copy of v");
-  MITA_TRY(forward_impl<T>(dq, dk, dv, B, H, N, d, gh, gw, m, topk, s, dout, st));
-  MITA_CUDA(cudaMemcpyAsync(out, dout, n * sizeof(T), cudaMemcpyDeviceToHost, st), "copy of out");
+  HostPipe* hp = nullptr;
+  MITA_TRY(host_pipe(&hp));
+  std::lock_guard<std::mutex> lk(hp->mu);
+  const int BH = B * H;
+  const int per = (BH + std::min(BH, kHostGroups) - 1) / std::min(BH, kHostGroups);
+  const int G = (BH + per - 1) / per;   // groups of `per` heads (the last may be smaller)
+  const size_t head = (size_t)N * d;    // elements per head
+  cudaEvent_t ev_start = hp->ev[0], ev_done = hp->ev[1];
+  MITA_CUDA(cudaEventRecord(ev_start, st), "event");
+  MITA_CUDA(cudaStreamWaitEvent(hp->h2d, ev_start, 0), "event wait");
+  MITA_CUDA(cudaStreamWaitEvent(hp->d2h, ev_start, 0), "event wait");
+  for (int g = 0; g < G; ++g) {
+    const size_t o = (size_t)g * per * head, c = (size_t)std::min(per, BH - g * per) * head;
+    MITA_CUDA(cudaMemcpyAsync(dq + o, q + o, c * sizeof(T), cudaMemcpyHostToDevice, hp->h2d),
+              "copy of q");
+    MITA_CUDA(cudaMemcpyAsync(dk + o, k + o, c * sizeof(T), cudaMemcpyHostToDevice, hp->h2d),
+              "copy of k");
+    MITA_CUDA(cudaMemcpyAsync(dv + o, v + o, c * sizeof(T), cudaMemcpyHostToDevice, hp->h2d),
+              "copy of v");
+    MITA_CUDA(cudaEventRecord(hp->ev[2 + g], hp->h2d), "event");
+  }
+  for (int g = 0; g < G; ++g) {
+    const int hg = std::min(per, BH - g * per);
+    const size_t o = (size_t)g * per * head, c = (size_t)hg * head;
+    MITA_CUDA(cudaStreamWaitEvent(st, hp->ev[2 + g], 0), "event wait");
+    // the heads are independent: a group runs as one batch of hg heads
+    MITA_TRY(forward_impl<T>(dq + o, dk + o, dv + o, 1, hg, N, d, gh, gw, m, topk, s, dout + o,
+                             st));
+    MITA_CUDA(cudaEventRecord(hp->ev[2 + kHostGroups + g], st), "event");
+    MITA_CUDA(cudaStreamWaitEvent(hp->d2h, hp->ev[2 + kHostGroups + g], 0), "event wait");
+    MITA_CUDA(cudaMemcpyAsync(out + o, dout + o, c * sizeof(T), cudaMemcpyDeviceToHost, hp->d2h),
+              "copy of out");
+  }
+  MITA_CUDA(cudaEventRecord(ev_done, hp->d2h), "event");
+  MITA_CUDA(cudaStreamWaitEvent(st, ev_done, 0), "event wait");
   MITA_CUDA(cudaStreamSynchronize(st), "synchronisation");
   return MITA_OK;
 }

@@ -169,6 +169,18 @@ def test_forward_end_to_end(name):
         assert_close(out.view(-1, w.d).cpu()[sel], ref, w.torch_dtype)
 
 
+def _host_reference(name):
+    w, q, k, v = inputs(name)
+    qt = oracle_pool(name)
+    oti, ovt, _ = oracle_landmark(name)
+    orr, _ = oracle.route(q, qt, 1)
+    return oracle.attend(q, k, v, qt, ovt, oti, orr)
+
+
+# The host-buffer forward pipelines groups of heads (copies of one group overlap the forward of
+# another), and each group runs as its own batch: some launch plans (e.g. the landmark stage's
+# key splits) depend on the batch's head count, so results may differ from the one-shot device
+# forward in the last bits.  Both must meet the oracle tolerance.
 def test_forward_host_buffers_match_device_path():
     mita = M()
     w, q, k, v = inputs("seg_32x32")
@@ -176,18 +188,28 @@ def test_forward_host_buffers_match_device_path():
     hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
     hout = mita.mita_forward(hq, hk, hv, w.grid_h, w.grid_w, w.m, w.topk)
     assert not hout.is_cuda
-    assert torch.equal(hout, dout.cpu())
+    ref = _host_reference("seg_32x32")
+    assert_close(hout, ref, w.torch_dtype)
+    assert_close(dout.cpu(), ref, w.torch_dtype)
+    # a single head runs as one group: identical to the device path
+    h1 = mita.mita_forward(hq[:1, :1].contiguous().pin_memory(), hk[:1, :1].contiguous().pin_memory(),
+                           hv[:1, :1].contiguous().pin_memory(), w.grid_h, w.grid_w, w.m, w.topk)
+    d1 = mita.mita_forward(dev(q[:1, :1]), dev(k[:1, :1]), dev(v[:1, :1]), w.grid_h, w.grid_w,
+                           w.m, w.topk)
+    assert torch.equal(h1, d1.cpu())
 
 
 def test_forward_host_pageable_buffers_match_device_path():
     mita = M()
     w, q, k, v = inputs("seg_32x32")
-    dout = mita.mita_forward(dev(q), dev(k), dev(v), w.grid_h, w.grid_w, w.m, w.topk)
     hout = torch.empty_like(q)                    # pageable, caller-owned
     r = mita.mita_forward(q.contiguous(), k.contiguous(), v.contiguous(), w.grid_h, w.grid_w,
                           w.m, w.topk, out=hout)
     assert r is hout
-    assert torch.equal(hout, dout.cpu())
+    assert_close(hout, _host_reference("seg_32x32"), w.torch_dtype)
+    pinned = mita.mita_forward(q.pin_memory(), k.pin_memory(), v.pin_memory(), w.grid_h,
+                               w.grid_w, w.m, w.topk)
+    assert torch.equal(hout, pinned)
 
 
 @pytest.mark.parametrize("name", ["seg_32x32", "long_64k"])
