@@ -577,7 +577,8 @@ int backward_impl(const T* q, const T* k, const T* v, const T* dout, int B, int 
   MITA_CUDA(cudaMemsetAsync(ws + o_dqt, 0, (o_dvt - o_dqt) + (size_t)BH * m * d * 4, st),
             "clearing scratch");
   MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, mh, mw, qt, st), "pool launch");
-  const LandmarkWs lw = carve_landmark_ws(ws + o_lm, plan, BH, N, d, m);
+  LandmarkWs lw = carve_landmark_ws(ws + o_lm, plan, BH, N, d, m);
+  lw.lse_out = reinterpret_cast<float*>(ws + o_la);   // each landmark's softmax normaliser
   MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, plan, lw, ti, vt, ds->status, st),
             "landmark launch");
   MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, routed ? nullptr : sl,

@@ -17,7 +17,8 @@
 // Kernels (SIMT, fp32, gradients accumulated with atomics into fp32 buffers):
 //   bwd_stats_kernel     per query: lse_n and D_n from the shared partial and the s raw
 //                        partials (the forward's own kernels recompute those);
-//   bwd_landmark_lse     per landmark row: ln sum_j exp(q~_i . k_j c);
+//   (each landmark's softmax normaliser ln sum_j exp(q~_i . k_j c) comes from the
+//    landmark stage, which forms it while merging v~);
 //   bwd_raw_kernel       per 64 bucket entries of one expert (its k rows staged 32 at a
 //                        time): dq, and the chunk's dK / dV as dS^T Q and P^T dO;
 //   bwd_shared_kernel    per 64 queries (landmarks staged 32 at a time): dq, dq~, dv~;
@@ -89,43 +90,6 @@ bwd_stats_kernel(const float* __restrict__ sh_lse, const float* __restrict__ sh_
     lse[qi] = M + logf(z);
     Dn[qi] = dd;
   }
-}
-
-// ---- landmark softmax normaliser: one warp per landmark row -------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(256)
-bwd_landmark_lse(const T* __restrict__ q_tilde, const T* __restrict__ k, long long rows, int N,
-                 int m, float c, float* __restrict__ lseA) {
-  const int lane = threadIdx.x & 31;
-  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  const long long bh = r / m;
-  float qt[D];
-  load_row<T, D>(q_tilde + (size_t)r * D, qt);
-  float mx = -INFINITY, sum = 0.f;
-  for (int j = lane; j < N; j += 32) {
-    float kr[D];
-    load_row<T, D>(k + ((size_t)bh * N + j) * D, kr);
-    float a = 0.f;
-#pragma unroll
-    for (int l = 0; l < D; ++l) a = fmaf(qt[l], kr[l], a);
-    const float x = a * c;
-    if (x > mx) {
-      sum *= __expf(mx - x);
-      mx = x;
-    }
-    sum += __expf(x - mx);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-    const float mm = fmaxf(mx, m2);
-    sum = (mx == -INFINITY ? 0.f : sum * __expf(mx - mm)) +
-          (m2 == -INFINITY ? 0.f : s2 * __expf(m2 - mm));
-    mx = mm;
-  }
-  if (lane == 0) lseA[r] = mx + logf(sum);
 }
 
 // Shared-memory tiles of one CTA: its kT rows (q or k, and dO or v), and kC staged rows.
@@ -486,9 +450,6 @@ cudaError_t run(const BwdArgs<T>& A, cudaStream_t st) {
         A.q, A.dout, A.q_tilde, A.v_tilde, A.lse, A.Dn, N, m, A.c_sh, qtiles, A.dq, A.dqt, A.dvt);
     count_launch();
     const long long rows = (long long)BH * m;
-    bwd_landmark_lse<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
-        A.q_tilde, A.k, rows, N, m, (float)(1.0 / sqrt((double)D)), A.lseA);
-    count_launch();
     bwd_vt_dot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(A.dvt, A.v_tilde, rows, D,
                                                                   A.cvt);
     count_launch();

@@ -48,6 +48,8 @@ struct LandmarkWs {
   int* cnt;        // [BH, m]          candidates collected
   float* cand_s;   // [BH, m, cap]
   int* cand_i;     // [BH, m, cap]
+  float* lse_out;  // [BH, m] or null: ln sum_j exp(q~_i . k_j / sqrt(d)) of every landmark
+                   // (the softmax normaliser behind v~; the backward reads it)
 };
 
 LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms, bool bf16_input);

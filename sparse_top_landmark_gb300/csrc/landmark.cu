@@ -290,6 +290,7 @@ landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, in
       den = fmaf(w, ws.L[r0 + s], den);
     }
     v_tilde[rowflat * D + l] = num / den;
+    if (l == 0 && ws.lse_out) ws.lse_out[rowflat] = (mx + log2f(den)) * 0.6931471805599453f;
   }
 
   // --- gather the kept candidates of every split -----------------------------

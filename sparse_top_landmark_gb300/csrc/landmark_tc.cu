@@ -487,6 +487,8 @@ lm_threshold_kernel(const bf16* __restrict__ q_tilde, int m, int topk, int S2, i
     const float num = (vnum[0][tid] + vnum[1][tid]) + (vnum[2][tid] + vnum[3][tid]);
     const float den = (vden[0] + vden[1]) + (vden[2] + vden[3]);
     v_tilde[rf * 64 + tid] = num / den;
+    // the row's softmax normaliser (M in log2 units of the scaled scores)
+    if (tid == 0 && ws.lse_out) ws.lse_out[rf] = (mx + log2f(den)) * 0.6931471805599453f;
   }
   __syncthreads();
   if (w == 0) {
