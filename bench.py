@@ -244,6 +244,21 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(secs, device, world):
+    """The slowest rank's seconds, on every rank (replicas: one process per GPU, each timing
+    its own copy of the workload; no data-path collective)."""
+    if world <= 1:
+        return secs
+    t = torch.tensor([secs], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.item()
+
+
+def replica_throughput(queries_per_rank, steps, secs, world):
+    """Whole-job queries/s: every rank's queries over the slowest rank's time."""
+    return world * queries_per_rank * steps / secs
+
+
 def config_of(w, n_gpus):
     total = 3 * w.B * w.H * w.N * w.d * (2 if w.dtype == "bf16" else 4)
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m,
@@ -346,13 +361,11 @@ def bench_workload(mita, w, args, dev, stream, n_gpus, do_e2e=True):
     t1 = time.time()
     sampler.stop()
     torch.cuda.synchronize(dev)
+    secs = max_over_ranks(secs, dev, n_gpus)
     if n_gpus > 1:
-        t = torch.tensor([secs], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        secs = t.item()
         torch.distributed.barrier()
     res = {"secs": secs, "clocks": sampler.summary(t0, t1)}
-    res["value"] = n_gpus * w.queries * args.steps / secs
+    res["value"] = replica_throughput(w.queries, args.steps, secs, n_gpus)
     res["ms_per_step"] = secs / args.steps * 1e3
     res["stages"] = stage_times(mita, w, dq, dk, dv, max(3, min(args.steps, 10)), stream)
     res["launches"] = count_launches(mita, w, dq, dk, dv, out, stream)
@@ -369,13 +382,9 @@ def bench_workload(mita, w, args, dev, stream, n_gpus, do_e2e=True):
         for _ in range(esteps):
             mita.mita_forward(hq, hk, hv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=hout,
                               stream=stream, device=dev)
-        es = time.perf_counter() - t0
-        if n_gpus > 1:
-            t = torch.tensor([es], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            es = t.item()
+        es = max_over_ranks(time.perf_counter() - t0, dev, n_gpus)
         e = q.element_size()
-        res["e2e"] = {"value": n_gpus * w.queries * esteps / es, "unit": UNIT,
+        res["e2e"] = {"value": replica_throughput(w.queries, esteps, es, n_gpus), "unit": UNIT,
                       "h2d_bytes_per_step": 3 * q.numel() * e,
                       "d2h_bytes_per_step": q.numel() * e}
     res["inputs"] = (q, k, v)
