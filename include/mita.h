@@ -333,6 +333,15 @@ int mita_get_last_device_error(mita_stream_t stream, int* bits);
 int mita_workspace_release(void);
 
 /*
+ * Caps the size one cached buffer (workspace or staging) may grow to; 0 removes
+ * the cap.  A call that would grow a buffer past it returns MITA_ERR_OOM before
+ * any allocation, exactly as when cudaMallocAsync fails, so callers can test
+ * their out-of-memory handling without exhausting a GPU.  Buffers already
+ * larger are kept.  Returns the previous cap.  Thread-safe.
+ */
+uint64_t mita_workspace_set_limit(uint64_t bytes);
+
+/*
  * Number of kernel launches this library has issued in this process so far
  * (all devices, all threads; a launch counts when it is enqueued).  The
  * difference of two readings around a section of host code is the number of

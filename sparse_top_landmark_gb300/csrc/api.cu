@@ -48,6 +48,10 @@ struct WsEntry {
 };
 std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws;
 std::map<std::pair<int, cudaStream_t>, WsEntry> g_stage;
+// Bytes one cached buffer may grow to (0: no limit).  A growth beyond it fails exactly as a
+// failed cudaMallocAsync does, before the allocator is called: the host-side way to make the
+// allocation failure path run without exhausting a GPU.
+std::atomic<unsigned long long> g_ws_limit{0};
 
 int device_state(DevState** out) {
   int dev = 0;
@@ -100,6 +104,10 @@ int cached_buffer(std::map<std::pair<int, cudaStream_t>, WsEntry>& cache, const 
     w.bytes = 0;
   }
   const size_t want = bytes + bytes / 8;
+  const unsigned long long limit = g_ws_limit.load();
+  if (limit != 0 && want > limit)
+    return fail(MITA_ERR_OOM, "%s of %zu bytes: above the workspace limit of %llu bytes", what,
+                want, limit);
   void* p = nullptr;
   e = cudaMallocAsync(&p, want, st);
   if (e != cudaSuccess) {
@@ -899,6 +907,10 @@ int mita_get_last_device_error(mita_stream_t stream, int* bits) {
 }
 
 uint64_t mita_kernel_launches(void) { return mita::g_launches.load(std::memory_order_relaxed); }
+
+uint64_t mita_workspace_set_limit(uint64_t bytes) {
+  return mita::g_ws_limit.exchange(bytes);
+}
 
 int mita_workspace_release(void) {
   std::lock_guard<std::mutex> lk(mita::g_mu);

@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
             lib.mita_get_last_device_error.restype = I
             lib.mita_workspace_release.argtypes = []
             lib.mita_workspace_release.restype = I
+            lib.mita_workspace_set_limit.argtypes = [ctypes.c_uint64]
+            lib.mita_workspace_set_limit.restype = ctypes.c_uint64
             lib.mita_kernel_launches.argtypes = []
             lib.mita_kernel_launches.restype = ctypes.c_uint64
             _lib = lib
@@ -386,6 +388,12 @@ def get_last_device_error(stream=None, device=None) -> int:
 
 def workspace_release() -> None:
     _check(load().mita_workspace_release())
+
+
+def workspace_set_limit(nbytes: int) -> int:
+    """Cap the growth of each cached buffer (0: no cap); returns the previous cap.  Growth past
+    it raises MitaError(MITA_ERR_OOM) before any allocation."""
+    return int(load().mita_workspace_set_limit(int(nbytes)))
 
 
 def kernel_launches() -> int:

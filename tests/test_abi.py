@@ -146,3 +146,8 @@ def test_backward_validation(lib):
              GOOD, NULL) == 1
     assert lib.mita_backward_f32(GOOD, GOOD, GOOD, GOOD, 1, 1, 64, 48, 1, 64, 4, 4, 1, None, GOOD,
                                  GOOD, GOOD, NULL) == 2
+
+
+def test_workspace_limit_setter_returns_the_previous_cap(lib):
+    assert mita.workspace_set_limit(1 << 20) == 0
+    assert mita.workspace_set_limit(0) == 1 << 20
