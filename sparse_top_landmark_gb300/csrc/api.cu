@@ -669,6 +669,19 @@ int forward_host_impl(const T* q, const T* k, const T* v, int B, int H, int N, i
   HostPipe* hp = nullptr;
   MITA_TRY(host_pipe(&hp));
   std::lock_guard<std::mutex> lk(hp->mu);
+  // On an error return, wait for every copy already queued: they read and write the caller's
+  // host buffers, which the caller may free as soon as this call returns.
+  struct Drain {
+    HostPipe* hp;
+    cudaStream_t st;
+    bool armed = true;
+    ~Drain() {
+      if (!armed) return;
+      cudaStreamSynchronize(hp->h2d);
+      cudaStreamSynchronize(hp->d2h);
+      cudaStreamSynchronize(st);
+    }
+  } drain{hp, st};
   const int BH = B * H;
   const int per = (BH + std::min(BH, kHostGroups) - 1) / std::min(BH, kHostGroups);
   const int G = (BH + per - 1) / per;   // groups of `per` heads (the last may be smaller)
@@ -702,6 +715,7 @@ int forward_host_impl(const T* q, const T* k, const T* v, int B, int H, int N, i
   MITA_CUDA(cudaEventRecord(ev_done, hp->d2h), "event");
   MITA_CUDA(cudaStreamWaitEvent(st, ev_done, 0), "event wait");
   MITA_CUDA(cudaStreamSynchronize(st), "synchronisation");
+  drain.armed = false;   // every stream is idle: st waited for the last copy out
   return MITA_OK;
 }
 
