@@ -189,8 +189,11 @@ int mita_bucket(const int32_t* route_idx, int B, int H, int N, int m, int s,
  *   The array is shared by every call and keeps the last call's contents;
  *   each call clears what it uses first.  Calls that overlap on the GPU
  *   (unordered streams) race on it: order them.
- *   The first call on a device looks up the array's address with that device
- *   current; make it before any stream capture starts.
+ *   The first call in each CUDA context (normally the device's primary
+ *   context) looks up the array's address in that context and caches it; make
+ *   it before any stream capture starts.  After cudaDeviceReset, or in another
+ *   context the caller makes current, the next call looks it up again, so
+ *   that call too belongs before any capture.
  *   Out-of-range route values are skipped but not recorded in the status word
  *   of mita_get_last_device_error.
  */
@@ -340,6 +343,22 @@ int mita_workspace_release(void);
  * larger are kept.  Returns the previous cap.  Thread-safe.
  */
 uint64_t mita_workspace_set_limit(uint64_t bytes);
+
+/*
+ * mita_check_bounded_wait -- exercises the failure path of the kernels' waits.
+ * Not a step of the paper's method: a diagnostic.  Every wait inside this
+ * library's kernels gives up after about one second (2^31 SM cycles), sets
+ * the timeout bit (8) of the device status word and lets its kernel return, so
+ * a lost arrival can never hang the GPU.  This call launches one small kernel
+ * that waits, with the same two wait routines the kernels use, on an mbarrier
+ * that nothing ever arrives on.
+ *   gave_up  device int[2]: 1 where the whole-warp (index 0) and the
+ *            single-thread (index 1) wait gave up, 0 where it completed.
+ * Asynchronous on `stream`; about one second later the kernel has returned,
+ * and mita_get_last_device_error reports bit 8.  Other work on the device is
+ * unaffected.  Returns MITA_ERR_INVALID_ARG for a NULL gave_up.
+ */
+int mita_check_bounded_wait(int* gave_up, mita_stream_t stream);
 
 /*
  * Number of kernel launches this library has issued in this process so far

@@ -659,6 +659,11 @@ int forward_host_impl(const T* q, const T* k, const T* v, int B, int H, int N, i
   if (!q || !k || !v || !out) return fail(MITA_ERR_INVALID_ARG, "null host pointer");
   const size_t n = (size_t)B * H * N * d;
   const size_t bytes = align256(n * sizeof(T));
+  HostPipe* hp = nullptr;
+  MITA_TRY(host_pipe(&hp));
+  // Held before the staging buffer is looked up: a call that grows (frees and reallocates)
+  // the buffer must not do so while another host-buffer forward is still copying into it.
+  std::lock_guard<std::mutex> lk(hp->mu);
   void* sv = nullptr;
   MITA_TRY(staging(4 * bytes, st, &sv));
   char* sb = static_cast<char*>(sv);
@@ -666,9 +671,6 @@ int forward_host_impl(const T* q, const T* k, const T* v, int B, int H, int N, i
   T* dk = reinterpret_cast<T*>(sb + bytes);
   T* dv = reinterpret_cast<T*>(sb + 2 * bytes);
   T* dout = reinterpret_cast<T*>(sb + 3 * bytes);
-  HostPipe* hp = nullptr;
-  MITA_TRY(host_pipe(&hp));
-  std::lock_guard<std::mutex> lk(hp->mu);
   // On an error return, wait for every copy already queued: they read and write the caller's
   // host buffers, which the caller may free as soon as this call returns.
   struct Drain {
@@ -921,6 +923,15 @@ int mita_get_last_device_error(mita_stream_t stream, int* bits) {
 }
 
 uint64_t mita_kernel_launches(void) { return mita::g_launches.load(std::memory_order_relaxed); }
+
+int mita_check_bounded_wait(int* gave_up, mita_stream_t stream) {
+  if (!gave_up) return mita::fail(MITA_ERR_INVALID_ARG, "mita_check_bounded_wait: NULL gave_up");
+  mita::DevState* ds = nullptr;
+  int rc = mita::device_state(&ds);
+  if (rc != MITA_OK) return rc;
+  const cudaError_t e = mita::launch_bounded_wait_probe(ds->status, gave_up, stream);
+  return e == cudaSuccess ? MITA_OK : mita::cuda_fail(e, "mita_check_bounded_wait launch");
+}
 
 uint64_t mita_workspace_set_limit(uint64_t bytes) {
   return mita::g_ws_limit.exchange(bytes);

@@ -18,15 +18,23 @@
 //     left there.  Each call writes every counter it uses before reading it.  Calls
 //     whose executions overlap on the GPU (different streams, no ordering
 //     between them) race on the array and give wrong results: order them.
-//   * The first call on a device looks up the array's device address
-//     (cudaGetSymbolAddress) with that device current and caches it.  Make
-//     that first call before any stream capture begins.
+//   * The first call in a CUDA context (a device's primary context, or any
+//     other context the caller makes current) looks up the array's device
+//     address there (cudaGetSymbolAddress) and caches it under that context.
+//     Make that first call before any stream capture begins; after a
+//     cudaDeviceReset the device gets a new context, and the next call looks
+//     the address up again (so it, too, should come before any capture).
 //   * Route values outside [0, m) are skipped, as in mita_bucket, but are not
 //     recorded in the status word read by mita_get_last_device_error (that
 //     word needs a one-time allocation).
 #include "mita.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -38,9 +46,28 @@ constexpr size_t kNoAllocScratchInts = size_t(1) << 20;   // 4 MiB of int32
 
 static __device__ __align__(256) int g_bucket_scratch[kNoAllocScratchInts];
 
-constexpr int kMaxDevices = 256;
+// The array's address in each CUDA context the entry point has run in.  A
+// module is loaded per context, so the address belongs to the context, not to
+// the device ordinal.  The driver's cuCtxGetCurrent is looked up through the
+// runtime (the library does not link libcuda directly).
 std::mutex g_na_mu;
-void* g_na_ptr[kMaxDevices] = {};
+std::vector<std::pair<CUcontext, void*>> g_na_ptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+bool g_ctx_looked_up = false;
+
+bool current_context(CUcontext* ctx) {
+  if (!g_ctx_looked_up) {
+    g_ctx_looked_up = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    cudaGetLastError();
+  }
+  return g_ctx_current && g_ctx_current(ctx) == CUDA_SUCCESS && *ctx != nullptr;
+}
 
 }  // namespace
 }  // namespace mita
@@ -62,23 +89,37 @@ extern "C" int mita_bucket_noalloc(const int32_t* route_idx, int B, int H, int N
                         "(4 MiB) of its static scratch; use mita_bucket");
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return report_error(MITA_ERR_CUDA, "mita_bucket_noalloc: no current CUDA device");
   }
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_na_mu);
-    if (g_na_ptr[dev] == nullptr) {
+    // No context is current yet on a thread whose first runtime call this is;
+    // cudaGetSymbolAddress then makes the device's primary context current.
+    CUcontext ctx = nullptr;
+    const bool had_ctx = current_context(&ctx);
+    if (had_ctx)
+      for (const auto& e : g_na_ptr)
+        if (e.first == ctx) scratch = e.second;
+    if (scratch == nullptr) {
       void* p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_bucket_scratch);
       if (e != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return report_error(MITA_ERR_CUDA, "mita_bucket_noalloc: cudaGetSymbolAddress failed");
       }
-      g_na_ptr[dev] = p;
+      if (!had_ctx && !current_context(&ctx)) {
+        cudaGetLastError();
+        return report_error(MITA_ERR_CUDA, "mita_bucket_noalloc: no current CUDA context");
+      }
+      bool known = false;
+      for (auto& c : g_na_ptr)
+        if (c.first == ctx) { c.second = p; known = true; }
+      if (!known) g_na_ptr.emplace_back(ctx, p);
+      scratch = p;
     }
-    scratch = g_na_ptr[dev];
   }
   const cudaError_t e =
       launch_bucket(route_idx, B * H, N, m, scratch, bucket_off, bucket_qidx, nullptr, stream,

@@ -179,4 +179,9 @@ void count_launch();
 // thread and returns `code`.
 int report_error(int code, const char* text);
 
+// A one-CTA kernel whose two bounded waits (whole-warp and single-thread) run out on an
+// mbarrier nothing arrives on: each flags kDevErrTimeout in *status and writes 1 to
+// gave_up[0] / gave_up[1] (device memory) when it gave up.
+cudaError_t launch_bounded_wait_probe(int* status, int* gave_up, cudaStream_t st);
+
 }  // namespace mita

@@ -46,13 +46,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
-// Bounded wait: returns false after `limit` unsuccessful polls (each poll
-// suspends the thread for a hardware-chosen interval), so a lost arrival can
-// never hang the GPU.
+// Bounded wait of one thread: gives up after `limit` unsuccessful polls (each
+// poll suspends the thread for a hardware-chosen interval) or about 2^31 SM
+// cycles (~1 s), whichever comes first, so a lost arrival can never hang the
+// GPU.  Inline (a call here costs the softmax warps registers).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint32_t limit = 1u << 24) {
-  for (uint32_t i = 0; i < limit; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > (1ll << 31)) break;
+  }
   return false;
 }
 

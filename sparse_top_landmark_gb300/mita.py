@@ -80,6 +80,8 @@ def load() -> ctypes.CDLL:
             lib.mita_workspace_set_limit.restype = ctypes.c_uint64
             lib.mita_kernel_launches.argtypes = []
             lib.mita_kernel_launches.restype = ctypes.c_uint64
+            lib.mita_check_bounded_wait.argtypes = [P, P]
+            lib.mita_check_bounded_wait.restype = I
             _lib = lib
     return _lib
 
@@ -399,3 +401,13 @@ def workspace_set_limit(nbytes: int) -> int:
 def kernel_launches() -> int:
     """Kernel launches this library has issued in this process so far."""
     return int(load().mita_kernel_launches())
+
+
+def check_bounded_wait(stream=None, device=None) -> torch.Tensor:
+    """Runs the library's wait-timeout probe (mita_check_bounded_wait): a kernel whose
+    two bounded waits on a never-arrived mbarrier must give up after about a second.
+    Returns the device int32[2] gave-up flags (1 = that wait gave up)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    gave_up = torch.full((2,), -1, dtype=torch.int32, device=dev)
+    _check(load().mita_check_bounded_wait(_ptr(gave_up), _stream(stream, dev)))
+    return gave_up

@@ -151,3 +151,8 @@ def test_backward_validation(lib):
 def test_workspace_limit_setter_returns_the_previous_cap(lib):
     assert mita.workspace_set_limit(1 << 20) == 0
     assert mita.workspace_set_limit(0) == 1 << 20
+
+
+def test_bounded_wait_probe_rejects_a_null_result(lib):
+    assert lib.mita_check_bounded_wait(NULL, NULL) == 1
+    assert "gave_up" in _msg(lib)

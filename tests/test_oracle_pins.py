@@ -248,6 +248,27 @@ def test_route_matches_full_sort(s):
             for n in range(N):
                 order = np.lexsort((np.arange(m), -S[b, h, n]))
                 assert np.array_equal(r[b, h, n].numpy(), order[:s])
+                # the boundary gap: s-th minus (s+1)-th best logit over max |logit|
+                amax = np.abs(S[b, h, n]).max()
+                g = (S[b, h, n][order[s - 1]] - S[b, h, n][order[s]]) / amax
+                assert abs(gap[b, h, n].item() - g) < 1e-15
+    # sampled queries give the same routes and gaps as the full run
+    sel = torch.tensor([0, 5, N + 3, 4 * N - 1])
+    r2, g2 = oracle.route(q, qt, s, queries=sel)
+    assert torch.equal(r2, r.view(-1, s)[sel])
+    assert torch.equal(g2, gap.view(-1)[sel])
+
+
+def test_route_gap_when_every_landmark_is_chosen():
+    """s = m: there is no boundary, the gap is reported as +inf-like (1e300)."""
+    q = _rand((1, 1, 5, 8), torch.float32, 25)
+    qt = _rand((1, 1, 3, 8), torch.float32, 26).double()
+    r, gap = oracle.route(q, qt, 3)
+    assert bool((gap > 1e299).all())
+    S = (q.double() @ qt.transpose(-1, -2))[0, 0]
+    for n in range(5):
+        order = np.lexsort((np.arange(3), -S[n].numpy()))
+        assert np.array_equal(r[0, 0, n].numpy(), order)
 
 
 def test_route_ties_go_to_lowest_landmark():
