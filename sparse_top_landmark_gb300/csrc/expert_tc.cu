@@ -13,8 +13,7 @@
 //   expert_gather_kernel  the k K / V rows of every (head, expert), copied once
 //                         into contiguous [head*m + expert][k][64] blocks; one
 //                         more CTA builds the work-unit table (unit = (head,
-//                         expert, up to 256 of its queries)); v~ to fp16 and
-//                         bf16, with a per-head choice between them;
+//                         expert, up to 256 of its queries)); v~ to bf16;
 //   expert_tc_kernel      persistent CTAs, each over a contiguous run of units
 //                         (units of one expert follow each other, so its
 //                         gathered rows are re-read from L2):
@@ -27,17 +26,15 @@
 //                tcgen05.mma only every ~130 cycles, so the two tiles get an
 //                issuer each): S = Q . B^T into the tile's S columns, and as
 //                soon as the softmax has copied S out, the next chunk's S;
-//                then O += P . V with P read from tensor memory (shared chunks
-//                as fp16 x fp16 with v~ in fp16, or bf16 x bf16 for a head whose
-//                v~ lies outside fp16's range; raw chunks bf16 x bf16);
+//                then O += P . V with P read from tensor memory (bf16 x bf16
+//                for both kinds of chunk: v~ is kept in bf16, fp32's range);
 //     warps 4-7 / 8-11   online softmax of query tile 0 / 1 (one query row per
-//                thread, lazy O rescaling; the exponentials of a chunk are
-//                computed before waiting for the previous P . V), then O / l
-//                to the output rows.
+//                thread, lazy O rescaling; half of a chunk's exponentials are
+//                computed before waiting for the previous P . V), then O / l to
+//                the output rows.  One code path for every chunk: a second,
+//                fp16 copy of the unrolled exponential loop (for an fp16 v~)
+//                cost ~8 % of the forward's time, measured.
 #include <algorithm>
-#include <type_traits>
-
-#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -75,19 +72,15 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
-__device__ __forceinline__ uint32_t pack_pair(float a, float b, bool fp16) {
-  if (fp16) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
+// two floats to a bf16 pair (a in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(a), "f"(b));
+  return r;
 }
 
 struct ExpertTcWs {
-  __half* vt16;      // [BH*m][64]
-  bf16* vtb;         // [BH*m][64]: the same values in bf16
-  int* vt_wide;      // [BH]: 1 = the head's shared chunks use vtb (v~ outside fp16's range)
+  bf16* vtb;         // [BH*m][64]: v~ in bf16
   int* unit_start;   // [BH*m + 1]
   int4* unit;        // [max units]: (head*m + expert, first bucket slot, count, 0)
   bf16* kg;          // [BH*m][topk][64]
@@ -106,9 +99,7 @@ ExpertTcWs carve(void* ws, int BH, int N, int m, int topk) {
     return r;
   };
   ExpertTcWs w;
-  w.vt16 = reinterpret_cast<__half*>(take((size_t)BH * m * 64 * 2));
   w.vtb = reinterpret_cast<bf16*>(take((size_t)BH * m * 64 * 2));
-  w.vt_wide = reinterpret_cast<int*>(take((size_t)BH * 4));
   w.unit_start = reinterpret_cast<int*>(take(((size_t)BH * m + 1) * 4));
   w.unit = reinterpret_cast<int4*>(take(max_units(BH, N, m) * 16));
   w.kg = reinterpret_cast<bf16*>(take((size_t)BH * m * topk * 128));
@@ -116,20 +107,12 @@ ExpertTcWs carve(void* ws, int BH, int N, int m, int topk) {
   return w;
 }
 
-// fp16 keeps three more mantissa bits than bf16 but covers only magnitudes up to 65504 (and
-// full precision only down to 2^-14).  A head's shared chunks take fp16 when its largest
-// |v~| lies in [2^-8, 2^15]: every value then converts without overflow, and values far
-// below the largest lose only absolute error far below the largest value's rounding.
-// Otherwise they take bf16 (fp32's exponent range).
-constexpr float kFp16VtMax = 32768.f, kFp16VtMin = 0.00390625f;
-
 // -------------------------------------------------------------------------------------------
 // Preparation, one launch: the last CTA builds the work-unit table (unit = (head*m + e, first
 // bucket slot, count <= 256); unit_start[head*m + e] = the expert's first unit, then one
-// entry per unit); the other CTAs convert v~ head by head to fp16 and bf16 (and record which
-// of the two the head's shared chunks use), then gather the experts' rows: row j of expert
-// (head, e) -> kg / vg[(head*m + e)*topk + j], eight lanes per row, 16 bytes each, four rows
-// per warp step.
+// entry per unit); every CTA converts a slice of v~ to bf16, and the other CTAs gather the
+// experts' rows: row j of expert (head, e) -> kg / vg[(head*m + e)*topk + j], eight lanes per
+// row, 16 bytes each, four rows per warp step.
 // -------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kGatherThreads)
 expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
@@ -137,39 +120,16 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
                      const int32_t* __restrict__ bucket_off, const float* __restrict__ v_tilde,
                      int BH, ExpertTcWs w, int* status) {
   griddep_wait();
-  if (blockIdx.x < gridDim.x - 1) {
-    // v~ of head bh in fp16 and in bf16, four values per thread step, and its largest |v~|
-    __shared__ float red[kGatherThreads / 32];
-    for (int bh = blockIdx.x; bh < BH; bh += gridDim.x - 1) {
-      const long long n4 = (long long)m * 16, base = (long long)bh * n4;
-      float amax = 0.f;
-      for (long long t = threadIdx.x; t < n4; t += blockDim.x) {
-        const float4 x = reinterpret_cast<const float4*>(v_tilde)[base + t];
-        // NaN compares false and keeps the head on bf16 below
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-        if (x.x != x.x || x.y != x.y || x.z != x.z || x.w != x.w) amax = INFINITY;
-        const __half2 lo = __floats2half2_rn(x.x, x.y), hi = __floats2half2_rn(x.z, x.w);
-        uint2 o;
-        o.x = *reinterpret_cast<const uint32_t*>(&lo);
-        o.y = *reinterpret_cast<const uint32_t*>(&hi);
-        reinterpret_cast<uint2*>(w.vt16)[base + t] = o;
-        const __nv_bfloat162 blo = __floats2bfloat162_rn(x.x, x.y),
-                             bhi = __floats2bfloat162_rn(x.z, x.w);
-        o.x = *reinterpret_cast<const uint32_t*>(&blo);
-        o.y = *reinterpret_cast<const uint32_t*>(&bhi);
-        reinterpret_cast<uint2*>(w.vtb)[base + t] = o;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float a = 0.f;
-        for (int i = 0; i < kGatherThreads / 32; ++i) a = fmaxf(a, red[i]);
-        w.vt_wide[bh] = (a <= kFp16VtMax && a >= kFp16VtMin) ? 0 : 1;
-      }
-      __syncthreads();
+  // v~ in bf16, four values per thread step
+  {
+    const long long n4 = (long long)BH * m * 16;
+    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n4;
+         t += (long long)gridDim.x * blockDim.x) {
+      const float4 x = reinterpret_cast<const float4*>(v_tilde)[t];
+      uint2 o;
+      o.x = pack_bf16(x.x, x.y);
+      o.y = pack_bf16(x.z, x.w);
+      reinterpret_cast<uint2*>(w.vtb)[t] = o;
     }
   }
   if (blockIdx.x == gridDim.x - 1) {
@@ -237,8 +197,7 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
 __global__ void __launch_bounds__(kThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_constant__ CUtensorMap map_kg,
                  const __grid_constant__ CUtensorMap map_vg, const __grid_constant__ CUtensorMap map_qt,
-                 const __grid_constant__ CUtensorMap map_vt, const __grid_constant__ CUtensorMap map_vtb,
-                 const int* __restrict__ vt_wide, const int32_t* __restrict__ bucket_qidx,
+                 const __grid_constant__ CUtensorMap map_vt, const int32_t* __restrict__ bucket_qidx,
                  const int* __restrict__ unit_count, const int4* __restrict__ unit_tab, int BH,
                  int N, int m, int topk, float cs_shared, int use_shared, bf16* __restrict__ out,
                  int* status) {
@@ -298,7 +257,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         prefetch_tmap(&map_vg);
         prefetch_tmap(&map_qt);
         prefetch_tmap(&map_vt);
-        prefetch_tmap(&map_vtb);
       }
       int gi = 0;
       int4 nxt = units > 0 ? unit_tab[ubase] : make_int4(0, 0, 0, 0);
@@ -307,8 +265,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         if (it + 1 < units) nxt = unit_tab[ubase + it + 1];
         const int idx = cur.x, bh = idx / m, qbase = cur.y, qcnt = cur.z;
         const int qb = it & 1;
-        // the head's shared chunks in fp16 or, outside fp16's range, in bf16
-        const CUtensorMap* mvt = (nsc > 0 && vt_wide[bh]) ? &map_vtb : &map_vt;
         // ---- query tile 0 of the unit (warp 3 gathers tile 1): lane l owns rows 4l .. 4l+3
         int rows[4];
 #pragma unroll
@@ -337,7 +293,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
               tma_load_3d(s.vb[st], &map_vg, &s.kv_full[st], 0, c * BN, idx);
             } else {
               tma_load_3d(s.kb[st], &map_qt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
-              tma_load_3d(s.vb[st], mvt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
+              tma_load_3d(s.vb[st], &map_vt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
             }
           }
           __syncwarp();
@@ -350,19 +306,12 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       // one elected lane issues each batch of MMAs and its commits
       const int slot = warp - 1;
       const uint32_t id_s = idesc_f16(128, BN, false);
-      const uint32_t id_pv_raw = idesc_f16(128, 64, true, false);
-      const uint32_t id_pv_sh = idesc_f16(128, 64, true, true);
+      const uint32_t id_pv = idesc_f16(128, 64, true);
       const uint32_t tS = tbase + slot * 256, tP = tS + 128, tO = tS + 192;
       bool ok = true;
-      // whether a unit's shared chunks hold bf16 v~: read when its first S is issued
-      // (wide_s), taken over by its first P . V (wide_pv).  S(g + 1) is issued before
-      // P . V(g), but a unit with shared chunks has at least two chunks, so the first
-      // P . V of a unit always sees its own unit's flag in wide_s.
-      int wide_s = 0, wide_pv = 0;
       // S(g) = Q_slot . B(g)^T
       auto issue_s = [&](int g) -> bool {
         const int it = g / nc, c = g % nc, qb = it & 1, st = g % kStages;
-        if (c == 0 && nsc > 0) wide_s = vt_wide[unit_tab[ubase + it].x / m];
         if (c == 0 && !mbar_wait_warp(&s.q_full[qb], (it >> 1) & 1)) return false;
         if (!mbar_wait_warp(&s.kv_full[st], (g / kStages) & 1)) return false;
         tc_fence_after();
@@ -387,8 +336,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         }
         if (!mbar_wait_warp(&s.p_full[slot], g & 1)) { ok = false; break; }
         tc_fence_after();
-        if (c == 0) wide_pv = wide_s;
-        const uint32_t id_pv = (c < nrc || wide_pv) ? id_pv_raw : id_pv_sh;
         const uint32_t vb = smem_u32(s.vb[st]);
         if (elect_one()) {
 #pragma unroll
@@ -449,23 +396,25 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
     };
     // O / l of the finished unit to its query's output row
     auto write_row = [&](int bh, int qi, float lsum) {
-      float o[64];
-      tmem_ld32(tO, o);
-      tmem_ld32(tO + 32, o + 32);
-      tmem_ld_wait();
-      tmem_fence_regs<64>(o);
-      if (ok && qi >= 0) {
-        const float inv = 1.f / lsum;
-        bf16* dst = out + ((size_t)bh * N + qi) * 64;
+      const float inv = 1.f / lsum;
+      bf16* dst = out + ((size_t)bh * N + (qi >= 0 ? qi : 0)) * 64;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {   // 32-byte stores
-          uint32_t w[8];
+      for (int half = 0; half < 2; ++half) {
+        float o[32];
+        tmem_ld32(tO + half * 32, o);
+        tmem_ld_wait();
+        tmem_fence_regs<32>(o);
+        if (ok && qi >= 0) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) w[e] = pack_pair(o[16 * i + 2 * e] * inv, o[16 * i + 2 * e + 1] * inv, false);
-          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * i),
-                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                       "r"(w[7])
-                       : "memory");
+          for (int i = 0; i < 2; ++i) {   // 32-byte stores
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = pack_bf16(o[16 * i + 2 * e] * inv, o[16 * i + 2 * e + 1] * inv);
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 32 * half + 16 * i),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                         "r"(w[7])
+                         : "memory");
+          }
         }
       }
     };
@@ -475,8 +424,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
     int4 cur = units > 0 ? unit_tab[ubase] : make_int4(0, 0, 0, 0);
     int4 nxt = units > 1 ? unit_tab[ubase + 1] : cur;
     int qi = units > 0 ? row_query(cur) : -1;
-    // the unit's shared chunks in bf16 instead of fp16 (v~ outside fp16's range)
-    int wide = (units > 0 && nsc > 0) ? vt_wide[cur.x / m] : 0;
     int it = 0, c = 0;
     int prev_bh = 0, prev_qi = -1;
     float prev_lsum = 1.f;
@@ -495,7 +442,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         cur = nxt;
         if (it + 1 < units) nxt = unit_tab[ubase + it + 1];
         qi = row_query(cur);
-        wide = nsc > 0 ? vt_wide[cur.x / m] : 0;
         mref = -INFINITY;
         lsum = 0.f;
       }
@@ -523,7 +469,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
 #pragma unroll
         for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
       const float tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      const bool fp16 = c >= nrc && !wide;         // shared chunk with v~ in fp16
       const float csc = c >= nrc ? cs_shared : cs;  // the chunk's logit scale, log2 units
       const float xm = tm * csc;
       const bool need = (c == 0) || (xm > mref + kLazy);
@@ -532,12 +477,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         lsum *= f;
         mref = xm;
       }
-      const float nm = -mref;
-      // P = 2^(s * cs - mref) in fp32 pairs, packed to the branch's type (the type is
-      // uniform per chunk, so each loop is specialised); row sum in two pair chains
-      const unsigned long long c2 = f2pack(csc, csc), nm2 = f2pack(nm, nm);
+      // P = 2^(s * csc - mref) in fp32 pairs, packed to bf16 pairs; the row sum in two
+      // pair chains (from the unrounded values)
+      const unsigned long long c2 = f2pack(csc, csc), nm2 = f2pack(-mref, -mref);
       unsigned long long lsa = f2pack(0.f, 0.f), lsb = lsa;
-      auto exp_half = [&](auto is_fp16, int base, uint32_t* pk) {
+      auto exp_half = [&](int base, uint32_t* pk) {
 #pragma unroll
         for (int i = 0; i < BN / 2; i += 2) {
           float x0, x1;
@@ -545,13 +489,12 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
           const float p0 = ex2(x0), p1 = ex2(x1);
           if ((i >> 1) & 1) lsb = add2(lsb, f2pack(p0, p1));
           else lsa = add2(lsa, f2pack(p0, p1));
-          pk[i / 2] = pack_pair(p0, p1, decltype(is_fp16)::value);
+          pk[i / 2] = pack_bf16(p0, p1);
         }
       };
       // first half of P while the previous P . V may still run
       uint32_t pk0[BN / 4];
-      if (fp16) exp_half(std::true_type{}, 0, pk0);
-      else exp_half(std::false_type{}, 0, pk0);
+      exp_half(0, pk0);
       // the previous P . V must have read P and finished with O
       if (g > 0 && ok && !mbar_wait(&s.pv_done[slot], (g - 1) & 1)) ok = false;
       tc_fence_after();
@@ -562,8 +505,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         pending = false;
       }
       uint32_t pk1[BN / 4];
-      if (fp16) exp_half(std::true_type{}, BN / 2, pk1);
-      else exp_half(std::false_type{}, BN / 2, pk1);
+      exp_half(BN / 2, pk1);
       tmem_st16(tP + 32, pk1);
       tmem_st16(tP + 48, pk1 + 16);
       float la0, la1, lb0, lb1;
@@ -607,7 +549,7 @@ bool expert_tc_supported(int d, int m, int topk) { return d == 64 && m >= 1 && t
 
 size_t expert_tc_ws_bytes(int BH, int N, int m, int topk) {
   auto r = [](size_t b) { return (b + 255) / 256 * 256; };
-  return 2 * r((size_t)BH * m * 64 * 2) + r((size_t)BH * 4) + r(((size_t)BH * m + 1) * 4) +
+  return r((size_t)BH * m * 64 * 2) + r(((size_t)BH * m + 1) * 4) +
          r(max_units(BH, N, m) * 16) + 2 * r((size_t)BH * m * topk * 128);
 }
 
@@ -628,19 +570,18 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
                              status);
   count_launch();
   if (e != cudaSuccess) return e;
-  CUtensorMap mqg, mkg, mvg, mqt, mvt, mvtb;
+  CUtensorMap mqg, mkg, mvg, mqt, mvt;
   if (!make_tmap_gather64(&mqg, q, (uint64_t)BH * N) ||
       !make_tmap_rows64(&mkg, w.kg, (uint64_t)topk, (uint64_t)BH * m, BN) ||
       !make_tmap_rows64(&mvg, w.vg, (uint64_t)topk, (uint64_t)BH * m, BN) ||
       !make_tmap_rows64(&mqt, q_tilde, (uint64_t)m, (uint64_t)BH, BN) ||
-      !make_tmap_rows64(&mvt, w.vt16, (uint64_t)m, (uint64_t)BH, BN, true) ||
-      !make_tmap_rows64(&mvtb, w.vtb, (uint64_t)m, (uint64_t)BH, BN))
+      !make_tmap_rows64(&mvt, w.vtb, (uint64_t)m, (uint64_t)BH, BN))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(ExpertSmem) + 1024;
   e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(expert_tc_kernel, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
-                 mqg, mkg, mvg, mqt, mvt, mvtb, static_cast<const int*>(w.vt_wide), bucket_qidx,
+                 mqg, mkg, mvg, mqt, mvt, bucket_qidx,
                  static_cast<const int*>(w.unit_start + (size_t)BH * m),
                  static_cast<const int4*>(w.unit), BH, N, m, topk, cs_shared, routed_only ? 0 : 1,
                  out, status);
@@ -704,10 +645,8 @@ cudaError_t launch_dense_tc(const bf16* q, const bf16* k, const bf16* v, int BH,
   const size_t smem = sizeof(ExpertSmem) + 1024;
   e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // no shared chunks: the v~ range flags are never read
   e = launch_pdl(expert_tc_kernel, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
-                 mqg, mkg, mvg, mqt, mvt, mvt, static_cast<const int*>(nullptr),
-                 static_cast<const int32_t*>(qidx),
+                 mqg, mkg, mvg, mqt, mvt, static_cast<const int32_t*>(qidx),
                  static_cast<const int*>(ucount), static_cast<const int4*>(unit), BH, N, 1, N,
                  0.18033688011112042f, 0, out, status);
   count_launch();

@@ -368,11 +368,11 @@ def test_bad_expert_index_is_flagged_not_dereferenced():
 
 @pytest.mark.parametrize("scale_log2", [17, -20], ids=["values_1e5", "values_1e-6"])
 def test_values_outside_fp16_range(scale_log2):
-    """The expert kernel keeps v~ in fp16 for its shared chunks (three more mantissa bits
-    than bf16) only for a head whose largest |v~| fits fp16's normal range; a head whose
-    values are far larger (|V| ~ 1e5, beyond fp16's 65504) or far smaller takes bf16.
-    Head 0's V is scaled by a power of two (exact in bf16), head 1's is not; each head
-    must meet the bf16 tolerance at its own scale, with no overflow."""
+    """Values far beyond fp16's range (|V| ~ 1e5, above 65504) or far below its normal
+    range: the shared values v~ and the softmax weights stay in bf16 (fp32's exponent
+    range) on the tensor cores, so nothing overflows or flushes.  Head 0's V is scaled by
+    a power of two (exact in bf16), head 1's is not; each head must meet the bf16
+    tolerance at its own scale."""
     mita = M()
     w = W.custom("scaled_v", 1, 2, 8192, 64, "bf16", 1, 8192, 32, 64, index=410)
     q, k, v = W.make_qkv(w, 0)
