@@ -274,6 +274,12 @@ template <typename T>
 bool route_uses_tc(int d, int m, int s, const float* lse, const float* so) {
   return std::is_same<T, bf16>::value && s == 1 && !lse && !so && route_tc_supported(d, m);
 }
+// s = 1 with the shared branch's partial requested (both outputs): the tensor-core kernel
+// that reuses the routing logits as the shared logits
+template <typename T>
+bool route_shared_uses_tc(int d, int m, int s, const float* lse, const float* so) {
+  return std::is_same<T, bf16>::value && s == 1 && lse && so && route_shared_tc_supported(d, m);
+}
 
 template <typename T>
 cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int N, int d, int m,
@@ -285,6 +291,11 @@ cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int
       if (counted) *counted = hist != nullptr;
       return launch_route_tc(q, qt, BH, N, m, ds->num_sms, route, static_cast<int*>(ws),
                              ds->status, hist, st, prezeroed);
+    }
+    if (route_shared_uses_tc<T>(d, m, s, lse, so)) {
+      if (counted) *counted = hist != nullptr;
+      return launch_route_shared_tc(q, qt, vt, BH, N, m, ds->num_sms, 0, 0, route, lse, so,
+                                    static_cast<int*>(ws), ds->status, hist, st, prezeroed);
     }
   }
   return launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st);
@@ -303,7 +314,8 @@ int route_impl(const T* q, const T* qt, const float* vt, int B, int H, int N, in
   DevState* ds = nullptr;
   MITA_TRY(device_state(&ds));
   void* ws = nullptr;
-  if (route_uses_tc<T>(d, m, s, lse, so)) MITA_TRY(workspace(route_ws_bytes(B * H, N), st, &ws));
+  if (route_uses_tc<T>(d, m, s, lse, so) || route_shared_uses_tc<T>(d, m, s, lse, so))
+    MITA_TRY(workspace(route_ws_bytes(B * H, N), st, &ws));
   MITA_CUDA(route_dispatch<T>(q, qt, vt, B * H, N, d, m, s, route, lse, so, ds, ws, st),
             "route launch");
   return MITA_OK;
@@ -367,11 +379,12 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
     return MITA_OK;
   }
   if constexpr (std::is_same<T, bf16>::value) {
-    if (so == nullptr && expert_tc_supported(d, m, topk)) {
+    if (expert_tc_supported(d, m, topk)) {
+      // with a carried shared partial the kernel attends over the raw pairs only and merges
       void* ws = nullptr;
       MITA_TRY(workspace(expert_tc_ws_bytes(B * H, N, m, topk), st, &ws));
       MITA_CUDA(launch_expert_tc(q, k, v, qt, vt, ti, off, qidx, B * H, N, m, topk, ds->num_sms,
-                                 ws, out, ds->status, st),
+                                 ws, out, ds->status, st, 0, 0, lse, so, 0),
                 "expert launch");
       return MITA_OK;
     }
@@ -483,6 +496,9 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
               "expert launch");
     return MITA_OK;
   }
+  // s = 1: the expert kernel recomputes the shared logits q . q~ on the tensor cores rather
+  // than taking them from the route stage as a carried partial (measured: the carried split,
+  // route_shared_tc + raw-pairs-only expert, is slower at both long workloads)
   // the tensor-core route also counts the bucket stage's (expert, chunk) histogram
   bool counted = false;
   MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, 1, route, nullptr, nullptr, ds, ws + L.rt,

@@ -120,8 +120,9 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
                      const int32_t* __restrict__ bucket_off, const float* __restrict__ v_tilde,
                      int BH, ExpertTcWs w, int* status) {
   griddep_wait();
-  // v~ in bf16, four values per thread step
-  {
+  // v~ in bf16, four values per thread step (not needed, and possibly absent, when the
+  // kernel runs no shared chunks)
+  if (v_tilde != nullptr) {
     const long long n4 = (long long)BH * m * 16;
     for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n4;
          t += (long long)gridDim.x * blockDim.x) {
@@ -194,13 +195,15 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
 }
 
 // -------------------------------------------------------------------------------------------
+template <bool kCarried>
 __global__ void __launch_bounds__(kThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_constant__ CUtensorMap map_kg,
                  const __grid_constant__ CUtensorMap map_vg, const __grid_constant__ CUtensorMap map_qt,
                  const __grid_constant__ CUtensorMap map_vt, const int32_t* __restrict__ bucket_qidx,
                  const int* __restrict__ unit_count, const int4* __restrict__ unit_tab, int BH,
-                 int N, int m, int topk, float cs_shared, int use_shared, bf16* __restrict__ out,
-                 int* status) {
+                 int N, int m, int topk, float cs_shared, int use_shared,
+                 const float* __restrict__ sh_lse, const void* __restrict__ sh_o, int o_bf16,
+                 bf16* __restrict__ out, int* status) {
   griddep_wait();
   extern __shared__ unsigned char smem_raw[];
   ExpertSmem& s = *reinterpret_cast<ExpertSmem*>(
@@ -395,26 +398,67 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       return (qi >= 0 && qi < N) ? qi : -1;
     };
     // O / l of the finished unit to its query's output row
-    auto write_row = [&](int bh, int qi, float lsum) {
-      const float inv = 1.f / lsum;
-      bf16* dst = out + ((size_t)bh * N + (qi >= 0 ? qi : 0)) * 64;
+    // With a carried shared partial (sh_lse, sh_o: the route stage's log-sum-exp and
+    // normalised output of the m shared pairs) this unit attended over the raw pairs only,
+    // and the two partials merge here: tutorial ch. 4, (Z1 o1 + Z2 o2) / (Z1 + Z2).
+    constexpr bool carried = kCarried;
+    auto write_row = [&](int bh, int qi, float lsum, float mr, float l1) {
+      const bool wr = ok && qi >= 0;
+      const size_t rowi = (size_t)bh * N + (wr ? qi : 0);
+      float w1 = 0.f, w2 = 1.f / lsum;
+      if (carried) {
+        const float L1 = l1 * 1.4426950408889634f, L2 = mr + log2f(lsum);   // log2 units
+        const float M = fmaxf(L1, L2);
+        const float a1 = ex2(L1 - M), a2 = ex2(L2 - M);
+        const float inv = 1.f / (a1 + a2);
+        w1 = a1 * inv;
+        w2 = a2 * inv / lsum;
+      }
+      bf16* dst = out + rowi * 64;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float o[32];
-        tmem_ld32(tO + half * 32, o);
+        tmem_ld32(tO + half * 32, o);   // warp-collective: every lane takes part
         tmem_ld_wait();
         tmem_fence_regs<32>(o);
-        if (ok && qi >= 0) {
+        if (!wr) continue;
+        if (carried) {
+          float o1[32];
+          if (o_bf16) {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const bf16*>(sh_o) + rowi * 64 + half * 32);
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {   // 32-byte stores
-            uint32_t w[8];
+            for (int i = 0; i < 4; ++i) {
+              const uint4 x = src[i];
+              const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = pack_bf16(o[16 * i + 2 * e] * inv, o[16 * i + 2 * e + 1] * inv);
-            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 32 * half + 16 * i),
-                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                         "r"(w[7])
-                         : "memory");
+              for (int e = 0; e < 4; ++e) {
+                o1[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
+                o1[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+              }
+            }
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(sh_o) + rowi * 64 + half * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = src[i];
+              o1[4 * i] = x.x; o1[4 * i + 1] = x.y; o1[4 * i + 2] = x.z; o1[4 * i + 3] = x.w;
+            }
           }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = fmaf(w1, o1[i], w2 * o[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= w2;
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {   // 32-byte stores
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[e] = pack_bf16(o[16 * i + 2 * e], o[16 * i + 2 * e + 1]);
+          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 32 * half + 16 * i),
+                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                       "r"(w[7])
+                       : "memory");
         }
       }
     };
@@ -424,9 +468,22 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
     int4 cur = units > 0 ? unit_tab[ubase] : make_int4(0, 0, 0, 0);
     int4 nxt = units > 1 ? unit_tab[ubase + 1] : cur;
     int qi = units > 0 ? row_query(cur) : -1;
+    // the carried shared log-sum-exp of this thread's query in the current unit
+    // (and the carried output row is prefetched into L2 now: it is read only when the unit
+    // is written out, a unit of chunks later)
+    auto row_lse = [&](const int4& u, int q) -> float {
+      if (!(carried && q >= 0)) return 0.f;
+      const size_t r = (size_t)(u.x / m) * N + q;
+      const char* p = o_bf16 ? reinterpret_cast<const char*>(static_cast<const bf16*>(sh_o) + r * 64)
+                             : reinterpret_cast<const char*>(static_cast<const float*>(sh_o) + r * 64);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+      if (!o_bf16) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128));
+      return sh_lse[r];
+    };
+    float l1 = units > 0 ? row_lse(cur, qi) : 0.f;
     int it = 0, c = 0;
     int prev_bh = 0, prev_qi = -1;
-    float prev_lsum = 1.f;
+    float prev_lsum = 1.f, prev_mref = 0.f, prev_l1 = 0.f;
     bool pending = false;          // a finished unit's O still waits in tensor memory
     float mref = -INFINITY, lsum = 0.f;
     for (int g = 0; g < G; ++g, ++c) {
@@ -436,12 +493,15 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         prev_bh = cur.x / m;
         prev_qi = qi;
         prev_lsum = lsum;
+        prev_mref = mref;
+        prev_l1 = l1;
         pending = true;
         ++it;
         c = 0;
         cur = nxt;
         if (it + 1 < units) nxt = unit_tab[ubase + it + 1];
         qi = row_query(cur);
+        l1 = row_lse(cur, qi);
         mref = -INFINITY;
         lsum = 0.f;
       }
@@ -501,7 +561,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       tmem_st16(tP, pk0);
       tmem_st16(tP + 16, pk0 + 16);
       if (pending) {
-        write_row(prev_bh, prev_qi, prev_lsum);
+        write_row(prev_bh, prev_qi, prev_lsum, prev_mref, prev_l1);
         pending = false;
       }
       uint32_t pk1[BN / 4];
@@ -532,7 +592,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
     if (G > 0) {
       if (ok && !mbar_wait(&s.pv_done[slot], (G - 1) & 1)) ok = false;
       tc_fence_after();
-      write_row(cur.x / m, qi, lsum);
+      write_row(cur.x / m, qi, lsum, mref, l1);
     }
     tc_fence_before();
     if (!ok) flag_error(status, kDevErrTimeout);
@@ -557,7 +617,8 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
                              const float* v_tilde, const int32_t* topk_idx,
                              const int32_t* bucket_off, const int32_t* bucket_qidx, int BH, int N,
                              int m, int topk, int num_sms, void* ws, bf16* out, int* status,
-                             cudaStream_t st, int shared_temp, int routed_only) {
+                             cudaStream_t st, int shared_temp, int routed_only,
+                             const float* shared_lse, const void* shared_o, int o_bf16) {
   const ExpertTcWs w = carve(ws, BH, N, m, topk);
   // log2(e) / sqrt(64), or log2(e) / 64 for the shared logits at the official code's temperature
   const float cs_shared = shared_temp ? 0.022542110013890052f : 0.18033688011112042f;
@@ -565,8 +626,12 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   const long long gblocks = std::min<long long>((rows + kGatherThreads / 8 - 1) / (kGatherThreads / 8),
                                                 (long long)std::max(num_sms, 1) * 8);
   // gblocks gathering CTAs plus the one that builds the unit table
+  // shared chunks run in the kernel unless the routing-only ablation drops the branch or the
+  // route stage carried its partial
+  const bool shared_chunks = !(routed_only || shared_lse);
   cudaError_t e = launch_pdl(expert_gather_kernel, dim3((unsigned)gblocks + 1), dim3(kGatherThreads),
-                             0, st, k, v, topk_idx, rows, N, m, topk, bucket_off, v_tilde, BH, w,
+                             0, st, k, v, topk_idx, rows, N, m, topk, bucket_off,
+                             shared_chunks ? v_tilde : static_cast<const float*>(nullptr), BH, w,
                              status);
   count_launch();
   if (e != cudaSuccess) return e;
@@ -574,17 +639,23 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   if (!make_tmap_gather64(&mqg, q, (uint64_t)BH * N) ||
       !make_tmap_rows64(&mkg, w.kg, (uint64_t)topk, (uint64_t)BH * m, BN) ||
       !make_tmap_rows64(&mvg, w.vg, (uint64_t)topk, (uint64_t)BH * m, BN) ||
-      !make_tmap_rows64(&mqt, q_tilde, (uint64_t)m, (uint64_t)BH, BN) ||
-      !make_tmap_rows64(&mvt, w.vtb, (uint64_t)m, (uint64_t)BH, BN))
+      // (without shared chunks these two maps are never loaded: any valid map will do)
+      !make_tmap_rows64(&mqt, shared_chunks ? static_cast<const void*>(q_tilde) : w.kg,
+                        (uint64_t)(shared_chunks ? m : topk), (uint64_t)(shared_chunks ? BH : BH * m), BN) ||
+      !make_tmap_rows64(&mvt, shared_chunks ? static_cast<const void*>(w.vtb) : w.vg,
+                        (uint64_t)(shared_chunks ? m : topk), (uint64_t)(shared_chunks ? BH : BH * m), BN))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(ExpertSmem) + 1024;
-  e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(expert_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(expert_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(expert_tc_kernel, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
+  e = launch_pdl(shared_lse ? expert_tc_kernel<true> : expert_tc_kernel<false>,
+                 dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
                  mqg, mkg, mvg, mqt, mvt, bucket_qidx,
                  static_cast<const int*>(w.unit_start + (size_t)BH * m),
-                 static_cast<const int4*>(w.unit), BH, N, m, topk, cs_shared, routed_only ? 0 : 1,
-                 out, status);
+                 static_cast<const int4*>(w.unit), BH, N, m, topk, cs_shared, shared_chunks ? 1 : 0,
+                 shared_lse, shared_o, o_bf16, out, status);
   count_launch();
   return e;
 }
@@ -643,12 +714,15 @@ cudaError_t launch_dense_tc(const bf16* q, const bf16* k, const bf16* v, int BH,
       !make_tmap_rows64(&mvt, v, (uint64_t)N, (uint64_t)BH, BN))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(ExpertSmem) + 1024;
-  e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(expert_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(expert_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(expert_tc_kernel, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
+  e = launch_pdl(expert_tc_kernel<false>, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
                  mqg, mkg, mvg, mqt, mvt, static_cast<const int32_t*>(qidx),
                  static_cast<const int*>(ucount), static_cast<const int4*>(unit), BH, N, 1, N,
-                 0.18033688011112042f, 0, out, status);
+                 0.18033688011112042f, 0, static_cast<const float*>(nullptr),
+                 static_cast<const void*>(nullptr), 0, out, status);
   count_launch();
   return e;
 }

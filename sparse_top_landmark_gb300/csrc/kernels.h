@@ -134,6 +134,22 @@ cudaError_t launch_route_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde
                             int m, int num_sms, int32_t* route, int* amb, int* status, int* hist,
                             cudaStream_t st, bool prezeroed = false);   // amb counts, hist cleared
 
+// exact re-routing of the queries route_tc / route_shared_tc left on the heads'
+// ambiguous lists in `amb` (counted into `hist` under their exact route, if not null)
+cudaError_t launch_route_fixup(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH,
+                               int N, int m, int num_sms, int32_t* route, const int* amb,
+                               int* hist, cudaStream_t st);
+// Routing (s = 1) together with the shared branch's partial from the same logits: per
+// query the route, shared_lse (natural log-sum-exp of the scaled shared logits) and
+// shared_o = the normalised shared output, [BH*N][64] in bf16 (o_bf16 = 1) or fp32.
+// `amb` and `hist` as for launch_route_tc (the fix-up runs inside).
+bool route_shared_tc_supported(int d, int m);
+cudaError_t launch_route_shared_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde,
+                                   const float* v_tilde, int BH, int N, int m, int num_sms,
+                                   int shared_temp, int o_bf16, int32_t* route,
+                                   float* shared_lse, void* shared_o, int* amb, int* status,
+                                   int* hist, cudaStream_t st, bool prezeroed = false);
+
 bool expert_tc_supported(int d, int m, int topk);
 size_t expert_tc_ws_bytes(int BH, int N, int m, int topk);
 cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
@@ -142,7 +158,8 @@ cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                              const int32_t* bucket_off, const int32_t* bucket_qidx, int BH, int N,
                              int m, int topk, int num_sms, void* ws, __nv_bfloat16* out,
                              int* status, cudaStream_t st, int shared_temp = 0,
-                             int routed_only = 0);
+                             int routed_only = 0, const float* shared_lse = nullptr,
+                             const void* shared_o = nullptr, int o_bf16 = 0);
 // dense softmax attention of every query over all N keys of its head (bf16, d = 64)
 size_t dense_tc_ws_bytes(int BH, int N);
 cudaError_t launch_dense_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,

@@ -499,6 +499,13 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
                  m, W, nch, G_h, cols, route, amb, status, hist);
   count_launch();
   if (e != cudaSuccess) return e;
+  return launch_route_fixup(q, q_tilde, BH, N, m, num_sms, route, amb, hist, st);
+}
+
+cudaError_t launch_route_fixup(const bf16* q, const bf16* q_tilde, int BH, int N, int m,
+                               int num_sms, int32_t* route, const int* amb, int* hist,
+                               cudaStream_t st) {
+  cudaError_t e;
   const int per_head = std::max(1, std::max(num_sms, 1) / BH);
   const size_t fsm = (size_t)m * kFixRow * 2;
   e = cudaFuncSetAttribute(route_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm);

@@ -386,3 +386,31 @@ def test_values_outside_fp16_range(scale_log2):
     assert bool(torch.isfinite(out.float()).all())
     assert_close(out[:, 0], res["out"][:, 0], torch.bfloat16, "scaled head", scale=scale)
     assert_close(out[:, 1], res["out"][:, 1], torch.bfloat16, "unscaled head")
+
+
+@pytest.mark.parametrize("name", ["vit_s_14x14", "seg_32x32", "long_64k"])
+def test_route_with_shared_partial(name):
+    """mita_route with both shared outputs requested: the tensor-core kernel reuses the
+    routing logits q . q~_i as the shared logits (tutorial ch. 6: one dot product for both)
+    and emits each query's route, the natural log-sum-exp of the scaled shared logits and
+    the normalised shared output.  Routes are exact; lse and o are compared with fp64
+    values formed from the oracle's q~ and v~ (o to the bf16 tolerance: P and v~ enter the
+    tensor cores in bf16)."""
+    mita = M()
+    w, q, k, v = inputs(name)
+    qt = oracle_pool(name)
+    _, ovt, _ = oracle_landmark(name)
+    r, lse, so = mita.mita_route(dev(q), dev(qt.to(w.torch_dtype)), dev(ovt.float()), shared=True)
+    assert mita.get_last_device_error() == 0
+    sel = sample_queries(w, 4096) if name == "long_64k" else torch.arange(w.B * w.H * w.N)
+    orr, gap = oracle.route(q, qt, 1, queries=sel)
+    assert_routes_match(r.view(-1, 1).cpu()[sel], orr, gap, q, qt, rows=sel)
+    qd = q.reshape(-1, w.d)[sel].double()
+    lt = qt.reshape(w.B * w.H, w.m, w.d)[sel // w.N]
+    vt = ovt.reshape(w.B * w.H, w.m, w.d)[sel // w.N]
+    logits = torch.einsum("rd,rmd->rm", qd, lt) / w.d ** 0.5
+    ref_lse = torch.logsumexp(logits, -1)
+    ref_o = torch.einsum("rm,rmd->rd", torch.softmax(logits, -1), vt)
+    got_lse = lse.view(-1).cpu()[sel].double()
+    assert (got_lse - ref_lse).abs().max().item() <= 1e-4 * max(1.0, ref_lse.abs().max().item())
+    assert_close(so.view(-1, w.d).cpu()[sel], ref_o, torch.bfloat16, "shared o")

@@ -63,9 +63,15 @@ def test_route_top_s(name):
     # the s chosen landmarks are distinct
     rs = r.cpu().sort(-1).values
     assert bool((rs[..., 1:] != rs[..., :-1]).all())
-    # the shared partial does not depend on s
+    # the shared partial does not depend on s: bit for bit where s = 1 also runs the SIMT
+    # route kernel; bf16 with d = 64 routes s = 1 on the tensor cores (P and v~ in bf16), so
+    # there the two agree to the bf16 output tolerance
     _, lse1, so1 = mita.mita_route(dq, dqt, dvt, s=1, shared=True)
-    assert torch.equal(lse.cpu(), lse1.cpu()) and torch.equal(so.cpu(), so1.cpu())
+    if w.dtype == "bf16" and w.d == 64:
+        assert (lse.cpu() - lse1.cpu()).abs().max().item() <= 1e-4 * max(1.0, lse.abs().max().item())
+        assert_close(so1.cpu(), so.cpu().double(), torch.bfloat16, "shared o, s = 1 vs s")
+    else:
+        assert torch.equal(lse.cpu(), lse1.cpu()) and torch.equal(so.cpu(), so1.cpu())
     assert mita.get_last_device_error() == 0
 
 
