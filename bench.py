@@ -152,6 +152,80 @@ class ClockSampler:
                 "samples": len(inside), "window_ms": round((t1 - t0) * 1e3, 1)}
 
 
+class NvmlClockSampler(ClockSampler):
+    """The same summary from NVML read in-process (every ~2 ms, so even a window of a few
+    tens of milliseconds holds many samples).  Reads only: SM clock, its maximum and the
+    clock-event reason bits.  start() returns False when NVML cannot be loaded."""
+    # clock-event reason bits (nvml.h): sw power cap, hw slowdown, sw thermal, hw thermal
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, gpu_index, period_s=0.002):
+        super().__init__(gpu_index)
+        self.period = period_s
+        self.samples = []          # (time, sm_mhz, max_mhz, reason bits)
+        self._stop = False
+
+    def start(self):
+        import ctypes
+        import threading
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                return False
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError):
+            return False
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+
+        def read():
+            lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))        # 1 = SM clock
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            reasons_fn(h, ctypes.byref(rs))
+            return (time.time(), float(clk.value), float(mx.value), int(rs.value))
+
+        def loop():
+            while not self._stop:
+                self.samples.append(read())
+                time.sleep(self.period)
+        read()
+        self._t = threading.Thread(target=loop, daemon=True)
+        self._t.start()
+        return True
+
+    def stop(self):
+        self._stop = True
+        if getattr(self, "_t", None) is not None:
+            self._t.join(timeout=5)
+
+    def summary(self, t0, t1):
+        self.lines = []
+        for ts, sm, mx, bits in self.samples:
+            stamp = __import__("datetime").datetime.fromtimestamp(ts).strftime("%Y/%m/%d %H:%M:%S.%f")
+            flags = ["Active" if bits & self.BITS[n] else "Not Active"
+                     for n in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                               "sw_power_cap")]
+            self.lines.append(", ".join([stamp, str(self.gpu), str(sm), str(mx), "0", hex(bits)]
+                                        + flags))
+        out = ClockSampler.summary(self, t0, t1)
+        out["source"] = "nvml"
+        return out
+
+
+def clock_sampler(gpu_index):
+    """NVML in-process sampling when available, else nvidia-smi."""
+    s = NvmlClockSampler(gpu_index)
+    if s.start():
+        return s
+    s = ClockSampler(gpu_index)
+    s.start()
+    return s
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing on a bounded sample (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
@@ -276,17 +350,22 @@ def run_reference(args):
         return 0
     w = workload_of(args.workload, args.s)
     q, k, v = W.make_qkv(w, 0)
-    per = []
+    per, spent_s = [], []
     budget = max(2.0, min(15.0, 150.0 / (args.warmup + args.steps)))
     for i in range(args.warmup + args.steps):
         est, desc, threads, spent = oracle_sample_time(w, q, k, v, budget=budget, seed=i)
         if i >= args.warmup:
             per.append(est)
+            spent_s.append(spent)
     est = statistics.median(per)
     value = w.queries / est
+    # one step is one bounded sample: ms_per_step is its measured wall time; the value is the
+    # sample's rate (its time scaled to the whole workload gives workload_ms_estimate)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": statistics.median(spent_s) * 1e3,
+            "ms_per_step_kind": "measured wall time of one bounded oracle sample",
+            "workload_ms_estimate": est * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, 1),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -341,33 +420,44 @@ def stage_times(mita, w, dq, dk, dv, reps, stream):
     return res
 
 
-def bench_workload(mita, w, args, dev, stream, n_gpus, do_e2e=True):
+def bench_workload(mita, w, args, dev, stream, n_gpus, do_e2e=True, min_window_s=0.0,
+                   stages=True):
+    """Times `args.steps` forwards, or more when `min_window_s` asks for a longer window (the
+    secondary workloads: their forwards are short, and the clock samples must fall inside)."""
     q, k, v = W.make_qkv(w, 0)
     dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
     out = torch.empty_like(dq)
     # clocks: sampling runs from before the warm-up, the timed window is cut out below
-    sampler = ClockSampler(smi_index(dev.index))
-    sampler.start()
+    sampler = clock_sampler(smi_index(dev.index))
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             mita.mita_forward(dq, dk, dv, w.grid_h, w.grid_w, w.m, w.topk, w.s, out=out,
                               stream=stream)
     torch.cuda.synchronize(dev)
+    steps = args.steps
+    if min_window_s > 0:
+        probe = time_forward(mita, w, dq, dk, dv, out, 3, stream) / 3
+        steps = max(steps, int(min_window_s / max(probe, 1e-6)) + 1)
+        if n_gpus > 1:   # every rank times the same number of steps
+            t = torch.tensor([steps], dtype=torch.int64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            steps = int(t.item())
     if n_gpus > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.time()
-    secs = time_forward(mita, w, dq, dk, dv, out, args.steps, stream)
+    secs = time_forward(mita, w, dq, dk, dv, out, steps, stream)
     t1 = time.time()
     sampler.stop()
     torch.cuda.synchronize(dev)
     secs = max_over_ranks(secs, dev, n_gpus)
     if n_gpus > 1:
         torch.distributed.barrier()
-    res = {"secs": secs, "clocks": sampler.summary(t0, t1)}
-    res["value"] = replica_throughput(w.queries, args.steps, secs, n_gpus)
-    res["ms_per_step"] = secs / args.steps * 1e3
-    res["stages"] = stage_times(mita, w, dq, dk, dv, max(3, min(args.steps, 10)), stream)
+    res = {"secs": secs, "clocks": sampler.summary(t0, t1), "steps": steps}
+    res["value"] = replica_throughput(w.queries, steps, secs, n_gpus)
+    res["ms_per_step"] = secs / steps * 1e3
+    if stages:
+        res["stages"] = stage_times(mita, w, dq, dk, dv, max(3, min(args.steps, 10)), stream)
     res["launches"] = count_launches(mita, w, dq, dk, dv, out, stream)
     if do_e2e:
         hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
@@ -534,6 +624,8 @@ def main():
     ap.add_argument("--workload", default="long_1m", choices=list(W.WORKLOADS))
     ap.add_argument("--secondary", default="long_64k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-images", dest="images", action="store_false",
+                    help="skip the image-grid workloads' lines")
     ap.add_argument("--backward", action="store_true",
                     help="time mita_backward on --workload next to the forward")
     ap.add_argument("--fig5", action="store_true",
@@ -575,10 +667,25 @@ def main():
     sec = None
     if args.secondary and args.secondary not in ("none", args.workload):
         w2 = workload_of(args.secondary, args.s)
-        r2 = bench_workload(mita, w2, args, dev, stream, n_gpus, do_e2e=False)
+        r2 = bench_workload(mita, w2, args, dev, stream, n_gpus, do_e2e=False, min_window_s=1.0)
         roof2, per2 = roofline_entry(w2, r2["stages"], pk)
+        total2 = sum(roofline_s(*wk, pk) for wk in stage_work(w2).values())
         sec = {"workload": w2.name, "value": r2["value"], "ms_per_step": r2["ms_per_step"],
+               "steps": r2["steps"], "forward_roofline_frac": total2 / (r2["ms_per_step"] / 1e3),
                "roofline": roof2, "stages": per2, "clocks": r2["clocks"]}
+    # the image-grid workloads (ViT-S 14x14 tokens, segmentation 32x32): whole forwards only,
+    # each over a window of about a second
+    images = []
+    if args.images and args.s in (None, 1):
+        for nm in ("vit_s_14x14", "seg_32x32"):
+            wi = workload_of(nm, None)
+            ri = bench_workload(mita, wi, args, dev, stream, n_gpus, do_e2e=False,
+                                min_window_s=1.0, stages=False)
+            tot = sum(roofline_s(*wk, pk) for wk in stage_work(wi).values())
+            images.append({"workload": wi.name, "value": ri["value"], "unit": UNIT,
+                           "ms_per_step": ri["ms_per_step"], "steps": ri["steps"],
+                           "forward_roofline_frac": tot / (ri["ms_per_step"] / 1e3),
+                           "roofline_ms": tot * 1e3, "clocks": ri["clocks"]})
 
     cpu = None
     if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
@@ -604,6 +711,7 @@ def main():
             "stages": per_stage,
             "cpu_baseline": cpu,
             "secondary": sec,
+            "image_workloads": images,
         }
         print(json.dumps(line))
     if ws > 1:

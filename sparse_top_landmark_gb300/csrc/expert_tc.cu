@@ -165,15 +165,29 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
   const int piece = threadIdx.x & 7;
   const long long lane_row = (long long)blockIdx.x * (kGatherThreads / 8) + (threadIdx.x >> 3);
   const long long stride = (long long)(gridDim.x - 1) * (kGatherThreads / 8);
+  // the key indices of the next step are loaded while this step's rows are in flight
+  int jn[UNR];
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) {
+    const long long r = lane_row + u * stride;
+    jn[u] = r < rows ? topk_idx[r] : 0;
+  }
   for (long long r0 = lane_row; r0 < rows; r0 += stride * UNR) {
     uint4 kr[UNR], vr[UNR];
+    int jc[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      jc[u] = jn[u];
+      const long long rn = r0 + stride * UNR + u * stride;
+      jn[u] = rn < rows ? topk_idx[rn] : 0;
+    }
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const long long r = r0 + u * stride;
       kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
       if (r < rows) {
         const long long bh = r / ((long long)m * topk);
-        const int j = topk_idx[r];
+        const int j = jc[u];
         if (j >= 0 && j < N) {
           const size_t src = ((size_t)bh * N + j) * 64 + piece * 8;
           kr[u] = *reinterpret_cast<const uint4*>(k + src);

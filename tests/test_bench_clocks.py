@@ -35,3 +35,18 @@ def test_a_window_shorter_than_the_period_takes_the_nearest_sample():
     s.lines = [_line(t0 - 0.5, 1500), _line(t0 + 0.03, 2070)]
     c = s.summary(t0, t0 + 0.01)
     assert c["samples"] == 0 and c["sm_mhz"] == 2070
+
+
+def test_nvml_samples_are_summarised_like_smi_lines():
+    """In-process NVML samples (time, SM MHz, max MHz, reason bits): the same window cut and
+    reason names; the power-cap bit alone is reported, not rejected."""
+    s = bench.NvmlClockSampler(0)
+    t0 = 1_700_000_000.0
+    s.samples = [(t0 - 0.5, 1200.0, 2070.0, 0), (t0 + 0.002, 2070.0, 2070.0, 0),
+                 (t0 + 0.004, 2040.0, 2070.0, 0x4), (t0 + 0.006, 2070.0, 2070.0, 0),
+                 (t0 + 1.0, 900.0, 2070.0, 0x40)]
+    c = s.summary(t0, t0 + 0.008)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2070 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"] and c["source"] == "nvml"
+    c2 = s.summary(t0 + 0.9, t0 + 1.1)
+    assert c2["reasons"] == ["hw_thermal_slowdown"]
