@@ -37,7 +37,8 @@ struct LandmarkWs {
   int* ci;         // [BH, m, S, Tcap] candidate key indices
   int* cn;         // [BH, m, S]       candidates kept
   float* theta;    // [BH, m, S]       worst kept score if the split dropped keys, else -inf
-  float* kmax2;    // [BH, S]          max squared key norm per split
+  float* kmax2;    // [BH, S(, nrt)]   max squared key norm per split (tensor-core path: a
+                   // partial maximum per 128-landmark block of the split)
   int* nslow;      // [1]              rows routed to the exact fallback
   int* slow_rows;  // [BH * m]
   double* exact;   // [kExactCtas, N]  fp64 score scratch of the fallback

@@ -664,7 +664,7 @@ size_t landmark_ws_bytes(const LandmarkPlan& p, int BH, int N, int d, int m) {
   auto add = [&](size_t n) { b += (n + 255) / 256 * 256; };
   add(parts * 4); add(parts * 4); add(parts * d * 4);
   if (!p.tc) { add(parts * p.Tcap * 4); add(parts * p.Tcap * 4); add(parts * 4); add(parts * 4); }
-  add((size_t)BH * p.S * 4);
+  add((size_t)BH * p.S * std::max(1, p.nrt) * 4);
   add(4); add(rows * 4);
   add((size_t)kExactCtas * N * 8);
   if (p.tc) {
@@ -690,7 +690,7 @@ LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, i
     w.cn = (int*)take(parts * 4);
     w.theta = (float*)take(parts * 4);
   }
-  w.kmax2 = (float*)take((size_t)BH * p.S * 4);
+  w.kmax2 = (float*)take((size_t)BH * p.S * std::max(1, p.nrt) * 4);
   w.nslow = (int*)take(4);
   w.slow_rows = (int*)take(rows * 4);
   w.exact = (double*)take((size_t)kExactCtas * N * 8);

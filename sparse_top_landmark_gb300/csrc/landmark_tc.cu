@@ -211,7 +211,10 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
     } else {
       // V producer (tile j into the V ring as soon as its slot is free), and the
       // largest |k| element of the split (bounds every key norm by 8 max|k|);
-      // zero-filled rows past N are harmless
+      // zero-filled rows past N are harmless.  The nrt CTAs of a key split (one per
+      // 128-landmark block) share that maximum: each reads every nrt-th K tile (the
+      // reads compete with the MMAs for shared-memory bandwidth), and the threshold
+      // pass takes the maximum of their nrt partial maxima.
       uint32_t mx = 0u;
       bool ok = true;
       int vj = 0;                       // next V tile to request
@@ -230,7 +233,7 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       for (int j = 0; j < ntl; ++j) {
         const int st = j % kKRing;
         if (ok && !mbar_wait(&s.k_full[st], (j / kKRing) & 1)) ok = false;
-        if (ok) {
+        if (ok && j % nrt == rt) {
           const uint4* src = reinterpret_cast<const uint4*>(s.k[st]);
 #pragma unroll 8
           for (int i = lane; i < 1024; i += 32) {
@@ -383,7 +386,7 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (threadIdx.x == 0 && rt == 0) ws.kmax2[(size_t)bh * S + sp] = s.nred;
+  if (threadIdx.x == 0) ws.kmax2[((size_t)bh * S + sp) * nrt + rt] = s.nred;
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
@@ -782,8 +785,9 @@ cudaError_t launch_landmark_tc_passes(const bf16* q_tilde, const bf16* k, const 
                  p.split_len, ws, status);
   count_launch();
   if (e != cudaSuccess) return e;
+  // (kmax2 holds nrt partial maxima per key split: S * nrt per head)
   e = launch_pdl(lm_threshold_kernel, dim3((unsigned)((long long)BH * m)), dim3(256), 0, st,
-                 q_tilde, m, topk, 2 * p.S, p.S, p.ntiles, ws, v_tilde);
+                 q_tilde, m, topk, 2 * p.S, p.S * p.nrt, p.ntiles, ws, v_tilde);
   count_launch();
   if (e != cudaSuccess) return e;
   const size_t sm2 = sizeof(CollectSmem) + 1024;
