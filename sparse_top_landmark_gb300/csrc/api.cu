@@ -415,7 +415,9 @@ ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, int s, size_
   L.bk = o; o += align256(bucket_ws_bytes(BH, (int)NS, m));
   L.ex = o;
   if (s > 1) o += align256(expert_partials_ws_bytes(BH, N, d, s));
-  else if (esize == 2 && expert_tc_supported(d, m, topk)) o += align256(expert_tc_ws_bytes(BH, N, m, topk));
+  else if (esize == 2 && expert_tc_supported(d, m, topk))
+    o += align256(std::max(expert_tc_ws_bytes(BH, N, m, topk),
+                           N <= 1024 ? expert_masked_ws_bytes(BH, N, m) : size_t(0)));
   L.rt = o; o += align256(route_ws_bytes(BH, N));
   // s > 1: the shared branch's partial, emitted by the route kernel
   L.lse = o; if (s > 1) o += align256((size_t)BH * N * 4);
@@ -495,6 +497,19 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
                                     ws + L.ex, out, ds->status, st, temp, routed),
               "expert launch");
     return MITA_OK;
+  }
+  if constexpr (std::is_same<T, bf16>::value) {
+    if (expert_tc_supported(d, m, topk) && expert_masked_preferred(N, m, topk, routed)) {
+      // short sequences: each query's expert from the route, then per-head query tiles over
+      // all keys masked to that expert's set -- no grouping needed
+      MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, 1, route, nullptr, nullptr, ds,
+                                  ws + L.rt, st, nullptr, nullptr, true),
+                "route launch");
+      MITA_CUDA(launch_expert_masked_tc(q, k, v, qt, vt, ti, route, BH, N, m, topk, ds->num_sms,
+                                        ws + L.ex, out, ds->status, st, temp, routed),
+                "expert launch");
+      return MITA_OK;
+    }
   }
   // s = 1: the expert kernel recomputes the shared logits q . q~ on the tensor cores rather
   // than taking them from the route stage as a carried partial (measured: the carried split,

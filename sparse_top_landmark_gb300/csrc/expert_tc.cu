@@ -209,7 +209,12 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
 }
 
 // -------------------------------------------------------------------------------------------
-template <bool kCarried>
+// kMasked: the short-sequence form -- units are tiles of a head's consecutive queries, the
+// raw chunks are all of the head's keys in place (K / V maps over [BH, N, 64]), and each
+// query keeps only the keys of its routed expert's top-k set (bit mask kmask[bh][e][words],
+// the expert from qroute), so one softmax still spans the m shared pairs and exactly the k
+// raw pairs of eq. 11-12.
+template <bool kCarried, bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_constant__ CUtensorMap map_kg,
                  const __grid_constant__ CUtensorMap map_vg, const __grid_constant__ CUtensorMap map_qt,
@@ -217,6 +222,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
                  const int* __restrict__ unit_count, const int4* __restrict__ unit_tab, int BH,
                  int N, int m, int topk, float cs_shared, int use_shared,
                  const float* __restrict__ sh_lse, const void* __restrict__ sh_o, int o_bf16,
+                 const uint32_t* __restrict__ kmask, int mwords, const int32_t* __restrict__ qroute,
                  bf16* __restrict__ out, int* status) {
   griddep_wait();
   extern __shared__ unsigned char smem_raw[];
@@ -306,8 +312,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
           if (elect_one()) {
             mbar_expect_tx(&s.kv_full[st], 2 * BN * 128);
             if (c < nrc) {
-              tma_load_3d(s.kb[st], &map_kg, &s.kv_full[st], 0, c * BN, idx);
-              tma_load_3d(s.vb[st], &map_vg, &s.kv_full[st], 0, c * BN, idx);
+              const int rawb = kMasked ? bh : idx;   // the head's keys, or the expert's block
+              tma_load_3d(s.kb[st], &map_kg, &s.kv_full[st], 0, c * BN, rawb);
+              tma_load_3d(s.vb[st], &map_vg, &s.kv_full[st], 0, c * BN, rawb);
             } else {
               tma_load_3d(s.kb[st], &map_qt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
               tma_load_3d(s.vb[st], &map_vt, &s.kv_full[st], 0, (c - nrc) * BN, bh);
@@ -495,6 +502,13 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       return sh_lse[r];
     };
     float l1 = units > 0 ? row_lse(cur, qi) : 0.f;
+    // masked form: the routed expert of this thread's query (-1: a padding row)
+    auto row_expert = [&](const int4& u, int q) -> int {
+      if (!kMasked || q < 0) return -1;
+      const int e = qroute[(size_t)(u.x / m) * N + q];
+      return (e >= 0 && e < m) ? e : -1;
+    };
+    int eq = units > 0 ? row_expert(cur, qi) : -1;
     int it = 0, c = 0;
     int prev_bh = 0, prev_qi = -1;
     float prev_lsum = 1.f, prev_mref = 0.f, prev_l1 = 0.f;
@@ -516,6 +530,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         if (it + 1 < units) nxt = unit_tab[ubase + it + 1];
         qi = row_query(cur);
         l1 = row_lse(cur, qi);
+        eq = row_expert(cur, qi);
         mref = -INFINITY;
         lsum = 0.f;
       }
@@ -536,6 +551,17 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
 #pragma unroll
         for (int i = 0; i < BN; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
       }
+      if (kMasked && c < nrc) {
+        // only the keys of the query's expert (a padding row keeps none)
+        const uint32_t* mw = kmask + ((size_t)(cur.x / m) * m + (eq >= 0 ? eq : 0)) * mwords;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const int wi = c * 4 + w4;
+          const uint32_t bits = (eq >= 0 && wi < mwords) ? mw[wi] : 0u;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * w4 + i] = ((bits >> i) & 1u) ? v[32 * w4 + i] : -INFINITY;
+        }
+      }
       // row maximum with four independent chains
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -552,8 +578,10 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         mref = xm;
       }
       // P = 2^(s * csc - mref) in fp32 pairs, packed to bf16 pairs; the row sum in two
-      // pair chains (from the unrounded values)
-      const unsigned long long c2 = f2pack(csc, csc), nm2 = f2pack(-mref, -mref);
+      // pair chains (from the unrounded values).  (Masked form: a row with no key of its
+      // expert so far keeps mref = -inf; its P is 0, not inf - inf.)
+      const float mr_off = (kMasked && mref == -INFINITY) ? 0.f : mref;
+      const unsigned long long c2 = f2pack(csc, csc), nm2 = f2pack(-mr_off, -mr_off);
       unsigned long long lsa = f2pack(0.f, 0.f), lsb = lsa;
       auto exp_half = [&](int base, uint32_t* pk) {
 #pragma unroll
@@ -660,16 +688,17 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
                         (uint64_t)(shared_chunks ? m : topk), (uint64_t)(shared_chunks ? BH : BH * m), BN))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(ExpertSmem) + 1024;
-  e = cudaFuncSetAttribute(expert_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(expert_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(expert_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(expert_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(shared_lse ? expert_tc_kernel<true> : expert_tc_kernel<false>,
+  e = launch_pdl(shared_lse ? expert_tc_kernel<true, false> : expert_tc_kernel<false, false>,
                  dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
                  mqg, mkg, mvg, mqt, mvt, bucket_qidx,
                  static_cast<const int*>(w.unit_start + (size_t)BH * m),
                  static_cast<const int4*>(w.unit), BH, N, m, topk, cs_shared, shared_chunks ? 1 : 0,
-                 shared_lse, shared_o, o_bf16, out, status);
+                 shared_lse, shared_o, o_bf16, static_cast<const uint32_t*>(nullptr), 0,
+                 static_cast<const int32_t*>(nullptr), out, status);
   count_launch();
   return e;
 }
@@ -728,15 +757,162 @@ cudaError_t launch_dense_tc(const bf16* q, const bf16* k, const bf16* v, int BH,
       !make_tmap_rows64(&mvt, v, (uint64_t)N, (uint64_t)BH, BN))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(ExpertSmem) + 1024;
-  e = cudaFuncSetAttribute(expert_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(expert_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(expert_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(expert_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(expert_tc_kernel<false>, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
+  e = launch_pdl(expert_tc_kernel<false, false>, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st,
                  mqg, mkg, mvg, mqt, mvt, static_cast<const int32_t*>(qidx),
                  static_cast<const int*>(ucount), static_cast<const int4*>(unit), BH, N, 1, N,
                  0.18033688011112042f, 0, static_cast<const float*>(nullptr),
-                 static_cast<const void*>(nullptr), 0, out, status);
+                 static_cast<const void*>(nullptr), 0, static_cast<const uint32_t*>(nullptr), 0,
+                 static_cast<const int32_t*>(nullptr), out, status);
+  count_launch();
+  return e;
+}
+
+}  // namespace mita
+
+// ---------------------------------------------------------------------------------------------
+// Short sequences (N <= 1024): tiles of a head's consecutive queries attend over the m shared
+// pairs and all N keys, each query's raw keys masked to its routed expert's top-k set
+// (expert_tc_kernel<false, true>).  When experts hold only a handful of queries each (ViT-S:
+// ~8 of 196), this replaces ~m mostly empty 256-query units per head by ceil(N / 256) full
+// ones and needs neither the bucket stage nor the gathered K / V blocks.
+// ---------------------------------------------------------------------------------------------
+namespace mita {
+namespace {
+
+// One launch: each CTA takes (head, expert) rows in turn and builds the expert's key bit mask
+// (32 keys per word) in shared memory; the grid also writes the unit table (unit = (head * m,
+// first query, count <= 256)), the identity query list and v~ in bf16.
+__global__ void __launch_bounds__(256)
+expert_mask_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ v_tilde,
+                   int BH, int N, int m, int topk, int mwords, uint32_t* __restrict__ kmask,
+                   bf16* __restrict__ vtb, int4* __restrict__ unit, int* __restrict__ ucount,
+                   int32_t* __restrict__ qidx, int* status) {
+  griddep_wait();
+  extern __shared__ uint32_t words[];       // [mwords]
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v_tilde != nullptr) {
+    const long long n4 = (long long)BH * m * 16;
+    for (long long t = t0; t < n4; t += stride) {
+      const float4 x = reinterpret_cast<const float4*>(v_tilde)[t];
+      uint2 o;
+      o.x = pack_bf16(x.x, x.y);
+      o.y = pack_bf16(x.z, x.w);
+      reinterpret_cast<uint2*>(vtb)[t] = o;
+    }
+  }
+  const long long per = (N + kUnitQ - 1) / kUnitQ, nu = (long long)BH * per;
+  const long long nq = (long long)BH * N;
+  for (long long t = t0; t < nu || t < nq; t += stride) {
+    if (t < nu) {
+      const int bh = (int)(t / per), j = (int)(t % per);
+      unit[t] = make_int4(bh * m, j * kUnitQ, min(kUnitQ, N - j * kUnitQ), 0);
+    }
+    if (t < nq) qidx[t] = (int32_t)(t % N);
+  }
+  if (t0 == 0) *ucount = (int)nu;
+  const long long rows = (long long)BH * m;
+  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+    for (int w = threadIdx.x; w < mwords; w += blockDim.x) words[w] = 0u;
+    __syncthreads();
+    for (int t = threadIdx.x; t < topk; t += blockDim.x) {
+      const int j = topk_idx[r * topk + t];
+      if (j >= 0 && j < N) atomicOr(&words[j >> 5], 1u << (j & 31));
+      else flag_error(status, kDevErrBadIndex);
+    }
+    __syncthreads();
+    for (int w = threadIdx.x; w < mwords; w += blockDim.x) kmask[r * mwords + w] = words[w];
+    __syncthreads();
+  }
+}
+
+struct MaskedWs {
+  int4* unit;
+  int* ucount;
+  int32_t* qidx;
+  bf16* vtb;
+  uint32_t* kmask;
+};
+
+MaskedWs carve_masked(void* ws, int BH, int N, int m) {
+  auto r = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t nu = (size_t)BH * ((N + kUnitQ - 1) / kUnitQ);
+  const int mwords = (N + 31) / 32;
+  char* p = static_cast<char*>(ws);
+  MaskedWs w;
+  w.unit = reinterpret_cast<int4*>(p); p += r(nu * 16);
+  w.ucount = reinterpret_cast<int*>(p); p += r(4);
+  w.qidx = reinterpret_cast<int32_t*>(p); p += r((size_t)BH * N * 4);
+  w.vtb = reinterpret_cast<bf16*>(p); p += r((size_t)BH * m * 64 * 2);
+  w.kmask = reinterpret_cast<uint32_t*>(p);
+  (void)mwords;
+  return w;
+}
+
+}  // namespace
+
+bool expert_masked_preferred(int N, int m, int topk, int routed_only) {
+  if (N > 1024 || N < 1) return false;
+  const long long nsc = routed_only ? 0 : (m + BN - 1) / BN;
+  const long long tiles = (N + kUnitQ - 1) / kUnitQ;
+  // MMA chunks per head: masked tiles over all keys, against ~one unit per expert (plus the
+  // ragged ones) over the expert's keys
+  const long long masked = tiles * ((N + BN - 1) / BN + nsc);
+  const long long grouped = ((long long)m + tiles) * ((topk + BN - 1) / BN + nsc);
+  return masked < grouped;
+}
+
+size_t expert_masked_ws_bytes(int BH, int N, int m) {
+  auto r = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t nu = (size_t)BH * ((N + kUnitQ - 1) / kUnitQ);
+  const size_t mwords = (size_t)(N + 31) / 32;
+  return r(nu * 16) + r(4) + r((size_t)BH * N * 4) + r((size_t)BH * m * 64 * 2) +
+         r((size_t)BH * m * mwords * 4);
+}
+
+cudaError_t launch_expert_masked_tc(const bf16* q, const bf16* k, const bf16* v,
+                                    const bf16* q_tilde, const float* v_tilde,
+                                    const int32_t* topk_idx, const int32_t* route, int BH, int N,
+                                    int m, int topk, int num_sms, void* ws, bf16* out,
+                                    int* status, cudaStream_t st, int shared_temp,
+                                    int routed_only) {
+  const MaskedWs w = carve_masked(ws, BH, N, m);
+  const int mwords = (N + 31) / 32;
+  const bool shared_chunks = !routed_only;
+  const float cs_shared = shared_temp ? 0.022542110013890052f : 0.18033688011112042f;
+  const long long work = std::max<long long>((long long)BH * m, (long long)BH * N / 256 + 1);
+  const unsigned blocks = (unsigned)std::min<long long>(work, (long long)std::max(num_sms, 1) * 8);
+  cudaError_t e = launch_pdl(expert_mask_kernel, dim3(blocks), dim3(256), (size_t)mwords * 4, st,
+                             topk_idx, shared_chunks ? v_tilde : static_cast<const float*>(nullptr),
+                             BH, N, m, topk, mwords, w.kmask, w.vtb, w.unit, w.ucount, w.qidx,
+                             status);
+  count_launch();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mqg, mkg, mvg, mqt, mvt;
+  if (!make_tmap_gather64(&mqg, q, (uint64_t)BH * N) ||
+      !make_tmap_rows64(&mkg, k, (uint64_t)N, (uint64_t)BH, BN) ||
+      !make_tmap_rows64(&mvg, v, (uint64_t)N, (uint64_t)BH, BN) ||
+      // (without shared chunks these two maps are never loaded: any valid map will do)
+      !make_tmap_rows64(&mqt, shared_chunks ? static_cast<const void*>(q_tilde) : k,
+                        (uint64_t)(shared_chunks ? m : N), (uint64_t)BH, BN) ||
+      !make_tmap_rows64(&mvt, shared_chunks ? static_cast<const void*>(w.vtb) : v,
+                        (uint64_t)(shared_chunks ? m : N), (uint64_t)BH, BN))
+    return cudaErrorInvalidValue;
+  const size_t smem = sizeof(ExpertSmem) + 1024;
+  e = cudaFuncSetAttribute(expert_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  // the raw "entries" of a unit are all N keys of its head (topk = N for the chunk count)
+  e = launch_pdl(expert_tc_kernel<false, true>, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads),
+                 smem, st, mqg, mkg, mvg, mqt, mvt, static_cast<const int32_t*>(w.qidx),
+                 static_cast<const int*>(w.ucount), static_cast<const int4*>(w.unit), BH, N, m, N,
+                 cs_shared, shared_chunks ? 1 : 0, static_cast<const float*>(nullptr),
+                 static_cast<const void*>(nullptr), 0, static_cast<const uint32_t*>(w.kmask),
+                 mwords, route, out, status);
   count_launch();
   return e;
 }

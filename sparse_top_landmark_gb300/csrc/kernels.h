@@ -26,7 +26,8 @@ struct LandmarkPlan {
   int split_len;  // keys per split (last one may be shorter)
   int P;          // padded candidate count per row in the merge (power of 2)
   int ntiles;     // 128-key tiles per head                      (tc path)
-  int cap;        // candidate capacity per row                  (tc path)
+  int cap;        // candidate capacity per row                  (tc and small paths)
+  bool small = false;   // N <= 1024 without the tc path: every key is a candidate
 };
 
 struct LandmarkWs {
@@ -161,6 +162,17 @@ cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                              int* status, cudaStream_t st, int shared_temp = 0,
                              int routed_only = 0, const float* shared_lse = nullptr,
                              const void* shared_o = nullptr, int o_bf16 = 0);
+// Short sequences (N <= 1024): per-head query tiles over the shared pairs and all N keys,
+// each query's raw keys masked to its routed expert's top-k set; no bucket stage (route is
+// [BH, N] s = 1).  expert_masked_preferred: fewer MMA chunks than the grouped form.
+bool expert_masked_preferred(int N, int m, int topk, int routed_only);
+size_t expert_masked_ws_bytes(int BH, int N, int m);
+cudaError_t launch_expert_masked_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                    const __nv_bfloat16* v, const __nv_bfloat16* q_tilde,
+                                    const float* v_tilde, const int32_t* topk_idx,
+                                    const int32_t* route, int BH, int N, int m, int topk,
+                                    int num_sms, void* ws, __nv_bfloat16* out, int* status,
+                                    cudaStream_t st, int shared_temp, int routed_only);
 // dense softmax attention of every query over all N keys of its head (bf16, d = 64)
 size_t dense_tc_ws_bytes(int BH, int N);
 cudaError_t launch_dense_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,

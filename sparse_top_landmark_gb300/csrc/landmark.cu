@@ -340,7 +340,7 @@ landmark_merge_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k, in
 // Returns hi + lo on every lane; like dot_f2, exact up to ~2^-48 relative.
 template <typename T, int D>
 __device__ __forceinline__ F2 dot_f2_warp(const float* qd, const T* krow, int lane) {
-  static_assert(D % 32 == 0 && D <= 128, "row split over the warp's lanes");
+  static_assert(D <= 128, "row split over the warp's lanes");   // lanes past D add zeros
   float s = 0.f, c = 0.f;
 #pragma unroll
   for (int l = lane; l < D; l += 32) {
@@ -587,6 +587,412 @@ cudaError_t run_partial(const T* qt, const T* k, const T* v, int BH, int N, int 
   return cudaGetLastError();
 }
 
+// Short sequences (N <= kSmallMaxN, too few key tiles for the tensor-core two-pass
+// selection): one CTA holds up to kSmallRows landmark rows of one head and takes all N keys
+// through shared memory twice -- K for the fp32 scores, then V for the shared values v~
+// (tutorial ch. 4 steps 2-3) -- in chunks staged by cp.async into a double buffer.  The
+// score block S[key][row] stays in shared memory; between the two passes each warp selects
+// its row's top-k exactly (the landmark_select_kernel rule: tau, the k-th largest fp32 score,
+// by a radix select over the order-preserving keys; keys above tau + 2E are members, the band
+// [tau - 2E, tau + 2E] is re-scored exactly and ranked by (score desc, index asc)) and turns
+// its scores into softmax weights in place.  Rows whose band holds more than 32 keys go to
+// the exact fallback.
+constexpr int kSmallMaxN = 1024;
+constexpr int kSmallRows = 8;              // landmark rows per CTA, one warp each
+constexpr int kSmallThreads = 256;
+constexpr int kSmallSP = kSmallRows + 1;   // S row stride in floats (odd: no bank conflicts)
+
+template <typename T, int D>
+struct SmallCfg {
+  static constexpr int VEC = Vec<T>::N;                       // elements per 16-byte slice
+  static constexpr int NS = D / VEC;                          // slices per row
+  static constexpr int KC0 = 16384 / (D * (int)sizeof(T));
+  static constexpr int KC = KC0 > 256 ? 256 : KC0;            // keys per staged chunk
+  static constexpr int RS = D * (int)sizeof(T) + 16;          // staged row stride (bytes)
+  static constexpr size_t BUF = (size_t)KC * RS;
+  static_assert((size_t)kSmallThreads / 32 * kSmallRows * D * 4 <= 2 * BUF,
+                "the cross-warp reduction fits in the staging buffers");
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// S[N][kSmallSP] floats, rounded up to keep what follows 16-byte aligned
+__host__ __device__ inline size_t small_s_floats(int N) {
+  return ((size_t)N * kSmallSP + 3) & ~(size_t)3;
+}
+
+// four consecutive elements as floats (8-byte aligned for bf16, 16-byte for fp32)
+__device__ __forceinline__ void load4(const bf16* p, float* o) {
+  const uint2 x = *reinterpret_cast<const uint2*>(p);
+  o[0] = __uint_as_float(x.x << 16);
+  o[1] = __uint_as_float(x.x & 0xffff0000u);
+  o[2] = __uint_as_float(x.y << 16);
+  o[3] = __uint_as_float(x.y & 0xffff0000u);
+}
+__device__ __forceinline__ void load4(const float* p, float* o) {
+  const float4 x = *reinterpret_cast<const float4*>(p);
+  o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+}
+
+template <typename T, int D>
+size_t small_smem_bytes(int N) {
+  using C = SmallCfg<T, D>;
+  return 2 * C::BUF + small_s_floats(N) * 4 + (size_t)kSmallRows * D * (4 + sizeof(T)) +
+         (size_t)kSmallRows * 256 * 4 + (size_t)kSmallRows * 32 * 8 + 64;
+}
+
+// One landmark row of landmark_small_kernel, on one warp: the exact top-k of the row's N fp32
+// scores (key j at Sw[j * kSmallSP]), then the softmax weights in place of the scores.  Lane
+// l holds keys l + 32 i for i < NI (32 NI >= N) in registers.
+template <typename T, int D, int NI>
+__device__ __forceinline__ void small_row(float* Sw, const float* qd, const T* kb, int N, int topk,
+                                          long long row, float km2, int* hist, int* bjw,
+                                          unsigned* sw, float* lsum_out, const LandmarkWs& ws,
+                                          int32_t* __restrict__ topk_idx, int lane) {
+  // the scores as order keys (fkey is a bijection: fkey_inv gives the score back)
+  uint32_t u[NI];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int j = lane + 32 * i;
+    const float x = j < N ? Sw[(size_t)j * kSmallSP] : -INFINITY;
+    mx = fmaxf(mx, x);
+    u[i] = j < N ? fkey(x) : 0u;             // 0: below every key
+  }
+  // tau: the topk-th largest order key, bit by bit from the top (the largest prefix that
+  // at least topk keys reach).  Bits 31..16 count every key; the keys sharing the 16-bit
+  // prefix found are then the only ones the low bits can still order, so they are listed:
+  // up to 32 of them are ranked directly, up to 256 finish the bit search alone.
+  uint32_t prefix = 0u;
+#pragma unroll 1
+  for (int b = 31; b >= 16; --b) {
+    const uint32_t cand = prefix | (1u << b);
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) c += u[i] >= cand ? 1 : 0;
+    if ((int)__reduce_add_sync(0xffffffffu, (unsigned)c) >= topk) prefix = cand;
+  }
+  {
+    const uint32_t top = prefix >> 16;
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) c += (u[i] >> 16) > top ? 1 : 0;
+    const int need = topk - (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
+    uint32_t* al = reinterpret_cast<uint32_t*>(hist);   // [256] keys sharing the prefix
+    int na16 = 0;
+    const unsigned lt16 = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      if (32 * i < N) {
+        const bool in = (u[i] >> 16) == top && u[i] != 0u;
+        const unsigned bm = __ballot_sync(0xffffffffu, in);
+        if (in && na16 + __popc(bm & lt16) < 256) al[na16 + __popc(bm & lt16)] = u[i];
+        na16 += __popc(bm);
+      }
+    }
+    __syncwarp();
+    if (na16 <= 32) {
+      // at most one listed key a lane: tau is the one whose rank among them brackets need
+      const uint32_t mine = lane < na16 ? al[lane] : 0u;
+      int gt = 0, eq = 0;
+      for (int f = 0; f < na16; ++f) {
+        const uint32_t o = al[f];
+        gt += o > mine ? 1 : 0;
+        eq += o == mine ? 1 : 0;
+      }
+      const bool hit = lane < na16 && gt < need && need <= gt + eq;
+      prefix = __shfl_sync(0xffffffffu, mine, __ffs(__ballot_sync(0xffffffffu, hit)) - 1);
+    } else if (na16 <= 256) {
+      uint32_t v[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v[t] = lane + 32 * t < na16 ? al[lane + 32 * t] : 0u;
+#pragma unroll 1
+      for (int b = 15; b >= 0; --b) {
+        const uint32_t cand = prefix | (1u << b);
+        int cc = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) cc += v[t] >= cand ? 1 : 0;
+        if ((int)__reduce_add_sync(0xffffffffu, (unsigned)cc) >= need) prefix = cand;
+      }
+    } else {
+#pragma unroll 1
+      for (int b = 15; b >= 0; --b) {
+        const uint32_t cand = prefix | (1u << b);
+        int cc = 0;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) cc += u[i] >= cand ? 1 : 0;
+        if ((int)__reduce_add_sync(0xffffffffu, (unsigned)cc) >= topk) prefix = cand;
+      }
+    }
+    __syncwarp();
+  }
+  const float tau = fkey_inv(prefix);
+  float qn2 = 0.f;
+  for (int l = lane; l < D; l += 32) qn2 = fmaf(qd[l], qd[l], qn2);
+  qn2 = warp_sum(qn2);
+  const float E = err_gamma(D) * sqrtf(qn2) * sqrtf(km2);
+  const float hi_band = tau + 2.f * E, lo_band = tau - 2.f * E;
+  const unsigned lt = (1u << lane) - 1u;
+  // members above the band (bit i: key lane + 32 i), and the band listed by ascending key
+  sw[lane] = 0u;
+  uint32_t above = 0u;
+  int nb = 0, na = 0;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    if (32 * i < N) {
+      const bool ok = lane + 32 * i < N;
+      const float x = fkey_inv(u[i]);
+      const bool ab = ok && x > hi_band, in = ok && !ab && x >= lo_band;
+      above |= (uint32_t)ab << i;
+      na += __popc(__ballot_sync(0xffffffffu, ab));
+      const unsigned bm = __ballot_sync(0xffffffffu, in);
+      if (in && nb + __popc(bm & lt) < 32) bjw[nb + __popc(bm & lt)] = lane + 32 * i;
+      nb += __popc(bm);
+    }
+  }
+  if (nb > 32) {
+    if (lane == 0) ws.slow_rows[atomicAdd(ws.nslow, 1)] = (int)row;
+  } else {
+    __syncwarp();
+    F2 mine{-INFINITY, 0.f};
+    int mj = 0x7fffffff;
+    for (int e = 0; e < nb; ++e) {
+      const int j = bjw[e];
+      const F2 x = dot_f2_warp<T, D>(qd, kb + (size_t)j * D, lane);
+      if (lane == e) { mine = x; mj = j; }
+    }
+    int rank = 0;
+    for (int f = 0; f < nb; ++f) {
+      const F2 y{__shfl_sync(0xffffffffu, mine.hi, f), __shfl_sync(0xffffffffu, mine.lo, f)};
+      const int jf = __shfl_sync(0xffffffffu, mj, f);
+      if (f != lane && ranks_before(y, jf, mine, mj)) ++rank;
+    }
+    if (lane < nb && rank < topk - na) atomicOr(&sw[mj & 31], 1u << (mj >> 5));
+    __syncwarp();
+    const uint32_t mem = above | sw[lane];
+    int32_t* out = topk_idx + row * topk;
+    int pos = 0;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      if (32 * i < N) {
+        const bool take = (mem >> i) & 1u;
+        const unsigned mm = __ballot_sync(0xffffffffu, take);
+        if (take && pos + __popc(mm & lt) < topk) out[pos + __popc(mm & lt)] = lane + 32 * i;
+        pos += __popc(mm);
+      }
+    }
+  }
+  const float cl = softmax_scale_log2(D);
+  const float M = warp_max(mx) * cl;         // log2 units
+  float ls = 0.f;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int j = lane + 32 * i;
+    if (32 * i < N && j < N) {
+      const float p = exp2f(fkey_inv(u[i]) * cl - M);
+      Sw[(size_t)j * kSmallSP] = p;
+      ls += p;
+    }
+  }
+  const float lsum = warp_sum(ls);
+  if (lane == 0) {
+    *lsum_out = lsum;
+    if (ws.lse_out) ws.lse_out[row] = (M + log2f(lsum)) * 0.6931471805599453f;
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kSmallThreads, 3)
+landmark_small_kernel(const T* __restrict__ q_tilde, const T* __restrict__ k,
+                      const T* __restrict__ v, int N, int m, int groups, int rpg, int topk,
+                      LandmarkWs ws, int32_t* __restrict__ topk_idx, float* __restrict__ v_tilde) {
+  using C = SmallCfg<T, D>;
+  constexpr int VEC = C::VEC, NS = C::NS, KC = C::KC;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* buf = smem_raw;                                       // [2][KC][RS]
+  float* S = reinterpret_cast<float*>(smem_raw + 2 * C::BUF);          // [N][kSmallSP]
+  float* qs = S + small_s_floats(N);                                   // [rows][D]
+  T* qsT = reinterpret_cast<T*>(qs + kSmallRows * D);                  // [rows][D]
+  int* whist = reinterpret_cast<int*>(qsT + kSmallRows * D);           // [rows][256]
+  int* bj = whist + kSmallRows * 256;                                  // [rows][32]
+  unsigned* selw = reinterpret_cast<unsigned*>(bj + kSmallRows * 32);  // [rows][32]
+  float* lsum_s = reinterpret_cast<float*>(selw + kSmallRows * 32);    // [rows]
+  unsigned* km2_s = reinterpret_cast<unsigned*>(lsum_s + kSmallRows);  // [1]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long bh = blockIdx.x / groups;
+  const int r0 = (int)(blockIdx.x % groups) * rpg;
+  const int nrows = min(rpg, m - r0);
+  const long long row0 = bh * m + r0;
+  const T* kb = k + (size_t)bh * N * D;
+  const T* vb = v + (size_t)bh * N * D;
+  const int nc = (N + KC - 1) / KC;
+
+  auto stage = [&](int c) {                  // chunk c < nc: K rows; c >= nc: V rows
+    const T* src = c < nc ? kb : vb;
+    const int j0 = (c < nc ? c : c - nc) * KC;
+    unsigned char* dst = buf + (size_t)(c & 1) * C::BUF;
+    for (int t = tid; t < KC * NS; t += kSmallThreads) {
+      const int jl = t / NS, s = t % NS;
+      if (j0 + jl < N)
+        cp_async16(dst + (size_t)jl * C::RS + s * 16, src + (size_t)(j0 + jl) * D + s * VEC);
+    }
+    cp_async_commit();
+  };
+
+  griddep_wait();
+  stage(0);
+  for (int t = tid; t < kSmallRows * D; t += kSmallThreads) {
+    const int r = t / D;
+    const T x = r < nrows ? q_tilde[(row0 + r) * D + t % D] : T(0.f);
+    qsT[t] = x;
+    qs[t] = to_f(x);
+  }
+  if (tid == 0) *km2_s = 0u;
+
+  // ---- pass 1: S[j][r] = q~_r . k_j (fp32), and the largest squared key norm; a thread
+  // takes keys jl and jl + KC / 2 of the chunk, on every TPP-th slice
+  constexpr int KP = KC / 2, TPP = kSmallThreads / KP;
+  static_assert(NS % TPP == 0 && TPP <= 32, "pair threads split a row's slices");
+  float km2 = 0.f;
+  for (int c = 0; c < nc; ++c) {
+    stage(c + 1);
+    cp_async_wait<1>();
+    __syncthreads();
+    const unsigned char* kbuf = buf + (size_t)(c & 1) * C::BUF;
+    const int kp = tid / TPP, part = tid % TPP;
+    const int j0 = c * KC + kp, j1 = j0 + KP;
+    float a0[kSmallRows], a1[kSmallRows];
+#pragma unroll
+    for (int r = 0; r < kSmallRows; ++r) { a0[r] = 0.f; a1[r] = 0.f; }
+    float n0 = 0.f, n1 = 0.f;
+    if (j0 < N) {
+#pragma unroll
+      for (int s = part; s < NS; s += TPP) {
+        float x0[VEC], x1[VEC];
+        Vec<T>::load(reinterpret_cast<const T*>(kbuf + (size_t)kp * C::RS + s * 16), x0);
+        Vec<T>::load(reinterpret_cast<const T*>(kbuf + (size_t)(kp + KP) * C::RS + s * 16), x1);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          n0 = fmaf(x0[e], x0[e], n0);
+          n1 = fmaf(x1[e], x1[e], n1);
+        }
+#pragma unroll
+        for (int r = 0; r < kSmallRows; ++r) {
+          float q[VEC];
+          Vec<T>::load(qsT + r * D + s * VEC, q);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            a0[r] = fmaf(q[e], x0[e], a0[r]);
+            a1[r] = fmaf(q[e], x1[e], a1[r]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < TPP; o <<= 1) {
+      n0 += __shfl_xor_sync(0xffffffffu, n0, o);
+      n1 += __shfl_xor_sync(0xffffffffu, n1, o);
+#pragma unroll
+      for (int r = 0; r < kSmallRows; ++r) {
+        a0[r] += __shfl_xor_sync(0xffffffffu, a0[r], o);
+        a1[r] += __shfl_xor_sync(0xffffffffu, a1[r], o);
+      }
+    }
+    if (part == 0) {
+      if (j0 < N) {
+#pragma unroll
+        for (int r = 0; r < kSmallRows; ++r) S[(size_t)j0 * kSmallSP + r] = a0[r];
+        km2 = fmaxf(km2, n0);
+      }
+      if (j1 < N) {              // the second key's staged row is stale past N: unused then
+#pragma unroll
+        for (int r = 0; r < kSmallRows; ++r) S[(size_t)j1 * kSmallSP + r] = a1[r];
+        km2 = fmaxf(km2, n1);
+      }
+    }
+    __syncthreads();
+  }
+  km2 = warp_max(km2);
+  if (lane == 0) atomicMax(km2_s, __float_as_uint(km2));   // non-negative: bits order as values
+  __syncthreads();
+
+  // ---- per row (one warp): exact top-k, then softmax weights in place of the scores
+  if (warp < nrows) {
+    const float km2h = __uint_as_float(*km2_s);
+    float* Sw = S + warp;
+    if (N <= 256)
+      small_row<T, D, 8>(Sw, qs + warp * D, kb, N, topk, row0 + warp, km2h, whist + warp * 256,
+                         bj + warp * 32, selw + warp * 32, lsum_s + warp, ws, topk_idx, lane);
+    else
+      small_row<T, D, 32>(Sw, qs + warp * D, kb, N, topk, row0 + warp, km2h, whist + warp * 256,
+                          bj + warp * 32, selw + warp * 32, lsum_s + warp, ws, topk_idx, lane);
+  }
+  __syncthreads();
+
+  // ---- pass 2: sum_j p_rj v_j; thread = (key group g, 4-element piece s of the row)
+  constexpr int NP = D / 4;                  // pieces per row
+  constexpr int GP = kSmallThreads / NP;     // key groups
+  static_assert(NP <= 32 && 32 % NP == 0, "a warp spans whole rows in the V pass");
+  const int s = tid % NP, g = tid / NP;
+  float acc[kSmallRows][4];
+#pragma unroll
+  for (int r = 0; r < kSmallRows; ++r)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+  for (int c = nc; c < 2 * nc; ++c) {
+    if (c + 1 < 2 * nc) stage(c + 1);
+    if (c + 1 < 2 * nc) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    __syncthreads();
+    const unsigned char* vbuf = buf + (size_t)(c & 1) * C::BUF;
+    const int jn = min(KC, N - (c - nc) * KC);
+    const float* Sc = S + (size_t)(c - nc) * KC * kSmallSP;
+#pragma unroll 4
+    for (int jl = g; jl < jn; jl += GP) {
+      float x[4];
+      load4(reinterpret_cast<const T*>(vbuf + (size_t)jl * C::RS) + 4 * s, x);
+      const float* pj = Sc + (size_t)jl * kSmallSP;
+#pragma unroll
+      for (int r = 0; r < kSmallRows; ++r) {
+        const float p = pj[r];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[r][e] = fmaf(p, x[e], acc[r][e]);
+      }
+    }
+    __syncthreads();
+  }
+  // lanes of a warp that share a piece, then the warps through shared memory
+#pragma unroll
+  for (int o = NP; o < 32; o <<= 1)
+#pragma unroll
+    for (int r = 0; r < kSmallRows; ++r)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], o);
+  float* red = reinterpret_cast<float*>(buf);                          // [warps][rows][D]
+  if (lane < NP) {
+#pragma unroll
+    for (int r = 0; r < kSmallRows; ++r)
+      *reinterpret_cast<float4*>(red + ((size_t)warp * kSmallRows + r) * D + 4 * s) =
+          make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  }
+  __syncthreads();
+  for (int t = tid; t < nrows * D; t += kSmallThreads) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSmallThreads / 32; ++w) sum += red[(size_t)w * kSmallRows * D + t];
+    const int r = t / D;
+    v_tilde[(row0 + r) * D + t % D] = sum / lsum_s[r];
+  }
+}
+
 template <typename T, int D>
 cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int topk,
                 const LandmarkPlan& p, const LandmarkWs& ws, int32_t* topk_idx, float* vt,
@@ -613,6 +1019,22 @@ cudaError_t run(const T* qt, const T* k, const T* v, int BH, int N, int m, int t
     }
   }
   (void)status;
+  if (p.small) {
+    const int groups = (m + kSmallRows - 1) / kSmallRows;
+    const int rpg = (m + groups - 1) / groups;
+    const size_t smem = small_smem_bytes<T, D>(N);
+    auto kern = landmark_small_kernel<T, D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, dim3((unsigned)((long long)BH * groups)), dim3(kSmallThreads), smem, st,
+                   qt, k, v, N, m, groups, rpg, topk, ws, topk_idx, vt);
+    count_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(landmark_exact_kernel<T, D>, dim3(kExactCtas), dim3(512), 0, st, qt, k, N, m,
+                   topk, ws, topk_idx);
+    count_launch();
+    return e;
+  }
   switch (p.RT) {
     case 32: e = run_partial<T, D, 32>(qt, k, v, BH, N, m, p, ws, st); break;
     case 64: e = run_partial<T, D, 64>(qt, k, v, BH, N, m, p, ws, st); break;
@@ -641,6 +1063,19 @@ LandmarkPlan plan_landmark(int BH, int N, int d, int m, int topk, int num_sms, b
     return p;
   }
   p.tc = false;
+  if (N <= kSmallMaxN) {
+    // one CTA per block of landmark rows of a head, all N keys staged through shared memory
+    p.small = true;
+    p.RT = kSmallRows;
+    p.nrt = 1;
+    p.S = 1;
+    p.split_len = N;
+    p.Tcap = 0;
+    p.cap = 0;
+    p.P = 0;
+    p.ntiles = 0;
+    return p;
+  }
   p.RT = m >= 128 ? 128 : (m > 32 ? 64 : 32);
   p.nrt = (m + p.RT - 1) / p.RT;
   p.Tcap = std::min(kTcapMax, topk + 32);
@@ -663,7 +1098,9 @@ size_t landmark_ws_bytes(const LandmarkPlan& p, int BH, int N, int d, int m) {
   size_t b = 0;
   auto add = [&](size_t n) { b += (n + 255) / 256 * 256; };
   add(parts * 4); add(parts * 4); add(parts * d * 4);
-  if (!p.tc) { add(parts * p.Tcap * 4); add(parts * p.Tcap * 4); add(parts * 4); add(parts * 4); }
+  if (!p.tc && !p.small) {
+    add(parts * p.Tcap * 4); add(parts * p.Tcap * 4); add(parts * 4); add(parts * 4);
+  }
   add((size_t)BH * p.S * std::max(1, p.nrt) * 4);
   add(4); add(rows * 4);
   add((size_t)kExactCtas * N * 8);
@@ -684,7 +1121,7 @@ LandmarkWs carve_landmark_ws(void* base, const LandmarkPlan& p, int BH, int N, i
   w.M = (float*)take(parts * 4);
   w.L = (float*)take(parts * 4);
   w.A = (float*)take(parts * d * 4);
-  if (!p.tc) {
+  if (!p.tc && !p.small) {
     w.cs = (float*)take(parts * p.Tcap * 4);
     w.ci = (int*)take(parts * p.Tcap * 4);
     w.cn = (int*)take(parts * 4);
