@@ -9,21 +9,26 @@
 // Two sweeps over the keys, each split over CTAs (flash-decoding style):
 //
 // sweep (pass 1), CTA = (head, 128 landmarks, key split):
-//   warp 0       TMA: K and V tiles of 128 keys into a 4-stage ring;
+//   warp 0       TMA: K and V tiles of 128 keys into an 8-deep K ring and a
+//                4-deep V ring (a K slot is freed as soon as S is computed,
+//                a V slot once P V is done);
 //   warps 1-2    MMA, one issuing warp per softmax group: S = q~ K^T into the
 //                group's tensor memory, the group's next S as soon as the
 //                softmax has copied S out, then O += P V with P read from
 //                tensor memory;
-//   warp 3       largest |k| element (error bound of the fp32 scores);
+//   warp 3       largest |k| element of the split's keys, a bound on |k|^2
+//                for the error bound of the fp32 scores (the split's nrt
+//                row-block CTAs scan every nrt-th tile each; the threshold
+//                kernel takes the maximum);
 //   warps 4-7,   two softmax warpgroups that take alternate key tiles, each
 //   warps 8-11   with its own online-softmax state (max, sum) and its own O
 //                accumulator, so one computes while the other's MMAs run.
 //                Rescaling of O is lazy (only when the max grows by more than
-//                2^8).  Each also keeps the 32 largest tile maxima (raw
-//                scores) it saw, in a small shared-memory min-heap.
+//                2^8).  Each also writes every key tile's largest raw score
+//                per landmark row to a tile-maximum table (bm).
 // threshold, CTA = one landmark: merges the softmax partials into v~
 //   (tutorial ch. 4: (Z1 o1 + Z2 o2) / (Z1 + Z2)) and takes the k-th largest
-//   kept tile maximum tau_L.  k distinct tiles reach tau_L, so at least k
+//   tile maximum tau_L of the row.  k distinct tiles reach tau_L, so at least k
 //   keys score >= tau_L: every top-k key scores >= tau_L - E (exactly) and
 //   >= tau_L - 2E in fp32 (E bounds the fp32 error).  Collection uses
 //   tau_L - 4E, which stays valid even if pass 2's fp32 scores differ from
