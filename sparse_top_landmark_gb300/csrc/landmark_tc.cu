@@ -9,14 +9,15 @@
 // Two sweeps over the keys, each split over CTAs (flash-decoding style):
 //
 // sweep (pass 1), CTA = (head, 128 landmarks, key split):
-//   warp 0       TMA: K and V tiles of 128 keys into an 8-deep K ring and a
-//                4-deep V ring (a K slot is freed as soon as S is computed,
-//                a V slot once P V is done);
+//   warp 0       TMA: K tiles of 128 keys into an 8-deep ring (a slot is freed
+//                as soon as S is computed);
 //   warps 1-2    MMA, one issuing warp per softmax group: S = q~ K^T into the
 //                group's tensor memory, the group's next S as soon as the
 //                softmax has copied S out, then O += P V with P read from
 //                tensor memory;
-//   warp 3       largest |k| element of the split's keys, a bound on |k|^2
+//   warp 3       TMA: V tiles into a 4-deep ring (a slot is freed once P V is
+//                done), so K runs ahead of V by the softmax latency; and the
+//                largest |k| element of the split's keys, a bound on |k|^2
 //                for the error bound of the fp32 scores (the split's nrt
 //                row-block CTAs scan every nrt-th tile each; the threshold
 //                kernel takes the maximum);
