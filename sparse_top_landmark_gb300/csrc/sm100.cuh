@@ -46,6 +46,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// Bounded wait of one thread: gives up after `limit` unsuccessful polls (each
+// poll suspends the thread for a hardware-chosen interval) or about 2^31 SM
+// cycles (~1 s), whichever comes first, so a lost arrival can never hang the
+// GPU.  Inline (a call here costs the softmax warps registers).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t limit = 1u << 24) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > (1ll << 31)) break;
+  }
+  return false;
+}
+
 // One poll that may suspend the thread until the phase completes (the hint, in
 // ns, caps the suspension; the thread wakes as soon as the phase completes).
 __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity) {
@@ -57,22 +72,6 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
       : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
       : "memory");
   return done != 0;
-}
-
-// Bounded wait of one thread: gives up after `limit` unsuccessful polls (after
-// the first, each poll suspends the thread until the phase completes or the
-// hint runs out) or about 2^31 SM cycles (~1 s), whichever comes first, so a
-// lost arrival can never hang the GPU.  Inline (a call here costs the softmax
-// warps registers).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint32_t limit = 1u << 24) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (uint32_t i = 0; i < limit; ++i) {
-    if (mbar_try_wait_hint(bar, parity)) return true;
-    if (clock64() - t0 > (1ll << 31)) break;
-  }
-  return false;
 }
 
 // Slow path of mbar_wait_warp, kept out of line: a loop anywhere near a
