@@ -9,7 +9,7 @@
 // bit.fan article: queries are grouped by expert and an online softmax runs
 // over the concatenated entries; each expert's k KV rows are gathered once.
 //
-// Two launches:
+// Two launches (grouped form):
 //   expert_gather_kernel  the k K / V rows of every (head, expert), copied once
 //                         into contiguous [head*m + expert][k][64] blocks; one
 //                         more CTA builds the work-unit table (unit = (head,
@@ -34,6 +34,16 @@
 //                the output rows.  One code path for every chunk: a second,
 //                fp16 copy of the unrolled exponential loop (for an fp16 v~)
 //                cost ~8 % of the forward's time, measured.
+// Two more forms of expert_tc_kernel (template flags):
+//   carried  the shared branch arrives as a partial (log-sum-exp and output
+//            over the m shared pairs, from the route stage); only raw chunks
+//            run, and the partial joins each row at write-out by the
+//            branch-merge identity (Z1 o1 + Z2 o2) / (Z1 + Z2);
+//   masked   short sequences: a unit is a tile of a head's consecutive
+//            queries and its raw entries are all N keys of the head, each
+//            masked per query to its routed expert's top-k set (membership bit
+//            masks from expert_mask_kernel) -- fewer chunks than grouping
+//            when N is small.
 #include <algorithm>
 
 #include "common.cuh"
@@ -54,7 +64,7 @@ constexpr int kGatherThreads = 256;
 struct alignas(1024) ExpertSmem {
   bf16 q[2][2][128 * 64];          // [unit buffer][query tile]
   bf16 kb[kStages][BN * 64];       // q~ block or the expert's K rows
-  bf16 vb[kStages][BN * 64];       // v~ block (fp16) or the expert's V rows
+  bf16 vb[kStages][BN * 64];       // v~ block (bf16) or the expert's V rows
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
