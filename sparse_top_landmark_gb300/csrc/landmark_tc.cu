@@ -28,8 +28,10 @@
 //                2^8).  Each also writes every key tile's largest raw score
 //                per landmark row to a tile-maximum table (bm).
 // threshold, CTA = one landmark: merges the softmax partials into v~
-//   (tutorial ch. 4: (Z1 o1 + Z2 o2) / (Z1 + Z2)) and takes the k-th largest
-//   tile maximum tau_L of the row.  k distinct tiles reach tau_L, so at least k
+//   (tutorial ch. 4: (Z1 o1 + Z2 o2) / (Z1 + Z2)) and takes tau_L, a lower
+//   bound of the row's k-th largest tile maximum (the lower edge of the
+//   histogram bin where the count from the top reaches k).  k distinct tiles
+//   reach tau_L, so at least k
 //   keys score >= tau_L: every top-k key scores >= tau_L - E (exactly) and
 //   >= tau_L - 2E in fp32 (E bounds the fp32 error).  Collection uses
 //   tau_L - 4E, which stays valid even if pass 2's fp32 scores differ from
