@@ -274,18 +274,18 @@ template <typename T>
 bool route_uses_tc(int d, int m, int s, const float* lse, const float* so) {
   return std::is_same<T, bf16>::value && s == 1 && !lse && !so && route_tc_supported(d, m);
 }
-// s = 1 with the shared branch's partial requested (both outputs): the tensor-core kernel
+// the shared branch's partial requested (both outputs), s = 1 or 2: the tensor-core kernel
 // that reuses the routing logits as the shared logits
 template <typename T>
 bool route_shared_uses_tc(int d, int m, int s, const float* lse, const float* so) {
-  return std::is_same<T, bf16>::value && s == 1 && lse && so && route_shared_tc_supported(d, m);
+  return std::is_same<T, bf16>::value && lse && so && route_shared_tc_supported(d, m, s);
 }
 
 template <typename T>
 cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int N, int d, int m,
                            int s, int32_t* route, float* lse, float* so, DevState* ds, void* ws,
                            cudaStream_t st, int* hist = nullptr, bool* counted = nullptr,
-                           bool prezeroed = false) {
+                           bool prezeroed = false, int temp = 0) {
   if constexpr (std::is_same<T, bf16>::value) {
     if (route_uses_tc<T>(d, m, s, lse, so)) {
       if (counted) *counted = hist != nullptr;
@@ -293,12 +293,13 @@ cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int
                              ds->status, hist, st, prezeroed);
     }
     if (route_shared_uses_tc<T>(d, m, s, lse, so)) {
-      if (counted) *counted = hist != nullptr;
-      return launch_route_shared_tc(q, qt, vt, BH, N, m, ds->num_sms, 0, 0, route, lse, so,
-                                    static_cast<int*>(ws), ds->status, hist, st, prezeroed);
+      if (counted) *counted = hist != nullptr && s == 1;   // s > 1: the bucket stage counts
+      return launch_route_shared_tc(q, qt, vt, BH, N, m, ds->num_sms, temp, 0, route, lse, so,
+                                    static_cast<int*>(ws), ds->status, s == 1 ? hist : nullptr,
+                                    st, prezeroed, s);
     }
   }
-  return launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st);
+  return launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st, temp);
 }
 
 template <typename T>
@@ -362,16 +363,29 @@ int expert_impl(const T* q, const T* k, const T* v, const T* qt, const float* vt
     const size_t pb = align256(expert_partials_ws_bytes(BH, N, d, s));
     const size_t rb = align256((size_t)BH * N * 4), lb = align256((size_t)BH * N * 4);
     const size_t ob = align256((size_t)BH * N * d * 4);
+    const bool tc = std::is_same<T, bf16>::value && expert_tc_supported(d, m, topk);
+    const size_t tb = tc ? align256(expert_tc_partials_ws_bytes(BH, N, m, topk, s)) : 0;
     void* wsv = nullptr;
-    MITA_TRY(workspace(pb + (so ? 0 : rb + lb + ob), st, &wsv));
+    MITA_TRY(workspace(pb + tb + (so ? 0 : rb + lb + ob), st, &wsv));
     char* ws = static_cast<char*>(wsv);
     if (so == nullptr) {
-      int32_t* r1 = reinterpret_cast<int32_t*>(ws + pb);
-      float* l1 = reinterpret_cast<float*>(ws + pb + rb);
-      float* o1 = reinterpret_cast<float*>(ws + pb + rb + lb);
+      int32_t* r1 = reinterpret_cast<int32_t*>(ws + pb + tb);
+      float* l1 = reinterpret_cast<float*>(ws + pb + tb + rb);
+      float* o1 = reinterpret_cast<float*>(ws + pb + tb + rb + lb);
       MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, 1, r1, l1, o1, st), "shared partial");
       lse = l1;
       so = o1;
+    }
+    if constexpr (std::is_same<T, bf16>::value) {
+      if (tc) {
+        const ExpertPartials part = carve_expert_partials(ws, BH, N, d, s);
+        MITA_CUDA(launch_expert_tc_partials(q, k, v, ti, off, qidx, BH, N, m, topk, s,
+                                            ds->num_sms, ws + pb, part, ds->status, st),
+                  "expert launch");
+        MITA_CUDA(launch_expert_merge<T>(lse, so, 0, part, BH, N, d, s, out, ds->status, st),
+                  "merge launch");
+        return MITA_OK;
+      }
     }
     MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, BH, N, d, m, topk, s,
                                     ws, out, ds->status, st),
@@ -414,7 +428,11 @@ ForwardLayout forward_layout(int BH, int N, int d, int m, int topk, int s, size_
   L.lm = o; o += align256(landmark_ws_bytes(L.plan, BH, N, d, m));
   L.bk = o; o += align256(bucket_ws_bytes(BH, (int)NS, m));
   L.ex = o;
-  if (s > 1) o += align256(expert_partials_ws_bytes(BH, N, d, s));
+  if (s > 1) {
+    o += align256(expert_partials_ws_bytes(BH, N, d, s));
+    if (esize == 2 && expert_tc_supported(d, m, topk))
+      o += align256(expert_tc_partials_ws_bytes(BH, N, m, topk, s));
+  }
   else if (esize == 2 && expert_tc_supported(d, m, topk))
     o += align256(std::max(expert_tc_ws_bytes(BH, N, m, topk),
                            N <= 1024 ? expert_masked_ws_bytes(BH, N, m) : size_t(0)));
@@ -487,12 +505,41 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
     // entries, per-expert partials and their merge
     float* lse = reinterpret_cast<float*>(ws + L.lse);
     float* so = reinterpret_cast<float*>(ws + L.so);
-    // routing only: no shared partial
-    MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, routed ? nullptr : lse,
-                              routed ? nullptr : so, st, temp),
-              "route launch");
+    // routing only: no shared partial (the SIMT route then lists the routes alone); with the
+    // shared branch, s = 2 and m <= 256 route on the tensor cores, the shared partial's output
+    // in bf16
+    int so_bf16 = 0;
+    if constexpr (std::is_same<T, bf16>::value) {
+      if (!routed && route_shared_tc_supported(d, m, s)) {
+        so_bf16 = 1;
+        MITA_CUDA(launch_route_shared_tc(q, qt, vt, BH, N, m, ds->num_sms, temp, 1, route, lse, so,
+                                         reinterpret_cast<int*>(ws + L.rt), ds->status, nullptr,
+                                         st, true, s),
+                  "route launch");
+      }
+    }
+    if (!so_bf16)
+      MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, s, route, routed ? nullptr : lse,
+                                  routed ? nullptr : so, ds, ws + L.rt, st, nullptr, nullptr, true,
+                                  temp),
+                "route launch");
     MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, false, s),
               "bucket launch");
+    if constexpr (std::is_same<T, bf16>::value) {
+      if (expert_tc_supported(d, m, topk)) {
+        // every (query, expert) entry's raw-pair partial on the tensor cores (fp32 outputs:
+        // bf16 partials measured beyond the output tolerance), then the merge
+        const ExpertPartials part = carve_expert_partials(ws + L.ex, BH, N, d, s);
+        void* tws = ws + L.ex + align256(expert_partials_ws_bytes(BH, N, d, s));
+        MITA_CUDA(launch_expert_tc_partials(q, k, v, ti, off, qidx, BH, N, m, topk, s,
+                                            ds->num_sms, tws, part, ds->status, st),
+                  "expert launch");
+        MITA_CUDA(launch_expert_merge<T>(routed ? nullptr : lse, routed ? nullptr : so, so_bf16,
+                                         part, BH, N, d, s, out, ds->status, st),
+                  "merge launch");
+        return MITA_OK;
+      }
+    }
     MITA_CUDA(launch_expert_attn<T>(q, k, v, qt, vt, ti, off, qidx, lse, so, BH, N, d, m, topk, s,
                                     ws + L.ex, out, ds->status, st, temp, routed),
               "expert launch");

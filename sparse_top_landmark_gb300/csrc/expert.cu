@@ -213,65 +213,127 @@ expert_attn_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     *reinterpret_cast<float4*>(part.o + pi * D + l) = make_float4(acc[l], acc[l + 1], acc[l + 2], acc[l + 3]);
 }
 
-// s > 1: out = (Z_sh o_sh + sum_t Z_t o_t) / (Z_sh + sum_t Z_t), Z = exp(lse), one warp per
-// query; the s partials are taken in ascending bucket position.
-template <typename T, int D>
+// s > 1: out = (Z_sh o_sh + sum_t Z_t o_t) / (Z_sh + sum_t Z_t), Z = exp(lse) (the
+// tutorial's branch merge).  D / 4 lanes per query, four dimensions each (16-byte loads; the
+// shared output may come in bf16); every load of a query is issued before its arithmetic, and KS >= s
+// slots are read, so a small KS keeps registers (and more queries in flight) for small s.
+// The s partials are added in ascending bucket position (their slots were taken by atomics),
+// so the result does not depend on which CTA wrote which slot.
+__device__ __forceinline__ float4 load4f(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float4 load4f(const bf16* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+__device__ __forceinline__ void store4(float* out, const float* a) {
+  *reinterpret_cast<float4*>(out) = make_float4(a[0], a[1], a[2], a[3]);
+}
+__device__ __forceinline__ void store4(bf16* out, const float* a) {
+  __nv_bfloat162 h0 = __floats2bfloat162_rn(a[0], a[1]), h1 = __floats2bfloat162_rn(a[2], a[3]);
+  uint2 w;
+  w.x = *reinterpret_cast<uint32_t*>(&h0);
+  w.y = *reinterpret_cast<uint32_t*>(&h1);
+  *reinterpret_cast<uint2*>(out) = w;
+}
+
+template <typename T, int D, int KS>
 __global__ void __launch_bounds__(kMergeWarps * 32)
-expert_merge_kernel(const float* __restrict__ shared_lse, const float* __restrict__ shared_o,
-                    Partials part, long long BHN, int s, T* __restrict__ out, int* status) {
-  const int lane = threadIdx.x & 31;
-  const long long qi = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  if (qi >= BHN) return;
-  if (part.cnt[qi] != s) {
-    if (lane == 0) flag_error(status, kDevErrBadBucket);
+expert_merge_kernel(const float* __restrict__ shared_lse, const void* __restrict__ shared_o,
+                    int so_bf16, Partials part, long long BHN, int s, T* __restrict__ out,
+                    int* status) {
+  constexpr int LPQ = D / 4;                 // lanes per query
+  constexpr int QPB = kMergeWarps * 32 / LPQ;
+  const int c = threadIdx.x % LPQ;
+  const long long qi = (long long)blockIdx.x * QPB + threadIdx.x / LPQ;
+  if (qi >= BHN) return;                     // whole query groups
+  const bool sh = shared_lse != nullptr;     // routing only: no shared partial
+  const int cnt = part.cnt[qi];
+  float pl[KS];
+  int pp[KS];
+  float4 po[KS];
+#pragma unroll
+  for (int t = 0; t < KS; ++t) {
+    pl[t] = -INFINITY;
+    pp[t] = 0x7fffffff;
+    po[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < s) {
+      pl[t] = part.lse[qi * s + t];
+      pp[t] = part.pos[qi * s + t];
+      const size_t off = ((size_t)qi * s + t) * D + 4 * c;
+      po[t] = load4f(part.o + off);
+    }
+  }
+  const float lsh = sh ? shared_lse[qi] : -INFINITY;
+  float4 osh = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (sh) {
+    const size_t off = (size_t)qi * D + 4 * c;
+    osh = so_bf16 ? load4f(static_cast<const bf16*>(shared_o) + off)
+                  : load4f(static_cast<const float*>(shared_o) + off);
+  }
+  if (cnt != s) {
+    if (c == 0) flag_error(status, kDevErrBadBucket);
     return;
   }
-  float pl = -INFINITY;
-  int pp = 0x7fffffff;
-  if (lane < s) {
-    pl = part.lse[qi * s + lane];
-    pp = part.pos[qi * s + lane];
-  }
-  int rank = 0;
-  // routing only: no shared partial
-  const bool sh = shared_lse != nullptr;
-  float M = sh ? shared_lse[qi] : -INFINITY;
-  for (int t = 0; t < s; ++t) {
-    rank += __shfl_sync(0xffffffffu, pp, t) < pp ? 1 : 0;
-    M = fmaxf(M, __shfl_sync(0xffffffffu, pl, t));
-  }
-  constexpr float kL2e = 1.4426950408889634f;
-  constexpr int PER = (D + 31) / 32;
-  const float wsh = sh ? exp2f((shared_lse[qi] - M) * kL2e) : 0.f;
-  float z = wsh;
-  float acc[PER];
+  float M = lsh;
 #pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int l = lane + 32 * j;
-    acc[j] = (sh && l < D) ? wsh * shared_o[qi * D + l] : 0.f;
-  }
-  for (int r = 0; r < s; ++r) {
-    const unsigned who = __ballot_sync(0xffffffffu, lane < s && rank == r);
-    if (who == 0) {   // two partials claim one bucket position
-      if (lane == 0) flag_error(status, kDevErrBadBucket);
+  for (int t = 0; t < KS; ++t) M = fmaxf(M, pl[t]);
+  constexpr float kL2e = 1.4426950408889634f;
+  const float wsh = sh ? exp2f((lsh - M) * kL2e) : 0.f;
+  float z = wsh;
+  float acc[4] = {wsh * osh.x, wsh * osh.y, wsh * osh.z, wsh * osh.w};
+  // rank r: the slot holding the r-th smallest bucket position
+#pragma unroll
+  for (int r = 0; r < KS; ++r) {
+    if (r >= s) break;
+    int src = -1;
+#pragma unroll
+    for (int t = 0; t < KS; ++t) {
+      int rank = 0;
+#pragma unroll
+      for (int u = 0; u < KS; ++u) rank += (u < s && pp[u] < pp[t]) ? 1 : 0;
+      if (t < s && rank == r) src = t;
+    }
+    if (src < 0) {                           // two partials claim one bucket position
+      if (c == 0) flag_error(status, kDevErrBadBucket);
       return;
     }
-    const int src = __ffs(who) - 1;
-    const float w = exp2f((__shfl_sync(0xffffffffu, pl, src) - M) * kL2e);
-    z += w;
-    const float* o = part.o + ((size_t)qi * s + src) * D;
+    float wl = -INFINITY;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int l = lane + 32 * j;
-      if (l < D) acc[j] = fmaf(w, o[l], acc[j]);
-    }
+    for (int t = 0; t < KS; ++t)
+      if (t == src) { wl = pl[t]; o = po[t]; }
+    const float w = exp2f((wl - M) * kL2e);
+    z += w;
+    acc[0] = fmaf(w, o.x, acc[0]);
+    acc[1] = fmaf(w, o.y, acc[1]);
+    acc[2] = fmaf(w, o.z, acc[2]);
+    acc[3] = fmaf(w, o.w, acc[3]);
   }
   const float inv = 1.f / z;
 #pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int l = lane + 32 * j;
-    if (l < D) put(out + qi * D + l, acc[j] * inv);
-  }
+  for (int e = 0; e < 4; ++e) acc[e] *= inv;
+  store4(out + (size_t)qi * D + 4 * c, acc);
+}
+
+template <typename T, int D>
+cudaError_t launch_merge_d(const float* shared_lse, const void* shared_o, int so_bf16,
+                           Partials part, long long BHN, int s, T* out, int* status,
+                           cudaStream_t st) {
+  constexpr long long QPB = kMergeWarps * 32 / (D / 4);
+  const unsigned grid = (unsigned)((BHN + QPB - 1) / QPB);
+  if (s <= 2)
+    expert_merge_kernel<T, D, 2><<<grid, kMergeWarps * 32, 0, st>>>(shared_lse, shared_o, so_bf16,
+                                                                    part, BHN, s, out, status);
+  else if (s <= 4)
+    expert_merge_kernel<T, D, 4><<<grid, kMergeWarps * 32, 0, st>>>(shared_lse, shared_o, so_bf16,
+                                                                    part, BHN, s, out, status);
+  else
+    expert_merge_kernel<T, D, kMaxRouteS><<<grid, kMergeWarps * 32, 0, st>>>(
+        shared_lse, shared_o, so_bf16, part, BHN, s, out, status);
+  count_launch();
+  return cudaGetLastError();
 }
 
 template <typename T, int D>
@@ -303,11 +365,8 @@ cudaError_t run(const T* q, const T* k, const T* v, const T* qt, const float* vt
   if (s > 1) {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    expert_merge_kernel<T, D><<<(unsigned)((BHN + kMergeWarps - 1) / kMergeWarps),
-                                kMergeWarps * 32, 0, st>>>(routed ? nullptr : lse,
-                                                           routed ? nullptr : so, part, BHN, s,
-                                                           out, status);
-    count_launch();
+    return launch_merge_d<T, D>(routed ? nullptr : lse, routed ? nullptr : so, 0, part, BHN, s,
+                                out, status, st);
   }
   return cudaGetLastError();
 }
@@ -355,6 +414,38 @@ size_t expert_partials_ws_bytes(int BH, int N, int d, int s) {
   const size_t r = (size_t)BH * N;
   return r * s * d * sizeof(float) + 2 * r * s * sizeof(float) + r * sizeof(int);
 }
+
+ExpertPartials carve_expert_partials(void* ws, int BH, int N, int d, int s) {
+  const size_t r = (size_t)BH * N;
+  char* p = static_cast<char*>(ws);
+  ExpertPartials part{};
+  part.o = reinterpret_cast<float*>(p);
+  p += r * s * d * sizeof(float);
+  part.lse = reinterpret_cast<float*>(p);
+  p += r * s * sizeof(float);
+  part.pos = reinterpret_cast<int*>(p);
+  p += r * s * sizeof(int);
+  part.cnt = reinterpret_cast<int*>(p);
+  return part;
+}
+
+template <typename T>
+cudaError_t launch_expert_merge(const float* shared_lse, const void* shared_o, int so_bf16,
+                                ExpertPartials part, int BH, int N, int d, int s, T* out,
+                                int* status, cudaStream_t st) {
+  const long long BHN = (long long)BH * N;
+  switch (d) {
+    case 16: return launch_merge_d<T, 16>(shared_lse, shared_o, so_bf16, part, BHN, s, out, status, st);
+    case 32: return launch_merge_d<T, 32>(shared_lse, shared_o, so_bf16, part, BHN, s, out, status, st);
+    case 64: return launch_merge_d<T, 64>(shared_lse, shared_o, so_bf16, part, BHN, s, out, status, st);
+    case 128: return launch_merge_d<T, 128>(shared_lse, shared_o, so_bf16, part, BHN, s, out, status, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+template cudaError_t launch_expert_merge<float>(const float*, const void*, int, ExpertPartials,
+                                                int, int, int, int, float*, int*, cudaStream_t);
+template cudaError_t launch_expert_merge<bf16>(const float*, const void*, int, ExpertPartials,
+                                               int, int, int, int, bf16*, int*, cudaStream_t);
 
 template <typename T>
 cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_tilde,

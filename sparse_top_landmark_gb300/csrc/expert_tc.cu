@@ -43,7 +43,13 @@
 //            queries and its raw entries are all N keys of the head, each
 //            masked per query to its routed expert's top-k set (membership bit
 //            masks from expert_mask_kernel) -- fewer chunks than grouping
-//            when N is small.
+//            when N is small;
+//   partial  top-s routing (s > 1; tutorial ch. 4 step 4, eq. 10-12): the
+//            buckets hold N * s (query, expert) entries; each entry runs the
+//            raw chunks of its expert and leaves its partial (natural
+//            log-sum-exp and O / l in fp32, with its bucket position) in one of
+//            its query's s slots; expert_merge_kernel joins the shared partial
+//            and the s raw ones by the branch-merge identity.
 #include <algorithm>
 
 #include "common.cuh"
@@ -128,7 +134,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
                      const int32_t* __restrict__ topk_idx, long long rows, int N, int m, int topk,
                      const int32_t* __restrict__ bucket_off, const float* __restrict__ v_tilde,
-                     int BH, ExpertTcWs w, int* status) {
+                     int BH, ExpertTcWs w, int* status, int nent) {
   griddep_wait();
   // v~ in bf16, four values per thread step (not needed, and possibly absent, when the
   // kernel runs no shared chunks)
@@ -155,7 +161,7 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
         const int bh = i / m, e = i % m;
         a = bucket_off[(size_t)bh * (m + 1) + e];
         const int b = bucket_off[(size_t)bh * (m + 1) + e + 1];
-        if (a < 0 || b > N || b < a) flag_error(status, kDevErrBadBucket);
+        if (a < 0 || b > nent || b < a) flag_error(status, kDevErrBadBucket);
         else { cnt = b - a; units = (cnt + kUnitQ - 1) / kUnitQ; }
       }
       int tot;
@@ -224,7 +230,7 @@ expert_gather_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v,
 // query keeps only the keys of its routed expert's top-k set (bit mask kmask[bh][e][words],
 // the expert from qroute), so one softmax still spans the m shared pairs and exactly the k
 // raw pairs of eq. 11-12.
-template <bool kCarried, bool kMasked>
+template <bool kCarried, bool kMasked, bool kPartial = false>
 __global__ void __launch_bounds__(kThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_constant__ CUtensorMap map_kg,
                  const __grid_constant__ CUtensorMap map_vg, const __grid_constant__ CUtensorMap map_qt,
@@ -233,7 +239,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
                  int N, int m, int topk, float cs_shared, int use_shared,
                  const float* __restrict__ sh_lse, const void* __restrict__ sh_o, int o_bf16,
                  const uint32_t* __restrict__ kmask, int mwords, const int32_t* __restrict__ qroute,
-                 bf16* __restrict__ out, int* status) {
+                 bf16* __restrict__ out, int* status, int nent, int nroutes, ExpertPartials part) {
   griddep_wait();
   extern __shared__ unsigned char smem_raw[];
   ExpertSmem& s = *reinterpret_cast<ExpertSmem*>(
@@ -305,7 +311,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
           const int r = 4 * lane + j;
           rows[j] = null_row;
           if (r < qcnt) {
-            const int qi = bucket_qidx[(size_t)bh * N + qbase + r];
+            const int qi = bucket_qidx[(size_t)bh * nent + qbase + r];
             if (qi >= 0 && qi < N) rows[j] = bh * N + qi;
             else flag_error(status, kDevErrBadBucket);
           }
@@ -398,7 +404,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
           const int r = 128 + 4 * lane + j;
           rows[j] = null_row;
           if (r < qcnt) {
-            const int qi = bucket_qidx[(size_t)bh * N + qbase + r];
+            const int qi = bucket_qidx[(size_t)bh * nent + qbase + r];
             if (qi >= 0 && qi < N) rows[j] = bh * N + qi;
             else flag_error(status, kDevErrBadBucket);
           }
@@ -425,7 +431,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
     // query id of this thread's row in unit u (-1: padding row)
     auto row_query = [&](const int4& u) -> int {
       if (qr >= u.z) return -1;
-      const int qi = bucket_qidx[(size_t)(u.x / m) * N + u.y + qr];
+      const int qi = bucket_qidx[(size_t)(u.x / m) * nent + u.y + qr];
       return (qi >= 0 && qi < N) ? qi : -1;
     };
     // O / l of the finished unit to its query's output row
@@ -433,9 +439,22 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
     // normalised output of the m shared pairs) this unit attended over the raw pairs only,
     // and the two partials merge here: tutorial ch. 4, (Z1 o1 + Z2 o2) / (Z1 + Z2).
     constexpr bool carried = kCarried;
-    auto write_row = [&](int bh, int qi, float lsum, float mr, float l1) {
-      const bool wr = ok && qi >= 0;
+    auto write_row = [&](int bh, int qi, float lsum, float mr, float l1, int pos) {
+      bool wr = ok && qi >= 0;
       const size_t rowi = (size_t)bh * N + (wr ? qi : 0);
+      size_t pi = 0;
+      if (kPartial && wr) {
+        // this (query, expert) entry's slot among the query's s partials
+        const int ps = atomicAdd(&part.cnt[rowi], 1);
+        if (ps >= nroutes) {
+          flag_error(status, kDevErrBadBucket);
+          wr = false;
+        } else {
+          pi = rowi * nroutes + ps;
+          part.lse[pi] = (mr + log2f(lsum)) * 0.6931471805599453f;   // natural log
+          part.pos[pi] = pos;
+        }
+      }
       float w1 = 0.f, w2 = 1.f / lsum;
       if (carried) {
         const float L1 = l1 * 1.4426950408889634f, L2 = mr + log2f(lsum);   // log2 units
@@ -453,6 +472,15 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         tmem_ld_wait();
         tmem_fence_regs<32>(o);
         if (!wr) continue;
+        if (kPartial) {
+          const float inv = 1.f / lsum;
+          float4* dp = reinterpret_cast<float4*>(part.o + pi * 64 + half * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dp[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                o[4 * i + 3] * inv);
+          continue;
+        }
         if (carried) {
           float o1[32];
           if (o_bf16) {
@@ -520,7 +548,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
     };
     int eq = units > 0 ? row_expert(cur, qi) : -1;
     int it = 0, c = 0;
-    int prev_bh = 0, prev_qi = -1;
+    int prev_bh = 0, prev_qi = -1, prev_pos = 0;
     float prev_lsum = 1.f, prev_mref = 0.f, prev_l1 = 0.f;
     bool pending = false;          // a finished unit's O still waits in tensor memory
     float mref = -INFINITY, lsum = 0.f;
@@ -530,6 +558,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
         // last P . V is done
         prev_bh = cur.x / m;
         prev_qi = qi;
+        prev_pos = cur.y + qr;
         prev_lsum = lsum;
         prev_mref = mref;
         prev_l1 = l1;
@@ -613,7 +642,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       tmem_st16(tP, pk0);
       tmem_st16(tP + 16, pk0 + 16);
       if (pending) {
-        write_row(prev_bh, prev_qi, prev_lsum, prev_mref, prev_l1);
+        write_row(prev_bh, prev_qi, prev_lsum, prev_mref, prev_l1, prev_pos);
         pending = false;
       }
       uint32_t pk1[BN / 4];
@@ -644,7 +673,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
     if (G > 0) {
       if (ok && !mbar_wait(&s.pv_done[slot], (G - 1) & 1)) ok = false;
       tc_fence_after();
-      write_row(cur.x / m, qi, lsum, mref, l1);
+      write_row(cur.x / m, qi, lsum, mref, l1, cur.y + qr);
     }
     tc_fence_before();
     if (!ok) flag_error(status, kDevErrTimeout);
@@ -684,7 +713,7 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
   cudaError_t e = launch_pdl(expert_gather_kernel, dim3((unsigned)gblocks + 1), dim3(kGatherThreads),
                              0, st, k, v, topk_idx, rows, N, m, topk, bucket_off,
                              shared_chunks ? v_tilde : static_cast<const float*>(nullptr), BH, w,
-                             status);
+                             status, N);
   count_launch();
   if (e != cudaSuccess) return e;
   CUtensorMap mqg, mkg, mvg, mqt, mvt;
@@ -708,7 +737,52 @@ cudaError_t launch_expert_tc(const bf16* q, const bf16* k, const bf16* v, const 
                  static_cast<const int*>(w.unit_start + (size_t)BH * m),
                  static_cast<const int4*>(w.unit), BH, N, m, topk, cs_shared, shared_chunks ? 1 : 0,
                  shared_lse, shared_o, o_bf16, static_cast<const uint32_t*>(nullptr), 0,
-                 static_cast<const int32_t*>(nullptr), out, status);
+                 static_cast<const int32_t*>(nullptr), out, status, N, 1, ExpertPartials{});
+  count_launch();
+  return e;
+}
+
+// Top-s partials (s > 1): the raw pairs of every (query, expert) entry of the N * s-entry
+// buckets, one partial per entry into `part` (cleared slot counters: the caller merges).
+size_t expert_tc_partials_ws_bytes(int BH, int N, int m, int topk, int s) {
+  return expert_tc_ws_bytes(BH, N * s, m, topk);
+}
+
+cudaError_t launch_expert_tc_partials(const bf16* q, const bf16* k, const bf16* v,
+                                      const int32_t* topk_idx, const int32_t* bucket_off,
+                                      const int32_t* bucket_qidx, int BH, int N, int m, int topk,
+                                      int s, int num_sms, void* ws, ExpertPartials part,
+                                      int* status, cudaStream_t st) {
+  if (s < 1 || (long long)N * s >= (1LL << 31)) return cudaErrorInvalidValue;
+  const int nent = N * s;
+  const ExpertTcWs w = carve(ws, BH, nent, m, topk);
+  const long long rows = (long long)BH * m * topk;
+  const long long gblocks = std::min<long long>((rows + kGatherThreads / 8 - 1) / (kGatherThreads / 8),
+                                                (long long)std::max(num_sms, 1) * 8);
+  cudaError_t e = cudaMemsetAsync(part.cnt, 0, (size_t)BH * N * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(expert_gather_kernel, dim3((unsigned)gblocks + 1), dim3(kGatherThreads), 0, st, k,
+                 v, topk_idx, rows, N, m, topk, bucket_off, static_cast<const float*>(nullptr), BH,
+                 w, status, nent);
+  count_launch();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mqg, mkg, mvg;
+  if (!make_tmap_gather64(&mqg, q, (uint64_t)BH * N) ||
+      !make_tmap_rows64(&mkg, w.kg, (uint64_t)topk, (uint64_t)BH * m, BN) ||
+      !make_tmap_rows64(&mvg, w.vg, (uint64_t)topk, (uint64_t)BH * m, BN))
+    return cudaErrorInvalidValue;
+  const size_t smem = sizeof(ExpertSmem) + 1024;
+  auto kern = expert_tc_kernel<false, false, true>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // no shared chunks: the q~ / v~ maps are never loaded (the expert block maps stand in)
+  e = launch_pdl(kern, dim3((unsigned)std::max(num_sms, 1)), dim3(kThreads), smem, st, mqg, mkg,
+                 mvg, mkg, mvg, bucket_qidx,
+                 static_cast<const int*>(w.unit_start + (size_t)BH * m),
+                 static_cast<const int4*>(w.unit), BH, N, m, topk, 0.18033688011112042f, 0,
+                 static_cast<const float*>(nullptr), static_cast<const void*>(nullptr), 0,
+                 static_cast<const uint32_t*>(nullptr), 0, static_cast<const int32_t*>(nullptr),
+                 static_cast<bf16*>(nullptr), status, nent, s, part);
   count_launch();
   return e;
 }
@@ -776,7 +850,7 @@ cudaError_t launch_dense_tc(const bf16* q, const bf16* k, const bf16* v, int BH,
                  static_cast<const int*>(ucount), static_cast<const int4*>(unit), BH, N, 1, N,
                  0.18033688011112042f, 0, static_cast<const float*>(nullptr),
                  static_cast<const void*>(nullptr), 0, static_cast<const uint32_t*>(nullptr), 0,
-                 static_cast<const int32_t*>(nullptr), out, status);
+                 static_cast<const int32_t*>(nullptr), out, status, N, 1, ExpertPartials{});
   count_launch();
   return e;
 }
@@ -922,7 +996,7 @@ cudaError_t launch_expert_masked_tc(const bf16* q, const bf16* k, const bf16* v,
                  static_cast<const int*>(w.ucount), static_cast<const int4*>(w.unit), BH, N, m, N,
                  cs_shared, shared_chunks ? 1 : 0, static_cast<const float*>(nullptr),
                  static_cast<const void*>(nullptr), 0, static_cast<const uint32_t*>(w.kmask),
-                 mwords, route, out, status);
+                 mwords, route, out, status, N, 1, ExpertPartials{});
   count_launch();
   return e;
 }

@@ -107,6 +107,15 @@ cudaError_t launch_expert_partials(const T* q, const T* k, const T* v, const int
 // s > 1 needs the shared partial (shared_lse, shared_o) and `ws` of
 // expert_partials_ws_bytes(BH, N, d, s) bytes for the per-expert partials.
 size_t expert_partials_ws_bytes(int BH, int N, int d, int s);
+// the partial arrays inside such a workspace (lse, o, pos, then the slot counters)
+ExpertPartials carve_expert_partials(void* ws, int BH, int N, int d, int s);
+// out = the branch-merge of the shared partial (none when shared_lse is null) and each
+// query's s raw partials, taken in ascending bucket position
+// (shared_o in bf16 when so_bf16, else fp32)
+template <typename T>
+cudaError_t launch_expert_merge(const float* shared_lse, const void* shared_o, int so_bf16,
+                                ExpertPartials part, int BH, int N, int d, int s, T* out,
+                                int* status, cudaStream_t st);
 template <typename T>
 cudaError_t launch_expert_attn(const T* q, const T* k, const T* v, const T* q_tilde,
                                const float* v_tilde, const int32_t* topk_idx,
@@ -141,19 +150,36 @@ cudaError_t launch_route_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde
 cudaError_t launch_route_fixup(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH,
                                int N, int m, int num_sms, int32_t* route, const int* amb,
                                int* hist, cudaStream_t st);
-// Routing (s = 1) together with the shared branch's partial from the same logits: per
-// query the route, shared_lse (natural log-sum-exp of the scaled shared logits) and
-// shared_o = the normalised shared output, [BH*N][64] in bf16 (o_bf16 = 1) or fp32.
-// `amb` and `hist` as for launch_route_tc (the fix-up runs inside).
-bool route_shared_tc_supported(int d, int m);
+// exact top-s re-routing (2 <= s <= 8) of the queries route_shared_tc (s = 2) left on the
+// ambiguous lists in `amb`; route is [BH*N][s]
+cudaError_t launch_route_fixup_top(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH,
+                                   int N, int m, int s, int num_sms, int32_t* route,
+                                   const int* amb, cudaStream_t st);
+// Routing (s = 1, or the best two with s = 2) together with the shared branch's partial from
+// the same logits: per query the route ([BH*N][s], best first), shared_lse (natural
+// log-sum-exp of the scaled shared logits) and shared_o = the normalised shared output,
+// [BH*N][64] in bf16 (o_bf16 = 1) or fp32.  `amb` and `hist` as for launch_route_tc (the
+// fix-up runs inside; with s = 2 `hist` is ignored: the bucket stage counts the N*s entries).
+bool route_shared_tc_supported(int d, int m, int s = 1);
 cudaError_t launch_route_shared_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde,
                                    const float* v_tilde, int BH, int N, int m, int num_sms,
                                    int shared_temp, int o_bf16, int32_t* route,
                                    float* shared_lse, void* shared_o, int* amb, int* status,
-                                   int* hist, cudaStream_t st, bool prezeroed = false);
+                                   int* hist, cudaStream_t st, bool prezeroed = false,
+                                   int s = 1);
 
 bool expert_tc_supported(int d, int m, int topk);
 size_t expert_tc_ws_bytes(int BH, int N, int m, int topk);
+// top-s (s > 1) raw-pair partials on the tensor cores: one per (query, expert) entry of the
+// N*s-entry buckets, into `part` (its slot counters are cleared here); ws of
+// expert_tc_partials_ws_bytes bytes
+size_t expert_tc_partials_ws_bytes(int BH, int N, int m, int topk, int s);
+cudaError_t launch_expert_tc_partials(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                      const __nv_bfloat16* v, const int32_t* topk_idx,
+                                      const int32_t* bucket_off, const int32_t* bucket_qidx,
+                                      int BH, int N, int m, int topk, int s, int num_sms,
+                                      void* ws, ExpertPartials part, int* status,
+                                      cudaStream_t st);
 cudaError_t launch_expert_tc(const __nv_bfloat16* q, const __nv_bfloat16* k,
                              const __nv_bfloat16* v, const __nv_bfloat16* q_tilde,
                              const float* v_tilde, const int32_t* topk_idx,

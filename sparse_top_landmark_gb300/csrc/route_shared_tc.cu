@@ -1,6 +1,7 @@
-// Step 4 on the tensor cores together with the shared branch of step 6 (s = 1,
-// bf16, d = 64, m <= 512): each query's best landmark AND the partial result of
-// its m shared pairs, from one set of query-landmark logits.
+// Step 4 on the tensor cores together with the shared branch of step 6 (bf16,
+// d = 64; s = 1 with m <= 512, s = 2 with m <= 256): each query's best landmark
+// (or best two) AND the partial result of its m shared pairs, from one set of
+// query-landmark logits.
 //
 // MiTA tutorial (iwxt.cn), ch. 4 step 4 (paper eq. 10): the logits q . q~_i
 // choose the expert (argmax, no gate); ch. 6 counts the same dot product once
@@ -28,6 +29,15 @@
 // The exact argmax follows route_tc.cu's rules; route_fixup_kernel (same file
 // there) re-routes the ambiguous queries.  Routing only needs the logits, so the
 // shared branch's partial does not depend on the fix-up.
+// s = 2 (tutorial ch. 4 step 4, eq. 10: the top-s landmarks): each thread keeps
+// the three best 32-score blocks of its row, ranked by (block maximum desc,
+// position asc), each copied to shared memory.  A score outside those blocks
+// has three block maxima ranking ahead of it (a tie between maxima goes to the
+// earlier block, whose tied score has the lower index), hence three scores
+// ahead of it; so the row's best three scores, and the route (best two, ranked)
+// with its gap test, come from the copies alone.  The route is exact when both
+// gaps (first to second, second to third) exceed 2E; otherwise the query goes
+// to the exact top-s fix-up.
 #include <algorithm>
 
 #include "common.cuh"
@@ -39,19 +49,24 @@ namespace {
 using namespace sm100;
 
 constexpr int BN = 128;             // landmarks per chunk
-constexpr int kMaxM = 512;
-constexpr int kQStages = 4;
 constexpr int kThreads = 384;       // producer, two issuers, one idle warp, 8 softmax warps
 constexpr int kSoftThreads = 256;
 constexpr float kLazy = 8.0f;
 
+// per route count s: landmark limit, query-tile ring depth, 32-score block copies per thread
+template <int kS> struct RsCfg;
+template <> struct RsCfg<1> { static constexpr int kMaxM = 512, kQStages = 4, kBlocks = 1; };
+template <> struct RsCfg<2> { static constexpr int kMaxM = 256, kQStages = 2, kBlocks = 3; };
+
+template <int kS>
 struct alignas(1024) RsSmem {
-  bf16 qt[kMaxM * 64];              // landmark rows (128B-swizzled, TMA)
-  bf16 vt[kMaxM * 64];              // shared values, bf16 (128B-swizzled, written here)
-  bf16 q[kQStages][128 * 64];       // query tiles
-  float4 bbuf[kSoftThreads][8];     // per softmax thread: copy of its best 32-score block
-  uint64_t q_full[kQStages], q_empty[kQStages];
-  uint64_t res_full;                // q~ loaded and v~ converted
+  using C = RsCfg<kS>;
+  bf16 qt[C::kMaxM * 64];                 // landmark rows (128B-swizzled, TMA)
+  bf16 vt[C::kMaxM * 64];                 // shared values, bf16 (128B-swizzled, written here)
+  bf16 q[C::kQStages][128 * 64];          // query tiles
+  float4 bbuf[C::kBlocks][kSoftThreads][8];   // per softmax thread: copies of 32-score blocks
+  uint64_t q_full[C::kQStages], q_empty[C::kQStages];
+  uint64_t res_full;                      // q~ loaded and v~ converted
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], drain[2];
   float red[8];
   uint32_t tmem;
@@ -150,6 +165,93 @@ __device__ __forceinline__ Cand finish_top(const RowTop& t, const float4* bbs, i
   return c;
 }
 
+// ---- s = 2: the three best 32-score blocks, ranked by (maximum desc, position asc) -------
+__device__ __forceinline__ float block_max32(const float* v) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[10] = fmaxf(v[30], v[31]);
+  return fmaxf(max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), max3f(a[6], a[7], a[8])),
+               fmaxf(a[9], a[10]));
+}
+struct Top3Blocks {
+  float bv[3] = {-INFINITY, -INFINITY, -INFINITY};   // block maxima, best first
+  int b0[3] = {0, 0, 0};                             // first landmark index of each block
+  int slot[3] = {0, 1, 2};                           // its copy's shared-memory slot
+};
+// bb: this thread's slot-0 copy; slot t lies t * slot_stride float4s further
+__device__ __forceinline__ void top3_block(Top3Blocks& t, const float* v, float mb, int i0,
+                                           float4* bb, int slot_stride, int sw) {
+  // blocks already kept with an equal maximum come earlier, so they stay ahead
+  const int p = (t.bv[0] >= mb ? 1 : 0) + (t.bv[1] >= mb ? 1 : 0) + (t.bv[2] >= mb ? 1 : 0);
+  if (p < 3) {
+    const int fs = t.slot[2];              // the third block's copy is dropped
+    if (p <= 1) { t.bv[2] = t.bv[1]; t.b0[2] = t.b0[1]; t.slot[2] = t.slot[1]; }
+    if (p == 0) { t.bv[1] = t.bv[0]; t.b0[1] = t.b0[0]; t.slot[1] = t.slot[0]; }
+    if (p == 0) { t.bv[0] = mb; t.b0[0] = i0; t.slot[0] = fs; }
+    else if (p == 1) { t.bv[1] = mb; t.b0[1] = i0; t.slot[1] = fs; }
+    else { t.bv[2] = mb; t.b0[2] = i0; t.slot[2] = fs; }
+    float4* dst = bb + fs * slot_stride;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      dst[c ^ sw] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  }
+}
+struct Top3 {
+  float v[3];
+  int i[3];
+};
+// the row's three best (score, index) pairs, ranked by (score desc, index asc), from the
+// kept blocks' copies: three rounds of (best current block maximum, the lowest index holding
+// it among the blocks that reach it, removal from its block and that block's new maximum)
+__device__ __forceinline__ Top3 finish_top3(const Top3Blocks& t, const float4* bb,
+                                            int slot_stride, int sw) {
+  float x[3][32];
+#pragma unroll
+  for (int b = 0; b < 3; ++b) {
+    const bool kept = t.bv[b] > -INFINITY;
+    const float4* src = bb + t.slot[b] * slot_stride;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4 y = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      if (kept) y = src[q ^ sw];
+      x[b][4 * q] = y.x; x[b][4 * q + 1] = y.y; x[b][4 * q + 2] = y.z; x[b][4 * q + 3] = y.w;
+    }
+  }
+  float cm[3] = {t.bv[0], t.bv[1], t.bv[2]};   // each block's current maximum
+  Top3 r;
+#pragma unroll
+  for (int e = 0; e < 3; ++e) {
+    const float mx = fmaxf(fmaxf(cm[0], cm[1]), cm[2]);
+    int best = 0x7fffffff, bsel = -1, isel = 0;
+#pragma unroll
+    for (int b = 0; b < 3; ++b) {
+      if (cm[b] == mx && t.bv[b] > -INFINITY) {
+        uint32_t eq[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) eq[i & 3] |= (x[b][i] == mx ? 1u : 0u) << i;
+        const uint32_t msk = (eq[0] | eq[1]) | (eq[2] | eq[3]);
+        const int i = __ffs(msk) - 1;
+        if (msk && t.b0[b] + i < best) { best = t.b0[b] + i; bsel = b; isel = i; }
+      }
+    }
+    r.v[e] = mx;
+    r.i[e] = best;
+    if (e < 2) {
+#pragma unroll
+      for (int b = 0; b < 3; ++b) {
+        if (b == bsel) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[b][i] = (i == isel) ? -INFINITY : x[b][i];
+          cm[b] = block_max32(x[b]);
+        }
+      }
+    }
+  }
+  return r;
+}
+
+template <int kS>
 __global__ void __launch_bounds__(kThreads, 1)
 route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_qt,
@@ -161,8 +263,10 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   // amb: the heads' counts at amb[0, BH), then head bh's query ids at amb + BH + bh * N,
   // then (as floats) their fp32 best scores at amb + BH + BH * N + bh * N
   extern __shared__ unsigned char smem_raw[];
-  RsSmem& s = *reinterpret_cast<RsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                         ~uintptr_t(1023));
+  using Cfg = RsCfg<kS>;
+  constexpr int kQStages = Cfg::kQStages;
+  RsSmem<kS>& s = *reinterpret_cast<RsSmem<kS>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x / G_h, c0 = blockIdx.x % G_h;
   const int nqt = (N + 127) / 128;
@@ -277,7 +381,8 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tbase + lane_off + slot * 256, tP = tS + 128, tO = tS + 192;
-    float4* bb = s.bbuf[et];
+    float4* bb = s.bbuf[0][et];
+    constexpr int kSlotStride = kSoftThreads * 8;   // float4s from one block copy slot to the next
     const int sw = et & 7;
     bool ok = true;
     // v~ (fp32 in global memory) -> bf16 rows in the MMA's 128B-swizzled layout; rows from m
@@ -392,6 +497,7 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       if (lane == 0) mbar_arrive(&s.q_empty[st]);   // this warp is done with the tile
       const bool live = ok && n < N;
       RowTop top;
+      Top3Blocks top3;
       float mref = -INFINITY, lsum = 0.f;
       for (int c = 0; c < nch; ++c, ++g) {
         if (ok && !mbar_wait(&s.s_full[slot], g & 1)) ok = false;
@@ -409,11 +515,21 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
 #pragma unroll
           for (int i = 0; i < BN; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
         }
-        // the running best over 32-score blocks; the chunk maximum is the blocks' maximum
+        // the running best over 32-score blocks (s = 2: the three best blocks); the chunk
+        // maximum is the blocks' maximum
         float tm = -INFINITY;
 #pragma unroll
-        for (int b = 0; b < BN / 32; ++b)
-          if (b * 32 < nvalid) tm = fmaxf(tm, top_block(top, v + 32 * b, c * BN + b * 32, bb, sw));
+        for (int b = 0; b < BN / 32; ++b) {
+          if (b * 32 < nvalid) {
+            if constexpr (kS == 1) {
+              tm = fmaxf(tm, top_block(top, v + 32 * b, c * BN + b * 32, bb, sw));
+            } else {
+              const float mb = block_max32(v + 32 * b);
+              tm = fmaxf(tm, mb);
+              top3_block(top3, v + 32 * b, mb, c * BN + b * 32, bb, kSlotStride, sw);
+            }
+          }
+        }
         const float xm = tm * cs;
         const bool need = (c == 0) || (xm > mref + kLazy);
         const float f = (c > 0 && need) ? ex2(mref - xm) : 1.f;
@@ -470,14 +586,29 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.p_full[slot]);
       }
-      // the route: exact when the best beats the runner-up by more than 2E
-      const Cand cd = finish_top(top, bb, sw);
-      const bool ambiguous = live && !(cd.v1 - cd.v2 > twoE);
-      if (live) {
-        route[(size_t)bh * N + n] = cd.i1;
-        if (hist && !ambiguous && cd.i1 >= 0 && cd.i1 < m)
-          atomicAdd(&hist[((size_t)bh * m + cd.i1) * ((N + kBucketChunk - 1) / kBucketChunk) +
-                          n / kBucketChunk], 1);
+      // the route: exact when the best beats the runner-up by more than 2E (s = 2: when
+      // both the first and the second gap exceed 2E); `keep` is the fp32 score of the
+      // s-th route, the fix-up's screening reference
+      bool ambiguous;
+      float keep;
+      if constexpr (kS == 1) {
+        const Cand cd = finish_top(top, bb, sw);
+        ambiguous = live && !(cd.v1 - cd.v2 > twoE);
+        keep = cd.v1;
+        if (live) {
+          route[(size_t)bh * N + n] = cd.i1;
+          if (hist && !ambiguous && cd.i1 >= 0 && cd.i1 < m)
+            atomicAdd(&hist[((size_t)bh * m + cd.i1) * ((N + kBucketChunk - 1) / kBucketChunk) +
+                            n / kBucketChunk], 1);
+        }
+      } else {
+        const Top3 t3 = finish_top3(top3, bb, kSlotStride, sw);
+        ambiguous = live && !(t3.v[0] - t3.v[1] > twoE && t3.v[1] - t3.v[2] > twoE);
+        keep = t3.v[1];
+        if (live) {
+          route[((size_t)bh * N + n) * 2] = t3.i[0];
+          route[((size_t)bh * N + n) * 2 + 1] = t3.i[1];
+        }
       }
       const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
       if (am) {
@@ -487,7 +618,7 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         if (ambiguous) {
           const int pos = base + __popc(am & ((1u << lane) - 1u));
           hids[pos] = n;
-          hbest[pos] = cd.v1;
+          hbest[pos] = keep;
         }
       }
       prev_n = live ? n : -1;
@@ -511,13 +642,19 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
 
 }  // namespace
 
-bool route_shared_tc_supported(int d, int m) { return d == 64 && m >= 1 && m <= kMaxM; }
+bool route_shared_tc_supported(int d, int m, int s) {
+  if (d != 64 || m < 1 || m < s) return false;
+  if (s == 1) return m <= RsCfg<1>::kMaxM;
+  if (s == 2) return m <= RsCfg<2>::kMaxM;
+  return false;
+}
 
 cudaError_t launch_route_shared_tc(const bf16* q, const bf16* q_tilde, const float* v_tilde,
                                    int BH, int N, int m, int num_sms, int shared_temp,
                                    int o_bf16, int32_t* route, float* shared_lse, void* shared_o,
                                    int* amb, int* status, int* hist, cudaStream_t st,
-                                   bool prezeroed) {
+                                   bool prezeroed, int s) {
+  if (!route_shared_tc_supported(64, m, s)) return cudaErrorInvalidValue;
   const int nch = (m + BN - 1) / BN;
   CUtensorMap mq, mqt;
   if (!make_tmap_rows64(&mq, q, (uint64_t)N, (uint64_t)BH, 128) ||
@@ -526,9 +663,10 @@ cudaError_t launch_route_shared_tc(const bf16* q, const bf16* q_tilde, const flo
   const int nqt = (N + 127) / 128;
   int G_h = std::max(1, (num_sms + BH - 1) / BH);
   G_h = std::min(G_h, nqt);
-  const size_t smem = sizeof(RsSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(route_shared_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (s > 1) hist = nullptr;   // the bucket stage counts the N * s entries itself
+  const size_t smem = (s == 1 ? sizeof(RsSmem<1>) : sizeof(RsSmem<2>)) + 1024;
+  auto kern = s == 1 ? route_shared_tc_kernel<1> : route_shared_tc_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (!prezeroed && (e = cudaMemsetAsync(amb, 0, (size_t)BH * sizeof(int), st)) != cudaSuccess)
     return e;
@@ -538,12 +676,12 @@ cudaError_t launch_route_shared_tc(const bf16* q, const bf16* q_tilde, const flo
   }
   // shared logits in log2 units: log2(e) / sqrt(64), or log2(e) / 64 (the official code's)
   const float cs = shared_temp ? 0.022542110013890052f : 0.18033688011112042f;
-  e = launch_pdl(route_shared_tc_kernel, dim3((unsigned)(BH * G_h)), dim3(kThreads), smem, st, mq,
-                 mqt, v_tilde, N, m, nch, G_h, cs, o_bf16, route, shared_lse, shared_o, amb,
-                 status, hist);
+  e = launch_pdl(kern, dim3((unsigned)(BH * G_h)), dim3(kThreads), smem, st, mq, mqt, v_tilde, N,
+                 m, nch, G_h, cs, o_bf16, route, shared_lse, shared_o, amb, status, hist);
   count_launch();
   if (e != cudaSuccess) return e;
-  return launch_route_fixup(q, q_tilde, BH, N, m, num_sms, route, amb, hist, st);
+  if (s == 1) return launch_route_fixup(q, q_tilde, BH, N, m, num_sms, route, amb, hist, st);
+  return launch_route_fixup_top(q, q_tilde, BH, N, m, s, num_sms, route, amb, st);
 }
 
 }  // namespace mita

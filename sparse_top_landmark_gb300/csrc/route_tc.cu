@@ -463,6 +463,105 @@ route_fixup_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde,
   }
 }
 
+// Exact top-s (s >= 2) re-routing of the queries route_shared_tc left ambiguous (its
+// fp32 route list had a gap within 2E).  Same staging as route_fixup_kernel; the stored
+// reference is the fp32 score of the s-th route, so every landmark of the exact top-s has
+// its fp32 dot here within 2E of it.  Each lane keeps the best s of its survivors (exact
+// products, ranked by (score desc, index asc)); s rounds of a warp-wide best-of-heads merge
+// give the list, best first.
+constexpr int kFixMaxS = 8;
+
+__device__ __forceinline__ void fix_insert(F2 (&lv)[kFixMaxS], int (&li)[kFixMaxS], int s, F2 x,
+                                           int j) {
+#pragma unroll
+  for (int t = kFixMaxS - 1; t > 0; --t) {
+    if (t < s) {
+      if (ranks_before(x, j, lv[t - 1], li[t - 1])) { lv[t] = lv[t - 1]; li[t] = li[t - 1]; }
+      else if (ranks_before(x, j, lv[t], li[t])) { lv[t] = x; li[t] = j; }
+    }
+  }
+  if (ranks_before(x, j, lv[0], li[0])) { lv[0] = x; li[0] = j; }
+}
+
+__global__ void __launch_bounds__(256)
+route_fixup_top_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde, int N, int m,
+                       int s, int per_head, const int* __restrict__ amb,
+                       int32_t* __restrict__ route) {
+  griddep_wait();
+  extern __shared__ __align__(16) unsigned char fix_raw[];
+  bf16* qt = reinterpret_cast<bf16*>(fix_raw);       // [m][kFixRow]
+  __shared__ float red[8];
+  const int bh = blockIdx.x / per_head, part = blockIdx.x % per_head;
+  const int count = amb[bh];
+  const size_t BHs = gridDim.x / per_head;
+  const int* hids = amb + BHs + (size_t)bh * N;
+  const float* hkeep = reinterpret_cast<const float*>(amb + BHs + BHs * N) + (size_t)bh * N;
+  if (count <= part * 8) return;                      // no query for this CTA
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bf16* qtb = q_tilde + (size_t)bh * m * 64;
+  float n2 = 0.f;
+  for (int t = threadIdx.x; t < m * 8; t += 256) {
+    const int i = t >> 3, c = t & 7;
+    const uint4 x = reinterpret_cast<const uint4*>(qtb + (size_t)i * 64)[c];
+    *reinterpret_cast<uint4*>(qt + i * kFixRow + c * 8) = x;
+    float f[8];
+    Vec<bf16>::load(reinterpret_cast<const bf16*>(&x), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) n2 = fmaf(f[e], f[e], n2);
+  }
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 4);
+  n2 = warp_max(n2);
+  if (lane == 0) red[warp] = n2;
+  __syncthreads();
+  float qt2 = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) qt2 = fmaxf(qt2, red[w]);
+  for (int w = part * 8 + warp; w < count; w += per_head * 8) {
+    const int n = hids[w];
+    if (n < 0 || n >= N) continue;
+    float qr[64];
+    load_row<bf16, 64>(q + ((size_t)bh * N + n) * 64, qr);
+    float qn2 = 0.f;
+#pragma unroll
+    for (int l = 0; l < 64; ++l) qn2 = fmaf(qr[l], qr[l], qn2);
+    const float keep = hkeep[w];
+    const float twoE = 2.f * err_gamma(64) * sqrtf(qn2) * sqrtf(qt2);
+    F2 lv[kFixMaxS];
+    int li[kFixMaxS];
+#pragma unroll
+    for (int t = 0; t < kFixMaxS; ++t) { lv[t] = F2{-INFINITY, 0.f}; li[t] = 0x7fffffff; }
+#pragma unroll 1
+    for (int i = lane; i < m; i += 32) {
+      float r[64];
+      load_row<bf16, 64>(qt + i * kFixRow, r);
+      float a = 0.f;
+#pragma unroll
+      for (int l = 0; l < 64; ++l) a = fmaf(qr[l], r[l], a);
+      if (a >= keep - twoE) fix_insert(lv, li, s, dot_f2<64, 64>(qr, r), i);
+    }
+    // s rounds: the best head over the lanes, which its lane then pops
+    for (int r = 0; r < s; ++r) {
+      F2 bv = lv[0];
+      int bi = li[0];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const F2 ov{__shfl_xor_sync(0xffffffffu, bv.hi, o), __shfl_xor_sync(0xffffffffu, bv.lo, o)};
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) route[((size_t)bh * N + n) * s + r] = bi;
+      if (li[0] == bi) {
+#pragma unroll
+        for (int t = 0; t < kFixMaxS - 1; ++t) { lv[t] = lv[t + 1]; li[t] = li[t + 1]; }
+        lv[kFixMaxS - 1] = F2{-INFINITY, 0.f};
+        li[kFixMaxS - 1] = 0x7fffffff;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 size_t route_tc_smem_bytes() { return sizeof(RouteSmem) + 1024; }
@@ -500,6 +599,21 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
   count_launch();
   if (e != cudaSuccess) return e;
   return launch_route_fixup(q, q_tilde, BH, N, m, num_sms, route, amb, hist, st);
+}
+
+cudaError_t launch_route_fixup_top(const bf16* q, const bf16* q_tilde, int BH, int N, int m,
+                                   int s, int num_sms, int32_t* route, const int* amb,
+                                   cudaStream_t st) {
+  if (s < 2 || s > kFixMaxS || s > m) return cudaErrorInvalidValue;
+  const int per_head = std::max(1, std::max(num_sms, 1) / BH);
+  const size_t fsm = (size_t)m * kFixRow * 2;
+  cudaError_t e = cudaFuncSetAttribute(route_fixup_top_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(route_fixup_top_kernel, dim3((unsigned)(BH * per_head)), dim3(256), fsm, st, q,
+                 q_tilde, N, m, s, per_head, amb, route);
+  count_launch();
+  return e;
 }
 
 cudaError_t launch_route_fixup(const bf16* q, const bf16* q_tilde, int BH, int N, int m,

@@ -28,6 +28,16 @@ CASES = {
                                    index=31), 3),
     "d128_bf16_s2": (W.custom("d128_bf16", 1, 2, 2048, 128, "bf16", 1, 2048, 16, 64,
                               index=32), 2),
+    # bf16, d = 64, s = 2: the tensor-core route (m <= 256) and expert partials
+    "vit_bf16_s2": (W.WORKLOADS["vit_s_14x14"], 2),
+    "seg_bf16_s2": (W.WORKLOADS["seg_32x32"], 2),
+    "ragged_bf16_m200_s2": (W.custom("ragged_bf16", 2, 2, 3000, 64, "bf16", 1, 3000, 200, 40,
+                                     index=34), 2),
+    "m256_bf16_s2": (W.custom("m256_bf16", 1, 2, 4096, 64, "bf16", 1, 4096, 256, 24,
+                              index=35), 2),
+    # m > 256: the SIMT route, then the tensor-core expert partials
+    "m300_bf16_s2": (W.custom("m300_bf16", 1, 1, 3000, 64, "bf16", 1, 3000, 300, 20,
+                              index=36), 2),
 }
 NAMES = list(CASES)
 
@@ -154,6 +164,11 @@ def test_route_top_s_equal_landmarks_take_lowest_index():
         r = mita.mita_route(dev(q), dev(qt), s=s)
         orr, _ = oracle.route(q, qt, s)
         assert torch.equal(r.cpu(), orr)
+    # with the shared partial, s = 2 routes on the tensor cores (ties go to the exact fix-up)
+    vt = torch.randn((w.B, w.H, w.m, w.d), generator=torch.Generator().manual_seed(3))
+    r, _, _ = mita.mita_route(dev(q), dev(qt), dev(vt), s=2, shared=True)
+    orr, _ = oracle.route(q, qt, 2)
+    assert torch.equal(r.cpu(), orr)
     assert mita.get_last_device_error() == 0
 
 
