@@ -293,10 +293,9 @@ cudaError_t route_dispatch(const T* q, const T* qt, const float* vt, int BH, int
                              ds->status, hist, st, prezeroed);
     }
     if (route_shared_uses_tc<T>(d, m, s, lse, so)) {
-      if (counted) *counted = hist != nullptr && s == 1;   // s > 1: the bucket stage counts
+      if (counted) *counted = hist != nullptr;
       return launch_route_shared_tc(q, qt, vt, BH, N, m, ds->num_sms, temp, 0, route, lse, so,
-                                    static_cast<int*>(ws), ds->status, s == 1 ? hist : nullptr,
-                                    st, prezeroed, s);
+                                    static_cast<int*>(ws), ds->status, hist, st, prezeroed, s);
     }
   }
   return launch_route<T>(q, qt, vt, BH, N, d, m, s, route, lse, so, st, temp);
@@ -509,12 +508,14 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
     // shared branch, s = 2 and m <= 256 route on the tensor cores, the shared partial's output
     // in bf16
     int so_bf16 = 0;
+    bool counted = false;       // the tensor-core route counts the bucket histogram too
     if constexpr (std::is_same<T, bf16>::value) {
       if (!routed && route_shared_tc_supported(d, m, s)) {
         so_bf16 = 1;
+        counted = true;
         MITA_CUDA(launch_route_shared_tc(q, qt, vt, BH, N, m, ds->num_sms, temp, 1, route, lse, so,
-                                         reinterpret_cast<int*>(ws + L.rt), ds->status, nullptr,
-                                         st, true, s),
+                                         reinterpret_cast<int*>(ws + L.rt), ds->status,
+                                         reinterpret_cast<int*>(ws + L.bk), st, true, s),
                   "route launch");
       }
     }
@@ -523,7 +524,7 @@ int forward_impl(const T* q, const T* k, const T* v, int B, int H, int N, int d,
                                   routed ? nullptr : so, ds, ws + L.rt, st, nullptr, nullptr, true,
                                   temp),
                 "route launch");
-    MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, false, s),
+    MITA_CUDA(launch_bucket(route, BH, N, m, ws + L.bk, off, qidx, ds->status, st, counted, s),
               "bucket launch");
     if constexpr (std::is_same<T, bf16>::value) {
       if (expert_tc_supported(d, m, topk)) {

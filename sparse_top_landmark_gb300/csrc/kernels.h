@@ -151,15 +151,16 @@ cudaError_t launch_route_fixup(const __nv_bfloat16* q, const __nv_bfloat16* q_ti
                                int N, int m, int num_sms, int32_t* route, const int* amb,
                                int* hist, cudaStream_t st);
 // exact top-s re-routing (2 <= s <= 8) of the queries route_shared_tc (s = 2) left on the
-// ambiguous lists in `amb`; route is [BH*N][s]
+// ambiguous lists in `amb`; route is [BH*N][s]; their N*s entries counted into `hist`
+// ([BH][m][ceil(N*s / kBucketChunk)]) if not null
 cudaError_t launch_route_fixup_top(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde, int BH,
                                    int N, int m, int s, int num_sms, int32_t* route,
-                                   const int* amb, cudaStream_t st);
+                                   const int* amb, int* hist, cudaStream_t st);
 // Routing (s = 1, or the best two with s = 2) together with the shared branch's partial from
 // the same logits: per query the route ([BH*N][s], best first), shared_lse (natural
 // log-sum-exp of the scaled shared logits) and shared_o = the normalised shared output,
 // [BH*N][64] in bf16 (o_bf16 = 1) or fp32.  `amb` and `hist` as for launch_route_tc (the
-// fix-up runs inside; with s = 2 `hist` is ignored: the bucket stage counts the N*s entries).
+// fix-up runs inside; with s = 2 `hist` counts the N*s entries, [BH][m][ceil(2N / chunk)]).
 bool route_shared_tc_supported(int d, int m, int s = 1);
 cudaError_t launch_route_shared_tc(const __nv_bfloat16* q, const __nv_bfloat16* q_tilde,
                                    const float* v_tilde, int BH, int N, int m, int num_sms,

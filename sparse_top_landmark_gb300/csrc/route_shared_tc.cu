@@ -608,6 +608,16 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         if (live) {
           route[((size_t)bh * N + n) * 2] = t3.i[0];
           route[((size_t)bh * N + n) * 2 + 1] = t3.i[1];
+          // the bucket stage's counts of its N * 2 entries (entry 2n + r)
+          if (hist && !ambiguous) {
+            const long long nck = ((long long)N * 2 + kBucketChunk - 1) / kBucketChunk;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int e = t3.i[r];
+              if (e >= 0 && e < m)
+                atomicAdd(&hist[((size_t)bh * m + e) * nck + (2LL * n + r) / kBucketChunk], 1);
+            }
+          }
         }
       }
       const unsigned am = __ballot_sync(0xffffffffu, ambiguous);
@@ -663,7 +673,6 @@ cudaError_t launch_route_shared_tc(const bf16* q, const bf16* q_tilde, const flo
   const int nqt = (N + 127) / 128;
   int G_h = std::max(1, (num_sms + BH - 1) / BH);
   G_h = std::min(G_h, nqt);
-  if (s > 1) hist = nullptr;   // the bucket stage counts the N * s entries itself
   const size_t smem = (s == 1 ? sizeof(RsSmem<1>) : sizeof(RsSmem<2>)) + 1024;
   auto kern = s == 1 ? route_shared_tc_kernel<1> : route_shared_tc_kernel<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -671,7 +680,7 @@ cudaError_t launch_route_shared_tc(const bf16* q, const bf16* q_tilde, const flo
   if (!prezeroed && (e = cudaMemsetAsync(amb, 0, (size_t)BH * sizeof(int), st)) != cudaSuccess)
     return e;
   if (hist && !prezeroed) {
-    const size_t nh = (size_t)BH * m * ((N + kBucketChunk - 1) / kBucketChunk);
+    const size_t nh = (size_t)BH * m * (((size_t)N * s + kBucketChunk - 1) / kBucketChunk);
     if ((e = cudaMemsetAsync(hist, 0, nh * sizeof(int), st)) != cudaSuccess) return e;
   }
   // shared logits in log2 units: log2(e) / sqrt(64), or log2(e) / 64 (the official code's)
@@ -681,7 +690,7 @@ cudaError_t launch_route_shared_tc(const bf16* q, const bf16* q_tilde, const flo
   count_launch();
   if (e != cudaSuccess) return e;
   if (s == 1) return launch_route_fixup(q, q_tilde, BH, N, m, num_sms, route, amb, hist, st);
-  return launch_route_fixup_top(q, q_tilde, BH, N, m, s, num_sms, route, amb, st);
+  return launch_route_fixup_top(q, q_tilde, BH, N, m, s, num_sms, route, amb, hist, st);
 }
 
 }  // namespace mita

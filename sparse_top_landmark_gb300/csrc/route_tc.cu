@@ -486,7 +486,7 @@ __device__ __forceinline__ void fix_insert(F2 (&lv)[kFixMaxS], int (&li)[kFixMax
 __global__ void __launch_bounds__(256)
 route_fixup_top_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_tilde, int N, int m,
                        int s, int per_head, const int* __restrict__ amb,
-                       int32_t* __restrict__ route) {
+                       int32_t* __restrict__ route, int* __restrict__ hist) {
   griddep_wait();
   extern __shared__ __align__(16) unsigned char fix_raw[];
   bf16* qt = reinterpret_cast<bf16*>(fix_raw);       // [m][kFixRow]
@@ -551,7 +551,12 @@ route_fixup_top_kernel(const bf16* __restrict__ q, const bf16* __restrict__ q_ti
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
       }
-      if (lane == 0) route[((size_t)bh * N + n) * s + r] = bi;
+      if (lane == 0) {
+        route[((size_t)bh * N + n) * s + r] = bi;
+        if (hist && bi >= 0 && bi < m)   // the routing kernel left this query uncounted
+          atomicAdd(&hist[((size_t)bh * m + bi) * (((long long)N * s + kBucketChunk - 1) / kBucketChunk) +
+                          ((long long)n * s + r) / kBucketChunk], 1);
+      }
       if (li[0] == bi) {
 #pragma unroll
         for (int t = 0; t < kFixMaxS - 1; ++t) { lv[t] = lv[t + 1]; li[t] = li[t + 1]; }
@@ -602,7 +607,7 @@ cudaError_t launch_route_tc(const bf16* q, const bf16* q_tilde, int BH, int N, i
 }
 
 cudaError_t launch_route_fixup_top(const bf16* q, const bf16* q_tilde, int BH, int N, int m,
-                                   int s, int num_sms, int32_t* route, const int* amb,
+                                   int s, int num_sms, int32_t* route, const int* amb, int* hist,
                                    cudaStream_t st) {
   if (s < 2 || s > kFixMaxS || s > m) return cudaErrorInvalidValue;
   const int per_head = std::max(1, std::max(num_sms, 1) / BH);
@@ -611,7 +616,7 @@ cudaError_t launch_route_fixup_top(const bf16* q, const bf16* q_tilde, int BH, i
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm);
   if (e != cudaSuccess) return e;
   e = launch_pdl(route_fixup_top_kernel, dim3((unsigned)(BH * per_head)), dim3(256), fsm, st, q,
-                 q_tilde, N, m, s, per_head, amb, route);
+                 q_tilde, N, m, s, per_head, amb, route, hist);
   count_launch();
   return e;
 }
