@@ -649,28 +649,15 @@ size_t small_smem_bytes(int N) {
          (size_t)kSmallRows * 256 * 4 + (size_t)kSmallRows * 32 * 8 + 64;
 }
 
-// One landmark row of landmark_small_kernel, on one warp: the exact top-k of the row's N fp32
-// scores (key j at Sw[j * kSmallSP]), then the softmax weights in place of the scores.  Lane
-// l holds keys l + 32 i for i < NI (32 NI >= N) in registers.
-template <typename T, int D, int NI>
-__device__ __forceinline__ void small_row(float* Sw, const float* qd, const T* kb, int N, int topk,
-                                          long long row, float km2, int* hist, int* bjw,
-                                          unsigned* sw, float* lsum_out, const LandmarkWs& ws,
-                                          int32_t* __restrict__ topk_idx, int lane) {
-  // the scores as order keys (fkey is a bijection: fkey_inv gives the score back)
-  uint32_t u[NI];
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int j = lane + 32 * i;
-    const float x = j < N ? Sw[(size_t)j * kSmallSP] : -INFINITY;
-    mx = fmaxf(mx, x);
-    u[i] = j < N ? fkey(x) : 0u;             // 0: below every key
-  }
-  // tau: the topk-th largest order key, bit by bit from the top (the largest prefix that
-  // at least topk keys reach).  Bits 31..16 count every key; the keys sharing the 16-bit
-  // prefix found are then the only ones the low bits can still order, so they are listed:
-  // up to 32 of them are ranked directly, up to 256 finish the bit search alone.
+// The topk-th largest of a warp's n order keys (lane l holds items l + 32 i, i < NI; 0 marks
+// no item: below every key), bit by bit from the top (the largest prefix that at least topk
+// keys reach).  Bits 31..16 count every key; the keys sharing the 16-bit prefix found are then
+// the only ones the low bits can still order, so they are listed in `al` (256 words of
+// scratch): up to 32 of them are ranked directly, up to 256 finish the bit search alone.
+template <int NI>
+__device__ __forceinline__ uint32_t warp_kth_key(const uint32_t (&u)[NI], int n, int topk,
+                                                 uint32_t* al, int lane) {
+  const int N = n;
   uint32_t prefix = 0u;
 #pragma unroll 1
   for (int b = 31; b >= 16; --b) {
@@ -686,7 +673,6 @@ __device__ __forceinline__ void small_row(float* Sw, const float* qd, const T* k
 #pragma unroll
     for (int i = 0; i < NI; ++i) c += (u[i] >> 16) > top ? 1 : 0;
     const int need = topk - (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
-    uint32_t* al = reinterpret_cast<uint32_t*>(hist);   // [256] keys sharing the prefix
     int na16 = 0;
     const unsigned lt16 = (1u << lane) - 1u;
 #pragma unroll
@@ -734,6 +720,28 @@ __device__ __forceinline__ void small_row(float* Sw, const float* qd, const T* k
     }
     __syncwarp();
   }
+  return prefix;
+}
+
+// One landmark row of landmark_small_kernel, on one warp: the exact top-k of the row's N fp32
+// scores (key j at Sw[j * kSmallSP]), then the softmax weights in place of the scores.  Lane
+// l holds keys l + 32 i for i < NI (32 NI >= N) in registers.
+template <typename T, int D, int NI>
+__device__ __forceinline__ void small_row(float* Sw, const float* qd, const T* kb, int N, int topk,
+                                          long long row, float km2, int* hist, int* bjw,
+                                          unsigned* sw, float* lsum_out, const LandmarkWs& ws,
+                                          int32_t* __restrict__ topk_idx, int lane) {
+  // the scores as order keys (fkey is a bijection: fkey_inv gives the score back)
+  uint32_t u[NI];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int j = lane + 32 * i;
+    const float x = j < N ? Sw[(size_t)j * kSmallSP] : -INFINITY;
+    mx = fmaxf(mx, x);
+    u[i] = j < N ? fkey(x) : 0u;             // 0: below every key
+  }
+  const uint32_t prefix = warp_kth_key<NI>(u, N, topk, reinterpret_cast<uint32_t*>(hist), lane);
   const float tau = fkey_inv(prefix);
   float qn2 = 0.f;
   for (int l = lane; l < D; l += 32) qn2 = fmaf(qd[l], qd[l], qn2);
