@@ -576,12 +576,15 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
       if (ok && !mbar_wait(&s.s_full[slot], g & 1)) ok = false;
       tc_fence_after();
       const int nvalid = c < nrc ? min(BN, topk - c * BN) : min(BN, m - (c - nrc) * BN);
+      // the chunk's scores, with the maximum of each 32-column block from the reducing load
       float v[BN];
+      float q4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (ok) {
-        tmem_ld64(tS, v);
-        tmem_ld64(tS + 64, v + 64);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) q4[b] = tmem_ld32_max(tS + 32 * b, v + 32 * b);
         tmem_ld_wait();
         tmem_fence_regs<BN>(v);
+        tmem_fence_regs<4>(q4);
       }
       tc_fence_before();
       __syncwarp();
@@ -601,13 +604,17 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap map_qg, const __grid_consta
           for (int i = 0; i < 32; ++i) v[32 * w4 + i] = ((bits >> i) & 1u) ? v[32 * w4 + i] : -INFINITY;
         }
       }
-      // row maximum with four independent chains
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // row maximum: the loads' block maxima, or (a ragged chunk, or keys masked out) four
+      // independent chains over the valid entries
+      float tm = fmaxf(fmaxf(q4[0], q4[1]), fmaxf(q4[2], q4[3]));
+      if (kMasked || nvalid < BN) {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < BN; i += 8)
+        for (int i = 0; i < BN; i += 8)
 #pragma unroll
-        for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
-      const float tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
+        tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      }
       const float csc = c >= nrc ? cs_shared : cs;  // the chunk's logit scale, log2 units
       const float xm = tm * csc;
       const bool need = (c == 0) || (xm > mref + kLazy);

@@ -287,27 +287,31 @@ lm_sweep_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_constan
       const int kbase = j0 + j * BN;
       const int nvalid = min(BN, j1 - kbase);
       const bool full = nvalid == BN;
+      // the tile's scores, with the maximum of each 32-column block from the reducing load
       float v[BN];
+      float q4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (ok) {
-        tmem_ld64(tS, v);
-        tmem_ld64(tS + 64, v + 64);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) q4[b] = tmem_ld32_max(tS + 32 * b, v + 32 * b);
         tmem_ld_wait();
         tmem_fence_regs<BN>(v);
+        tmem_fence_regs<4>(q4);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.s_free[slot]);   // the next S may overwrite these columns
+      // the tile's largest raw score (a ragged tile: over its valid keys only)
+      float tm = fmaxf(fmaxf(q4[0], q4[1]), fmaxf(q4[2], q4[3]));
       if (!full) {
 #pragma unroll
         for (int i = 0; i < BN; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four independent chains
+#pragma unroll
+        for (int i = 0; i < BN; i += 8)
+#pragma unroll
+          for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
+        tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
-      // the tile's largest raw score
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four independent chains
-#pragma unroll
-      for (int i = 0; i < BN; i += 8)
-#pragma unroll
-        for (int a = 0; a < 4; ++a) m4[a] = max3(m4[a], v[i + 2 * a], v[i + 2 * a + 1]);
-      const float tm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       // every tile's maximum raw score goes out; the threshold pass takes the
       // k-th largest of the row's
       if (live_row) tmax[j] = tm;
@@ -672,11 +676,15 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
       const int nvalid = min(BN, j1 - kbase);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
+        // two 32-score blocks, each with its maximum from the reducing load
         float v[64];
+        float bmx[2] = {-INFINITY, -INFINITY};
         if (ok) {
-          tmem_ld64(tS + h * 64, v);
+          bmx[0] = tmem_ld32_max(tS + h * 64, v);
+          bmx[1] = tmem_ld32_max(tS + h * 64 + 32, v + 32);
           tmem_ld_wait();
           tmem_fence_regs<64>(v);
+          tmem_fence_regs<2>(bmx);
         }
         if (h == 1) {
           tc_fence_before();
@@ -689,16 +697,9 @@ lm_collect_kernel(const __grid_constant__ CUtensorMap map_qt, const __grid_const
           const float* vv = v + cc;
           const int c0 = h * 64 + cc;
           // most blocks of 32 hold no candidate for any row of the warp: screen with
-          // the block maximum (half an operation per score) before building the mask
-          float bm[4];
-#pragma unroll
-          for (int a = 0; a < 4; ++a) bm[a] = max3(vv[8 * a], vv[8 * a + 1], vv[8 * a + 2]);
-#pragma unroll
-          for (int a = 0; a < 4; ++a) bm[a] = max3(bm[a], vv[8 * a + 3], vv[8 * a + 4]);
-#pragma unroll
-          for (int a = 0; a < 4; ++a) bm[a] = max3(bm[a], vv[8 * a + 5], vv[8 * a + 6]);
-          const float bmax = fmaxf(max3(max3(bm[0], bm[1], bm[2]), max3(bm[3], vv[7], vv[15]), vv[23]),
-                                   vv[31]);
+          // the block maximum (from the load itself; past the split's end it may count
+          // keys outside it, which the mask below drops) before building the mask
+          const float bmax = bmx[cc / 32];
           if (!__any_sync(0xffffffffu, bmax >= thr)) continue;
           // bitmask of the scores at or above the threshold (branch-free), then
           // visit only its set bits

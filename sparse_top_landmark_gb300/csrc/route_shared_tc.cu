@@ -108,19 +108,13 @@ __device__ __forceinline__ void load_swizzled_row(const bf16* tile, int r, float
 
 // Running best over blocks of 32 scores (as in route_tc.cu): per block only its maximum;
 // the block holding the running best is copied to shared memory, every other block gives
-// its maximum to v2c.  Returns the block's maximum (the softmax reuses it).
+// its maximum (mb, read by the loading instruction) to v2c.  Returns mb.
 struct RowTop {
   float v1 = -INFINITY, v2c = -INFINITY;
   int bb0 = 0;
 };
-__device__ __forceinline__ float top_block(RowTop& t, const float* v, int i0, float4* bb, int sw) {
-  float a[11];
-#pragma unroll
-  for (int i = 0; i < 10; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
-  a[10] = fmaxf(v[30], v[31]);
-  const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]);
-  const float b2 = max3f(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
-  const float mb = fmaxf(max3f(b0, b1, b2), b3);
+__device__ __forceinline__ float top_block(RowTop& t, const float* v, float mb, int i0,
+                                           float4* bb, int sw) {
   const bool up = mb > t.v1;
   t.v2c = fmaxf(t.v2c, up ? t.v1 : mb);
   t.v1 = up ? mb : t.v1;
@@ -503,17 +497,22 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         if (ok && !mbar_wait(&s.s_full[slot], g & 1)) ok = false;
         tc_fence_after();
         const int nvalid = min(BN, m - c * BN);
+        // warp-collective loads (no lane may skip them), with each 32-column block's maximum
         float v[BN];
-        tmem_ld64(tS, v);            // warp-collective: no lane may skip it
-        tmem_ld64(tS + 64, v + 64);
+        float q4[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) q4[b] = tmem_ld32_max(tS + 32 * b, v + 32 * b);
         tmem_ld_wait();
         tmem_fence_regs<BN>(v);
+        tmem_fence_regs<4>(q4);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.s_free[slot]);   // the next S may overwrite these columns
-        if (nvalid < BN) {
+        if (nvalid < BN) {           // a ragged chunk: its blocks' maxima over valid entries
 #pragma unroll
           for (int i = 0; i < BN; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) q4[b] = block_max32(v + 32 * b);
         }
         // the running best over 32-score blocks (s = 2: the three best blocks); the chunk
         // maximum is the blocks' maximum
@@ -522,11 +521,10 @@ route_shared_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         for (int b = 0; b < BN / 32; ++b) {
           if (b * 32 < nvalid) {
             if constexpr (kS == 1) {
-              tm = fmaxf(tm, top_block(top, v + 32 * b, c * BN + b * 32, bb, sw));
+              tm = fmaxf(tm, top_block(top, v + 32 * b, q4[b], c * BN + b * 32, bb, sw));
             } else {
-              const float mb = block_max32(v + 32 * b);
-              tm = fmaxf(tm, mb);
-              top3_block(top3, v + 32 * b, mb, c * BN + b * 32, bb, kSlotStride, sw);
+              tm = fmaxf(tm, q4[b]);
+              top3_block(top3, v + 32 * b, q4[b], c * BN + b * 32, bb, kSlotStride, sw);
             }
           }
         }

@@ -98,19 +98,22 @@ struct RowTop {
 // stored at chunk c ^ sw (sw = thread % 8), so a warp's 16-byte accesses spread
 // over all banks.  The copy goes through shared memory (a few stores, only when
 // the block improves the best) instead of 32 register selects per block.
-__device__ __forceinline__ void top_block(RowTop& t, float* v, int i0, int nvalid, float4* bb,
-                                          int sw) {
-  if (nvalid < 32) {                 // ragged last block (uniform across the warp)
+// mb_hw: the block's maximum from the reducing tensor-memory load; a ragged last block (its
+// columns past m hold zeros, uniform across the warp) recomputes it over its valid entries.
+__device__ __forceinline__ void top_block(RowTop& t, float* v, float mb_hw, int i0, int nvalid,
+                                          float4* bb, int sw) {
+  float mb = mb_hw;
+  if (nvalid < 32) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = i < nvalid ? v[i] : -INFINITY;
-  }
-  float a[11];
+    float a[11];
 #pragma unroll
-  for (int i = 0; i < 10; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
-  a[10] = fmaxf(v[30], v[31]);
-  const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]);
-  const float b2 = max3f(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
-  const float mb = fmaxf(max3f(b0, b1, b2), b3);
+    for (int i = 0; i < 10; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+    a[10] = fmaxf(v[30], v[31]);
+    const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]);
+    const float b2 = max3f(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+    mb = fmaxf(max3f(b0, b1, b2), b3);
+  }
   const bool up = mb > t.v1;
   t.v2c = fmaxf(t.v2c, up ? t.v1 : mb);
   t.v1 = up ? mb : t.v1;
@@ -320,15 +323,15 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
         for (int p = 0; p < kMaxW / 64; ++p) {
           if (p * 64 < W) {
+            // the two 32-score blocks of this piece, each with its maximum
             float v[64];
+            float bmx[2] = {-INFINITY, -INFINITY};
             if (ok) {
-              if (W - p * 64 >= 64) {
-                tmem_ld64(tb + p * 64, v);
-              } else {
-                tmem_ld32(tb + p * 64, v);
-              }
+              bmx[0] = tmem_ld32_max(tb + p * 64, v);
+              if (W - p * 64 >= 64) bmx[1] = tmem_ld32_max(tb + p * 64 + 32, v + 32);
               tmem_ld_wait();
               tmem_fence_regs<64>(v);
+              tmem_fence_regs<2>(bmx);
             }
             if (p * 64 + 64 >= W) {                  // the buffer may be overwritten now
               tc_fence_before();
@@ -339,7 +342,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
               for (int cc = 0; cc < 64; cc += 32) {
                 const int i0 = ch * W + p * 64 + cc;
-                if (p * 64 + cc < W && i0 < m) top_block(top, v + cc, i0, min(m - i0, 32), bb, sw);
+                if (p * 64 + cc < W && i0 < m)
+                  top_block(top, v + cc, bmx[cc / 32], i0, min(m - i0, 32), bb, sw);
               }
             }
           }
