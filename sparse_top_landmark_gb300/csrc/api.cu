@@ -641,6 +641,16 @@ int backward_impl(const T* q, const T* k, const T* v, const T* dout, int B, int 
   const size_t o_lse = take(BHN * 4), o_dn = take(BHN * 4);
   const size_t o_la = take((size_t)BH * m * 4), o_cv = take((size_t)BH * m * 4);
   const size_t o_dqt = take((size_t)BH * m * d * 4), o_dvt = take((size_t)BH * m * d * 4);
+  // bf16 with d = 64: the selections are recomputed by the tensor-core route and expert
+  // kernels where they apply, and the gradient passes run on the tensor cores
+  const bool mma = std::is_same<T, bf16>::value && d == 64;
+  const bool tc_expert = mma && expert_tc_supported(d, m, topk);
+  const bool tc_route = std::is_same<T, bf16>::value &&
+                        (routed ? s == 1 && route_tc_supported(d, m) : route_shared_tc_supported(d, m, s));
+  const size_t o_v16 = mma ? take((size_t)BH * m * 64 * 2) : 0;
+  const size_t o_dv16 = mma ? take((size_t)BH * m * 64 * 2) : 0;
+  const size_t o_rws = tc_route ? take(route_ws_bytes(BH, N)) : 0;
+  const size_t o_tcx = tc_expert ? take(expert_tc_partials_ws_bytes(BH, N, m, topk, s)) : 0;
   void* wsv = nullptr;
   MITA_TRY(workspace(o, st, &wsv));
   char* ws = static_cast<char*>(wsv);
@@ -668,14 +678,22 @@ int backward_impl(const T* q, const T* k, const T* v, const T* dout, int B, int 
   lw.lse_out = reinterpret_cast<float*>(ws + o_la);   // each landmark's softmax normaliser
   MITA_CUDA(launch_landmark<T>(qt, k, v, BH, N, d, m, topk, plan, lw, ti, vt, ds->status, st),
             "landmark launch");
-  MITA_CUDA(launch_route<T>(q, qt, vt, BH, N, d, m, s, route, routed ? nullptr : sl,
-                            routed ? nullptr : so, st, temp),
+  MITA_CUDA(route_dispatch<T>(q, qt, vt, BH, N, d, m, s, route, routed ? nullptr : sl,
+                              routed ? nullptr : so, ds, tc_route ? ws + o_rws : nullptr, st,
+                              nullptr, nullptr, false, temp),
             "route launch");
   MITA_CUDA(launch_bucket(route, BH, N, m, ws + o_bk, off, qidx, ds->status, st, false, s),
             "bucket launch");
-  MITA_CUDA(launch_expert_partials<T>(q, k, v, ti, off, qidx, BH, N, d, m, topk, s, part,
-                                      ds->status, st),
-            "expert partials");
+  if constexpr (std::is_same<T, bf16>::value) {
+    if (tc_expert)
+      MITA_CUDA(launch_expert_tc_partials(q, k, v, ti, off, qidx, BH, N, m, topk, s,
+                                          ds->num_sms, ws + o_tcx, part, ds->status, st),
+                "expert partials");
+  }
+  if (!tc_expert)
+    MITA_CUDA(launch_expert_partials<T>(q, k, v, ti, off, qidx, BH, N, d, m, topk, s, part,
+                                        ds->status, st),
+              "expert partials");
   BwdArgs<T> a{};
   a.q = q; a.k = k; a.v = v; a.dout = dout; a.q_tilde = qt; a.v_tilde = vt;
   a.topk_idx = ti; a.bucket_off = off; a.bucket_qidx = qidx;
@@ -687,6 +705,10 @@ int backward_impl(const T* q, const T* k, const T* v, const T* dout, int B, int 
   a.lseA = reinterpret_cast<float*>(ws + o_la); a.cvt = reinterpret_cast<float*>(ws + o_cv);
   a.dqt = reinterpret_cast<float*>(ws + o_dqt); a.dvt = reinterpret_cast<float*>(ws + o_dvt);
   a.dq = dq; a.dk = dk; a.dv = dv; a.status = ds->status;
+  if (mma) {
+    a.vt16 = reinterpret_cast<bf16*>(ws + o_v16);
+    a.dvt16 = reinterpret_cast<bf16*>(ws + o_dv16);
+  }
   MITA_CUDA(launch_backward<T>(a, d, st), "backward launch");
   return MITA_OK;
 }

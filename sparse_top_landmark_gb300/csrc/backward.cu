@@ -14,7 +14,10 @@
 //   dv_j += sum_i A_ij dv~_i;  dS_ij = A_ij (dv~_i . v_j - dv~_i . v~_i);
 //   dk_j += sum_i dS_ij q~_i c;  dq~_i += sum_j dS_ij k_j c;  dq_t += dq~_i / |window_i|.
 //
-// Kernels (SIMT, fp32, gradients accumulated with atomics into fp32 buffers):
+// bf16 inputs with d = 64 run the three gradient passes (raw, shared, through v~) on the
+// tensor cores (backward_mma.cu: one query-major and one key-major launch per pass); every
+// other shape runs these SIMT kernels (fp32, gradients accumulated with atomics into fp32
+// buffers):
 //   bwd_stats_kernel     per query: lse_n and D_n from the shared partial and the s raw
 //                        partials (the forward's own kernels recompute those);
 //   (each landmark's softmax normaliser ln sum_j exp(q~_i . k_j c) comes from the
@@ -58,6 +61,12 @@ bwd_stats_kernel(const float* __restrict__ sh_lse, const float* __restrict__ sh_
   for (int t = 0; t < s; ++t) M = fmaxf(M, __shfl_sync(0xffffffffu, pl, t));
   constexpr int PER = (D + 31) / 32;
   const float wsh = sh ? exp2f((sh_lse[qi] - M) * kL2e) : 0.f;
+  if (Dn == nullptr) {   // the log-sum-exp only (D is summed by the gradient passes)
+    float z = wsh;
+    for (int t = 0; t < s; ++t) z += exp2f((__shfl_sync(0xffffffffu, pl, t) - M) * kL2e);
+    if (lane == 0) lse[qi] = M + logf(z);
+    return;
+  }
   float z = wsh, acc[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
@@ -424,6 +433,72 @@ bwd_pool_kernel(const float* __restrict__ dqt, int N, int D, int grid_h, int gri
 template <int D>
 size_t smem_bytes() { return sizeof(BwdSmem<D>); }
 
+__global__ void __launch_bounds__(256)
+to_bf16_kernel(const float* __restrict__ x, long long n, bf16* __restrict__ y) {
+  for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n; i += (long long)gridDim.x * 256)
+    y[i] = __float2bfloat16_rn(x[i]);
+}
+cudaError_t to_bf16(const float* x, long long n, bf16* y, cudaStream_t st) {
+  const long long blocks = std::min<long long>((n + 255) / 256, 4096);
+  to_bf16_kernel<<<(unsigned)std::max<long long>(blocks, 1), 256, 0, st>>>(x, n, y);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// The gradient passes on the tensor cores (bf16, d = 64), after bwd_stats.  With kRowSumD
+// each query's D (and each landmark's dv~ . v~) is summed as P dP over the same bf16 operands
+// the gradient launches use (launch kind 2), so the dS of a row sum to zero up to fp32
+// rounding; else D comes from the recomputed outputs (bwd_stats, bwd_vt_dot).
+constexpr bool kRowSumD = true;
+cudaError_t run_mma(const BwdArgs<bf16>& A, cudaStream_t st) {
+  const float c = 0.125f;   // 1 / sqrt(64)
+  const long long rows = (long long)A.BH * A.m;
+  cudaError_t e;
+  // routed pairs: each expert's bucket entries against its top-k rows
+  BwdPass p{};
+  p.q = A.q; p.g = A.dout; p.k = A.k; p.v = A.v; p.L = A.lse; p.D = A.Dn; p.Dacc = A.Dn;
+  p.dq = A.dq; p.dk = A.dk; p.dv = A.dv; p.c = c; p.BH = A.BH;
+  p.bucket_off = A.bucket_off; p.bucket_qidx = A.bucket_qidx; p.topk_idx = A.topk_idx;
+  p.N = A.N; p.m = A.m; p.topk = A.topk; p.NS = A.N * A.s; p.status = A.status;
+  // shared pairs: every query against the m landmarks (q~, v~) -> dq, dq~, dv~
+  BwdPass sp{};
+  sp.q = A.q; sp.g = A.dout; sp.k = A.q_tilde; sp.v = A.vt16; sp.L = A.lse; sp.D = A.Dn;
+  sp.Dacc = A.Dn; sp.dq = A.dq; sp.dk = A.dqt; sp.dv = A.dvt; sp.c = A.c_sh; sp.BH = A.BH;
+  sp.nq = A.N; sp.nk = A.m; sp.status = A.status;
+  if (!A.routed && (e = to_bf16(A.v_tilde, rows * 64, A.vt16, st)) != cudaSuccess) return e;
+  if (kRowSumD) {
+    if ((e = cudaMemsetAsync(A.Dn, 0, (size_t)A.BH * A.N * sizeof(float), st)) != cudaSuccess)
+      return e;
+    if ((e = launch_bwd_pass_mma(p, 2, st)) != cudaSuccess) return e;
+    if (!A.routed && (e = launch_bwd_pass_mma(sp, 2, st)) != cudaSuccess) return e;
+  }
+  if ((e = launch_bwd_pass_mma(p, 0, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd_pass_mma(p, 1, st)) != cudaSuccess) return e;
+  if (A.routed) return cudaSuccess;
+  if ((e = launch_bwd_pass_mma(sp, 0, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd_pass_mma(sp, 1, st)) != cudaSuccess) return e;
+  // through v~ = A V: the landmarks (q~, dv~, normaliser, dv~.v~) against every key
+  if ((e = to_bf16(A.dvt, rows * 64, A.dvt16, st)) != cudaSuccess) return e;
+  BwdPass vp{};
+  vp.q = A.q_tilde; vp.g = A.dvt16; vp.k = A.k; vp.v = A.v; vp.L = A.lseA; vp.D = A.cvt;
+  vp.Dacc = A.cvt; vp.dq = A.dqt; vp.dk = A.dk; vp.dv = A.dv; vp.c = c; vp.BH = A.BH;
+  vp.nq = A.m; vp.nk = A.N; vp.status = A.status;
+  if (kRowSumD) {
+    if ((e = cudaMemsetAsync(A.cvt, 0, (size_t)rows * sizeof(float), st)) != cudaSuccess) return e;
+    if ((e = launch_bwd_pass_mma(vp, 2, st)) != cudaSuccess) return e;
+  } else {
+    bwd_vt_dot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(A.dvt, A.v_tilde, rows, 64,
+                                                                  A.cvt);
+    count_launch();
+  }
+  if ((e = launch_bwd_pass_mma(vp, 0, st)) != cudaSuccess) return e;
+  if ((e = launch_bwd_pass_mma(vp, 1, st)) != cudaSuccess) return e;
+  bwd_pool_kernel<<<(unsigned)rows, 128, 0, st>>>(A.dqt, A.N, 64, A.grid_h, A.grid_w, A.mh, A.mw,
+                                                  A.dq);
+  count_launch();
+  return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t run(const BwdArgs<T>& A, cudaStream_t st) {
   const int BH = A.BH, N = A.N, m = A.m;
@@ -435,10 +510,15 @@ cudaError_t run(const BwdArgs<T>& A, cudaStream_t st) {
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
   }
+  bool mma = false;
+  if constexpr (std::is_same<T, bf16>::value && D == 64) mma = A.vt16 && A.dvt16;
   bwd_stats_kernel<D><<<(unsigned)((BHN + 7) / 8), 256, 0, st>>>(
       A.routed ? nullptr : A.sh_lse, A.routed ? nullptr : A.sh_o, A.part, BHN, A.s, A.dout,
-      std::is_same<T, bf16>::value ? 1 : 0, A.lse, A.Dn, A.status);
+      std::is_same<T, bf16>::value ? 1 : 0, A.lse, (mma && kRowSumD) ? nullptr : A.Dn, A.status);
   count_launch();
+  if constexpr (std::is_same<T, bf16>::value && D == 64) {
+    if (mma) return run_mma(A, st);
+  }
   const int qtiles = (N + kT - 1) / kT;
   const int rtiles = (int)(((long long)N * A.s + kT - 1) / kT) + m;
   bwd_raw_kernel<T, D><<<(unsigned)((long long)BH * rtiles), kT, sm, st>>>(

@@ -222,9 +222,32 @@ struct BwdArgs {
   float *dqt, *dvt;                       // [BH*m*d] scratch, cleared
   float *dq, *dk, *dv;                    // [BH*N*d] outputs, cleared
   int* status;
+  // bf16 with d = 64: [BH*m*64] scratch for bf16 copies of v~ and dv~; when both are set the
+  // gradient passes run on the tensor cores (backward_mma.cu), else on SIMT cores
+  __nv_bfloat16 *vt16, *dvt16;
 };
 template <typename T>
 cudaError_t launch_backward(const BwdArgs<T>& a, int d, cudaStream_t st);
+
+// One gradient pass of the backward on the tensor cores (bf16 rows of 64, fp32 results):
+// queries (q, g, L, D) against keys (k, v) under logit scale c, P = exp(c q.k - L),
+// dS = P (g.v - D); kind 0 (query-major) adds c dS k to dq; kind 1 (key-major) adds
+// c dS^T q to dk and P^T g to dv (a null output is skipped); kind 2 (query-major) adds
+// each query's sum of P (g.v) over the pass's keys to Dacc.  Segments: with bucket_off set, one per (head, expert)
+// -- queries n = bucket_qidx[bh][off[e] ..] and keys j = topk_idx[bh][e][0 .. topk), rows
+// bh*N + n and bh*N + j -- else one per head with nq query rows at bh*nq and nk key rows at
+// bh*nk.  `items` is set by the launcher.
+struct BwdPass {
+  const __nv_bfloat16 *q, *g, *k, *v;
+  const float *L, *D;
+  float *dq, *dk, *dv, *Dacc;
+  float c;
+  int BH, nq, nk;
+  const int32_t *bucket_off, *bucket_qidx, *topk_idx;
+  int N, m, topk, NS, items;
+  int* status;
+};
+cudaError_t launch_bwd_pass_mma(BwdPass p, int kind, cudaStream_t st);
 
 int num_sms_of_current_device();
 

@@ -32,6 +32,14 @@ CASES = {
     "bf16_d64_s3": (W.custom("b6", 1, 2, 400, 64, "bf16", 1, 400, 10, 16, index=76), 3, {}),
     "bf16_d128": (W.custom("b7", 1, 2, 256, 128, "bf16", 1, 256, 4, 20, index=77), 1, {}),
     "bf16_vit_2d": (W.custom("b8", 2, 2, 196, 64, "bf16", 14, 14, 25, 25, index=78), 1, {}),
+    # several 64-row chunks per CTA, and streams split over CTAs (shared and v~ passes)
+    "bf16_multi_chunk": (W.custom("b10", 1, 2, 4096, 64, "bf16", 1, 4096, 64, 256, index=80), 1,
+                         {}),
+    # top-k and buckets longer than one CTA's stream (the raw pass split both ways), s = 2
+    "bf16_long_lists_s2": (W.custom("b11", 1, 1, 3000, 64, "bf16", 1, 3000, 3, 1100, index=81), 2,
+                           {}),
+    "bf16_routed_d64": (W.custom("b12", 1, 2, 2048, 64, "bf16", 1, 2048, 32, 96, index=82), 1,
+                        {"branches": "routed"}),
 }
 
 
