@@ -15,9 +15,10 @@
 //   dk_j += sum_i dS_ij q~_i c;  dq~_i += sum_j dS_ij k_j c;  dq_t += dq~_i / |window_i|.
 //
 // bf16 inputs with d = 64 run the three gradient passes (raw, shared, through v~) on the
-// tensor cores (backward_mma.cu: one query-major and one key-major launch per pass); every
-// other shape runs these SIMT kernels (fp32, gradients accumulated with atomics into fp32
-// buffers):
+// tensor cores (backward_mma.cu: row-sum, query-major and key-major launches per pass,
+// after bwd_lse_kernel, which forms lse_n alone: those passes sum D_n as P dP themselves);
+// every other shape runs these SIMT kernels (fp32, gradients accumulated with atomics into
+// fp32 buffers):
 //   bwd_stats_kernel     per query: lse_n and D_n from the shared partial and the s raw
 //                        partials (the forward's own kernels recompute those);
 //   (each landmark's softmax normaliser ln sum_j exp(q~_i . k_j c) comes from the
@@ -26,7 +27,8 @@
 //                        time): dq, and the chunk's dK / dV as dS^T Q and P^T dO;
 //   bwd_shared_kernel    per 64 queries (landmarks staged 32 at a time): dq, dq~, dv~;
 //   bwd_vtilde_kernel    per 64 keys (landmarks staged 32 at a time): dk, dv, dq~;
-//   bwd_pool_kernel      per landmark: dq~ / |window| to every query of its window.
+//   bwd_pool_gather_kernel  per token: the sum of dq~ / |window| over the windows holding it
+//                        (bwd_pool_kernel, per landmark with atomics, when dq is not 16-byte aligned).
 #include <algorithm>
 #include <cmath>
 #include <type_traits>
@@ -61,12 +63,6 @@ bwd_stats_kernel(const float* __restrict__ sh_lse, const float* __restrict__ sh_
   for (int t = 0; t < s; ++t) M = fmaxf(M, __shfl_sync(0xffffffffu, pl, t));
   constexpr int PER = (D + 31) / 32;
   const float wsh = sh ? exp2f((sh_lse[qi] - M) * kL2e) : 0.f;
-  if (Dn == nullptr) {   // the log-sum-exp only (D is summed by the gradient passes)
-    float z = wsh;
-    for (int t = 0; t < s; ++t) z += exp2f((__shfl_sync(0xffffffffu, pl, t) - M) * kL2e);
-    if (lane == 0) lse[qi] = M + logf(z);
-    return;
-  }
   float z = wsh, acc[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
@@ -99,6 +95,23 @@ bwd_stats_kernel(const float* __restrict__ sh_lse, const float* __restrict__ sh_
     lse[qi] = M + logf(z);
     Dn[qi] = dd;
   }
+}
+
+// per query (one thread each): lse_n only, for the tensor-core passes that sum D themselves
+__global__ void __launch_bounds__(256)
+bwd_lse_kernel(const float* __restrict__ sh_lse, ExpertPartials part, long long BHN, int s,
+               float* __restrict__ lse, int* status) {
+  const long long qi = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (qi >= BHN) return;
+  if (part.cnt[qi] != s) {
+    flag_error(status, kDevErrBadBucket);
+    return;
+  }
+  float M = sh_lse ? sh_lse[qi] : -INFINITY;
+  for (int t = 0; t < s; ++t) M = fmaxf(M, part.lse[qi * s + t]);
+  float z = sh_lse ? exp2f((sh_lse[qi] - M) * kL2e) : 0.f;
+  for (int t = 0; t < s; ++t) z += exp2f((part.lse[qi * s + t] - M) * kL2e);
+  lse[qi] = M + logf(z);
 }
 
 // Shared-memory tiles of one CTA: its kT rows (q or k, and dO or v), and kC staged rows.
@@ -430,6 +443,55 @@ bwd_pool_kernel(const float* __restrict__ dqt, int N, int D, int grid_h, int gri
   }
 }
 
+// The same as a gather: per (token, 4 columns), the sum over the windows holding the token
+// (adaptive windows: along each axis they start at window floor(r * out / in) and overlap by
+// at most one token), added to dq with one read-modify-write (no other launch writes dq then).
+__global__ void __launch_bounds__(256)
+bwd_pool_gather_kernel(const float* __restrict__ dqt, long long BH, int N, int D, int grid_h,
+                       int grid_w, int mh, int mw, float* __restrict__ dq) {
+  const int D4 = D / 4;
+  const long long x = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (x >= BH * N * D4) return;
+  const long long tok = x / D4;
+  const int c4 = (int)(x % D4);
+  const long long bh = tok / N;
+  const int n = (int)(tok % N), r = n / grid_w, cc = n % grid_w;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = (int)((long long)r * mh / grid_h); i < mh; ++i) {
+    int r0, r1;
+    adaptive_window(i, grid_h, mh, &r0, &r1);
+    if (r0 > r) break;
+    if (r >= r1) continue;
+    for (int j = (int)((long long)cc * mw / grid_w); j < mw; ++j) {
+      int c0, c1;
+      adaptive_window(j, grid_w, mw, &c0, &c1);
+      if (c0 > cc) break;
+      if (cc >= c1) continue;
+      const float inv = 1.f / (float)((r1 - r0) * (c1 - c0));
+      const float4 gq = reinterpret_cast<const float4*>(
+          dqt + ((size_t)bh * mh * mw + (size_t)i * mw + j) * D)[c4];
+      acc.x = fmaf(gq.x, inv, acc.x); acc.y = fmaf(gq.y, inv, acc.y);
+      acc.z = fmaf(gq.z, inv, acc.z); acc.w = fmaf(gq.w, inv, acc.w);
+    }
+  }
+  float4* o = reinterpret_cast<float4*>(dq + (size_t)tok * D) + c4;
+  float4 v = *o;
+  v.x += acc.x; v.y += acc.y; v.z += acc.z; v.w += acc.w;
+  *o = v;
+}
+void launch_pool_grad(const float* dqt, int BH, int N, int D, int gh, int gw, int mh, int mw,
+                      float* dq, cudaStream_t st) {
+  if (reinterpret_cast<uintptr_t>(dq) % 16 == 0) {
+    const long long n = (long long)BH * N * (D / 4);
+    bwd_pool_gather_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(dqt, BH, N, D, gh, gw, mh,
+                                                                      mw, dq);
+  } else {
+    bwd_pool_kernel<<<(unsigned)((long long)BH * mh * mw), 128, 0, st>>>(dqt, N, D, gh, gw, mh, mw,
+                                                                       dq);
+  }
+  count_launch();
+}
+
 template <int D>
 size_t smem_bytes() { return sizeof(BwdSmem<D>); }
 
@@ -493,9 +555,7 @@ cudaError_t run_mma(const BwdArgs<bf16>& A, cudaStream_t st) {
   }
   if ((e = launch_bwd_pass_mma(vp, 0, st)) != cudaSuccess) return e;
   if ((e = launch_bwd_pass_mma(vp, 1, st)) != cudaSuccess) return e;
-  bwd_pool_kernel<<<(unsigned)rows, 128, 0, st>>>(A.dqt, A.N, 64, A.grid_h, A.grid_w, A.mh, A.mw,
-                                                  A.dq);
-  count_launch();
+  launch_pool_grad(A.dqt, A.BH, A.N, 64, A.grid_h, A.grid_w, A.mh, A.mw, A.dq, st);
   return cudaGetLastError();
 }
 
@@ -512,9 +572,14 @@ cudaError_t run(const BwdArgs<T>& A, cudaStream_t st) {
   }
   bool mma = false;
   if constexpr (std::is_same<T, bf16>::value && D == 64) mma = A.vt16 && A.dvt16;
-  bwd_stats_kernel<D><<<(unsigned)((BHN + 7) / 8), 256, 0, st>>>(
-      A.routed ? nullptr : A.sh_lse, A.routed ? nullptr : A.sh_o, A.part, BHN, A.s, A.dout,
-      std::is_same<T, bf16>::value ? 1 : 0, A.lse, (mma && kRowSumD) ? nullptr : A.Dn, A.status);
+  if (mma && kRowSumD) {
+    bwd_lse_kernel<<<(unsigned)((BHN + 255) / 256), 256, 0, st>>>(
+        A.routed ? nullptr : A.sh_lse, A.part, BHN, A.s, A.lse, A.status);
+  } else {
+    bwd_stats_kernel<D><<<(unsigned)((BHN + 7) / 8), 256, 0, st>>>(
+        A.routed ? nullptr : A.sh_lse, A.routed ? nullptr : A.sh_o, A.part, BHN, A.s, A.dout,
+        std::is_same<T, bf16>::value ? 1 : 0, A.lse, A.Dn, A.status);
+  }
   count_launch();
   if constexpr (std::is_same<T, bf16>::value && D == 64) {
     if (mma) return run_mma(A, st);
@@ -536,9 +601,7 @@ cudaError_t run(const BwdArgs<T>& A, cudaStream_t st) {
     bwd_vtilde_kernel<T, D><<<(unsigned)((long long)BH * qtiles), kT, sm, st>>>(
         A.k, A.v, A.q_tilde, A.dvt, A.lseA, A.cvt, N, m, qtiles, A.dk, A.dv, A.dqt);
     count_launch();
-    bwd_pool_kernel<<<(unsigned)rows, 128, 0, st>>>(A.dqt, N, D, A.grid_h, A.grid_w, A.mh, A.mw,
-                                                    A.dq);
-    count_launch();
+    launch_pool_grad(A.dqt, BH, N, D, A.grid_h, A.grid_w, A.mh, A.mw, A.dq, st);
   }
   return cudaGetLastError();
 }

@@ -48,7 +48,7 @@ enum { kQueryMajor = 0, kKeyMajor = 1, kRowSums = 2 };
 struct MmaSmem {
   bf16 own[2][kRows][kPad];        // owned rows: (q, g) or (k, v)
   bf16 st[2][2][kRows][kPad];      // [buffer][matrix][row]: streamed (k, v) or (q, g)
-  float sa[2][kRows];              // per streamed row: key bias (0 / -inf), or L log2e (+inf: none)
+  float sa[2][kRows];              // per streamed row: key bias (0 / -inf), or the query's L
   float sb[2][kRows];              // per streamed query row: D
   long long own_row[kRows];        // global row of each owned row, -1 past the end
 };
@@ -59,6 +59,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // 16-byte copy, zero-filled when src_bytes is 0 (nothing is read then)
 __device__ __forceinline__ void cp16(void* dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+// 4-byte copy, zero-filled when src_bytes is 0
+__device__ __forceinline__ void cp4(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
                "r"(src_bytes)
                : "memory");
 }
@@ -108,31 +114,33 @@ struct Side {
   long long base;
   int cnt, lim;
 };
-__device__ __forceinline__ long long side_row(const Side& s, int p, int* status) {
-  if (p >= s.cnt) return -1;
-  if (!s.list) return s.base + p;
-  const int x = s.list[p];
-  if (x < 0 || x >= s.lim) {
-    if (status) flag_error(status, kDevErrBadIndex);
-    return -1;
-  }
-  return s.base + x;
-}
-
-// Stages rows [p0, p0 + 64) of a side: two matrices of 64-wide bf16 rows, zero past the end.
-// The thread that copies piece 0 of a row returns through `row_of` (row index, global row).
-template <typename F>
-__device__ __forceinline__ void stage_rows(bf16 (*d0)[kPad], bf16 (*d1)[kPad], const bf16* s0,
-                                           const bf16* s1, const Side& sd, int p0, int* status,
-                                           F row_of) {
+// A thread stages four rows of a 64-row block, rows (tid >> 3) + 16 j, 16 bytes (piece
+// tid & 7) of each.  side_fetch reads their list values (kPastEnd past the end); the kernel
+// fetches them one block ahead, so a block's copies never wait on its index loads.
+constexpr int kPastEnd = -2147483647 - 1;
+__device__ __forceinline__ void side_fetch(const Side& s, int p0, int* x) {
 #pragma unroll
-  for (int j = 0; j < 2 * kRows * 8 / kThreads; ++j) {
-    const int i = j * kThreads + threadIdx.x;
-    const int mat = i >> 9, r = (i >> 3) & (kRows - 1), piece = i & 7;
-    const long long g = side_row(sd, p0 + r, (mat == 0 && piece == 0) ? status : nullptr);
-    const bf16* src = (mat ? s1 : s0) + (g < 0 ? 0 : g * 64) + piece * 8;
-    cp16((mat ? d1 : d0)[r] + piece * 8, src, g < 0 ? 0 : 16);
-    if (mat == 0 && piece == 0) row_of(r, g);
+  for (int j = 0; j < 4; ++j) {
+    const int p = p0 + (threadIdx.x >> 3) + 16 * j;
+    x[j] = p < s.cnt ? (s.list ? s.list[p] : p) : kPastEnd;
+  }
+}
+// Copies the two 64-wide bf16 rows of each of the thread's four rows, zero-filled past the
+// end and for invalid list values (flagged); gr[j] = the global row, or -1.
+__device__ __forceinline__ void stage4(bf16 (*d0)[kPad], bf16 (*d1)[kPad], const bf16* s0,
+                                       const bf16* s1, const Side& sd, const int* x, int* status,
+                                       long long* gr) {
+  const int piece = threadIdx.x & 7;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = (threadIdx.x >> 3) + 16 * j;
+    long long g = -1;
+    if (x[j] >= 0 && x[j] < sd.lim) g = sd.base + x[j];
+    else if (x[j] != kPastEnd && piece == 0) flag_error(status, kDevErrBadIndex);
+    gr[j] = g;
+    const size_t o = (g < 0 ? 0 : (size_t)g * 64) + piece * 8;
+    cp16(d0[r] + piece * 8, s0 + o, g < 0 ? 0 : 16);
+    cp16(d1[r] + piece * 8, s1 + o, g < 0 ? 0 : 16);
   }
 }
 
@@ -143,7 +151,7 @@ __device__ __forceinline__ int seg_items(int own_cnt, int st_cnt) {
 }
 
 template <int kMode>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)   // three CTAs (twelve warps) per SM
 bwd_mma_kernel(BwdPass a) {
   constexpr bool kKM = kMode == kKeyMajor, kRS = kMode == kRowSums;
   extern __shared__ __align__(128) unsigned char smraw[];
@@ -207,22 +215,41 @@ bwd_mma_kernel(BwdPass a) {
   const bf16* st0 = kKM ? a.q : a.k;
   const bf16* st1 = kKM ? a.g : a.v;
 
-  stage_rows(sm.own[0], sm.own[1], own0, own1, os, o0, a.status,
-             [&](int r, long long gr) { sm.own_row[r] = gr; });
+  const bool piece0 = (tid & 7) == 0;
+  {
+    int xo[4];
+    long long go[4];
+    side_fetch(os, o0, xo);
+    stage4(sm.own[0], sm.own[1], own0, own1, os, xo, a.status, go);
+    if (piece0)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sm.own_row[(tid >> 3) + 16 * j] = go[j];
+  }
   cp_commit();
-  auto stage_stream = [&](int buf, int p0) {
-    stage_rows(sm.st[buf][0], sm.st[buf][1], st0, st1, ss, p0, a.status,
-               [&](int r, long long gr) {
-                 if constexpr (kKM) {
-                   sm.sa[buf][r] = gr < 0 ? INFINITY : a.L[gr] * kLog2e;
-                   sm.sb[buf][r] = gr < 0 ? 0.f : a.D[gr];
-                 } else {
-                   sm.sa[buf][r] = gr < 0 ? -INFINITY : 0.f;
-                 }
-               });
+  // A streamed block from its fetched list values.  Per row: key-major copies L and D
+  // (zero for a missing query row, whose q and g rows are zero too, so its P = 1 meets
+  // zero rows and adds nothing); query-major writes the key's bias (-inf: no key).
+  auto stage_stream = [&](int buf, const int* x) {
+    long long gs[4];
+    stage4(sm.st[buf][0], sm.st[buf][1], st0, st1, ss, x, a.status, gs);
+    if (piece0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = (tid >> 3) + 16 * j;
+        if constexpr (kKM) {
+          cp4(&sm.sa[buf][r], a.L + (gs[j] < 0 ? 0 : gs[j]), gs[j] < 0 ? 0 : 4);
+          cp4(&sm.sb[buf][r], a.D + (gs[j] < 0 ? 0 : gs[j]), gs[j] < 0 ? 0 : 4);
+        } else {
+          sm.sa[buf][r] = gs[j] < 0 ? -INFINITY : 0.f;
+        }
+      }
+    }
   };
-  stage_stream(0, s0);
+  int xs[4];
+  side_fetch(ss, s0, xs);
+  stage_stream(0, xs);
   cp_commit();
+  if (nch > 1) side_fetch(ss, s0 + kRows, xs);
   cp_wait<1>();
   __syncthreads();
 
@@ -257,8 +284,9 @@ bwd_mma_kernel(BwdPass a) {
   for (int c = 0; c < nch; ++c) {
     const int buf = c & 1;
     if (c + 1 < nch) {
-      stage_stream(buf ^ 1, s0 + (c + 1) * kRows);
+      stage_stream(buf ^ 1, xs);                  // fetched one block ago
       cp_commit();
+      if (c + 2 < nch) side_fetch(ss, s0 + (c + 2) * kRows, xs);
       cp_wait<1>();
     } else {
       cp_wait<0>();
@@ -292,9 +320,10 @@ bwd_mma_kernel(BwdPass a) {
         if constexpr (kKM) {
           const float2 L2 = *reinterpret_cast<const float2*>(&sm.sa[buf][col]);
           const float2 D2 = *reinterpret_cast<const float2*>(&sm.sb[buf][col]);
+          const float nl0 = -L2.x * kLog2e, nl1 = -L2.y * kLog2e;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float p = exp2a(fmaf(s[nt][j], cl2, -((j & 1) ? L2.y : L2.x)));
+            const float p = exp2a(fmaf(s[nt][j], cl2, (j & 1) ? nl1 : nl0));
             dp[nt][j] = p * (dp[nt][j] - ((j & 1) ? D2.y : D2.x));
             s[nt][j] = p;
           }
