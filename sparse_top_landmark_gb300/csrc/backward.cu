@@ -443,9 +443,12 @@ bwd_pool_kernel(const float* __restrict__ dqt, int N, int D, int grid_h, int gri
   }
 }
 
-// The same as a gather: per (token, 4 columns), the sum over the windows holding the token
-// (adaptive windows: along each axis they start at window floor(r * out / in) and overlap by
-// at most one token), added to dq with one read-modify-write (no other launch writes dq then).
+// The same as a gather: per (token, 4 columns), the sum over the windows holding the token,
+// added to dq with one read-modify-write (no other launch writes dq then).  kEven: every
+// window along an axis has in / out tokens, so token r lies in window r / (in / out) alone;
+// else adaptive windows, which along each axis start at window floor(r * out / in) and
+// overlap by at most one token (32-bit index arithmetic; the host checks it fits).
+template <bool kEven>
 __global__ void __launch_bounds__(256)
 bwd_pool_gather_kernel(const float* __restrict__ dqt, long long BH, int N, int D, int grid_h,
                        int grid_w, int mh, int mw, float* __restrict__ dq) {
@@ -455,23 +458,29 @@ bwd_pool_gather_kernel(const float* __restrict__ dqt, long long BH, int N, int D
   const long long tok = x / D4;
   const int c4 = (int)(x % D4);
   const long long bh = tok / N;
-  const int n = (int)(tok % N), r = n / grid_w, cc = n % grid_w;
+  const unsigned n = (unsigned)(tok - bh * N), r = n / (unsigned)grid_w, cc = n - r * grid_w;
+  const float* base = dqt + (size_t)bh * mh * mw * D;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = (int)((long long)r * mh / grid_h); i < mh; ++i) {
-    int r0, r1;
-    adaptive_window(i, grid_h, mh, &r0, &r1);
-    if (r0 > r) break;
-    if (r >= r1) continue;
-    for (int j = (int)((long long)cc * mw / grid_w); j < mw; ++j) {
-      int c0, c1;
-      adaptive_window(j, grid_w, mw, &c0, &c1);
-      if (c0 > cc) break;
-      if (cc >= c1) continue;
-      const float inv = 1.f / (float)((r1 - r0) * (c1 - c0));
-      const float4 gq = reinterpret_cast<const float4*>(
-          dqt + ((size_t)bh * mh * mw + (size_t)i * mw + j) * D)[c4];
-      acc.x = fmaf(gq.x, inv, acc.x); acc.y = fmaf(gq.y, inv, acc.y);
-      acc.z = fmaf(gq.z, inv, acc.z); acc.w = fmaf(gq.w, inv, acc.w);
+  auto add = [&](unsigned i, unsigned j, float inv) {
+    const float4 gq = reinterpret_cast<const float4*>(base + ((size_t)i * mw + j) * D)[c4];
+    acc.x = fmaf(gq.x, inv, acc.x); acc.y = fmaf(gq.y, inv, acc.y);
+    acc.z = fmaf(gq.z, inv, acc.z); acc.w = fmaf(gq.w, inv, acc.w);
+  };
+  if constexpr (kEven) {
+    const unsigned wh = (unsigned)(grid_h / mh), ww = (unsigned)(grid_w / mw);
+    add(r / wh, cc / ww, 1.f / (float)(wh * ww));
+  } else {
+    const unsigned uh = grid_h, uw = grid_w, umh = mh, umw = mw;
+    for (unsigned i = r * umh / uh; i < umh; ++i) {
+      const unsigned r0 = i * uh / umh, r1 = ((i + 1) * uh + umh - 1) / umh;
+      if (r0 > r) break;
+      if (r >= r1) continue;
+      for (unsigned j = cc * umw / uw; j < umw; ++j) {
+        const unsigned c0 = j * uw / umw, c1 = ((j + 1) * uw + umw - 1) / umw;
+        if (c0 > cc) break;
+        if (cc >= c1) continue;
+        add(i, j, 1.f / (float)((r1 - r0) * (c1 - c0)));
+      }
     }
   }
   float4* o = reinterpret_cast<float4*>(dq + (size_t)tok * D) + c4;
@@ -481,10 +490,14 @@ bwd_pool_gather_kernel(const float* __restrict__ dqt, long long BH, int N, int D
 }
 void launch_pool_grad(const float* dqt, int BH, int N, int D, int gh, int gw, int mh, int mw,
                       float* dq, cudaStream_t st) {
-  if (reinterpret_cast<uintptr_t>(dq) % 16 == 0) {
+  // the adaptive form's products (index + 1) * extent stay below 2^32
+  const bool fits = ((long long)gh + 1) * (mh + 1) < (1LL << 32) &&
+                    ((long long)gw + 1) * (mw + 1) < (1LL << 32);
+  const bool even = gh % mh == 0 && gw % mw == 0;
+  if (reinterpret_cast<uintptr_t>(dq) % 16 == 0 && (even || fits)) {
     const long long n = (long long)BH * N * (D / 4);
-    bwd_pool_gather_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(dqt, BH, N, D, gh, gw, mh,
-                                                                      mw, dq);
+    auto kern = even ? bwd_pool_gather_kernel<true> : bwd_pool_gather_kernel<false>;
+    kern<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(dqt, BH, N, D, gh, gw, mh, mw, dq);
   } else {
     bwd_pool_kernel<<<(unsigned)((long long)BH * mh * mw), 128, 0, st>>>(dqt, N, D, gh, gw, mh, mw,
                                                                        dq);

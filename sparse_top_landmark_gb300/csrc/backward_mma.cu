@@ -27,7 +27,7 @@
 // Both recompute S and dP, three extra products per pair, but every accumulator stays in
 // the registers of the warp that owns its row: no cross-warp reduction and no per-chunk
 // atomics.  Streams longer than kSplitRows are split over CTAs (the v~ pass's N keys, the
-// shared pass's N queries), whose results meet in the final atomic adds.
+// shared pass's N queries), whose results meet in the final atomic adds (16 bytes each).
 // Operands: bf16 rows staged by cp.async (double-buffered, zero-filled past the end) into
 // shared memory with a 144-byte row stride, so the eight rows of an ldmatrix hit distinct
 // banks; P and dS are rounded to bf16 for the second products; accumulation is fp32.
@@ -397,23 +397,40 @@ bwd_mma_kernel(BwdPass a) {
     }
     return;
   }
-  // ---- one atomic add per owned element: rows g and g + 8, columns 8 nt + 2 t, +1
-  float* out0 = kKM ? a.dk : a.dq;
-  float* out1 = kKM ? a.dv : nullptr;
+  // ---- one 16-byte atomic add per lane and n-tile: lanes t and t ^ 1 swap halves, so an
+  // even t adds row g's columns 8 nt + 2 t .. +3 and an odd t row g + 8's columns
+  // 8 nt + 2 t - 2 .. +1
+  const bool ev = (t & 1) == 0;
+  const long long row = ev ? row_g : row_g8;
+  auto flush = [&](float* out, float (*acc)[4], float scale) {
+    if (!a.vec4) {   // outputs not 16-byte aligned: 8-byte adds at rows g and g + 8
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const long long row = half ? row_g8 : row_g;
-    if (row < 0) continue;
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const long long rr = hf ? row_g8 : row_g;
+          if (rr >= 0)
+            atomicAdd(reinterpret_cast<float2*>(out + (size_t)rr * 64 + 8 * nt + 2 * t),
+                      make_float2(scale * acc[nt][2 * hf], scale * acc[nt][2 * hf + 1]));
+        }
+      return;
+    }
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      const size_t o = (size_t)row * 64 + 8 * nt + 2 * t;
-      if (out0)
-        atomicAdd(reinterpret_cast<float2*>(out0 + o),
-                  make_float2(a.c * acc0[nt][2 * half], a.c * acc0[nt][2 * half + 1]));
-      if (out1)
-        atomicAdd(reinterpret_cast<float2*>(out1 + o),
-                  make_float2(acc1[nt][2 * half], acc1[nt][2 * half + 1]));
+      const float r0 = __shfl_xor_sync(0xffffffffu, ev ? acc[nt][2] : acc[nt][0], 1);
+      const float r1 = __shfl_xor_sync(0xffffffffu, ev ? acc[nt][3] : acc[nt][1], 1);
+      const float4 v = ev ? make_float4(acc[nt][0], acc[nt][1], r0, r1)
+                          : make_float4(r0, r1, acc[nt][2], acc[nt][3]);
+      if (row >= 0)
+        atomicAdd(reinterpret_cast<float4*>(out + (size_t)row * 64 + 8 * nt + 2 * t - (ev ? 0 : 2)),
+                  make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w));
     }
+  };
+  if constexpr (kKM) {
+    if (a.dk) flush(a.dk, acc0, a.c);
+    if (a.dv) flush(a.dv, acc1, 1.f);
+  } else {
+    if (a.dq) flush(a.dq, acc0, a.c);
   }
 }
 
@@ -435,6 +452,8 @@ cudaError_t launch_bwd_pass_mma(BwdPass p, int kind, cudaStream_t st) {
   if (items <= 0) return cudaSuccess;
   if (items * p.BH >= (1LL << 31)) return cudaErrorInvalidValue;
   p.items = (int)items;
+  auto al16 = [](const float* x) { return reinterpret_cast<uintptr_t>(x) % 16 == 0; };
+  p.vec4 = al16(p.dq) && al16(p.dk) && al16(p.dv);
   const size_t smem = sizeof(MmaSmem);
   auto kern = kind == 1 ? bwd_mma_kernel<kKeyMajor>
                         : kind == 2 ? bwd_mma_kernel<kRowSums> : bwd_mma_kernel<kQueryMajor>;
