@@ -278,11 +278,15 @@ int mita_dense_attn_f32(const float* q, const float* k, const float* v, int B, i
  * through the joint softmax (tutorial ch. 4 steps 5-6), the shared values
  * v~ = softmax(q~ K^T / sqrt(d)) V (steps 2-3) and the pooling (step 1).
  *   q, k, v, dout [B,H,N,d]  inputs (device, bf16 or fp32); dout = dL/dout.
- *   dq, dk, dv [B,H,N,d]     outputs, fp32 (device; cleared, then accumulated).
+ *   dq, dk, dv [B,H,N,d]     outputs, fp32 (device, 16-byte aligned like every
+ *                            buffer here; cleared, then accumulated).
  *   options                  as for mita_forward_ex (NULL: the defaults).
  * Recomputes the forward's selections and partials with the forward's kernels,
- * then runs SIMT gradient kernels (fp32 atomics; results vary in the last bits
- * between runs).  Uses the workspace cache.
+ * then runs the gradient kernels: bf16 with d = 64 on the tensor cores (warp-
+ * level MMAs; per pass, each query's D = sum of P dP over the same operands,
+ * then dq query-major and dk / dv key-major), other shapes on SIMT cores.
+ * Gradients are added with fp32 atomics, so results vary in the last bits
+ * between runs.  Uses the workspace cache.
  */
 int mita_backward(const void* q, const void* k, const void* v, const void* dout, int B, int H,
                   int N, int d, int grid_h, int grid_w, int m, int topk, int s,

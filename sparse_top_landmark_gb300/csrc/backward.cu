@@ -28,7 +28,8 @@
 //   bwd_shared_kernel    per 64 queries (landmarks staged 32 at a time): dq, dq~, dv~;
 //   bwd_vtilde_kernel    per 64 keys (landmarks staged 32 at a time): dk, dv, dq~;
 //   bwd_pool_gather_kernel  per token: the sum of dq~ / |window| over the windows holding it
-//                        (bwd_pool_kernel, per landmark with atomics, when dq is not 16-byte aligned).
+//                        (bwd_pool_kernel, per landmark with atomics, for grids whose window
+//                        arithmetic would not fit 32 bits).
 #include <algorithm>
 #include <cmath>
 #include <type_traits>
@@ -490,11 +491,12 @@ bwd_pool_gather_kernel(const float* __restrict__ dqt, long long BH, int N, int D
 }
 void launch_pool_grad(const float* dqt, int BH, int N, int D, int gh, int gw, int mh, int mw,
                       float* dq, cudaStream_t st) {
-  // the adaptive form's products (index + 1) * extent stay below 2^32
+  // the adaptive form's products (index + 1) * extent stay below 2^32; dq is 16-byte aligned
+  // (the entry point checks every buffer)
   const bool fits = ((long long)gh + 1) * (mh + 1) < (1LL << 32) &&
                     ((long long)gw + 1) * (mw + 1) < (1LL << 32);
   const bool even = gh % mh == 0 && gw % mw == 0;
-  if (reinterpret_cast<uintptr_t>(dq) % 16 == 0 && (even || fits)) {
+  if (even || fits) {
     const long long n = (long long)BH * N * (D / 4);
     auto kern = even ? bwd_pool_gather_kernel<true> : bwd_pool_gather_kernel<false>;
     kern<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(dqt, BH, N, D, gh, gw, mh, mw, dq);

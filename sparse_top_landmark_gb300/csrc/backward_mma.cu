@@ -403,18 +403,6 @@ bwd_mma_kernel(BwdPass a) {
   const bool ev = (t & 1) == 0;
   const long long row = ev ? row_g : row_g8;
   auto flush = [&](float* out, float (*acc)[4], float scale) {
-    if (!a.vec4) {   // outputs not 16-byte aligned: 8-byte adds at rows g and g + 8
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const long long rr = hf ? row_g8 : row_g;
-          if (rr >= 0)
-            atomicAdd(reinterpret_cast<float2*>(out + (size_t)rr * 64 + 8 * nt + 2 * t),
-                      make_float2(scale * acc[nt][2 * hf], scale * acc[nt][2 * hf + 1]));
-        }
-      return;
-    }
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const float r0 = __shfl_xor_sync(0xffffffffu, ev ? acc[nt][2] : acc[nt][0], 1);
@@ -452,8 +440,8 @@ cudaError_t launch_bwd_pass_mma(BwdPass p, int kind, cudaStream_t st) {
   if (items <= 0) return cudaSuccess;
   if (items * p.BH >= (1LL << 31)) return cudaErrorInvalidValue;
   p.items = (int)items;
-  auto al16 = [](const float* x) { return reinterpret_cast<uintptr_t>(x) % 16 == 0; };
-  p.vec4 = al16(p.dq) && al16(p.dk) && al16(p.dv);
+  for (const float* x : {p.dq, p.dk, p.dv})   // the 16-byte atomic adds
+    if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return cudaErrorMisalignedAddress;
   const size_t smem = sizeof(MmaSmem);
   auto kern = kind == 1 ? bwd_mma_kernel<kKeyMajor>
                         : kind == 2 ? bwd_mma_kernel<kRowSums> : bwd_mma_kernel<kQueryMajor>;

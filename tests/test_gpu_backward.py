@@ -93,3 +93,28 @@ def test_autograd_function_trains_like_the_oracle():
         assert _rel(got.cpu(), want) <= 1e-5
         mx, scale = _max_abs(got.cpu(), want)
         assert mx <= 1e-4 * max(scale, 1.0)
+
+
+
+@pytest.mark.parametrize("offset", [1, 2])
+def test_backward_rejects_unaligned_gradient_buffers(offset):
+    """Gradient buffers offset by 4 or 8 bytes are refused on the host (invalid argument,
+    the 16-byte atomic adds need aligned rows) before anything is written to them."""
+    import ctypes
+    mita = M()
+    w = W.custom("b13", 1, 2, 1024, 64, "bf16", 32, 32, 16, 48, index=83)
+    q, k, v = (t.cuda() for t in W.make_qkv(w, 0))
+    dout = torch.randn(q.shape, generator=torch.Generator().manual_seed(7)).to(q.dtype).cuda()
+    n = q.numel()
+    bufs = [torch.full((n + 4,), 7.0, dtype=torch.float32, device="cuda") for _ in range(3)]
+    views = [b[offset:offset + n].view(q.shape) for b in bufs]
+    B, H, N, d = q.shape
+    opt = mita._options("sqrt_d", None, "both")
+    rc = mita._fn("mita_backward", q.dtype)(
+        mita._ptr(q), mita._ptr(k), mita._ptr(v), mita._ptr(dout), B, H, N, d, w.grid_h,
+        w.grid_w, w.m, w.topk, 1, ctypes.byref(opt), mita._ptr(views[0]), mita._ptr(views[1]),
+        mita._ptr(views[2]), mita._stream(None, q.device))
+    assert rc == 1, rc   # MITA_ERR_INVALID_ARG
+    assert "16-byte aligned" in mita.load().mita_last_error_message().decode()
+    torch.cuda.synchronize()
+    assert all(torch.all(b == 7.0).item() for b in bufs)
