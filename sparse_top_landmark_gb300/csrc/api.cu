@@ -667,10 +667,7 @@ int backward_impl(const T* q, const T* k, const T* v, const T* dout, int B, int 
   part.lse = part.o + BHN * s * d;
   part.pos = reinterpret_cast<int*>(part.lse + BHN * s);
   part.cnt = part.pos + BHN * s;
-  const size_t gbytes = BHN * d * sizeof(float);
-  MITA_CUDA(cudaMemsetAsync(dq, 0, gbytes, st), "clearing dq");
-  MITA_CUDA(cudaMemsetAsync(dk, 0, gbytes, st), "clearing dk");
-  MITA_CUDA(cudaMemsetAsync(dv, 0, gbytes, st), "clearing dv");
+  // dq, dk, dv are cleared by the gradient launcher where its kernels add rather than store
   MITA_CUDA(cudaMemsetAsync(ws + o_dqt, 0, (o_dvt - o_dqt) + (size_t)BH * m * d * 4, st),
             "clearing scratch");
   MITA_CUDA(launch_pool<T>(q, BH, N, d, gh, gw, mh, mw, qt, st), "pool launch");

@@ -522,15 +522,30 @@ cudaError_t to_bf16(const float* x, long long n, bf16* y, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// The gradient passes on the tensor cores (bf16, d = 64), after bwd_stats.  With kRowSumD
-// each query's D (and each landmark's dv~ . v~) is summed as P dP over the same bf16 operands
-// the gradient launches use (launch kind 2), so the dS of a row sum to zero up to fp32
-// rounding; else D comes from the recomputed outputs (bwd_stats, bwd_vt_dot).
-constexpr bool kRowSumD = true;
+// The gradient passes on the tensor cores (bf16, d = 64), after bwd_lse.  Each query's D
+// (and each landmark's dv~ . v~) is summed as P dP over the same bf16 operands the gradient
+// launches use (launch kind 2), so the dS of a row sum to zero up to fp32 rounding.
+// Order: routed and shared row sums, dq (routed, shared), dq~ / dv~ (shared key-major), the
+// pass through v~ (its row sums, dq~, then dk / dv), the routed dk / dv last, the pooling
+// gradient.  A launch that is the first writer of rows it alone owns stores them (`first`),
+// which saves clearing dq (the routed query-major launch with s = 1 and an unsplit top-k
+// list), dk and dv (the v~ pass's key-major launch, before the routed one adds to them) and
+// D (the routed row sums).
 cudaError_t run_mma(const BwdArgs<bf16>& A, cudaStream_t st) {
   const float c = 0.125f;   // 1 / sqrt(64)
   const long long rows = (long long)A.BH * A.m;
+  const size_t gbytes = (size_t)A.BH * A.N * 64 * sizeof(float);
+  const bool q_first = A.s == 1 && A.topk <= kBwdSplitRows;    // one routed segment per query
+  const bool kv_first = !A.routed && A.m <= kBwdSplitRows;     // the v~ pass owns every key once
   cudaError_t e;
+  if (!q_first && (e = cudaMemsetAsync(A.dq, 0, gbytes, st)) != cudaSuccess) return e;
+  if (!kv_first) {
+    if ((e = cudaMemsetAsync(A.dk, 0, gbytes, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(A.dv, 0, gbytes, st)) != cudaSuccess) return e;
+  }
+  if (!q_first &&
+      (e = cudaMemsetAsync(A.Dn, 0, (size_t)A.BH * A.N * sizeof(float), st)) != cudaSuccess)
+    return e;
   // routed pairs: each expert's bucket entries against its top-k rows
   BwdPass p{};
   p.q = A.q; p.g = A.dout; p.k = A.k; p.v = A.v; p.L = A.lse; p.D = A.Dn; p.Dacc = A.Dn;
@@ -543,34 +558,29 @@ cudaError_t run_mma(const BwdArgs<bf16>& A, cudaStream_t st) {
   sp.Dacc = A.Dn; sp.dq = A.dq; sp.dk = A.dqt; sp.dv = A.dvt; sp.c = A.c_sh; sp.BH = A.BH;
   sp.nq = A.N; sp.nk = A.m; sp.status = A.status;
   if (!A.routed && (e = to_bf16(A.v_tilde, rows * 64, A.vt16, st)) != cudaSuccess) return e;
-  if (kRowSumD) {
-    if ((e = cudaMemsetAsync(A.Dn, 0, (size_t)A.BH * A.N * sizeof(float), st)) != cudaSuccess)
-      return e;
-    if ((e = launch_bwd_pass_mma(p, 2, st)) != cudaSuccess) return e;
-    if (!A.routed && (e = launch_bwd_pass_mma(sp, 2, st)) != cudaSuccess) return e;
-  }
+  p.first = q_first;
+  if ((e = launch_bwd_pass_mma(p, 2, st)) != cudaSuccess) return e;
+  if (!A.routed && (e = launch_bwd_pass_mma(sp, 2, st)) != cudaSuccess) return e;
   if ((e = launch_bwd_pass_mma(p, 0, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd_pass_mma(p, 1, st)) != cudaSuccess) return e;
-  if (A.routed) return cudaSuccess;
-  if ((e = launch_bwd_pass_mma(sp, 0, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd_pass_mma(sp, 1, st)) != cudaSuccess) return e;
-  // through v~ = A V: the landmarks (q~, dv~, normaliser, dv~.v~) against every key
-  if ((e = to_bf16(A.dvt, rows * 64, A.dvt16, st)) != cudaSuccess) return e;
-  BwdPass vp{};
-  vp.q = A.q_tilde; vp.g = A.dvt16; vp.k = A.k; vp.v = A.v; vp.L = A.lseA; vp.D = A.cvt;
-  vp.Dacc = A.cvt; vp.dq = A.dqt; vp.dk = A.dk; vp.dv = A.dv; vp.c = c; vp.BH = A.BH;
-  vp.nq = A.m; vp.nk = A.N; vp.status = A.status;
-  if (kRowSumD) {
+  p.first = 0;
+  if (!A.routed) {
+    if ((e = launch_bwd_pass_mma(sp, 0, st)) != cudaSuccess) return e;
+    if ((e = launch_bwd_pass_mma(sp, 1, st)) != cudaSuccess) return e;
+    // through v~ = A V: the landmarks (q~, dv~, normaliser, dv~.v~) against every key
+    if ((e = to_bf16(A.dvt, rows * 64, A.dvt16, st)) != cudaSuccess) return e;
+    BwdPass vp{};
+    vp.q = A.q_tilde; vp.g = A.dvt16; vp.k = A.k; vp.v = A.v; vp.L = A.lseA; vp.D = A.cvt;
+    vp.Dacc = A.cvt; vp.dq = A.dqt; vp.dk = A.dk; vp.dv = A.dv; vp.c = c; vp.BH = A.BH;
+    vp.nq = A.m; vp.nk = A.N; vp.status = A.status;
     if ((e = cudaMemsetAsync(A.cvt, 0, (size_t)rows * sizeof(float), st)) != cudaSuccess) return e;
     if ((e = launch_bwd_pass_mma(vp, 2, st)) != cudaSuccess) return e;
-  } else {
-    bwd_vt_dot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(A.dvt, A.v_tilde, rows, 64,
-                                                                  A.cvt);
-    count_launch();
+    if ((e = launch_bwd_pass_mma(vp, 0, st)) != cudaSuccess) return e;
+    vp.first = kv_first;
+    if ((e = launch_bwd_pass_mma(vp, 1, st)) != cudaSuccess) return e;
   }
-  if ((e = launch_bwd_pass_mma(vp, 0, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd_pass_mma(vp, 1, st)) != cudaSuccess) return e;
-  launch_pool_grad(A.dqt, A.BH, A.N, 64, A.grid_h, A.grid_w, A.mh, A.mw, A.dq, st);
+  if ((e = launch_bwd_pass_mma(p, 1, st)) != cudaSuccess) return e;   // adds to dk, dv
+  if (!A.routed)
+    launch_pool_grad(A.dqt, A.BH, A.N, 64, A.grid_h, A.grid_w, A.mh, A.mw, A.dq, st);
   return cudaGetLastError();
 }
 
@@ -587,7 +597,15 @@ cudaError_t run(const BwdArgs<T>& A, cudaStream_t st) {
   }
   bool mma = false;
   if constexpr (std::is_same<T, bf16>::value && D == 64) mma = A.vt16 && A.dvt16;
-  if (mma && kRowSumD) {
+  if (!mma) {   // the SIMT kernels add into cleared gradients (run_mma clears what it must)
+    const size_t gbytes = (size_t)BHN * D * sizeof(float);
+    float* const grads[3] = {A.dq, A.dk, A.dv};
+    for (int i = 0; i < 3; ++i) {
+      e = cudaMemsetAsync(grads[i], 0, gbytes, st);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  if (mma) {
     bwd_lse_kernel<<<(unsigned)((BHN + 255) / 256), 256, 0, st>>>(
         A.routed ? nullptr : A.sh_lse, A.part, BHN, A.s, A.lse, A.status);
   } else {

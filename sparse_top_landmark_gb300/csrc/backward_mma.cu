@@ -27,7 +27,9 @@
 // Both recompute S and dP, three extra products per pair, but every accumulator stays in
 // the registers of the warp that owns its row: no cross-warp reduction and no per-chunk
 // atomics.  Streams longer than kSplitRows are split over CTAs (the v~ pass's N keys, the
-// shared pass's N queries), whose results meet in the final atomic adds (16 bytes each).
+// shared pass's N queries), whose results meet in the final atomic adds (16 bytes each);
+// a launch that is the first and only writer of its owned rows (BwdPass::first: one
+// segment per row and an unsplit stream) stores them instead, so they need no clearing.
 // Operands: bf16 rows staged by cp.async (double-buffered, zero-filled past the end) into
 // shared memory with a 144-byte row stride, so the eight rows of an ldmatrix hit distinct
 // banks; P and dS are rounded to bf16 for the second products; accumulation is fp32.
@@ -39,7 +41,7 @@ namespace {
 
 constexpr int kRows = 64;          // owned rows per CTA and streamed rows per chunk
 constexpr int kPad = 72;           // shared-memory row stride in bf16 elements (144 B)
-constexpr int kSplitRows = 1024;   // streamed rows per CTA
+constexpr int kSplitRows = kBwdSplitRows;   // streamed rows per CTA
 constexpr int kThreads = 128;      // four warps, 16 owned rows each
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr bool kSplitDs = true;    // dq += (dS_hi + dS_lo) k
@@ -392,8 +394,13 @@ bwd_mma_kernel(BwdPass a) {
       rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
     }
     if (t == 0) {
-      if (row_g >= 0) atomicAdd(a.Dacc + row_g, rs[0]);
-      if (row_g8 >= 0) atomicAdd(a.Dacc + row_g8, rs[1]);
+      if (a.first) {
+        if (row_g >= 0) a.Dacc[row_g] = rs[0];
+        if (row_g8 >= 0) a.Dacc[row_g8] = rs[1];
+      } else {
+        if (row_g >= 0) atomicAdd(a.Dacc + row_g, rs[0]);
+        if (row_g8 >= 0) atomicAdd(a.Dacc + row_g8, rs[1]);
+      }
     }
     return;
   }
@@ -409,9 +416,11 @@ bwd_mma_kernel(BwdPass a) {
       const float r1 = __shfl_xor_sync(0xffffffffu, ev ? acc[nt][3] : acc[nt][1], 1);
       const float4 v = ev ? make_float4(acc[nt][0], acc[nt][1], r0, r1)
                           : make_float4(r0, r1, acc[nt][2], acc[nt][3]);
-      if (row >= 0)
-        atomicAdd(reinterpret_cast<float4*>(out + (size_t)row * 64 + 8 * nt + 2 * t - (ev ? 0 : 2)),
-                  make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w));
+      if (row < 0) continue;
+      float4* o = reinterpret_cast<float4*>(out + (size_t)row * 64 + 8 * nt + 2 * t - (ev ? 0 : 2));
+      const float4 x = make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w);
+      if (a.first) *o = x;
+      else atomicAdd(o, x);
     }
   };
   if constexpr (kKM) {
@@ -439,6 +448,10 @@ cudaError_t launch_bwd_pass_mma(BwdPass p, int kind, cudaStream_t st) {
   }
   if (items <= 0) return cudaSuccess;
   if (items * p.BH >= (1LL << 31)) return cudaErrorInvalidValue;
+  // a first writer must own each of its rows in one CTA: one segment per owned row (the
+  // caller's promise) and a stream short enough not to be split
+  if (p.first && (raw ? (key_major ? p.NS : p.topk) : (key_major ? p.nq : p.nk)) > kSplitRows)
+    return cudaErrorInvalidValue;
   p.items = (int)items;
   for (const float* x : {p.dq, p.dk, p.dv})   // the 16-byte atomic adds
     if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return cudaErrorMisalignedAddress;

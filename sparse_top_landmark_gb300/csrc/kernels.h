@@ -236,7 +236,10 @@ cudaError_t launch_backward(const BwdArgs<T>& a, int d, cudaStream_t st);
 // each query's sum of P (g.v) over the pass's keys to Dacc.  Segments: with bucket_off set, one per (head, expert)
 // -- queries n = bucket_qidx[bh][off[e] ..] and keys j = topk_idx[bh][e][0 .. topk), rows
 // bh*N + n and bh*N + j -- else one per head with nq query rows at bh*nq and nk key rows at
-// bh*nk.  Outputs 16-byte aligned.  `items` is set by the launcher.
+// bh*nk.  Outputs 16-byte aligned.  `first`: no earlier launch wrote the outputs and each
+// owned row lies in one segment, so the results are stored, not added (the launcher refuses
+// it when the stream would be split over CTAs: longer than kBwdSplitRows rows).  `items` is
+// set by the launcher.
 struct BwdPass {
   const __nv_bfloat16 *q, *g, *k, *v;
   const float *L, *D;
@@ -244,9 +247,10 @@ struct BwdPass {
   float c;
   int BH, nq, nk;
   const int32_t *bucket_off, *bucket_qidx, *topk_idx;
-  int N, m, topk, NS, items;
+  int N, m, topk, NS, items, first;
   int* status;
 };
+constexpr int kBwdSplitRows = 1024;   // streamed rows per CTA of the tensor-core passes
 cudaError_t launch_bwd_pass_mma(BwdPass p, int kind, cudaStream_t st);
 
 int num_sms_of_current_device();
