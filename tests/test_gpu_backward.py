@@ -40,6 +40,12 @@ CASES = {
                            {}),
     "bf16_routed_d64": (W.custom("b12", 1, 2, 2048, 64, "bf16", 1, 2048, 32, 96, index=82), 1,
                         {"branches": "routed"}),
+    # more than 1 024 landmarks: the v~ pass splits its landmark stream (dk, dv are added)
+    "bf16_many_landmarks": (W.custom("b14", 1, 1, 2048, 64, "bf16", 1, 2048, 1100, 8, index=84),
+                            1, {}),
+    # s = 1 with top-k lists over 1 024 rows: the routed dq launch is split (dq is added)
+    "bf16_s1_long_topk": (W.custom("b15", 1, 2, 2048, 64, "bf16", 1, 2048, 2, 1100, index=85), 1,
+                          {}),
 }
 
 
