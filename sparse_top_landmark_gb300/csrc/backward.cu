@@ -525,9 +525,9 @@ cudaError_t to_bf16(const float* x, long long n, bf16* y, cudaStream_t st) {
 // The gradient passes on the tensor cores (bf16, d = 64), after bwd_lse.  Each query's D
 // (and each landmark's dv~ . v~) is summed as P dP over the same bf16 operands the gradient
 // launches use (launch kind 2), so the dS of a row sum to zero up to fp32 rounding.
-// Order: routed and shared row sums, dq (routed, shared), dq~ / dv~ (shared key-major), the
-// pass through v~ (its row sums, dq~, then dk / dv), the routed dk / dv last, the pooling
-// gradient.  A launch that is the first writer of rows it alone owns stores them (`first`),
+// Order: routed and shared row sums, dq (routed, shared) -- with s = 1 one joint launch for
+// these four -- dq~ / dv~ (shared key-major), the pass through v~ (its row sums, dq~, then
+// dk / dv), the routed dk / dv last, the pooling gradient.  A launch that is the first writer of rows it alone owns stores them (`first`),
 // which saves clearing dq (the routed query-major launch with s = 1 and an unsplit top-k
 // list), dk and dv (the v~ pass's key-major launch, before the routed one adds to them) and
 // D (the routed row sums).
@@ -535,7 +535,8 @@ cudaError_t run_mma(const BwdArgs<bf16>& A, cudaStream_t st) {
   const float c = 0.125f;   // 1 / sqrt(64)
   const long long rows = (long long)A.BH * A.m;
   const size_t gbytes = (size_t)A.BH * A.N * 64 * sizeof(float);
-  const bool q_first = A.s == 1 && A.topk <= kBwdSplitRows;    // one routed segment per query
+  const bool joint = A.s == 1 && !A.routed;                    // a query's whole softmax per CTA
+  const bool q_first = joint || (A.s == 1 && A.topk <= kBwdSplitRows);   // one routed segment
   const bool kv_first = !A.routed && A.m <= kBwdSplitRows;     // the v~ pass owns every key once
   cudaError_t e;
   if (!q_first && (e = cudaMemsetAsync(A.dq, 0, gbytes, st)) != cudaSuccess) return e;
@@ -558,13 +559,19 @@ cudaError_t run_mma(const BwdArgs<bf16>& A, cudaStream_t st) {
   sp.Dacc = A.Dn; sp.dq = A.dq; sp.dk = A.dqt; sp.dv = A.dvt; sp.c = A.c_sh; sp.BH = A.BH;
   sp.nq = A.N; sp.nk = A.m; sp.status = A.status;
   if (!A.routed && (e = to_bf16(A.v_tilde, rows * 64, A.vt16, st)) != cudaSuccess) return e;
-  p.first = q_first;
-  if ((e = launch_bwd_pass_mma(p, 2, st)) != cudaSuccess) return e;
-  if (!A.routed && (e = launch_bwd_pass_mma(sp, 2, st)) != cudaSuccess) return e;
-  if ((e = launch_bwd_pass_mma(p, 0, st)) != cudaSuccess) return e;
-  p.first = 0;
+  if (joint) {   // both passes' D and dq in one launch
+    BwdPass jp = p;
+    jp.k2 = A.q_tilde; jp.v2 = A.vt16; jp.c2 = A.c_sh; jp.n2 = A.m; jp.first = 1;
+    if ((e = launch_bwd_pass_mma(jp, 3, st)) != cudaSuccess) return e;
+  } else {
+    p.first = q_first;
+    if ((e = launch_bwd_pass_mma(p, 2, st)) != cudaSuccess) return e;
+    if (!A.routed && (e = launch_bwd_pass_mma(sp, 2, st)) != cudaSuccess) return e;
+    if ((e = launch_bwd_pass_mma(p, 0, st)) != cudaSuccess) return e;
+    p.first = 0;
+  }
   if (!A.routed) {
-    if ((e = launch_bwd_pass_mma(sp, 0, st)) != cudaSuccess) return e;
+    if (!joint && (e = launch_bwd_pass_mma(sp, 0, st)) != cudaSuccess) return e;
     if ((e = launch_bwd_pass_mma(sp, 1, st)) != cudaSuccess) return e;
     // through v~ = A V: the landmarks (q~, dv~, normaliser, dv~.v~) against every key
     if ((e = to_bf16(A.dvt, rows * 64, A.dvt16, st)) != cudaSuccess) return e;

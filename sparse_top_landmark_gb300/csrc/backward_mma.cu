@@ -12,7 +12,9 @@
 //                (the shared pairs of the joint softmax);
 //   v~ pass      queries = the m landmarks (q~, dv~, the landmark softmax normaliser,
 //                dv~ . v~), keys = all N keys (tutorial ch. 4 step 3, v~ = softmax(q~ K^T c) V).
-// Each pass runs two or three launches of bwd_mma_kernel:
+// Each pass runs two or three launches of bwd_mma_kernel (with s = 1 one joint launch does
+// the routed and shared passes' row sums and dq together: a query's whole joint softmax is
+// its expert's top-k rows and the head's landmarks, swept once for D and once for dq):
 //   row sums     query-major, D = sum over the pass's keys of P dP added to each query's D
 //                (the forward's outputs, recomputed with bf16 operands, would give a D that
 //                does not match these P and dP; the gradient of q sums dS = P (dP - D) k
@@ -45,7 +47,7 @@ constexpr int kSplitRows = kBwdSplitRows;   // streamed rows per CTA
 constexpr int kThreads = 128;      // four warps, 16 owned rows each
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr bool kSplitDs = true;    // dq += (dS_hi + dS_lo) k
-enum { kQueryMajor = 0, kKeyMajor = 1, kRowSums = 2 };
+enum { kQueryMajor = 0, kKeyMajor = 1, kRowSums = 2, kJoint = 3 };
 
 struct MmaSmem {
   bf16 own[2][kRows][kPad];        // owned rows: (q, g) or (k, v)
@@ -155,7 +157,7 @@ __device__ __forceinline__ int seg_items(int own_cnt, int st_cnt) {
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 3)   // three CTAs (twelve warps) per SM
 bwd_mma_kernel(BwdPass a) {
-  constexpr bool kKM = kMode == kKeyMajor, kRS = kMode == kRowSums;
+  constexpr bool kKM = kMode == kKeyMajor, kRS = kMode == kRowSums, kJ = kMode == kJoint;
   extern __shared__ __align__(128) unsigned char smraw[];
   MmaSmem& sm = *reinterpret_cast<MmaSmem*>(smraw);
   __shared__ int s_e, s_w;
@@ -180,7 +182,7 @@ bwd_mma_kernel(BwdPass a) {
           if (x0 < 0 || x1 > a.NS || x1 < x0) flag_error(a.status, kDevErrBadBucket);
           else cnt = x1 - x0;
         }
-        const int W = kKM ? seg_items(a.topk, cnt) : seg_items(cnt, a.topk);
+        const int W = kKM ? seg_items(a.topk, cnt) : kJ ? seg_items(cnt, 1) : seg_items(cnt, a.topk);
         const int inc = warp_incl_scan(W);
         const int tot = __shfl_sync(0xffffffffu, inc, 31);
         if (item < run + tot) {
@@ -207,10 +209,22 @@ bwd_mma_kernel(BwdPass a) {
   }
   const Side& os = kKM ? ks : qs;   // owned side
   const Side& ss = kKM ? qs : ks;   // streamed side
-  const int splits = (ss.cnt + kSplitRows - 1) / kSplitRows;
+  const int splits = kJ ? 1 : (ss.cnt + kSplitRows - 1) / kSplitRows;
   const int o0 = (w / splits) * kRows;
   const int s0 = (w % splits) * kSplitRows;
-  const int nch = (min(ss.cnt - s0, kSplitRows) + kRows - 1) / kRows;
+  // joint: the expert's top-k rows, then the head's n2 rows of (k2, v2), each swept twice
+  const Side sb2{nullptr, bh * (long long)a.n2, a.n2, a.n2};
+  const int ncA = kJ ? (ss.cnt + kRows - 1) / kRows
+                     : (min(ss.cnt - s0, kSplitRows) + kRows - 1) / kRows;
+  const int nch = kJ ? ncA + (a.n2 + kRows - 1) / kRows : ncA;
+  const int nv = kJ ? 2 * nch : nch;
+  // virtual block v: (second side?, its first row)
+  auto block_of = [&](int v, int& p0) {
+    const int c = kJ ? v % nch : v;
+    const bool b2 = kJ && c >= ncA;
+    p0 = b2 ? (c - ncA) * kRows : s0 + c * kRows;
+    return b2;
+  };
 
   const bf16* own0 = kKM ? a.k : a.q;
   const bf16* own1 = kKM ? a.v : a.g;
@@ -231,9 +245,10 @@ bwd_mma_kernel(BwdPass a) {
   // A streamed block from its fetched list values.  Per row: key-major copies L and D
   // (zero for a missing query row, whose q and g rows are zero too, so its P = 1 meets
   // zero rows and adds nothing); query-major writes the key's bias (-inf: no key).
-  auto stage_stream = [&](int buf, const int* x) {
+  auto stage_stream = [&](int buf, const int* x, bool b2) {
     long long gs[4];
-    stage4(sm.st[buf][0], sm.st[buf][1], st0, st1, ss, x, a.status, gs);
+    stage4(sm.st[buf][0], sm.st[buf][1], b2 ? a.k2 : st0, b2 ? a.v2 : st1, b2 ? sb2 : ss, x,
+           a.status, gs);
     if (piece0) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -247,11 +262,15 @@ bwd_mma_kernel(BwdPass a) {
       }
     }
   };
-  int xs[4];
-  side_fetch(ss, s0, xs);
-  stage_stream(0, xs);
+  int xs[4], p0;
+  bool xb = block_of(0, p0);
+  side_fetch(xb ? sb2 : ss, p0, xs);
+  stage_stream(0, xs, xb);
   cp_commit();
-  if (nch > 1) side_fetch(ss, s0 + kRows, xs);
+  if (nv > 1) {
+    xb = block_of(1, p0);
+    side_fetch(xb ? sb2 : ss, p0, xs);
+  }
   cp_wait<1>();
   __syncthreads();
 
@@ -269,10 +288,10 @@ bwd_mma_kernel(BwdPass a) {
   // query-major: the owned rows' L log2e and D
   float Lr[2] = {0.f, 0.f}, Dr[2] = {0.f, 0.f}, rs[2] = {0.f, 0.f};
   if constexpr (!kKM) {
-    if (row_g >= 0) { Lr[0] = a.L[row_g] * kLog2e; if (!kRS) Dr[0] = a.D[row_g]; }
-    if (row_g8 >= 0) { Lr[1] = a.L[row_g8] * kLog2e; if (!kRS) Dr[1] = a.D[row_g8]; }
+    if (row_g >= 0) { Lr[0] = a.L[row_g] * kLog2e; if (!kRS && !kJ) Dr[0] = a.D[row_g]; }
+    if (row_g8 >= 0) { Lr[1] = a.L[row_g8] * kLog2e; if (!kRS && !kJ) Dr[1] = a.D[row_g8]; }
   }
-  const float cl2 = a.c * kLog2e;
+  float cl2 = a.c * kLog2e;
   float acc0[8][4], acc1[8][4];    // dq (query-major); dk and dv (key-major)
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -283,17 +302,41 @@ bwd_mma_kernel(BwdPass a) {
   const int rb = (lane & 7) + (lane >> 4) * 8, cb = ((lane >> 3) & 1) * 8;    // B, n = rows
   const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = (lane >> 4) * 8;     // B, k = rows
 
-  for (int c = 0; c < nch; ++c) {
+  for (int c = 0; c < nv; ++c) {
     const int buf = c & 1;
-    if (c + 1 < nch) {
-      stage_stream(buf ^ 1, xs);                  // fetched one block ago
+    if (c + 1 < nv) {
+      stage_stream(buf ^ 1, xs, xb);              // fetched one block ago
       cp_commit();
-      if (c + 2 < nch) side_fetch(ss, s0 + (c + 2) * kRows, xs);
+      if (c + 2 < nv) {
+        xb = block_of(c + 2, p0);
+        side_fetch(xb ? sb2 : ss, p0, xs);
+      }
       cp_wait<1>();
     } else {
       cp_wait<0>();
     }
     __syncthreads();
+    // joint: the block's scale, and after the first sweep each row's D from its sums
+    bool grad = !kRS;
+    float cs = 1.f;
+    if constexpr (kJ) {
+      int pz;
+      cs = block_of(c, pz) ? a.c2 : a.c;
+      cl2 = cs * kLog2e;
+      grad = c >= nch;
+      if (c == nch) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
+          rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
+          Dr[i] = rs[i];
+        }
+        if (t == 0) {
+          if (row_g >= 0) a.Dacc[row_g] = Dr[0];
+          if (row_g8 >= 0) a.Dacc[row_g8] = Dr[1];
+        }
+      }
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {          // 32 streamed rows at a time
       float s[4][4], dp[4][4];
@@ -334,14 +377,14 @@ bwd_mma_kernel(BwdPass a) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float p = exp2a(fmaf(s[nt][j], cl2, -Lr[j >> 1]) + ((j & 1) ? B2.y : B2.x));
-            if constexpr (kRS) rs[j >> 1] = fmaf(p, dp[nt][j], rs[j >> 1]);
-            else dp[nt][j] = p * (dp[nt][j] - Dr[j >> 1]);
+            if (!grad) rs[j >> 1] = fmaf(p, dp[nt][j], rs[j >> 1]);
+            else dp[nt][j] = (kJ ? cs * p : p) * (dp[nt][j] - Dr[j >> 1]);   // joint: c dS
           }
         }
       }
       // second products over these 32 streamed rows (two k-steps), d as eight n-tiles
 #pragma unroll
-      for (int ksx = 0; ksx < 2 && !kRS; ++ksx) {
+      for (int ksx = 0; ksx < 2 && grad; ++ksx) {
         const uint32_t ad[4] = {pack2(dp[2 * ksx][0], dp[2 * ksx][1]),
                                 pack2(dp[2 * ksx][2], dp[2 * ksx][3]),
                                 pack2(dp[2 * ksx + 1][0], dp[2 * ksx + 1][1]),
@@ -427,7 +470,7 @@ bwd_mma_kernel(BwdPass a) {
     if (a.dk) flush(a.dk, acc0, a.c);
     if (a.dv) flush(a.dv, acc1, 1.f);
   } else {
-    if (a.dq) flush(a.dq, acc0, a.c);
+    if (a.dq) flush(a.dq, acc0, kJ ? 1.f : a.c);   // joint: the scale is in dS already
   }
 }
 
@@ -438,7 +481,10 @@ cudaError_t launch_bwd_pass_mma(BwdPass p, int kind, cudaStream_t st) {
   const bool raw = p.bucket_off != nullptr;
   auto ceil_div = [](long long x, long long y) { return (x + y - 1) / y; };
   long long items;
-  if (raw) {
+  if (kind == 3) {   // joint: routed segments, every query row once, streams not split
+    if (!raw || !p.first || p.n2 < 0) return cudaErrorInvalidValue;
+    items = ceil_div(p.NS, kRows) + p.m;
+  } else if (raw) {
     // upper bound: sum over experts of ceil(cnt_e / 64) <= NS / 64 + m (and likewise for splits)
     items = key_major ? ceil_div(p.topk, kRows) * (ceil_div(p.NS, kSplitRows) + p.m)
                       : (ceil_div(p.NS, kRows) + p.m) * ceil_div(p.topk, kSplitRows);
@@ -450,14 +496,17 @@ cudaError_t launch_bwd_pass_mma(BwdPass p, int kind, cudaStream_t st) {
   if (items * p.BH >= (1LL << 31)) return cudaErrorInvalidValue;
   // a first writer must own each of its rows in one CTA: one segment per owned row (the
   // caller's promise) and a stream short enough not to be split
-  if (p.first && (raw ? (key_major ? p.NS : p.topk) : (key_major ? p.nq : p.nk)) > kSplitRows)
+  if (kind != 3 && p.first &&
+      (raw ? (key_major ? p.NS : p.topk) : (key_major ? p.nq : p.nk)) > kSplitRows)
     return cudaErrorInvalidValue;
   p.items = (int)items;
   for (const float* x : {p.dq, p.dk, p.dv})   // the 16-byte atomic adds
     if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return cudaErrorMisalignedAddress;
   const size_t smem = sizeof(MmaSmem);
-  auto kern = kind == 1 ? bwd_mma_kernel<kKeyMajor>
-                        : kind == 2 ? bwd_mma_kernel<kRowSums> : bwd_mma_kernel<kQueryMajor>;
+  auto kern = kind == 1   ? bwd_mma_kernel<kKeyMajor>
+              : kind == 2 ? bwd_mma_kernel<kRowSums>
+              : kind == 3 ? bwd_mma_kernel<kJoint>
+                          : bwd_mma_kernel<kQueryMajor>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)(items * p.BH), kThreads, smem, st>>>(p);

@@ -233,7 +233,10 @@ cudaError_t launch_backward(const BwdArgs<T>& a, int d, cudaStream_t st);
 // queries (q, g, L, D) against keys (k, v) under logit scale c, P = exp(c q.k - L),
 // dS = P (g.v - D); kind 0 (query-major) adds c dS k to dq; kind 1 (key-major) adds
 // c dS^T q to dk and P^T g to dv (a null output is skipped); kind 2 (query-major) adds
-// each query's sum of P (g.v) over the pass's keys to Dacc.  Segments: with bucket_off set, one per (head, expert)
+// each query's sum of P (g.v) over the pass's keys to Dacc; kind 3 (joint, routed segments,
+// each query in one segment: s = 1) streams each expert's top-k rows and then the head's n2
+// rows of (k2, v2) under scale c2 twice -- first to sum D, stored to Dacc, then for dq,
+// stored (`first` must be set).  Segments: with bucket_off set, one per (head, expert)
 // -- queries n = bucket_qidx[bh][off[e] ..] and keys j = topk_idx[bh][e][0 .. topk), rows
 // bh*N + n and bh*N + j -- else one per head with nq query rows at bh*nq and nk key rows at
 // bh*nk.  Outputs 16-byte aligned.  `first`: no earlier launch wrote the outputs and each
@@ -245,6 +248,9 @@ struct BwdPass {
   const float *L, *D;
   float *dq, *dk, *dv, *Dacc;
   float c;
+  const __nv_bfloat16 *k2, *v2;   // joint: the second key set (rows bh*n2 ..), scale c2
+  float c2;
+  int n2;
   int BH, nq, nk;
   const int32_t *bucket_off, *bucket_qidx, *topk_idx;
   int N, m, topk, NS, items, first;
